@@ -1,0 +1,229 @@
+/*
+ * gdnspec.h — C ABI of the GB300 speculative-verify path for GatedDeltaNet (GDN) layers.
+ *
+ * One speculative round on the GDN layers of a hybrid model is three calls:
+ *
+ *   gdn_verify    run T draft positions through the GDN layers: causal depthwise conv + SiLU,
+ *                 L2-normalised q/k, the gated delta rule, per-position outputs, and an
+ *                 innovation tape. The recurrent state and the conv state are READ ONLY, so the
+ *                 pre-verify snapshot stays in place.
+ *   spec_accept   decide how many drafts to keep from the verify logits: greedy longest-prefix
+ *                 argmax match, or Leviathan rejection sampling with point-mass drafts.
+ *   gdn_rollback  commit the accepted prefix: restore-from-snapshot (implicit: the state was never
+ *                 written) and replay only the accepted steps from the tape, O(n_accepted); rebuild
+ *                 the conv state from the raw qkv rows.
+ *
+ * Tree variants (gdn_verify_tree, spec_accept_tree, gdn_rollback_path) walk a draft token tree
+ * instead of a chain.
+ *
+ * Sources. "GDN investigation" below is the write-up "Speculative Decoding on GDN Hybrid
+ * Architectures: A 31-Experiment Investigation"; "xserv docs/25" is "Phase 25: 三种投机解码方法对比
+ * (Small Model / EAGLE / MTP)"; "colibrì ch.08" is the colibrì analysis chapter "MTP 投机解码与预取".
+ *
+ * Conventions common to every call.
+ *  - Ownership: the caller owns every buffer. No call allocates, frees or synchronises.
+ *  - Device pointers unless stated. Every call enqueues on `stream` and returns at once.
+ *  - Layouts are dense row-major in the order written, e.g. [L][B][T][C] means
+ *    element (l,b,t,c) lives at ((l*B + b)*T + t)*C + c.
+ *  - Return value: GDN_OK, or an error code with a message in gdn_last_error(). On a non-OK
+ *    return nothing was enqueued. Host-side argument checks never touch the GPU.
+ *  - `status` (optional, may be NULL): one device uint32_t. Kernels OR GDN_STATUS_* bits into it
+ *    when they meet an out-of-range device value (an accepted count, a parent index, a token);
+ *    the offending unit is skipped. Kernels never trap. Read it after synchronising the stream.
+ */
+#ifndef GDNSPEC_H
+#define GDNSPEC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- return codes ---------------------------------------------------------------------- */
+#define GDN_OK                0
+#define GDN_ERR_INVALID_ARG   1  /* null pointer, negative or inconsistent size, misalignment */
+#define GDN_ERR_UNSUPPORTED   2  /* valid but not built: head dims, T, W outside the kernel set */
+#define GDN_ERR_CUDA          3  /* a CUDA launch or attribute call failed (message has the name) */
+
+/* ---- device status bits (OR-ed into *status by the kernels) ----------------------------- */
+#define GDN_STATUS_BAD_NACC    0x1u  /* rollback: accepted count outside [0, T] */
+#define GDN_STATUS_BAD_PARENT  0x2u  /* tree: parent not in [-1, v) for node v */
+#define GDN_STATUS_BAD_TOKEN   0x4u  /* accept: draft / tree token outside [0, V) */
+#define GDN_STATUS_BAD_PATH    0x8u  /* path rollback: path node out of range */
+#define GDN_STATUS_EMPTY_DIST  0x10u /* sampling: a distribution with zero total weight */
+
+/* ---- element types ---------------------------------------------------------------------- */
+#define GDN_DTYPE_F32   0
+#define GDN_DTYPE_BF16  1
+
+/* ---- accept modes ----------------------------------------------------------------------- */
+#define SPEC_MODE_GREEDY  0
+#define SPEC_MODE_SAMPLE  1
+
+/*
+ * Shapes of one gdn_verify / gdn_rollback call.
+ *  L   layers covered by the call (each layer has its own inputs, weights and state slices)
+ *  B   sequences
+ *  T   verify positions per sequence (chain: the N drafts; tree: the node count)
+ *  Hk, Hv  key heads and value heads, Hv a multiple of Hk; value head h reads key head
+ *          h / (Hv/Hk) (consecutive grouping)
+ *  Dk, Dv  head dims; the kernels are built for Dk == Dv in {32, 64, 128}
+ *  W   conv width, 1..4
+ *  C   qkv channels; must equal 2*Hk*Dk + Hv*Dv, ordered [q | k | v], each head-major
+ *  io_dtype  GDN_DTYPE_BF16 or GDN_DTYPE_F32 for qkv, conv_w, conv_state and out
+ *  qk_scale  multiplies the output o_t (1.0 for the plain o_t = S_t q_t)
+ *  l2_eps    x / sqrt(sum x^2 + l2_eps) normalises q and k (1e-6)
+ */
+typedef struct gdn_dims {
+    int32_t L, B, T;
+    int32_t Hk, Hv, Dk, Dv;
+    int32_t W, C;
+    int32_t io_dtype;
+    float qk_scale;
+    float l2_eps;
+} gdn_dims;
+
+/*
+ * gdn_verify — batched multi-token verification through GDN layers, with the innovation tape.
+ *
+ * Computes (GDN investigation §2.1 "Conv1D state + gated delta state", §2.2 multi-token
+ * verification, §4 tape recording; the update is the standard gated delta rule):
+ *   x̂ = concat(conv_state rows 0..W-2, qkv rows 0..T-1) per channel
+ *   y[t,c] = silu( sum_{j<W} conv_w[c][j] * x̂[t+j, c] )      (tap W-1 is the current token)
+ *   q_t, k_t = L2-normalised q and k heads of y;  v_t = v head of y
+ *   per value head, from S = S_0:  u = g_t S k_t;  δ_t = β_t (v_t − u);  S ← g_t S + δ_t k_tᵀ;
+ *                                  o_t = qk_scale · S q_t
+ * Arguments (device):
+ *   qkv        [L][B][T][C]        io_dtype   raw projections of the T verify positions
+ *   conv_w     [L][C][W]           io_dtype   depthwise conv taps
+ *   conv_state [L][B][W-1][C]      io_dtype   last W-1 raw rows before the round (read only)
+ *   g, beta    [L][B][T][Hv]       f32        decay gate in (0,1] and write strength
+ *   state      [L][B][Hv][Dk][Dv]  f32        S_0, stored key-major: element (i,j) of S — row i
+ *                                             in Dv, column j in Dk — is at [j][i] (read only)
+ *   out        [L][B][T][Hv][Dv]   io_dtype   o_t
+ *   tape_delta [L][B][T][Hv][Dv]   f32        δ_t          (written)
+ *   tape_k     [L][B][T][Hk][Dk]   f32        normalised k_t (written)
+ * The tape's gate and raw-conv parts are the caller's g and qkv themselves: keep them alive and
+ * unchanged until gdn_rollback. All pointers 16-byte aligned. The tape buffers hold
+ * gdn_tape_bytes() bytes in total.
+ */
+int gdn_verify(const gdn_dims* d, const void* qkv, const void* conv_w, const void* conv_state,
+               const float* g, const float* beta, const float* state, void* out,
+               float* tape_delta, float* tape_k, uint32_t* status, void* stream);
+
+/*
+ * gdn_verify_tree — gdn_verify over a draft token tree (GDN investigation §2.2 update note and
+ * §8 path 3: tree-aware GDN kernels walk the draft tree through the recurrent state).
+ *   parent [B][T] int32: parent node of node v, in [-1, v) (-1 = child of the committed context).
+ * Node v starts from its parent's state (S_0 for parent -1); its conv window is its own raw row
+ * and its W-1 nearest ancestors' rows, continued into conv_state when the path is shorter.
+ * Other arguments and layouts as gdn_verify with T = node count; the tape is per node.
+ * A bad parent sets GDN_STATUS_BAD_PARENT and skips that (layer, sequence).
+ */
+int gdn_verify_tree(const gdn_dims* d, const int32_t* parent, const void* qkv,
+                    const void* conv_w, const void* conv_state, const float* g,
+                    const float* beta, const float* state, void* out, float* tape_delta,
+                    float* tape_k, uint32_t* status, void* stream);
+
+/*
+ * gdn_rollback — tape-replay rollback (GDN investigation §4 "Tape-Replay 回滚"): for every layer
+ * and sequence with n = n_acc[b] > 0, replay the accepted steps
+ *     S ← g_t S + δ_t k_tᵀ,  t = 0..n-1,
+ * from the untouched snapshot S_0 and store S_n in place; rebuild the conv state as the last W-1
+ * rows of (conv_state ++ qkv rows 0..n-1). n = 0 leaves both untouched. Cost O(n), all L layers
+ * in one launch; n is read on the device (no host sync).
+ *   n_acc [B] int32 device; tape_delta, tape_k, g, qkv as written/passed to gdn_verify;
+ *   state and conv_state are updated in place. n outside [0, T] sets GDN_STATUS_BAD_NACC.
+ */
+int gdn_rollback(const gdn_dims* d, const int32_t* n_acc, const float* tape_delta,
+                 const float* tape_k, const float* g, const void* qkv, float* state,
+                 void* conv_state, uint32_t* status, void* stream);
+
+/*
+ * gdn_rollback_path — gdn_rollback along an accepted tree path: the replayed steps are the nodes
+ * path[b][0..n-1] (root-most first) of a gdn_verify_tree call, n = n_acc[b] ≤ P.
+ *   path [B][P] int32 device (P = path capacity, e.g. the tree depth).
+ */
+int gdn_rollback_path(const gdn_dims* d, const int32_t* path, int32_t P, const int32_t* n_acc,
+                      const float* tape_delta, const float* tape_k, const float* g,
+                      const void* qkv, float* state, void* conv_state, uint32_t* status,
+                      void* stream);
+
+/* Bytes of tape_delta plus tape_k for the shape d (host only, no GPU). 0 on invalid d. */
+size_t gdn_tape_bytes(const gdn_dims* d);
+
+/*
+ * Shapes of one spec_accept call.
+ *  B  sequences;  N  drafts per sequence (logits rows per sequence: N + 1, row i judges draft i,
+ *  row N is the bonus row);  V  vocabulary;  dtype  GDN_DTYPE_BF16 or GDN_DTYPE_F32 logits;
+ *  row_stride, seq_stride  elements between rows / sequences of logits (row_stride ≥ V; a
+ *  seq_stride of 0 lets all sequences share one block of rows). Both multiples of 8 for bf16
+ *  and of 4 for f32 (16-byte rows).
+ */
+typedef struct spec_dims {
+    int32_t B, N, V, dtype;
+    int64_t row_stride, seq_stride;
+} spec_dims;
+
+/*
+ * spec_accept — acceptance over the verify logits.
+ *
+ * SPEC_MODE_GREEDY (xserv docs/25 §2 algorithm; colibrì ch.08 §5 greedy path): with
+ * am_i = argmax of row i (lowest index among equal maxima), n = the number of leading drafts with
+ * drafts[i] == am_i; out = drafts[0..n-1] ++ am_n (the correction, or the bonus when n = N).
+ *
+ * SPEC_MODE_SAMPLE (colibrì ch.08 §5 Leviathan rejection sampling with point-mass drafts): per
+ * row the target law is p = softmax(row / temperature), realised as integer weights
+ *   w_v = floor(2^32 · 2^((float(l_v) − float(max)) · c)),  c = fp32(log2(e) / temperature),
+ * with the power of two evaluated by a fixed Cody–Waite + degree-7 polynomial so any
+ * implementation of this contract draws bit-identical results. Draw r uniform on [0, Z)
+ * (Z = Σ w) from Philox4x32-10 with key = seed and counter = (round mod 2^32, b, row, purpose);
+ * accept draft i iff r < w[draft_i]. On the first rejection, ban draft i (weight 0), renormalise
+ * and sample the emitted token from what is left; if all N are accepted, sample the bonus from
+ * row N. temperature ≤ 0 selects greedy.
+ *
+ * Arguments:
+ *   logits     device, laid out by d (row i of sequence b at b*seq_stride + i*row_stride)
+ *   drafts     [B][N] int32 device; a token outside [0, V) sets GDN_STATUS_BAD_TOKEN and that
+ *              sequence reports n = 0 and out = {-1...}
+ *   workspace  device scratch of spec_workspace_bytes(d, mode) bytes, 16-byte aligned; no state
+ *              is kept in it between calls
+ *   n_acc      [B] int32 device: accepted drafts n in [0, N]
+ *   out_tokens [B][N+1] int32 device: the n accepted drafts, then the correction/bonus token,
+ *              then -1 padding
+ */
+int spec_accept(const spec_dims* d, const void* logits, const int32_t* drafts, int32_t mode,
+                float temperature, uint64_t seed, uint64_t round, void* workspace,
+                size_t workspace_bytes, int32_t* n_acc, int32_t* out_tokens, uint32_t* status,
+                void* stream);
+
+/* Workspace bytes spec_accept needs for d and mode (host only). 0 on invalid d. */
+size_t spec_workspace_bytes(const spec_dims* d, int32_t mode);
+
+/*
+ * spec_accept_tree — greedy acceptance of the longest matching root-to-leaf path of a draft
+ * tree (GDN investigation §2.2 / §8: DDTree verification). Rows: row 0 judges the children of
+ * the committed context, row 1+v judges the children of node v. From the context, repeatedly
+ * move to the lowest-numbered child whose token equals the argmax of the current row; stop when
+ * none matches or after P steps. The argmax of the last row reached is the bonus token.
+ *   d          B, N = T (nodes; rows per sequence are T + 1), V, dtype, strides as spec_dims
+ *   parent     [B][T] int32, tokens [B][T] int32 device (tree of gdn_verify_tree)
+ *   path       [B][P] int32 device: accepted nodes root-most first, -1 padded
+ *   n_acc      [B] int32; out_tokens [B][P+1] int32 (path tokens, bonus, -1 padding)
+ * workspace as spec_accept with SPEC_MODE_GREEDY.
+ */
+int spec_accept_tree(const spec_dims* d, const void* logits, const int32_t* parent,
+                     const int32_t* tokens, int32_t P, void* workspace, size_t workspace_bytes,
+                     int32_t* path, int32_t* n_acc, int32_t* out_tokens, uint32_t* status,
+                     void* stream);
+
+/* Thread-local message for the last non-OK return on this thread ("" if none). */
+const char* gdn_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDNSPEC_H */
