@@ -1,0 +1,568 @@
+"""Benchmark: verified draft tokens/s through 30 GDN layers of verify + accept + rollback.
+
+One step = one speculative round of the workload: gdn_verify over all layers (one launch),
+spec_accept over the verify logits, gdn_rollback over all layers (one launch). Inputs are seeded
+synthetic tensors with the workload's shapes, resident in HBM before timing (a pool of rounds is
+cycled); the recurrent state (4 GB for the batched workload) is far larger than L2, so every step
+streams it from HBM.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config 2]
+
+Prints one JSON line (rank 0). Under torchrun each rank runs its own copy of the workload on its
+own GPU (weak scaling; sequences are independent, so there is no collective on the data path).
+--impl reference times the CPU oracle on the host cores on the same workload and metric.
+"""
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "verified draft tokens/sec (30 GDN layers+accept+rollback); % HBM roofline"
+UNIT = "tokens/s"
+DEFAULT_CONFIG = 2
+POOL = 4
+
+
+# ------------------------------------------------------------------------------ distributed
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def init_dist(backend):
+    import torch.distributed as dist
+    ws, rank, _ = dist_env()
+    if ws > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+    return ws, rank
+
+
+def rank_seed(seed, rank):
+    """Each rank draws its own sequences (weak scaling): distinct, reproducible seeds."""
+    return int(seed) * 1000003 + int(rank)
+
+
+def reduce_max(x, device=None):
+    """Max of a float over ranks (identity without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(device=None):
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        if device is not None and dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def aggregate_tokens_per_s(world, B, N, ms_per_step):
+    return world * B * N / (ms_per_step / 1e3)
+
+
+# ------------------------------------------------------------------------------ accounting
+def bytes_verify(w):
+    """Algorithmic HBM bytes of one gdn_verify launch over the whole workload: each input read
+    once, each output written once (state S_0 read, never written)."""
+    io = 2 if str(w.io_dtype).endswith("bfloat16") else 4
+    S = w.Hv * w.D * w.D * 4
+    T, C = w.N, w.C
+    per_unit = (S + T * (io * C + 8 * w.Hv + io * w.Hv * w.D + 4 * w.Hv * w.D + 4 * w.Hk * w.D)
+                + io * (w.W - 1) * C)
+    return w.L * w.B * per_unit + w.L * io * C * w.W
+
+
+def bytes_rollback(w, n_list):
+    """Algorithmic bytes of one gdn_rollback launch for accepted counts n_list (one per seq)."""
+    io = 2 if str(w.io_dtype).endswith("bfloat16") else 4
+    S = w.Hv * w.D * w.D * 4
+    C, W = w.C, w.W
+    tot = 0
+    for n in n_list:
+        n = int(n)
+        if n <= 0:
+            continue
+        m = min(n, W - 1)
+        tot += (2 * S + n * (4 * w.Hv * w.D + 4 * w.Hk * w.D + 4 * w.Hv)
+                + io * (W - 1 - m) * C + io * m * C + io * (W - 1) * C)
+    return w.L * tot + 4 * w.B
+
+
+def bytes_accept(w):
+    io = 2 if str(w.io_dtype).endswith("bfloat16") else 4
+    return w.B * (w.N + 1) * w.V * io + 4 * w.B * (2 * w.N + 2)
+
+
+def read_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_sources_sha():
+    """Hash of the kernel sources: profile counters are stale once this changes."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "speculative_verify_gdn_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload_name, kernel):
+    """dram read+write bytes per launch from a committed ncu summary, if it matches the sources."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        e = d.get(workload_name, {}).get(kernel)
+        if e and e.get("src_sha") == kernel_sources_sha():
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        return None
+    return None
+
+
+# ------------------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.Q,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+        time.sleep(0.3)
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.t:
+            self.t.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------ CPU oracle leg
+def oracle_unit_times(w, seed, budget_s, units_min):
+    """Time the CPU oracle on (layer, sequence) units of verify+rollback and on per-sequence
+    accepts of the workload. Returns (seconds per unit, seconds per accepted sequence, units)."""
+    import numpy as np
+    import torch
+    import oracle
+    from speculative_verify_gdn_gb300 import inputs as I
+
+    small = I.custom(w, name=w.name, L=1, B=1)
+    cw = I.model_weights(small, seed).double().numpy()
+    st, cs = I.initial_state(small, seed)
+    st, cs = st.double().numpy(), cs.double().numpy()
+    qkv, g, beta = I.round_stream(small, 0, seed)
+    qkv, g, beta = qkv.double().numpy(), g.double().numpy(), beta.double().numpy()
+    d = oracle.OracleDims(L=1, B=1, T=w.N, Hk=w.Hk, Hv=w.Hv, Dk=w.D, Dv=w.D, W=w.W)
+    parent = None
+    if w.accept == "tree":
+        parent = I.random_tree(I.custom(w, name=w.name, B=1), 0, seed).numpy()
+    t0 = time.perf_counter()
+    units = 0
+    while units < units_min or time.perf_counter() - t0 < budget_s:
+        ref = oracle.verify(d, qkv, cw, cs, g, beta, st, parent=parent)
+        n = np.array([max(1, w.N // 2)], np.int32)
+        path = None
+        if parent is not None:
+            path = np.full((1, w.P), -1, np.int32)
+            x, k = 0, 0
+            while x >= 0 and k < n[0]:
+                path[0, k] = x
+                k += 1
+                ch = [v for v in range(w.N) if parent[0, v] == x]
+                x = ch[0] if ch else -1
+            n = np.array([k], np.int32)
+        oracle.rollback(d, n, ref["tape_delta"], ref["tape_k"], g, qkv, st, cs, path=path)
+        units += 1
+    t_unit = (time.perf_counter() - t0) / units
+    # accept: one sequence's N+1 rows
+    one = I.custom(w, name=w.name, B=1)
+    if w.accept == "sample":
+        lg, dr = I.sample_logits(one, 0, seed)
+    elif w.accept == "tree":
+        par = I.random_tree(one, 0, seed)
+        tok, lg, _ = I.tree_tokens_and_logits(one, par, 0, seed)
+    else:
+        lg, dr, _ = I.greedy_logits(one, 0, seed)
+    lgf = lg.float().numpy()
+    reps = 0
+    t1 = time.perf_counter()
+    while reps < 2 or time.perf_counter() - t1 < min(2.0, budget_s / 5):
+        if w.accept == "sample":
+            oracle.accept_sample(lgf, dr.numpy(), w.temperature, seed, reps)
+        elif w.accept == "tree":
+            oracle.accept_tree(lgf, par.numpy(), tok.numpy(), w.P)
+        else:
+            oracle.accept_greedy(lgf, dr.numpy())
+        reps += 1
+    t_acc = (time.perf_counter() - t1) / reps
+    del torch
+    return t_unit, t_acc, units
+
+
+def cpu_tokens_per_s(w, t_unit, t_acc):
+    """A sequence-round is L units of verify+rollback and one accept; it verifies N tokens."""
+    return w.N / (w.L * t_unit + t_acc)
+
+
+# ------------------------------------------------------------------------------ GPU leg
+def workload_description(w):
+    d = {"workload": "%s: %d GDN layers (Qwen3.6-shaped: Hk=%d, Hv=%d, d=%d, conv %d over C=%d), "
+                     "batch %d, N=%d, %s accept over V=%d" % (
+                         w.name, w.L, w.Hk, w.Hv, w.D, w.W, w.C, w.B, w.N, w.accept, w.V),
+         "layers": w.L, "batch": w.B, "drafts": w.N, "vocab": w.V, "accept": w.accept,
+         "io_dtype": "bf16" if str(w.io_dtype).endswith("bfloat16") else "f32",
+         "state": "fp32 128x128 per value head, key-major",
+         "l2": "inputs larger than L2: the %.2f GB recurrent state is streamed from HBM every step"
+               % (w.L * w.B * w.Hv * w.D * w.D * 4 / 1e9)}
+    if w.accept in ("greedy", "tree"):
+        d["alphas"] = list(w.alphas)
+    if w.accept == "sample":
+        d["temperature"] = w.temperature
+    if w.accept == "tree":
+        d["tree"] = {"nodes": w.N, "depth": w.tree_depth, "branching": w.tree_branch}
+    return d
+
+
+def make_pool(w, seed, device, pool):
+    import torch
+    from speculative_verify_gdn_gb300 import inputs as I
+    slots = []
+    for k in range(pool):
+        qkv, g, beta = I.round_stream(w, k, seed, device)
+        parent = None
+        if w.accept == "tree":
+            par = I.random_tree(w, k, seed)
+            tok, lg, _ = I.tree_tokens_and_logits(w, par, k, seed)
+            parent, drafts, lg = par.to(device), tok.to(device), lg.to(device)
+        elif w.accept == "sample":
+            lg, drafts = I.sample_logits(w, k, seed, device)
+        else:
+            lg, drafts, _ = I.greedy_logits(w, k, seed, device)
+        slots.append(dict(qkv=qkv, g=g, beta=beta, logits=lg, drafts=drafts, parent=parent))
+    torch.cuda.synchronize(device)
+    return slots
+
+
+def run_gpu(args, w, world, rank, device):
+    import torch
+    from speculative_verify_gdn_gb300 import build as lib_build, inputs as I
+    from speculative_verify_gdn_gb300.round import SpecRound
+
+    lib_build.build()
+    seed = rank_seed(args.seed, rank)
+    cw = I.model_weights(w, seed, device)
+    state, conv_state = I.initial_state(w, seed, device)
+    pool = make_pool(w, seed, device, POOL)
+    r = SpecRound(w, device)
+    stream = torch.cuda.current_stream(device)
+
+    def step(k, rnd, evs=None):
+        s = pool[k % POOL]
+        if evs is not None:
+            evs[0].record(stream)
+        r.verify(s["qkv"], cw, conv_state, s["g"], s["beta"], state, parent=s["parent"])
+        if evs is not None:
+            evs[1].record(stream)
+        r.accept(s["logits"], s["drafts"], round_=rnd, seed=seed, parent=s["parent"])
+        if evs is not None:
+            evs[2].record(stream)
+        r.rollback(s["qkv"], s["g"], state, conv_state)
+        if evs is not None:
+            evs[3].record(stream)
+
+    for k in range(args.warmup):
+        step(k, k)
+    r.check_status()
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    nlog = torch.zeros((K, w.B), dtype=torch.int32, device=device)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(device.index if device.index is not None else 0)
+    clocks.start()
+    barrier(device)
+    torch.cuda.synchronize(device)
+    start.record(stream)
+    for k in range(K):
+        step(args.warmup + k, args.warmup + k, evs[k])
+        nlog[k].copy_(r.n_acc, non_blocking=True)
+    end.record(stream)
+    torch.cuda.synchronize(device)
+    barrier(device)
+    clk = clocks.stop()
+    r.check_status()
+    ms_total = start.elapsed_time(end)
+    ms_total = reduce_max(ms_total, device)
+    ms_step = ms_total / K
+    t_ver = [evs[k][0].elapsed_time(evs[k][1]) for k in range(K)]
+    t_acc = [evs[k][1].elapsed_time(evs[k][2]) for k in range(K)]
+    t_rb = [evs[k][2].elapsed_time(evs[k][3]) for k in range(K)]
+    nl = nlog.cpu().numpy()
+
+    peak, peak_kind = read_peaks()
+    bv = bytes_verify(w)
+    ba = bytes_accept(w)
+    brb = [bytes_rollback(w, nl[k]) for k in range(K)]
+    kern = {
+        "gdn_verify": {"ms": statistics.mean(t_ver), "bytes": bv},
+        "spec_accept": {"ms": statistics.mean(t_acc), "bytes": ba},
+        "gdn_rollback": {"ms": statistics.mean(t_rb), "bytes": statistics.mean(brb)},
+    }
+    for name, e in kern.items():
+        e["GBps"] = e["bytes"] / (e["ms"] / 1e3) / 1e9
+        e["frac_of_%s_peak" % peak_kind] = e["GBps"] / peak
+    dom = max(kern, key=lambda n: kern[n]["ms"])
+    step_bytes = bv + ba + statistics.mean(brb)
+    roof = {"bound": "hbm", "kernel": dom, "achieved": kern[dom]["GBps"], "peak": peak,
+            "peak_source": "MEASURED_PEAKS.json hbm_gbs (%s)" % peak_kind, "unit": "GB/s",
+            "frac": kern[dom]["GBps"] / peak,
+            "traffic": profiled_traffic(w.name, dom),
+            "algorithmic_bytes_per_launch": kern[dom]["bytes"],
+            "step_frac": step_bytes / (ms_step / 1e3) / 1e9 / peak}
+    mean_n = float(nl.mean())
+    res = dict(ms_step=ms_step, kernels=kern, roofline=roof, clocks=clk, mean_n=mean_n,
+               launches=K * r.launches_per_step(), ms_total=ms_total)
+
+    # ---- end to end: host (pinned) inputs copied in, results copied out, every step
+    if not args.no_e2e:
+        res["e2e"] = run_e2e(args, w, r, pool, cw, state, conv_state, device, seed)
+    return res
+
+
+def run_e2e(args, w, r, pool, cw, state, conv_state, device, seed):
+    import torch
+    keys = ("qkv", "g", "beta", "logits", "drafts")
+    host = []
+    for s in pool[:2]:
+        host.append({k: s[k].cpu().pin_memory() for k in keys})
+    dev = {k: torch.empty_like(pool[0][k]) for k in keys}
+    parent = pool[0]["parent"]
+    out_h = torch.empty((w.B, r.out_tokens.shape[1]), dtype=torch.int32).pin_memory()
+    n_h = torch.empty((w.B,), dtype=torch.int32).pin_memory()
+    stream = torch.cuda.current_stream(device)
+    h2d = sum(host[0][k].numel() * host[0][k].element_size() for k in keys)
+    d2h = out_h.numel() * 4 + n_h.numel() * 4
+    K = max(3, min(args.steps, args.e2e_steps))
+
+    def step(k):
+        hs = host[k % len(host)]
+        for key in keys:
+            dev[key].copy_(hs[key], non_blocking=True)
+        r.step(dev["qkv"], dev["g"], dev["beta"], dev["logits"], dev["drafts"], cw, state,
+               conv_state, round_=k, seed=seed, parent=parent)
+        n_h.copy_(r.n_acc, non_blocking=True)
+        out_h.copy_(r.out_tokens, non_blocking=True)
+
+    for k in range(2):
+        step(k)
+    torch.cuda.synchronize(device)
+    barrier(device)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for k in range(K):
+        step(k)
+    t1.record(stream)
+    torch.cuda.synchronize(device)
+    ms = reduce_max(t0.elapsed_time(t1), device) / K
+    world = dist_env()[0]
+    return {"value": aggregate_tokens_per_s(world, w.B, w.N, ms), "unit": UNIT,
+            "ms_per_step": ms, "steps": K, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+# ------------------------------------------------------------------------------ main
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, default=DEFAULT_CONFIG)
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    args = ap.parse_args(argv)
+
+    from speculative_verify_gdn_gb300 import inputs as I
+    w = I.WORKLOADS[args.config]
+    ws, rank, local = dist_env()
+
+    if args.impl == "reference":
+        if ws > 1:
+            init_dist("gloo")
+            if rank != 0:
+                return 0
+        return run_reference(args, w)
+
+    import torch
+    assert torch.cuda.is_available(), "bench.py needs a CUDA device"
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    world, rank = init_dist("nccl")
+    res = run_gpu(args, w, world, rank, device)
+    line = {
+        "metric": METRIC, "value": aggregate_tokens_per_s(world, w.B, w.N, res["ms_step"]),
+        "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": res["ms_step"], "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "io_dtype": "bf16", "data": "synthetic",
+        "config": workload_description(w), "roofline": res["roofline"],
+        "kernels": res["kernels"], "mean_accepted": res["mean_n"],
+        "committed_tokens_per_s": world * w.B * (res["mean_n"] + 1) / (res["ms_step"] / 1e3),
+        "gpu_launches": res["launches"], "clocks": res["clocks"],
+        "e2e": res.get("e2e"),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        t_unit, t_acc, units = oracle_unit_times(w, args.seed, args.cpu_budget, w.L)
+        line["cpu_baseline"] = {
+            "value": cpu_tokens_per_s(w, t_unit, t_acc), "unit": UNIT, "cores": 1,
+            "kind": "oracle",
+            "sample": "%d (layer, sequence) units of verify+rollback (%.1f ms each) and one "
+                      "sequence's accept (%.1f ms) of this workload, single-threaded fp64 oracle; "
+                      "tokens/s = N / (L * unit + accept)" % (units, t_unit * 1e3, t_acc * 1e3)}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_reference(args, w):
+    """The oracle on the host cores, on this workload and metric; each step one (layer,
+    sequence) unit of verify+rollback, plus one sequence's accept every L steps."""
+    import numpy as np
+    import oracle
+    from speculative_verify_gdn_gb300 import inputs as I
+
+    seed = args.seed
+    small = I.custom(w, name=w.name, L=1, B=1)
+    cw = I.model_weights(small, seed).double().numpy()
+    st, cs = I.initial_state(small, seed)
+    st, cs = st.double().numpy(), cs.double().numpy()
+    d = oracle.OracleDims(L=1, B=1, T=w.N, Hk=w.Hk, Hv=w.Hv, Dk=w.D, Dv=w.D, W=w.W)
+    one = I.custom(w, name=w.name, B=1)
+    parent = tok = None
+    if w.accept == "sample":
+        lg, dr = I.sample_logits(one, 0, seed)
+    elif w.accept == "tree":
+        parent = I.random_tree(one, 0, seed).numpy()
+        tok, lg, _ = I.tree_tokens_and_logits(one, I.random_tree(one, 0, seed), 0, seed)
+        tok = tok.numpy()
+    else:
+        lg, dr, _ = I.greedy_logits(one, 0, seed)
+    lgf = lg.float().numpy()
+    streams = [I.round_stream(small, k, seed) for k in range(2)]
+    streams = [tuple(t.double().numpy() for t in s) for s in streams]
+
+    def step(k):
+        qkv, g, beta = streams[k % 2]
+        ref = oracle.verify(d, qkv, cw, cs, g, beta, st, parent=parent)
+        path = None
+        n = np.array([max(1, w.N // 2)], np.int32)
+        if parent is not None:
+            path = np.full((1, w.P), -1, np.int32)
+            path[0, 0] = 0
+            n = np.array([1], np.int32)
+        oracle.rollback(d, n, ref["tape_delta"], ref["tape_k"], g, qkv, st, cs, path=path)
+        if k % w.L == w.L - 1:
+            if w.accept == "sample":
+                oracle.accept_sample(lgf, dr.numpy(), w.temperature, seed, k)
+            elif w.accept == "tree":
+                oracle.accept_tree(lgf, parent, tok, w.P)
+            else:
+                oracle.accept_greedy(lgf, dr.numpy())
+
+    for k in range(args.warmup):
+        step(k)
+    t0 = time.perf_counter()
+    for k in range(args.steps):
+        step(k)
+    dt = time.perf_counter() - t0
+    ms_step = dt / args.steps * 1e3
+    value = w.N * (args.steps / w.L) / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 0,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_description(w),
+        "cpu_baseline": {"value": value, "unit": UNIT, "kind": "oracle", "cores": 1,
+                         "sample": "each step one (layer, sequence) unit of verify+rollback, one "
+                                   "sequence's accept every %d steps; tokens/s = N per %d steps"
+                                   % (w.L, w.L)},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

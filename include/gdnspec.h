@@ -37,6 +37,12 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#if defined(__GNUC__)
+#define GDN_API __attribute__((visibility("default")))
+#else
+#define GDN_API
+#endif
+
 #ifdef __cplusplus
 extern "C" {
 #endif
@@ -109,7 +115,7 @@ typedef struct gdn_dims {
  * unchanged until gdn_rollback. All pointers 16-byte aligned. The tape buffers hold
  * gdn_tape_bytes() bytes in total.
  */
-int gdn_verify(const gdn_dims* d, const void* qkv, const void* conv_w, const void* conv_state,
+GDN_API int gdn_verify(const gdn_dims* d, const void* qkv, const void* conv_w, const void* conv_state,
                const float* g, const float* beta, const float* state, void* out,
                float* tape_delta, float* tape_k, uint32_t* status, void* stream);
 
@@ -122,7 +128,7 @@ int gdn_verify(const gdn_dims* d, const void* qkv, const void* conv_w, const voi
  * Other arguments and layouts as gdn_verify with T = node count; the tape is per node.
  * A bad parent sets GDN_STATUS_BAD_PARENT and skips that (layer, sequence).
  */
-int gdn_verify_tree(const gdn_dims* d, const int32_t* parent, const void* qkv,
+GDN_API int gdn_verify_tree(const gdn_dims* d, const int32_t* parent, const void* qkv,
                     const void* conv_w, const void* conv_state, const float* g,
                     const float* beta, const float* state, void* out, float* tape_delta,
                     float* tape_k, uint32_t* status, void* stream);
@@ -137,7 +143,7 @@ int gdn_verify_tree(const gdn_dims* d, const int32_t* parent, const void* qkv,
  *   n_acc [B] int32 device; tape_delta, tape_k, g, qkv as written/passed to gdn_verify;
  *   state and conv_state are updated in place. n outside [0, T] sets GDN_STATUS_BAD_NACC.
  */
-int gdn_rollback(const gdn_dims* d, const int32_t* n_acc, const float* tape_delta,
+GDN_API int gdn_rollback(const gdn_dims* d, const int32_t* n_acc, const float* tape_delta,
                  const float* tape_k, const float* g, const void* qkv, float* state,
                  void* conv_state, uint32_t* status, void* stream);
 
@@ -146,13 +152,13 @@ int gdn_rollback(const gdn_dims* d, const int32_t* n_acc, const float* tape_delt
  * path[b][0..n-1] (root-most first) of a gdn_verify_tree call, n = n_acc[b] ≤ P.
  *   path [B][P] int32 device (P = path capacity, e.g. the tree depth).
  */
-int gdn_rollback_path(const gdn_dims* d, const int32_t* path, int32_t P, const int32_t* n_acc,
+GDN_API int gdn_rollback_path(const gdn_dims* d, const int32_t* path, int32_t P, const int32_t* n_acc,
                       const float* tape_delta, const float* tape_k, const float* g,
                       const void* qkv, float* state, void* conv_state, uint32_t* status,
                       void* stream);
 
 /* Bytes of tape_delta plus tape_k for the shape d (host only, no GPU). 0 on invalid d. */
-size_t gdn_tape_bytes(const gdn_dims* d);
+GDN_API size_t gdn_tape_bytes(const gdn_dims* d);
 
 /*
  * Shapes of one spec_accept call.
@@ -194,13 +200,13 @@ typedef struct spec_dims {
  *   out_tokens [B][N+1] int32 device: the n accepted drafts, then the correction/bonus token,
  *              then -1 padding
  */
-int spec_accept(const spec_dims* d, const void* logits, const int32_t* drafts, int32_t mode,
+GDN_API int spec_accept(const spec_dims* d, const void* logits, const int32_t* drafts, int32_t mode,
                 float temperature, uint64_t seed, uint64_t round, void* workspace,
                 size_t workspace_bytes, int32_t* n_acc, int32_t* out_tokens, uint32_t* status,
                 void* stream);
 
 /* Workspace bytes spec_accept needs for d and mode (host only). 0 on invalid d. */
-size_t spec_workspace_bytes(const spec_dims* d, int32_t mode);
+GDN_API size_t spec_workspace_bytes(const spec_dims* d, int32_t mode);
 
 /*
  * spec_accept_tree — greedy acceptance of the longest matching root-to-leaf path of a draft
@@ -214,13 +220,13 @@ size_t spec_workspace_bytes(const spec_dims* d, int32_t mode);
  *   n_acc      [B] int32; out_tokens [B][P+1] int32 (path tokens, bonus, -1 padding)
  * workspace as spec_accept with SPEC_MODE_GREEDY.
  */
-int spec_accept_tree(const spec_dims* d, const void* logits, const int32_t* parent,
+GDN_API int spec_accept_tree(const spec_dims* d, const void* logits, const int32_t* parent,
                      const int32_t* tokens, int32_t P, void* workspace, size_t workspace_bytes,
                      int32_t* path, int32_t* n_acc, int32_t* out_tokens, uint32_t* status,
                      void* stream);
 
 /* Thread-local message for the last non-OK return on this thread ("" if none). */
-const char* gdn_last_error(void);
+GDN_API const char* gdn_last_error(void);
 
 #ifdef __cplusplus
 }

@@ -1,0 +1,262 @@
+// api.cu — the extern "C" boundary of libgdnspec: argument validation, shape dispatch and the
+// thread-local error message. Every entry point only enqueues work on the caller's stream; none
+// allocates, frees or synchronises. See include/gdnspec.h for the contract of each call.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+
+#include "../../include/gdnspec.h"
+#include "kernels.h"
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+    return fail(GDN_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+size_t io_size(int dtype) { return dtype == GDN_DTYPE_BF16 ? 2 : 4; }
+
+// Validates a gdn_dims. Returns GDN_OK, or an error code with g_err set.
+int check_dims(const gdn_dims* d) {
+    if (!d) return fail(GDN_ERR_INVALID_ARG, "dims is NULL");
+    if (d->L < 0 || d->B < 0 || d->T < 0)
+        return fail(GDN_ERR_INVALID_ARG, "negative L/B/T (%d, %d, %d)", d->L, d->B, d->T);
+    if (d->Hk < 1 || d->Hv < 1 || d->Hv % d->Hk != 0)
+        return fail(GDN_ERR_INVALID_ARG, "Hv (%d) must be a positive multiple of Hk (%d)", d->Hv,
+                    d->Hk);
+    if (d->W < 1 || d->W > 4) return fail(GDN_ERR_UNSUPPORTED, "conv width W=%d not in 1..4", d->W);
+    if (d->io_dtype != GDN_DTYPE_BF16 && d->io_dtype != GDN_DTYPE_F32)
+        return fail(GDN_ERR_INVALID_ARG, "io_dtype %d unknown", d->io_dtype);
+    if (d->Dk != d->Dv || (d->Dk != 32 && d->Dk != 64 && d->Dk != 128))
+        return fail(GDN_ERR_UNSUPPORTED, "head dims Dk=%d Dv=%d: built for Dk == Dv in {32,64,128}",
+                    d->Dk, d->Dv);
+    const long long C = 2LL * d->Hk * d->Dk + 1LL * d->Hv * d->Dv;
+    if (d->C != C) return fail(GDN_ERR_INVALID_ARG, "C=%d but 2*Hk*Dk + Hv*Dv = %lld", d->C, C);
+    if (d->T > 32) return fail(GDN_ERR_UNSUPPORTED, "T=%d > 32 positions per call", d->T);
+    if (d->B > 65535 || d->L > 65535 || d->Hv > 65535)
+        return fail(GDN_ERR_UNSUPPORTED, "grid limits: B, L, Hv must be <= 65535");
+    if (!(d->l2_eps >= 0.f) || !std::isfinite(d->qk_scale))
+        return fail(GDN_ERR_INVALID_ARG, "l2_eps must be >= 0 and qk_scale finite");
+    return GDN_OK;
+}
+
+bool empty(const gdn_dims* d) { return d->L == 0 || d->B == 0 || d->T == 0; }
+
+int verify_common(const gdn_dims* d, const int32_t* parent, const void* qkv, const void* conv_w,
+                  const void* conv_state, const float* g, const float* beta, const float* state,
+                  void* out, float* tape_delta, float* tape_k, uint32_t* status, void* stream,
+                  bool tree) {
+    int rc = check_dims(d);
+    if (rc) return rc;
+    if (empty(d)) return GDN_OK;
+    if (!qkv || !conv_w || !g || !beta || !state || !out || !tape_delta || !tape_k ||
+        (d->W > 1 && !conv_state) || (tree && !parent))
+        return fail(GDN_ERR_INVALID_ARG, "NULL tensor pointer");
+    if (!aligned(state, 16))
+        return fail(GDN_ERR_INVALID_ARG, "state must be 16-byte aligned (bulk copies)");
+    const size_t es = io_size(d->io_dtype);
+    if (!aligned(qkv, es) || !aligned(conv_w, es) || (conv_state && !aligned(conv_state, es)) ||
+        !aligned(out, es) || !aligned(g, 4) || !aligned(beta, 4) || !aligned(tape_delta, 4) ||
+        !aligned(tape_k, 4))
+        return fail(GDN_ERR_INVALID_ARG, "misaligned tensor pointer");
+    gdn::VerifyArgs a{};
+    a.L = d->L; a.B = d->B; a.T = d->T; a.Hk = d->Hk; a.Hv = d->Hv; a.W = d->W; a.C = d->C;
+    a.qk_scale = d->qk_scale; a.l2_eps = d->l2_eps;
+    a.qkv = qkv; a.conv_w = conv_w; a.conv_state = conv_state; a.g = g; a.beta = beta;
+    a.state = state; a.out = out; a.tape_delta = tape_delta; a.tape_k = tape_k;
+    a.parent = tree ? parent : nullptr; a.status = status;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = d->io_dtype == GDN_DTYPE_BF16 ? gdn::launch_verify_bf16(a, d->Dk, tree, s)
+                                                  : gdn::launch_verify_f32(a, d->Dk, tree, s);
+    if (e != cudaSuccess) return cuda_fail(e, tree ? "gdn_verify_tree launch" : "gdn_verify launch");
+    return GDN_OK;
+}
+
+int rollback_common(const gdn_dims* d, const int32_t* path, int32_t P, const int32_t* n_acc,
+                    const float* tape_delta, const float* tape_k, const float* g, const void* qkv,
+                    float* state, void* conv_state, uint32_t* status, void* stream) {
+    int rc = check_dims(d);
+    if (rc) return rc;
+    if (path && P < 0) return fail(GDN_ERR_INVALID_ARG, "path capacity P=%d < 0", P);
+    if (empty(d) || (path && P == 0)) return GDN_OK;
+    if (!n_acc || !tape_delta || !tape_k || !g || !qkv || !state || (d->W > 1 && !conv_state))
+        return fail(GDN_ERR_INVALID_ARG, "NULL tensor pointer");
+    if (!aligned(state, 16) || !aligned(tape_delta, 16))
+        return fail(GDN_ERR_INVALID_ARG, "state and tape_delta must be 16-byte aligned");
+    const size_t es = io_size(d->io_dtype);
+    if (!aligned(qkv, es) || (conv_state && !aligned(conv_state, es)) || !aligned(tape_k, 4) ||
+        !aligned(g, 4) || !aligned(n_acc, 4) || (path && !aligned(path, 4)))
+        return fail(GDN_ERR_INVALID_ARG, "misaligned tensor pointer");
+    gdn::RollbackArgs a{};
+    a.L = d->L; a.B = d->B; a.T = d->T; a.Hk = d->Hk; a.Hv = d->Hv; a.W = d->W; a.C = d->C;
+    a.P = path ? P : 0;
+    a.n_acc = n_acc; a.path = path; a.tape_delta = tape_delta; a.tape_k = tape_k; a.g = g;
+    a.qkv = qkv; a.state = state; a.conv_state = conv_state; a.status = status;
+    cudaError_t e = gdn::launch_rollback(a, d->Dk, d->io_dtype, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, path ? "gdn_rollback_path launch" : "gdn_rollback launch");
+    return GDN_OK;
+}
+
+int check_spec(const spec_dims* d) {
+    if (!d) return fail(GDN_ERR_INVALID_ARG, "dims is NULL");
+    if (d->B < 0 || d->N < 0 || d->V < 1)
+        return fail(GDN_ERR_INVALID_ARG, "bad B=%d N=%d V=%d", d->B, d->N, d->V);
+    if (d->dtype != GDN_DTYPE_BF16 && d->dtype != GDN_DTYPE_F32)
+        return fail(GDN_ERR_INVALID_ARG, "logits dtype %d unknown", d->dtype);
+    const int64_t vecn = d->dtype == GDN_DTYPE_BF16 ? 8 : 4;
+    if (d->row_stride < d->V || d->row_stride % vecn != 0)
+        return fail(GDN_ERR_INVALID_ARG, "row_stride %lld must be >= V and a multiple of %lld",
+                    (long long)d->row_stride, (long long)vecn);
+    if (d->seq_stride < 0 || d->seq_stride % vecn != 0)
+        return fail(GDN_ERR_INVALID_ARG, "seq_stride %lld must be >= 0 and a multiple of %lld",
+                    (long long)d->seq_stride, (long long)vecn);
+    if (1LL * d->B * (d->N + 1) > 0x7fffffffLL)
+        return fail(GDN_ERR_UNSUPPORTED, "B*(N+1) rows exceed the grid");
+    return GDN_OK;
+}
+
+size_t ws_bytes(const spec_dims* d, int32_t mode) {
+    const int rows = d->B * (d->N + 1);
+    int CH, CS;
+    gdn::accept_chunking(rows, d->V, &CH, &CS);
+    const size_t keys = size_t(rows) * CH * 8;
+    if (mode == SPEC_MODE_SAMPLE) return keys * 2 + size_t(rows) * 8;
+    return keys;
+}
+
+gdn::AcceptArgs accept_args(const spec_dims* d, const void* logits, void* workspace) {
+    gdn::AcceptArgs a{};
+    a.B = d->B; a.N = d->N; a.V = d->V;
+    const int rows = d->B * (d->N + 1);
+    gdn::accept_chunking(rows, d->V, &a.CH, &a.CS);
+    a.row_stride = d->row_stride; a.seq_stride = d->seq_stride;
+    a.logits = logits;
+    auto* ws = static_cast<unsigned long long*>(workspace);
+    a.ws_key = ws;
+    a.ws_sum = ws + size_t(rows) * a.CH;
+    a.ws_wd = ws + size_t(rows) * a.CH * 2;
+    return a;
+}
+
+}  // namespace
+
+extern "C" {
+
+int gdn_verify(const gdn_dims* d, const void* qkv, const void* conv_w, const void* conv_state,
+               const float* g, const float* beta, const float* state, void* out,
+               float* tape_delta, float* tape_k, uint32_t* status, void* stream) {
+    return verify_common(d, nullptr, qkv, conv_w, conv_state, g, beta, state, out, tape_delta,
+                         tape_k, status, stream, false);
+}
+
+int gdn_verify_tree(const gdn_dims* d, const int32_t* parent, const void* qkv,
+                    const void* conv_w, const void* conv_state, const float* g,
+                    const float* beta, const float* state, void* out, float* tape_delta,
+                    float* tape_k, uint32_t* status, void* stream) {
+    return verify_common(d, parent, qkv, conv_w, conv_state, g, beta, state, out, tape_delta,
+                         tape_k, status, stream, true);
+}
+
+int gdn_rollback(const gdn_dims* d, const int32_t* n_acc, const float* tape_delta,
+                 const float* tape_k, const float* g, const void* qkv, float* state,
+                 void* conv_state, uint32_t* status, void* stream) {
+    return rollback_common(d, nullptr, 0, n_acc, tape_delta, tape_k, g, qkv, state, conv_state,
+                           status, stream);
+}
+
+int gdn_rollback_path(const gdn_dims* d, const int32_t* path, int32_t P, const int32_t* n_acc,
+                      const float* tape_delta, const float* tape_k, const float* g,
+                      const void* qkv, float* state, void* conv_state, uint32_t* status,
+                      void* stream) {
+    if (!path) return fail(GDN_ERR_INVALID_ARG, "path is NULL");
+    return rollback_common(d, path, P, n_acc, tape_delta, tape_k, g, qkv, state, conv_state,
+                           status, stream);
+}
+
+size_t gdn_tape_bytes(const gdn_dims* d) {
+    if (check_dims(d) != GDN_OK) return 0;
+    const size_t lbt = size_t(d->L) * d->B * d->T;
+    return lbt * (size_t(d->Hv) * d->Dv + size_t(d->Hk) * d->Dk) * 4;
+}
+
+int spec_accept(const spec_dims* d, const void* logits, const int32_t* drafts, int32_t mode,
+                float temperature, uint64_t seed, uint64_t round, void* workspace,
+                size_t workspace_bytes, int32_t* n_acc, int32_t* out_tokens, uint32_t* status,
+                void* stream) {
+    int rc = check_spec(d);
+    if (rc) return rc;
+    if (mode != SPEC_MODE_GREEDY && mode != SPEC_MODE_SAMPLE)
+        return fail(GDN_ERR_INVALID_ARG, "mode %d unknown", mode);
+    if (mode == SPEC_MODE_SAMPLE && !(temperature > 0.f)) mode = SPEC_MODE_GREEDY;
+    if (mode == SPEC_MODE_SAMPLE && !std::isfinite(temperature))
+        return fail(GDN_ERR_INVALID_ARG, "temperature must be finite");
+    if (d->B == 0) return GDN_OK;
+    if (!logits || !n_acc || !out_tokens || !workspace || (d->N > 0 && !drafts))
+        return fail(GDN_ERR_INVALID_ARG, "NULL pointer");
+    if (!aligned(logits, 16) || !aligned(workspace, 16))
+        return fail(GDN_ERR_INVALID_ARG, "logits and workspace must be 16-byte aligned");
+    const size_t need = ws_bytes(d, mode);
+    if (workspace_bytes < need)
+        return fail(GDN_ERR_INVALID_ARG, "workspace %zu bytes < %zu required", workspace_bytes, need);
+    gdn::AcceptArgs a = accept_args(d, logits, workspace);
+    a.drafts = drafts; a.n_acc = n_acc; a.out_tokens = out_tokens; a.status = status;
+    a.seed = seed; a.round = uint32_t(round);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (mode == SPEC_MODE_SAMPLE) {
+        a.c = float((1.0 / std::log(2.0)) / double(temperature));
+        e = gdn::launch_accept_sample(a, d->dtype, s);
+    } else {
+        e = gdn::launch_accept_greedy(a, d->dtype, s);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "spec_accept launch");
+    return GDN_OK;
+}
+
+size_t spec_workspace_bytes(const spec_dims* d, int32_t mode) {
+    if (check_spec(d) != GDN_OK) return 0;
+    if (mode != SPEC_MODE_GREEDY && mode != SPEC_MODE_SAMPLE) return 0;
+    return ws_bytes(d, mode);
+}
+
+int spec_accept_tree(const spec_dims* d, const void* logits, const int32_t* parent,
+                     const int32_t* tokens, int32_t P, void* workspace, size_t workspace_bytes,
+                     int32_t* path, int32_t* n_acc, int32_t* out_tokens, uint32_t* status,
+                     void* stream) {
+    int rc = check_spec(d);
+    if (rc) return rc;
+    if (P < 0) return fail(GDN_ERR_INVALID_ARG, "path capacity P=%d < 0", P);
+    if (d->B == 0) return GDN_OK;
+    if (!logits || !n_acc || !out_tokens || !workspace || !path ||
+        (d->N > 0 && (!parent || !tokens)))
+        return fail(GDN_ERR_INVALID_ARG, "NULL pointer");
+    if (!aligned(logits, 16) || !aligned(workspace, 16))
+        return fail(GDN_ERR_INVALID_ARG, "logits and workspace must be 16-byte aligned");
+    const size_t need = ws_bytes(d, SPEC_MODE_GREEDY);
+    if (workspace_bytes < need)
+        return fail(GDN_ERR_INVALID_ARG, "workspace %zu bytes < %zu required", workspace_bytes, need);
+    gdn::AcceptArgs a = accept_args(d, logits, workspace);
+    a.drafts = tokens; a.parent = parent; a.P = P;
+    a.n_acc = n_acc; a.out_tokens = out_tokens; a.path = path; a.status = status;
+    cudaError_t e = gdn::launch_accept_tree(a, d->dtype, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "spec_accept_tree launch");
+    return GDN_OK;
+}
+
+const char* gdn_last_error(void) { return g_err; }
+
+}  // extern "C"

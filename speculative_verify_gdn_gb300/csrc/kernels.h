@@ -1,0 +1,70 @@
+// kernels.h — host-side launch entry points of the gdnspec kernels (internal to the library).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace gdn {
+
+struct VerifyArgs {
+    int L, B, T, Hk, Hv, W, C;
+    float qk_scale, l2_eps;
+    const void* qkv;
+    const void* conv_w;
+    const void* conv_state;
+    const float* g;
+    const float* beta;
+    const float* state;
+    void* out;
+    float* tape_delta;
+    float* tape_k;
+    const int32_t* parent;   // tree only (null for the chain)
+    uint32_t* status;
+};
+
+// verify: D = Dk = Dv; one translation unit per element type of qkv / conv / out.
+cudaError_t launch_verify_bf16(const VerifyArgs& a, int D, bool tree, cudaStream_t s);
+cudaError_t launch_verify_f32(const VerifyArgs& a, int D, bool tree, cudaStream_t s);
+
+struct RollbackArgs {
+    int L, B, T, Hk, Hv, W, C, P;
+    const int32_t* n_acc;
+    const int32_t* path;      // null for the chain
+    const float* tape_delta;
+    const float* tape_k;
+    const float* g;
+    const void* qkv;
+    float* state;
+    void* conv_state;
+    uint32_t* status;
+};
+cudaError_t launch_rollback(const RollbackArgs& a, int D, int io_dtype, cudaStream_t s);
+
+struct AcceptArgs {
+    int B, N, V;              // N = drafts (chain) or nodes (tree); rows per sequence = N + 1
+    int CH, CS;               // vocabulary chunks per row and chunk length
+    int64_t row_stride, seq_stride;
+    const void* logits;
+    const int32_t* drafts;    // chain drafts, or the tree's node tokens
+    const int32_t* parent;    // tree only
+    int P;                    // tree path capacity
+    float c;                  // sampling: fp32(log2(e) / temperature)
+    uint64_t seed;
+    uint32_t round;
+    unsigned long long* ws_key;
+    unsigned long long* ws_sum;
+    unsigned long long* ws_wd;
+    int32_t* n_acc;
+    int32_t* out_tokens;
+    int32_t* path;
+    uint32_t* status;
+};
+
+// Vocabulary chunking shared by spec_accept's workspace size query and its launches.
+void accept_chunking(int rows, int V, int* CH, int* CS);
+
+cudaError_t launch_accept_greedy(const AcceptArgs& a, int dtype, cudaStream_t s);
+cudaError_t launch_accept_sample(const AcceptArgs& a, int dtype, cudaStream_t s);
+cudaError_t launch_accept_tree(const AcceptArgs& a, int dtype, cudaStream_t s);
+
+}  // namespace gdn

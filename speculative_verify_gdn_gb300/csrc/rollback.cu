@@ -1,0 +1,178 @@
+// rollback.cu — gdn_rollback / gdn_rollback_path: tape-replay rollback (sm_103a).
+//
+// "Speculative Decoding on GDN Hybrid Architectures: A 31-Experiment Investigation", §4
+// (Tape-Replay 回滚): after a partial acceptance of n of the T verified positions, restore the
+// pre-verify snapshot and replay only the accepted steps, state = state·g[t] + δ[t] k[t]ᵀ for
+// t < n, at cost O(n); rebuild the conv state from the last (W−1) raw qkv rows.
+//
+// Here the snapshot is the state buffer itself (verify never writes it), so "restore" is free and
+// the replay of n steps is folded into one pass over the state:
+//     S_n = Γ_total · S_0 + Σ_{s<n} (Γ_{s+1..n-1} δ_s) k_sᵀ,   Γ_total = Π_{s<n} g_s,
+// which reads and writes each state element once (HBM-bound) with n+1 FMAs per element.
+// One 256-thread CTA per (layer, sequence, value head); n is read on the device, so a CTA whose
+// sequence accepted nothing exits at once and the whole call needs no host synchronisation.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace gdn {
+
+template <typename IO, int D, int NMAX, bool PATH>
+__global__ void __launch_bounds__(256)
+gdn_rollback_kernel(const RollbackArgs a) {
+    constexpr int RPL = D / 32;      // consecutive state rows i per lane
+    constexpr int NW = 8;            // warps; warp w owns key columns j = w, w + 8, ...
+    constexpr int JPW = D / NW;
+    __shared__ float Ks[NMAX][D];
+    __shared__ float coef[NMAX];
+    __shared__ int nodes[NMAX];
+    __shared__ float gtot;
+    __shared__ int bad;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int h = blockIdx.x, b = blockIdx.y, l = blockIdx.z;
+    const int T = a.T, Hv = a.Hv, Hk = a.Hk, C = a.C, W = a.W;
+    const int kh = h / (Hv / Hk);
+    const size_t lb = size_t(l) * a.B + b;
+
+    const int n = __ldg(a.n_acc + b);
+    const int cap = PATH ? (a.P < T ? a.P : T) : T;
+    if (n < 0 || n > cap) {
+        if (tid == 0 && h == 0 && l == 0) set_status(a.status, GDN_STATUS_BAD_NACC);
+        return;
+    }
+    if (n == 0) return;              // the snapshot is still in place
+
+    if (tid == 0) bad = 0;
+    __syncthreads();
+    if (tid < n) {
+        const int nd = PATH ? __ldg(a.path + size_t(b) * a.P + tid) : tid;
+        if (nd < 0 || nd >= T) atomicOr(&bad, 1);
+        nodes[tid] = nd;
+    }
+    __syncthreads();
+    if (bad) {
+        if (tid == 0 && h == 0 && l == 0) set_status(a.status, GDN_STATUS_BAD_PATH);
+        return;
+    }
+    if (tid == 0) {
+        float c = 1.f;
+        for (int s = n - 1; s >= 0; --s) {
+            coef[s] = c;                                   // Γ_{s+1..n-1}
+            c *= __ldg(a.g + (lb * T + nodes[s]) * Hv + h);
+        }
+        gtot = c;                                          // Γ_{0..n-1}
+    }
+    for (int idx = tid; idx < n * D; idx += 256) {
+        const int s = idx / D, j = idx - s * D;
+        Ks[s][j] = __ldg(a.tape_k + ((lb * T + nodes[s]) * Hk + kh) * size_t(D) + j);
+    }
+    __syncthreads();
+
+    // scaled innovations of this lane's rows, δ'_s[i] = Γ_{s+1..n-1} δ_s[i]
+    const int i0 = lane * RPL;
+    float dl[NMAX][RPL];
+#pragma unroll
+    for (int s = 0; s < NMAX; ++s) {
+#pragma unroll
+        for (int r = 0; r < RPL; ++r) dl[s][r] = 0.f;
+        if (s < n) {
+            const float* src = a.tape_delta + ((lb * T + nodes[s]) * Hv + h) * size_t(D) + i0;
+#pragma unroll
+            for (int r = 0; r < RPL; ++r) dl[s][r] = coef[s] * __ldg(src + r);
+        }
+    }
+    const float G = gtot;
+
+    float* S = a.state + (lb * Hv + h) * size_t(D) * D;   // [j][i]
+    constexpr int UN = JPW < 8 ? JPW : 8;
+#pragma unroll 1
+    for (int j0 = 0; j0 < JPW; j0 += UN) {
+        float v[UN][RPL];
+#pragma unroll
+        for (int u = 0; u < UN; ++u) {
+            const int j = warp + NW * (j0 + u);
+            const float* p = S + size_t(j) * D + i0;
+            if constexpr (RPL == 4) {
+                const float4 x = __ldcs(reinterpret_cast<const float4*>(p));
+                v[u][0] = x.x; v[u][1] = x.y; v[u][2] = x.z; v[u][3] = x.w;
+            } else if constexpr (RPL == 2) {
+                const float2 x = __ldcs(reinterpret_cast<const float2*>(p));
+                v[u][0] = x.x; v[u][1] = x.y;
+            } else {
+                v[u][0] = __ldcs(p);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < UN; ++u) {
+            const int j = warp + NW * (j0 + u);
+#pragma unroll
+            for (int r = 0; r < RPL; ++r) v[u][r] *= G;
+#pragma unroll
+            for (int s = 0; s < NMAX; ++s) {
+                if (s < n) {
+                    const float k = Ks[s][j];
+#pragma unroll
+                    for (int r = 0; r < RPL; ++r) v[u][r] = fmaf(dl[s][r], k, v[u][r]);
+                }
+            }
+            float* p = S + size_t(j) * D + i0;
+            if constexpr (RPL == 4) {
+                __stcs(reinterpret_cast<float4*>(p), make_float4(v[u][0], v[u][1], v[u][2], v[u][3]));
+            } else if constexpr (RPL == 2) {
+                __stcs(reinterpret_cast<float2*>(p), make_float2(v[u][0], v[u][1]));
+            } else {
+                __stcs(p, v[u][0]);
+            }
+        }
+    }
+
+    // conv state: last W-1 rows of (conv_state ++ accepted raw rows); channels split over heads
+    const int cper = (C + Hv - 1) / Hv;
+    const int c_lo = h * cper, c_hi = min(C, c_lo + cper);
+    IO* cs = static_cast<IO*>(a.conv_state) + lb * size_t(W - 1) * C;
+    const IO* x = static_cast<const IO*>(a.qkv) + lb * size_t(T) * C;
+    for (int c = c_lo + tid; c < c_hi; c += 256) {
+        IO vals[3];
+#pragma unroll
+        for (int r = 0; r < 3; ++r) {
+            if (r < W - 1) {
+                const int q = n + r;   // index in the combined sequence
+                vals[r] = (q < W - 1) ? cs[size_t(q) * C + c]
+                                      : x[size_t(nodes[q - (W - 1)]) * C + c];
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < 3; ++r)
+            if (r < W - 1) cs[size_t(r) * C + c] = vals[r];
+    }
+}
+
+template <typename IO, int D, int NMAX, bool PATH>
+static cudaError_t launch_rb(const RollbackArgs& a, cudaStream_t s) {
+    dim3 grid(a.Hv, a.B, a.L);
+    gdn_rollback_kernel<IO, D, NMAX, PATH><<<grid, 256, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+template <typename IO, bool PATH>
+static cudaError_t launch_rb_io(const RollbackArgs& a, int D, cudaStream_t s) {
+    const int cap = PATH ? (a.P < a.T ? a.P : a.T) : a.T;
+    const int nm = cap <= 4 ? 4 : cap <= 8 ? 8 : cap <= 16 ? 16 : 32;
+#define GDN_R_CASE(DD, NM) \
+    if (D == DD && nm == NM) return launch_rb<IO, DD, NM, PATH>(a, s);
+    GDN_R_CASE(32, 4) GDN_R_CASE(32, 8) GDN_R_CASE(32, 16) GDN_R_CASE(32, 32)
+    GDN_R_CASE(64, 4) GDN_R_CASE(64, 8) GDN_R_CASE(64, 16) GDN_R_CASE(64, 32)
+    GDN_R_CASE(128, 4) GDN_R_CASE(128, 8) GDN_R_CASE(128, 16) GDN_R_CASE(128, 32)
+#undef GDN_R_CASE
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_rollback(const RollbackArgs& a, int D, int io_dtype, cudaStream_t s) {
+    const bool path = a.path != nullptr;
+    if (io_dtype == GDN_DTYPE_BF16)
+        return path ? launch_rb_io<__nv_bfloat16, true>(a, D, s)
+                    : launch_rb_io<__nv_bfloat16, false>(a, D, s);
+    return path ? launch_rb_io<float, true>(a, D, s) : launch_rb_io<float, false>(a, D, s);
+}
+
+}  // namespace gdn

@@ -1,0 +1,105 @@
+"""The C-ABI library builds, loads without a GPU, exports every entry point include/*.h declares,
+and its host-side checks (sizes, argument validation) work with no device. No compute calls."""
+import ctypes as ct
+import glob
+import os
+import re
+
+import pytest
+
+from speculative_verify_gdn_gb300 import _lib, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = []
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = open(h).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        names += re.findall(r"GDN_API\s+[\w\s\*]+?\b(\w+)\s*\(", src)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return _lib.load()
+
+
+def test_header_declares_the_expected_calls():
+    assert set(declared_functions()) == set(_lib.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_no_unexpected_exports(lib):
+    import subprocess
+    out = subprocess.run(["nm", "-D", "--defined-only", _lib.library_path()], capture_output=True,
+                         text=True).stdout
+    syms = {ln.split()[-1] for ln in out.splitlines() if " T " in ln}
+    extra = {s for s in syms if not s.startswith("_")} - set(_lib.EXPORTS)
+    assert not extra, extra
+
+
+def qwen_shape(**kw):
+    d = dict(L=30, B=64, T=8, Hk=16, Hv=32, Dk=128, Dv=128, W=4)
+    d.update(kw)
+    return _lib.GdnShape(**d)
+
+
+def test_tape_bytes(lib):
+    sh = qwen_shape()
+    expect = 30 * 64 * 8 * (32 * 128 + 16 * 128) * 4
+    assert _lib.tape_bytes(sh) == expect
+    assert _lib.tape_bytes(qwen_shape(Dk=96, Dv=96)) == 0       # unsupported head dim
+    assert _lib.tape_bytes(qwen_shape(Hv=24)) == 0             # Hv not a multiple of Hk... 24%16
+
+
+def test_workspace_bytes(lib):
+    g = _lib.workspace_bytes(64, 8, 151936)
+    s = _lib.workspace_bytes(64, 8, 151936, _lib.SPEC_MODE_SAMPLE)
+    assert g > 0 and s > 2 * g - 1
+    assert _lib.workspace_bytes(1, 4, 151936) >= 5 * 8
+
+
+def call_verify(lib, d, ptrs):
+    return lib.gdn_verify(ct.byref(d), *ptrs, None, None)
+
+
+def test_host_validation_rejects_bad_arguments_without_a_gpu(lib):
+    fake = ct.c_void_p(0x100000)        # never dereferenced: validation fails first
+    d = qwen_shape().c()
+    # NULL tensors
+    assert call_verify(lib, d, [None] * 9) == 1
+    assert "NULL" in _lib.last_error()
+    # inconsistent channel count
+    d2 = qwen_shape().c()
+    d2.C = 100
+    assert call_verify(lib, d2, [fake] * 9) == 1
+    assert "C=" in _lib.last_error()
+    # unsupported head dim / conv width / T
+    assert call_verify(lib, qwen_shape(Dk=96, Dv=96).c(), [fake] * 9) == 2
+    assert call_verify(lib, qwen_shape(W=5).c(), [fake] * 9) == 2
+    assert call_verify(lib, qwen_shape(T=33).c(), [fake] * 9) == 2
+    # misaligned state
+    bad = [fake] * 9
+    bad[5] = ct.c_void_p(0x100004)
+    assert call_verify(lib, d, bad) == 1 and "aligned" in _lib.last_error()
+    # empty shapes are no-ops (no launch)
+    assert call_verify(lib, qwen_shape(B=0).c(), [None] * 9) == 0
+    # rollback / accept argument checks
+    assert lib.gdn_rollback(ct.byref(d), None, None, None, None, None, None, None, None,
+                            None) == 1
+    sd = _lib._SpecDims(4, 3, 1000, _lib.GDN_DTYPE_BF16, 1001, 0)    # stride not 16-byte
+    assert lib.spec_accept(ct.byref(sd), fake, fake, 0, 0.0, 0, 0, fake, 1 << 20, fake, fake,
+                           None, None) == 1
+    sd = _lib._SpecDims(4, 3, 1000, _lib.GDN_DTYPE_BF16, 1000, 4000)
+    assert lib.spec_accept(ct.byref(sd), fake, fake, 0, 0.0, 0, 0, fake, 8, fake, fake,
+                           None, None) == 1
+    assert "workspace" in _lib.last_error()
+    assert lib.spec_accept(ct.byref(sd), fake, fake, 7, 0.0, 0, 0, fake, 1 << 20, fake, fake,
+                           None, None) == 1

@@ -1,0 +1,342 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle on the same seeded inputs.
+
+Small shapes are compared in full; the full-size workloads are compared on sampled
+(layer, sequence) units plus every accept output, with inputs drawn on the device (seeded) and the
+sampled slices copied to the host for the oracle.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from speculative_verify_gdn_gb300 import _lib, inputs as I
+from speculative_verify_gdn_gb300.round import SpecRound
+from parity_util import (assert_close, f64, logits_f32, oracle_rollback, oracle_verify, to_dev)
+
+pytestmark = pytest.mark.gpu
+
+
+def small(base, **kw):
+    kw.setdefault("name", "small_" + "_".join("%s%s" % (k, v) for k, v in sorted(kw.items())))
+    return I.custom(base, **kw)
+
+
+def make_model(w, seed=0, device="cpu"):
+    cw = I.model_weights(w, seed, device)
+    st, cs = I.initial_state(w, seed, device)
+    return cw, st, cs
+
+
+def run_verify_case(w, seed=0, parent=None):
+    cw, st, cs = make_model(w, seed)
+    qkv, g, beta = I.round_stream(w, 0, seed)
+    r = SpecRound(w)
+    dq, dcw, dcs, dg, db, dst = to_dev(qkv, cw, cs, g, beta, st)
+    dpar = None if parent is None else parent.cuda()
+    r.verify(dq, dcw, dcs, dg, db, dst, parent=dpar)
+    r.check_status()
+    ref = oracle_verify(w, qkv, cw, cs, g, beta, st, parent=parent)
+    assert_close(f64(r.out), ref["out"], "out")
+    assert_close(f64(r.tape_delta), ref["tape_delta"], "tape_delta")
+    assert_close(f64(r.tape_k), ref["tape_k"], "tape_k")
+    # the snapshot is untouched
+    assert torch.equal(dst.cpu(), st) and torch.equal(dcs.cpu(), cs)
+    return r, ref, (qkv, cw, cs, g, beta, st), (dq, dcw, dcs, dg, db, dst)
+
+
+# ------------------------------------------------------------------------------ verify
+def test_verify_tiny_workload(gdnlib):
+    run_verify_case(I.WORKLOADS[0])
+
+
+@pytest.mark.parametrize("D", [32, 64, 128])
+@pytest.mark.parametrize("T", [1, 3, 4, 5, 8, 13, 16, 32])
+def test_verify_shapes(gdnlib, D, T):
+    w = small(I.WORKLOADS[1], L=2, B=3, N=T, Hk=2, Hv=4, D=D, W=4, V=64)
+    run_verify_case(w, seed=T * 7 + D)
+
+
+@pytest.mark.parametrize("W", [1, 2, 3])
+@pytest.mark.parametrize("io", [torch.float32, torch.bfloat16])
+def test_verify_conv_widths_and_dtypes(gdnlib, W, io):
+    w = small(I.WORKLOADS[1], L=1, B=2, N=6, Hk=1, Hv=3, D=32, W=W, V=64, io_dtype=io)
+    run_verify_case(w, seed=W)
+
+
+def test_verify_qwen36_b1(gdnlib):
+    """The 30-layer Qwen3.6-shaped stack at batch 1, N = 4, every output compared."""
+    run_verify_case(I.WORKLOADS[1])
+
+
+def test_verify_empty_is_noop(gdnlib):
+    sh = _lib.GdnShape(L=1, B=1, T=0, Hk=2, Hv=4, Dk=32, Dv=32, W=4, io_dtype=torch.float32)
+    z = lambda *s: torch.zeros(s, device="cuda")
+    _lib.verify(sh, z(1, 1, 0, sh.C), z(1, sh.C, 4), z(1, 1, 3, sh.C), z(1, 1, 0, 4),
+                z(1, 1, 0, 4), z(1, 1, 4, 32, 32), z(1, 1, 0, 4, 32), z(1, 1, 0, 4, 32),
+                z(1, 1, 0, 2, 32))
+
+
+# ------------------------------------------------------------------------------ rollback
+@pytest.mark.parametrize("D,T", [(32, 4), (64, 8), (128, 5), (128, 16), (32, 32)])
+def test_rollback_matches_oracle(gdnlib, D, T):
+    w = small(I.WORKLOADS[1], L=2, B=5, N=T, Hk=2, Hv=4, D=D, W=4, V=64)
+    r, ref, host, dev = run_verify_case(w, seed=D + T)
+    qkv, cw, cs, g, beta, st = host
+    dq, dcw, dcs, dg, db, dst = dev
+    n = np.array([0, T, 1, min(2, T), T // 2], np.int32)
+    r.n_acc.copy_(torch.from_numpy(n))
+    r.rollback(dq, dg, dst, dcs)
+    r.check_status()
+    st_ref, cs_ref, bad = oracle_rollback(w, n, ref, g, qkv, st, cs)
+    assert bad == 0
+    assert_close(f64(dst), st_ref, "state")
+    # the conv state is a copy of raw rows: exact
+    assert np.array_equal(f64(dcs), cs_ref)
+    # n = 0 leaves the snapshot bit-identical
+    assert torch.equal(dst[:, 0].cpu(), st[:, 0])
+
+
+def test_rollback_bad_count_sets_status_and_skips(gdnlib):
+    w = small(I.WORKLOADS[1], L=1, B=2, N=4, Hk=2, Hv=4, D=32, V=64)
+    r, ref, host, dev = run_verify_case(w)
+    dq, dcw, dcs, dg, db, dst = dev
+    before = dst.clone()
+    r.n_acc.copy_(torch.tensor([5, -1], dtype=torch.int32))
+    r.rollback(dq, dg, dst, dcs)
+    torch.cuda.synchronize()
+    assert int(r.status.item()) & 0x1
+    assert torch.equal(before, dst)
+
+
+# ------------------------------------------------------------------------------ greedy accept
+@pytest.mark.parametrize("wid", [0, 1])
+def test_greedy_accept_bit_exact(gdnlib, wid):
+    w = I.WORKLOADS[wid]
+    r = SpecRound(w)
+    for rnd in range(8):
+        lg, dr, L = I.greedy_logits(w, rnd)
+        dlg, ddr = to_dev(lg, dr)
+        r.accept(dlg, ddr, round_=rnd)
+        r.check_status()
+        n, out, bad = oracle.accept_greedy(logits_f32(lg), dr.numpy())
+        assert np.array_equal(r.n_acc.cpu().numpy(), n)
+        assert np.array_equal(r.out_tokens.cpu().numpy(), out)
+        assert np.array_equal(n, L.numpy())
+
+
+@pytest.mark.parametrize("V", [1000, 1003, 8191, 151936])
+def test_greedy_accept_ties_and_ragged_vocab(gdnlib, V):
+    torch.manual_seed(V)
+    B, N = 7, 5
+    Vpad = (V + 7) // 8 * 8
+    lg = torch.randint(-3, 3, (B, N + 1, Vpad)).to(torch.bfloat16)   # many exact ties
+    lg[..., V:] = 100                                                   # padding never read
+    am = lg[..., :V].float().argmax(-1)
+    dr = am[:, :N].clone().to(torch.int32)
+    dr[1, 0] = (dr[1, 0] + 1) % V
+    dr[3, 2] = (dr[3, 2] + 1) % V
+    ws = torch.empty(_lib.workspace_bytes(B, N, V), dtype=torch.uint8, device="cuda")
+    n_acc = torch.empty(B, dtype=torch.int32, device="cuda")
+    out = torch.empty(B, N + 1, dtype=torch.int32, device="cuda")
+    dlg, ddr = to_dev(lg, dr)
+    _lib.spec_accept(dlg, ddr, n_acc, out, ws, V=V)
+    torch.cuda.synchronize()
+    n_ref, out_ref, _ = oracle.accept_greedy(logits_f32(lg[..., :V].contiguous()), dr.numpy())
+    assert np.array_equal(n_acc.cpu().numpy(), n_ref)
+    assert np.array_equal(out.cpu().numpy(), out_ref)
+
+
+def test_accept_bad_draft_token(gdnlib):
+    w = small(I.WORKLOADS[0], B=3, name="bad_tok")
+    r = SpecRound(w)
+    lg, dr, _ = I.greedy_logits(w, 0)
+    dr[1, 2] = w.V + 5
+    dlg, ddr = to_dev(lg, dr)
+    r.accept(dlg, ddr)
+    torch.cuda.synchronize()
+    assert int(r.status.item()) & 0x4
+    n_ref, out_ref, bad = oracle.accept_greedy(logits_f32(lg), dr.numpy())
+    assert bad == 4
+    assert np.array_equal(r.n_acc.cpu().numpy(), n_ref)
+    assert np.array_equal(r.out_tokens.cpu().numpy(), out_ref)
+
+
+# ------------------------------------------------------------------------------ sampling accept
+@pytest.mark.parametrize("V,B,N", [(4096, 16, 16), (151936, 16, 16), (1000, 5, 0), (333, 9, 3)])
+def test_sample_accept_bit_exact(gdnlib, V, B, N):
+    w = I.custom(I.WORKLOADS[3], name="samp_%d_%d_%d" % (V, B, N), V=V, B=B, N=N, L=1)
+    Vpad = (V + 7) // 8 * 8
+    ws = torch.empty(_lib.workspace_bytes(B, N, V, _lib.SPEC_MODE_SAMPLE), dtype=torch.uint8,
+                     device="cuda")
+    n_acc = torch.empty(B, dtype=torch.int32, device="cuda")
+    out = torch.empty(B, N + 1, dtype=torch.int32, device="cuda")
+    for rnd in range(3):
+        lg, dr = I.sample_logits(w, rnd)
+        # perturb some drafts away from the argmax so both accept and reject paths run
+        dr[::2, ::3] = (dr[::2, ::3] + 1) % V
+        pad = torch.full((B, N + 1, Vpad), 50.0).to(lg.dtype)     # padding is never read
+        pad[..., :V] = lg
+        dlg, ddr = to_dev(pad, dr)
+        _lib.spec_accept(dlg, ddr, n_acc, out, ws, mode=_lib.SPEC_MODE_SAMPLE,
+                         temperature=w.temperature, seed=77, round_=rnd, V=V)
+        torch.cuda.synchronize()
+        n, out_ref, bad = oracle.accept_sample(logits_f32(lg), dr.numpy(), w.temperature, 77, rnd)
+        assert bad == 0
+        assert np.array_equal(n_acc.cpu().numpy(), n)
+        assert np.array_equal(out.cpu().numpy(), out_ref)
+
+
+def test_sample_accept_chi_square_gpu(gdnlib):
+    """Emitted first tokens follow p over 10^6 GPU draws (all sequences share one logits block)."""
+    from scipy import stats
+    V, T, Bn = 48, 0.7, 1_000_000
+    g = np.random.default_rng(3)
+    lg = torch.from_numpy((g.standard_normal((1, 2, V)) * 2).astype(np.float32))
+    p = np.exp((lg[0, 0].double().numpy() - lg[0, 0].double().numpy().max()) / np.float32(T))
+    p /= p.sum()
+    dr = torch.from_numpy(g.integers(0, V, (Bn, 1)).astype(np.int32))
+    ws = torch.empty(_lib.workspace_bytes(Bn, 1, V, _lib.SPEC_MODE_SAMPLE, torch.float32),
+                     dtype=torch.uint8, device="cuda")
+    n_acc = torch.empty(Bn, dtype=torch.int32, device="cuda")
+    out = torch.empty(Bn, 2, dtype=torch.int32, device="cuda")
+    _lib.spec_accept(lg.cuda(), dr.cuda(), n_acc, out, ws, mode=_lib.SPEC_MODE_SAMPLE,
+                     temperature=T, seed=99, round_=4, broadcast_B=Bn)
+    first = out[:, 0].cpu().numpy()
+    counts = np.bincount(first, minlength=V)
+    exp = p * Bn
+    keep = exp >= 5
+    obs = np.append(counts[keep], counts[~keep].sum())
+    ex = np.append(exp[keep], exp[~keep].sum())
+    assert stats.chisquare(obs, ex * obs.sum() / ex.sum()).pvalue > 1e-3
+    # the same draws as the oracle on a subset
+    n_o, out_o, _ = oracle.accept_sample(lg.numpy(), dr.numpy()[:5000], T, 99, 4,
+                                         seq_shared=True, B=5000)
+    assert np.array_equal(out.cpu().numpy()[:5000], out_o)
+
+
+# ------------------------------------------------------------------------------ tree
+def tree_case(B=3, T=12, D=32, L=2, depth=5, seed=0):
+    w = I.custom(I.WORKLOADS[4], name="tree_%d_%d_%d" % (B, T, D), L=L, B=B, N=T, Hk=2, Hv=4,
+                 D=D, V=500, tree_depth=depth)
+    par = I.random_tree(w, 0, seed)
+    return w, par
+
+
+@pytest.mark.parametrize("T,D", [(12, 32), (32, 64), (7, 128)])
+def test_tree_verify_matches_oracle(gdnlib, T, D):
+    w, par = tree_case(T=T, D=D, depth=min(8, T))
+    run_verify_case(w, parent=par)
+
+
+def test_tree_accept_and_path_rollback(gdnlib):
+    w, par = tree_case(B=4, T=20, D=32, depth=6)
+    r, ref, host, dev = run_verify_case(w, parent=par)
+    qkv, cw, cs, g, beta, st = host
+    dq, dcw, dcs, dg, db, dst = dev
+    tok, lg, Ls = I.tree_tokens_and_logits(w, par, 0)
+    dpar, dtok, dlg = to_dev(par, tok, lg)
+    r.accept(dlg, dtok, parent=dpar)
+    r.check_status()
+    path, n, out, bad = oracle.accept_tree(logits_f32(lg), par.numpy(), tok.numpy(), w.P)
+    assert bad == 0
+    assert np.array_equal(n, Ls.numpy())
+    assert np.array_equal(r.n_acc.cpu().numpy(), n)
+    assert np.array_equal(r.path.cpu().numpy(), path)
+    assert np.array_equal(r.out_tokens.cpu().numpy(), out)
+    r.rollback(dq, dg, dst, dcs)
+    r.check_status()
+    st_ref, cs_ref, bad = oracle_rollback(w, n, ref, g, qkv, st, cs, path=path)
+    assert bad == 0
+    assert_close(f64(dst), st_ref, "state")
+    assert np.array_equal(f64(dcs), cs_ref)
+
+
+def test_tree_bad_parent_sets_status(gdnlib):
+    w, par = tree_case(B=2, T=6, D=32, depth=4)
+    par = par.clone()
+    par[1, 3] = 5            # parent after the node
+    cw, st, cs = make_model(w)
+    qkv, g, beta = I.round_stream(w, 0)
+    r = SpecRound(w)
+    dq, dcw, dcs, dg, db, dst = to_dev(qkv, cw, cs, g, beta, st)
+    r.verify(dq, dcw, dcs, dg, db, dst, parent=par.cuda())
+    torch.cuda.synchronize()
+    assert int(r.status.item()) & 0x2
+
+
+# ------------------------------------------------------------------------------ multi-round
+def test_three_rounds_small_stack(gdnlib):
+    """verify -> accept -> rollback chained over rounds, state carried on both sides."""
+    w = small(I.WORKLOADS[2], L=3, B=6, N=8, Hk=2, Hv=4, D=64, V=2048, name="rounds3")
+    cw, st, cs = make_model(w)
+    dcw, dst, dcs = to_dev(cw, st, cs)
+    r = SpecRound(w)
+    st_ref, cs_ref = f64(st), f64(cs)
+    for rnd in range(3):
+        qkv, g, beta = I.round_stream(w, rnd)
+        lg, dr, L = I.greedy_logits(w, rnd)
+        dq, dg, db, dlg, ddr = to_dev(qkv, g, beta, lg, dr)
+        r.step(dq, dg, db, dlg, ddr, dcw, dst, dcs, round_=rnd)
+        r.check_status()
+        d = oracle.OracleDims(L=w.L, B=w.B, T=w.N, Hk=w.Hk, Hv=w.Hv, Dk=w.D, Dv=w.D, W=w.W)
+        ref = oracle.verify(d, f64(qkv), f64(cw), cs_ref, f64(g), f64(beta), st_ref)
+        n, out, _ = oracle.accept_greedy(logits_f32(lg), dr.numpy())
+        assert np.array_equal(r.n_acc.cpu().numpy(), n)
+        assert_close(f64(r.out), ref["out"], "out round %d" % rnd)
+        st_ref, cs_ref, _ = oracle.rollback(d, n, ref["tape_delta"], ref["tape_k"], f64(g),
+                                            f64(qkv), st_ref, cs_ref)
+        assert_close(f64(dst), st_ref, "state round %d" % rnd)
+        assert_close(f64(dcs), cs_ref, "conv_state round %d" % rnd, rtol=0, atol_frac=0)
+
+
+# ------------------------------------------------------------------------------ full-size, sampled
+@pytest.mark.parametrize("wid", [2, 3, 4])
+def test_full_size_round_sampled_units(gdnlib, wid):
+    """One round of the full workload in the bench's launch configuration; every accept output is
+    compared, and 16 random (layer, sequence) units of verify and rollback."""
+    w = I.WORKLOADS[wid]
+    dev = "cuda"
+    cw = I.model_weights(w, 0, dev)
+    st, cs = I.initial_state(w, 0, dev)
+    qkv, g, beta = I.round_stream(w, 0, 0, dev)
+    parent = tok = None
+    if w.accept == "tree":
+        parent = I.random_tree(w, 0)
+        tok, lg, _ = I.tree_tokens_and_logits(w, parent, 0)
+        parent, tok, lg = to_dev(parent, tok, lg)
+        drafts = tok
+    elif w.accept == "sample":
+        lg, drafts = I.sample_logits(w, 0, 0, dev)
+    else:
+        lg, drafts, _ = I.greedy_logits(w, 0, 0, dev)
+    st0, cs0 = st.clone(), cs.clone()
+    r = SpecRound(w)
+    r.step(qkv, g, beta, lg, drafts, cw, st, cs, round_=0, seed=5, parent=parent)
+    r.check_status()
+    lgh = logits_f32(lg)
+    if w.accept == "tree":
+        path, n, out, _ = oracle.accept_tree(lgh, parent.cpu().numpy(), tok.cpu().numpy(), w.P)
+        assert np.array_equal(r.path.cpu().numpy(), path)
+    elif w.accept == "sample":
+        n, out, _ = oracle.accept_sample(lgh, drafts.cpu().numpy(), w.temperature, 5, 0)
+        path = None
+    else:
+        n, out, _ = oracle.accept_greedy(lgh, drafts.cpu().numpy())
+        path = None
+    assert np.array_equal(r.n_acc.cpu().numpy(), n)
+    assert np.array_equal(r.out_tokens.cpu().numpy(), out)
+    rng = np.random.default_rng(wid)
+    units = {(int(rng.integers(0, w.L)), int(rng.integers(0, w.B))) for _ in range(16)}
+    for (l, b) in sorted(units):
+        sl = lambda t: t[l:l + 1, b:b + 1].cpu()
+        par_b = None if parent is None else parent[b:b + 1].cpu()
+        ref = oracle_verify(w, sl(qkv), cw[l:l + 1].cpu(), sl(cs0), sl(g), sl(beta), sl(st0),
+                            parent=par_b, L=1, B=1)
+        assert_close(f64(r.out[l:l + 1, b:b + 1]), ref["out"], "out (l=%d,b=%d)" % (l, b))
+        assert_close(f64(r.tape_delta[l:l + 1, b:b + 1]), ref["tape_delta"], "delta")
+        st_ref, cs_ref, bad = oracle_rollback(w, n[b:b + 1], ref, sl(g), sl(qkv), sl(st0),
+                                              sl(cs0), path=None if path is None
+                                              else path[b:b + 1], L=1, B=1)
+        assert bad == 0
+        assert_close(f64(st[l:l + 1, b:b + 1]), st_ref, "state (l=%d,b=%d)" % (l, b))
+        assert np.array_equal(f64(cs[l:l + 1, b:b + 1]), cs_ref)
