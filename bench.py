@@ -281,7 +281,7 @@ def workload_description(w):
                          w.name, w.L, w.Hk, w.Hv, w.D, w.W, w.C, w.B, w.N, w.accept, w.V),
          "layers": w.L, "batch": w.B, "drafts": w.N, "vocab": w.V, "accept": w.accept,
          "io_dtype": "bf16" if str(w.io_dtype).endswith("bfloat16") else "f32",
-         "state": "fp32 128x128 per value head, key-major",
+         "state": "fp32 128x128 per value head, row-major S",
          "l2": "inputs larger than L2: the %.2f GB recurrent state is streamed from HBM every step"
                % (w.L * w.B * w.Hv * w.D * w.D * 4 / 1e9)}
     if w.accept in ("greedy", "tree"):
@@ -453,10 +453,16 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
+    ap.add_argument("--batch", type=int, default=None,
+                    help="override the workload's batch (smaller profiling cases)")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="override the workload's layer count (smaller profiling cases)")
     args = ap.parse_args(argv)
 
     from speculative_verify_gdn_gb300 import inputs as I
     w = I.WORKLOADS[args.config]
+    if args.batch is not None or args.layers is not None:
+        w = I.custom(w, name=w.name, B=args.batch or w.B, L=args.layers or w.L)
     ws, rank, local = dist_env()
 
     if args.impl == "reference":

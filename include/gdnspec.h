@@ -106,14 +106,15 @@ typedef struct gdn_dims {
  *   conv_w     [L][C][W]           io_dtype   depthwise conv taps
  *   conv_state [L][B][W-1][C]      io_dtype   last W-1 raw rows before the round (read only)
  *   g, beta    [L][B][T][Hv]       f32        decay gate in (0,1] and write strength
- *   state      [L][B][Hv][Dk][Dv]  f32        S_0, stored key-major: element (i,j) of S — row i
- *                                             in Dv, column j in Dk — is at [j][i] (read only)
+ *   state      [L][B][Hv][Dv][Dk]  f32        S_0, row-major: element (i,j) of S — row i in
+ *                                             Dv, column j in Dk — is at [i][j] (read only)
  *   out        [L][B][T][Hv][Dv]   io_dtype   o_t
  *   tape_delta [L][B][T][Hv][Dv]   f32        δ_t          (written)
  *   tape_k     [L][B][T][Hk][Dk]   f32        normalised k_t (written)
  * The tape's gate and raw-conv parts are the caller's g and qkv themselves: keep them alive and
- * unchanged until gdn_rollback. All pointers 16-byte aligned. The tape buffers hold
- * gdn_tape_bytes() bytes in total.
+ * unchanged until gdn_rollback. state, qkv, conv_w and conv_state must be 16-byte aligned (they
+ * are read by TMA / bulk copies); every other pointer aligned to its element size. The tape
+ * buffers hold gdn_tape_bytes() bytes in total.
  */
 GDN_API int gdn_verify(const gdn_dims* d, const void* qkv, const void* conv_w, const void* conv_state,
                const float* g, const float* beta, const float* state, void* out,

@@ -106,13 +106,13 @@ void oracle_verify(const oracle_dims* dm, const int32_t* parent, const double* q
             /* (3) gated delta recurrence per value head, node by node from the parent's state */
             for (int h = 0; h < Hv; ++h) {
                 const int hk = h / group;
-                const double* S0 = state + (lb * Hv + h) * (size_t)Dk * Dv; /* [j][i] */
+                const double* S0 = state + (lb * Hv + h) * (size_t)Dv * Dk; /* [i][j] */
                 for (int v = 0; v < T; ++v) {
                     int p = par ? par[v] : v - 1;
                     /* parent state S_p as a plain row-major Dv x Dk matrix */
                     for (int i = 0; i < Dv; ++i)
                         for (int j = 0; j < Dk; ++j)
-                            Sp[IDX2(i, j, Dk)] = (p < 0) ? S0[IDX2(j, i, Dv)]
+                            Sp[IDX2(i, j, Dk)] = (p < 0) ? S0[IDX2(i, j, Dk)]
                                                          : S_nodes[((size_t)p * Dv + i) * Dk + j];
                     const double* k = y + IDX2(v, koff + hk * Dk, C);
                     const double* q = y + IDX2(v, qoff + hk * Dk, C);
@@ -135,9 +135,9 @@ void oracle_verify(const oracle_dims* dm, const int32_t* parent, const double* q
                         out[(((lb * T + v) * Hv) + h) * (size_t)Dv + i] = dm->qk_scale * o;
                     }
                     if (node_state) {
-                        double* dst = node_state + ((lb * T + v) * Hv + h) * (size_t)Dk * Dv;
+                        double* dst = node_state + ((lb * T + v) * Hv + h) * (size_t)Dv * Dk;
                         for (int i = 0; i < Dv; ++i)
-                            for (int j = 0; j < Dk; ++j) dst[IDX2(j, i, Dv)] = Sv[IDX2(i, j, Dk)];
+                            for (int j = 0; j < Dk; ++j) dst[IDX2(i, j, Dk)] = Sv[IDX2(i, j, Dk)];
                     }
                 }
             }
@@ -176,7 +176,7 @@ int oracle_rollback(const oracle_dims* dm, const int32_t* path, int P, const int
             const size_t lb = (size_t)l * B + b;
             for (int h = 0; h < Hv; ++h) {
                 const int hk = h / group;
-                double* S = state + (lb * Hv + h) * (size_t)Dk * Dv; /* [j][i] */
+                double* S = state + (lb * Hv + h) * (size_t)Dv * Dk; /* [i][j] */
                 for (int s = 0; s < n; ++s) {
                     const int t = nodes[s];
                     const double gt = g[(lb * T + t) * Hv + h];
@@ -185,7 +185,7 @@ int oracle_rollback(const oracle_dims* dm, const int32_t* path, int P, const int
                     /* state = state * g[t] + k[t] * tape[t], elementwise S(i,j) */
                     for (int i = 0; i < Dv; ++i)
                         for (int j = 0; j < Dk; ++j)
-                            S[IDX2(j, i, Dv)] = gt * S[IDX2(j, i, Dv)] + dl[i] * kt[j];
+                            S[IDX2(i, j, Dk)] = gt * S[IDX2(i, j, Dk)] + dl[i] * kt[j];
                 }
             }
             /* conv state: last W-1 raw rows of (conv_state ++ accepted qkv rows) */

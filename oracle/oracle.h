@@ -20,8 +20,8 @@ typedef struct oracle_dims {
 } oracle_dims;
 
 /* qkv [L][B][T][C], conv_w [L][C][W], conv_state [L][B][W-1][C], g/beta [L][B][T][Hv],
- * state [L][B][Hv][Dk][Dv] (S(i,j) at [j][i]); out [L][B][T][Hv][Dv], tape_delta same,
- * tape_k [L][B][T][Hk][Dk]; node_state (optional) [L][B][T][Hv][Dk][Dv] = state after node.
+ * state [L][B][Hv][Dv][Dk] (row-major S: S(i,j) at [i][j]); out [L][B][T][Hv][Dv], tape_delta
+ * same, tape_k [L][B][T][Hk][Dk]; node_state (optional) [L][B][T][Hv][Dv][Dk] = state after node.
  * parent [B][T] or NULL for a chain. */
 void oracle_verify(const oracle_dims* dm, const int32_t* parent, const double* qkv,
                    const double* conv_w, const double* conv_state, const double* g,

@@ -97,7 +97,7 @@ def verify(dims: OracleDims, qkv, conv_w, conv_state, g, beta, state, parent=Non
     """Returns dict(out, tape_delta, tape_k[, node_state]) as float64 arrays.
 
     Shapes as the C ABI: qkv [L,B,T,C], conv_w [L,C,W], conv_state [L,B,W-1,C], g/beta
-    [L,B,T,Hv], state [L,B,Hv,Dk,Dv]; parent [B,T] int32 or None for the chain.
+    [L,B,T,Hv], state [L,B,Hv,Dv,Dk] (row-major S); parent [B,T] int32 or None for the chain.
     """
     lib = _load()
     d = dims
@@ -107,14 +107,14 @@ def verify(dims: OracleDims, qkv, conv_w, conv_state, g, beta, state, parent=Non
     assert conv_w.shape == (d.L, d.C, d.W)
     assert conv_state.shape == (d.L, d.B, d.W - 1, d.C)
     assert g.shape == (d.L, d.B, d.T, d.Hv) and beta.shape == g.shape
-    assert state.shape == (d.L, d.B, d.Hv, d.Dk, d.Dv)
+    assert state.shape == (d.L, d.B, d.Hv, d.Dv, d.Dk)
     par = None if parent is None else _i32(parent)
     if par is not None:
         assert par.shape == (d.B, d.T)
     out = np.zeros((d.L, d.B, d.T, d.Hv, d.Dv))
     tdl = np.zeros_like(out)
     tk = np.zeros((d.L, d.B, d.T, d.Hk, d.Dk))
-    ns = np.zeros((d.L, d.B, d.T, d.Hv, d.Dk, d.Dv)) if node_states else None
+    ns = np.zeros((d.L, d.B, d.T, d.Hv, d.Dv, d.Dk)) if node_states else None
     cd = d.c()
     lib.oracle_verify(ct.byref(cd), _p(par), _p(qkv), _p(conv_w), _p(conv_state), _p(g),
                       _p(beta), _p(state), _p(out), _p(tdl), _p(tk), _p(ns))

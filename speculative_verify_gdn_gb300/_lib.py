@@ -134,7 +134,7 @@ class GdnShape:
         return (self.L, self.B, self.T, self.Hv)
 
     def state_shape(self):
-        return (self.L, self.B, self.Hv, self.Dk, self.Dv)
+        return (self.L, self.B, self.Hv, self.Dv, self.Dk)
 
     def out_shape(self):
         return (self.L, self.B, self.T, self.Hv, self.Dv)

@@ -1,6 +1,7 @@
 // api.cu — the extern "C" boundary of libgdnspec: argument validation, shape dispatch and the
 // thread-local error message. Every entry point only enqueues work on the caller's stream; none
 // allocates, frees or synchronises. See include/gdnspec.h for the contract of each call.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -56,6 +57,42 @@ int check_dims(const gdn_dims* d) {
 
 bool empty(const gdn_dims* d) { return d->L == 0 || d->B == 0 || d->T == 0; }
 
+// cuTensorMapEncodeTiled, fetched once from the driver through the runtime (no libcuda link).
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+    static EncodeTiledFn fn = [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            p = nullptr;
+        return reinterpret_cast<EncodeTiledFn>(p);
+    }();
+    return fn;
+}
+
+// 2-D view of the state: rows (l, b, h, i) x columns j; boxes of 32 columns x Dv rows with the
+// 128-byte swizzle, which is the tensor cores' K-major operand layout.
+int state_tensor_map(const gdn_dims* d, const float* state, CUtensorMap* map) {
+    EncodeTiledFn enc = encode_tiled();
+    if (!enc) return fail(GDN_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable from the driver");
+    const cuuint64_t rows = cuuint64_t(d->L) * d->B * d->Hv * d->Dv;
+    cuuint64_t dims[2] = {cuuint64_t(d->Dk), rows};
+    cuuint64_t strides[1] = {cuuint64_t(d->Dk) * 4};
+    cuuint32_t box[2] = {32, cuuint32_t(d->Dv)};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<float*>(state), dims,
+                     strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(GDN_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", int(r));
+    return GDN_OK;
+}
+
 int verify_common(const gdn_dims* d, const int32_t* parent, const void* qkv, const void* conv_w,
                   const void* conv_state, const float* g, const float* beta, const float* state,
                   void* out, float* tape_delta, float* tape_k, uint32_t* status, void* stream,
@@ -66,11 +103,12 @@ int verify_common(const gdn_dims* d, const int32_t* parent, const void* qkv, con
     if (!qkv || !conv_w || !g || !beta || !state || !out || !tape_delta || !tape_k ||
         (d->W > 1 && !conv_state) || (tree && !parent))
         return fail(GDN_ERR_INVALID_ARG, "NULL tensor pointer");
-    if (!aligned(state, 16))
-        return fail(GDN_ERR_INVALID_ARG, "state must be 16-byte aligned (bulk copies)");
+    if (!aligned(state, 16) || !aligned(qkv, 16) || !aligned(conv_w, 16) ||
+        (conv_state && !aligned(conv_state, 16)))
+        return fail(GDN_ERR_INVALID_ARG,
+                    "state, qkv, conv_w and conv_state must be 16-byte aligned (TMA / bulk copies)");
     const size_t es = io_size(d->io_dtype);
-    if (!aligned(qkv, es) || !aligned(conv_w, es) || (conv_state && !aligned(conv_state, es)) ||
-        !aligned(out, es) || !aligned(g, 4) || !aligned(beta, 4) || !aligned(tape_delta, 4) ||
+    if (!aligned(out, es) || !aligned(g, 4) || !aligned(beta, 4) || !aligned(tape_delta, 4) ||
         !aligned(tape_k, 4))
         return fail(GDN_ERR_INVALID_ARG, "misaligned tensor pointer");
     gdn::VerifyArgs a{};
@@ -79,9 +117,13 @@ int verify_common(const gdn_dims* d, const int32_t* parent, const void* qkv, con
     a.qkv = qkv; a.conv_w = conv_w; a.conv_state = conv_state; a.g = g; a.beta = beta;
     a.state = state; a.out = out; a.tape_delta = tape_delta; a.tape_k = tape_k;
     a.parent = tree ? parent : nullptr; a.status = status;
+    CUtensorMap map;
+    rc = state_tensor_map(d, state, &map);
+    if (rc) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = d->io_dtype == GDN_DTYPE_BF16 ? gdn::launch_verify_bf16(a, d->Dk, tree, s)
-                                                  : gdn::launch_verify_f32(a, d->Dk, tree, s);
+    cudaError_t e = d->io_dtype == GDN_DTYPE_BF16
+                        ? gdn::launch_verify_bf16(a, map, d->Dk, tree, s)
+                        : gdn::launch_verify_f32(a, map, d->Dk, tree, s);
     if (e != cudaSuccess) return cuda_fail(e, tree ? "gdn_verify_tree launch" : "gdn_verify launch");
     return GDN_OK;
 }

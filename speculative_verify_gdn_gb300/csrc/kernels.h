@@ -1,6 +1,7 @@
 // kernels.h — host-side launch entry points of the gdnspec kernels (internal to the library).
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -22,9 +23,12 @@ struct VerifyArgs {
     uint32_t* status;
 };
 
-// verify: D = Dk = Dv; one translation unit per element type of qkv / conv / out.
-cudaError_t launch_verify_bf16(const VerifyArgs& a, int D, bool tree, cudaStream_t s);
-cudaError_t launch_verify_f32(const VerifyArgs& a, int D, bool tree, cudaStream_t s);
+// verify: D = Dk = Dv; `smap` is the 2-D TMA map of the state (rows [L*B*Hv*Dv] x cols [Dk],
+// 32 x Dv boxes, 128-byte swizzle). One translation unit per element type of qkv / conv / out.
+cudaError_t launch_verify_bf16(const VerifyArgs& a, const CUtensorMap& smap, int D, bool tree,
+                               cudaStream_t s);
+cudaError_t launch_verify_f32(const VerifyArgs& a, const CUtensorMap& smap, int D, bool tree,
+                              cudaStream_t s);
 
 struct RollbackArgs {
     int L, B, T, Hk, Hv, W, C, P;

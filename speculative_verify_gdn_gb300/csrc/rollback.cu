@@ -9,21 +9,48 @@
 // the replay of n steps is folded into one pass over the state:
 //     S_n = Γ_total · S_0 + Σ_{s<n} (Γ_{s+1..n-1} δ_s) k_sᵀ,   Γ_total = Π_{s<n} g_s,
 // which reads and writes each state element once (HBM-bound) with n+1 FMAs per element.
-// One 256-thread CTA per (layer, sequence, value head); n is read on the device, so a CTA whose
-// sequence accepted nothing exits at once and the whole call needs no host synchronisation.
+// The state is row-major S ([i][j], j contiguous): lanes own consecutive key columns j (16-byte
+// accesses, coalesced rows), warps own rows i. One 256-thread CTA per (layer, sequence, value
+// head); n is read on the device, so a CTA whose sequence accepted nothing exits at once and the
+// whole call needs no host synchronisation.
 #include "common.cuh"
 #include "kernels.h"
 
 namespace gdn {
 
+template <int RPL>
+__device__ __forceinline__ void ld_rows_cs(const float* p, float (&v)[RPL]) {
+    if constexpr (RPL == 4) {
+        const float4 x = __ldcs(reinterpret_cast<const float4*>(p));
+        v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+    } else if constexpr (RPL == 2) {
+        const float2 x = __ldcs(reinterpret_cast<const float2*>(p));
+        v[0] = x.x; v[1] = x.y;
+    } else {
+        v[0] = __ldcs(p);
+    }
+}
+
+template <int RPL>
+__device__ __forceinline__ void st_rows_cs(float* p, const float (&v)[RPL]) {
+    if constexpr (RPL == 4) {
+        __stcs(reinterpret_cast<float4*>(p), make_float4(v[0], v[1], v[2], v[3]));
+    } else if constexpr (RPL == 2) {
+        __stcs(reinterpret_cast<float2*>(p), make_float2(v[0], v[1]));
+    } else {
+        __stcs(p, v[0]);
+    }
+}
+
 template <typename IO, int D, int NMAX, bool PATH>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, (NMAX <= 8 ? 2 : 1))
 gdn_rollback_kernel(const RollbackArgs a) {
-    constexpr int RPL = D / 32;      // consecutive state rows i per lane
-    constexpr int NW = 8;            // warps; warp w owns key columns j = w, w + 8, ...
-    constexpr int JPW = D / NW;
-    __shared__ float Ks[NMAX][D];
+    constexpr int CPL = D / 32;      // consecutive key columns j per lane
+    constexpr int NW = 8;            // warps; warp w owns state rows i = w, w + 8, ...
+    constexpr int RPW = D / NW;
+    __shared__ float Ds[NMAX][D];    // scaled innovations δ'_s[i] = Γ_{s+1..n-1} δ_s[i]
     __shared__ float coef[NMAX];
+    __shared__ float gs[NMAX];
     __shared__ int nodes[NMAX];
     __shared__ float gtot;
     __shared__ int bad;
@@ -42,12 +69,21 @@ gdn_rollback_kernel(const RollbackArgs a) {
     }
     if (n == 0) return;              // the snapshot is still in place
 
+    // issue the whole state slice of this thread first: its latency hides the tape prologue
+    float* S = a.state + (lb * Hv + h) * size_t(D) * D;   // row-major S: [i][j]
+    const int j0 = lane * CPL;
+    float v[RPW][CPL];
+#pragma unroll
+    for (int u = 0; u < RPW; ++u) ld_rows_cs<CPL>(S + size_t(warp + NW * u) * D + j0, v[u]);
+
     if (tid == 0) bad = 0;
     __syncthreads();
     if (tid < n) {
         const int nd = PATH ? __ldg(a.path + size_t(b) * a.P + tid) : tid;
-        if (nd < 0 || nd >= T) atomicOr(&bad, 1);
-        nodes[tid] = nd;
+        const bool ok = nd >= 0 && nd < T;
+        if (!ok) atomicOr(&bad, 1);
+        nodes[tid] = ok ? nd : 0;
+        gs[tid] = ok ? __ldg(a.g + (lb * T + nd) * Hv + h) : 0.f;
     }
     __syncthreads();
     if (bad) {
@@ -58,72 +94,44 @@ gdn_rollback_kernel(const RollbackArgs a) {
         float c = 1.f;
         for (int s = n - 1; s >= 0; --s) {
             coef[s] = c;                                   // Γ_{s+1..n-1}
-            c *= __ldg(a.g + (lb * T + nodes[s]) * Hv + h);
+            c *= gs[s];
         }
         gtot = c;                                          // Γ_{0..n-1}
     }
-    for (int idx = tid; idx < n * D; idx += 256) {
-        const int s = idx / D, j = idx - s * D;
-        Ks[s][j] = __ldg(a.tape_k + ((lb * T + nodes[s]) * Hk + kh) * size_t(D) + j);
-    }
-    __syncthreads();
-
-    // scaled innovations of this lane's rows, δ'_s[i] = Γ_{s+1..n-1} δ_s[i]
-    const int i0 = lane * RPL;
-    float dl[NMAX][RPL];
+    float kr[NMAX][CPL];   // k_s[j0 .. j0+CPL) of this lane's columns
 #pragma unroll
     for (int s = 0; s < NMAX; ++s) {
 #pragma unroll
-        for (int r = 0; r < RPL; ++r) dl[s][r] = 0.f;
+        for (int r = 0; r < CPL; ++r) kr[s][r] = 0.f;
         if (s < n) {
-            const float* src = a.tape_delta + ((lb * T + nodes[s]) * Hv + h) * size_t(D) + i0;
+            const float* src = a.tape_k + ((lb * T + nodes[s]) * Hk + kh) * size_t(D) + j0;
 #pragma unroll
-            for (int r = 0; r < RPL; ++r) dl[s][r] = coef[s] * __ldg(src + r);
+            for (int r = 0; r < CPL; ++r) kr[s][r] = __ldg(src + r);
         }
     }
+    __syncthreads();
+    for (int idx = tid; idx < n * D; idx += 256) {
+        const int s = idx / D, i = idx - s * D;
+        Ds[s][i] = coef[s] * __ldg(a.tape_delta + ((lb * T + nodes[s]) * Hv + h) * size_t(D) + i);
+    }
+    __syncthreads();
     const float G = gtot;
 
-    float* S = a.state + (lb * Hv + h) * size_t(D) * D;   // [j][i]
-    constexpr int UN = JPW < 8 ? JPW : 8;
-#pragma unroll 1
-    for (int j0 = 0; j0 < JPW; j0 += UN) {
-        float v[UN][RPL];
+    // S_n[i][j] = Γ_total S_0[i][j] + Σ_s δ'_s[i] k_s[j]
 #pragma unroll
-        for (int u = 0; u < UN; ++u) {
-            const int j = warp + NW * (j0 + u);
-            const float* p = S + size_t(j) * D + i0;
-            if constexpr (RPL == 4) {
-                const float4 x = __ldcs(reinterpret_cast<const float4*>(p));
-                v[u][0] = x.x; v[u][1] = x.y; v[u][2] = x.z; v[u][3] = x.w;
-            } else if constexpr (RPL == 2) {
-                const float2 x = __ldcs(reinterpret_cast<const float2*>(p));
-                v[u][0] = x.x; v[u][1] = x.y;
-            } else {
-                v[u][0] = __ldcs(p);
+    for (int u = 0; u < RPW; ++u) {
+        const int i = warp + NW * u;
+#pragma unroll
+        for (int r = 0; r < CPL; ++r) v[u][r] *= G;
+#pragma unroll
+        for (int s = 0; s < NMAX; ++s) {
+            if (s < n) {
+                const float d = Ds[s][i];
+#pragma unroll
+                for (int r = 0; r < CPL; ++r) v[u][r] = fmaf(d, kr[s][r], v[u][r]);
             }
         }
-#pragma unroll
-        for (int u = 0; u < UN; ++u) {
-            const int j = warp + NW * (j0 + u);
-#pragma unroll
-            for (int r = 0; r < RPL; ++r) v[u][r] *= G;
-#pragma unroll
-            for (int s = 0; s < NMAX; ++s) {
-                if (s < n) {
-                    const float k = Ks[s][j];
-#pragma unroll
-                    for (int r = 0; r < RPL; ++r) v[u][r] = fmaf(dl[s][r], k, v[u][r]);
-                }
-            }
-            float* p = S + size_t(j) * D + i0;
-            if constexpr (RPL == 4) {
-                __stcs(reinterpret_cast<float4*>(p), make_float4(v[u][0], v[u][1], v[u][2], v[u][3]));
-            } else if constexpr (RPL == 2) {
-                __stcs(reinterpret_cast<float2*>(p), make_float2(v[u][0], v[u][1]));
-            } else {
-                __stcs(p, v[u][0]);
-            }
-        }
+        st_rows_cs<CPL>(S + size_t(i) * D + j0, v[u]);
     }
 
     // conv state: last W-1 rows of (conv_state ++ accepted raw rows); channels split over heads

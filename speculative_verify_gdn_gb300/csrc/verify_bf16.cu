@@ -2,8 +2,9 @@
 #include "verify_impl.cuh"
 
 namespace gdn {
-cudaError_t launch_verify_bf16(const VerifyArgs& a, int D, bool tree, cudaStream_t s) {
-    return tree ? launch_verify_io<__nv_bfloat16, true>(a, D, s)
-                : launch_verify_io<__nv_bfloat16, false>(a, D, s);
+cudaError_t launch_verify_bf16(const VerifyArgs& a, const CUtensorMap& smap, int D, bool tree,
+                               cudaStream_t s) {
+    return tree ? launch_verify_io<__nv_bfloat16, true>(a, smap, D, s)
+                : launch_verify_io<__nv_bfloat16, false>(a, smap, D, s);
 }
 }  // namespace gdn

@@ -2,7 +2,9 @@
 #include "verify_impl.cuh"
 
 namespace gdn {
-cudaError_t launch_verify_f32(const VerifyArgs& a, int D, bool tree, cudaStream_t s) {
-    return tree ? launch_verify_io<float, true>(a, D, s) : launch_verify_io<float, false>(a, D, s);
+cudaError_t launch_verify_f32(const VerifyArgs& a, const CUtensorMap& smap, int D, bool tree,
+                              cudaStream_t s) {
+    return tree ? launch_verify_io<float, true>(a, smap, D, s)
+                : launch_verify_io<float, false>(a, smap, D, s);
 }
 }  // namespace gdn

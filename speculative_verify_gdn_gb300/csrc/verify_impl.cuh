@@ -1,4 +1,4 @@
-// verify_impl.cuh — gdn_verify / gdn_verify_tree kernel (sm_103a).
+// verify_impl.cuh — gdn_verify / gdn_verify_tree kernel (sm_103a, tcgen05 tensor cores).
 //
 // What it computes (per layer l, sequence b, value head h; "GDN investigation" = "Speculative
 // Decoding on GDN Hybrid Architectures: A 31-Experiment Investigation", §2.1, §2.2, §4):
@@ -8,106 +8,206 @@
 //   Writes o, the tape (δ per value head, normalised k per key head). S_0 is never written.
 //
 // How (GB300 design):
-//   * One 128-thread CTA per (l, b, h). S_0 is stored key-major (S(i,j) at [j][i]), so the head's
-//     64 KiB tile is contiguous; four 1-D bulk copies (TMA, one per warp's quarter of Dk) stream
-//     it into shared memory while the CTA does the conv, the norms and the small Gram matrices.
 //   * The state update is never materialised. With Γ(a→p) the product of the gates strictly
 //     after node a up to node p on the path, the parent state of node v satisfies
 //         S_p k_v = Γ(root→p) S_0 k_v + Σ_{a ∈ path(p)} Γ(a→p) δ_a (k_a·k_v)
-//     (and the same with q_v), so the only O(D²) work is the product S_0·[K|Q] — 2T dot products
-//     per state element, done on CUDA cores in fp32 with each S_0 element read from shared
-//     memory once — followed by an O(T²) recurrence per state row for δ and o.
-//   * The product splits Dk over the 4 warps (each lane owns D/32 consecutive rows i, so the
-//     shared-memory reads of S_0 are conflict-free and the [K|Q] reads are broadcasts); partial
-//     sums are reduced through shared memory in a fixed order (deterministic).
+//     (and the same with q_v). So the O(D²) work is one dense product per head,
+//         P = S_0 · [K | Q]      (M = Dv rows, K = Dk, N = 2T columns),
+//     plus the small Gram block k_a·[K|Q] and an O(T²) recurrence per state row for δ and o.
+//   * P runs on the 5th-generation tensor cores (tcgen05.mma kind::tf32, fp32 accumulators in
+//     TMEM) in three TF32 products for fp32 accuracy: with x = hi + lo, hi = x truncated to TF32
+//     (exactly what the tensor core reads from an fp32 word) and lo = x − hi exact in fp32,
+//         P ≈ S_hi·X_hi + S_hi·X_lo + S_lo·X_hi.
+//     The first two share one pass over the state tile (B = [X_hi ; X_lo], N = 4T); the tile is
+//     then overwritten in place by S_lo for the second pass. The tensor core reads its operands
+//     from shared memory, so the number of passes over the 64 KiB tile is what it costs.
+//   * One 256-thread CTA per (l, b, h). At entry one thread starts the 2-D TMA of the head's S_0
+//     tile (row-major, 128-byte-swizzled K-major boxes: directly the UMMA operand layout) and a
+//     warp starts 1-D bulk copies of the head's qkv / conv-state / conv-weight / gate rows into
+//     shared memory; conv, norms, [K|Q] and the Gram block (CUDA cores) overlap the state load.
 #pragma once
+
+#include <cuda.h>
 
 #include "common.cuh"
 #include "kernels.h"
 
 namespace gdn {
 
-template <int D, int TMAX, bool TREE>
+template <typename IO, int D, int TMAX, bool TREE>
 struct VerifyCfg {
-    static constexpr int NWARP = 4;
-    static constexpr int NTHR = 128;
-    static constexpr int RPL = D / 32;            // state rows per lane
-    static constexpr int JPW = D / NWARP;         // Dk rows of S_0ᵀ per warp
-    static constexpr int XC = 2 * TMAX;           // columns k_0..k_{TMAX-1}, q_0..q_{TMAX-1}
-    static constexpr int XS = XC;                 // row stride of X (floats)
-    static constexpr int NPASS = (XC + 31) / 32;  // at most 32 accumulator columns per pass
-    static constexpr int PC = XC / NPASS;
-    static constexpr bool PART_IN_CHUNK = (NPASS == 1) && (JPW >= PC) && !TREE;
-    static constexpr bool USE_R = !PART_IN_CHUNK;
+    static constexpr int NWARP = 8;
+    static constexpr int NTHR = 256;
+    static constexpr int ES = int(sizeof(IO));
+    static constexpr int KB = D / 32;                        // K-blocks of 32 tf32 (128 bytes)
+    static constexpr int NP = 2 * TMAX < 16 ? 16 : 2 * TMAX; // columns k_*, q_*, zero padding
+    static constexpr int XROWS = 2 * NP;                     // B tile rows: X_hi then X_lo
+    static constexpr int XKB = XROWS * 128;                  // bytes per K-block of the B tile
+    static constexpr int X_BYTES = KB * XKB;
+    static constexpr int A_KB = 128 * 128;                   // bytes per K-block of A (M = 128)
+    static constexpr int A_BYTES = KB * A_KB;
+    static constexpr int TMEM_COLS = XROWS <= 32 ? 32 : (XROWS <= 64 ? 64 : 128);
+    // staging of the head's raw inputs: [3 parts q,k,v][W-1+T rows][D] and conv taps [3][D][W];
+    // reused for the plain [K|Q] copy once the conv has read it
+    static constexpr int XP_STRIDE = D + 4;                  // floats per plain row (padded)
+    static constexpr int XP_BYTES = 2 * TMAX * XP_STRIDE * 4;
 
-    static constexpr size_t S_BYTES = size_t(D) * D * 4;
-    static constexpr size_t X_BYTES = size_t(D) * XS * 4;
-    static constexpr size_t R_BYTES = USE_R ? size_t(XC) * D * 4 : 0;
-    static constexpr size_t DL_BYTES = TREE ? size_t(TMAX) * D * 4 : 0;
-    // meta block
+    // meta block (floats)
     static constexpr int M_GAM = 0, M_BET = M_GAM + TMAX, M_C0 = M_BET + TMAX,
-                         M_KQ = M_C0 + TMAX, M_INV = M_KQ + TMAX, M_NRM = M_INV + XC,
-                         M_CK = M_NRM + NWARP * XC, M_CQ = M_CK + TMAX * TMAX,
-                         M_FLOATS = M_CQ + TMAX * TMAX;
+                         M_KQ = M_C0 + TMAX, M_INV = M_KQ + TMAX, M_NRM = M_INV + 2 * TMAX,
+                         M_CK = M_NRM + NWARP * TMAX, M_CQ = M_CK + TMAX * TMAX,
+                         M_DL = M_CQ + TMAX * TMAX, M_FLOATS = M_DL + (TREE ? TMAX * D : 0);
     static constexpr int I_PAR = 0, I_NANC = I_PAR + TMAX, I_ANC = I_NANC + TMAX,
                          I_WIN = I_ANC + (TREE ? TMAX * TMAX : 0),
                          I_FLAG = I_WIN + (TREE ? TMAX * 4 : 0), I_INTS = I_FLAG + 4;
 
-    static constexpr size_t OFF_S = 0;
-    static constexpr size_t OFF_X = OFF_S + S_BYTES;
-    static constexpr size_t OFF_R = OFF_X + X_BYTES;
-    static constexpr size_t OFF_DL = OFF_R + R_BYTES;
-    static constexpr size_t OFF_MF = OFF_DL + DL_BYTES;
+    static constexpr size_t OFF_X = 0;
+    static constexpr size_t OFF_A = OFF_X + X_BYTES;
+    static constexpr size_t OFF_MF = OFF_A + A_BYTES;
     static constexpr size_t OFF_MI = OFF_MF + size_t(M_FLOATS) * 4;
     static constexpr size_t OFF_BAR = (OFF_MI + size_t(I_INTS) * 4 + 15) / 16 * 16;
-    static constexpr size_t SMEM = OFF_BAR + NWARP * 8;
+    static constexpr size_t OFF_TSLOT = OFF_BAR + 3 * 8;
+    static constexpr size_t OFF_STAGE = (OFF_TSLOT + 16 + 127) / 128 * 128;
+
+    static __host__ __device__ constexpr size_t stage_bytes(int T_, int W_) {
+        const size_t raw = size_t(3) * (W_ - 1 + T_) * D * ES + size_t(3) * D * W_ * ES;
+        return raw > size_t(XP_BYTES) ? raw : size_t(XP_BYTES);
+    }
+    static __host__ __device__ constexpr size_t smem_bytes(int T_, int W_) {
+        return OFF_STAGE + stage_bytes(T_, W_) + 1024;   // + alignment slack for the base
+    }
 
     static_assert(D == 32 || D == 64 || D == 128, "head dim");
-    static_assert(XC % PC == 0 && PC % 4 == 0, "columns");
-    static_assert((size_t(JPW) * D * 4) % 16 == 0, "bulk copy size");
+    static_assert(OFF_A % 1024 == 0, "swizzle atoms need 1024-byte bases");
 };
 
-template <int RPL>
-__device__ __forceinline__ void load_rows(const float* p, float (&s)[RPL]) {
-    if constexpr (RPL == 4) {
-        float4 v = *reinterpret_cast<const float4*>(p);
-        s[0] = v.x; s[1] = v.y; s[2] = v.z; s[3] = v.w;
-    } else if constexpr (RPL == 2) {
-        float2 v = *reinterpret_cast<const float2*>(p);
-        s[0] = v.x; s[1] = v.y;
-    } else {
-        s[0] = *p;
-    }
+// ---------------------------------------------------------------- tcgen05 helpers
+// Shared-memory matrix descriptor: K-major, 128-byte swizzle, 8-row groups 1024 bytes apart.
+__device__ __forceinline__ uint64_t umma_desc_sw128(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= uint64_t((saddr >> 4) & 0x3FFFu);          // start address
+    d |= uint64_t(1) << 16;                         // leading byte offset (unused for this layout)
+    d |= uint64_t(1024 >> 4) << 32;                 // stride byte offset: next 8-row group
+    d |= uint64_t(1) << 46;                         // descriptor version
+    d |= uint64_t(2) << 61;                         // 128-byte swizzle
+    return d;
 }
 
-template <int RPL>
-__device__ __forceinline__ void store_rows(float* p, const float (&s)[RPL]) {
-    if constexpr (RPL == 4) {
-        *reinterpret_cast<float4*>(p) = make_float4(s[0], s[1], s[2], s[3]);
-    } else if constexpr (RPL == 2) {
-        *reinterpret_cast<float2*>(p) = make_float2(s[0], s[1]);
-    } else {
-        *p = s[0];
-    }
+// Instruction descriptor: kind::tf32, fp32 accumulate, both operands K-major, M x N.
+__host__ __device__ constexpr uint32_t umma_idesc_tf32(int M, int N) {
+    return (1u << 4) | (2u << 7) | (2u << 10) | (uint32_t(N >> 3) << 17) | (uint32_t(M >> 4) << 24);
 }
 
-__device__ __forceinline__ float silu_f(float y) { return y / (1.0f + expf(-y)); }
+__device__ __forceinline__ void umma_tf32(uint32_t dtmem, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n\t}"
+        ::"r"(dtmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void fence_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// 32 lanes x 16 consecutive fp32 columns of TMEM (this warp's lane quarter) into v[0..15].
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+    for (int k = 0; k < 16; ++k) v[k] = __uint_as_float(r[k]);
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
+                                            uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(smem_u32(dst)), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y),
+          "r"(smem_u32(bar))
+        : "memory");
+}
+
+// byte offset of element (row, j) in a K-major 128B-swizzled tile with the given K-block size
+__device__ __forceinline__ uint32_t sw128_off(int row, int j, int kblock_bytes) {
+    const int kb = j >> 5, grp = row >> 3, r = row & 7, chunk = (j & 31) >> 2;
+    return uint32_t(kb * kblock_bytes + grp * 1024 + r * 128 + ((chunk ^ r) << 4) + (j & 3) * 4);
+}
+
+__device__ __forceinline__ float tf32_trunc(float x) {
+    return __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
+}
+
+// y · sigmoid(y) with the fast exponential and division (relative error ~1e-6)
+__device__ __forceinline__ float silu_fast(float y) {
+    return __fdividef(y, 1.0f + __expf(-y));
+}
+
+// Sum each of V per-lane values over the warp by recursive halving: V-1 + log2(32/V) shuffles.
+// Returns the total of value index *idx (valid in every lane; lanes sharing idx agree).
+template <int V>
+__device__ __forceinline__ float warp_sum_many(float (&v)[V], int lane, int* idx) {
+    int base = 0;
+#pragma unroll
+    for (int m = V, o = 16; m > 1; m >>= 1, o >>= 1) {
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int k = 0; k < m / 2; ++k) {
+            const float send = up ? v[k] : v[k + m / 2];
+            const float keep = up ? v[k + m / 2] : v[k];
+            v[k] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        }
+        base += up ? m / 2 : 0;
+    }
+    float s = v[0];
+#pragma unroll
+    for (int o = 16 / V; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    *idx = base;
+    return s;
+}
+
+template <typename IO>
+__device__ __forceinline__ float io_to_f(IO x) {
+    if constexpr (sizeof(IO) == 2) return __bfloat162float(x);
+    else return x;
+}
 
 template <typename IO, int D, int TMAX, bool TREE>
-__global__ void __launch_bounds__(128)
-gdn_verify_kernel(const VerifyArgs a) {
-    using Cfg = VerifyCfg<D, TMAX, TREE>;
+__global__ void __launch_bounds__(256)
+gdn_verify_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap smap) {
+    using Cfg = VerifyCfg<IO, D, TMAX, TREE>;
     using Tr = IoTraits<IO>;
-    constexpr int RPL = Cfg::RPL, JPW = Cfg::JPW, XS = Cfg::XS, PC = Cfg::PC, XC = Cfg::XC;
+    constexpr int NP = Cfg::NP, KB = Cfg::KB, XKB = Cfg::XKB, XS = Cfg::XP_STRIDE;
 
-    extern __shared__ __align__(128) unsigned char smem[];
-    float* Ss = reinterpret_cast<float*>(smem + Cfg::OFF_S);
-    float* X = reinterpret_cast<float*>(smem + Cfg::OFF_X);
-    float* R = reinterpret_cast<float*>(smem + Cfg::OFF_R);
-    float* DL = reinterpret_cast<float*>(smem + Cfg::OFF_DL);
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* smem = reinterpret_cast<unsigned char*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    unsigned char* Xb = smem + Cfg::OFF_X;          // B tile: [K-block][X_hi rows; X_lo rows]
+    unsigned char* As = smem + Cfg::OFF_A;          // S_0 tile (then S_lo)
     float* mf = reinterpret_cast<float*>(smem + Cfg::OFF_MF);
     int* mi = reinterpret_cast<int*>(smem + Cfg::OFF_MI);
-    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + Cfg::OFF_BAR);
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + Cfg::OFF_BAR);   // TMA, inputs, MMA
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + Cfg::OFF_TSLOT);
+    unsigned char* stage = smem + Cfg::OFF_STAGE;
     float* gam = mf + Cfg::M_GAM;
     float* bet = mf + Cfg::M_BET;
     float* c0 = mf + Cfg::M_C0;
@@ -116,6 +216,7 @@ gdn_verify_kernel(const VerifyArgs a) {
     float* nrm = mf + Cfg::M_NRM;
     float* CK = mf + Cfg::M_CK;
     float* CQ = mf + Cfg::M_CQ;
+    float* DL = mf + Cfg::M_DL;
     int* par = mi + Cfg::I_PAR;
     int* nanc = mi + Cfg::I_NANC;
     int* anc = mi + Cfg::I_ANC;
@@ -127,40 +228,83 @@ gdn_verify_kernel(const VerifyArgs a) {
     const int T = a.T, Hk = a.Hk, Hv = a.Hv, C = a.C, W = a.W;
     const int group = Hv / Hk, kh = h / group;
     const size_t lb = size_t(l) * a.B + b;
+    const int NR = W - 1 + T;                       // staged rows per part
 
-    // ---- 0. start streaming S_0 (key-major, contiguous 4*D*D bytes) into shared memory
-    if (tid == 0) {
-        for (int w = 0; w < Cfg::NWARP; ++w) mbar_init(&bar[w], 1);
-        fence_mbar_init();
-        const float* src = a.state + (lb * Hv + h) * size_t(D) * D;
-        constexpr uint32_t chunk = uint32_t(JPW) * D * 4;
-        for (int w = 0; w < Cfg::NWARP; ++w) {
-            mbar_arrive_expect_tx(&bar[w], chunk);
-            bulk_g2s(Ss + size_t(w) * JPW * D, src + size_t(w) * JPW * D, chunk, &bar[w]);
+    // staging layout (bytes from `stage`)
+    IO* qs = reinterpret_cast<IO*>(stage);                                   // [3][NR][D]
+    IO* cws = qs + size_t(3) * NR * D;                                       // [3][D][W]
+    float* XP = reinterpret_cast<float*>(stage);    // later: plain [K|Q] rows, stride XS
+
+    // ---- 0. state tile by 2-D TMA; raw input rows by 1-D bulk copies; TMEM
+    if (warp == 0) {
+        if (lane == 0) {
+            mbar_init(&bar[0], 1);
+            mbar_init(&bar[1], 1);
+            mbar_init(&bar[2], 1);
+            fence_mbar_init();
+            mbar_arrive_expect_tx(&bar[0], uint32_t(D) * D * 4);
+            const int row0 = int((lb * Hv + h) * D);
+            for (int kb = 0; kb < KB; ++kb)
+                tma_load_2d(As + kb * Cfg::A_KB, &smap, kb * 32, row0, &bar[0]);
+            const uint32_t in_bytes = uint32_t(3 * NR * D * Cfg::ES + 3 * D * W * Cfg::ES);
+            mbar_arrive_expect_tx(&bar[1], in_bytes);
+            flag[0] = 0;
         }
-        flag[0] = 0;
+        __syncwarp();
+        const IO* qkv = static_cast<const IO*>(a.qkv);
+        const IO* cst = static_cast<const IO*>(a.conv_state);
+        const IO* cw = static_cast<const IO*>(a.conv_w);
+        const int ncopy = 3 * NR + 3;
+        for (int i = lane; i < ncopy; i += 32) {
+            const void* src;
+            void* dst;
+            uint32_t bytes;
+            if (i < 3 * NR) {
+                const int p = i / NR, r = i - p * NR;
+                const int cb = p == 0 ? kh * D : (p == 1 ? Hk * D + kh * D : 2 * Hk * D + h * D);
+                src = r < W - 1 ? static_cast<const void*>(cst + (lb * (W - 1) + r) * size_t(C) + cb)
+                                : static_cast<const void*>(qkv + (lb * T + (r - (W - 1))) * size_t(C) + cb);
+                dst = qs + size_t(i) * D;
+                bytes = uint32_t(D * Cfg::ES);
+            } else {
+                const int p = i - 3 * NR;
+                const int cb = p == 0 ? kh * D : (p == 1 ? Hk * D + kh * D : 2 * Hk * D + h * D);
+                src = cw + (size_t(l) * C + cb) * W;
+                dst = cws + size_t(p) * D * W;
+                bytes = uint32_t(D * W * Cfg::ES);
+            }
+            bulk_g2s(dst, src, bytes, &bar[1]);
+        }
     }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(smem_u32(tslot)), "r"(uint32_t(Cfg::TMEM_COLS)));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    if constexpr (TREE) {
+        if (tid < T) par[tid] = __ldg(a.parent + size_t(b) * T + tid);
+    }
+    // this thread's gate pair (tid < T): loaded now, stored once the conv is under way
+    float g_in = 0.f, b_in = 0.f;
     if (tid < T) {
-        gam[tid] = __ldg(a.g + (lb * T + tid) * Hv + h);
-        bet[tid] = __ldg(a.beta + (lb * T + tid) * Hv + h);
-        if constexpr (TREE) par[tid] = __ldg(a.parent + size_t(b) * T + tid);
+        g_in = __ldg(a.g + (lb * T + tid) * Hv + h);
+        b_in = __ldg(a.beta + (lb * T + tid) * Hv + h);
     }
+    tc_fence_before();
     __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = *tslot;
 
-    // ---- 1. tree topology: validate parents, conv windows, ancestor lists
+    // ---- 1. tree topology: validate parents, conv windows
+    bool skip = false;
     if constexpr (TREE) {
         if (tid < T) {
             const int p = par[tid];
             if (p < -1 || p >= tid) atomicOr(flag, 1);
         }
         __syncthreads();
-        if (flag[0]) {
-            if (tid == 0) set_status(a.status, GDN_STATUS_BAD_PARENT);
-            if (!mbar_wait_bounded(&bar[warp], 0) && lane == 0)
-                set_status(a.status, GDN_STATUS_WAIT_TIMEOUT);
-            return;
-        }
-        if (tid < T) {
+        skip = flag[0] != 0;
+        if (!skip && tid < T) {
             int x = tid, e = 0;
             for (int d = 0; d < 4; ++d) {
                 int src = -1;
@@ -171,40 +315,61 @@ gdn_verify_kernel(const VerifyArgs a) {
                 win[tid * 4 + d] = src;
             }
         }
+    }
+    if (!mbar_wait_bounded(&bar[1], 0) && tid == 0) set_status(a.status, GDN_STATUS_WAIT_TIMEOUT);
+    if (tid < T) {
+        gam[tid] = g_in;
+        bet[tid] = b_in;
+    }
+    __syncthreads();
+    if (skip) {   // bad tree: report, let the TMA land, free TMEM, leave
+        if (tid == 0) {
+            set_status(a.status, GDN_STATUS_BAD_PARENT);
+            if (!mbar_wait_bounded(&bar[0], 0)) set_status(a.status, GDN_STATUS_WAIT_TIMEOUT);
+        }
+        tc_fence_before();
         __syncthreads();
+        tc_fence_after();
+        if (warp == 1)
+            asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;"
+                         ::"r"(tbase), "r"(uint32_t(Cfg::TMEM_COLS)));
+        return;
     }
 
-    // ---- 2. causal depthwise conv + SiLU for this head's q, k (key head kh) and v (head h)
-    const IO* qkv = static_cast<const IO*>(a.qkv) + lb * size_t(T) * C;
-    const IO* cst = static_cast<const IO*>(a.conv_state) + lb * size_t(W - 1) * C;
-    const IO* cw = static_cast<const IO*>(a.conv_w) + size_t(l) * C * W;
-    float yq[TMAX], yk[TMAX], yv[TMAX];
-    if (tid < D) {
-        const int chq = kh * D + tid, chk = Hk * D + kh * D + tid, chv = 2 * Hk * D + h * D + tid;
-        const int chs[3] = {chq, chk, chv};
+    // ---- 2. causal depthwise conv + SiLU from the staged rows. Threads [0, D): q and v channels
+    //         of row idx; threads [D, 2D): k channels. (Value row i = thread i keeps its v.)
+    const int part = tid / D, idx = tid - part * D;
+    float yqk[TMAX], yv[TMAX];
 #pragma unroll
-        for (int part = 0; part < 3; ++part) {
-            const int c = chs[part];
+    for (int t = 0; t < TMAX; ++t) { yqk[t] = 0.f; yv[t] = 0.f; }
+    if (part < 2) {
+#pragma unroll
+        for (int pc = 0; pc < 2; ++pc) {
+            if (pc == 1 && part == 1) break;
+            const int p = part == 1 ? 1 : (pc == 0 ? 0 : 2);
+            const IO* col = qs + size_t(p) * NR * D + idx;     // column of channel idx, part p
+            const IO* wp = cws + (size_t(p) * D + idx) * W;
             float wr[4];  // wr[d] multiplies the row at distance d (0 = current token)
 #pragma unroll
-            for (int d = 0; d < 4; ++d) wr[d] = (d < W) ? Tr::load(cw, size_t(c) * W + (W - 1 - d)) : 0.f;
+            for (int d = 0; d < 4; ++d) wr[d] = (d < W) ? io_to_f(wp[W - 1 - d]) : 0.f;
             float y[TMAX];
             if constexpr (!TREE) {
                 float E[3 + TMAX];
 #pragma unroll
                 for (int k = 0; k < 3; ++k) {
                     const int r = k + W - 4;
-                    E[k] = (r >= 0) ? Tr::load(cst, size_t(r) * C + c) : 0.f;
+                    E[k] = (r >= 0) ? io_to_f(col[size_t(r) * D]) : 0.f;
                 }
 #pragma unroll
-                for (int t = 0; t < TMAX; ++t) E[3 + t] = (t < T) ? Tr::load(qkv, size_t(t) * C + c) : 0.f;
+                for (int t = 0; t < TMAX; ++t)
+                    E[3 + t] = (t < T) ? io_to_f(col[size_t(W - 1 + t) * D]) : 0.f;
 #pragma unroll
                 for (int t = 0; t < TMAX; ++t) {
                     float acc = wr[3] * E[t];
                     acc = fmaf(wr[2], E[t + 1], acc);
                     acc = fmaf(wr[1], E[t + 2], acc);
                     acc = fmaf(wr[0], E[t + 3], acc);
-                    y[t] = (t < T) ? silu_f(acc) : 0.f;
+                    y[t] = (t < T) ? silu_fast(acc) : 0.f;
                 }
             } else {
 #pragma unroll
@@ -213,89 +378,116 @@ gdn_verify_kernel(const VerifyArgs a) {
                     if (t < T) {
 #pragma unroll
                         for (int d = 3; d >= 0; --d) {
-                            const int src = win[t * 4 + d];
-                            if (src >= 0) {
-                                const float x = (src < W - 1) ? Tr::load(cst, size_t(src) * C + c)
-                                                              : Tr::load(qkv, size_t(src - (W - 1)) * C + c);
-                                acc = fmaf(wr[d], x, acc);
-                            }
+                            const int src = win[t * 4 + d];     // staged row index
+                            if (src >= 0) acc = fmaf(wr[d], io_to_f(col[size_t(src) * D]), acc);
                         }
-                        acc = silu_f(acc);
+                        acc = silu_fast(acc);
                     }
                     y[t] = acc;
                 }
             }
 #pragma unroll
             for (int t = 0; t < TMAX; ++t) {
-                if (part == 0) yq[t] = y[t];
-                else if (part == 1) yk[t] = y[t];
+                if (pc == 0) yqk[t] = y[t];
                 else yv[t] = y[t];
             }
         }
-    } else {
-#pragma unroll
-        for (int t = 0; t < TMAX; ++t) { yq[t] = 0.f; yk[t] = 0.f; yv[t] = 0.f; }
     }
 
-    // ---- 3. L2 norms of q_t and k_t (per head, over D channels)
+    // ---- 3. L2 norms of q_t (warps of part 0) and k_t (part 1), per head over D channels
+    {
+        float sq[TMAX];
 #pragma unroll
-    for (int t = 0; t < TMAX; ++t) {
-        const float sk = warp_sum(yk[t] * yk[t]);
-        const float sq = warp_sum(yq[t] * yq[t]);
-        if (lane == 0) { nrm[warp * XC + t] = sk; nrm[warp * XC + TMAX + t] = sq; }
+        for (int t = 0; t < TMAX; ++t) sq[t] = yqk[t] * yqk[t];
+        int ix;
+        const float s = warp_sum_many<TMAX>(sq, lane, &ix);
+        if ((lane & (32 / TMAX - 1)) == 0) nrm[warp * TMAX + ix] = s;
     }
-    __syncthreads();
-    if (tid < XC) {
+    __syncthreads();   // also: every read of the staged rows is done, XP may overwrite them
+    if (tid < 2 * TMAX) {
+        // column c < TMAX: k_c (part-1 warps), c >= TMAX: q (part-0 warps)
+        const int t = tid < TMAX ? tid : tid - TMAX;
+        const int want = tid < TMAX ? 1 : 0;
         float s = 0.f;
 #pragma unroll
-        for (int w = 0; w < Cfg::NWARP; ++w) s += nrm[w * XC + tid];
+        for (int w = 0; w < Cfg::NWARP; ++w)
+            if ((w * 32) / D == want) s += nrm[w * TMAX + t];
         inv[tid] = 1.0f / sqrtf(s + a.l2_eps);
     }
     __syncthreads();
-    if (tid < D) {
-        float* xr = X + size_t(tid) * XS;
-        const bool write_k = (h % group) == 0;
+    // [K|Q] columns: n < TMAX -> k_n, TMAX <= n < 2 TMAX -> q, the rest zero. B tile rows n
+    // (hi) and NP + n (lo) in the swizzled K-major layout; plain fp32 rows XP[n] for the Gram.
+    if (part < 2) {
+        const int n0 = part == 1 ? 0 : TMAX;
 #pragma unroll
         for (int t = 0; t < TMAX; ++t) {
-            const float kn = yk[t] * inv[t];
-            xr[t] = kn;
-            xr[TMAX + t] = yq[t] * inv[TMAX + t];
-            if (write_k && t < T) a.tape_k[((lb * T + t) * Hk + kh) * size_t(D) + tid] = kn;
+            const float x = yqk[t] * inv[n0 + t];
+            const float hi = tf32_trunc(x);
+            *reinterpret_cast<float*>(Xb + sw128_off(n0 + t, idx, XKB)) = hi;
+            *reinterpret_cast<float*>(Xb + sw128_off(NP + n0 + t, idx, XKB)) = x - hi;
+            XP[(n0 + t) * XS + idx] = x;
+            if (part == 1 && (h % group) == 0 && t < T)
+                a.tape_k[((lb * T + t) * Hk + kh) * size_t(D) + idx] = x;
         }
-        if constexpr (TREE) {
+        if (part == 0) {
 #pragma unroll
-            for (int t = 0; t < TMAX; ++t)
-                if (t < T) DL[size_t(t) * D + tid] = yv[t];
+            for (int n = 2 * TMAX; n < NP; ++n) {
+                *reinterpret_cast<float*>(Xb + sw128_off(n, idx, XKB)) = 0.f;
+                *reinterpret_cast<float*>(Xb + sw128_off(NP + n, idx, XKB)) = 0.f;
+            }
+            if constexpr (TREE) {
+#pragma unroll
+                for (int t = 0; t < TMAX; ++t)
+                    if (t < T) DL[size_t(t) * D + idx] = yv[t];
+            }
         }
     }
+    fence_async_smem();
+    tc_fence_before();
     __syncthreads();
+    tc_fence_after();
 
-    // ---- 4. Gram entries k_a·k_v (a strict ancestor of v) and k_a·q_v (a ancestor or v)
+    // ---- 4. tensor cores, first pass over S_0: P[:, 0:NP] = S_hi·X_hi, P[:, NP:2NP] = S_hi·X_lo
+    const uint32_t sX = smem_u32(Xb), sA = smem_u32(As);
+    if (tid == 0) {
+        if (!mbar_wait_bounded(&bar[0], 0)) set_status(a.status, GDN_STATUS_WAIT_TIMEOUT);
+        tc_fence_after();
+        constexpr uint32_t IDESC1 = umma_idesc_tf32(128, 2 * NP);
+        const uint64_t da = umma_desc_sw128(sA), db = umma_desc_sw128(sX);
+#pragma unroll
+        for (int kb = 0; kb < KB; ++kb)
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks)
+                umma_tf32(tbase, da + uint64_t((kb * Cfg::A_KB + ks * 32) >> 4),
+                          db + uint64_t((kb * XKB + ks * 32) >> 4), IDESC1, (kb | ks) ? 1u : 0u);
+        umma_commit(&bar[2]);
+    }
+    __syncwarp();
+
+    // ---- 5. Gram block on CUDA cores: G[a][c] = k_a · X_c (a < TMAX, c < 2 TMAX), 2 threads
+    //         per entry; CK[v][a] = k_a·k_v, CQ[v][a] = k_a·q_v
     {
-        const int npair = T * (T + 1) / 2;
-        for (int p = tid; p < npair; p += Cfg::NTHR) {
-            int v = int((sqrtf(8.f * p + 1.f) - 1.f) * 0.5f);
-            while (v * (v + 1) / 2 > p) --v;
-            while ((v + 1) * (v + 2) / 2 <= p) ++v;
-            const int an = p - v * (v + 1) / 2;
-            bool need = true;
-            if constexpr (TREE) {
-                int x = v;
-                need = false;
-                while (x >= 0) { if (x == an) { need = true; break; } x = par[x]; }
+        constexpr int NENT = TMAX * 2 * TMAX;
+        const int half = tid & 1;
+        for (int e = tid >> 1; e < NENT; e += Cfg::NTHR / 2) {
+            const int an = e / (2 * TMAX), c = e - an * (2 * TMAX);
+            const float4* xa = reinterpret_cast<const float4*>(XP + an * XS + half * (D / 2));
+            const float4* xc = reinterpret_cast<const float4*>(XP + c * XS + half * (D / 2));
+            float s0 = 0.f, s1 = 0.f;
+#pragma unroll 4
+            for (int q = 0; q < D / 8; ++q) {
+                const float4 u = xa[q], w = xc[q];
+                s0 = fmaf(u.x, w.x, s0);
+                s1 = fmaf(u.y, w.y, s1);
+                s0 = fmaf(u.z, w.z, s0);
+                s1 = fmaf(u.w, w.w, s1);
             }
-            float kk = 0.f, kq = 0.f;
-            if (need) {
-#pragma unroll 8
-                for (int j = 0; j < D; ++j) {
-                    const float* xr = X + size_t(j) * XS;
-                    const float ka = xr[an];
-                    kk = fmaf(ka, xr[v], kk);
-                    kq = fmaf(ka, xr[TMAX + v], kq);
-                }
+            float s = s0 + s1;
+            s += __shfl_xor_sync(0xffffffffu, s, 1);
+            if (half == 0) {
+                if (c < TMAX) CK[c * TMAX + an] = s;
+                else CQ[(c - TMAX) * TMAX + an] = s;
             }
-            CK[v * TMAX + an] = kk;
-            CQ[v * TMAX + an] = kq;
         }
     }
     __syncthreads();
@@ -318,165 +510,129 @@ gdn_verify_kernel(const VerifyArgs a) {
         if constexpr (TREE) nanc[v] = m;
     }
 
-    // ---- 5. S_0·[K|Q]: each warp reduces over its quarter of Dk
-    if (!mbar_wait_bounded(&bar[warp], 0) && lane == 0) set_status(a.status, GDN_STATUS_WAIT_TIMEOUT);
-    __syncwarp();
-    const float* Sw = Ss + size_t(warp) * JPW * D;
-    float av[TMAX], bv[TMAX];
-#pragma unroll
-    for (int pass = 0; pass < Cfg::NPASS; ++pass) {
-        float acc[RPL][PC];
-#pragma unroll
-        for (int r = 0; r < RPL; ++r)
-#pragma unroll
-            for (int c = 0; c < PC; ++c) acc[r][c] = 0.f;
-        const float* Xp = X + size_t(warp) * JPW * XS + pass * PC;
-#pragma unroll 2
-        for (int jj = 0; jj < JPW; ++jj) {
-            float s[RPL];
-            load_rows<RPL>(Sw + size_t(jj) * D + lane * RPL, s);
-            const float4* xr = reinterpret_cast<const float4*>(Xp + size_t(jj) * XS);
-#pragma unroll
-            for (int c4 = 0; c4 < PC / 4; ++c4) {
-                const float4 x = xr[c4];
-#pragma unroll
-                for (int r = 0; r < RPL; ++r) {
-                    acc[r][4 * c4 + 0] = fmaf(s[r], x.x, acc[r][4 * c4 + 0]);
-                    acc[r][4 * c4 + 1] = fmaf(s[r], x.y, acc[r][4 * c4 + 1]);
-                    acc[r][4 * c4 + 2] = fmaf(s[r], x.z, acc[r][4 * c4 + 2]);
-                    acc[r][4 * c4 + 3] = fmaf(s[r], x.w, acc[r][4 * c4 + 3]);
-                }
-            }
+    // ---- 6. once the first pass is done: S_0 tile -> S_lo in place; second pass S_lo·X_hi
+    if (!mbar_wait_bounded(&bar[2], 0) && lane == 0) set_status(a.status, GDN_STATUS_WAIT_TIMEOUT);
+    tc_fence_after();
+    {
+        constexpr int CHUNKS = KB * D * 8;          // 16-byte chunks of rows < D
+#pragma unroll 4
+        for (int c = tid; c < CHUNKS; c += Cfg::NTHR) {
+            const int kb = c / (D * 8), w = c - kb * (D * 8);
+            float4* p = reinterpret_cast<float4*>(As + kb * Cfg::A_KB + w * 16);
+            float4 v = *p;
+            v.x -= tf32_trunc(v.x);
+            v.y -= tf32_trunc(v.y);
+            v.z -= tf32_trunc(v.z);
+            v.w -= tf32_trunc(v.w);
+            *p = v;
         }
-        if constexpr (Cfg::PART_IN_CHUNK) {
-            // the warp's own S_0 quarter is dead now: park the partial sums there as [c][i]
-            __syncwarp();
-            float* P = Ss + size_t(warp) * JPW * D;
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (tid == 0) {
+        constexpr uint32_t IDESC2 = umma_idesc_tf32(128, NP);
+        const uint64_t da = umma_desc_sw128(sA), db = umma_desc_sw128(sX);
 #pragma unroll
-            for (int c = 0; c < PC; ++c) {
-                float v[RPL];
+        for (int kb = 0; kb < KB; ++kb)
 #pragma unroll
-                for (int r = 0; r < RPL; ++r) v[r] = acc[r][c];
-                store_rows<RPL>(P + size_t(c) * D + lane * RPL, v);
-            }
-            __syncthreads();
-            if (tid < D) {
+            for (int ks = 0; ks < 4; ++ks)
+                umma_tf32(tbase, da + uint64_t((kb * Cfg::A_KB + ks * 32) >> 4),
+                          db + uint64_t((kb * XKB + ks * 32) >> 4), IDESC2, 1u);
+        umma_commit(&bar[2]);
+    }
+    __syncwarp();
+    if (!mbar_wait_bounded(&bar[2], 1) && lane == 0) set_status(a.status, GDN_STATUS_WAIT_TIMEOUT);
+    tc_fence_after();
+
+    // ---- 7. per-row recurrence for δ and o (thread = state row i, TMEM lane i)
+    if (tid < D) {
+        float pr[2 * NP];
 #pragma unroll
-                for (int t = 0; t < TMAX; ++t) {
-                    float sa = 0.f, sb = 0.f;
+        for (int c = 0; c < 2 * NP; c += 16) tmem_ld16(tbase + (uint32_t(warp * 32) << 16) + c, pr + c);
 #pragma unroll
-                    for (int w = 0; w < Cfg::NWARP; ++w) {
-                        sa += Ss[size_t(w) * JPW * D + size_t(t) * D + tid];
-                        sb += Ss[size_t(w) * JPW * D + size_t(TMAX + t) * D + tid];
+        for (int c = 0; c < NP; ++c) pr[c] += pr[NP + c];     // + S_hi·X_lo
+        const int i = tid;
+        IO* out = static_cast<IO*>(a.out);
+        const float scale = a.qk_scale;
+        if constexpr (!TREE) {
+            float dl[TMAX];
+#pragma unroll
+            for (int t = 0; t < TMAX; ++t) {
+                dl[t] = 0.f;
+                if (t < T) {
+                    float sk = c0[t] * pr[t], sq = c0[t] * pr[TMAX + t];
+#pragma unroll
+                    for (int s = 0; s < t; ++s) {
+                        sk = fmaf(CK[t * TMAX + s], dl[s], sk);
+                        sq = fmaf(CQ[t * TMAX + s], dl[s], sq);
                     }
-                    av[t] = sa;
-                    bv[t] = sb;
+                    const float u = gam[t] * sk;
+                    const float d = bet[t] * (yv[t] - u);
+                    dl[t] = d;
+                    const float o = scale * fmaf(d, kqv[t], gam[t] * sq);
+                    const size_t oi = ((lb * T + t) * Hv + h) * size_t(D) + i;
+                    a.tape_delta[oi] = d;
+                    Tr::store(out, oi, o);
                 }
             }
         } else {
-            // deterministic warp-ordered accumulation into R[col][row]
+#pragma unroll
+            for (int v = 0; v < TMAX; ++v) {
+                if (v < T) {
+                    const float ca = c0[v];
+                    float sk = ca * pr[v], sq = ca * pr[TMAX + v];
+                    const int m = nanc[v];
 #pragma unroll 1
-            for (int w = 0; w < Cfg::NWARP; ++w) {
-                if (warp == w) {
-#pragma unroll
-                    for (int c = 0; c < PC; ++c) {
-                        float* dst = R + size_t(pass * PC + c) * D + lane * RPL;
-                        float v[RPL];
-                        if (w == 0) {
-#pragma unroll
-                            for (int r = 0; r < RPL; ++r) v[r] = acc[r][c];
-                        } else {
-                            float o[RPL];
-                            load_rows<RPL>(dst, o);
-#pragma unroll
-                            for (int r = 0; r < RPL; ++r) v[r] = o[r] + acc[r][c];
-                        }
-                        store_rows<RPL>(dst, v);
+                    for (int q = 0; q < m; ++q) {
+                        const int an = anc[v * TMAX + q];
+                        const float da = DL[size_t(an) * D + i];
+                        sk = fmaf(CK[v * TMAX + an], da, sk);
+                        sq = fmaf(CQ[v * TMAX + an], da, sq);
                     }
+                    const float u = gam[v] * sk;
+                    const float d = bet[v] * (DL[size_t(v) * D + i] - u);
+                    DL[size_t(v) * D + i] = d;
+                    const float o = scale * fmaf(d, kqv[v], gam[v] * sq);
+                    const size_t oi = ((lb * T + v) * Hv + h) * size_t(D) + i;
+                    a.tape_delta[oi] = d;
+                    Tr::store(out, oi, o);
                 }
-                __syncthreads();
             }
         }
     }
-
-    // ---- 6. per-row recurrence for δ and o (thread = state row i)
-    if (tid >= D) return;
-    const int i = tid;
-    IO* out = static_cast<IO*>(a.out);
-    const float scale = a.qk_scale;
-    if constexpr (!TREE) {
-        if constexpr (Cfg::USE_R) {
-#pragma unroll
-            for (int t = 0; t < TMAX; ++t) {
-                av[t] = R[size_t(t) * D + i];
-                bv[t] = R[size_t(TMAX + t) * D + i];
-            }
-        }
-        float dl[TMAX];
-#pragma unroll
-        for (int t = 0; t < TMAX; ++t) {
-            dl[t] = 0.f;
-            if (t < T) {
-                float sk = c0[t] * av[t], sq = c0[t] * bv[t];
-#pragma unroll
-                for (int s = 0; s < t; ++s) {
-                    sk = fmaf(CK[t * TMAX + s], dl[s], sk);
-                    sq = fmaf(CQ[t * TMAX + s], dl[s], sq);
-                }
-                const float u = gam[t] * sk;
-                const float d = bet[t] * (yv[t] - u);
-                dl[t] = d;
-                const float o = scale * fmaf(d, kqv[t], gam[t] * sq);
-                const size_t oi = ((lb * T + t) * Hv + h) * size_t(D) + i;
-                a.tape_delta[oi] = d;
-                Tr::store(out, oi, o);
-            }
-        }
-    } else {
-#pragma unroll 1
-        for (int v = 0; v < T; ++v) {
-            const float ca = c0[v];
-            float sk = ca * R[size_t(v) * D + i], sq = ca * R[size_t(TMAX + v) * D + i];
-            const int m = nanc[v];
-#pragma unroll 1
-            for (int q = 0; q < m; ++q) {
-                const int an = anc[v * TMAX + q];
-                const float da = DL[size_t(an) * D + i];
-                sk = fmaf(CK[v * TMAX + an], da, sk);
-                sq = fmaf(CQ[v * TMAX + an], da, sq);
-            }
-            const float u = gam[v] * sk;
-            const float d = bet[v] * (DL[size_t(v) * D + i] - u);
-            DL[size_t(v) * D + i] = d;
-            const float o = scale * fmaf(d, kqv[v], gam[v] * sq);
-            const size_t oi = ((lb * T + v) * Hv + h) * size_t(D) + i;
-            a.tape_delta[oi] = d;
-            Tr::store(out, oi, o);
-        }
-    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 1)
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;"
+                     ::"r"(tbase), "r"(uint32_t(Cfg::TMEM_COLS)));
 }
 
 template <typename IO, int D, int TMAX, bool TREE>
-cudaError_t launch_verify_t(const VerifyArgs& a, cudaStream_t stream) {
-    using Cfg = VerifyCfg<D, TMAX, TREE>;
+cudaError_t launch_verify_t(const VerifyArgs& a, const CUtensorMap& map, cudaStream_t stream) {
+    using Cfg = VerifyCfg<IO, D, TMAX, TREE>;
     auto kern = gdn_verify_kernel<IO, D, TMAX, TREE>;
-    static bool attr_done = false;   // benign race: setting the attribute twice is harmless
-    if (!attr_done) {
+    const size_t smem = Cfg::smem_bytes(a.T, a.W);
+    if (smem > 227 * 1024) return cudaErrorInvalidValue;
+    static int attr_set = 0;   // largest size configured so far (benign race: idempotent)
+    if (int(smem) > attr_set) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             int(Cfg::SMEM));
+                                             int(smem));
         if (e != cudaSuccess) return e;
-        attr_done = true;
+        attr_set = int(smem);
     }
     dim3 grid(a.Hv, a.B, a.L);
-    kern<<<grid, Cfg::NTHR, Cfg::SMEM, stream>>>(a);
+    kern<<<grid, Cfg::NTHR, smem, stream>>>(a, map);
     return cudaGetLastError();
 }
 
 template <typename IO, bool TREE>
-cudaError_t launch_verify_io(const VerifyArgs& a, int D, cudaStream_t s) {
+cudaError_t launch_verify_io(const VerifyArgs& a, const CUtensorMap& map, int D, cudaStream_t s) {
     const int tm = a.T <= 4 ? 4 : a.T <= 8 ? 8 : a.T <= 16 ? 16 : 32;
 #define GDN_V_CASE(DD, TM) \
-    if (D == DD && tm == TM) return launch_verify_t<IO, DD, TM, TREE>(a, s);
+    if (D == DD && tm == TM) return launch_verify_t<IO, DD, TM, TREE>(a, map, s);
     GDN_V_CASE(32, 4) GDN_V_CASE(32, 8) GDN_V_CASE(32, 16) GDN_V_CASE(32, 32)
     GDN_V_CASE(64, 4) GDN_V_CASE(64, 8) GDN_V_CASE(64, 16) GDN_V_CASE(64, 32)
     GDN_V_CASE(128, 4) GDN_V_CASE(128, 8) GDN_V_CASE(128, 16) GDN_V_CASE(128, 32)

@@ -104,7 +104,7 @@ def model_weights(w: Workload, seed=0, device="cpu"):
 
 
 def initial_state(w: Workload, seed=0, device="cpu"):
-    """(state [L, B, Hv, Dk, Dv] fp32, conv_state [L, B, W-1, C] io dtype)."""
+    """(state [L, B, Hv, Dv, Dk] fp32 (row-major S), conv_state [L, B, W-1, C] io dtype)."""
     g = generator(seed, _wid(w), 0, "state", device)
     st = torch.randn((w.L, w.B, w.Hv, w.D, w.D), generator=g, device=device)
     st.mul_(0.1)

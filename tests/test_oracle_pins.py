@@ -28,9 +28,9 @@ def rand_inputs(rng, L=1, B=1, T=4, Hk=2, Hv=4, D=8, W=4, state_std=0.1):
     return dims, x
 
 
-def S_of(state_kv):
-    """[..., Dk, Dv] key-major storage -> S [..., Dv, Dk]."""
-    return np.swapaxes(state_kv, -1, -2)
+def S_of(state):
+    """Stored state [..., Dv, Dk] is S itself (row i in Dv, column j in Dk)."""
+    return state
 
 
 def silu(y):
