@@ -226,6 +226,28 @@ GDN_API int spec_accept_tree(const spec_dims* d, const void* logits, const int32
                      int32_t* path, int32_t* n_acc, int32_t* out_tokens, uint32_t* status,
                      void* stream);
 
+/*
+ * spec_accept_static — spec_accept without a caller-provided workspace, for callers that cannot
+ * allocate device memory (code that only receives device pointers from its host framework, runs
+ * where cudaMalloc is not allowed, or must not allocate on this path). The pages describe no such
+ * call; it is a deployment convenience of this library.
+ *
+ * The scratch is a fixed array of GDN_STATIC_SCRATCH_BYTES bytes in the library's device image,
+ * held by every device that loads the library until the process exits; nothing is allocated or
+ * freed. Arguments and results are those of spec_accept. Limits:
+ *  - a shape whose spec_workspace_bytes() exceeds GDN_STATIC_SCRATCH_BYTES returns
+ *    GDN_ERR_UNSUPPORTED (use spec_accept with a workspace instead);
+ *  - all calls on a device share the array: calls whose kernels may overlap on the GPU (different
+ *    streams without ordering) race and must not be issued;
+ *  - the first call on each device looks up the array's device address with that device current;
+ *    make that first call outside of any stream capture.
+ */
+#define GDN_STATIC_SCRATCH_BYTES (1u << 20)
+GDN_API int spec_accept_static(const spec_dims* d, const void* logits, const int32_t* drafts,
+                               int32_t mode, float temperature, uint64_t seed, uint64_t round,
+                               int32_t* n_acc, int32_t* out_tokens, uint32_t* status,
+                               void* stream);
+
 /* Thread-local message for the last non-OK return on this thread ("" if none). */
 GDN_API const char* gdn_last_error(void);
 

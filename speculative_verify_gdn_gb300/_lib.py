@@ -31,7 +31,7 @@ STATUS_BITS = {
 # exported entry points of include/gdnspec.h
 EXPORTS = ("gdn_verify", "gdn_verify_tree", "gdn_rollback", "gdn_rollback_path",
            "gdn_tape_bytes", "spec_accept", "spec_workspace_bytes", "spec_accept_tree",
-           "gdn_last_error")
+           "spec_accept_static", "gdn_last_error")
 
 
 class GdnError(RuntimeError):
@@ -81,6 +81,8 @@ def load(require_file=True):
     lib.spec_workspace_bytes.restype = sz
     lib.spec_accept_tree.argtypes = [P, P, P, P, i32, P, sz, P, P, P, P, P]
     lib.spec_accept_tree.restype = ct.c_int
+    lib.spec_accept_static.argtypes = [P, P, P, i32, f32, u64, u64, P, P, P, P]
+    lib.spec_accept_static.restype = ct.c_int
     lib.gdn_last_error.argtypes = []
     lib.gdn_last_error.restype = ct.c_char_p
     _lib = lib

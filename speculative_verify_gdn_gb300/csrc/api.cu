@@ -196,6 +196,16 @@ gdn::AcceptArgs accept_args(const spec_dims* d, const void* logits, void* worksp
 
 }  // namespace
 
+namespace gdn {
+int report_error(int code, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return code;
+}
+}  // namespace gdn
+
 extern "C" {
 
 int gdn_verify(const gdn_dims* d, const void* qkv, const void* conv_w, const void* conv_state,

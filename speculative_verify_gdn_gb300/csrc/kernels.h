@@ -64,6 +64,9 @@ struct AcceptArgs {
     uint32_t* status;
 };
 
+// Sets the calling thread's gdn_last_error() message and returns `code`.
+int report_error(int code, const char* fmt, ...);
+
 // Vocabulary chunking shared by spec_accept's workspace size query and its launches.
 void accept_chunking(int rows, int V, int* CH, int* CS);
 
