@@ -67,6 +67,13 @@ def test_verify_conv_widths_and_dtypes(gdnlib, W, io):
     run_verify_case(w, seed=W)
 
 
+@pytest.mark.parametrize("Hk,Hv,T", [(4, 4, 8), (3, 6, 2), (1, 2, 7)])
+def test_verify_head_groupings(gdnlib, Hk, Hv, T):
+    """One and two value heads per key head at d = 128 (both layouts of the pipelined kernel)."""
+    w = small(I.WORKLOADS[1], L=2, B=3, N=T, Hk=Hk, Hv=Hv, D=128, V=64)
+    run_verify_case(w, seed=Hk * 10 + Hv)
+
+
 def test_verify_qwen36_b1(gdnlib):
     """The 30-layer Qwen3.6-shaped stack at batch 1, N = 4, every output compared."""
     run_verify_case(I.WORKLOADS[1])
