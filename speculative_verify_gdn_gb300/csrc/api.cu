@@ -93,6 +93,36 @@ int state_tensor_map(const gdn_dims* d, const float* state, CUtensorMap* map) {
     return GDN_OK;
 }
 
+// 2-D views of the bf16 inputs for the pipelined verify: qkv rows (l, b, t) x channels, boxes of
+// 128 channels x T rows; conv-state rows (l, b, w) x channels, boxes of 128 channels x (W-1) rows.
+// Returns false (no error) when the shape does not suit them.
+bool input_tensor_maps(const gdn_dims* d, const void* qkv, const void* conv_state,
+                       gdn::VerifyMaps* m) {
+    EncodeTiledFn enc = encode_tiled();
+    if (!enc || d->io_dtype != GDN_DTYPE_BF16 || d->Dk != 128 || d->Dv != 128 || d->T > 256 ||
+        (size_t(d->C) * 2) % 16 != 0)
+        return false;
+    cuuint32_t estr[2] = {1, 1};
+    cuuint64_t strides[1] = {cuuint64_t(d->C) * 2};
+    cuuint64_t qdims[2] = {cuuint64_t(d->C), cuuint64_t(d->L) * d->B * d->T};
+    cuuint32_t qbox[2] = {128, cuuint32_t(d->T)};
+    if (enc(&m->qkv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(qkv), qdims, strides, qbox,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return false;
+    if (d->W > 1) {
+        cuuint64_t cdims[2] = {cuuint64_t(d->C), cuuint64_t(d->L) * d->B * (d->W - 1)};
+        cuuint32_t cbox[2] = {128, cuuint32_t(d->W - 1)};
+        if (enc(&m->conv_state, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(conv_state),
+                cdims, strides, cbox, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return false;
+    } else {
+        m->conv_state = m->qkv;   // never read: no conv-state rows when W == 1
+    }
+    return true;
+}
+
 int verify_common(const gdn_dims* d, const int32_t* parent, const void* qkv, const void* conv_w,
                   const void* conv_state, const float* g, const float* beta, const float* state,
                   void* out, float* tape_delta, float* tape_k, uint32_t* status, void* stream,
@@ -117,13 +147,14 @@ int verify_common(const gdn_dims* d, const int32_t* parent, const void* qkv, con
     a.qkv = qkv; a.conv_w = conv_w; a.conv_state = conv_state; a.g = g; a.beta = beta;
     a.state = state; a.out = out; a.tape_delta = tape_delta; a.tape_k = tape_k;
     a.parent = tree ? parent : nullptr; a.status = status;
-    CUtensorMap map;
-    rc = state_tensor_map(d, state, &map);
+    gdn::VerifyMaps maps;
+    rc = state_tensor_map(d, state, &maps.state);
     if (rc) return rc;
+    maps.inputs_ok = !tree && input_tensor_maps(d, qkv, conv_state, &maps);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = d->io_dtype == GDN_DTYPE_BF16
-                        ? gdn::launch_verify_bf16(a, map, d->Dk, tree, s)
-                        : gdn::launch_verify_f32(a, map, d->Dk, tree, s);
+                        ? gdn::launch_verify_bf16(a, maps, d->Dk, tree, s)
+                        : gdn::launch_verify_f32(a, maps, d->Dk, tree, s);
     if (e != cudaSuccess) return cuda_fail(e, tree ? "gdn_verify_tree launch" : "gdn_verify launch");
     return GDN_OK;
 }

@@ -23,11 +23,21 @@ struct VerifyArgs {
     uint32_t* status;
 };
 
-// verify: D = Dk = Dv; `smap` is the 2-D TMA map of the state (rows [L*B*Hv*Dv] x cols [Dk],
-// 32 x Dv boxes, 128-byte swizzle). One translation unit per element type of qkv / conv / out.
-cudaError_t launch_verify_bf16(const VerifyArgs& a, const CUtensorMap& smap, int D, bool tree,
+// TMA maps of one verify call. `state`: rows [L*B*Hv*Dv] x cols [Dk], 32 x Dv boxes, 128-byte
+// swizzle. `qkv`: rows [L*B*T] x channels [C], boxes of 128 channels x T rows; `conv_state`: rows
+// [L*B*(W-1)] x channels [C], boxes of 128 channels x (W-1) rows (no swizzle). `inputs_ok` is false
+// when the two input maps could not be made (then only kernels that do not use them run).
+struct VerifyMaps {
+    CUtensorMap state;
+    CUtensorMap qkv;
+    CUtensorMap conv_state;
+    bool inputs_ok;
+};
+
+// verify: D = Dk = Dv. One translation unit per element type of qkv / conv / out.
+cudaError_t launch_verify_bf16(const VerifyArgs& a, const VerifyMaps& m, int D, bool tree,
                                cudaStream_t s);
-cudaError_t launch_verify_f32(const VerifyArgs& a, const CUtensorMap& smap, int D, bool tree,
+cudaError_t launch_verify_f32(const VerifyArgs& a, const VerifyMaps& m, int D, bool tree,
                               cudaStream_t s);
 
 struct RollbackArgs {

@@ -157,9 +157,14 @@ __device__ __forceinline__ float tf32_trunc(float x) {
     return __uint_as_float(__float_as_uint(x) & 0xFFFFE000u);
 }
 
-// y · sigmoid(y) with the fast exponential and division (relative error ~1e-6)
+// y · sigmoid(y) = y / (1 + 2^(−y·log2 e)) on the special-function unit: ex2.approx and
+// rcp.approx, each within a few ulp (relative error ~1e-6 overall); subnormals flush to zero, so
+// very negative y gives 2^+big = +inf and a result of −0, very positive y gives y.
 __device__ __forceinline__ float silu_fast(float y) {
-    return __fdividef(y, 1.0f + __expf(-y));
+    float e, r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(y * -1.4426950408889634f));
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.0f + e));
+    return y * r;
 }
 
 // Sum each of V per-lane values over the warp by recursive halving: V-1 + log2(32/V) shuffles.

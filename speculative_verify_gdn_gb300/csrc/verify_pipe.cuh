@@ -4,23 +4,31 @@
 // Same computation as verify_impl.cuh (see its header for the method and the sources): per value
 // head, P = S_0·[K|Q] in three TF32 products on tcgen05, the Gram block, and the per-row
 // recurrence for δ and o. What changes is the schedule. One CTA per SM walks a sequence of key
-// heads ("units": (layer, sequence, key head), each with its value heads) through a pipeline of
-// warp roles that hand work to each other through mbarriers:
+// heads ("units": (layer, sequence, key head), each with its value heads) through warp roles that
+// hand work to each other through mbarriers:
 //
-//   warp 0       loader    bulk copies of a unit's raw qkv / conv rows (staging ring, 2 slots) and
-//                          the 2-D TMA of each value head's 64 KiB state tile (tile ring, 2 slots)
-//   warp 1       mma       allocates TMEM; per head: first pass S_raw·[X_hi ; X_lo] (A from shared
-//                          memory), then, once the lo tile is in TMEM, S_lo·X_hi (A from TMEM)
-//   warps 2-5    prep      per unit: conv + SiLU, norms, the [X_hi ; X_lo] tile, the Gram block and
-//                          each value head's gate coefficients (unit ring, 2 slots)
-//   warps 6-9    convert   per head: S_lo = S − trunc_tf32(S) from the shared-memory tile into TMEM
-//                          (then the tile slot is free for the next TMA)
-//   warps 10-13  epilogue  per head: P rows from TMEM, recurrence, o and δ stores (TMEM ring, 4)
+//   warp 0       state loader  2-D TMA of each state K-block (128 rows x 32 fp32 = 16 KiB) into a
+//                              ring of shared-memory slots
+//   warp 14      input loader  per part (q, k, each v): one 2-D TMA box of the conv-state rows, one
+//                              of the unit's T qkv rows and one bulk copy of the conv taps (staging
+//                              ring, 2 slots)
+//   warps 6-9    convert       per K-block: S_hi = trunc_tf32(S) and S_lo = S − S_hi from the slot
+//                              into a ring of TMEM slots (32 + 32 columns); the shared-memory slot is
+//                              free as soon as it has been read
+//   warp 1       mma           per K-block: S_hi·[X_hi ; X_lo] and S_lo·X_hi, both with A from TMEM,
+//                              into separate accumulators; the unit's value heads (or, with one
+//                              value head, even and odd K-steps) in turn, so that consecutive MMAs
+//                              never update the same accumulator (2 unit slots of P in TMEM)
+//   warps 2-5    prep          per unit: conv + SiLU, norms, the [X_hi ; X_lo] tile, the Gram block
+//                              (mma.sync, 3xTF32) and each value head's coefficient records
+//   warps 10-13  epilogue      per head: P rows from TMEM (sum of its partial accumulators),
+//                              recurrence, o and δ stores
 //
-// So a state tile occupies shared memory only from its TMA to the end of its conversion, the key
-// head's prologue is computed once for its value heads, and the prologue / epilogue of other heads
-// overlap every tile's load. Every wait is bounded: on a timeout the CTA records WAIT_TIMEOUT and
-// stops waiting (results are then garbage, never a hang).
+// The state stream is read from shared memory exactly once (by the convert warps: the tensor core
+// takes both operand halves from TMEM), and a shared-memory slot is held only from its TMA until
+// its K-block has been split, so the loader runs ahead of the unit prologue by the whole ring.
+// Every wait is bounded: on a timeout the CTA records WAIT_TIMEOUT, the producers stop issuing, and
+// the other roles run on without waiting (results are then garbage, never a hang).
 #pragma once
 
 #include "verify_impl.cuh"
@@ -30,38 +38,52 @@ namespace gdn {
 template <typename IO, int TMAX, int G>
 struct PipeCfg {
     static constexpr int D = 128, KB = 4, ES = int(sizeof(IO));
-    static constexpr int NTHR = 448;
+    static constexpr int NWARP = 15, NTHR = 32 * NWARP;
     static constexpr int NP = 2 * TMAX < 16 ? 16 : 2 * TMAX;
     static constexpr int XROWS = 2 * NP, XKB = XROWS * 128, X_BYTES = KB * XKB;
-    static constexpr int A_BYTES = KB * 128 * 128;          // 64 KiB state tile
-    static constexpr int NPARTS = 2 + G;                    // q, k, v of each value head
-    static constexpr int NRMAX = 3 + TMAX;                  // staged rows per part (W <= 4)
-    static constexpr int XP_STRIDE = D + 4;
+    static constexpr int KSLOT = 128 * 128;                 // one state K-block: 128 rows x 128 B
+    static constexpr int NKS = 8;                            // shared-memory K-block slots
+    static constexpr int NTS = 4;                            // TMEM K-block slots (hi 32 + lo 32)
+    // accumulator chains per value head: with one value head per unit, even and odd K-steps go to
+    // separate accumulators, so every unit has two chains to alternate with
+    static constexpr int S = G == 1 ? 2 : 1;
+    // TMEM: 2 unit slots of 2 chains x (hi pass: 2NP columns, lo pass: NP columns, 32-aligned),
+    // then the K-block ring
+    static constexpr int CH_COLS = 64, P_COLS = 2 * CH_COLS;
+    static constexpr int T_RING = 2 * P_COLS;
+    static constexpr int TMEM_COLS = 512;
+    static constexpr int NPARTS = 2 + G;                     // q, k, v of each value head
+    static constexpr int NRMAX = 3 + TMAX;                   // staged rows per part (W <= 4)
     static constexpr int RAW_BYTES = NPARTS * NRMAX * D * ES + NPARTS * D * 4 * ES;
-    static constexpr int XP_BYTES = 2 * TMAX * XP_STRIDE * 4;
-    static constexpr int STAGE_BYTES = ((RAW_BYTES > XP_BYTES ? RAW_BYTES : XP_BYTES) + 127) / 128 * 128;
-    // meta slot (floats): Graw[TMAX][2TMAX], kq[TMAX], per head {CK, CQ [TMAX][TMAX], c0, gam, bet
-    // [TMAX]}, V[G][TMAX][D]
-    static constexpr int MH = 2 * TMAX * TMAX + 3 * TMAX;
-    static constexpr int M_GRAW = 0, M_KQ = M_GRAW + 2 * TMAX * TMAX, M_HEAD = M_KQ + TMAX,
-                         M_V = M_HEAD + G * MH, M_FLOATS = M_V + G * TMAX * D;
+    static constexpr int STAGE_BYTES = (RAW_BYTES + 127) / 128 * 128;
+    // meta slot (floats): per value head j and position t a record {c0, γ, β, k_t·q_t, CK[TMAX],
+    // CQ[TMAX]} (16-byte aligned), then the conv outputs V[G][TMAX][D]
+    static constexpr int RS = 4 + 2 * TMAX;
+    static constexpr int M_REC = 0, M_V = G * TMAX * RS, M_FLOATS = M_V + G * TMAX * D;
     static constexpr int META_BYTES = (M_FLOATS * 4 + 127) / 128 * 128;
-    // TMEM: 4 P slots of 2NP columns at 0.., 2 lo tiles of 128 columns at 128..
-    static constexpr int TMEM_COLS = 512, T_LO = 128;
+    // prep scratch (floats): norm partials [4][2TMAX], inverse norms [2TMAX], Gram partials
+    // [4 warps][16][8], Gram [TMAX][2TMAX]
+    static constexpr int S_NRM = 0, S_INV = S_NRM + 8 * TMAX, S_GP = S_INV + 2 * TMAX,
+                         S_GRAM = S_GP + 4 * 128, S_FLOATS = S_GRAM + 2 * TMAX * TMAX;
 
-    static constexpr size_t OFF_A = 0;
-    static constexpr size_t OFF_X = OFF_A + 2 * size_t(A_BYTES);
+    static constexpr size_t OFF_RING = 0;
+    static constexpr size_t OFF_X = OFF_RING + size_t(NKS) * KSLOT;
     static constexpr size_t OFF_STAGE = OFF_X + 2 * size_t(X_BYTES);
     static constexpr size_t OFF_META = OFF_STAGE + 2 * size_t(STAGE_BYTES);
-    static constexpr size_t OFF_NRM = OFF_META + 2 * size_t(META_BYTES);   // [4][2TMAX] + inv
-    static constexpr size_t OFF_BAR = (OFF_NRM + size_t(4 * 2 * TMAX + 2 * TMAX) * 4 + 15) / 16 * 16;
-    static constexpr int NBAR = 26;
-    static constexpr size_t OFF_MISC = OFF_BAR + NBAR * 8;                   // tslot, abort
+    static constexpr size_t OFF_SCR = OFF_META + 2 * size_t(META_BYTES);
+    static constexpr size_t OFF_BAR = (OFF_SCR + size_t(S_FLOATS) * 4 + 15) / 16 * 16;
+    static constexpr int NBAR = 2 * NKS + 2 * NTS + 2 + 2 + 2 + 2 + 2 + 2 + 1;
+    static constexpr size_t OFF_MISC = OFF_BAR + NBAR * 8;   // TMEM base, abort flag
     static constexpr size_t SMEM = OFF_MISC + 16 + 1024;
 
-    static_assert(2 * NP * 4 <= 128, "4 P slots must fit below the lo tiles");
+    static_assert(T_RING + NTS * 64 <= TMEM_COLS, "TMEM budget");
+    static_assert(2 * NP + NP <= CH_COLS && 2 * NP == 32, "one chain: hi pass at +0, lo pass at +32");
+    static_assert(G * S == 2, "two accumulator chains per unit");
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
     static_assert(OFF_X % 1024 == 0 && X_BYTES % 1024 == 0, "swizzle atoms need 1024-byte bases");
+    static_assert((RS * 4) % 16 == 0 && (M_V * 4) % 16 == 0, "records are read as float4");
+    static_assert(2 * TMAX <= 16 && TMAX <= 8, "Gram block is one m16n8 tile");
+    static_assert(G * TMAX * TMAX <= 128, "one prep thread per coefficient");
 };
 
 __device__ __forceinline__ void named_bar(int id, int nthreads) {
@@ -85,17 +107,37 @@ __device__ __forceinline__ bool pwait(uint64_t* bar, uint32_t parity, volatile i
     }
 }
 
+// pwait by lane 0, result broadcast: every lane of the warp takes the same branch
+__device__ __forceinline__ bool pwait_warp(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
+                                           uint32_t* status) {
+    int ok = 0;
+    if ((threadIdx.x & 31) == 0) ok = pwait(bar, parity, abort_flag, status) ? 1 : 0;
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    __syncwarp();
+    return ok != 0;
+}
+
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
-__device__ __forceinline__ void umma_tf32_ts(uint32_t dtmem, uint32_t atmem, uint64_t bdesc,
-                                             uint32_t idesc, uint32_t accumulate) {
+// D[tmem] (+)= A[tmem] · B[smem descriptor]ᵀ, kind::tf32. Called by a whole converged warp with
+// warp-uniform operands; one elected lane issues. (Issue from a lone diverged lane costs about three
+// times as many cycles per MMA as the tensor core needs for these small shapes.)
+__device__ __forceinline__ void umma_tf32_ts_warp(uint32_t dtmem, uint32_t atmem, uint64_t bdesc,
+                                                  uint32_t idesc, uint32_t accumulate) {
     asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}"
+        "{\n\t.reg .pred p, e;\n\telect.sync _|e, 0xffffffff;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "@e tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}"
         ::"r"(dtmem), "r"(atmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
+}
+
+__device__ __forceinline__ void umma_commit_warp(uint64_t* bar) {
+    asm volatile(
+        "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}"
+        ::"r"(smem_u32(bar)) : "memory");
 }
 
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
@@ -110,41 +152,61 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
         : "memory");
 }
 
+__device__ __forceinline__ bool elect_one() {
+    uint32_t e;
+    asm volatile("{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}" : "=r"(e));
+    return e != 0;
+}
+
+// warp-level D(16x8) += A(16x8) · B(8x8), TF32 operands (already truncated), fp32 accumulate
+__device__ __forceinline__ void mma_tf32_16x8x8(float (&d)[4], const uint32_t (&av)[4], uint32_t b0,
+                                                uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(av[0]), "r"(av[1]), "r"(av[2]), "r"(av[3]), "r"(b0), "r"(b1));
+}
+
 template <typename IO, int TMAX, int G>
-__global__ void __launch_bounds__(448, 1)
-gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap smap, int n_units) {
+__global__ void __launch_bounds__(PipeCfg<IO, TMAX, G>::NTHR, 1)
+gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap smap,
+                       const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap cmap,
+                       int n_units) {
     using Cfg = PipeCfg<IO, TMAX, G>;
-    constexpr int D = Cfg::D, NP = Cfg::NP, XKB = Cfg::XKB, XS = Cfg::XP_STRIDE;
+    constexpr int D = Cfg::D, NP = Cfg::NP, XKB = Cfg::XKB, RS = Cfg::RS;
+    constexpr int NKS = Cfg::NKS, NTS = Cfg::NTS;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    // mbarriers: state tiles (full / empty), first pass done, lo tile ready / free, P slots
-    // (full / empty), staging slots (full / empty), unit slots (full / empty)
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::OFF_BAR);
-    uint64_t* afull = bars + 0;
-    uint64_t* aempty = bars + 2;
-    uint64_t* p1done = bars + 4;
-    uint64_t* convdone = bars + 6;
-    uint64_t* loempty = bars + 8;
-    uint64_t* tfull = bars + 10;
-    uint64_t* tempty = bars + 14;
-    uint64_t* sfull = bars + 18;
-    uint64_t* sempty = bars + 20;
-    uint64_t* ufull = bars + 22;
-    uint64_t* uempty = bars + 24;     // two arrivals: last MMA pass of the unit, epilogue
+    uint64_t* kfull = bars;                      // K-block landed in its shared-memory slot
+    uint64_t* kempty = kfull + NKS;              // slot read by the 4 convert warps
+    uint64_t* tmfull = kempty + NKS;             // hi / lo of a K-block in its TMEM slot (4 warps)
+    uint64_t* tmempty = tmfull + NTS;            // TMEM slot consumed by the MMAs (commit)
+    uint64_t* tfull = tmempty + NTS;             // unit's P slot complete (commit)
+    uint64_t* tempty = tfull + 2;                // unit's P slot read by the 4 epilogue warps
+    uint64_t* sfull = tempty + 2;                // staged inputs landed
+    uint64_t* sempty = sfull + 2;                // staging slot released by prep
+    uint64_t* ufull = sempty + 2;                // unit prologue (X tile, meta) ready
+    uint64_t* uempty = ufull + 2;                // unit slot free: last MMA commit + 4 epilogue warps
+    uint64_t* mdone = uempty + 2;                // every MMA of this CTA complete
     uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + Cfg::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::OFF_MISC + 4);
-    float* nrm = reinterpret_cast<float*>(smem + Cfg::OFF_NRM);              // [4][2TMAX]
-    float* inv = nrm + 4 * 2 * TMAX;                                         // [2TMAX]
+    float* scr = reinterpret_cast<float*>(smem + Cfg::OFF_SCR);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int T = a.T, Hk = a.Hk, Hv = a.Hv, C = a.C, W = a.W, B = a.B;
     const int NR = W - 1 + T;
+    const int n_my = blockIdx.x < n_units ? (n_units - 1 - int(blockIdx.x)) / int(gridDim.x) + 1 : 0;
 
     if (tid == 0) {
-        for (int i = 0; i < 24; ++i) mbar_init(&bars[i], 1);
-        mbar_init(&uempty[0], 2);
-        mbar_init(&uempty[1], 2);
+        for (int i = 0; i < Cfg::NBAR; ++i) {
+            uint64_t* bb = &bars[i];
+            const bool four = (bb >= kempty && bb < kempty + NKS) || (bb >= tmfull && bb < tmfull + NTS) ||
+                              (bb >= tempty && bb < tempty + 2);
+            mbar_init(bb, four ? 4 : (bb >= uempty && bb < uempty + 2) ? 5 : 1);
+        }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -158,140 +220,157 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
     tc_fence_after();
     const uint32_t tbase = *tslot;
 
-    auto unit_of = [&](int iu, int& l, int& b, int& kh) -> bool {
+    auto unit_of = [&](int iu, int& l, int& b, int& kh) {
         const int u = blockIdx.x + iu * gridDim.x;
-        if (u >= n_units) return false;
         kh = u % Hk;
         const int lbi = u / Hk;
         l = lbi / B;
         b = lbi - l * B;
-        return true;
     };
 
     if (warp == 0) {
-        // ------------------------------------------------------------------ loader
-        const IO* qkv = static_cast<const IO*>(a.qkv);
-        const IO* cst = static_cast<const IO*>(a.conv_state);
+        // ------------------------------------------------------------------ state loader (whole warp)
+        int s = 0, issued = 0;
+        uint32_t ph = 0;
+        bool ok = true;
+        for (int iu = 0; iu < n_my && ok; ++iu) {
+            int l, b, kh;
+            unit_of(iu, l, b, kh);
+            const size_t lb = size_t(l) * B + b;
+            // K-block major, value heads minor: the order in which the MMAs consume them
+            for (int kb = 0; kb < Cfg::KB && ok; ++kb) {
+                for (int j = 0; j < G; ++j) {
+                    const int row0 = int((lb * Hv + kh * G + j) * D);
+                    if (!pwait_warp(&kempty[s], ph ^ 1, abort_flag, a.status)) { ok = false; break; }
+                    if (elect_one()) {
+                        mbar_arrive_expect_tx(&kfull[s], uint32_t(Cfg::KSLOT));
+                        tma_load_2d(smem + Cfg::OFF_RING + size_t(s) * Cfg::KSLOT, &smap, kb * 32, row0,
+                                    &kfull[s]);
+                    }
+                    __syncwarp();
+                    ++issued;
+                    if (++s == NKS) { s = 0; ph ^= 1; }
+                }
+            }
+        }
+        // drain: the copies in flight must land before the CTA may exit
+        volatile int no_abort = 0;
+        for (int k = 1; k <= NKS && k <= issued; ++k) {
+            const int q = issued - k;
+            pwait_warp(&kfull[q % NKS], uint32_t(q / NKS) & 1u, &no_abort, a.status);
+        }
+    } else if (warp == 14) {
+        // ------------------------------------------------------------------ input loader (whole warp)
+        // staged layout per part: W-1 conv-state rows then T qkv rows (D channels each), then the
+        // conv taps of every part [NPARTS][D][W]; all destinations are multiples of 128 bytes
         const IO* cw = static_cast<const IO*>(a.conv_w);
-        int n = 0, l, b, kh;
-        for (int iu = 0; unit_of(iu, l, b, kh); ++iu) {
+        const uint32_t bytes = uint32_t(Cfg::NPARTS * NR * D * Cfg::ES + Cfg::NPARTS * D * W * Cfg::ES);
+        int issued = 0;
+        for (int iu = 0; iu < n_my; ++iu) {
+            int l, b, kh;
+            unit_of(iu, l, b, kh);
             const size_t lb = size_t(l) * B + b;
             const int ss = iu & 1;
-            unsigned char* st = smem + Cfg::OFF_STAGE + size_t(ss) * Cfg::STAGE_BYTES;
-            IO* qs = reinterpret_cast<IO*>(st);
+            IO* qs = reinterpret_cast<IO*>(smem + Cfg::OFF_STAGE + size_t(ss) * Cfg::STAGE_BYTES);
             IO* cws = qs + size_t(Cfg::NPARTS) * NR * D;
-            if (lane == 0) {
-                pwait(&sempty[ss], ((iu >> 1) & 1) ^ 1, abort_flag, a.status);
-                mbar_arrive_expect_tx(&sfull[ss],
-                                      uint32_t(Cfg::NPARTS * NR * D * Cfg::ES + Cfg::NPARTS * D * W * Cfg::ES));
-            }
-            __syncwarp();
-            const int ncopy = Cfg::NPARTS * NR + Cfg::NPARTS;
-            for (int i = lane; i < ncopy; i += 32) {
-                const int p = i < Cfg::NPARTS * NR ? i / NR : i - Cfg::NPARTS * NR;
-                const int cb = p == 0 ? kh * D : (p == 1 ? Hk * D + kh * D : 2 * Hk * D + (kh * G + p - 2) * D);
-                if (i < Cfg::NPARTS * NR) {
-                    const int r = i - p * NR;
-                    const IO* src = r < W - 1 ? cst + (lb * (W - 1) + r) * size_t(C) + cb
-                                              : qkv + (lb * T + (r - (W - 1))) * size_t(C) + cb;
-                    bulk_g2s(qs + size_t(i) * D, src, uint32_t(D * Cfg::ES), &sfull[ss]);
-                } else {
-                    bulk_g2s(cws + size_t(p) * D * W, cw + (size_t(l) * C + cb) * W,
+            if (!pwait_warp(&sempty[ss], ((iu >> 1) & 1) ^ 1, abort_flag, a.status)) break;
+            if (elect_one()) {
+                mbar_arrive_expect_tx(&sfull[ss], bytes);
+#pragma unroll
+                for (int part = 0; part < Cfg::NPARTS; ++part) {
+                    const int cb = part == 0 ? kh * D
+                                 : part == 1 ? Hk * D + kh * D : 2 * Hk * D + (kh * G + part - 2) * D;
+                    IO* dst = qs + size_t(part) * NR * D;
+                    if (W > 1) tma_load_2d(dst, &cmap, cb, int(lb * (W - 1)), &sfull[ss]);
+                    tma_load_2d(dst + size_t(W - 1) * D, &qmap, cb, int(lb * T), &sfull[ss]);
+                    bulk_g2s(cws + size_t(part) * D * W, cw + (size_t(l) * C + cb) * W,
                              uint32_t(D * W * Cfg::ES), &sfull[ss]);
                 }
             }
-            if (lane == 0) {
-                for (int j = 0; j < G; ++j, ++n) {
-                    const int sa = n & 1;
-                    pwait(&aempty[sa], ((n >> 1) & 1) ^ 1, abort_flag, a.status);
-                    mbar_arrive_expect_tx(&afull[sa], uint32_t(Cfg::A_BYTES));
-                    unsigned char* At = smem + Cfg::OFF_A + size_t(sa) * Cfg::A_BYTES;
-                    const int row0 = int((lb * Hv + kh * G + j) * D);
-                    for (int kb = 0; kb < Cfg::KB; ++kb)
-                        tma_load_2d(At + kb * 16384, &smap, kb * 32, row0, &afull[sa]);
-                }
-            }
             __syncwarp();
+            ++issued;
         }
-        // drain: the last copies must land before the CTA may exit
-        if (lane == 0) {
-            volatile int no_abort = 0;
-            for (int k = 0; k < 2; ++k) {
-                if (n - 1 - k >= 0)
-                    pwait(&afull[(n - 1 - k) & 1], ((n - 1 - k) >> 1) & 1, &no_abort, a.status);
-            }
-            int nu = 0;
-            for (int l2, b2, k2; unit_of(nu, l2, b2, k2);) ++nu;
-            for (int k = 0; k < 2; ++k) {
-                if (nu - 1 - k >= 0)
-                    pwait(&sfull[(nu - 1 - k) & 1], ((nu - 1 - k) >> 1) & 1, &no_abort, a.status);
-            }
+        volatile int no_abort = 0;
+        for (int k = 1; k <= 2 && k <= issued; ++k) {
+            const int q = issued - k;
+            pwait_warp(&sfull[q & 1], uint32_t(q >> 1) & 1u, &no_abort, a.status);
         }
     } else if (warp == 1) {
-        // ------------------------------------------------------------------ mma
+        // ------------------------------------------------------------------ mma (whole warp)
+        // chain c of a unit slot: hi pass (N = 2NP) at c * CH_COLS, lo pass (N = NP) at + 32. Per
+        // K-step the order is hi of every chain, then lo of every chain: the same accumulator comes
+        // back only every 4 MMAs, past the tensor core's accumulate latency.
+        constexpr int S = Cfg::S;
         constexpr uint32_t IDESC1 = umma_idesc_tf32(128, 2 * NP);
         constexpr uint32_t IDESC2 = umma_idesc_tf32(128, NP);
-        const uint32_t sA0 = smem_u32(smem + Cfg::OFF_A), sX0 = smem_u32(smem + Cfg::OFF_X);
-        int n = 0, l, b, kh;
-        auto second_pass = [&](int m) {
-            const int ium = m / G, jm = m - ium * G, us = ium & 1, st = m & 3, sl = m & 1;
-            pwait(&convdone[sl], (m >> 1) & 1, abort_flag, a.status);
-            tc_fence_after();
+        const uint32_t sX0 = smem_u32(smem + Cfg::OFF_X);
+        int ts = 0;
+        uint32_t tph = 0;
+        bool ok = true;
+        for (int iu = 0; iu < n_my && ok; ++iu) {
+            const int us = iu & 1;
+            if (!pwait_warp(&ufull[us], (iu >> 1) & 1, abort_flag, a.status)) break;
+            if (!pwait_warp(&tempty[us], ((iu >> 1) & 1) ^ 1, abort_flag, a.status)) break;
             const uint64_t db = umma_desc_sw128(sX0 + us * Cfg::X_BYTES);
-            const uint32_t dt = tbase + st * 2 * NP, at0 = tbase + Cfg::T_LO + sl * 128;
+            const uint32_t dt = tbase + us * Cfg::P_COLS;
+            for (int kb = 0; kb < Cfg::KB; ++kb) {
+                int slot[G];
 #pragma unroll
-            for (int kb = 0; kb < Cfg::KB; ++kb)
-#pragma unroll
-                for (int ks = 0; ks < 4; ++ks)
-                    umma_tf32_ts(dt, at0 + kb * 32 + ks * 8, db + uint64_t((kb * XKB + ks * 32) >> 4),
-                                 IDESC2, 1u);
-            umma_commit(&tfull[st]);
-            umma_commit(&loempty[sl]);
-            if (jm == G - 1) umma_commit(&uempty[us]);
-        };
-        if (lane == 0) {
-            for (int iu = 0; unit_of(iu, l, b, kh); ++iu) {
-                const int us = iu & 1;
-                for (int j = 0; j < G; ++j, ++n) {
-                    if (j == 0) pwait(&ufull[us], (iu >> 1) & 1, abort_flag, a.status);
-                    const int sa = n & 1, st = n & 3;
-                    pwait(&afull[sa], (n >> 1) & 1, abort_flag, a.status);
-                    pwait(&tempty[st], ((n >> 2) & 1) ^ 1, abort_flag, a.status);
-                    tc_fence_after();
-                    const uint64_t da = umma_desc_sw128(sA0 + sa * Cfg::A_BYTES);
-                    const uint64_t db = umma_desc_sw128(sX0 + us * Cfg::X_BYTES);
-                    const uint32_t dt = tbase + st * 2 * NP;
-#pragma unroll
-                    for (int kb = 0; kb < Cfg::KB; ++kb)
-#pragma unroll
-                        for (int ks = 0; ks < 4; ++ks)
-                            umma_tf32(dt, da + uint64_t((kb * 16384 + ks * 32) >> 4),
-                                      db + uint64_t((kb * XKB + ks * 32) >> 4), IDESC1,
-                                      (kb | ks) ? 1u : 0u);
-                    umma_commit(&p1done[sa]);
-                    if (n >= 1) second_pass(n - 1);
+                for (int j = 0; j < G; ++j) {
+                    if (!pwait_warp(&tmfull[ts], tph, abort_flag, a.status)) ok = false;
+                    slot[j] = ts;
+                    if (++ts == NTS) { ts = 0; tph ^= 1; }
                 }
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) {
+                    const uint64_t bk = db + uint64_t((kb * XKB + ks * 32) >> 4);
+                    const uint32_t acc = (kb > 0 || ks >= S) ? 1u : 0u;
+#pragma unroll
+                    for (int j = 0; j < G; ++j) {
+                        const int c = j * S + ks % S;
+                        umma_tf32_ts_warp(dt + c * Cfg::CH_COLS, tbase + Cfg::T_RING + slot[j] * 64 + ks * 8,
+                                          bk, IDESC1, acc);
+                    }
+#pragma unroll
+                    for (int j = 0; j < G; ++j) {
+                        const int c = j * S + ks % S;
+                        umma_tf32_ts_warp(dt + c * Cfg::CH_COLS + 32,
+                                          tbase + Cfg::T_RING + slot[j] * 64 + 32 + ks * 8, bk, IDESC2, acc);
+                    }
+                }
+#pragma unroll
+                for (int j = 0; j < G; ++j) umma_commit_warp(&tmempty[slot[j]]);
             }
-            if (n >= 1) second_pass(n - 1);
-            // drain: every MMA must have completed before TMEM is released
-            volatile int no_abort = 0;
-            if (n >= 1) pwait(&tfull[(n - 1) & 3], ((n - 1) >> 2) & 1, &no_abort, a.status);
+            if (ok) {
+                umma_commit_warp(&tfull[us]);
+                umma_commit_warp(&uempty[us]);
+            }
         }
-        __syncwarp();
+        // drain: every MMA must have completed before TMEM is released
+        umma_commit_warp(mdone);
+        volatile int no_abort = 0;
+        pwait_warp(mdone, 0, &no_abort, a.status);
     } else if (warp < 6) {
         // ------------------------------------------------------------------ prep (128 threads)
         const int p = tid - 64, pw = warp - 2;
-        int l, b, kh;
-        for (int iu = 0; unit_of(iu, l, b, kh); ++iu) {
+        const int gq = lane >> 2, gt4 = lane & 3;       // mma.sync fragment coordinates
+        float* nrm = scr + Cfg::S_NRM;
+        float* inv = scr + Cfg::S_INV;
+        float* gp = scr + Cfg::S_GP;
+        float* gram = scr + Cfg::S_GRAM;
+        for (int iu = 0; iu < n_my; ++iu) {
+            int l, b, kh;
+            unit_of(iu, l, b, kh);
             const size_t lb = size_t(l) * B + b;
             const int ss = iu & 1, us = iu & 1;
             unsigned char* st = smem + Cfg::OFF_STAGE + size_t(ss) * Cfg::STAGE_BYTES;
             const IO* qs = reinterpret_cast<const IO*>(st);
             const IO* cws = qs + size_t(Cfg::NPARTS) * NR * D;
-            float* XP = reinterpret_cast<float*>(st);
             unsigned char* Xb = smem + Cfg::OFF_X + size_t(us) * Cfg::X_BYTES;
             float* meta = reinterpret_cast<float*>(smem + Cfg::OFF_META + size_t(us) * Cfg::META_BYTES);
-            // gates of this thread's (value head j, position t), loaded early
+            // gates of this thread's (value head gj, position gt), loaded early
             float g_in = 0.f, b_in = 0.f;
             const int gj = p / TMAX, gt = p - gj * TMAX;
             if (p < G * TMAX && gt < T) {
@@ -306,9 +385,16 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
             for (int part = 0; part < Cfg::NPARTS; ++part) {
                 const IO* col = qs + size_t(part) * NR * D + p;
                 const IO* wp = cws + (size_t(part) * D + p) * W;
-                float wr[4];
+                float wr[4];     // wr[d] multiplies the row at distance d (0 = current token)
+                if (W == 4) {
+                    const uint2 w4 = *reinterpret_cast<const uint2*>(wp);
+                    const IO* wv = reinterpret_cast<const IO*>(&w4);
 #pragma unroll
-                for (int d = 0; d < 4; ++d) wr[d] = (d < W) ? io_to_f(wp[W - 1 - d]) : 0.f;
+                    for (int d = 0; d < 4; ++d) wr[d] = io_to_f(wv[3 - d]);
+                } else {
+#pragma unroll
+                    for (int d = 0; d < 4; ++d) wr[d] = (d < W) ? io_to_f(wp[W - 1 - d]) : 0.f;
+                }
                 float E[3 + TMAX];
 #pragma unroll
                 for (int k = 0; k < 3; ++k) {
@@ -326,34 +412,33 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
                     y[part][t] = (t < T) ? silu_fast(acc) : 0.f;
                 }
             }
-            // norms of q_t (part 0) and k_t (part 1)
+            // norms of k_t (columns 0..TMAX-1) and q_t (columns TMAX..2TMAX-1)
             {
                 float sq[2 * TMAX];
 #pragma unroll
                 for (int t = 0; t < TMAX; ++t) {
-                    sq[t] = y[1][t] * y[1][t];          // k first: columns 0..TMAX-1
-                    sq[TMAX + t] = y[0][t] * y[0][t];   // then q
+                    sq[t] = y[1][t] * y[1][t];
+                    sq[TMAX + t] = y[0][t] * y[0][t];
                 }
                 int ix;
                 const float s = warp_sum_many<2 * TMAX>(sq, lane, &ix);
                 if ((lane & (32 / (2 * TMAX) - 1)) == 0) nrm[pw * 2 * TMAX + ix] = s;
             }
             named_bar(1, 128);
+            if (p == 0) mbar_arrive(&sempty[ss]);         // every staged row has been read
             if (p < 2 * TMAX)
                 inv[p] = 1.0f / sqrtf(nrm[p] + nrm[2 * TMAX + p] + nrm[4 * TMAX + p] +
                                       nrm[6 * TMAX + p] + a.l2_eps);
             named_bar(1, 128);
-            // [X_hi ; X_lo] tile, plain rows for the Gram, tape k, v values, gates
+            // B tile rows n < NP: X as raw fp32 (the tensor core reads it as X_hi = trunc_tf32(X));
+            // rows NP + n: X_lo = X − X_hi. Also the tape k, v values, gates.
 #pragma unroll
             for (int t = 0; t < TMAX; ++t) {
                 const float kn = y[1][t] * inv[t], qn = y[0][t] * inv[TMAX + t];
-                const float kh_ = tf32_trunc(kn), qh_ = tf32_trunc(qn);
-                *reinterpret_cast<float*>(Xb + sw128_off(t, p, XKB)) = kh_;
-                *reinterpret_cast<float*>(Xb + sw128_off(NP + t, p, XKB)) = kn - kh_;
-                *reinterpret_cast<float*>(Xb + sw128_off(TMAX + t, p, XKB)) = qh_;
-                *reinterpret_cast<float*>(Xb + sw128_off(NP + TMAX + t, p, XKB)) = qn - qh_;
-                XP[t * XS + p] = kn;
-                XP[(TMAX + t) * XS + p] = qn;
+                *reinterpret_cast<float*>(Xb + sw128_off(t, p, XKB)) = kn;
+                *reinterpret_cast<float*>(Xb + sw128_off(NP + t, p, XKB)) = kn - tf32_trunc(kn);
+                *reinterpret_cast<float*>(Xb + sw128_off(TMAX + t, p, XKB)) = qn;
+                *reinterpret_cast<float*>(Xb + sw128_off(NP + TMAX + t, p, XKB)) = qn - tf32_trunc(qn);
                 if (t < T) a.tape_k[((lb * T + t) * Hk + kh) * size_t(D) + p] = kn;
             }
 #pragma unroll
@@ -366,143 +451,187 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
 #pragma unroll
                 for (int t = 0; t < TMAX; ++t) meta[Cfg::M_V + (j * TMAX + t) * D + p] = y[2 + j][t];
             if (p < G * TMAX) {
-                float* mh = meta + Cfg::M_HEAD + gj * Cfg::MH;
-                mh[2 * TMAX * TMAX + TMAX + gt] = g_in;         // gam
-                mh[2 * TMAX * TMAX + 2 * TMAX + gt] = b_in;     // bet
+                float* rec = meta + Cfg::M_REC + p * RS;      // record (gj, gt)
+                rec[1] = g_in;
+                rec[2] = b_in;
             }
             fence_async_smem();
             named_bar(1, 128);
-            // Gram block G[a][c] = k_a · X_c, one entry per thread
-            for (int e = p; e < TMAX * 2 * TMAX; e += 128) {
-                const int an = e / (2 * TMAX), c = e - an * (2 * TMAX);
-                const float4* xa = reinterpret_cast<const float4*>(XP + an * XS);
-                const float4* xc = reinterpret_cast<const float4*>(XP + c * XS);
-                float s0 = 0.f, s1 = 0.f;
-#pragma unroll 8
-                for (int q = 0; q < D / 4; ++q) {
-                    const float4 u4 = xa[q], w4 = xc[q];
-                    s0 = fmaf(u4.x, w4.x, s0);
-                    s1 = fmaf(u4.y, w4.y, s1);
-                    s0 = fmaf(u4.z, w4.z, s0);
-                    s1 = fmaf(u4.w, w4.w, s1);
+            // Gram block on the warp tensor path: D[m][n] = X_m · k_n over this warp's 32 channels,
+            // 3xTF32 (hi·hi + hi·lo + lo·hi); rows m: k_0.., q_0.. (zero beyond 2 TMAX)
+            {
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) {
+                    const int ch = 32 * pw + 8 * ks + gt4;
+                    float av[4];
+                    av[0] = *reinterpret_cast<const float*>(Xb + sw128_off(gq, ch, XKB));
+                    av[2] = *reinterpret_cast<const float*>(Xb + sw128_off(gq, ch + 4, XKB));
+                    av[1] = (gq + 8 < 2 * TMAX) ? *reinterpret_cast<const float*>(Xb + sw128_off(gq + 8, ch, XKB)) : 0.f;
+                    av[3] = (gq + 8 < 2 * TMAX) ? *reinterpret_cast<const float*>(Xb + sw128_off(gq + 8, ch + 4, XKB)) : 0.f;
+                    const float bv0 = gq < TMAX ? av[0] : 0.f, bv1 = gq < TMAX ? av[2] : 0.f;
+                    uint32_t ahi[4], alo[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float h = tf32_trunc(av[e]);
+                        ahi[e] = __float_as_uint(h);
+                        alo[e] = __float_as_uint(tf32_trunc(av[e] - h));
+                    }
+                    const float bh0 = tf32_trunc(bv0), bh1 = tf32_trunc(bv1);
+                    const uint32_t bl0 = __float_as_uint(tf32_trunc(bv0 - bh0));
+                    const uint32_t bl1 = __float_as_uint(tf32_trunc(bv1 - bh1));
+                    mma_tf32_16x8x8(acc, ahi, __float_as_uint(bh0), __float_as_uint(bh1));
+                    mma_tf32_16x8x8(acc, ahi, bl0, bl1);
+                    mma_tf32_16x8x8(acc, alo, __float_as_uint(bh0), __float_as_uint(bh1));
                 }
-                meta[Cfg::M_GRAW + e] = s0 + s1;
+                float* g4 = gp + pw * 128;
+                g4[gq * 8 + 2 * gt4] = acc[0];
+                g4[gq * 8 + 2 * gt4 + 1] = acc[1];
+                g4[(gq + 8) * 8 + 2 * gt4] = acc[2];
+                g4[(gq + 8) * 8 + 2 * gt4 + 1] = acc[3];
             }
             named_bar(1, 128);
-            // per value head: CK[v][a] = Γ(a→v-1) k_a·k_v, CQ[v][a] = Γ(a→v-1) k_a·q_v, c0[v]
-            if (p < G * TMAX && gt < T) {
-                float* mh = meta + Cfg::M_HEAD + gj * Cfg::MH;
-                float* CK = mh;
-                float* CQ = mh + TMAX * TMAX;
-                float* c0 = mh + 2 * TMAX * TMAX;
-                const float* gam = c0 + TMAX;
-                const float* Gr = meta + Cfg::M_GRAW;
-                const int v = gt;
-                float coef = 1.f;
-                for (int x = v - 1; x >= 0; --x) {
-                    CK[v * TMAX + x] = coef * Gr[x * 2 * TMAX + v];
-                    CQ[v * TMAX + x] = coef * Gr[x * 2 * TMAX + TMAX + v];
-                    coef *= gam[x];
-                }
-                c0[v] = coef;
-                if (gj == 0) meta[Cfg::M_KQ + v] = Gr[v * 2 * TMAX + TMAX + v];
+            {
+                const int m = p >> 3, n = p & 7;
+                if (m < 2 * TMAX && n < TMAX)
+                    gram[n * 2 * TMAX + m] = gp[p] + gp[128 + p] + gp[256 + p] + gp[384 + p];
             }
             named_bar(1, 128);
-            if (p == 0) {
-                mbar_arrive(&ufull[us]);
-                mbar_arrive(&sempty[ss]);
+            // per value head, one thread per (v, x ≤ v): CK[v][x] = Γ(x→v-1) k_x·k_v and
+            // CQ[v][x] = Γ(x→v-1) k_x·q_v for x < v; c0[v] = Γ(root→v-1) and k_v·q_v for x = v
+            {
+                const int fj = p / (TMAX * TMAX), fv = (p / TMAX) % TMAX, fx = p % TMAX;
+                if (fj < G && fv < T && fx <= fv) {
+                    const float* hrec = meta + Cfg::M_REC + fj * TMAX * RS;     // γ at [y * RS + 1]
+                    float* rec = meta + Cfg::M_REC + (fj * TMAX + fv) * RS;
+                    const int y0 = fx < fv ? fx + 1 : 0;
+                    float coef = 1.f;
+#pragma unroll
+                    for (int yy = 0; yy < TMAX - 1; ++yy)
+                        if (yy >= y0 && yy < fv) coef *= hrec[yy * RS + 1];
+                    if (fx < fv) {
+                        rec[4 + fx] = coef * gram[fx * 2 * TMAX + fv];
+                        rec[4 + TMAX + fx] = coef * gram[fx * 2 * TMAX + TMAX + fv];
+                    } else {
+                        rec[0] = coef;
+                        rec[3] = gram[fv * 2 * TMAX + TMAX + fv];
+                    }
+                }
             }
+            named_bar(1, 128);
+            if (p == 0) mbar_arrive(&ufull[us]);
         }
     } else if (warp < 10) {
         // ------------------------------------------------------------------ convert (128 threads)
         const int q4 = warp & 3, row = 32 * q4 + lane;
-        int n = 0, l, b, kh;
-        for (int iu = 0; unit_of(iu, l, b, kh); ++iu) {
-            for (int j = 0; j < G; ++j, ++n) {
-                const int sa = n & 1, sl = n & 1;
-                pwait(&afull[sa], (n >> 1) & 1, abort_flag, a.status);
-                pwait(&p1done[sa], (n >> 1) & 1, abort_flag, a.status);
-                pwait(&loempty[sl], ((n >> 1) & 1) ^ 1, abort_flag, a.status);
-                tc_fence_after();
-                const unsigned char* At = smem + Cfg::OFF_A + size_t(sa) * Cfg::A_BYTES +
-                                          (row >> 3) * 1024 + (row & 7) * 128;
+        const int nkb = n_my * G * Cfg::KB;
+        int s = 0, ts = 0;
+        uint32_t ph = 0, tph = 0;
+        for (int k = 0; k < nkb; ++k) {
+            pwait(&kfull[s], ph, abort_flag, a.status);
+            const unsigned char* At = smem + Cfg::OFF_RING + size_t(s) * Cfg::KSLOT + row * 128;
+            uint32_t hi[32], lo[32];
 #pragma unroll
-                for (int kb = 0; kb < Cfg::KB; ++kb) {
-                    uint32_t r[32];
-#pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        const float4 v = *reinterpret_cast<const float4*>(At + kb * 16384 + ((c ^ (row & 7)) << 4));
-                        r[4 * c + 0] = __float_as_uint(v.x - tf32_trunc(v.x));
-                        r[4 * c + 1] = __float_as_uint(v.y - tf32_trunc(v.y));
-                        r[4 * c + 2] = __float_as_uint(v.z - tf32_trunc(v.z));
-                        r[4 * c + 3] = __float_as_uint(v.w - tf32_trunc(v.w));
-                    }
-                    tmem_st32(tbase + Cfg::T_LO + sl * 128 + kb * 32 + (uint32_t(32 * q4) << 16), r);
-                }
-                asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-                tc_fence_before();
-                named_bar(2, 128);
-                if (warp == 6 && lane == 0) {
-                    mbar_arrive(&aempty[sa]);
-                    mbar_arrive(&convdone[sl]);
-                }
+            for (int c = 0; c < 8; ++c) {
+                const float4 v = *reinterpret_cast<const float4*>(At + ((c ^ (row & 7)) << 4));
+                const float h0 = tf32_trunc(v.x), h1 = tf32_trunc(v.y), h2 = tf32_trunc(v.z),
+                            h3 = tf32_trunc(v.w);
+                hi[4 * c + 0] = __float_as_uint(h0);
+                hi[4 * c + 1] = __float_as_uint(h1);
+                hi[4 * c + 2] = __float_as_uint(h2);
+                hi[4 * c + 3] = __float_as_uint(h3);
+                lo[4 * c + 0] = __float_as_uint(v.x - h0);
+                lo[4 * c + 1] = __float_as_uint(v.y - h1);
+                lo[4 * c + 2] = __float_as_uint(v.z - h2);
+                lo[4 * c + 3] = __float_as_uint(v.w - h3);
             }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&kempty[s]);
+            pwait(&tmempty[ts], tph ^ 1, abort_flag, a.status);
+            tc_fence_after();
+            const uint32_t ta = tbase + Cfg::T_RING + ts * 64 + (uint32_t(32 * q4) << 16);
+            tmem_st32(ta, hi);
+            tmem_st32(ta + 32, lo);
+            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tmfull[ts]);
+            if (++s == NKS) { s = 0; ph ^= 1; }
+            if (++ts == NTS) { ts = 0; tph ^= 1; }
         }
     } else {
         // ------------------------------------------------------------------ epilogue (128 threads)
         const int q4 = warp & 3, i = 32 * q4 + lane;
         IO* out = static_cast<IO*>(a.out);
         const float scale = a.qk_scale;
-        int n = 0, l, b, kh;
-        for (int iu = 0; unit_of(iu, l, b, kh); ++iu) {
+        constexpr int S = Cfg::S;
+        for (int iu = 0; iu < n_my; ++iu) {
+            int l, b, kh;
+            unit_of(iu, l, b, kh);
             const size_t lb = size_t(l) * B + b;
             const int us = iu & 1;
             const float* meta = reinterpret_cast<const float*>(smem + Cfg::OFF_META + size_t(us) * Cfg::META_BYTES);
             pwait(&ufull[us], (iu >> 1) & 1, abort_flag, a.status);
-            for (int j = 0; j < G; ++j, ++n) {
-                const int st = n & 3, h = kh * G + j;
-                pwait(&tfull[st], (n >> 2) & 1, abort_flag, a.status);
-                tc_fence_after();
-                float pr[2 * NP];
+            pwait(&tfull[us], (iu >> 1) & 1, abort_flag, a.status);
+            tc_fence_after();
+            const uint32_t dt = tbase + us * Cfg::P_COLS + (uint32_t(32 * q4) << 16);
 #pragma unroll
-                for (int c = 0; c < 2 * NP; c += 16)
-                    tmem_ld16(tbase + st * 2 * NP + (uint32_t(32 * q4) << 16) + c, pr + c);
-                tc_fence_before();
-                named_bar(3, 128);
-                if (warp == 10 && lane == 0) mbar_arrive(&tempty[st]);
+            for (int j = 0; j < G; ++j) {
+                const int h = kh * G + j;
+                // P row i of this head: S_hi·X_hi + S_hi·X_lo + S_lo·X_hi over its chains
+                float pr[NP];
 #pragma unroll
-                for (int c = 0; c < NP; ++c) pr[c] += pr[NP + c];
-                const float* mh = meta + Cfg::M_HEAD + j * Cfg::MH;
-                const float* CK = mh;
-                const float* CQ = mh + TMAX * TMAX;
-                const float* c0 = mh + 2 * TMAX * TMAX;
-                const float* gam = c0 + TMAX;
-                const float* bet = gam + TMAX;
-                const float* kqv = meta + Cfg::M_KQ;
+                for (int c = 0; c < NP; ++c) pr[c] = 0.f;
+#pragma unroll
+                for (int sc = 0; sc < S; ++sc) {
+                    const uint32_t ca = dt + (j * S + sc) * Cfg::CH_COLS;
+                    float part[NP];
+#pragma unroll
+                    for (int off = 0; off < 48; off += 16) {
+                        tmem_ld16(ca + off, part);
+#pragma unroll
+                        for (int c = 0; c < NP; ++c) pr[c] += part[c];
+                    }
+                }
+                if (j == G - 1) {
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&tempty[us]);
+                }
+                const float* R = meta + Cfg::M_REC + j * TMAX * RS;
                 const float* vv = meta + Cfg::M_V + size_t(j) * TMAX * D + i;
                 float dl[TMAX];
 #pragma unroll
                 for (int t = 0; t < TMAX; ++t) {
                     dl[t] = 0.f;
                     if (t < T) {
-                        float sk = c0[t] * pr[t], sq = c0[t] * pr[TMAX + t];
+                        const float4 hd = *reinterpret_cast<const float4*>(R + t * RS);  // c0 γ β kq
+                        float ck[TMAX], cq[TMAX];
+#pragma unroll
+                        for (int q = 0; q < (t + 3) / 4; ++q) {
+                            const float4 x = *reinterpret_cast<const float4*>(R + t * RS + 4 + 4 * q);
+                            const float4 y = *reinterpret_cast<const float4*>(R + t * RS + 4 + TMAX + 4 * q);
+                            ck[4 * q] = x.x; ck[4 * q + 1] = x.y; ck[4 * q + 2] = x.z; ck[4 * q + 3] = x.w;
+                            cq[4 * q] = y.x; cq[4 * q + 1] = y.y; cq[4 * q + 2] = y.z; cq[4 * q + 3] = y.w;
+                        }
+                        float sk = hd.x * pr[t], sq = hd.x * pr[TMAX + t];
 #pragma unroll
                         for (int s = 0; s < t; ++s) {
-                            sk = fmaf(CK[t * TMAX + s], dl[s], sk);
-                            sq = fmaf(CQ[t * TMAX + s], dl[s], sq);
+                            sk = fmaf(ck[s], dl[s], sk);
+                            sq = fmaf(cq[s], dl[s], sq);
                         }
-                        const float u = gam[t] * sk;
-                        const float d = bet[t] * (vv[t * D] - u);
+                        const float u = hd.y * sk;
+                        const float d = hd.z * (vv[t * D] - u);
                         dl[t] = d;
-                        const float o = scale * fmaf(d, kqv[t], gam[t] * sq);
+                        const float o = scale * fmaf(d, hd.w, hd.y * sq);
                         const size_t oi = ((lb * T + t) * Hv + h) * size_t(D) + i;
                         a.tape_delta[oi] = d;
                         IoTraits<IO>::store(out, oi, o);
                     }
                 }
             }
-            named_bar(3, 128);
-            if (warp == 10 && lane == 0) mbar_arrive(&uempty[us]);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&uempty[us]);
         }
     }
     tc_fence_before();
@@ -514,7 +643,7 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
 }
 
 template <typename IO, int TMAX, int G>
-cudaError_t launch_verify_pipe_t(const VerifyArgs& a, const CUtensorMap& map, cudaStream_t stream) {
+cudaError_t launch_verify_pipe_t(const VerifyArgs& a, const VerifyMaps& m, cudaStream_t stream) {
     using Cfg = PipeCfg<IO, TMAX, G>;
     auto kern = gdn_verify_pipe_kernel<IO, TMAX, G>;
     static bool attr_done = false;   // benign race: setting the attribute twice is harmless
@@ -532,21 +661,22 @@ cudaError_t launch_verify_pipe_t(const VerifyArgs& a, const CUtensorMap& map, cu
     }
     const int n_units = a.L * a.B * a.Hk;
     const int grid = n_units < nsm ? n_units : nsm;
-    kern<<<grid, Cfg::NTHR, Cfg::SMEM, stream>>>(a, map, n_units);
+    kern<<<grid, Cfg::NTHR, Cfg::SMEM, stream>>>(a, m.state, m.qkv, m.conv_state, n_units);
     return cudaGetLastError();
 }
 
 // The pipelined kernel serves the Qwen3.6 head shape; everything else uses the per-head kernel.
 template <typename IO>
-bool verify_pipe_eligible(const VerifyArgs& a, int D, bool tree) {
-    return !tree && D == 128 && sizeof(IO) == 2 && a.T <= 8 && (a.Hv == a.Hk || a.Hv == 2 * a.Hk);
+bool verify_pipe_eligible(const VerifyArgs& a, const VerifyMaps& m, int D, bool tree) {
+    return m.inputs_ok && !tree && D == 128 && sizeof(IO) == 2 && a.T <= 8 &&
+           (a.Hv == a.Hk || a.Hv == 2 * a.Hk);
 }
 
 template <typename IO>
-cudaError_t launch_verify_pipe(const VerifyArgs& a, const CUtensorMap& map, cudaStream_t s) {
+cudaError_t launch_verify_pipe(const VerifyArgs& a, const VerifyMaps& m, cudaStream_t s) {
     const int G = a.Hv / a.Hk;
-    if (a.T <= 4) return G == 1 ? launch_verify_pipe_t<IO, 4, 1>(a, map, s) : launch_verify_pipe_t<IO, 4, 2>(a, map, s);
-    return G == 1 ? launch_verify_pipe_t<IO, 8, 1>(a, map, s) : launch_verify_pipe_t<IO, 8, 2>(a, map, s);
+    if (a.T <= 4) return G == 1 ? launch_verify_pipe_t<IO, 4, 1>(a, m, s) : launch_verify_pipe_t<IO, 4, 2>(a, m, s);
+    return G == 1 ? launch_verify_pipe_t<IO, 8, 1>(a, m, s) : launch_verify_pipe_t<IO, 8, 2>(a, m, s);
 }
 
 }  // namespace gdn
