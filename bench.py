@@ -106,6 +106,23 @@ def bytes_rollback(w, n_list):
     return w.L * tot + 4 * w.B
 
 
+def bytes_rollback_verify(w, n_list):
+    """Algorithmic bytes of one gdn_rollback_verify launch: the verify's bytes (state read once)
+    plus, for every (layer, sequence) with n > 0, the committed state written back, the previous
+    tape read (δ, k, gates) and the conv window's previous rows read and the new conv rows
+    written."""
+    io = 2 if str(w.io_dtype).endswith("bfloat16") else 4
+    S = w.Hv * w.D * w.D * 4
+    C, W = w.C, w.W
+    tot = 0
+    for n in n_list:
+        n = int(n)
+        if n <= 0:
+            continue
+        tot += S + n * (4 * w.Hv * w.D + 4 * w.Hk * w.D + 4 * w.Hv) + 2 * io * (W - 1) * C
+    return bytes_verify(w) + w.L * tot + 4 * w.B
+
+
 def bytes_accept(w):
     io = 2 if str(w.io_dtype).endswith("bfloat16") else 4
     return w.B * (w.N + 1) * w.V * io + 4 * w.B * (2 * w.N + 2)
@@ -325,18 +342,24 @@ def run_gpu(args, w, world, rank, device):
     pool = make_pool(w, seed, device, POOL)
     r = SpecRound(w, device)
     stream = torch.cuda.current_stream(device)
+    fused = args.fused and w.accept != "tree"
 
     def step(k, rnd, evs=None):
         s = pool[k % POOL]
         if evs is not None:
             evs[0].record(stream)
-        r.verify(s["qkv"], cw, conv_state, s["g"], s["beta"], state, parent=s["parent"])
+        if fused:
+            # the previous round's rollback and this round's verify, one pass over the state
+            r.rollback_verify(s["qkv"], cw, conv_state, s["g"], s["beta"], state)
+        else:
+            r.verify(s["qkv"], cw, conv_state, s["g"], s["beta"], state, parent=s["parent"])
         if evs is not None:
             evs[1].record(stream)
         r.accept(s["logits"], s["drafts"], round_=rnd, seed=seed, parent=s["parent"])
         if evs is not None:
             evs[2].record(stream)
-        r.rollback(s["qkv"], s["g"], state, conv_state)
+        if not fused:
+            r.rollback(s["qkv"], s["g"], state, conv_state)
         if evs is not None:
             evs[3].record(stream)
 
@@ -346,6 +369,9 @@ def run_gpu(args, w, world, rank, device):
 
     K = args.steps
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+    # nlog[k]: accepted counts after timed step k; nlog0: after the last warm-up step (the counts
+    # the first timed fused step commits)
+    nlog0 = r.n_acc.clone()
     nlog = torch.zeros((K, w.B), dtype=torch.int32, device=device)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(device.index if device.index is not None else 0)
@@ -370,19 +396,28 @@ def run_gpu(args, w, world, rank, device):
     nl = nlog.cpu().numpy()
 
     peak, peak_kind = read_peaks()
-    bv = bytes_verify(w)
     ba = bytes_accept(w)
-    brb = [bytes_rollback(w, nl[k]) for k in range(K)]
-    kern = {
-        "gdn_verify": {"ms": statistics.mean(t_ver), "bytes": bv},
-        "spec_accept": {"ms": statistics.mean(t_acc), "bytes": ba},
-        "gdn_rollback": {"ms": statistics.mean(t_rb), "bytes": statistics.mean(brb)},
-    }
+    if fused:
+        nprev = [nlog0.cpu().numpy()] + [nl[k] for k in range(K - 1)]
+        brv = [bytes_rollback_verify(w, nprev[k]) for k in range(K)]
+        kern = {
+            "gdn_rollback_verify": {"ms": statistics.mean(t_ver), "bytes": statistics.mean(brv)},
+            "spec_accept": {"ms": statistics.mean(t_acc), "bytes": ba},
+        }
+        step_bytes = statistics.mean(brv) + ba
+    else:
+        bv = bytes_verify(w)
+        brb = [bytes_rollback(w, nl[k]) for k in range(K)]
+        kern = {
+            "gdn_verify": {"ms": statistics.mean(t_ver), "bytes": bv},
+            "spec_accept": {"ms": statistics.mean(t_acc), "bytes": ba},
+            "gdn_rollback": {"ms": statistics.mean(t_rb), "bytes": statistics.mean(brb)},
+        }
+        step_bytes = bv + ba + statistics.mean(brb)
     for name, e in kern.items():
         e["GBps"] = e["bytes"] / (e["ms"] / 1e3) / 1e9
         e["frac_of_%s_peak" % peak_kind] = e["GBps"] / peak
     dom = max(kern, key=lambda n: kern[n]["ms"])
-    step_bytes = bv + ba + statistics.mean(brb)
     roof = {"bound": "hbm", "kernel": dom, "achieved": kern[dom]["GBps"], "peak": peak,
             "peak_source": "MEASURED_PEAKS.json hbm_gbs (%s)" % peak_kind, "unit": "GB/s",
             "frac": kern[dom]["GBps"] / peak,
@@ -391,21 +426,22 @@ def run_gpu(args, w, world, rank, device):
             "step_frac": step_bytes / (ms_step / 1e3) / 1e9 / peak}
     mean_n = float(nl.mean())
     res = dict(ms_step=ms_step, kernels=kern, roofline=roof, clocks=clk, mean_n=mean_n,
-               launches=K * r.launches_per_step(), ms_total=ms_total)
+               launches=K * r.launches_per_step(fused), ms_total=ms_total, fused=fused)
 
     # ---- end to end: host (pinned) inputs copied in, results copied out, every step
     if not args.no_e2e:
-        res["e2e"] = run_e2e(args, w, r, pool, cw, state, conv_state, device, seed)
+        res["e2e"] = run_e2e(args, w, r, pool, cw, state, conv_state, device, seed, fused)
     return res
 
 
-def run_e2e(args, w, r, pool, cw, state, conv_state, device, seed):
+def run_e2e(args, w, r, pool, cw, state, conv_state, device, seed, fused=False):
     import torch
     keys = ("qkv", "g", "beta", "logits", "drafts")
     host = []
     for s in pool[:2]:
         host.append({k: s[k].cpu().pin_memory() for k in keys})
-    dev = {k: torch.empty_like(pool[0][k]) for k in keys}
+    # two device sets: a fused step commits the previous round from its qkv / g
+    devs = [{k: torch.empty_like(pool[0][k]) for k in keys} for _ in range(2)]
     parent = pool[0]["parent"]
     out_h = torch.empty((w.B, r.out_tokens.shape[1]), dtype=torch.int32).pin_memory()
     n_h = torch.empty((w.B,), dtype=torch.int32).pin_memory()
@@ -416,10 +452,15 @@ def run_e2e(args, w, r, pool, cw, state, conv_state, device, seed):
 
     def step(k):
         hs = host[k % len(host)]
+        dev = devs[k % 2]
         for key in keys:
             dev[key].copy_(hs[key], non_blocking=True)
-        r.step(dev["qkv"], dev["g"], dev["beta"], dev["logits"], dev["drafts"], cw, state,
-               conv_state, round_=k, seed=seed, parent=parent)
+        if fused:
+            r.step_fused(dev["qkv"], dev["g"], dev["beta"], dev["logits"], dev["drafts"], cw,
+                         state, conv_state, round_=k, seed=seed)
+        else:
+            r.step(dev["qkv"], dev["g"], dev["beta"], dev["logits"], dev["drafts"], cw, state,
+                   conv_state, round_=k, seed=seed, parent=parent)
         n_h.copy_(r.n_acc, non_blocking=True)
         out_h.copy_(r.out_tokens, non_blocking=True)
 
@@ -450,6 +491,9 @@ def main(argv=None):
     ap.add_argument("--config", type=int, default=DEFAULT_CONFIG)
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--fused", action="store_true",
+                    help="time the fused step (gdn_rollback_verify + accept) instead of the "
+                         "three calls verify / accept / rollback")
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
@@ -478,12 +522,16 @@ def main(argv=None):
     torch.cuda.set_device(device)
     world, rank = init_dist("nccl")
     res = run_gpu(args, w, world, rank, device)
+    cfg = workload_description(w)
+    cfg["step"] = ("gdn_rollback_verify (the previous round's tape-replay rollback and this "
+                   "round's verify, one pass over the state) + spec_accept" if res["fused"] else
+                   "gdn_verify + spec_accept + gdn_rollback")
     line = {
         "metric": METRIC, "value": aggregate_tokens_per_s(world, w.B, w.N, res["ms_step"]),
         "unit": UNIT, "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": res["ms_step"], "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "io_dtype": "bf16", "data": "synthetic",
-        "config": workload_description(w), "roofline": res["roofline"],
+        "config": cfg, "roofline": res["roofline"],
         "kernels": res["kernels"], "mean_accepted": res["mean_n"],
         "committed_tokens_per_s": world * w.B * (res["mean_n"] + 1) / (res["ms_step"] / 1e3),
         "gpu_launches": res["launches"], "clocks": res["clocks"],

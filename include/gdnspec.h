@@ -158,6 +158,31 @@ GDN_API int gdn_rollback_path(const gdn_dims* d, const int32_t* path, int32_t P,
                       const void* qkv, float* state, void* conv_state, uint32_t* status,
                       void* stream);
 
+/*
+ * gdn_rollback_verify — the previous round's gdn_rollback and this round's gdn_verify in one pass
+ * over the recurrent state (GDN investigation §4 tape replay, §2.2 multi-token verification; the
+ * fusion is this library's scheduling, the pages run the two steps apart). Same result as
+ *     gdn_rollback(d, n_acc_prev, tape_delta_prev, tape_k_prev, g_prev, qkv_prev, state, conv_state)
+ *     gdn_verify  (d, qkv, conv_w, conv_state, g, beta, state, out, tape_delta, tape_k)
+ * up to floating-point rounding: the committed state is formed in fp32 as gdn_rollback forms it and
+ * the verify products are taken from it. With bf16 I/O, Dk = Dv = 128, T ≤ 8 and Hv ∈ {Hk, 2Hk} it
+ * is one kernel that reads each state tile once, commits the previous round's accepted steps where
+ * n_acc_prev[b] > 0, writes the tile back and verifies the new round from it; other shapes run the
+ * two calls. A round loop is then: gdn_rollback_verify (with the previous round's accept result; a
+ * first round passes n_acc_prev = 0), spec_accept; after the last round, gdn_rollback.
+ * Arguments: the previous round's n_acc_prev [B], tape_delta_prev, tape_k_prev, g_prev, qkv_prev
+ * (as gdn_rollback takes them) and this round's verify arguments (as gdn_verify). state and
+ * conv_state are updated in place. tape_delta, tape_k and out must not overlap the previous round's
+ * tape, qkv or g. state, qkv, qkv_prev, conv_w, conv_state, tape_delta_prev and tape_k_prev must be
+ * 16-byte aligned. n outside [0, T] sets GDN_STATUS_BAD_NACC and commits nothing for that sequence.
+ */
+GDN_API int gdn_rollback_verify(const gdn_dims* d, const int32_t* n_acc_prev,
+                        const float* tape_delta_prev, const float* tape_k_prev,
+                        const float* g_prev, const void* qkv_prev, const void* qkv,
+                        const void* conv_w, void* conv_state, const float* g, const float* beta,
+                        float* state, void* out, float* tape_delta, float* tape_k,
+                        uint32_t* status, void* stream);
+
 /* Bytes of tape_delta plus tape_k for the shape d (host only, no GPU). 0 on invalid d. */
 GDN_API size_t gdn_tape_bytes(const gdn_dims* d);
 

@@ -30,7 +30,7 @@ STATUS_BITS = {
 
 # exported entry points of include/gdnspec.h
 EXPORTS = ("gdn_verify", "gdn_verify_tree", "gdn_rollback", "gdn_rollback_path",
-           "gdn_tape_bytes", "spec_accept", "spec_workspace_bytes", "spec_accept_tree",
+           "gdn_rollback_verify", "gdn_tape_bytes", "spec_accept", "spec_workspace_bytes", "spec_accept_tree",
            "spec_accept_static", "gdn_last_error")
 
 
@@ -71,7 +71,9 @@ def load(require_file=True):
     lib.gdn_verify_tree.argtypes = [P] * 13
     lib.gdn_rollback.argtypes = [P] * 10
     lib.gdn_rollback_path.argtypes = [P, P, i32] + [P] * 9
-    for f in (lib.gdn_verify, lib.gdn_verify_tree, lib.gdn_rollback, lib.gdn_rollback_path):
+    lib.gdn_rollback_verify.argtypes = [P] * 17
+    for f in (lib.gdn_verify, lib.gdn_verify_tree, lib.gdn_rollback, lib.gdn_rollback_path,
+              lib.gdn_rollback_verify):
         f.restype = ct.c_int
     lib.gdn_tape_bytes.argtypes = [P]
     lib.gdn_tape_bytes.restype = sz
@@ -213,6 +215,31 @@ def rollback(shape: GdnShape, n_acc, tape_delta, tape_k, g, qkv, state, conv_sta
         pp = _ptr(path, torch.int32, None, "path")
         _check(lib.gdn_rollback_path(ct.byref(d), pp, int(path.shape[1]), *args),
                "gdn_rollback_path")
+
+
+def rollback_verify(shape: GdnShape, n_acc_prev, tape_delta_prev, tape_k_prev, g_prev, qkv_prev,
+                    qkv, conv_w, conv_state, g, beta, state, out, tape_delta, tape_k,
+                    status=None, stream=None):
+    """gdn_rollback_verify: the previous round's rollback and this round's verify in one call."""
+    lib = load()
+    io = shape.io_dtype
+    f32 = torch.float32
+    d = shape.c()
+    args = [_ptr(n_acc_prev, torch.int32, (shape.B,), "n_acc_prev"),
+            _ptr(tape_delta_prev, f32, shape.out_shape(), "tape_delta_prev"),
+            _ptr(tape_k_prev, f32, shape.tape_k_shape(), "tape_k_prev"),
+            _ptr(g_prev, f32, shape.gate_shape(), "g_prev"),
+            _ptr(qkv_prev, io, shape.qkv_shape(), "qkv_prev"),
+            _ptr(qkv, io, shape.qkv_shape(), "qkv"),
+            _ptr(conv_w, io, shape.conv_w_shape(), "conv_w"),
+            _ptr(conv_state, io, shape.conv_state_shape(), "conv_state"),
+            _ptr(g, f32, shape.gate_shape(), "g"), _ptr(beta, f32, shape.gate_shape(), "beta"),
+            _ptr(state, f32, shape.state_shape(), "state"),
+            _ptr(out, io, shape.out_shape(), "out"),
+            _ptr(tape_delta, f32, shape.out_shape(), "tape_delta"),
+            _ptr(tape_k, f32, shape.tape_k_shape(), "tape_k"),
+            _ptr(status, torch.int32, None, "status"), _stream(stream)]
+    _check(lib.gdn_rollback_verify(ct.byref(d), *args), "gdn_rollback_verify")
 
 
 def _spec_dims(logits, B=None, V=None):

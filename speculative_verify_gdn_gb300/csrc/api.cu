@@ -159,6 +159,29 @@ int verify_common(const gdn_dims* d, const int32_t* parent, const void* qkv, con
     return GDN_OK;
 }
 
+// 2-D view of the previous round's qkv for the fused rollback + verify: rows (l, b, t) x channels,
+// boxes of 128 channels x (W-1) rows (the last W-1 raw rows of the new conv window).
+bool prev_qkv_map(const gdn_dims* d, const void* qkv_prev, gdn::VerifyMaps* m) {
+    if (d->W == 1) {
+        m->qkv_prev = m->qkv;      // never read
+        return true;
+    }
+    EncodeTiledFn enc = encode_tiled();
+    if (!enc) return false;
+    cuuint32_t estr[2] = {1, 1};
+    cuuint64_t strides[1] = {cuuint64_t(d->C) * 2};
+    cuuint64_t dims[2] = {cuuint64_t(d->C), cuuint64_t(d->L) * d->B * d->T};
+    cuuint32_t box[2] = {128, cuuint32_t(d->W - 1)};
+    return enc(&m->qkv_prev, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(qkv_prev), dims,
+               strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool overlaps(const void* p, size_t n, const void* q, size_t m) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p), b = reinterpret_cast<uintptr_t>(q);
+    return n && m && a < b + m && b < a + n;
+}
+
 int rollback_common(const gdn_dims* d, const int32_t* path, int32_t P, const int32_t* n_acc,
                     const float* tape_delta, const float* tape_k, const float* g, const void* qkv,
                     float* state, void* conv_state, uint32_t* status, void* stream) {
@@ -341,5 +364,65 @@ int spec_accept_tree(const spec_dims* d, const void* logits, const int32_t* pare
 }
 
 const char* gdn_last_error(void) { return g_err; }
+
+int gdn_rollback_verify(const gdn_dims* d, const int32_t* n_acc_prev, const float* tape_delta_prev,
+                        const float* tape_k_prev, const float* g_prev, const void* qkv_prev,
+                        const void* qkv, const void* conv_w, void* conv_state, const float* g,
+                        const float* beta, float* state, void* out, float* tape_delta,
+                        float* tape_k, uint32_t* status, void* stream) {
+    int rc = check_dims(d);
+    if (rc) return rc;
+    if (empty(d)) return GDN_OK;
+    // every check of both calls comes first: on an error nothing is enqueued
+    if (!n_acc_prev || !tape_delta_prev || !tape_k_prev || !g_prev || !qkv_prev || !qkv || !conv_w ||
+        !g || !beta || !state || !out || !tape_delta || !tape_k || (d->W > 1 && !conv_state))
+        return fail(GDN_ERR_INVALID_ARG, "NULL tensor pointer");
+    if (!aligned(state, 16) || !aligned(qkv, 16) || !aligned(conv_w, 16) || !aligned(qkv_prev, 16) ||
+        !aligned(tape_delta_prev, 16) || !aligned(tape_k_prev, 16) ||
+        (conv_state && !aligned(conv_state, 16)))
+        return fail(GDN_ERR_INVALID_ARG,
+                    "state, qkv, qkv_prev, conv_w, conv_state and the previous tape must be 16-byte "
+                    "aligned (TMA / bulk copies)");
+    const size_t es = io_size(d->io_dtype);
+    if (!aligned(out, es) || !aligned(g, 4) || !aligned(beta, 4) || !aligned(g_prev, 4) ||
+        !aligned(tape_delta, 4) || !aligned(tape_k, 4) || !aligned(n_acc_prev, 4))
+        return fail(GDN_ERR_INVALID_ARG, "misaligned tensor pointer");
+    const size_t lbt = size_t(d->L) * d->B * d->T;
+    const size_t dl_bytes = lbt * d->Hv * d->Dv * 4, k_bytes = lbt * d->Hk * d->Dk * 4;
+    const size_t q_bytes = lbt * d->C * es, o_bytes = lbt * d->Hv * d->Dv * es;
+    const void* outs[3] = {tape_delta, tape_k, out};
+    const size_t out_n[3] = {dl_bytes, k_bytes, o_bytes};
+    const void* ins[4] = {tape_delta_prev, tape_k_prev, qkv_prev, g_prev};
+    const size_t in_n[4] = {dl_bytes, k_bytes, q_bytes, lbt * d->Hv * 4};
+    for (int i = 0; i < 3; ++i)
+        for (int j = 0; j < 4; ++j)
+            if (overlaps(outs[i], out_n[i], ins[j], in_n[j]))
+                return fail(GDN_ERR_INVALID_ARG,
+                            "this round's tape / out overlap the previous round's tape, qkv or g");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (d->io_dtype == GDN_DTYPE_BF16) {
+        gdn::VerifyArgs a{};
+        a.L = d->L; a.B = d->B; a.T = d->T; a.Hk = d->Hk; a.Hv = d->Hv; a.W = d->W; a.C = d->C;
+        a.qk_scale = d->qk_scale; a.l2_eps = d->l2_eps;
+        a.qkv = qkv; a.conv_w = conv_w; a.conv_state = conv_state; a.g = g; a.beta = beta;
+        a.state = state; a.out = out; a.tape_delta = tape_delta; a.tape_k = tape_k;
+        a.parent = nullptr; a.status = status;
+        a.n_acc_prev = n_acc_prev; a.tape_delta_prev = tape_delta_prev; a.tape_k_prev = tape_k_prev;
+        a.g_prev = g_prev; a.qkv_prev = qkv_prev; a.conv_state_out = conv_state;
+        gdn::VerifyMaps maps;
+        rc = state_tensor_map(d, state, &maps.state);
+        if (rc) return rc;
+        maps.inputs_ok = input_tensor_maps(d, qkv, conv_state, &maps) && prev_qkv_map(d, qkv_prev, &maps);
+        cudaError_t e = gdn::launch_rollback_verify_bf16(a, maps, d->Dk, s);
+        if (e == cudaSuccess) return GDN_OK;
+        if (e != cudaErrorNotSupported) return cuda_fail(e, "gdn_rollback_verify launch");
+    }
+    // other shapes: the two calls in sequence (same result)
+    rc = rollback_common(d, nullptr, 0, n_acc_prev, tape_delta_prev, tape_k_prev, g_prev, qkv_prev,
+                         state, conv_state, status, stream);
+    if (rc) return rc;
+    return verify_common(d, nullptr, qkv, conv_w, conv_state, g, beta, state, out, tape_delta,
+                         tape_k, status, stream, false);
+}
 
 }  // extern "C"

@@ -21,6 +21,15 @@ struct VerifyArgs {
     float* tape_k;
     const int32_t* parent;   // tree only (null for the chain)
     uint32_t* status;
+    // gdn_rollback_verify only (null otherwise): the previous round's accepted counts [B], tape
+    // (δ [L][B][T][Hv][Dv], k [L][B][T][Hk][Dk]), gates [L][B][T][Hv] and raw rows [L][B][T][C];
+    // the state and conv_state buffers are then updated in place
+    const int32_t* n_acc_prev;
+    const float* tape_delta_prev;
+    const float* tape_k_prev;
+    const float* g_prev;
+    const void* qkv_prev;
+    void* conv_state_out;
 };
 
 // TMA maps of one verify call. `state`: rows [L*B*Hv*Dv] x cols [Dk], 32 x Dv boxes, 128-byte
@@ -31,6 +40,7 @@ struct VerifyMaps {
     CUtensorMap state;
     CUtensorMap qkv;
     CUtensorMap conv_state;
+    CUtensorMap qkv_prev;    // gdn_rollback_verify: previous round's qkv, boxes of 128 x (W-1)
     bool inputs_ok;
 };
 
@@ -39,6 +49,11 @@ cudaError_t launch_verify_bf16(const VerifyArgs& a, const VerifyMaps& m, int D, 
                                cudaStream_t s);
 cudaError_t launch_verify_f32(const VerifyArgs& a, const VerifyMaps& m, int D, bool tree,
                               cudaStream_t s);
+// gdn_rollback_verify in one kernel when the shape suits the pipelined kernel (bf16, D = 128,
+// T <= 8, Hv in {Hk, 2Hk}); returns cudaErrorNotSupported otherwise (the caller then runs the
+// rollback and the verify as two launches).
+cudaError_t launch_rollback_verify_bf16(const VerifyArgs& a, const VerifyMaps& m, int D,
+                                        cudaStream_t s);
 
 struct RollbackArgs {
     int L, B, T, Hk, Hv, W, C, P;

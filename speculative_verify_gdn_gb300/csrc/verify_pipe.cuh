@@ -29,20 +29,31 @@
 // its K-block has been split, so the loader runs ahead of the unit prologue by the whole ring.
 // Every wait is bounded: on a timeout the CTA records WAIT_TIMEOUT, the producers stop issuing, and
 // the other roles run on without waiting (results are then garbage, never a hang).
+//
+// COMMIT (gdn_rollback_verify): the same pass first commits the previous round's accepted steps,
+// exactly as gdn_rollback does ("GDN investigation" §4, tape replay), then verifies the new round
+// from the committed state. Per unit with n = n_acc_prev[b] > 0 the input loader stages the
+// previous round's k_s and δ_s rows and the coefficients c_s = Γ(s+1 .. n-1), Γ = Γ(0 .. n-1); the
+// convert warps replace each state K-block in shared memory by
+//     S_n = Γ · S_0 + Σ_{s<n} (c_s δ_s) k_sᵀ
+// before splitting it, and a store warp (warp 15) writes it back by TMA store. The conv window is
+// the last W-1 rows of (old conv state ++ the previous round's accepted raw rows), staged from both
+// buffers, and the input loader writes those rows back as the new conv state. So each state tile is
+// read once and written once per round, instead of read by verify, read and written by rollback.
 #pragma once
 
 #include "verify_impl.cuh"
 
 namespace gdn {
 
-template <typename IO, int TMAX, int G>
+template <typename IO, int TMAX, int G, bool COMMIT>
 struct PipeCfg {
     static constexpr int D = 128, KB = 4, ES = int(sizeof(IO));
-    static constexpr int NWARP = 15, NTHR = 32 * NWARP;
+    static constexpr int NWARP = COMMIT ? 16 : 15, NTHR = 32 * NWARP;
     static constexpr int NP = 2 * TMAX < 16 ? 16 : 2 * TMAX;
     static constexpr int XROWS = 2 * NP, XKB = XROWS * 128, X_BYTES = KB * XKB;
     static constexpr int KSLOT = 128 * 128;                 // one state K-block: 128 rows x 128 B
-    static constexpr int NKS = 8;                            // shared-memory K-block slots
+    static constexpr int NKS = COMMIT ? 6 : 8;               // shared-memory K-block slots
     static constexpr int NTS = 4;                            // TMEM K-block slots (hi 32 + lo 32)
     // accumulator chains per value head: with one value head per unit, even and odd K-steps go to
     // separate accumulators, so every unit has two chains to alternate with
@@ -53,7 +64,9 @@ struct PipeCfg {
     static constexpr int T_RING = 2 * P_COLS;
     static constexpr int TMEM_COLS = 512;
     static constexpr int NPARTS = 2 + G;                     // q, k, v of each value head
-    static constexpr int NRMAX = 3 + TMAX;                   // staged rows per part (W <= 4)
+    // staged rows per part (W <= 4): W-1 old conv-state rows, the T qkv rows and, when committing,
+    // W-1 rows of the previous round's qkv ending at its accepted count
+    static constexpr int NRMAX = 3 + TMAX + (COMMIT ? 3 : 0);
     static constexpr int RAW_BYTES = NPARTS * NRMAX * D * ES + NPARTS * D * 4 * ES;
     static constexpr int STAGE_BYTES = (RAW_BYTES + 127) / 128 * 128;
     // meta slot (floats): per value head j and position t a record {c0, γ, β, k_t·q_t, CK[TMAX],
@@ -61,6 +74,11 @@ struct PipeCfg {
     static constexpr int RS = 4 + 2 * TMAX;
     static constexpr int M_REC = 0, M_V = G * TMAX * RS, M_FLOATS = M_V + G * TMAX * D;
     static constexpr int META_BYTES = (M_FLOATS * 4 + 127) / 128 * 128;
+    // commit slot (floats): previous round's k_s rows [TMAX][D], δ_s rows [G][TMAX][D],
+    // c_s = Γ(s+1 .. n-1) [G][TMAX], Γ(0 .. n-1) [G]
+    static constexpr int KP_K = 0, KP_DL = TMAX * D, KP_C = KP_DL + G * TMAX * D,
+                         KP_GAM = KP_C + G * TMAX, KP_FLOATS = KP_GAM + 4;
+    static constexpr int KP_BYTES = COMMIT ? (KP_FLOATS * 4 + 127) / 128 * 128 : 0;
     // prep scratch (floats): norm partials [4][2TMAX], inverse norms [2TMAX], Gram partials
     // [4 warps][16][8], Gram [TMAX][2TMAX]
     static constexpr int S_NRM = 0, S_INV = S_NRM + 8 * TMAX, S_GP = S_INV + 2 * TMAX,
@@ -70,9 +88,10 @@ struct PipeCfg {
     static constexpr size_t OFF_X = OFF_RING + size_t(NKS) * KSLOT;
     static constexpr size_t OFF_STAGE = OFF_X + 2 * size_t(X_BYTES);
     static constexpr size_t OFF_META = OFF_STAGE + 2 * size_t(STAGE_BYTES);
-    static constexpr size_t OFF_SCR = OFF_META + 2 * size_t(META_BYTES);
+    static constexpr size_t OFF_KP = OFF_META + 2 * size_t(META_BYTES);
+    static constexpr size_t OFF_SCR = OFF_KP + 2 * size_t(KP_BYTES);
     static constexpr size_t OFF_BAR = (OFF_SCR + size_t(S_FLOATS) * 4 + 15) / 16 * 16;
-    static constexpr int NBAR = 2 * NKS + 2 * NTS + 2 + 2 + 2 + 2 + 2 + 2 + 1;
+    static constexpr int NBAR = 3 * NKS + 2 * NTS + 8 * 2 + 1;
     static constexpr size_t OFF_MISC = OFF_BAR + NBAR * 8;   // TMEM base, abort flag
     static constexpr size_t SMEM = OFF_MISC + 16 + 1024;
 
@@ -140,6 +159,39 @@ __device__ __forceinline__ void umma_commit_warp(uint64_t* bar) {
         ::"r"(smem_u32(bar)) : "memory");
 }
 
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
+        "%13,%14,%15,%16};"
+        ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]),
+          "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]),
+          "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+
+// shared -> global copies of the async proxy, tracked in the issuing thread's bulk groups
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* src, int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];"
+        ::"l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(src))
+        : "memory");
+}
+__device__ __forceinline__ void bulk_s2g(void* dst, const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;"
+                 ::"l"(dst), "r"(smem_u32(src)), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// every committed group has finished reading its shared-memory source
+__device__ __forceinline__ void bulk_wait_read_all() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// every committed group is complete (its writes are performed)
+__device__ __forceinline__ void bulk_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
@@ -168,12 +220,12 @@ __device__ __forceinline__ void mma_tf32_16x8x8(float (&d)[4], const uint32_t (&
         : "r"(av[0]), "r"(av[1]), "r"(av[2]), "r"(av[3]), "r"(b0), "r"(b1));
 }
 
-template <typename IO, int TMAX, int G>
-__global__ void __launch_bounds__(PipeCfg<IO, TMAX, G>::NTHR, 1)
+template <typename IO, int TMAX, int G, bool COMMIT>
+__global__ void __launch_bounds__(PipeCfg<IO, TMAX, G, COMMIT>::NTHR, 1)
 gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap smap,
                        const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap cmap,
-                       int n_units) {
-    using Cfg = PipeCfg<IO, TMAX, G>;
+                       const __grid_constant__ CUtensorMap pmap, int n_units) {
+    using Cfg = PipeCfg<IO, TMAX, G, COMMIT>;
     constexpr int D = Cfg::D, NP = Cfg::NP, XKB = Cfg::XKB, RS = Cfg::RS;
     constexpr int NKS = Cfg::NKS, NTS = Cfg::NTS;
     extern __shared__ unsigned char smem_raw[];
@@ -181,8 +233,10 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::OFF_BAR);
     uint64_t* kfull = bars;                      // K-block landed in its shared-memory slot
-    uint64_t* kempty = kfull + NKS;              // slot read by the 4 convert warps
-    uint64_t* tmfull = kempty + NKS;             // hi / lo of a K-block in its TMEM slot (4 warps)
+    uint64_t* kempty = kfull + NKS;              // slot free: read by the 4 convert warps, or
+                                                 // (COMMIT) stored back by the store warp
+    uint64_t* kconv = kempty + NKS;              // COMMIT: slot updated by the 4 convert warps
+    uint64_t* tmfull = kconv + NKS;              // hi / lo of a K-block in its TMEM slot (4 warps)
     uint64_t* tmempty = tmfull + NTS;            // TMEM slot consumed by the MMAs (commit)
     uint64_t* tfull = tmempty + NTS;             // unit's P slot complete (commit)
     uint64_t* tempty = tfull + 2;                // unit's P slot read by the 4 epilogue warps
@@ -190,21 +244,24 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
     uint64_t* sempty = sfull + 2;                // staging slot released by prep
     uint64_t* ufull = sempty + 2;                // unit prologue (X tile, meta) ready
     uint64_t* uempty = ufull + 2;                // unit slot free: last MMA commit + 4 epilogue warps
-    uint64_t* mdone = uempty + 2;                // every MMA of this CTA complete
+    uint64_t* kpfull = uempty + 2;               // COMMIT: previous round's tape rows staged
+    uint64_t* kpempty = kpfull + 2;              // COMMIT: commit slot read by the 4 convert warps
+    uint64_t* mdone = kpempty + 2;               // every MMA of this CTA complete
     uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + Cfg::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::OFF_MISC + 4);
     float* scr = reinterpret_cast<float*>(smem + Cfg::OFF_SCR);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int T = a.T, Hk = a.Hk, Hv = a.Hv, C = a.C, W = a.W, B = a.B;
-    const int NR = W - 1 + T;
+    const int NR = COMMIT ? 2 * (W - 1) + T : W - 1 + T;
     const int n_my = blockIdx.x < n_units ? (n_units - 1 - int(blockIdx.x)) / int(gridDim.x) + 1 : 0;
 
     if (tid == 0) {
         for (int i = 0; i < Cfg::NBAR; ++i) {
             uint64_t* bb = &bars[i];
-            const bool four = (bb >= kempty && bb < kempty + NKS) || (bb >= tmfull && bb < tmfull + NTS) ||
-                              (bb >= tempty && bb < tempty + 2);
+            const bool four = (!COMMIT && bb >= kempty && bb < kempty + NKS) ||
+                              (bb >= kconv && bb < kconv + NKS) || (bb >= tmfull && bb < tmfull + NTS) ||
+                              (bb >= tempty && bb < tempty + 2) || (bb >= kpempty && bb < kpempty + 2);
             mbar_init(bb, four ? 4 : (bb >= uempty && bb < uempty + 2) ? 5 : 1);
         }
         *abort_flag = 0;
@@ -226,6 +283,39 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
         const int lbi = u / Hk;
         l = lbi / B;
         b = lbi - l * B;
+    };
+    // previous round's accepted count of sequence b (COMMIT); outside [0, T] it commits nothing
+    // (the input loader reports it)
+    auto n_prev = [&](int b) -> int {
+        if (!COMMIT) return 0;
+        const int n = __ldg(a.n_acc_prev + b);
+        return (n < 0 || n > T) ? 0 : n;
+    };
+    // COMMIT, input-loader warp: once unit iu's staging has landed, write the last W-1 rows of
+    // (old conv state ++ previous accepted rows) — staged row r + n or W-1+T+r — back as the new
+    // conv state of its channels (lane 0 issues; bulk group of lane 0)
+    auto store_conv_rows = [&](int iu, int n) {
+        if (!COMMIT || n == 0 || W == 1) return;
+        int l, b, kh;
+        unit_of(iu, l, b, kh);
+        const size_t lb = size_t(l) * B + b;
+        volatile int no_abort = 0;
+        pwait_warp(&sfull[iu & 1], uint32_t(iu >> 1) & 1u, &no_abort, a.status);
+        if (lane == 0) {
+            const IO* qs = reinterpret_cast<const IO*>(smem + Cfg::OFF_STAGE + size_t(iu & 1) * Cfg::STAGE_BYTES);
+            IO* cso = static_cast<IO*>(a.conv_state_out);
+            for (int part = 0; part < Cfg::NPARTS; ++part) {
+                const int cb = part == 0 ? kh * D
+                             : part == 1 ? Hk * D + kh * D : 2 * Hk * D + (kh * G + part - 2) * D;
+                for (int r = 0; r < W - 1; ++r) {
+                    const int src = r + n < W - 1 ? r + n : W - 1 + T + r;
+                    bulk_s2g(cso + (lb * (W - 1) + r) * size_t(C) + cb, qs + (size_t(part) * NR + src) * D,
+                             uint32_t(D * Cfg::ES));
+                }
+            }
+            bulk_commit();
+        }
+        __syncwarp();
     };
 
     if (warp == 0) {
@@ -261,11 +351,12 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
         }
     } else if (warp == 14) {
         // ------------------------------------------------------------------ input loader (whole warp)
-        // staged layout per part: W-1 conv-state rows then T qkv rows (D channels each), then the
-        // conv taps of every part [NPARTS][D][W]; all destinations are multiples of 128 bytes
+        // staged layout per part: W-1 old conv-state rows, T qkv rows, (COMMIT) W-1 rows of the
+        // previous round's qkv ending at row n-1; then the conv taps of every part [NPARTS][D][W].
+        // All destinations are multiples of 128 bytes. Lane 0 issues every copy (the bulk stores
+        // below are tracked per thread).
         const IO* cw = static_cast<const IO*>(a.conv_w);
-        const uint32_t bytes = uint32_t(Cfg::NPARTS * NR * D * Cfg::ES + Cfg::NPARTS * D * W * Cfg::ES);
-        int issued = 0;
+        int issued = 0, n_last = 0;
         for (int iu = 0; iu < n_my; ++iu) {
             int l, b, kh;
             unit_of(iu, l, b, kh);
@@ -273,9 +364,19 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
             const int ss = iu & 1;
             IO* qs = reinterpret_cast<IO*>(smem + Cfg::OFF_STAGE + size_t(ss) * Cfg::STAGE_BYTES);
             IO* cws = qs + size_t(Cfg::NPARTS) * NR * D;
+            int n = 0;
+            if (COMMIT) {
+                const int nr = __ldg(a.n_acc_prev + b);
+                if ((nr < 0 || nr > T) && lane == 0 && kh == 0 && l == 0)
+                    set_status(a.status, GDN_STATUS_BAD_NACC);
+                n = n_prev(b);
+                // the conv-row stores of two units ago read this staging slot
+                if (lane == 0) bulk_wait_read_all();
+            }
             if (!pwait_warp(&sempty[ss], ((iu >> 1) & 1) ^ 1, abort_flag, a.status)) break;
-            if (elect_one()) {
-                mbar_arrive_expect_tx(&sfull[ss], bytes);
+            if (lane == 0) {
+                const int rows = (W - 1) + T + ((COMMIT && n > 0) ? W - 1 : 0);
+                mbar_arrive_expect_tx(&sfull[ss], uint32_t(Cfg::NPARTS * (rows * D + D * W) * Cfg::ES));
 #pragma unroll
                 for (int part = 0; part < Cfg::NPARTS; ++part) {
                     const int cb = part == 0 ? kh * D
@@ -283,18 +384,62 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
                     IO* dst = qs + size_t(part) * NR * D;
                     if (W > 1) tma_load_2d(dst, &cmap, cb, int(lb * (W - 1)), &sfull[ss]);
                     tma_load_2d(dst + size_t(W - 1) * D, &qmap, cb, int(lb * T), &sfull[ss]);
+                    if (COMMIT && n > 0 && W > 1)   // rows n-(W-1) .. n-1 (negative rows read as 0)
+                        tma_load_2d(dst + size_t(W - 1 + T) * D, &pmap, cb, int(lb * T) + n - (W - 1),
+                                    &sfull[ss]);
                     bulk_g2s(cws + size_t(part) * D * W, cw + (size_t(l) * C + cb) * W,
                              uint32_t(D * W * Cfg::ES), &sfull[ss]);
                 }
             }
             __syncwarp();
+            if (COMMIT) {
+                // previous round's tape rows and gate coefficients of this unit
+                const int ks = iu & 1;
+                float* kp = reinterpret_cast<float*>(smem + Cfg::OFF_KP + size_t(ks) * Cfg::KP_BYTES);
+                const int gj = lane / TMAX, gs = lane - gj * TMAX;
+                float gv = 1.f;
+                if (gj < G && gs < n) gv = __ldg(a.g_prev + (lb * T + gs) * Hv + kh * G + gj);
+                if (!pwait_warp(&kpempty[ks], ((iu >> 1) & 1) ^ 1, abort_flag, a.status)) break;
+#pragma unroll
+                for (int j = 0; j < G; ++j) {
+                    float c = 1.f;                   // the rollback kernel's order: c_s = Γ(s+1 .. n-1)
+#pragma unroll
+                    for (int s2 = TMAX - 1; s2 >= 0; --s2) {
+                        const float gsv = __shfl_sync(0xffffffffu, gv, j * TMAX + s2);
+                        if (s2 < n) {
+                            if (lane == 0) kp[Cfg::KP_C + j * TMAX + s2] = c;
+                            c *= gsv;
+                        }
+                    }
+                    if (lane == 0) kp[Cfg::KP_GAM + j] = c;
+                }
+                __syncwarp();
+                if (lane == 0) {
+                    mbar_arrive_expect_tx(&kpfull[ks], uint32_t(n * (1 + G) * D * 4));
+                    for (int s2 = 0; s2 < n; ++s2) {
+                        bulk_g2s(kp + Cfg::KP_K + s2 * D, a.tape_k_prev + ((lb * T + s2) * Hk + kh) * size_t(D),
+                                 uint32_t(D * 4), &kpfull[ks]);
+#pragma unroll
+                        for (int j = 0; j < G; ++j)
+                            bulk_g2s(kp + Cfg::KP_DL + (j * TMAX + s2) * D,
+                                     a.tape_delta_prev + ((lb * T + s2) * Hv + kh * G + j) * size_t(D),
+                                     uint32_t(D * 4), &kpfull[ks]);
+                    }
+                }
+                __syncwarp();
+                // the previous unit's new conv state: its staged window rows, written back
+                if (iu > 0) store_conv_rows(iu - 1, n_last);
+                n_last = n;
+            }
             ++issued;
         }
+        if (COMMIT && issued > 0) store_conv_rows(issued - 1, n_last);
         volatile int no_abort = 0;
         for (int k = 1; k <= 2 && k <= issued; ++k) {
             const int q = issued - k;
             pwait_warp(&sfull[q & 1], uint32_t(q >> 1) & 1u, &no_abort, a.status);
         }
+        if (COMMIT && lane == 0) bulk_wait_all();
     } else if (warp == 1) {
         // ------------------------------------------------------------------ mma (whole warp)
         // chain c of a unit slot: hi pass (N = 2NP) at c * CH_COLS, lo pass (N = NP) at + 32. Per
@@ -377,6 +522,9 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
                 g_in = __ldg(a.g + (lb * T + gt) * Hv + kh * G + gj);
                 b_in = __ldg(a.beta + (lb * T + gt) * Hv + kh * G + gj);
             }
+            // conv window row r (0 .. W-2): old conv-state row r + n, or (COMMIT, r + n ≥ W-1) the
+            // previous round's raw row staged at W-1+T+r
+            const int n = n_prev(b);
             pwait(&sfull[ss], (iu >> 1) & 1, abort_flag, a.status);
             pwait(&uempty[us], ((iu >> 1) & 1) ^ 1, abort_flag, a.status);
             // conv + SiLU of channel p of every part
@@ -399,7 +547,8 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
 #pragma unroll
                 for (int k = 0; k < 3; ++k) {
                     const int r = k + W - 4;
-                    E[k] = (r >= 0) ? io_to_f(col[size_t(r) * D]) : 0.f;
+                    const int src = r + n < W - 1 ? r + n : W - 1 + T + r;
+                    E[k] = (r >= 0) ? io_to_f(col[size_t(src) * D]) : 0.f;
                 }
 #pragma unroll
                 for (int t = 0; t < TMAX; ++t) E[3 + t] = (t < T) ? io_to_f(col[size_t(W - 1 + t) * D]) : 0.f;
@@ -523,43 +672,136 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
         }
     } else if (warp < 10) {
         // ------------------------------------------------------------------ convert (128 threads)
+        // thread = state row; per K-block (COMMIT: first S ← Γ S + Σ_s (c_s δ_s[row]) k_s, written
+        // back in place) S_hi and S_lo of its 32 columns into the TMEM ring, in two halves of 16
         const int q4 = warp & 3, row = 32 * q4 + lane;
-        const int nkb = n_my * G * Cfg::KB;
         int s = 0, ts = 0;
         uint32_t ph = 0, tph = 0;
-        for (int k = 0; k < nkb; ++k) {
-            pwait(&kfull[s], ph, abort_flag, a.status);
-            const unsigned char* At = smem + Cfg::OFF_RING + size_t(s) * Cfg::KSLOT + row * 128;
-            uint32_t hi[32], lo[32];
+        for (int iu = 0; iu < n_my; ++iu) {
+            int l, b, kh;
+            unit_of(iu, l, b, kh);
+            const int n = n_prev(b);
+            const float* kp = reinterpret_cast<const float*>(smem + Cfg::OFF_KP + size_t(iu & 1) * Cfg::KP_BYTES);
+            float coef[G][TMAX], gam[G];
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const float4 v = *reinterpret_cast<const float4*>(At + ((c ^ (row & 7)) << 4));
-                const float h0 = tf32_trunc(v.x), h1 = tf32_trunc(v.y), h2 = tf32_trunc(v.z),
-                            h3 = tf32_trunc(v.w);
-                hi[4 * c + 0] = __float_as_uint(h0);
-                hi[4 * c + 1] = __float_as_uint(h1);
-                hi[4 * c + 2] = __float_as_uint(h2);
-                hi[4 * c + 3] = __float_as_uint(h3);
-                lo[4 * c + 0] = __float_as_uint(v.x - h0);
-                lo[4 * c + 1] = __float_as_uint(v.y - h1);
-                lo[4 * c + 2] = __float_as_uint(v.z - h2);
-                lo[4 * c + 3] = __float_as_uint(v.w - h3);
+            for (int j = 0; j < G; ++j) {
+                gam[j] = 1.f;
+#pragma unroll
+                for (int s2 = 0; s2 < TMAX; ++s2) coef[j][s2] = 0.f;
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&kempty[s]);
-            pwait(&tmempty[ts], tph ^ 1, abort_flag, a.status);
-            tc_fence_after();
-            const uint32_t ta = tbase + Cfg::T_RING + ts * 64 + (uint32_t(32 * q4) << 16);
-            tmem_st32(ta, hi);
-            tmem_st32(ta + 32, lo);
-            asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&tmfull[ts]);
-            if (++s == NKS) { s = 0; ph ^= 1; }
-            if (++ts == NTS) { ts = 0; tph ^= 1; }
+            if (COMMIT) {
+                pwait(&kpfull[iu & 1], (iu >> 1) & 1, abort_flag, a.status);
+                if (n > 0) {
+#pragma unroll
+                    for (int j = 0; j < G; ++j) {
+                        gam[j] = kp[Cfg::KP_GAM + j];
+#pragma unroll
+                        for (int s2 = 0; s2 < TMAX; ++s2)
+                            if (s2 < n)
+                                coef[j][s2] = kp[Cfg::KP_C + j * TMAX + s2] *
+                                              kp[Cfg::KP_DL + (j * TMAX + s2) * D + row];
+                    }
+                }
+            }
+            for (int kb = 0; kb < Cfg::KB; ++kb) {
+#pragma unroll
+                for (int j = 0; j < G; ++j) {
+                    pwait(&kfull[s], ph, abort_flag, a.status);
+                    pwait(&tmempty[ts], tph ^ 1, abort_flag, a.status);
+                    tc_fence_after();
+                    unsigned char* At = smem + Cfg::OFF_RING + size_t(s) * Cfg::KSLOT + row * 128;
+                    const uint32_t ta = tbase + Cfg::T_RING + ts * 64 + (uint32_t(32 * q4) << 16);
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        float v[16];
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) {
+                            const float4 x = *reinterpret_cast<const float4*>(At + (((4 * hh + c) ^ (row & 7)) << 4));
+                            v[4 * c] = x.x; v[4 * c + 1] = x.y; v[4 * c + 2] = x.z; v[4 * c + 3] = x.w;
+                        }
+                        if (COMMIT && n > 0) {
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) v[e] *= gam[j];
+#pragma unroll
+                            for (int s2 = 0; s2 < TMAX; ++s2) {
+                                if (s2 < n) {
+                                    const float4* kr = reinterpret_cast<const float4*>(
+                                        kp + Cfg::KP_K + s2 * D + kb * 32 + hh * 16);
+#pragma unroll
+                                    for (int c = 0; c < 4; ++c) {
+                                        const float4 k4 = kr[c];
+                                        v[4 * c] = fmaf(coef[j][s2], k4.x, v[4 * c]);
+                                        v[4 * c + 1] = fmaf(coef[j][s2], k4.y, v[4 * c + 1]);
+                                        v[4 * c + 2] = fmaf(coef[j][s2], k4.z, v[4 * c + 2]);
+                                        v[4 * c + 3] = fmaf(coef[j][s2], k4.w, v[4 * c + 3]);
+                                    }
+                                }
+                            }
+#pragma unroll
+                            for (int c = 0; c < 4; ++c)
+                                *reinterpret_cast<float4*>(At + (((4 * hh + c) ^ (row & 7)) << 4)) =
+                                    make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+                        }
+                        uint32_t hi[16], lo[16];
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const float h = tf32_trunc(v[e]);
+                            hi[e] = __float_as_uint(h);
+                            lo[e] = __float_as_uint(v[e] - h);
+                        }
+                        tmem_st16(ta + hh * 16, hi);
+                        tmem_st16(ta + 32 + hh * 16, lo);
+                    }
+                    if (COMMIT) {
+                        if (n > 0) fence_async_smem();   // the store warp's TMA reads the update
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&kconv[s]);
+                    } else {
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&kempty[s]);
+                    }
+                    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&tmfull[ts]);
+                    if (++s == NKS) { s = 0; ph ^= 1; }
+                    if (++ts == NTS) { ts = 0; tph ^= 1; }
+                }
+            }
+            if (COMMIT) {
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&kpempty[iu & 1]);
+            }
         }
-    } else {
+    } else if (COMMIT && warp == 15) {
+        // ------------------------------------------------------------------ store (whole warp)
+        // committed K-blocks back to the state by TMA store (lane 0: its bulk groups), then free
+        int s = 0;
+        uint32_t ph = 0;
+        bool ok = true;
+        for (int iu = 0; iu < n_my && ok; ++iu) {
+            int l, b, kh;
+            unit_of(iu, l, b, kh);
+            const size_t lb = size_t(l) * B + b;
+            const int n = n_prev(b);
+            for (int kb = 0; kb < Cfg::KB && ok; ++kb) {
+                for (int j = 0; j < G; ++j) {
+                    if (!pwait_warp(&kconv[s], ph, abort_flag, a.status)) { ok = false; break; }
+                    if (n > 0 && lane == 0) {
+                        tma_store_2d(&smap, smem + Cfg::OFF_RING + size_t(s) * Cfg::KSLOT, kb * 32,
+                                     int((lb * Hv + kh * G + j) * D));
+                        bulk_commit();
+                        bulk_wait_read_all();
+                    }
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&kempty[s]);
+                    if (++s == NKS) { s = 0; ph ^= 1; }
+                }
+            }
+        }
+        if (lane == 0) bulk_wait_all();
+        __syncwarp();
+    } else if (warp >= 10 && warp < 14) {
         // ------------------------------------------------------------------ epilogue (128 threads)
         const int q4 = warp & 3, i = 32 * q4 + lane;
         IO* out = static_cast<IO*>(a.out);
@@ -642,10 +884,10 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
                      ::"r"(tbase), "r"(uint32_t(Cfg::TMEM_COLS)));
 }
 
-template <typename IO, int TMAX, int G>
+template <typename IO, int TMAX, int G, bool COMMIT>
 cudaError_t launch_verify_pipe_t(const VerifyArgs& a, const VerifyMaps& m, cudaStream_t stream) {
-    using Cfg = PipeCfg<IO, TMAX, G>;
-    auto kern = gdn_verify_pipe_kernel<IO, TMAX, G>;
+    using Cfg = PipeCfg<IO, TMAX, G, COMMIT>;
+    auto kern = gdn_verify_pipe_kernel<IO, TMAX, G, COMMIT>;
     static bool attr_done = false;   // benign race: setting the attribute twice is harmless
     static int nsm = 0;
     if (!attr_done) {
@@ -661,7 +903,8 @@ cudaError_t launch_verify_pipe_t(const VerifyArgs& a, const VerifyMaps& m, cudaS
     }
     const int n_units = a.L * a.B * a.Hk;
     const int grid = n_units < nsm ? n_units : nsm;
-    kern<<<grid, Cfg::NTHR, Cfg::SMEM, stream>>>(a, m.state, m.qkv, m.conv_state, n_units);
+    kern<<<grid, Cfg::NTHR, Cfg::SMEM, stream>>>(a, m.state, m.qkv, m.conv_state,
+                                                  COMMIT ? m.qkv_prev : m.qkv, n_units);
     return cudaGetLastError();
 }
 
@@ -672,11 +915,14 @@ bool verify_pipe_eligible(const VerifyArgs& a, const VerifyMaps& m, int D, bool 
            (a.Hv == a.Hk || a.Hv == 2 * a.Hk);
 }
 
-template <typename IO>
+template <typename IO, bool COMMIT>
 cudaError_t launch_verify_pipe(const VerifyArgs& a, const VerifyMaps& m, cudaStream_t s) {
     const int G = a.Hv / a.Hk;
-    if (a.T <= 4) return G == 1 ? launch_verify_pipe_t<IO, 4, 1>(a, m, s) : launch_verify_pipe_t<IO, 4, 2>(a, m, s);
-    return G == 1 ? launch_verify_pipe_t<IO, 8, 1>(a, m, s) : launch_verify_pipe_t<IO, 8, 2>(a, m, s);
+    if (a.T <= 4)
+        return G == 1 ? launch_verify_pipe_t<IO, 4, 1, COMMIT>(a, m, s)
+                      : launch_verify_pipe_t<IO, 4, 2, COMMIT>(a, m, s);
+    return G == 1 ? launch_verify_pipe_t<IO, 8, 1, COMMIT>(a, m, s)
+                  : launch_verify_pipe_t<IO, 8, 2, COMMIT>(a, m, s);
 }
 
 }  // namespace gdn

@@ -77,7 +77,10 @@ def custom(base: Workload, **kw) -> Workload:
 
 
 _TAGS = {"conv_w": 1, "state": 2, "conv_state": 3, "qkv": 4, "g": 5, "beta": 6, "logits": 7,
-         "drafts": 8, "lengths": 9, "tree": 10, "tokens": 11}
+         "drafts": 8, "lengths": 9, "tree": 10, "tokens": 11, "prev_delta": 12, "prev_k": 13}
+
+# round index of the synthetic previous round (no round loop reaches it)
+PREV_ROUND = 0x7FFFFFFF
 
 
 def generator(seed, wid, round_, tag, device="cpu"):
@@ -126,6 +129,22 @@ def round_stream(w: Workload, round_, seed=0, device="cpu"):
                      device=device)
     beta = torch.sigmoid(bb)
     return qkv, g.float().contiguous(), beta.float().contiguous()
+
+
+def previous_round(w: Workload, seed=0, device="cpu"):
+    """A synthetic previous round, the input of gdn_rollback_verify's commit half:
+    (n_acc [B] int32, tape_delta [L, B, T, Hv, Dv] fp32, tape_k [L, B, T, Hk, Dk] fp32,
+    g [L, B, T, Hv] fp32, qkv [L, B, T, C] io). Counts follow the workload's acceptance model;
+    δ ~ N(0, 0.5); k ~ N(0, 1/D) per element (about unit length); g and qkv as a round_stream
+    round."""
+    wid = _wid(w)
+    qkv, g, _ = round_stream(w, PREV_ROUND, seed, device)
+    n = accept_lengths(w, PREV_ROUND, seed, device).to(torch.int32)
+    dl = torch.randn((w.L, w.B, w.N, w.Hv, w.D),
+                     generator=generator(seed, wid, PREV_ROUND, "prev_delta", device), device=device)
+    k = torch.randn((w.L, w.B, w.N, w.Hk, w.D),
+                    generator=generator(seed, wid, PREV_ROUND, "prev_k", device), device=device)
+    return n, (dl * 0.5).contiguous(), (k * (1.0 / w.D ** 0.5)).contiguous(), g, qkv
 
 
 def accept_lengths(w: Workload, round_, seed=0, device="cpu"):

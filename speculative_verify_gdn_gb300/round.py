@@ -8,6 +8,13 @@ from . import _lib
 from .inputs import Workload
 
 
+def fused_in_one_kernel(w: Workload):
+    """Whether gdn_rollback_verify runs as one kernel for this workload (else as two calls)."""
+    import torch as _t
+    return (w.io_dtype == _t.bfloat16 and w.D == 128 and w.N <= 8 and w.accept != "tree"
+            and w.Hv in (w.Hk, 2 * w.Hk))
+
+
 class SpecRound:
     """Owns the per-round outputs (o, tape, accept results, workspace, status) of a workload.
 
@@ -64,9 +71,55 @@ class SpecRound:
         self.accept(logits, drafts, round_=round_, seed=seed, parent=parent, stream=stream)
         self.rollback(qkv, g, state, conv_state, stream=stream)
 
-    def launches_per_step(self):
-        """Kernel launches one step() enqueues (verify 1, accept 2 or 3, rollback 1)."""
-        return 1 + (3 if self.mode == _lib.SPEC_MODE_SAMPLE and self.w.accept != "tree" else 2) + 1
+    # ---------------------------------------------------------------- fused round loop
+    def rollback_verify(self, qkv, conv_w, conv_state, g, beta, state, stream=None):
+        """gdn_rollback_verify: commit the previous fused round (its accept result, tape, qkv, g)
+        and verify this one. The caller keeps qkv and g alive and unchanged until the next call
+        (they are the next commit's tape)."""
+        if self.w.accept == "tree":
+            raise ValueError("the fused round loop serves chains; trees use step()")
+        if not hasattr(self, "_prev"):
+            self._alloc_fused()
+        prev, cur = self._prev, self._cur
+        first = prev["qkv"] is None          # nothing to commit: n_acc_prev is zero
+        _lib.rollback_verify(self.shape, prev["n_acc"], prev["tape_delta"], prev["tape_k"],
+                             g if first else prev["g"], qkv if first else prev["qkv"], qkv,
+                             conv_w, conv_state, g, beta, state, self.out, cur["tape_delta"],
+                             cur["tape_k"], status=self.status, stream=stream)
+        self.tape_delta, self.tape_k, self.n_acc = cur["tape_delta"], cur["tape_k"], cur["n_acc"]
+        cur["g"], cur["qkv"] = g, qkv
+        self._prev, self._cur = cur, prev
+
+    def step_fused(self, qkv, g, beta, logits, drafts, conv_w, state, conv_state, round_=0,
+                   seed=0, stream=None):
+        """rollback_verify -> accept. The state lags one round behind: flush() after the last."""
+        self.rollback_verify(qkv, conv_w, conv_state, g, beta, state, stream=stream)
+        self.accept(logits, drafts, round_=round_, seed=seed, stream=stream)
+
+    def flush(self, state, conv_state, stream=None):
+        """Commit the last step_fused round (gdn_rollback with its accept result)."""
+        if not hasattr(self, "_prev") or self._prev["qkv"] is None:
+            return
+        p = self._prev
+        _lib.rollback(self.shape, p["n_acc"], p["tape_delta"], p["tape_k"], p["g"], p["qkv"],
+                      state, conv_state, status=self.status, stream=stream)
+        p["n_acc"].zero_()
+        p["qkv"] = p["g"] = None
+
+    def _alloc_fused(self):
+        sh, dev = self.shape, self.device
+        def buf():
+            return {"tape_delta": torch.empty(sh.out_shape(), dtype=torch.float32, device=dev),
+                    "tape_k": torch.empty(sh.tape_k_shape(), dtype=torch.float32, device=dev),
+                    "n_acc": torch.zeros(self.w.B, dtype=torch.int32, device=dev),
+                    "g": None, "qkv": None}
+        self._prev, self._cur = buf(), buf()
+
+    def launches_per_step(self, fused=False):
+        """Kernel launches one step() (verify 1, accept 2 or 3, rollback 1) or one step_fused()
+        (rollback_verify 1, accept 2 or 3) enqueues, for shapes the fused kernel serves."""
+        acc = 3 if self.mode == _lib.SPEC_MODE_SAMPLE and self.w.accept != "tree" else 2
+        return (1 if fused and fused_in_one_kernel(self.w) else 2) + acc
 
     def check_status(self):
         torch.cuda.synchronize(self.device)

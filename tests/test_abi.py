@@ -103,3 +103,23 @@ def test_host_validation_rejects_bad_arguments_without_a_gpu(lib):
     assert "workspace" in _lib.last_error()
     assert lib.spec_accept(ct.byref(sd), fake, fake, 7, 0.0, 0, 0, fake, 1 << 20, fake, fake,
                            None, None) == 1
+
+
+def test_rollback_verify_host_checks(lib):
+    d = qwen_shape().c()
+    # distinct, non-overlapping, never dereferenced (validation fails before any CUDA call)
+    args = [ct.c_void_p((i + 1) << 32) for i in range(15)]   # n_acc_prev .. tape_k
+    assert lib.gdn_rollback_verify(ct.byref(d), *([None] * 15), None, None) == 1
+    assert "NULL" in _lib.last_error()
+    # this round's tape on top of the previous round's tape
+    same = list(args)
+    same[1] = ct.c_void_p(0x200000)     # tape_delta_prev
+    same[13] = ct.c_void_p(0x200000)    # tape_delta
+    assert lib.gdn_rollback_verify(ct.byref(d), *same, None, None) == 1
+    assert "overlap" in _lib.last_error()
+    # misaligned previous tape (bulk copies need 16 bytes)
+    mis = list(args)
+    mis[2] = ct.c_void_p(0x300004)      # tape_k_prev
+    assert lib.gdn_rollback_verify(ct.byref(d), *mis, None, None) == 1
+    assert "aligned" in _lib.last_error()
+    assert lib.gdn_rollback_verify(ct.byref(qwen_shape(B=0).c()), *([None] * 15), None, None) == 0
