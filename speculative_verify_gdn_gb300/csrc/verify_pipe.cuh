@@ -31,15 +31,17 @@
 // the other roles run on without waiting (results are then garbage, never a hang).
 //
 // COMMIT (gdn_rollback_verify): the same pass first commits the previous round's accepted steps,
-// exactly as gdn_rollback does ("GDN investigation" §4, tape replay), then verifies the new round
-// from the committed state. Per unit with n = n_acc_prev[b] > 0 the input loader stages the
-// previous round's k_s and δ_s rows and the coefficients c_s = Γ(s+1 .. n-1), Γ = Γ(0 .. n-1); the
-// convert warps replace each state K-block in shared memory by
-//     S_n = Γ · S_0 + Σ_{s<n} (c_s δ_s) k_sᵀ
-// before splitting it, and a store warp (warp 15) writes it back by TMA store. The conv window is
-// the last W-1 rows of (old conv state ++ the previous round's accepted raw rows), staged from both
-// buffers, and the input loader writes those rows back as the new conv state. So each state tile is
-// read once and written once per round, instead of read by verify, read and written by rollback.
+// as gdn_rollback does ("GDN investigation" §4, tape replay), then verifies the new round from the
+// committed state. With n = n_acc_prev[b], c_s = Γ(s+1 .. n-1), Γ = Γ(0 .. n-1) and the rank-n
+// term A Kᵀ (A[i][s] = c_s δ_s[i], K[j][s] = k_s[j] of the previous round):
+//     S_n = Γ · S_0 + A Kᵀ,        S_n · X = Γ · (S_0 · X) + A · (Kᵀ X).
+// So the tensor-core products still run on the loaded S_0; the prep warps add Kᵀ X (n x 2T, beside
+// the Gram block) and the epilogue applies Γ and A · (Kᵀ X) to each P row. For the write-back the
+// convert warps form S_n = Γ S_0 + A Kᵀ of each K-block in shared memory with warp-level mma.sync
+// (3xTF32, K = 8) and a store warp (warp 15) writes it back by TMA store. The conv window is the last
+// W-1 rows of (old conv state ++ the previous round's accepted raw rows), staged from both buffers;
+// the prep warps write those rows back as the new conv state. So each state tile is read once and
+// written once per round, instead of read by verify, read and written by rollback.
 #pragma once
 
 #include "verify_impl.cuh"
@@ -70,19 +72,22 @@ struct PipeCfg {
     static constexpr int RAW_BYTES = NPARTS * NRMAX * D * ES + NPARTS * D * 4 * ES;
     static constexpr int STAGE_BYTES = (RAW_BYTES + 127) / 128 * 128;
     // meta slot (floats): per value head j and position t a record {c0, γ, β, k_t·q_t, CK[TMAX],
-    // CQ[TMAX]} (16-byte aligned), then the conv outputs V[G][TMAX][D]
+    // CQ[TMAX]} (16-byte aligned), the conv outputs V[G][TMAX][D] and (COMMIT) GP[s][c] = k'_s·X_c
+    // of the previous round's k'_s
     static constexpr int RS = 4 + 2 * TMAX;
-    static constexpr int M_REC = 0, M_V = G * TMAX * RS, M_FLOATS = M_V + G * TMAX * D;
+    static constexpr int M_REC = 0, M_V = G * TMAX * RS, M_GP = M_V + G * TMAX * D,
+                         M_FLOATS = M_GP + (COMMIT ? 2 * TMAX * TMAX : 0);
     static constexpr int META_BYTES = (M_FLOATS * 4 + 127) / 128 * 128;
     // commit slot (floats): previous round's k_s rows [TMAX][D], δ_s rows [G][TMAX][D],
     // c_s = Γ(s+1 .. n-1) [G][TMAX], Γ(0 .. n-1) [G]
-    static constexpr int KP_K = 0, KP_DL = TMAX * D, KP_C = KP_DL + G * TMAX * D,
+    static constexpr int KP_KS = D + 4;                      // padded k rows: conflict-free fragments
+    static constexpr int KP_K = 0, KP_DL = TMAX * KP_KS, KP_C = KP_DL + G * TMAX * D,
                          KP_GAM = KP_C + G * TMAX, KP_FLOATS = KP_GAM + 4;
     static constexpr int KP_BYTES = COMMIT ? (KP_FLOATS * 4 + 127) / 128 * 128 : 0;
     // prep scratch (floats): norm partials [4][2TMAX], inverse norms [2TMAX], Gram partials
     // [4 warps][16][8], Gram [TMAX][2TMAX]
     static constexpr int S_NRM = 0, S_INV = S_NRM + 8 * TMAX, S_GP = S_INV + 2 * TMAX,
-                         S_GRAM = S_GP + 4 * 128, S_FLOATS = S_GRAM + 2 * TMAX * TMAX;
+                         S_GRAM = S_GP + (COMMIT ? 8 : 4) * 128, S_FLOATS = S_GRAM + 2 * TMAX * TMAX;
 
     static constexpr size_t OFF_RING = 0;
     static constexpr size_t OFF_X = OFF_RING + size_t(NKS) * KSLOT;
@@ -100,7 +105,9 @@ struct PipeCfg {
     static_assert(G * S == 2, "two accumulator chains per unit");
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
     static_assert(OFF_X % 1024 == 0 && X_BYTES % 1024 == 0, "swizzle atoms need 1024-byte bases");
-    static_assert((RS * 4) % 16 == 0 && (M_V * 4) % 16 == 0, "records are read as float4");
+    static_assert((RS * 4) % 16 == 0 && (M_V * 4) % 16 == 0 && (M_GP * 4) % 16 == 0,
+                  "records are read as float4");
+    static_assert((KP_DL * 4) % 16 == 0 && (KP_KS * 4) % 16 == 0, "bulk-copy destinations");
     static_assert(2 * TMAX <= 16 && TMAX <= 8, "Gram block is one m16n8 tile");
     static_assert(G * TMAX * TMAX <= 128, "one prep thread per coefficient");
 };
@@ -245,7 +252,7 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
     uint64_t* ufull = sempty + 2;                // unit prologue (X tile, meta) ready
     uint64_t* uempty = ufull + 2;                // unit slot free: last MMA commit + 4 epilogue warps
     uint64_t* kpfull = uempty + 2;               // COMMIT: previous round's tape rows staged
-    uint64_t* kpempty = kpfull + 2;              // COMMIT: commit slot read by the 4 convert warps
+    uint64_t* kpempty = kpfull + 2;              // COMMIT: commit slot read by prep, convert, epilogue
     uint64_t* mdone = kpempty + 2;               // every MMA of this CTA complete
     uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + Cfg::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::OFF_MISC + 4);
@@ -261,8 +268,9 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
             uint64_t* bb = &bars[i];
             const bool four = (!COMMIT && bb >= kempty && bb < kempty + NKS) ||
                               (bb >= kconv && bb < kconv + NKS) || (bb >= tmfull && bb < tmfull + NTS) ||
-                              (bb >= tempty && bb < tempty + 2) || (bb >= kpempty && bb < kpempty + 2);
-            mbar_init(bb, four ? 4 : (bb >= uempty && bb < uempty + 2) ? 5 : 1);
+                              (bb >= tempty && bb < tempty + 2);
+            const bool kpe = bb >= kpempty && bb < kpempty + 2;
+            mbar_init(bb, four ? 4 : kpe ? 9 : (bb >= uempty && bb < uempty + 2) ? 5 : 1);
         }
         *abort_flag = 0;
         fence_mbar_init();
@@ -290,32 +298,6 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
         if (!COMMIT) return 0;
         const int n = __ldg(a.n_acc_prev + b);
         return (n < 0 || n > T) ? 0 : n;
-    };
-    // COMMIT, input-loader warp: once unit iu's staging has landed, write the last W-1 rows of
-    // (old conv state ++ previous accepted rows) — staged row r + n or W-1+T+r — back as the new
-    // conv state of its channels (lane 0 issues; bulk group of lane 0)
-    auto store_conv_rows = [&](int iu, int n) {
-        if (!COMMIT || n == 0 || W == 1) return;
-        int l, b, kh;
-        unit_of(iu, l, b, kh);
-        const size_t lb = size_t(l) * B + b;
-        volatile int no_abort = 0;
-        pwait_warp(&sfull[iu & 1], uint32_t(iu >> 1) & 1u, &no_abort, a.status);
-        if (lane == 0) {
-            const IO* qs = reinterpret_cast<const IO*>(smem + Cfg::OFF_STAGE + size_t(iu & 1) * Cfg::STAGE_BYTES);
-            IO* cso = static_cast<IO*>(a.conv_state_out);
-            for (int part = 0; part < Cfg::NPARTS; ++part) {
-                const int cb = part == 0 ? kh * D
-                             : part == 1 ? Hk * D + kh * D : 2 * Hk * D + (kh * G + part - 2) * D;
-                for (int r = 0; r < W - 1; ++r) {
-                    const int src = r + n < W - 1 ? r + n : W - 1 + T + r;
-                    bulk_s2g(cso + (lb * (W - 1) + r) * size_t(C) + cb, qs + (size_t(part) * NR + src) * D,
-                             uint32_t(D * Cfg::ES));
-                }
-            }
-            bulk_commit();
-        }
-        __syncwarp();
     };
 
     if (warp == 0) {
@@ -353,10 +335,9 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
         // ------------------------------------------------------------------ input loader (whole warp)
         // staged layout per part: W-1 old conv-state rows, T qkv rows, (COMMIT) W-1 rows of the
         // previous round's qkv ending at row n-1; then the conv taps of every part [NPARTS][D][W].
-        // All destinations are multiples of 128 bytes. Lane 0 issues every copy (the bulk stores
-        // below are tracked per thread).
+        // All destinations are multiples of 128 bytes.
         const IO* cw = static_cast<const IO*>(a.conv_w);
-        int issued = 0, n_last = 0;
+        int issued = 0;
         for (int iu = 0; iu < n_my; ++iu) {
             int l, b, kh;
             unit_of(iu, l, b, kh);
@@ -365,13 +346,14 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
             IO* qs = reinterpret_cast<IO*>(smem + Cfg::OFF_STAGE + size_t(ss) * Cfg::STAGE_BYTES);
             IO* cws = qs + size_t(Cfg::NPARTS) * NR * D;
             int n = 0;
+            float gv = 1.f;                          // COMMIT: gate g'_s of lane (j, s)
             if (COMMIT) {
                 const int nr = __ldg(a.n_acc_prev + b);
                 if ((nr < 0 || nr > T) && lane == 0 && kh == 0 && l == 0)
                     set_status(a.status, GDN_STATUS_BAD_NACC);
                 n = n_prev(b);
-                // the conv-row stores of two units ago read this staging slot
-                if (lane == 0) bulk_wait_read_all();
+                const int gj = lane / TMAX, gs = lane - gj * TMAX;
+                if (gj < G && gs < n) gv = __ldg(a.g_prev + (lb * T + gs) * Hv + kh * G + gj);
             }
             if (!pwait_warp(&sempty[ss], ((iu >> 1) & 1) ^ 1, abort_flag, a.status)) break;
             if (lane == 0) {
@@ -396,9 +378,6 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
                 // previous round's tape rows and gate coefficients of this unit
                 const int ks = iu & 1;
                 float* kp = reinterpret_cast<float*>(smem + Cfg::OFF_KP + size_t(ks) * Cfg::KP_BYTES);
-                const int gj = lane / TMAX, gs = lane - gj * TMAX;
-                float gv = 1.f;
-                if (gj < G && gs < n) gv = __ldg(a.g_prev + (lb * T + gs) * Hv + kh * G + gj);
                 if (!pwait_warp(&kpempty[ks], ((iu >> 1) & 1) ^ 1, abort_flag, a.status)) break;
 #pragma unroll
                 for (int j = 0; j < G; ++j) {
@@ -417,8 +396,9 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
                 if (lane == 0) {
                     mbar_arrive_expect_tx(&kpfull[ks], uint32_t(n * (1 + G) * D * 4));
                     for (int s2 = 0; s2 < n; ++s2) {
-                        bulk_g2s(kp + Cfg::KP_K + s2 * D, a.tape_k_prev + ((lb * T + s2) * Hk + kh) * size_t(D),
-                                 uint32_t(D * 4), &kpfull[ks]);
+                        bulk_g2s(kp + Cfg::KP_K + s2 * Cfg::KP_KS,
+                                 a.tape_k_prev + ((lb * T + s2) * Hk + kh) * size_t(D), uint32_t(D * 4),
+                                 &kpfull[ks]);
 #pragma unroll
                         for (int j = 0; j < G; ++j)
                             bulk_g2s(kp + Cfg::KP_DL + (j * TMAX + s2) * D,
@@ -427,19 +407,14 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
                     }
                 }
                 __syncwarp();
-                // the previous unit's new conv state: its staged window rows, written back
-                if (iu > 0) store_conv_rows(iu - 1, n_last);
-                n_last = n;
             }
             ++issued;
         }
-        if (COMMIT && issued > 0) store_conv_rows(issued - 1, n_last);
         volatile int no_abort = 0;
         for (int k = 1; k <= 2 && k <= issued; ++k) {
             const int q = issued - k;
             pwait_warp(&sfull[q & 1], uint32_t(q >> 1) & 1u, &no_abort, a.status);
         }
-        if (COMMIT && lane == 0) bulk_wait_all();
     } else if (warp == 1) {
         // ------------------------------------------------------------------ mma (whole warp)
         // chain c of a unit slot: hi pass (N = 2NP) at c * CH_COLS, lo pass (N = NP) at + 32. Per
@@ -527,9 +502,10 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
             const int n = n_prev(b);
             pwait(&sfull[ss], (iu >> 1) & 1, abort_flag, a.status);
             pwait(&uempty[us], ((iu >> 1) & 1) ^ 1, abort_flag, a.status);
-            // conv + SiLU of channel p of every part
-            float y[Cfg::NPARTS][TMAX];
-#pragma unroll
+            // conv + SiLU of channel p of every part (one loop body for all parts keeps the code
+            // small: q and k stay in registers, each v goes to the meta slot)
+            float yq[TMAX], yk[TMAX];
+#pragma unroll 1
             for (int part = 0; part < Cfg::NPARTS; ++part) {
                 const IO* col = qs + size_t(part) * NR * D + p;
                 const IO* wp = cws + (size_t(part) * D + p) * W;
@@ -552,13 +528,35 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
                 }
 #pragma unroll
                 for (int t = 0; t < TMAX; ++t) E[3 + t] = (t < T) ? io_to_f(col[size_t(W - 1 + t) * D]) : 0.f;
+                if (COMMIT && n > 0) {
+                    // the committed window is the new conv state: row r is E[r + 4 - W] (exact copies)
+                    const int cb = part == 0 ? kh * D
+                                 : part == 1 ? Hk * D + kh * D : 2 * Hk * D + (kh * G + part - 2) * D;
+                    IO* cso = static_cast<IO*>(a.conv_state_out) + lb * size_t(W - 1) * C + cb + p;
+#pragma unroll
+                    for (int k = 0; k < 3; ++k) {
+                        const int r = k + W - 4;
+                        if (r >= 0) IoTraits<IO>::store(cso, size_t(r) * C, E[k]);
+                    }
+                }
+                float yv[TMAX];
 #pragma unroll
                 for (int t = 0; t < TMAX; ++t) {
                     float acc = wr[3] * E[t];
                     acc = fmaf(wr[2], E[t + 1], acc);
                     acc = fmaf(wr[1], E[t + 2], acc);
                     acc = fmaf(wr[0], E[t + 3], acc);
-                    y[part][t] = (t < T) ? silu_fast(acc) : 0.f;
+                    yv[t] = (t < T) ? silu_fast(acc) : 0.f;
+                }
+                if (part == 0) {
+#pragma unroll
+                    for (int t = 0; t < TMAX; ++t) yq[t] = yv[t];
+                } else if (part == 1) {
+#pragma unroll
+                    for (int t = 0; t < TMAX; ++t) yk[t] = yv[t];
+                } else {
+#pragma unroll
+                    for (int t = 0; t < TMAX; ++t) meta[Cfg::M_V + ((part - 2) * TMAX + t) * D + p] = yv[t];
                 }
             }
             // norms of k_t (columns 0..TMAX-1) and q_t (columns TMAX..2TMAX-1)
@@ -566,8 +564,8 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
                 float sq[2 * TMAX];
 #pragma unroll
                 for (int t = 0; t < TMAX; ++t) {
-                    sq[t] = y[1][t] * y[1][t];
-                    sq[TMAX + t] = y[0][t] * y[0][t];
+                    sq[t] = yk[t] * yk[t];
+                    sq[TMAX + t] = yq[t] * yq[t];
                 }
                 int ix;
                 const float s = warp_sum_many<2 * TMAX>(sq, lane, &ix);
@@ -583,7 +581,7 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
             // rows NP + n: X_lo = X − X_hi. Also the tape k, v values, gates.
 #pragma unroll
             for (int t = 0; t < TMAX; ++t) {
-                const float kn = y[1][t] * inv[t], qn = y[0][t] * inv[TMAX + t];
+                const float kn = yk[t] * inv[t], qn = yq[t] * inv[TMAX + t];
                 *reinterpret_cast<float*>(Xb + sw128_off(t, p, XKB)) = kn;
                 *reinterpret_cast<float*>(Xb + sw128_off(NP + t, p, XKB)) = kn - tf32_trunc(kn);
                 *reinterpret_cast<float*>(Xb + sw128_off(TMAX + t, p, XKB)) = qn;
@@ -595,10 +593,6 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
                 *reinterpret_cast<float*>(Xb + sw128_off(n2, p, XKB)) = 0.f;
                 *reinterpret_cast<float*>(Xb + sw128_off(NP + n2, p, XKB)) = 0.f;
             }
-#pragma unroll
-            for (int j = 0; j < G; ++j)
-#pragma unroll
-                for (int t = 0; t < TMAX; ++t) meta[Cfg::M_V + (j * TMAX + t) * D + p] = y[2 + j][t];
             if (p < G * TMAX) {
                 float* rec = meta + Cfg::M_REC + p * RS;      // record (gj, gt)
                 rec[1] = g_in;
@@ -607,9 +601,12 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
             fence_async_smem();
             named_bar(1, 128);
             // Gram block on the warp tensor path: D[m][n] = X_m · k_n over this warp's 32 channels,
-            // 3xTF32 (hi·hi + hi·lo + lo·hi); rows m: k_0.., q_0.. (zero beyond 2 TMAX)
+            // 3xTF32 (hi·hi + hi·lo + lo·hi); rows m: k_0.., q_0.. (zero beyond 2 TMAX). COMMIT: also
+            // D'[m][s] = X_m · k'_s with the previous round's k'_s (zero for s ≥ n)
+            const float* kpp = reinterpret_cast<const float*>(smem + Cfg::OFF_KP + size_t(iu & 1) * Cfg::KP_BYTES);
+            if (COMMIT) pwait(&kpfull[iu & 1], (iu >> 1) & 1, abort_flag, a.status);
             {
-                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+                float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks) {
                     const int ch = 32 * pw + 8 * ks + gt4;
@@ -632,18 +629,39 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
                     mma_tf32_16x8x8(acc, ahi, __float_as_uint(bh0), __float_as_uint(bh1));
                     mma_tf32_16x8x8(acc, ahi, bl0, bl1);
                     mma_tf32_16x8x8(acc, alo, __float_as_uint(bh0), __float_as_uint(bh1));
+                    if (COMMIT && n > 0) {
+                        // B'[k][s] = k'_s[ch + k]: lane (gq, gt4) holds k'_gq at channels ch, ch + 4
+                        const float kv0 = gq < n ? kpp[Cfg::KP_K + gq * Cfg::KP_KS + ch] : 0.f;
+                        const float kv1 = gq < n ? kpp[Cfg::KP_K + gq * Cfg::KP_KS + ch + 4] : 0.f;
+                        const float kh0 = tf32_trunc(kv0), kh1 = tf32_trunc(kv1);
+                        const uint32_t kl0 = __float_as_uint(tf32_trunc(kv0 - kh0));
+                        const uint32_t kl1 = __float_as_uint(tf32_trunc(kv1 - kh1));
+                        mma_tf32_16x8x8(acc2, ahi, __float_as_uint(kh0), __float_as_uint(kh1));
+                        mma_tf32_16x8x8(acc2, ahi, kl0, kl1);
+                        mma_tf32_16x8x8(acc2, alo, __float_as_uint(kh0), __float_as_uint(kh1));
+                    }
                 }
                 float* g4 = gp + pw * 128;
                 g4[gq * 8 + 2 * gt4] = acc[0];
                 g4[gq * 8 + 2 * gt4 + 1] = acc[1];
                 g4[(gq + 8) * 8 + 2 * gt4] = acc[2];
                 g4[(gq + 8) * 8 + 2 * gt4 + 1] = acc[3];
+                if (COMMIT) {
+                    float* g5 = gp + 512 + pw * 128;
+                    g5[gq * 8 + 2 * gt4] = acc2[0];
+                    g5[gq * 8 + 2 * gt4 + 1] = acc2[1];
+                    g5[(gq + 8) * 8 + 2 * gt4] = acc2[2];
+                    g5[(gq + 8) * 8 + 2 * gt4 + 1] = acc2[3];
+                }
             }
             named_bar(1, 128);
             {
-                const int m = p >> 3, n = p & 7;
-                if (m < 2 * TMAX && n < TMAX)
-                    gram[n * 2 * TMAX + m] = gp[p] + gp[128 + p] + gp[256 + p] + gp[384 + p];
+                const int m = p >> 3, nn = p & 7;
+                if (m < 2 * TMAX && nn < TMAX) {
+                    gram[nn * 2 * TMAX + m] = gp[p] + gp[128 + p] + gp[256 + p] + gp[384 + p];
+                    if (COMMIT)    // GP[s][c] = k'_s · X_c
+                        meta[Cfg::M_GP + nn * 2 * TMAX + m] = gp[512 + p] + gp[640 + p] + gp[768 + p] + gp[896 + p];
+                }
             }
             named_bar(1, 128);
             // per value head, one thread per (v, x ≤ v): CK[v][x] = Γ(x→v-1) k_x·k_v and
@@ -668,13 +686,19 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
                 }
             }
             named_bar(1, 128);
-            if (p == 0) mbar_arrive(&ufull[us]);
+            if (p == 0) {
+                mbar_arrive(&ufull[us]);
+                if (COMMIT) mbar_arrive(&kpempty[iu & 1]);
+            }
         }
     } else if (warp < 10) {
         // ------------------------------------------------------------------ convert (128 threads)
-        // thread = state row; per K-block (COMMIT: first S ← Γ S + Σ_s (c_s δ_s[row]) k_s, written
-        // back in place) S_hi and S_lo of its 32 columns into the TMEM ring, in two halves of 16
+        // thread = state row: S_hi and S_lo of its 32 columns of each K-block into the TMEM ring (two
+        // halves of 16). COMMIT, n > 0: then S_n = Γ S_0 + A K'ᵀ for the warp's 32 rows of the K-block
+        // with mma.sync (rows r0 + gq and r0 + gq + 8, columns c0 + 2 gt4 and + 1 of each 16 x 8 tile),
+        // written back in place for the store warp.
         const int q4 = warp & 3, row = 32 * q4 + lane;
+        const int gq = lane >> 2, gt4 = lane & 3;
         int s = 0, ts = 0;
         uint32_t ph = 0, tph = 0;
         for (int iu = 0; iu < n_my; ++iu) {
@@ -682,81 +706,34 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
             unit_of(iu, l, b, kh);
             const int n = n_prev(b);
             const float* kp = reinterpret_cast<const float*>(smem + Cfg::OFF_KP + size_t(iu & 1) * Cfg::KP_BYTES);
-            float coef[G][TMAX], gam[G];
-#pragma unroll
-            for (int j = 0; j < G; ++j) {
-                gam[j] = 1.f;
-#pragma unroll
-                for (int s2 = 0; s2 < TMAX; ++s2) coef[j][s2] = 0.f;
-            }
-            if (COMMIT) {
-                pwait(&kpfull[iu & 1], (iu >> 1) & 1, abort_flag, a.status);
-                if (n > 0) {
-#pragma unroll
-                    for (int j = 0; j < G; ++j) {
-                        gam[j] = kp[Cfg::KP_GAM + j];
-#pragma unroll
-                        for (int s2 = 0; s2 < TMAX; ++s2)
-                            if (s2 < n)
-                                coef[j][s2] = kp[Cfg::KP_C + j * TMAX + s2] *
-                                              kp[Cfg::KP_DL + (j * TMAX + s2) * D + row];
-                    }
-                }
-            }
+            if (COMMIT) pwait(&kpfull[iu & 1], (iu >> 1) & 1, abort_flag, a.status);
             for (int kb = 0; kb < Cfg::KB; ++kb) {
-#pragma unroll
+#pragma unroll 1
                 for (int j = 0; j < G; ++j) {
                     pwait(&kfull[s], ph, abort_flag, a.status);
                     pwait(&tmempty[ts], tph ^ 1, abort_flag, a.status);
                     tc_fence_after();
-                    unsigned char* At = smem + Cfg::OFF_RING + size_t(s) * Cfg::KSLOT + row * 128;
+                    unsigned char* Ab = smem + Cfg::OFF_RING + size_t(s) * Cfg::KSLOT;
+                    const unsigned char* At = Ab + row * 128;
                     const uint32_t ta = tbase + Cfg::T_RING + ts * 64 + (uint32_t(32 * q4) << 16);
 #pragma unroll
                     for (int hh = 0; hh < 2; ++hh) {
-                        float v[16];
+                        uint32_t hi[16], lo[16];
 #pragma unroll
                         for (int c = 0; c < 4; ++c) {
                             const float4 x = *reinterpret_cast<const float4*>(At + (((4 * hh + c) ^ (row & 7)) << 4));
-                            v[4 * c] = x.x; v[4 * c + 1] = x.y; v[4 * c + 2] = x.z; v[4 * c + 3] = x.w;
-                        }
-                        if (COMMIT && n > 0) {
+                            const float v4[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
-                            for (int e = 0; e < 16; ++e) v[e] *= gam[j];
-#pragma unroll
-                            for (int s2 = 0; s2 < TMAX; ++s2) {
-                                if (s2 < n) {
-                                    const float4* kr = reinterpret_cast<const float4*>(
-                                        kp + Cfg::KP_K + s2 * D + kb * 32 + hh * 16);
-#pragma unroll
-                                    for (int c = 0; c < 4; ++c) {
-                                        const float4 k4 = kr[c];
-                                        v[4 * c] = fmaf(coef[j][s2], k4.x, v[4 * c]);
-                                        v[4 * c + 1] = fmaf(coef[j][s2], k4.y, v[4 * c + 1]);
-                                        v[4 * c + 2] = fmaf(coef[j][s2], k4.z, v[4 * c + 2]);
-                                        v[4 * c + 3] = fmaf(coef[j][s2], k4.w, v[4 * c + 3]);
-                                    }
-                                }
+                            for (int e = 0; e < 4; ++e) {
+                                const float h = tf32_trunc(v4[e]);
+                                hi[4 * c + e] = __float_as_uint(h);
+                                lo[4 * c + e] = __float_as_uint(v4[e] - h);
                             }
-#pragma unroll
-                            for (int c = 0; c < 4; ++c)
-                                *reinterpret_cast<float4*>(At + (((4 * hh + c) ^ (row & 7)) << 4)) =
-                                    make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
-                        }
-                        uint32_t hi[16], lo[16];
-#pragma unroll
-                        for (int e = 0; e < 16; ++e) {
-                            const float h = tf32_trunc(v[e]);
-                            hi[e] = __float_as_uint(h);
-                            lo[e] = __float_as_uint(v[e] - h);
                         }
                         tmem_st16(ta + hh * 16, hi);
                         tmem_st16(ta + 32 + hh * 16, lo);
                     }
-                    if (COMMIT) {
-                        if (n > 0) fence_async_smem();   // the store warp's TMA reads the update
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&kconv[s]);
-                    } else {
+                    if (!COMMIT) {
                         __syncwarp();
                         if (lane == 0) mbar_arrive(&kempty[s]);
                     }
@@ -764,6 +741,60 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&tmfull[ts]);
+                    if (COMMIT) {
+                        if (n > 0) {
+                            // A fragments (m16n8k8: a0 (r, s), a1 (r + 8, s), a2 (r, s + 4),
+                            // a3 (r + 8, s + 4), r = r0 + gq, s = gt4) of A[i][s] = c_s δ_s[i],
+                            // zero for s ≥ n; two 16-row tiles
+                            uint32_t afh[2][4], afl[2][4];
+                            const float gm = kp[Cfg::KP_GAM + j];
+#pragma unroll
+                            for (int rt = 0; rt < 2; ++rt)
+#pragma unroll
+                                for (int e = 0; e < 4; ++e) {
+                                    const int r = 32 * q4 + 16 * rt + gq + ((e & 1) ? 8 : 0);
+                                    const int s2 = gt4 + ((e & 2) ? 4 : 0);
+                                    const float av = s2 < n ? kp[Cfg::KP_C + j * TMAX + s2] *
+                                                                  kp[Cfg::KP_DL + (j * TMAX + s2) * D + r]
+                                                            : 0.f;
+                                    const float h = tf32_trunc(av);
+                                    afh[rt][e] = __float_as_uint(h);
+                                    afl[rt][e] = __float_as_uint(tf32_trunc(av - h));
+                                }
+#pragma unroll
+                            for (int ct = 0; ct < 4; ++ct) {
+                                // B'[k][col] = k'_k[kb * 32 + 8 ct + col]: b0 (k = gt4), b1 (k = gt4 + 4)
+                                const int cc = kb * 32 + 8 * ct + gq;
+                                const float kv0 = gt4 < n ? kp[Cfg::KP_K + gt4 * Cfg::KP_KS + cc] : 0.f;
+                                const float kv1 = gt4 + 4 < n ? kp[Cfg::KP_K + (gt4 + 4) * Cfg::KP_KS + cc] : 0.f;
+                                const float kb0 = tf32_trunc(kv0), kb1 = tf32_trunc(kv1);
+                                const uint32_t bh0 = __float_as_uint(kb0), bh1 = __float_as_uint(kb1);
+                                const uint32_t bl0 = __float_as_uint(tf32_trunc(kv0 - kb0));
+                                const uint32_t bl1 = __float_as_uint(tf32_trunc(kv1 - kb1));
+#pragma unroll
+                                for (int rt = 0; rt < 2; ++rt) {
+                                    float u[4] = {0.f, 0.f, 0.f, 0.f};
+                                    mma_tf32_16x8x8(u, afh[rt], bh0, bh1);
+                                    mma_tf32_16x8x8(u, afh[rt], bl0, bl1);
+                                    mma_tf32_16x8x8(u, afl[rt], bh0, bh1);
+                                    // u: (r, c), (r, c + 1), (r + 8, c), (r + 8, c + 1), c = 8 ct + 2 gt4
+#pragma unroll
+                                    for (int hr = 0; hr < 2; ++hr) {
+                                        const int r = 32 * q4 + 16 * rt + gq + 8 * hr;
+                                        const int c = 8 * ct + 2 * gt4;
+                                        float2* pp = reinterpret_cast<float2*>(
+                                            Ab + r * 128 + ((((c >> 2) ^ (r & 7))) << 4) + (c & 3) * 4);
+                                        const float2 old = *pp;
+                                        *pp = make_float2(fmaf(gm, old.x, u[2 * hr]),
+                                                          fmaf(gm, old.y, u[2 * hr + 1]));
+                                    }
+                                }
+                            }
+                            fence_async_smem();   // the store warp's TMA reads the update
+                        }
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&kconv[s]);
+                    }
                     if (++s == NKS) { s = 0; ph ^= 1; }
                     if (++ts == NTS) { ts = 0; tph ^= 1; }
                 }
@@ -813,11 +844,14 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
             const size_t lb = size_t(l) * B + b;
             const int us = iu & 1;
             const float* meta = reinterpret_cast<const float*>(smem + Cfg::OFF_META + size_t(us) * Cfg::META_BYTES);
+            const int n = n_prev(b);
+            const float* kp = reinterpret_cast<const float*>(smem + Cfg::OFF_KP + size_t(iu & 1) * Cfg::KP_BYTES);
+            if (COMMIT) pwait(&kpfull[iu & 1], (iu >> 1) & 1, abort_flag, a.status);
             pwait(&ufull[us], (iu >> 1) & 1, abort_flag, a.status);
             pwait(&tfull[us], (iu >> 1) & 1, abort_flag, a.status);
             tc_fence_after();
             const uint32_t dt = tbase + us * Cfg::P_COLS + (uint32_t(32 * q4) << 16);
-#pragma unroll
+#pragma unroll 1
             for (int j = 0; j < G; ++j) {
                 const int h = kh * G + j;
                 // P row i of this head: S_hi·X_hi + S_hi·X_lo + S_lo·X_hi over its chains
@@ -839,6 +873,25 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
                     tc_fence_before();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&tempty[us]);
+                }
+                if (COMMIT && n > 0) {
+                    // the committed state's products: Γ (S_0 X) + Σ_s (c_s δ_s[i]) (k'_s · X)
+                    const float gm = kp[Cfg::KP_GAM + j];
+#pragma unroll
+                    for (int c = 0; c < 2 * TMAX; ++c) pr[c] *= gm;
+#pragma unroll 1
+                    for (int s2 = 0; s2 < n; ++s2) {
+                        const float av = kp[Cfg::KP_C + j * TMAX + s2] * kp[Cfg::KP_DL + (j * TMAX + s2) * D + i];
+                        const float4* gpr = reinterpret_cast<const float4*>(meta + Cfg::M_GP + s2 * 2 * TMAX);
+#pragma unroll
+                        for (int c4 = 0; c4 < 2 * TMAX / 4; ++c4) {
+                            const float4 gv = gpr[c4];
+                            pr[4 * c4] = fmaf(av, gv.x, pr[4 * c4]);
+                            pr[4 * c4 + 1] = fmaf(av, gv.y, pr[4 * c4 + 1]);
+                            pr[4 * c4 + 2] = fmaf(av, gv.z, pr[4 * c4 + 2]);
+                            pr[4 * c4 + 3] = fmaf(av, gv.w, pr[4 * c4 + 3]);
+                        }
+                    }
                 }
                 const float* R = meta + Cfg::M_REC + j * TMAX * RS;
                 const float* vv = meta + Cfg::M_V + size_t(j) * TMAX * D + i;
@@ -873,7 +926,10 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
                 }
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&uempty[us]);
+            if (lane == 0) {
+                mbar_arrive(&uempty[us]);
+                if (COMMIT) mbar_arrive(&kpempty[iu & 1]);
+            }
         }
     }
     tc_fence_before();
