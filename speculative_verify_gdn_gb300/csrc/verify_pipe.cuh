@@ -55,16 +55,16 @@ struct PipeCfg {
     static constexpr int NP = 2 * TMAX < 16 ? 16 : 2 * TMAX;
     static constexpr int XROWS = 2 * NP, XKB = XROWS * 128, X_BYTES = KB * XKB;
     static constexpr int KSLOT = 128 * 128;                 // one state K-block: 128 rows x 128 B
-    static constexpr int NKS = COMMIT ? 6 : 8;               // shared-memory K-block slots
-    static constexpr int NTS = 4;                            // TMEM K-block slots (hi 32 + lo 32)
     // accumulator chains per value head: with one value head per unit, even and odd K-steps go to
     // separate accumulators, so every unit has two chains to alternate with
     static constexpr int S = G == 1 ? 2 : 1;
-    // TMEM: 2 unit slots of 2 chains x (hi pass: 2NP columns, lo pass: NP columns, 32-aligned),
-    // then the K-block ring
-    static constexpr int CH_COLS = 64, P_COLS = 2 * CH_COLS;
-    static constexpr int T_RING = 2 * P_COLS;
+    // TMEM: NUS unit slots of 2 chains x (hi pass: 2NP columns at +0, lo pass: NP columns at
+    // +2NP; 32-aligned), then a ring of NTS K-block slots (hi 32 + lo 32 columns)
     static constexpr int TMEM_COLS = 512;
+    static constexpr int CH_COLS = (3 * NP + 31) / 32 * 32, P_COLS = 2 * CH_COLS;
+    static constexpr int NUS = TMAX <= 8 ? 2 : 1;
+    static constexpr int T_RING = NUS * P_COLS;
+    static constexpr int NTS = (TMEM_COLS - T_RING) / 64 < 4 ? (TMEM_COLS - T_RING) / 64 : 4;
     static constexpr int NPARTS = 2 + G;                     // q, k, v of each value head
     // staged rows per part (W <= 4): W-1 old conv-state rows, the T qkv rows and, when committing,
     // W-1 rows of the previous round's qkv ending at its accepted count
@@ -72,22 +72,35 @@ struct PipeCfg {
     static constexpr int RAW_BYTES = NPARTS * NRMAX * D * ES + NPARTS * D * 4 * ES;
     static constexpr int STAGE_BYTES = (RAW_BYTES + 127) / 128 * 128;
     // meta slot (floats): per value head j and position t a record {c0, γ, β, k_t·q_t, CK[TMAX],
-    // CQ[TMAX]} (16-byte aligned), the conv outputs V[G][TMAX][D] and (COMMIT) GP[s][c] = k'_s·X_c
-    // of the previous round's k'_s
+    // CQ[TMAX]} (16-byte aligned), the conv outputs V[G][TMAX][D] and, COMMIT, GP[s][c] = k'_s·X_c
+    // of the previous round's k'_s and the new conv-state rows CW[NPARTS][3][D] (io type)
     static constexpr int RS = 4 + 2 * TMAX;
     static constexpr int M_REC = 0, M_V = G * TMAX * RS, M_GP = M_V + G * TMAX * D,
-                         M_FLOATS = M_GP + (COMMIT ? 2 * TMAX * TMAX : 0);
+                         M_CW = M_GP + (COMMIT ? 2 * TMAX * TMAX : 0),
+                         M_FLOATS = M_CW + (COMMIT ? (NPARTS * 3 * D * ES + 3) / 4 : 0);
     static constexpr int META_BYTES = (M_FLOATS * 4 + 127) / 128 * 128;
     // commit slot (floats): previous round's k_s rows [TMAX][D], δ_s rows [G][TMAX][D],
     // c_s = Γ(s+1 .. n-1) [G][TMAX], Γ(0 .. n-1) [G]
-    static constexpr int KP_KS = D + 4;                      // padded k rows: conflict-free fragments
-    static constexpr int KP_K = 0, KP_DL = TMAX * KP_KS, KP_C = KP_DL + G * TMAX * D,
+    // k and δ rows padded to 136 floats: the convert warps' fragment loads (row = lane & 3 or
+    // its +4, column / state row ~ lane >> 2) fall in distinct banks
+    static constexpr int KP_KS = D + 8;
+    static constexpr int KP_K = 0, KP_DL = TMAX * KP_KS, KP_C = KP_DL + G * TMAX * KP_KS,
                          KP_GAM = KP_C + G * TMAX, KP_FLOATS = KP_GAM + 4;
     static constexpr int KP_BYTES = COMMIT ? (KP_FLOATS * 4 + 127) / 128 * 128 : 0;
+    // Gram block X_m · k_n (m < 2 TMAX, n < TMAX) in 16 x 8 mma.sync tiles: one tile (TMAX <= 8)
+    // split over the 4 prep warps by channels, or (TMAX = 16) 4 tiles, one per warp
+    static constexpr int GRAM_TILES = ((2 * TMAX + 15) / 16) * ((TMAX + 7) / 8);
     // prep scratch (floats): norm partials [4][2TMAX], inverse norms [2TMAX], Gram partials
-    // [4 warps][16][8], Gram [TMAX][2TMAX]
+    // [4 warps][16][8] (one-tile case), Gram [TMAX][2TMAX]
+    // (COMMIT) epilogue: partials of k'_s · X_c [4 warps][16][8]
     static constexpr int S_NRM = 0, S_INV = S_NRM + 8 * TMAX, S_GP = S_INV + 2 * TMAX,
-                         S_GRAM = S_GP + (COMMIT ? 8 : 4) * 128, S_FLOATS = S_GRAM + 2 * TMAX * TMAX;
+                         S_GRAM = S_GP + (GRAM_TILES == 1 ? 4 * 128 : 0), S_EGP = S_GRAM + 2 * TMAX * TMAX,
+                         S_FLOATS = S_EGP + (COMMIT ? 4 * 128 : 0);
+    // shared-memory K-block ring: as many 16 KiB slots as the rest leaves room for (at most 8)
+    static constexpr size_t REST = 2 * size_t(X_BYTES) + 2 * size_t(STAGE_BYTES) + 2 * size_t(META_BYTES) +
+                                   2 * size_t(KP_BYTES) + size_t(S_FLOATS) * 4 + 64 * 8 + 16 + 16 + 1024;
+    static constexpr int NKS_FIT = int((227 * 1024 - REST) / KSLOT);
+    static constexpr int NKS = NKS_FIT > 8 ? 8 : NKS_FIT;
 
     static constexpr size_t OFF_RING = 0;
     static constexpr size_t OFF_X = OFF_RING + size_t(NKS) * KSLOT;
@@ -100,16 +113,16 @@ struct PipeCfg {
     static constexpr size_t OFF_MISC = OFF_BAR + NBAR * 8;   // TMEM base, abort flag
     static constexpr size_t SMEM = OFF_MISC + 16 + 1024;
 
-    static_assert(T_RING + NTS * 64 <= TMEM_COLS, "TMEM budget");
-    static_assert(2 * NP + NP <= CH_COLS && 2 * NP == 32, "one chain: hi pass at +0, lo pass at +32");
+    static_assert(T_RING + NTS * 64 <= TMEM_COLS && NTS >= G, "TMEM budget");
+    static_assert(NKS >= 2 * G, "shared-memory ring");
     static_assert(G * S == 2, "two accumulator chains per unit");
+    static_assert(!COMMIT || TMAX <= 8, "the fused rollback serves T <= 8");
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
     static_assert(OFF_X % 1024 == 0 && X_BYTES % 1024 == 0, "swizzle atoms need 1024-byte bases");
-    static_assert((RS * 4) % 16 == 0 && (M_V * 4) % 16 == 0 && (M_GP * 4) % 16 == 0,
-                  "records are read as float4");
+    static_assert((RS * 4) % 16 == 0 && (M_V * 4) % 16 == 0 && (M_GP * 4) % 16 == 0 &&
+                  (M_CW * 4) % 16 == 0, "records are read as float4, CW rows as 16-byte vectors");
     static_assert((KP_DL * 4) % 16 == 0 && (KP_KS * 4) % 16 == 0, "bulk-copy destinations");
-    static_assert(2 * TMAX <= 16 && TMAX <= 8, "Gram block is one m16n8 tile");
-    static_assert(G * TMAX * TMAX <= 128, "one prep thread per coefficient");
+    static_assert(GRAM_TILES == 1 || GRAM_TILES == 4, "Gram block: one tile, or one tile per prep warp");
 };
 
 __device__ __forceinline__ void named_bar(int id, int nthreads) {
@@ -252,7 +265,7 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
     uint64_t* ufull = sempty + 2;                // unit prologue (X tile, meta) ready
     uint64_t* uempty = ufull + 2;                // unit slot free: last MMA commit + 4 epilogue warps
     uint64_t* kpfull = uempty + 2;               // COMMIT: previous round's tape rows staged
-    uint64_t* kpempty = kpfull + 2;              // COMMIT: commit slot read by prep, convert, epilogue
+    uint64_t* kpempty = kpfull + 2;              // COMMIT: commit slot read by convert and epilogue
     uint64_t* mdone = kpempty + 2;               // every MMA of this CTA complete
     uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + Cfg::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::OFF_MISC + 4);
@@ -270,7 +283,7 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
                               (bb >= kconv && bb < kconv + NKS) || (bb >= tmfull && bb < tmfull + NTS) ||
                               (bb >= tempty && bb < tempty + 2);
             const bool kpe = bb >= kpempty && bb < kpempty + 2;
-            mbar_init(bb, four ? 4 : kpe ? 9 : (bb >= uempty && bb < uempty + 2) ? 5 : 1);
+            mbar_init(bb, four ? 4 : kpe ? 8 : (bb >= uempty && bb < uempty + 2) ? 5 : 1);
         }
         *abort_flag = 0;
         fence_mbar_init();
@@ -338,6 +351,17 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
         // All destinations are multiples of 128 bytes.
         const IO* cw = static_cast<const IO*>(a.conv_w);
         int issued = 0;
+        // COMMIT: gate g'_s of lane (j, s) of a unit's previous round, loaded one unit ahead
+        auto prev_gate = [&](int iu2) -> float {
+            if (!COMMIT || iu2 >= n_my) return 1.f;
+            int l2, b2, kh2;
+            unit_of(iu2, l2, b2, kh2);
+            const int n2 = n_prev(b2);
+            const int gj = lane / TMAX, gs = lane - gj * TMAX;
+            return (gj < G && gs < n2) ? __ldg(a.g_prev + ((size_t(l2) * B + b2) * T + gs) * Hv + kh2 * G + gj)
+                                       : 1.f;
+        };
+        float gv_next = prev_gate(0);
         for (int iu = 0; iu < n_my; ++iu) {
             int l, b, kh;
             unit_of(iu, l, b, kh);
@@ -346,14 +370,13 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
             IO* qs = reinterpret_cast<IO*>(smem + Cfg::OFF_STAGE + size_t(ss) * Cfg::STAGE_BYTES);
             IO* cws = qs + size_t(Cfg::NPARTS) * NR * D;
             int n = 0;
-            float gv = 1.f;                          // COMMIT: gate g'_s of lane (j, s)
+            const float gv = gv_next;
             if (COMMIT) {
                 const int nr = __ldg(a.n_acc_prev + b);
                 if ((nr < 0 || nr > T) && lane == 0 && kh == 0 && l == 0)
                     set_status(a.status, GDN_STATUS_BAD_NACC);
                 n = n_prev(b);
-                const int gj = lane / TMAX, gs = lane - gj * TMAX;
-                if (gj < G && gs < n) gv = __ldg(a.g_prev + (lb * T + gs) * Hv + kh * G + gj);
+                gv_next = prev_gate(iu + 1);
             }
             if (!pwait_warp(&sempty[ss], ((iu >> 1) & 1) ^ 1, abort_flag, a.status)) break;
             if (lane == 0) {
@@ -401,7 +424,7 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
                                  &kpfull[ks]);
 #pragma unroll
                         for (int j = 0; j < G; ++j)
-                            bulk_g2s(kp + Cfg::KP_DL + (j * TMAX + s2) * D,
+                            bulk_g2s(kp + Cfg::KP_DL + (j * TMAX + s2) * Cfg::KP_KS,
                                      a.tape_delta_prev + ((lb * T + s2) * Hv + kh * G + j) * size_t(D),
                                      uint32_t(D * 4), &kpfull[ks]);
                     }
@@ -417,7 +440,7 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------------ mma (whole warp)
-        // chain c of a unit slot: hi pass (N = 2NP) at c * CH_COLS, lo pass (N = NP) at + 32. Per
+        // chain c of a unit slot: hi pass (N = 2NP) at c * CH_COLS, lo pass (N = NP) at + 2NP. Per
         // K-step the order is hi of every chain, then lo of every chain: the same accumulator comes
         // back only every 4 MMAs, past the tensor core's accumulate latency.
         constexpr int S = Cfg::S;
@@ -428,11 +451,11 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
         uint32_t tph = 0;
         bool ok = true;
         for (int iu = 0; iu < n_my && ok; ++iu) {
-            const int us = iu & 1;
+            const int us = iu & 1, ps = iu % Cfg::NUS;
             if (!pwait_warp(&ufull[us], (iu >> 1) & 1, abort_flag, a.status)) break;
-            if (!pwait_warp(&tempty[us], ((iu >> 1) & 1) ^ 1, abort_flag, a.status)) break;
+            if (!pwait_warp(&tempty[ps], ((iu / Cfg::NUS) & 1) ^ 1, abort_flag, a.status)) break;
             const uint64_t db = umma_desc_sw128(sX0 + us * Cfg::X_BYTES);
-            const uint32_t dt = tbase + us * Cfg::P_COLS;
+            const uint32_t dt = tbase + ps * Cfg::P_COLS;
             for (int kb = 0; kb < Cfg::KB; ++kb) {
                 int slot[G];
 #pragma unroll
@@ -456,7 +479,7 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
 #pragma unroll
                     for (int j = 0; j < G; ++j) {
                         const int c = j * S + ks % S;
-                        umma_tf32_ts_warp(dt + c * Cfg::CH_COLS + 32,
+                        umma_tf32_ts_warp(dt + c * Cfg::CH_COLS + 2 * NP,
                                           tbase + Cfg::T_RING + slot[j] * 64 + 32 + ks * 8, bk, IDESC2, acc);
                     }
                 }
@@ -464,7 +487,7 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
                 for (int j = 0; j < G; ++j) umma_commit_warp(&tmempty[slot[j]]);
             }
             if (ok) {
-                umma_commit_warp(&tfull[us]);
+                umma_commit_warp(&tfull[ps]);
                 umma_commit_warp(&uempty[us]);
             }
         }
@@ -529,14 +552,13 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
 #pragma unroll
                 for (int t = 0; t < TMAX; ++t) E[3 + t] = (t < T) ? io_to_f(col[size_t(W - 1 + t) * D]) : 0.f;
                 if (COMMIT && n > 0) {
-                    // the committed window is the new conv state: row r is E[r + 4 - W] (exact copies)
-                    const int cb = part == 0 ? kh * D
-                                 : part == 1 ? Hk * D + kh * D : 2 * Hk * D + (kh * G + part - 2) * D;
-                    IO* cso = static_cast<IO*>(a.conv_state_out) + lb * size_t(W - 1) * C + cb + p;
+                    // the committed window is the new conv state: row r is E[r + 4 - W] (exact
+                    // copies), stashed for the epilogue warps to write out
+                    IO* cw_s = reinterpret_cast<IO*>(meta + Cfg::M_CW) + size_t(part) * 3 * D + p;
 #pragma unroll
                     for (int k = 0; k < 3; ++k) {
                         const int r = k + W - 4;
-                        if (r >= 0) IoTraits<IO>::store(cso, size_t(r) * C, E[k]);
+                        if (r >= 0) IoTraits<IO>::store(cw_s, size_t(r) * D, E[k]);
                     }
                 }
                 float yv[TMAX];
@@ -600,13 +622,45 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
             }
             fence_async_smem();
             named_bar(1, 128);
-            // Gram block on the warp tensor path: D[m][n] = X_m · k_n over this warp's 32 channels,
-            // 3xTF32 (hi·hi + hi·lo + lo·hi); rows m: k_0.., q_0.. (zero beyond 2 TMAX). COMMIT: also
-            // D'[m][s] = X_m · k'_s with the previous round's k'_s (zero for s ≥ n)
-            const float* kpp = reinterpret_cast<const float*>(smem + Cfg::OFF_KP + size_t(iu & 1) * Cfg::KP_BYTES);
-            if (COMMIT) pwait(&kpfull[iu & 1], (iu >> 1) & 1, abort_flag, a.status);
-            {
-                float acc[4] = {0.f, 0.f, 0.f, 0.f}, acc2[4] = {0.f, 0.f, 0.f, 0.f};
+            // Gram block on the warp tensor path: D[m][n] = X_m · k_n, 3xTF32 (hi·hi + hi·lo + lo·hi);
+            // rows m: k_0.., q_0.. (zero beyond 2 TMAX). One 16 x 8 tile: each warp takes 32 channels
+            // and the partials are summed; four tiles (TMAX = 16): warp pw takes tile pw, all channels.
+            if constexpr (Cfg::GRAM_TILES == 4) {
+                const int mt = pw >> 1, nt = pw & 1;
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+                for (int ks = 0; ks < 16; ++ks) {
+                    const int ch = 8 * ks + gt4;
+                    float av[4];
+                    av[0] = *reinterpret_cast<const float*>(Xb + sw128_off(16 * mt + gq, ch, XKB));
+                    av[2] = *reinterpret_cast<const float*>(Xb + sw128_off(16 * mt + gq, ch + 4, XKB));
+                    av[1] = *reinterpret_cast<const float*>(Xb + sw128_off(16 * mt + gq + 8, ch, XKB));
+                    av[3] = *reinterpret_cast<const float*>(Xb + sw128_off(16 * mt + gq + 8, ch + 4, XKB));
+                    const float bv0 = *reinterpret_cast<const float*>(Xb + sw128_off(8 * nt + gq, ch, XKB));
+                    const float bv1 = *reinterpret_cast<const float*>(Xb + sw128_off(8 * nt + gq, ch + 4, XKB));
+                    uint32_t ahi[4], alo[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float h = tf32_trunc(av[e]);
+                        ahi[e] = __float_as_uint(h);
+                        alo[e] = __float_as_uint(tf32_trunc(av[e] - h));
+                    }
+                    const float bh0 = tf32_trunc(bv0), bh1 = tf32_trunc(bv1);
+                    const uint32_t bl0 = __float_as_uint(tf32_trunc(bv0 - bh0));
+                    const uint32_t bl1 = __float_as_uint(tf32_trunc(bv1 - bh1));
+                    mma_tf32_16x8x8(acc, ahi, __float_as_uint(bh0), __float_as_uint(bh1));
+                    mma_tf32_16x8x8(acc, ahi, bl0, bl1);
+                    mma_tf32_16x8x8(acc, alo, __float_as_uint(bh0), __float_as_uint(bh1));
+                }
+                // Gr[a][c] = k_a · X_c = D[c][a]
+                const int c0 = 16 * mt + gq, a0 = 8 * nt + 2 * gt4;
+                gram[a0 * 2 * TMAX + c0] = acc[0];
+                gram[(a0 + 1) * 2 * TMAX + c0] = acc[1];
+                gram[a0 * 2 * TMAX + c0 + 8] = acc[2];
+                gram[(a0 + 1) * 2 * TMAX + c0 + 8] = acc[3];
+            } else {
+              {
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int ks = 0; ks < 4; ++ks) {
                     const int ch = 32 * pw + 8 * ks + gt4;
@@ -629,46 +683,26 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
                     mma_tf32_16x8x8(acc, ahi, __float_as_uint(bh0), __float_as_uint(bh1));
                     mma_tf32_16x8x8(acc, ahi, bl0, bl1);
                     mma_tf32_16x8x8(acc, alo, __float_as_uint(bh0), __float_as_uint(bh1));
-                    if (COMMIT && n > 0) {
-                        // B'[k][s] = k'_s[ch + k]: lane (gq, gt4) holds k'_gq at channels ch, ch + 4
-                        const float kv0 = gq < n ? kpp[Cfg::KP_K + gq * Cfg::KP_KS + ch] : 0.f;
-                        const float kv1 = gq < n ? kpp[Cfg::KP_K + gq * Cfg::KP_KS + ch + 4] : 0.f;
-                        const float kh0 = tf32_trunc(kv0), kh1 = tf32_trunc(kv1);
-                        const uint32_t kl0 = __float_as_uint(tf32_trunc(kv0 - kh0));
-                        const uint32_t kl1 = __float_as_uint(tf32_trunc(kv1 - kh1));
-                        mma_tf32_16x8x8(acc2, ahi, __float_as_uint(kh0), __float_as_uint(kh1));
-                        mma_tf32_16x8x8(acc2, ahi, kl0, kl1);
-                        mma_tf32_16x8x8(acc2, alo, __float_as_uint(kh0), __float_as_uint(kh1));
-                    }
                 }
                 float* g4 = gp + pw * 128;
                 g4[gq * 8 + 2 * gt4] = acc[0];
                 g4[gq * 8 + 2 * gt4 + 1] = acc[1];
                 g4[(gq + 8) * 8 + 2 * gt4] = acc[2];
                 g4[(gq + 8) * 8 + 2 * gt4 + 1] = acc[3];
-                if (COMMIT) {
-                    float* g5 = gp + 512 + pw * 128;
-                    g5[gq * 8 + 2 * gt4] = acc2[0];
-                    g5[gq * 8 + 2 * gt4 + 1] = acc2[1];
-                    g5[(gq + 8) * 8 + 2 * gt4] = acc2[2];
-                    g5[(gq + 8) * 8 + 2 * gt4 + 1] = acc2[3];
-                }
-            }
-            named_bar(1, 128);
-            {
+              }
+              named_bar(1, 128);
+              {
                 const int m = p >> 3, nn = p & 7;
-                if (m < 2 * TMAX && nn < TMAX) {
+                if (m < 2 * TMAX && nn < TMAX)
                     gram[nn * 2 * TMAX + m] = gp[p] + gp[128 + p] + gp[256 + p] + gp[384 + p];
-                    if (COMMIT)    // GP[s][c] = k'_s · X_c
-                        meta[Cfg::M_GP + nn * 2 * TMAX + m] = gp[512 + p] + gp[640 + p] + gp[768 + p] + gp[896 + p];
-                }
+              }
             }
             named_bar(1, 128);
             // per value head, one thread per (v, x ≤ v): CK[v][x] = Γ(x→v-1) k_x·k_v and
             // CQ[v][x] = Γ(x→v-1) k_x·q_v for x < v; c0[v] = Γ(root→v-1) and k_v·q_v for x = v
-            {
-                const int fj = p / (TMAX * TMAX), fv = (p / TMAX) % TMAX, fx = p % TMAX;
-                if (fj < G && fv < T && fx <= fv) {
+            for (int idx = p; idx < G * TMAX * TMAX; idx += 128) {
+                const int fj = idx / (TMAX * TMAX), fv = (idx / TMAX) % TMAX, fx = idx % TMAX;
+                if (fv < T && fx <= fv) {
                     const float* hrec = meta + Cfg::M_REC + fj * TMAX * RS;     // γ at [y * RS + 1]
                     float* rec = meta + Cfg::M_REC + (fj * TMAX + fv) * RS;
                     const int y0 = fx < fv ? fx + 1 : 0;
@@ -686,19 +720,19 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
                 }
             }
             named_bar(1, 128);
-            if (p == 0) {
-                mbar_arrive(&ufull[us]);
-                if (COMMIT) mbar_arrive(&kpempty[iu & 1]);
-            }
+            if (p == 0) mbar_arrive(&ufull[us]);
         }
     } else if (warp < 10) {
         // ------------------------------------------------------------------ convert (128 threads)
         // thread = state row: S_hi and S_lo of its 32 columns of each K-block into the TMEM ring (two
         // halves of 16). COMMIT, n > 0: then S_n = Γ S_0 + A K'ᵀ for the warp's 32 rows of the K-block
-        // with mma.sync (rows r0 + gq and r0 + gq + 8, columns c0 + 2 gt4 and + 1 of each 16 x 8 tile),
-        // written back in place for the store warp.
+        // with mma.sync and written back in place for the store warp. Fragment row m of a 16-row
+        // tile maps to state row 8 (m / 8) + 2 (m mod 4) + (m / 4 mod 2): each half-warp then touches
+        // rows with distinct (row mod 8) / 2, so its 8-byte accesses in the 128-byte-swizzled tile
+        // are free of bank conflicts.
         const int q4 = warp & 3, row = 32 * q4 + lane;
         const int gq = lane >> 2, gt4 = lane & 3;
+        const int prow = 2 * (gq & 3) + (gq >> 2);        // fragment row gq (and gq + 8) -> tile row
         int s = 0, ts = 0;
         uint32_t ph = 0, tph = 0;
         for (int iu = 0; iu < n_my; ++iu) {
@@ -752,10 +786,10 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
                             for (int rt = 0; rt < 2; ++rt)
 #pragma unroll
                                 for (int e = 0; e < 4; ++e) {
-                                    const int r = 32 * q4 + 16 * rt + gq + ((e & 1) ? 8 : 0);
+                                    const int r = 32 * q4 + 16 * rt + prow + ((e & 1) ? 8 : 0);
                                     const int s2 = gt4 + ((e & 2) ? 4 : 0);
                                     const float av = s2 < n ? kp[Cfg::KP_C + j * TMAX + s2] *
-                                                                  kp[Cfg::KP_DL + (j * TMAX + s2) * D + r]
+                                                                  kp[Cfg::KP_DL + (j * TMAX + s2) * Cfg::KP_KS + r]
                                                             : 0.f;
                                     const float h = tf32_trunc(av);
                                     afh[rt][e] = __float_as_uint(h);
@@ -780,7 +814,7 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
                                     // u: (r, c), (r, c + 1), (r + 8, c), (r + 8, c + 1), c = 8 ct + 2 gt4
 #pragma unroll
                                     for (int hr = 0; hr < 2; ++hr) {
-                                        const int r = 32 * q4 + 16 * rt + gq + 8 * hr;
+                                        const int r = 32 * q4 + 16 * rt + prow + 8 * hr;
                                         const int c = 8 * ct + 2 * gt4;
                                         float2* pp = reinterpret_cast<float2*>(
                                             Ab + r * 128 + ((((c >> 2) ^ (r & 7))) << 4) + (c & 3) * 4);
@@ -806,7 +840,9 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
         }
     } else if (COMMIT && warp == 15) {
         // ------------------------------------------------------------------ store (whole warp)
-        // committed K-blocks back to the state by TMA store (lane 0: its bulk groups), then free
+        // committed K-blocks back to the state by TMA store (lane 0: its bulk groups); a slot is
+        // freed as soon as its store has read it (keeping stores in flight longer holds slots the
+        // loader needs and measured slower)
         int s = 0;
         uint32_t ph = 0;
         bool ok = true;
@@ -848,9 +884,69 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
             const float* kp = reinterpret_cast<const float*>(smem + Cfg::OFF_KP + size_t(iu & 1) * Cfg::KP_BYTES);
             if (COMMIT) pwait(&kpfull[iu & 1], (iu >> 1) & 1, abort_flag, a.status);
             pwait(&ufull[us], (iu >> 1) & 1, abort_flag, a.status);
-            pwait(&tfull[us], (iu >> 1) & 1, abort_flag, a.status);
+            if (COMMIT && n > 0) {
+                const int et = tid - 320, ew = warp - 10;
+                // the new conv-state rows, stashed by the prep warps, to HBM as 16-byte vectors
+                const IO* cw_s = reinterpret_cast<const IO*>(meta + Cfg::M_CW);
+                IO* cso = static_cast<IO*>(a.conv_state_out) + lb * size_t(W - 1) * C;
+                constexpr int EPV = 16 / Cfg::ES, VPR = D / EPV;      // elements per vector, vectors per row
+                const int nvec = Cfg::NPARTS * (W - 1) * VPR;
+                for (int v = et; v < nvec; v += 128) {
+                    const int part = v / ((W - 1) * VPR), rem = v - part * (W - 1) * VPR;
+                    const int r = rem / VPR, c16 = rem - r * VPR;
+                    const int cb = part == 0 ? kh * D
+                                 : part == 1 ? Hk * D + kh * D : 2 * Hk * D + (kh * G + part - 2) * D;
+                    *reinterpret_cast<uint4*>(cso + size_t(r) * C + cb + c16 * EPV) =
+                        *reinterpret_cast<const uint4*>(cw_s + (size_t(part) * 3 + r) * D + c16 * EPV);
+                }
+                // GP[s][c] = k'_s · X_c on the warp tensor path (3xTF32), as the prep's Gram block:
+                // warp ew takes channels 32 ew .. 32 ew + 31, partials reduced over the 4 warps
+                const int gq = lane >> 2, gt4 = lane & 3;
+                const unsigned char* Xb = smem + Cfg::OFF_X + size_t(us) * Cfg::X_BYTES;
+                float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+                for (int ks = 0; ks < 4; ++ks) {
+                    const int ch = 32 * ew + 8 * ks + gt4;
+                    float av[4];
+                    av[0] = *reinterpret_cast<const float*>(Xb + sw128_off(gq, ch, XKB));
+                    av[2] = *reinterpret_cast<const float*>(Xb + sw128_off(gq, ch + 4, XKB));
+                    av[1] = (gq + 8 < 2 * TMAX) ? *reinterpret_cast<const float*>(Xb + sw128_off(gq + 8, ch, XKB)) : 0.f;
+                    av[3] = (gq + 8 < 2 * TMAX) ? *reinterpret_cast<const float*>(Xb + sw128_off(gq + 8, ch + 4, XKB)) : 0.f;
+                    uint32_t ahi[4], alo[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float h = tf32_trunc(av[e]);
+                        ahi[e] = __float_as_uint(h);
+                        alo[e] = __float_as_uint(tf32_trunc(av[e] - h));
+                    }
+                    const float kv0 = gq < n ? kp[Cfg::KP_K + gq * Cfg::KP_KS + ch] : 0.f;
+                    const float kv1 = gq < n ? kp[Cfg::KP_K + gq * Cfg::KP_KS + ch + 4] : 0.f;
+                    const float kh0 = tf32_trunc(kv0), kh1 = tf32_trunc(kv1);
+                    const uint32_t kl0 = __float_as_uint(tf32_trunc(kv0 - kh0));
+                    const uint32_t kl1 = __float_as_uint(tf32_trunc(kv1 - kh1));
+                    mma_tf32_16x8x8(acc, ahi, __float_as_uint(kh0), __float_as_uint(kh1));
+                    mma_tf32_16x8x8(acc, ahi, kl0, kl1);
+                    mma_tf32_16x8x8(acc, alo, __float_as_uint(kh0), __float_as_uint(kh1));
+                }
+                float* egp = scr + Cfg::S_EGP;
+                float* e4 = egp + ew * 128;
+                e4[gq * 8 + 2 * gt4] = acc[0];
+                e4[gq * 8 + 2 * gt4 + 1] = acc[1];
+                e4[(gq + 8) * 8 + 2 * gt4] = acc[2];
+                e4[(gq + 8) * 8 + 2 * gt4 + 1] = acc[3];
+                named_bar(2, 128);
+                {
+                    const int m = et >> 3, nn = et & 7;
+                    if (m < 2 * TMAX && nn < TMAX)
+                        const_cast<float*>(meta)[Cfg::M_GP + nn * 2 * TMAX + m] =
+                            egp[et] + egp[128 + et] + egp[256 + et] + egp[384 + et];
+                }
+                named_bar(2, 128);
+            }
+            const int ps = iu % Cfg::NUS;
+            pwait(&tfull[ps], (iu / Cfg::NUS) & 1, abort_flag, a.status);
             tc_fence_after();
-            const uint32_t dt = tbase + us * Cfg::P_COLS + (uint32_t(32 * q4) << 16);
+            const uint32_t dt = tbase + ps * Cfg::P_COLS + (uint32_t(32 * q4) << 16);
 #pragma unroll 1
             for (int j = 0; j < G; ++j) {
                 const int h = kh * G + j;
@@ -861,18 +957,19 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
 #pragma unroll
                 for (int sc = 0; sc < S; ++sc) {
                     const uint32_t ca = dt + (j * S + sc) * Cfg::CH_COLS;
-                    float part[NP];
 #pragma unroll
-                    for (int off = 0; off < 48; off += 16) {
+                    for (int off = 0; off < 3 * NP; off += 16) {     // X_hi, X_lo, lo-pass blocks
+                        float part[16];
                         tmem_ld16(ca + off, part);
+                        const int c0 = off % NP;
 #pragma unroll
-                        for (int c = 0; c < NP; ++c) pr[c] += part[c];
+                        for (int c = 0; c < 16; ++c) pr[c0 + c] += part[c];
                     }
                 }
                 if (j == G - 1) {
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&tempty[us]);
+                    if (lane == 0) mbar_arrive(&tempty[ps]);
                 }
                 if (COMMIT && n > 0) {
                     // the committed state's products: Γ (S_0 X) + Σ_s (c_s δ_s[i]) (k'_s · X)
@@ -881,7 +978,7 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
                     for (int c = 0; c < 2 * TMAX; ++c) pr[c] *= gm;
 #pragma unroll 1
                     for (int s2 = 0; s2 < n; ++s2) {
-                        const float av = kp[Cfg::KP_C + j * TMAX + s2] * kp[Cfg::KP_DL + (j * TMAX + s2) * D + i];
+                        const float av = kp[Cfg::KP_C + j * TMAX + s2] * kp[Cfg::KP_DL + (j * TMAX + s2) * Cfg::KP_KS + i];
                         const float4* gpr = reinterpret_cast<const float4*>(meta + Cfg::M_GP + s2 * 2 * TMAX);
 #pragma unroll
                         for (int c4 = 0; c4 < 2 * TMAX / 4; ++c4) {
@@ -966,8 +1063,8 @@ cudaError_t launch_verify_pipe_t(const VerifyArgs& a, const VerifyMaps& m, cudaS
 
 // The pipelined kernel serves the Qwen3.6 head shape; everything else uses the per-head kernel.
 template <typename IO>
-bool verify_pipe_eligible(const VerifyArgs& a, const VerifyMaps& m, int D, bool tree) {
-    return m.inputs_ok && !tree && D == 128 && sizeof(IO) == 2 && a.T <= 8 &&
+bool verify_pipe_eligible(const VerifyArgs& a, const VerifyMaps& m, int D, bool tree, bool commit) {
+    return m.inputs_ok && !tree && D == 128 && sizeof(IO) == 2 && a.T <= (commit ? 8 : 16) &&
            (a.Hv == a.Hk || a.Hv == 2 * a.Hk);
 }
 
@@ -977,8 +1074,13 @@ cudaError_t launch_verify_pipe(const VerifyArgs& a, const VerifyMaps& m, cudaStr
     if (a.T <= 4)
         return G == 1 ? launch_verify_pipe_t<IO, 4, 1, COMMIT>(a, m, s)
                       : launch_verify_pipe_t<IO, 4, 2, COMMIT>(a, m, s);
-    return G == 1 ? launch_verify_pipe_t<IO, 8, 1, COMMIT>(a, m, s)
-                  : launch_verify_pipe_t<IO, 8, 2, COMMIT>(a, m, s);
+    if (COMMIT || a.T <= 8)
+        return G == 1 ? launch_verify_pipe_t<IO, 8, 1, COMMIT>(a, m, s)
+                      : launch_verify_pipe_t<IO, 8, 2, COMMIT>(a, m, s);
+    if constexpr (!COMMIT)
+        return G == 1 ? launch_verify_pipe_t<IO, 16, 1, false>(a, m, s)
+                      : launch_verify_pipe_t<IO, 16, 2, false>(a, m, s);
+    return cudaErrorNotSupported;
 }
 
 }  // namespace gdn

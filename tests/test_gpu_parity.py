@@ -67,7 +67,7 @@ def test_verify_conv_widths_and_dtypes(gdnlib, W, io):
     run_verify_case(w, seed=W)
 
 
-@pytest.mark.parametrize("Hk,Hv,T", [(4, 4, 8), (3, 6, 2), (1, 2, 7)])
+@pytest.mark.parametrize("Hk,Hv,T", [(4, 4, 8), (3, 6, 2), (1, 2, 7), (2, 2, 16), (2, 4, 12), (1, 1, 9)])
 def test_verify_head_groupings(gdnlib, Hk, Hv, T):
     """One and two value heads per key head at d = 128 (both layouts of the pipelined kernel)."""
     w = small(I.WORKLOADS[1], L=2, B=3, N=T, Hk=Hk, Hv=Hv, D=128, V=64)
