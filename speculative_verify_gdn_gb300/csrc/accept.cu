@@ -64,13 +64,20 @@ __device__ __forceinline__ int key_index(unsigned long long k) {
 }
 
 // ---------------------------------------------------------------- integer-weight contract
-// 2^x for x <= 0 by Cody–Waite reduction (nearest integer n, remainder f in [-1/2, 1/2]) and the
-// degree-7 Taylor polynomial of 2^f, coefficients (ln 2)^k / k! rounded to fp32, Horner with
-// fused multiply-adds, then an exact scaling by 2^n. Results below 2^-63.5 flush to 0.
-__device__ __forceinline__ float exp2_spec(float x) {
-    const float n = rintf(x);
-    if (n < -64.0f) return 0.0f;
-    const float f = __fsub_rn(x, n);
+// The integer weight w = floor(2^32 · 2^x), x = (l − m)·c ≤ 0, with this library's 2^x: Cody–Waite
+// reduction x = n + f (n = rint(x), f in [-1/2, 1/2]), the degree-7 Taylor polynomial p of 2^f
+// (coefficients (ln 2)^k / k! rounded to fp32, Horner with fused multiply-adds), 2^x = p · 2^n,
+// zero for n < -64. p lies in [2^-1/2, 2^1/2] (a normal fp32 with 24-bit significand M, exponent
+// E), and p · 2^n · 2^32 is exact in fp32, so w = floor(M · 2^(E + n + 9)): a shift, no float to
+// 64-bit conversion. n comes from the bits of x + 1.5·2^23 (round to nearest even, exact for
+// |x| < 2^22).
+__device__ __forceinline__ unsigned long long weight_of(float l, float m, float c) {
+    const float x = __fmul_rn(__fsub_rn(l, m), c);
+    if (x < -100.0f) return 0ull;                       // rint(x) < -64 as well
+    const float t = __fadd_rn(x, 12582912.0f);
+    const int n = __float_as_int(t) - 0x4B400000;       // rint(x)
+    if (n < -64) return 0ull;
+    const float f = __fsub_rn(x, __fsub_rn(t, 12582912.0f));
     float p = 0x1.ffcbfcp-17f;
     p = __fmaf_rn(p, f, 0x1.430912p-13f);
     p = __fmaf_rn(p, f, 0x1.5d87fep-10f);
@@ -79,14 +86,10 @@ __device__ __forceinline__ float exp2_spec(float x) {
     p = __fmaf_rn(p, f, 0x1.ebfbe0p-3f);
     p = __fmaf_rn(p, f, 0x1.62e430p-1f);
     p = __fmaf_rn(p, f, 1.0f);
-    const float s = __int_as_float((int(n) + 127) << 23);   // 2^n, n in [-64, 0]
-    return __fmul_rn(p, s);
-}
-
-__device__ __forceinline__ unsigned long long weight_of(float l, float m, float c) {
-    const float x = __fmul_rn(__fsub_rn(l, m), c);
-    const float e = exp2_spec(x);
-    return __float2ull_rz(__fmul_rn(e, 4294967296.0f));
+    const uint32_t pb = __float_as_uint(p);
+    const unsigned long long M = (pb & 0x7FFFFFu) | 0x800000u;
+    const int sh = int(pb >> 23) - 127 + n + 9;
+    return sh >= 0 ? (M << sh) : (M >> (-sh));
 }
 
 // Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11), counter (c0..c3), key (k0, k1).
@@ -224,9 +227,13 @@ __device__ __forceinline__ unsigned long long row_best_key(const AcceptArgs& a, 
 }
 
 // ---------------------------------------------------------------- K2: chunk weight sums
+// One warp per tile of 32 consecutive 16-byte vectors (coalesced): the tile's exact u64 weight
+// sum goes to ws_tile (so a later search needs only one tile), the chunk sum to ws_sum, the draft
+// token's weight to ws_wd.
 template <typename LT>
 __global__ void __launch_bounds__(kAccThreads) accept_weights_kernel(const AcceptArgs a) {
     using LV = LogitVec<LT>;
+    constexpr int TILE = 32 * LV::N;
     __shared__ unsigned long long sh[kAccThreads / 32];
     __shared__ float s_m;
     const int RS = a.N + 1;
@@ -238,23 +245,33 @@ __global__ void __launch_bounds__(kAccThreads) accept_weights_kernel(const Accep
     const int d = (i < a.N) ? a.drafts[size_t(b) * a.N + i] : -1;
     const LT* row = static_cast<const LT*>(row_ptr(a, b, i, sizeof(LT)));
     const int lo = ch * a.CS, hi = min(a.V, lo + a.CS);
-    const int vec_hi = lo + (hi - lo) / LV::N * LV::N;
+    const int nt = (hi - lo + TILE - 1) / TILE;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    unsigned long long* tiles = a.ws_tile + (size_t(r) * a.CH + ch) * a.NT;
     unsigned long long sum = 0;
-#pragma unroll 2
-    for (int v0 = lo + threadIdx.x * LV::N; v0 < vec_hi; v0 += kAccThreads * LV::N) {
-        float x[LV::N];
-        LV::load(row + v0, x);
+    for (int t = warp; t < nt; t += kAccThreads / 32) {
+        const int v0 = lo + t * TILE + lane * LV::N;
+        unsigned long long ts = 0;
+        if (v0 + LV::N <= hi) {
+            float x[LV::N];
+            LV::load(row + v0, x);
 #pragma unroll
-        for (int k = 0; k < LV::N; ++k) {
-            const unsigned long long w = weight_of(x[k], m, c);
-            sum += w;
-            if (v0 + k == d) a.ws_wd[r] = w;
+            for (int k = 0; k < LV::N; ++k) {
+                const unsigned long long w = weight_of(x[k], m, c);
+                ts += w;
+                if (v0 + k == d) a.ws_wd[r] = w;
+            }
+        } else {
+            for (int k = 0; k < LV::N && v0 + k < hi; ++k) {
+                const unsigned long long w = weight_of(LV::one(row + v0 + k), m, c);
+                ts += w;
+                if (v0 + k == d) a.ws_wd[r] = w;
+            }
         }
-    }
-    for (int v = vec_hi + threadIdx.x; v < hi; v += kAccThreads) {
-        const unsigned long long w = weight_of(LV::one(row + v), m, c);
-        sum += w;
-        if (v == d) a.ws_wd[r] = w;
+        sum += ts;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ts += __shfl_xor_sync(0xffffffffu, ts, o);
+        if (lane == 0) tiles[t] = ts;
     }
     sum = block_sum_u64(sum, sh);
     if (threadIdx.x == 0) a.ws_sum[size_t(r) * a.CH + ch] = sum;
@@ -262,27 +279,73 @@ __global__ void __launch_bounds__(kAccThreads) accept_weights_kernel(const Accep
 
 // ---------------------------------------------------------------- K3 helpers
 // smallest v in chunk `ch` of row (b, i) whose in-chunk prefix of weights exceeds rr (ban = -1
-// for none); all threads of the block call it, the result is returned to all.
+// for none): the tile from a block scan of the chunk's tile sums, then one warp scans the tile's
+// weights. All threads of the block call it; the result is returned to all (-1 if rr is past the
+// chunk's total).
 template <typename LT>
 __device__ int chunk_search(const AcceptArgs& a, int b, int i, int ch, unsigned long long rr,
                             int ban, float m, unsigned long long* sh, int* s_tok) {
     using LV = LogitVec<LT>;
+    constexpr int TILE = 32 * LV::N;
+    __shared__ int s_tile;
+    __shared__ unsigned long long s_rem;
+    const int r = b * (a.N + 1) + i;
     const LT* row = static_cast<const LT*>(row_ptr(a, b, i, sizeof(LT)));
     const int lo = ch * a.CS, hi = min(a.V, lo + a.CS);
-    const int len = hi - lo;
-    const int per = (len + kAccThreads - 1) / kAccThreads;
-    const int t_lo = lo + min(len, int(threadIdx.x) * per), t_hi = min(hi, t_lo + per);
+    const int nt = (hi - lo + TILE - 1) / TILE;
+    const unsigned long long* tiles = a.ws_tile + (size_t(r) * a.CH + ch) * a.NT;
+    const int ban_t = (ban >= lo && ban < hi) ? (ban - lo) / TILE : -1;
+    const unsigned long long wban = ban_t >= 0 ? a.ws_wd[r] : 0ull;
+    // 1. the tile: thread k owns tiles [k per, (k + 1) per)
+    const int per = (nt + kAccThreads - 1) / kAccThreads;
+    const int t_lo = min(nt, int(threadIdx.x) * per), t_hi = min(nt, t_lo + per);
     unsigned long long s = 0;
-    for (int v = t_lo; v < t_hi; ++v)
-        s += (v == ban) ? 0ull : weight_of(LV::one(row + v), m, a.c);
-    if (threadIdx.x == 0) *s_tok = -1;
+    for (int t = t_lo; t < t_hi; ++t) s += tiles[t] - (t == ban_t ? wban : 0ull);
+    if (threadIdx.x == 0) { *s_tok = -1; s_tile = -1; }
     unsigned long long total;
     const unsigned long long pre = block_exscan_u64(s, sh, &total);
     if (pre <= rr && rr < pre + s) {
         unsigned long long acc = pre;
-        for (int v = t_lo; v < t_hi; ++v) {
-            acc += (v == ban) ? 0ull : weight_of(LV::one(row + v), m, a.c);
-            if (acc > rr) { *s_tok = v; break; }
+        for (int t = t_lo; t < t_hi; ++t) {
+            const unsigned long long w = tiles[t] - (t == ban_t ? wban : 0ull);
+            if (rr < acc + w) { s_tile = t; s_rem = rr - acc; break; }
+            acc += w;
+        }
+    }
+    __syncthreads();
+    const int tile = s_tile;
+    // 2. warp 0 scans the tile: lane l owns its 16-byte vector
+    if (tile >= 0 && threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        const unsigned long long rem = s_rem;
+        const int v0 = lo + tile * TILE + lane * LV::N;
+        float x[LV::N];
+        if (v0 + LV::N <= hi) {
+            LV::load(row + v0, x);
+        } else {
+#pragma unroll
+            for (int k = 0; k < LV::N; ++k) x[k] = v0 + k < hi ? LV::one(row + v0 + k) : 0.f;
+        }
+        unsigned long long w[LV::N], ls = 0;
+#pragma unroll
+        for (int k = 0; k < LV::N; ++k) {
+            w[k] = (v0 + k < hi && v0 + k != ban) ? weight_of(x[k], m, a.c) : 0ull;
+            ls += w[k];
+        }
+        unsigned long long inc = ls;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned long long y = __shfl_up_sync(0xffffffffu, inc, o);
+            if (lane >= o) inc += y;
+        }
+        const unsigned long long lpre = inc - ls;
+        if (lpre <= rem && rem < lpre + ls) {
+            unsigned long long acc = lpre;
+#pragma unroll
+            for (int k = 0; k < LV::N; ++k) {
+                acc += w[k];
+                if (acc > rem) { *s_tok = v0 + k; break; }
+            }
         }
     }
     __syncthreads();

@@ -225,12 +225,18 @@ int check_spec(const spec_dims* d) {
     return GDN_OK;
 }
 
+// tiles of one warp's 16-byte loads: 32 vectors of 8 bf16 or 4 fp32 logits
+int tile_elems(int dtype) { return dtype == GDN_DTYPE_BF16 ? 256 : 128; }
+
 size_t ws_bytes(const spec_dims* d, int32_t mode) {
     const int rows = d->B * (d->N + 1);
     int CH, CS;
     gdn::accept_chunking(rows, d->V, &CH, &CS);
     const size_t keys = size_t(rows) * CH * 8;
-    if (mode == SPEC_MODE_SAMPLE) return keys * 2 + size_t(rows) * 8;
+    if (mode == SPEC_MODE_SAMPLE) {
+        const int TE = tile_elems(d->dtype), NT = (CS + TE - 1) / TE;
+        return keys * 2 + size_t(rows) * 8 + keys * NT;
+    }
     return keys;
 }
 
@@ -245,6 +251,9 @@ gdn::AcceptArgs accept_args(const spec_dims* d, const void* logits, void* worksp
     a.ws_key = ws;
     a.ws_sum = ws + size_t(rows) * a.CH;
     a.ws_wd = ws + size_t(rows) * a.CH * 2;
+    const int TE = tile_elems(d->dtype);
+    a.NT = (a.CS + TE - 1) / TE;
+    a.ws_tile = a.ws_wd + rows;      // used by the sampling mode only (sized by ws_bytes)
     return a;
 }
 

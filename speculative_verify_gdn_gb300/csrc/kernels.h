@@ -83,6 +83,8 @@ struct AcceptArgs {
     unsigned long long* ws_key;
     unsigned long long* ws_sum;
     unsigned long long* ws_wd;
+    unsigned long long* ws_tile;   // sampling: weight sums of 32-vector tiles [rows][CH][NT]
+    int NT;                        // tiles per chunk
     int32_t* n_acc;
     int32_t* out_tokens;
     int32_t* path;
