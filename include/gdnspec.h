@@ -127,7 +127,8 @@ GDN_API int gdn_verify(const gdn_dims* d, const void* qkv, const void* conv_w, c
  * Node v starts from its parent's state (S_0 for parent -1); its conv window is its own raw row
  * and its W-1 nearest ancestors' rows, continued into conv_state when the path is shorter.
  * Other arguments and layouts as gdn_verify with T = node count; the tape is per node.
- * A bad parent sets GDN_STATUS_BAD_PARENT and skips that (layer, sequence).
+ * A bad parent sets GDN_STATUS_BAD_PARENT; that sequence's out / tape rows are then unspecified
+ * (left unwritten, or computed as if the nodes formed one chain).
  */
 GDN_API int gdn_verify_tree(const gdn_dims* d, const int32_t* parent, const void* qkv,
                     const void* conv_w, const void* conv_state, const float* g,

@@ -150,7 +150,7 @@ int verify_common(const gdn_dims* d, const int32_t* parent, const void* qkv, con
     gdn::VerifyMaps maps;
     rc = state_tensor_map(d, state, &maps.state);
     if (rc) return rc;
-    maps.inputs_ok = !tree && input_tensor_maps(d, qkv, conv_state, &maps);
+    maps.inputs_ok = input_tensor_maps(d, qkv, conv_state, &maps);
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e = d->io_dtype == GDN_DTYPE_BF16
                         ? gdn::launch_verify_bf16(a, maps, d->Dk, tree, s)

@@ -48,9 +48,14 @@
 
 namespace gdn {
 
-template <typename IO, int TMAX, int G, bool COMMIT>
+template <typename IO, int TMAX, int G, bool COMMIT, bool TREE>
 struct PipeCfg {
     static constexpr int D = 128, KB = 4, ES = int(sizeof(IO));
+    // T up to 32 (trees): one slot each for the B tile, the records and the staging (a unit's
+    // prologue then waits for the previous unit's epilogue), one accumulator per chain
+    static constexpr bool BIG = TMAX >= 32;
+    static constexpr int NXS = BIG ? 1 : 2;                  // B-tile / meta slots
+    static constexpr int NSS = BIG ? 1 : 2;                  // staging slots
     static constexpr int NWARP = COMMIT ? 16 : 15, NTHR = 32 * NWARP;
     static constexpr int NP = 2 * TMAX < 16 ? 16 : 2 * TMAX;
     static constexpr int XROWS = 2 * NP, XKB = XROWS * 128, X_BYTES = KB * XKB;
@@ -59,10 +64,11 @@ struct PipeCfg {
     // separate accumulators, so every unit has two chains to alternate with
     static constexpr int S = G == 1 ? 2 : 1;
     // TMEM: NUS unit slots of 2 chains x (hi pass: 2NP columns at +0, lo pass: NP columns at
-    // +2NP; 32-aligned), then a ring of NTS K-block slots (hi 32 + lo 32 columns)
+    // +2NP; 32-aligned — or, BIG, one NP-column accumulator that all three products add into),
+    // then a ring of NTS K-block slots (hi 32 + lo 32 columns)
     static constexpr int TMEM_COLS = 512;
-    static constexpr int CH_COLS = (3 * NP + 31) / 32 * 32, P_COLS = 2 * CH_COLS;
-    static constexpr int NUS = TMAX <= 8 ? 2 : 1;
+    static constexpr int CH_COLS = BIG ? NP : (3 * NP + 31) / 32 * 32, P_COLS = 2 * CH_COLS;
+    static constexpr int NUS = (TMAX <= 8 || BIG) ? 2 : 1;
     static constexpr int T_RING = NUS * P_COLS;
     static constexpr int NTS = (TMEM_COLS - T_RING) / 64 < 4 ? (TMEM_COLS - T_RING) / 64 : 4;
     static constexpr int NPARTS = 2 + G;                     // q, k, v of each value head
@@ -88,25 +94,28 @@ struct PipeCfg {
                          KP_GAM = KP_C + G * TMAX, KP_FLOATS = KP_GAM + 4;
     static constexpr int KP_BYTES = COMMIT ? (KP_FLOATS * 4 + 127) / 128 * 128 : 0;
     // Gram block X_m · k_n (m < 2 TMAX, n < TMAX) in 16 x 8 mma.sync tiles: one tile (TMAX <= 8)
-    // split over the 4 prep warps by channels, or (TMAX = 16) 4 tiles, one per warp
+    // split over the 4 prep warps by channels, or 4 / 16 tiles (TMAX = 16 / 32), a quarter per warp
     static constexpr int GRAM_TILES = ((2 * TMAX + 15) / 16) * ((TMAX + 7) / 8);
     // prep scratch (floats): norm partials [4][2TMAX], inverse norms [2TMAX], Gram partials
-    // [4 warps][16][8] (one-tile case), Gram [TMAX][2TMAX]
+    // [4 warps][16][8] (one-tile case), Gram [TMAX][2TMAX] (BIG: in the staging slot, which the
+    // conv has finished with), tree parents [TMAX] and conv-window rows [TMAX][4] (ints)
     // (COMMIT) epilogue: partials of k'_s · X_c [4 warps][16][8]
     static constexpr int S_NRM = 0, S_INV = S_NRM + 8 * TMAX, S_GP = S_INV + 2 * TMAX,
-                         S_GRAM = S_GP + (GRAM_TILES == 1 ? 4 * 128 : 0), S_EGP = S_GRAM + 2 * TMAX * TMAX,
+                         S_GRAM = S_GP + (GRAM_TILES == 1 ? 4 * 128 : 0),
+                         S_PAR = S_GRAM + (BIG ? 0 : 2 * TMAX * TMAX), S_WIN = S_PAR + (TREE ? TMAX : 0),
+                         S_EGP = S_WIN + (TREE ? 4 * TMAX + 4 : 0),
                          S_FLOATS = S_EGP + (COMMIT ? 4 * 128 : 0);
     // shared-memory K-block ring: as many 16 KiB slots as the rest leaves room for (at most 8)
-    static constexpr size_t REST = 2 * size_t(X_BYTES) + 2 * size_t(STAGE_BYTES) + 2 * size_t(META_BYTES) +
+    static constexpr size_t REST = NXS * size_t(X_BYTES) + NSS * size_t(STAGE_BYTES) + NXS * size_t(META_BYTES) +
                                    2 * size_t(KP_BYTES) + size_t(S_FLOATS) * 4 + 64 * 8 + 16 + 16 + 1024;
     static constexpr int NKS_FIT = int((227 * 1024 - REST) / KSLOT);
     static constexpr int NKS = NKS_FIT > 8 ? 8 : NKS_FIT;
 
     static constexpr size_t OFF_RING = 0;
     static constexpr size_t OFF_X = OFF_RING + size_t(NKS) * KSLOT;
-    static constexpr size_t OFF_STAGE = OFF_X + 2 * size_t(X_BYTES);
-    static constexpr size_t OFF_META = OFF_STAGE + 2 * size_t(STAGE_BYTES);
-    static constexpr size_t OFF_KP = OFF_META + 2 * size_t(META_BYTES);
+    static constexpr size_t OFF_STAGE = OFF_X + NXS * size_t(X_BYTES);
+    static constexpr size_t OFF_META = OFF_STAGE + NSS * size_t(STAGE_BYTES);
+    static constexpr size_t OFF_KP = OFF_META + NXS * size_t(META_BYTES);
     static constexpr size_t OFF_SCR = OFF_KP + 2 * size_t(KP_BYTES);
     static constexpr size_t OFF_BAR = (OFF_SCR + size_t(S_FLOATS) * 4 + 15) / 16 * 16;
     static constexpr int NBAR = 3 * NKS + 2 * NTS + 8 * 2 + 1;
@@ -117,12 +126,15 @@ struct PipeCfg {
     static_assert(NKS >= 2 * G, "shared-memory ring");
     static_assert(G * S == 2, "two accumulator chains per unit");
     static_assert(!COMMIT || TMAX <= 8, "the fused rollback serves T <= 8");
+    static_assert(!(COMMIT && TREE), "the fused rollback serves chains");
+    static_assert(!BIG || TREE, "T = 32 is the tree workload's size");
+    static_assert(!BIG || STAGE_BYTES >= 2 * TMAX * TMAX * 4, "the Gram block fits in the staging slot");
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
     static_assert(OFF_X % 1024 == 0 && X_BYTES % 1024 == 0, "swizzle atoms need 1024-byte bases");
     static_assert((RS * 4) % 16 == 0 && (M_V * 4) % 16 == 0 && (M_GP * 4) % 16 == 0 &&
                   (M_CW * 4) % 16 == 0, "records are read as float4, CW rows as 16-byte vectors");
     static_assert((KP_DL * 4) % 16 == 0 && (KP_KS * 4) % 16 == 0, "bulk-copy destinations");
-    static_assert(GRAM_TILES == 1 || GRAM_TILES == 4, "Gram block: one tile, or one tile per prep warp");
+    static_assert(GRAM_TILES == 1 || GRAM_TILES % 4 == 0, "Gram block: one tile, or a quarter per prep warp");
 };
 
 __device__ __forceinline__ void named_bar(int id, int nthreads) {
@@ -240,13 +252,14 @@ __device__ __forceinline__ void mma_tf32_16x8x8(float (&d)[4], const uint32_t (&
         : "r"(av[0]), "r"(av[1]), "r"(av[2]), "r"(av[3]), "r"(b0), "r"(b1));
 }
 
-template <typename IO, int TMAX, int G, bool COMMIT>
-__global__ void __launch_bounds__(PipeCfg<IO, TMAX, G, COMMIT>::NTHR, 1)
+template <typename IO, int TMAX, int G, bool COMMIT, bool TREE>
+__global__ void __launch_bounds__(PipeCfg<IO, TMAX, G, COMMIT, TREE>::NTHR, 1)
 gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap smap,
                        const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap cmap,
                        const __grid_constant__ CUtensorMap pmap, int n_units) {
-    using Cfg = PipeCfg<IO, TMAX, G, COMMIT>;
+    using Cfg = PipeCfg<IO, TMAX, G, COMMIT, TREE>;
     constexpr int D = Cfg::D, NP = Cfg::NP, XKB = Cfg::XKB, RS = Cfg::RS;
+    constexpr int NXS = Cfg::NXS, NSS = Cfg::NSS;
     constexpr int NKS = Cfg::NKS, NTS = Cfg::NTS;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = reinterpret_cast<unsigned char*>(
@@ -366,7 +379,7 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
             int l, b, kh;
             unit_of(iu, l, b, kh);
             const size_t lb = size_t(l) * B + b;
-            const int ss = iu & 1;
+            const int ss = iu % NSS;
             IO* qs = reinterpret_cast<IO*>(smem + Cfg::OFF_STAGE + size_t(ss) * Cfg::STAGE_BYTES);
             IO* cws = qs + size_t(Cfg::NPARTS) * NR * D;
             int n = 0;
@@ -378,7 +391,7 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
                 n = n_prev(b);
                 gv_next = prev_gate(iu + 1);
             }
-            if (!pwait_warp(&sempty[ss], ((iu >> 1) & 1) ^ 1, abort_flag, a.status)) break;
+            if (!pwait_warp(&sempty[ss], ((iu / NSS) & 1) ^ 1, abort_flag, a.status)) break;
             if (lane == 0) {
                 const int rows = (W - 1) + T + ((COMMIT && n > 0) ? W - 1 : 0);
                 mbar_arrive_expect_tx(&sfull[ss], uint32_t(Cfg::NPARTS * (rows * D + D * W) * Cfg::ES));
@@ -434,9 +447,9 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
             ++issued;
         }
         volatile int no_abort = 0;
-        for (int k = 1; k <= 2 && k <= issued; ++k) {
+        for (int k = 1; k <= NSS && k <= issued; ++k) {
             const int q = issued - k;
-            pwait_warp(&sfull[q & 1], uint32_t(q >> 1) & 1u, &no_abort, a.status);
+            pwait_warp(&sfull[q % NSS], uint32_t(q / NSS) & 1u, &no_abort, a.status);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------------------ mma (whole warp)
@@ -451,8 +464,8 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
         uint32_t tph = 0;
         bool ok = true;
         for (int iu = 0; iu < n_my && ok; ++iu) {
-            const int us = iu & 1, ps = iu % Cfg::NUS;
-            if (!pwait_warp(&ufull[us], (iu >> 1) & 1, abort_flag, a.status)) break;
+            const int us = iu % NXS, ps = iu % Cfg::NUS;
+            if (!pwait_warp(&ufull[us], (iu / NXS) & 1, abort_flag, a.status)) break;
             if (!pwait_warp(&tempty[ps], ((iu / Cfg::NUS) & 1) ^ 1, abort_flag, a.status)) break;
             const uint64_t db = umma_desc_sw128(sX0 + us * Cfg::X_BYTES);
             const uint32_t dt = tbase + ps * Cfg::P_COLS;
@@ -470,17 +483,34 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
                 for (int ks = 0; ks < 4; ++ks) {
                     const uint64_t bk = db + uint64_t((kb * XKB + ks * 32) >> 4);
                     const uint32_t acc = (kb > 0 || ks >= S) ? 1u : 0u;
+                    if constexpr (Cfg::BIG) {
+                        // one NP-column accumulator per chain: S_hi·X_hi, S_hi·X_lo, S_lo·X_hi
+                        const uint64_t bk_lo = bk + uint64_t((NP * 128) >> 4);
 #pragma unroll
-                    for (int j = 0; j < G; ++j) {
-                        const int c = j * S + ks % S;
-                        umma_tf32_ts_warp(dt + c * Cfg::CH_COLS, tbase + Cfg::T_RING + slot[j] * 64 + ks * 8,
-                                          bk, IDESC1, acc);
-                    }
+                        for (int j = 0; j < G; ++j)
+                            umma_tf32_ts_warp(dt + (j * S + ks % S) * Cfg::CH_COLS,
+                                              tbase + Cfg::T_RING + slot[j] * 64 + ks * 8, bk, IDESC2, acc);
 #pragma unroll
-                    for (int j = 0; j < G; ++j) {
-                        const int c = j * S + ks % S;
-                        umma_tf32_ts_warp(dt + c * Cfg::CH_COLS + 2 * NP,
-                                          tbase + Cfg::T_RING + slot[j] * 64 + 32 + ks * 8, bk, IDESC2, acc);
+                        for (int j = 0; j < G; ++j)
+                            umma_tf32_ts_warp(dt + (j * S + ks % S) * Cfg::CH_COLS,
+                                              tbase + Cfg::T_RING + slot[j] * 64 + ks * 8, bk_lo, IDESC2, 1u);
+#pragma unroll
+                        for (int j = 0; j < G; ++j)
+                            umma_tf32_ts_warp(dt + (j * S + ks % S) * Cfg::CH_COLS,
+                                              tbase + Cfg::T_RING + slot[j] * 64 + 32 + ks * 8, bk, IDESC2, 1u);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < G; ++j) {
+                            const int c = j * S + ks % S;
+                            umma_tf32_ts_warp(dt + c * Cfg::CH_COLS, tbase + Cfg::T_RING + slot[j] * 64 + ks * 8,
+                                              bk, IDESC1, acc);
+                        }
+#pragma unroll
+                        for (int j = 0; j < G; ++j) {
+                            const int c = j * S + ks % S;
+                            umma_tf32_ts_warp(dt + c * Cfg::CH_COLS + 2 * NP,
+                                              tbase + Cfg::T_RING + slot[j] * 64 + 32 + ks * 8, bk, IDESC2, acc);
+                        }
                     }
                 }
 #pragma unroll
@@ -507,7 +537,7 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
             int l, b, kh;
             unit_of(iu, l, b, kh);
             const size_t lb = size_t(l) * B + b;
-            const int ss = iu & 1, us = iu & 1;
+            const int ss = iu % NSS, us = iu % NXS;
             unsigned char* st = smem + Cfg::OFF_STAGE + size_t(ss) * Cfg::STAGE_BYTES;
             const IO* qs = reinterpret_cast<const IO*>(st);
             const IO* cws = qs + size_t(Cfg::NPARTS) * NR * D;
@@ -523,8 +553,107 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
             // conv window row r (0 .. W-2): old conv-state row r + n, or (COMMIT, r + n ≥ W-1) the
             // previous round's raw row staged at W-1+T+r
             const int n = n_prev(b);
-            pwait(&sfull[ss], (iu >> 1) & 1, abort_flag, a.status);
-            pwait(&uempty[us], ((iu >> 1) & 1) ^ 1, abort_flag, a.status);
+            int* par_s = reinterpret_cast<int*>(scr + Cfg::S_PAR);
+            int* win_s = reinterpret_cast<int*>(scr + Cfg::S_WIN);
+            if constexpr (TREE) {
+                // parents (a bad tree reports GDN_STATUS_BAD_PARENT and runs as a chain) and each
+                // node's conv window: itself, its nearest ancestors, then the conv state's rows
+                int* bad = win_s + 4 * TMAX;
+                const int pv = p < T ? __ldg(a.parent + size_t(b) * T + p) : 0;
+                if (p == 0) *bad = 0;
+                named_bar(1, 128);
+                if (p < T && (pv < -1 || pv >= p)) atomicOr(bad, 1);
+                named_bar(1, 128);
+                const int isbad = *bad;
+                if (p < T) par_s[p] = isbad ? p - 1 : pv;
+                if (isbad && p == 0) set_status(a.status, GDN_STATUS_BAD_PARENT);
+                named_bar(1, 128);
+                if (p < T) {
+                    int x = p, e = 0;
+#pragma unroll
+                    for (int d = 0; d < 4; ++d) {
+                        int src = -1;
+                        if (d < W) {
+                            if (x >= 0) { src = W - 1 + x; x = par_s[x]; }
+                            else { src = W - 2 - e; ++e; }
+                        }
+                        win_s[p * 4 + d] = src;
+                    }
+                }
+            }
+            pwait(&sfull[ss], (iu / NSS) & 1, abort_flag, a.status);
+            pwait(&uempty[us], ((iu / NXS) & 1) ^ 1, abort_flag, a.status);
+            if constexpr (TREE) {
+                named_bar(1, 128);      // windows written
+                // conv + SiLU over each node's window; raw k, q into B-tile rows t, TMAX + t (scaled
+                // in place below), v into the meta slot
+#pragma unroll 1
+                for (int part = 0; part < Cfg::NPARTS; ++part) {
+                    const IO* col = qs + size_t(part) * NR * D + p;
+                    const IO* wp = cws + (size_t(part) * D + p) * W;
+                    float wr[4];
+#pragma unroll
+                    for (int d = 0; d < 4; ++d) wr[d] = (d < W) ? io_to_f(wp[W - 1 - d]) : 0.f;
+#pragma unroll 4
+                    for (int t = 0; t < TMAX; ++t) {
+                        float y = 0.f;
+                        if (t < T) {
+                            float acc = 0.f;
+#pragma unroll
+                            for (int d = 3; d >= 0; --d) {
+                                const int src = win_s[t * 4 + d];
+                                if (src >= 0) acc = fmaf(wr[d], io_to_f(col[size_t(src) * D]), acc);
+                            }
+                            y = silu_fast(acc);
+                        }
+                        if (part == 0) *reinterpret_cast<float*>(Xb + sw128_off(TMAX + t, p, XKB)) = y;
+                        else if (part == 1) *reinterpret_cast<float*>(Xb + sw128_off(t, p, XKB)) = y;
+                        else meta[Cfg::M_V + ((part - 2) * TMAX + t) * D + p] = y;
+                    }
+                }
+                if (!Cfg::BIG) {
+                    named_bar(1, 128);
+                    if (p == 0) mbar_arrive(&sempty[ss]);     // every staged row has been read
+                }
+                // norms of the 2 TMAX rows (k then q), from the raw rows of this thread's channel
+#pragma unroll 1
+                for (int r0 = 0; r0 < 2 * TMAX; r0 += 32) {
+                    constexpr int NB = 2 * TMAX < 32 ? 2 * TMAX : 32;
+                    float sq[NB];
+#pragma unroll
+                    for (int e = 0; e < NB; ++e) {
+                        const float y = *reinterpret_cast<const float*>(Xb + sw128_off(r0 + e, p, XKB));
+                        sq[e] = y * y;
+                    }
+                    int ix;
+                    const float sv = warp_sum_many<NB>(sq, lane, &ix);
+                    if ((lane & (32 / NB - 1)) == 0) nrm[pw * 2 * TMAX + r0 + ix] = sv;
+                }
+                named_bar(1, 128);
+                if (p < 2 * TMAX)
+                    inv[p] = 1.0f / sqrtf(nrm[p] + nrm[2 * TMAX + p] + nrm[4 * TMAX + p] +
+                                          nrm[6 * TMAX + p] + a.l2_eps);
+                named_bar(1, 128);
+                // scale in place: rows r < NP hold X (the tensor core reads X_hi), rows NP + r X_lo
+#pragma unroll 4
+                for (int r = 0; r < 2 * TMAX; ++r) {
+                    float* xp = reinterpret_cast<float*>(Xb + sw128_off(r, p, XKB));
+                    const float x = *xp * inv[r];
+                    *xp = x;
+                    *reinterpret_cast<float*>(Xb + sw128_off(NP + r, p, XKB)) = x - tf32_trunc(x);
+                    if (r < T) a.tape_k[((lb * T + r) * Hk + kh) * size_t(D) + p] = x;
+                }
+#pragma unroll
+                for (int n2 = 2 * TMAX; n2 < NP; ++n2) {
+                    *reinterpret_cast<float*>(Xb + sw128_off(n2, p, XKB)) = 0.f;
+                    *reinterpret_cast<float*>(Xb + sw128_off(NP + n2, p, XKB)) = 0.f;
+                }
+                if (p < G * TMAX) {
+                    float* rec = meta + Cfg::M_REC + p * RS;
+                    rec[1] = g_in;
+                    rec[2] = b_in;
+                }
+            } else {
             // conv + SiLU of channel p of every part (one loop body for all parts keeps the code
             // small: q and k stay in registers, each v goes to the meta slot)
             float yq[TMAX], yk[TMAX];
@@ -620,13 +749,19 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
                 rec[1] = g_in;
                 rec[2] = b_in;
             }
+            }   // chain
             fence_async_smem();
             named_bar(1, 128);
+            // BIG: the Gram block lives in the staging slot (its rows have been read)
+            if constexpr (Cfg::BIG) gram = reinterpret_cast<float*>(st);
             // Gram block on the warp tensor path: D[m][n] = X_m · k_n, 3xTF32 (hi·hi + hi·lo + lo·hi);
             // rows m: k_0.., q_0.. (zero beyond 2 TMAX). One 16 x 8 tile: each warp takes 32 channels
             // and the partials are summed; four tiles (TMAX = 16): warp pw takes tile pw, all channels.
-            if constexpr (Cfg::GRAM_TILES == 4) {
-                const int mt = pw >> 1, nt = pw & 1;
+            if constexpr (Cfg::GRAM_TILES >= 4) {
+              constexpr int NTN = (TMAX + 7) / 8;
+#pragma unroll 1
+              for (int tt = pw; tt < Cfg::GRAM_TILES; tt += 4) {
+                const int mt = tt / NTN, nt = tt % NTN;
                 float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 4
                 for (int ks = 0; ks < 16; ++ks) {
@@ -658,6 +793,7 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
                 gram[(a0 + 1) * 2 * TMAX + c0] = acc[1];
                 gram[a0 * 2 * TMAX + c0 + 8] = acc[2];
                 gram[(a0 + 1) * 2 * TMAX + c0 + 8] = acc[3];
+              }
             } else {
               {
                 float acc[4] = {0.f, 0.f, 0.f, 0.f};
@@ -702,7 +838,24 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
             // CQ[v][x] = Γ(x→v-1) k_x·q_v for x < v; c0[v] = Γ(root→v-1) and k_v·q_v for x = v
             for (int idx = p; idx < G * TMAX * TMAX; idx += 128) {
                 const int fj = idx / (TMAX * TMAX), fv = (idx / TMAX) % TMAX, fx = idx % TMAX;
-                if (fv < T && fx <= fv) {
+                if (TREE && fv < T && fx <= fv) {
+                    // ancestors only: Γ(x→parent(v)) multiplies the gates from parent(v) up to x
+                    // (exclusive); x not on v's root path gives 0. c0[v]: every ancestor's gate.
+                    const float* hrec = meta + Cfg::M_REC + fj * TMAX * RS;     // γ at [y * RS + 1]
+                    float* rec = meta + Cfg::M_REC + (fj * TMAX + fv) * RS;
+                    float coef = 1.f;
+                    int y = par_s[fv];
+                    const int stop = fx < fv ? fx : -1;
+                    while (y > stop) { coef *= hrec[y * RS + 1]; y = par_s[y]; }
+                    if (fx < fv) {
+                        const bool anc = y == fx;
+                        rec[4 + fx] = anc ? coef * gram[fx * 2 * TMAX + fv] : 0.f;
+                        rec[4 + TMAX + fx] = anc ? coef * gram[fx * 2 * TMAX + TMAX + fv] : 0.f;
+                    } else {
+                        rec[0] = coef;
+                        rec[3] = gram[fv * 2 * TMAX + TMAX + fv];
+                    }
+                } else if (!TREE && fv < T && fx <= fv) {
                     const float* hrec = meta + Cfg::M_REC + fj * TMAX * RS;     // γ at [y * RS + 1]
                     float* rec = meta + Cfg::M_REC + (fj * TMAX + fv) * RS;
                     const int y0 = fx < fv ? fx + 1 : 0;
@@ -719,8 +872,12 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
                     }
                 }
             }
+            if constexpr (Cfg::BIG) fence_async_smem();      // Gram writes before the next TMA fill
             named_bar(1, 128);
-            if (p == 0) mbar_arrive(&ufull[us]);
+            if (p == 0) {
+                mbar_arrive(&ufull[us]);
+                if (Cfg::BIG) mbar_arrive(&sempty[ss]);      // the Gram block is done with it
+            }
         }
     } else if (warp < 10) {
         // ------------------------------------------------------------------ convert (128 threads)
@@ -878,12 +1035,12 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
             int l, b, kh;
             unit_of(iu, l, b, kh);
             const size_t lb = size_t(l) * B + b;
-            const int us = iu & 1;
+            const int us = iu % NXS;
             const float* meta = reinterpret_cast<const float*>(smem + Cfg::OFF_META + size_t(us) * Cfg::META_BYTES);
             const int n = n_prev(b);
             const float* kp = reinterpret_cast<const float*>(smem + Cfg::OFF_KP + size_t(iu & 1) * Cfg::KP_BYTES);
             if (COMMIT) pwait(&kpfull[iu & 1], (iu >> 1) & 1, abort_flag, a.status);
-            pwait(&ufull[us], (iu >> 1) & 1, abort_flag, a.status);
+            pwait(&ufull[us], (iu / NXS) & 1, abort_flag, a.status);
             if (COMMIT && n > 0) {
                 const int et = tid - 320, ew = warp - 10;
                 // the new conv-state rows, stashed by the prep warps, to HBM as 16-byte vectors
@@ -950,6 +1107,64 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
 #pragma unroll 1
             for (int j = 0; j < G; ++j) {
                 const int h = kh * G + j;
+                if constexpr (Cfg::BIG) {
+                    // P of this head: one accumulator per chain (k_t at column t, q_t at TMAX + t),
+                    // read 16 positions at a time; the coefficient rows are read 4 at a time
+                    const float* R = meta + Cfg::M_REC + j * TMAX * RS;
+                    const float* vv = meta + Cfg::M_V + size_t(j) * TMAX * D + i;
+                    float dl[TMAX];
+#pragma unroll
+                    for (int blk = 0; blk < TMAX / 16; ++blk) {
+                        float pk[16], pq[16];
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) { pk[e] = 0.f; pq[e] = 0.f; }
+#pragma unroll
+                        for (int sc = 0; sc < S; ++sc) {
+                            const uint32_t ca = dt + (j * S + sc) * Cfg::CH_COLS;
+                            float part[16];
+                            tmem_ld16(ca + 16 * blk, part);
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) pk[e] += part[e];
+                            tmem_ld16(ca + TMAX + 16 * blk, part);
+#pragma unroll
+                            for (int e = 0; e < 16; ++e) pq[e] += part[e];
+                        }
+                        if (blk == TMAX / 16 - 1 && j == G - 1) {
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(&tempty[ps]);
+                        }
+#pragma unroll
+                        for (int tt = 0; tt < 16; ++tt) {
+                            const int t = 16 * blk + tt;
+                            dl[t] = 0.f;
+                            if (t < T) {
+                                const float4 hd = *reinterpret_cast<const float4*>(R + t * RS);  // c0 γ β kq
+                                float sk = hd.x * pk[tt], sq = hd.x * pq[tt];
+#pragma unroll
+                                for (int q = 0; q < (t + 3) / 4; ++q) {
+                                    const float4 x = *reinterpret_cast<const float4*>(R + t * RS + 4 + 4 * q);
+                                    const float4 y = *reinterpret_cast<const float4*>(R + t * RS + 4 + TMAX + 4 * q);
+                                    const float xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+                                    for (int e = 0; e < 4; ++e) {
+                                        if (4 * q + e < t) {
+                                            sk = fmaf(xs[e], dl[4 * q + e], sk);
+                                            sq = fmaf(ys[e], dl[4 * q + e], sq);
+                                        }
+                                    }
+                                }
+                                const float u = hd.y * sk;
+                                const float d = hd.z * (vv[t * D] - u);
+                                dl[t] = d;
+                                const float o = scale * fmaf(d, hd.w, hd.y * sq);
+                                const size_t oi = ((lb * T + t) * Hv + h) * size_t(D) + i;
+                                a.tape_delta[oi] = d;
+                                IoTraits<IO>::store(out, oi, o);
+                            }
+                        }
+                    }
+                } else {
                 // P row i of this head: S_hi·X_hi + S_hi·X_lo + S_lo·X_hi over its chains
                 float pr[NP];
 #pragma unroll
@@ -1021,6 +1236,7 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
                         IoTraits<IO>::store(out, oi, o);
                     }
                 }
+                }
             }
             __syncwarp();
             if (lane == 0) {
@@ -1037,10 +1253,10 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
                      ::"r"(tbase), "r"(uint32_t(Cfg::TMEM_COLS)));
 }
 
-template <typename IO, int TMAX, int G, bool COMMIT>
+template <typename IO, int TMAX, int G, bool COMMIT, bool TREE = false>
 cudaError_t launch_verify_pipe_t(const VerifyArgs& a, const VerifyMaps& m, cudaStream_t stream) {
-    using Cfg = PipeCfg<IO, TMAX, G, COMMIT>;
-    auto kern = gdn_verify_pipe_kernel<IO, TMAX, G, COMMIT>;
+    using Cfg = PipeCfg<IO, TMAX, G, COMMIT, TREE>;
+    auto kern = gdn_verify_pipe_kernel<IO, TMAX, G, COMMIT, TREE>;
     static bool attr_done = false;   // benign race: setting the attribute twice is harmless
     static int nsm = 0;
     if (!attr_done) {
@@ -1061,25 +1277,33 @@ cudaError_t launch_verify_pipe_t(const VerifyArgs& a, const VerifyMaps& m, cudaS
     return cudaGetLastError();
 }
 
-// The pipelined kernel serves the Qwen3.6 head shape; everything else uses the per-head kernel.
+// The pipelined kernel serves the Qwen3.6 head shape (chains up to 16 positions, trees up to 32
+// nodes); everything else uses the per-head kernel.
 template <typename IO>
 bool verify_pipe_eligible(const VerifyArgs& a, const VerifyMaps& m, int D, bool tree, bool commit) {
-    return m.inputs_ok && !tree && D == 128 && sizeof(IO) == 2 && a.T <= (commit ? 8 : 16) &&
+    const int tmax = commit ? 8 : (tree ? 32 : 16);
+    return m.inputs_ok && !(tree && commit) && D == 128 && sizeof(IO) == 2 && a.T <= tmax &&
            (a.Hv == a.Hk || a.Hv == 2 * a.Hk);
 }
 
+template <typename IO, int TMAX, bool COMMIT, bool TREE>
+cudaError_t launch_verify_pipe_g(const VerifyArgs& a, const VerifyMaps& m, cudaStream_t s) {
+    return a.Hv == a.Hk ? launch_verify_pipe_t<IO, TMAX, 1, COMMIT, TREE>(a, m, s)
+                        : launch_verify_pipe_t<IO, TMAX, 2, COMMIT, TREE>(a, m, s);
+}
+
 template <typename IO, bool COMMIT>
-cudaError_t launch_verify_pipe(const VerifyArgs& a, const VerifyMaps& m, cudaStream_t s) {
-    const int G = a.Hv / a.Hk;
-    if (a.T <= 4)
-        return G == 1 ? launch_verify_pipe_t<IO, 4, 1, COMMIT>(a, m, s)
-                      : launch_verify_pipe_t<IO, 4, 2, COMMIT>(a, m, s);
-    if (COMMIT || a.T <= 8)
-        return G == 1 ? launch_verify_pipe_t<IO, 8, 1, COMMIT>(a, m, s)
-                      : launch_verify_pipe_t<IO, 8, 2, COMMIT>(a, m, s);
-    if constexpr (!COMMIT)
-        return G == 1 ? launch_verify_pipe_t<IO, 16, 1, false>(a, m, s)
-                      : launch_verify_pipe_t<IO, 16, 2, false>(a, m, s);
+cudaError_t launch_verify_pipe(const VerifyArgs& a, const VerifyMaps& m, bool tree, cudaStream_t s) {
+    if constexpr (!COMMIT) {
+        if (tree) {
+            if (a.T <= 8) return launch_verify_pipe_g<IO, 8, false, true>(a, m, s);
+            if (a.T <= 16) return launch_verify_pipe_g<IO, 16, false, true>(a, m, s);
+            return launch_verify_pipe_g<IO, 32, false, true>(a, m, s);
+        }
+    }
+    if (a.T <= 4) return launch_verify_pipe_g<IO, 4, COMMIT, false>(a, m, s);
+    if (COMMIT || a.T <= 8) return launch_verify_pipe_g<IO, 8, COMMIT, false>(a, m, s);
+    if constexpr (!COMMIT) return launch_verify_pipe_g<IO, 16, false, false>(a, m, s);
     return cudaErrorNotSupported;
 }
 

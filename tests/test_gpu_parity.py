@@ -226,17 +226,33 @@ def test_sample_accept_chi_square_gpu(gdnlib):
 
 
 # ------------------------------------------------------------------------------ tree
-def tree_case(B=3, T=12, D=32, L=2, depth=5, seed=0):
-    w = I.custom(I.WORKLOADS[4], name="tree_%d_%d_%d" % (B, T, D), L=L, B=B, N=T, Hk=2, Hv=4,
-                 D=D, V=512, tree_depth=depth)
+def tree_case(B=3, T=12, D=32, L=2, depth=5, seed=0, Hv=4, branch=None):
+    kw = {} if branch is None else {"tree_branch": branch}
+    w = I.custom(I.WORKLOADS[4], name="tree_%d_%d_%d_%d_%d" % (B, T, D, Hv, depth), L=L, B=B,
+                 N=T, Hk=2, Hv=Hv, D=D, V=512, tree_depth=depth, **kw)
     par = I.random_tree(w, 0, seed)
     return w, par
 
 
-@pytest.mark.parametrize("T,D", [(12, 32), (32, 64), (7, 128)])
-def test_tree_verify_matches_oracle(gdnlib, T, D):
-    w, par = tree_case(T=T, D=D, depth=min(8, T))
+# D = 128 bf16 trees run on the pipelined kernel (node counts up to 8, 16 and 32, one and two
+# value heads per key head, ragged counts); the others on the per-head kernel
+@pytest.mark.parametrize("T,D,Hv,depth", [(12, 32, 4, 8), (32, 64, 4, 8), (7, 128, 4, 7),
+                                          (16, 128, 4, 8), (13, 128, 2, 5), (32, 128, 4, 8),
+                                          (32, 128, 2, 6), (24, 128, 4, 3), (29, 128, 2, 12)])
+def test_tree_verify_matches_oracle(gdnlib, T, D, Hv, depth):
+    w, par = tree_case(T=T, D=D, depth=depth, Hv=Hv, B=4)
     run_verify_case(w, parent=par)
+
+
+@pytest.mark.parametrize("shape", ["chain", "star"])
+def test_tree_verify_degenerate_trees(gdnlib, shape):
+    """A tree that is one chain (every node the child of the one before) equals the chain
+    verify; a star (every node a child of the context) starts every node from S_0."""
+    T = 32
+    w, _ = tree_case(T=T, D=128, depth=T if shape == "chain" else 1, B=3, branch=T)
+    par = torch.arange(-1, T - 1, dtype=torch.int32) if shape == "chain" else \
+        torch.full((T,), -1, dtype=torch.int32)
+    run_verify_case(w, parent=par.repeat(w.B, 1).contiguous())
 
 
 def test_tree_accept_and_path_rollback(gdnlib):
@@ -262,8 +278,9 @@ def test_tree_accept_and_path_rollback(gdnlib):
     assert np.array_equal(f64(dcs), cs_ref)
 
 
-def test_tree_bad_parent_sets_status(gdnlib):
-    w, par = tree_case(B=2, T=6, D=32, depth=4)
+@pytest.mark.parametrize("T,D", [(6, 32), (20, 128)])
+def test_tree_bad_parent_sets_status(gdnlib, T, D):
+    w, par = tree_case(B=2, T=T, D=D, depth=4)
     par = par.clone()
     par[1, 3] = 5            # parent after the node
     cw, st, cs = make_model(w)
