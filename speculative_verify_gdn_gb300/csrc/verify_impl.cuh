@@ -204,8 +204,9 @@ gdn_verify_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap smap) 
     constexpr int NP = Cfg::NP, KB = Cfg::KB, XKB = Cfg::XKB, XS = Cfg::XP_STRIDE;
 
     extern __shared__ unsigned char smem_raw[];
-    unsigned char* smem = reinterpret_cast<unsigned char*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // 1024-byte aligned base, derived from the shared array itself so that every access stays
+    // a shared-memory access for the compiler
+    unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     unsigned char* Xb = smem + Cfg::OFF_X;          // B tile: [K-block][X_hi rows; X_lo rows]
     unsigned char* As = smem + Cfg::OFF_A;          // S_0 tile (then S_lo)
     float* mf = reinterpret_cast<float*>(smem + Cfg::OFF_MF);

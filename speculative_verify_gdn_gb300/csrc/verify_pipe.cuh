@@ -77,11 +77,20 @@ struct PipeCfg {
     static constexpr int NRMAX = 3 + TMAX + (COMMIT ? 3 : 0);
     static constexpr int RAW_BYTES = NPARTS * NRMAX * D * ES + NPARTS * D * 4 * ES;
     static constexpr int STAGE_BYTES = (RAW_BYTES + 127) / 128 * 128;
-    // meta slot (floats): per value head j and position t a record {c0, γ, β, k_t·q_t, CK[TMAX],
-    // CQ[TMAX]} (16-byte aligned), the conv outputs V[G][TMAX][D] and, COMMIT, GP[s][c] = k'_s·X_c
-    // of the previous round's k'_s and the new conv-state rows CW[NPARTS][3][D] (io type)
-    static constexpr int RS = 4 + 2 * TMAX;
-    static constexpr int M_REC = 0, M_V = G * TMAX * RS, M_GP = M_V + G * TMAX * D,
+    // meta slot (floats): per value head j and position t a record {c0, γ, β, k_t·q_t, (TREE)
+    // c0q, group mask, 0, 0, CK[TMAX], CQ[TMAX]} (16-byte aligned), the conv outputs V[G][TMAX][D]
+    // and, COMMIT, GP[s][c] = k'_s·X_c of the previous round's k'_s and the new conv-state rows
+    // CW[NPARTS][3][D] (io type). Trees keep raw (unnormalised) q, k in the B tile: c0 and c0q
+    // carry 1/|k_t| and 1/|q_t|, and bit g of the mask is set when CK / CQ entries 4g .. 4g+3 can
+    // be nonzero (ancestors only).
+    // BIG (T = 32 trees) uses a per-head block instead: fields c0k, c0q, γ, β, k·q [5][TMAX], then
+    // CK and CQ transposed ([x][t], the epilogue pushes δ_x into every later t)
+    static constexpr int HDR = TREE ? 8 : 4;
+    static constexpr int RS = HDR + 2 * TMAX;
+    static constexpr int RJ = BIG ? 5 * TMAX + 2 * TMAX * TMAX : TMAX * RS;
+    static constexpr int F_C0K = 0, F_C0Q = TMAX, F_GAM = 2 * TMAX, F_BET = 3 * TMAX, F_KQ = 4 * TMAX,
+                         F_CKT = 5 * TMAX, F_CQT = 5 * TMAX + TMAX * TMAX;
+    static constexpr int M_REC = 0, M_V = G * RJ, M_GP = M_V + G * TMAX * D,
                          M_CW = M_GP + (COMMIT ? 2 * TMAX * TMAX : 0),
                          M_FLOATS = M_CW + (COMMIT ? (NPARTS * 3 * D * ES + 3) / 4 : 0);
     static constexpr int META_BYTES = (M_FLOATS * 4 + 127) / 128 * 128;
@@ -131,7 +140,7 @@ struct PipeCfg {
     static_assert(!BIG || STAGE_BYTES >= 2 * TMAX * TMAX * 4, "the Gram block fits in the staging slot");
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
     static_assert(OFF_X % 1024 == 0 && X_BYTES % 1024 == 0, "swizzle atoms need 1024-byte bases");
-    static_assert((RS * 4) % 16 == 0 && (M_V * 4) % 16 == 0 && (M_GP * 4) % 16 == 0 &&
+    static_assert((RS * 4) % 16 == 0 && (RJ * 4) % 16 == 0 && (M_V * 4) % 16 == 0 && (M_GP * 4) % 16 == 0 &&
                   (M_CW * 4) % 16 == 0, "records are read as float4, CW rows as 16-byte vectors");
     static_assert((KP_DL * 4) % 16 == 0 && (KP_KS * 4) % 16 == 0, "bulk-copy destinations");
     static_assert(GRAM_TILES == 1 || GRAM_TILES % 4 == 0, "Gram block: one tile, or a quarter per prep warp");
@@ -252,6 +261,27 @@ __device__ __forceinline__ void mma_tf32_16x8x8(float (&d)[4], const uint32_t (&
         : "r"(av[0]), "r"(av[1]), "r"(av[2]), "r"(av[3]), "r"(b0), "r"(b1));
 }
 
+// 1/sqrt(s) for s > 0: the hardware approximation refined by one Newton-Raphson step
+// (y <- y (3 - s y^2) / 2), a few ulp from the correctly rounded value
+__device__ __forceinline__ float inv_sqrt_nr(float s) {
+    float y;
+    asm("rsqrt.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(s));
+    return y * fmaf(-0.5f * s * y, y, 1.5f);
+}
+
+// p + n, hidden from the compiler's address arithmetic: a fully unrolled loop of stores then
+// advances one pointer instead of holding every iteration's 64-bit address in registers
+template <typename P>
+__device__ __forceinline__ P* opaque_advance(P* p, size_t n) {
+    P* q = p + n;
+    asm volatile("" : "+l"(q));
+    return q;
+}
+
+// two bf16 values packed in a 32-bit word (element 0 in the low half) to floats (exact)
+__device__ __forceinline__ float bf2_lo(uint32_t u) { return __uint_as_float(u << 16); }
+__device__ __forceinline__ float bf2_hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
+
 template <typename IO, int TMAX, int G, bool COMMIT, bool TREE>
 __global__ void __launch_bounds__(PipeCfg<IO, TMAX, G, COMMIT, TREE>::NTHR, 1)
 gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap smap,
@@ -262,8 +292,9 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
     constexpr int NXS = Cfg::NXS, NSS = Cfg::NSS;
     constexpr int NKS = Cfg::NKS, NTS = Cfg::NTS;
     extern __shared__ unsigned char smem_raw[];
-    unsigned char* smem = reinterpret_cast<unsigned char*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // 1024-byte aligned base, derived from the shared array itself so that every access stays
+    // a shared-memory access for the compiler
+    unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::OFF_BAR);
     uint64_t* kfull = bars;                      // K-block landed in its shared-memory slot
     uint64_t* kempty = kfull + NKS;              // slot free: read by the 4 convert warps, or
@@ -568,16 +599,18 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
                 if (p < T) par_s[p] = isbad ? p - 1 : pv;
                 if (isbad && p == 0) set_status(a.status, GDN_STATUS_BAD_PARENT);
                 named_bar(1, 128);
-                if (p < T) {
-                    int x = p, e = 0;
+                // stored as element offsets of the staged rows; taps d >= W (weight 0) and nodes
+                // past T point at a valid row (the node's own, or row 0)
+                if (p < TMAX) {
+                    int x = p < T ? p : -1, e = 0;
 #pragma unroll
                     for (int d = 0; d < 4; ++d) {
-                        int src = -1;
-                        if (d < W) {
+                        int src = p < T ? W - 1 + p : 0;
+                        if (d < W && p < T) {
                             if (x >= 0) { src = W - 1 + x; x = par_s[x]; }
                             else { src = W - 2 - e; ++e; }
                         }
-                        win_s[p * 4 + d] = src;
+                        win_s[p * 4 + d] = src * D;
                     }
                 }
             }
@@ -585,63 +618,72 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
             pwait(&uempty[us], ((iu / NXS) & 1) ^ 1, abort_flag, a.status);
             if constexpr (TREE) {
                 named_bar(1, 128);      // windows written
-                // conv + SiLU over each node's window; raw k, q into B-tile rows t, TMAX + t (scaled
-                // in place below), v into the meta slot
-#pragma unroll 1
-                for (int part = 0; part < Cfg::NPARTS; ++part) {
-                    const IO* col = qs + size_t(part) * NR * D + p;
-                    const IO* wp = cws + (size_t(part) * D + p) * W;
-                    float wr[4];
+                // conv + SiLU over each node's window: thread p takes channels 2 (p mod 64) + {0, 1}
+                // of parts 2 (p / 64) + {0, 1} (q, k | v heads), 8 independent bf16-pair loads
+                // per node. Raw k, q (and their tf32 remainders) go to B-tile rows t, TMAX + t.
+                static_assert(sizeof(IO) == 2, "the tree conv reads bf16 pairs");
+                {
+                    const int half = p >> 6, c2 = 2 * (p & 63);
+                    constexpr int NPH = 2;                       // parts per thread
+                    float wr[NPH][4][2];
+                    bool on[NPH];
 #pragma unroll
-                    for (int d = 0; d < 4; ++d) wr[d] = (d < W) ? io_to_f(wp[W - 1 - d]) : 0.f;
-#pragma unroll 4
+                    for (int k = 0; k < NPH; ++k) {
+                        const int part = 2 * half + k;
+                        on[k] = part < Cfg::NPARTS;
+                        const IO* wp = cws + (size_t(on[k] ? part : 0) * D + c2) * W;
+#pragma unroll
+                        for (int d = 0; d < 4; ++d)
+#pragma unroll
+                            for (int c = 0; c < 2; ++c)
+                                wr[k][d][c] = (d < W && on[k]) ? io_to_f(wp[c * W + W - 1 - d]) : 0.f;
+                    }
+                    const int4* win4 = reinterpret_cast<const int4*>(win_s);
+#pragma unroll 2
                     for (int t = 0; t < TMAX; ++t) {
-                        float y = 0.f;
-                        if (t < T) {
-                            float acc = 0.f;
+                        const int4 w4 = win4[t];
+                        const int src[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+                        for (int k = 0; k < NPH; ++k) {
+                            const int part = 2 * half + k;
+                            const IO* col = qs + size_t(on[k] ? part : 0) * NR * D + c2;
+                            float a0 = 0.f, a1 = 0.f;
 #pragma unroll
                             for (int d = 3; d >= 0; --d) {
-                                const int src = win_s[t * 4 + d];
-                                if (src >= 0) acc = fmaf(wr[d], io_to_f(col[size_t(src) * D]), acc);
+                                const uint32_t u = *reinterpret_cast<const uint32_t*>(col + src[d]);
+                                a0 = fmaf(wr[k][d][0], bf2_lo(u), a0);
+                                a1 = fmaf(wr[k][d][1], bf2_hi(u), a1);
                             }
-                            y = silu_fast(acc);
+                            const float y0 = t < T ? silu_fast(a0) : 0.f, y1 = t < T ? silu_fast(a1) : 0.f;
+                            if (!on[k]) continue;
+                            if (part < 2) {
+                                const int r = part == 0 ? TMAX + t : t;
+                                *reinterpret_cast<float2*>(Xb + sw128_off(r, c2, XKB)) = make_float2(y0, y1);
+                                *reinterpret_cast<float2*>(Xb + sw128_off(NP + r, c2, XKB)) =
+                                    make_float2(y0 - tf32_trunc(y0), y1 - tf32_trunc(y1));
+                            } else {
+                                *reinterpret_cast<float2*>(meta + Cfg::M_V + ((part - 2) * TMAX + t) * D + c2) =
+                                    make_float2(y0, y1);
+                            }
                         }
-                        if (part == 0) *reinterpret_cast<float*>(Xb + sw128_off(TMAX + t, p, XKB)) = y;
-                        else if (part == 1) *reinterpret_cast<float*>(Xb + sw128_off(t, p, XKB)) = y;
-                        else meta[Cfg::M_V + ((part - 2) * TMAX + t) * D + p] = y;
                     }
                 }
-                if (!Cfg::BIG) {
-                    named_bar(1, 128);
-                    if (p == 0) mbar_arrive(&sempty[ss]);     // every staged row has been read
-                }
-                // norms of the 2 TMAX rows (k then q), from the raw rows of this thread's channel
-#pragma unroll 1
-                for (int r0 = 0; r0 < 2 * TMAX; r0 += 32) {
-                    constexpr int NB = 2 * TMAX < 32 ? 2 * TMAX : 32;
-                    float sq[NB];
-#pragma unroll
-                    for (int e = 0; e < NB; ++e) {
-                        const float y = *reinterpret_cast<const float*>(Xb + sw128_off(r0 + e, p, XKB));
-                        sq[e] = y * y;
-                    }
-                    int ix;
-                    const float sv = warp_sum_many<NB>(sq, lane, &ix);
-                    if ((lane & (32 / NB - 1)) == 0) nrm[pw * 2 * TMAX + r0 + ix] = sv;
-                }
                 named_bar(1, 128);
-                if (p < 2 * TMAX)
-                    inv[p] = 1.0f / sqrtf(nrm[p] + nrm[2 * TMAX + p] + nrm[4 * TMAX + p] +
-                                          nrm[6 * TMAX + p] + a.l2_eps);
-                named_bar(1, 128);
-                // scale in place: rows r < NP hold X (the tensor core reads X_hi), rows NP + r X_lo
+                if (!Cfg::BIG && p == 0) mbar_arrive(&sempty[ss]);     // every staged row has been read
+                // norms: warp pw takes rows pw, pw + 4, ..; lane = 4 channels (one 16-byte chunk).
+                // The tape keeps the normalised k; the B tile stays raw (the coefficients and the
+                // epilogue apply the inverse norms).
 #pragma unroll 4
-                for (int r = 0; r < 2 * TMAX; ++r) {
-                    float* xp = reinterpret_cast<float*>(Xb + sw128_off(r, p, XKB));
-                    const float x = *xp * inv[r];
-                    *xp = x;
-                    *reinterpret_cast<float*>(Xb + sw128_off(NP + r, p, XKB)) = x - tf32_trunc(x);
-                    if (r < T) a.tape_k[((lb * T + r) * Hk + kh) * size_t(D) + p] = x;
+                for (int r = pw; r < 2 * TMAX; r += 4) {
+                    const float4 x = *reinterpret_cast<const float4*>(Xb + sw128_off(r, 4 * lane, XKB));
+                    float sv = x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w;
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) sv += __shfl_xor_sync(0xffffffffu, sv, o);
+                    const float iv = inv_sqrt_nr(sv + a.l2_eps);
+                    if (lane == 0) inv[r] = iv;
+                    if (r < T)
+                        *reinterpret_cast<float4*>(a.tape_k + ((lb * T + r) * Hk + kh) * size_t(D) + 4 * lane) =
+                            make_float4(x.x * iv, x.y * iv, x.z * iv, x.w * iv);
                 }
 #pragma unroll
                 for (int n2 = 2 * TMAX; n2 < NP; ++n2) {
@@ -649,9 +691,14 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
                     *reinterpret_cast<float*>(Xb + sw128_off(NP + n2, p, XKB)) = 0.f;
                 }
                 if (p < G * TMAX) {
-                    float* rec = meta + Cfg::M_REC + p * RS;
-                    rec[1] = g_in;
-                    rec[2] = b_in;
+                    if constexpr (Cfg::BIG) {
+                        meta[Cfg::M_REC + gj * Cfg::RJ + Cfg::F_GAM + gt] = g_in;
+                        meta[Cfg::M_REC + gj * Cfg::RJ + Cfg::F_BET + gt] = b_in;
+                    } else {
+                        float* rec = meta + Cfg::M_REC + p * RS;
+                        rec[1] = g_in;
+                        rec[2] = b_in;
+                    }
                 }
             } else {
             // conv + SiLU of channel p of every part (one loop body for all parts keeps the code
@@ -758,41 +805,59 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
             // rows m: k_0.., q_0.. (zero beyond 2 TMAX). One 16 x 8 tile: each warp takes 32 channels
             // and the partials are summed; four tiles (TMAX = 16): warp pw takes tile pw, all channels.
             if constexpr (Cfg::GRAM_TILES >= 4) {
-              constexpr int NTN = (TMAX + 7) / 8;
-#pragma unroll 1
-              for (int tt = pw; tt < Cfg::GRAM_TILES; tt += 4) {
-                const int mt = tt / NTN, nt = tt % NTN;
-                float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-                for (int ks = 0; ks < 16; ++ks) {
-                    const int ch = 8 * ks + gt4;
+              // a warp's tiles (one, or four sharing the column block k_{8 pw ..}) in one pass over
+              // the channels, hi·hi + lo·hi and hi·lo in separate accumulators: 2 TPW independent
+              // chains
+              constexpr int NTN = (TMAX + 7) / 8, TPW = Cfg::GRAM_TILES / 4;
+              static_assert(TPW == 1 || NTN == 4, "a warp's tiles share their column block");
+              const int nt = pw % NTN;
+              float acc[TPW][4], acl[TPW][4];
+#pragma unroll
+              for (int m = 0; m < TPW; ++m)
+#pragma unroll
+                  for (int e = 0; e < 4; ++e) { acc[m][e] = 0.f; acl[m][e] = 0.f; }
+#pragma unroll 2
+              for (int ks = 0; ks < 16; ++ks) {
+                const int ch = 8 * ks + gt4;
+                const float bv0 = *reinterpret_cast<const float*>(Xb + sw128_off(8 * nt + gq, ch, XKB));
+                const float bv1 = *reinterpret_cast<const float*>(Xb + sw128_off(8 * nt + gq, ch + 4, XKB));
+                const float bh0 = tf32_trunc(bv0), bh1 = tf32_trunc(bv1);
+                const uint32_t bl0 = __float_as_uint(tf32_trunc(bv0 - bh0));
+                const uint32_t bl1 = __float_as_uint(tf32_trunc(bv1 - bh1));
+                uint32_t ahi[TPW][4], alo[TPW][4];
+#pragma unroll
+                for (int m = 0; m < TPW; ++m) {
+                    const int mt = TPW == 1 ? pw / NTN : m;
                     float av[4];
                     av[0] = *reinterpret_cast<const float*>(Xb + sw128_off(16 * mt + gq, ch, XKB));
                     av[2] = *reinterpret_cast<const float*>(Xb + sw128_off(16 * mt + gq, ch + 4, XKB));
                     av[1] = *reinterpret_cast<const float*>(Xb + sw128_off(16 * mt + gq + 8, ch, XKB));
                     av[3] = *reinterpret_cast<const float*>(Xb + sw128_off(16 * mt + gq + 8, ch + 4, XKB));
-                    const float bv0 = *reinterpret_cast<const float*>(Xb + sw128_off(8 * nt + gq, ch, XKB));
-                    const float bv1 = *reinterpret_cast<const float*>(Xb + sw128_off(8 * nt + gq, ch + 4, XKB));
-                    uint32_t ahi[4], alo[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const float h = tf32_trunc(av[e]);
-                        ahi[e] = __float_as_uint(h);
-                        alo[e] = __float_as_uint(tf32_trunc(av[e] - h));
+                        ahi[m][e] = __float_as_uint(h);
+                        alo[m][e] = __float_as_uint(tf32_trunc(av[e] - h));
                     }
-                    const float bh0 = tf32_trunc(bv0), bh1 = tf32_trunc(bv1);
-                    const uint32_t bl0 = __float_as_uint(tf32_trunc(bv0 - bh0));
-                    const uint32_t bl1 = __float_as_uint(tf32_trunc(bv1 - bh1));
-                    mma_tf32_16x8x8(acc, ahi, __float_as_uint(bh0), __float_as_uint(bh1));
-                    mma_tf32_16x8x8(acc, ahi, bl0, bl1);
-                    mma_tf32_16x8x8(acc, alo, __float_as_uint(bh0), __float_as_uint(bh1));
                 }
-                // Gr[a][c] = k_a · X_c = D[c][a]
+#pragma unroll
+                for (int m = 0; m < TPW; ++m) {
+                    mma_tf32_16x8x8(acc[m], ahi[m], __float_as_uint(bh0), __float_as_uint(bh1));
+                    mma_tf32_16x8x8(acl[m], ahi[m], bl0, bl1);
+                }
+#pragma unroll
+                for (int m = 0; m < TPW; ++m)
+                    mma_tf32_16x8x8(acc[m], alo[m], __float_as_uint(bh0), __float_as_uint(bh1));
+              }
+              // Gr[a][c] = k_a · X_c = D[c][a]
+#pragma unroll
+              for (int m = 0; m < TPW; ++m) {
+                const int mt = TPW == 1 ? pw / NTN : m;
                 const int c0 = 16 * mt + gq, a0 = 8 * nt + 2 * gt4;
-                gram[a0 * 2 * TMAX + c0] = acc[0];
-                gram[(a0 + 1) * 2 * TMAX + c0] = acc[1];
-                gram[a0 * 2 * TMAX + c0 + 8] = acc[2];
-                gram[(a0 + 1) * 2 * TMAX + c0 + 8] = acc[3];
+                gram[a0 * 2 * TMAX + c0] = acc[m][0] + acl[m][0];
+                gram[(a0 + 1) * 2 * TMAX + c0] = acc[m][1] + acl[m][1];
+                gram[a0 * 2 * TMAX + c0 + 8] = acc[m][2] + acl[m][2];
+                gram[(a0 + 1) * 2 * TMAX + c0 + 8] = acc[m][3] + acl[m][3];
               }
             } else {
               {
@@ -834,28 +899,71 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
               }
             }
             named_bar(1, 128);
+            if constexpr (TREE) {
+                // per (value head, node v): walk v's ancestors x (nearest first). CK[v][x] =
+                // Γ(x→v) k_x·k_v and CQ[v][x] = Γ(x→v) k_x·q_v, with Γ(x→v) the gates of the
+                // ancestors strictly between x and v; zero for every other x. c0 = every
+                // ancestor's gate. The Gram block is raw: the inverse norms are applied here.
+                if constexpr (Cfg::BIG) {
+                    constexpr int NZ = 2 * TMAX * TMAX / 4;          // CK, CQ of one head in float4
+#pragma unroll 1
+                    for (int z = p; z < G * NZ; z += 128) {
+                        const int zj = z / NZ;
+                        reinterpret_cast<float4*>(meta + Cfg::M_REC + zj * Cfg::RJ + Cfg::F_CKT)[z - zj * NZ] =
+                            make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+                    named_bar(1, 128);
+                    for (int idx = p; idx < G * TMAX; idx += 128) {
+                        const int fj = idx / TMAX, fv = idx - fj * TMAX;
+                        if (fv >= T) continue;
+                        float* hb = meta + Cfg::M_REC + fj * Cfg::RJ;
+                        const float ik = inv[fv], iq = inv[TMAX + fv];
+                        float coef = 1.f;
+                        int y = par_s[fv];
+                        while (y >= 0) {
+                            const float iy = inv[y] * coef;
+                            hb[Cfg::F_CKT + y * TMAX + fv] = iy * ik * gram[y * 2 * TMAX + fv];
+                            hb[Cfg::F_CQT + y * TMAX + fv] = iy * iq * gram[y * 2 * TMAX + TMAX + fv];
+                            coef *= hb[Cfg::F_GAM + y];
+                            y = par_s[y];
+                        }
+                        hb[Cfg::F_C0K + fv] = coef * ik;
+                        hb[Cfg::F_C0Q + fv] = coef * iq;
+                        hb[Cfg::F_KQ + fv] = gram[fv * 2 * TMAX + TMAX + fv] * ik * iq;
+                    }
+                } else
+                for (int idx = p; idx < G * TMAX; idx += 128) {
+                    const int fj = idx / TMAX, fv = idx - fj * TMAX;
+                    if (fv < T) {
+                        const float* hrec = meta + Cfg::M_REC + fj * TMAX * RS;     // γ at [y * RS + 1]
+                        float* rec = meta + Cfg::M_REC + idx * RS;
+                        float4* cz = reinterpret_cast<float4*>(rec + Cfg::HDR);
+#pragma unroll
+                        for (int z = 0; z < 2 * TMAX / 4; ++z) cz[z] = make_float4(0.f, 0.f, 0.f, 0.f);
+                        const float ik = inv[fv], iq = inv[TMAX + fv];
+                        float coef = 1.f;
+                        unsigned gmask = 0;
+                        int y = par_s[fv];
+                        while (y >= 0) {
+                            const float iy = inv[y] * coef;
+                            rec[Cfg::HDR + y] = iy * ik * gram[y * 2 * TMAX + fv];
+                            rec[Cfg::HDR + TMAX + y] = iy * iq * gram[y * 2 * TMAX + TMAX + fv];
+                            gmask |= 1u << (y >> 2);
+                            coef *= hrec[y * RS + 1];
+                            y = par_s[y];
+                        }
+                        rec[0] = coef * ik;
+                        rec[3] = gram[fv * 2 * TMAX + TMAX + fv] * ik * iq;
+                        rec[4] = coef * iq;
+                        rec[5] = __uint_as_float(gmask);
+                    }
+                }
+            } else {
             // per value head, one thread per (v, x ≤ v): CK[v][x] = Γ(x→v-1) k_x·k_v and
             // CQ[v][x] = Γ(x→v-1) k_x·q_v for x < v; c0[v] = Γ(root→v-1) and k_v·q_v for x = v
             for (int idx = p; idx < G * TMAX * TMAX; idx += 128) {
                 const int fj = idx / (TMAX * TMAX), fv = (idx / TMAX) % TMAX, fx = idx % TMAX;
-                if (TREE && fv < T && fx <= fv) {
-                    // ancestors only: Γ(x→parent(v)) multiplies the gates from parent(v) up to x
-                    // (exclusive); x not on v's root path gives 0. c0[v]: every ancestor's gate.
-                    const float* hrec = meta + Cfg::M_REC + fj * TMAX * RS;     // γ at [y * RS + 1]
-                    float* rec = meta + Cfg::M_REC + (fj * TMAX + fv) * RS;
-                    float coef = 1.f;
-                    int y = par_s[fv];
-                    const int stop = fx < fv ? fx : -1;
-                    while (y > stop) { coef *= hrec[y * RS + 1]; y = par_s[y]; }
-                    if (fx < fv) {
-                        const bool anc = y == fx;
-                        rec[4 + fx] = anc ? coef * gram[fx * 2 * TMAX + fv] : 0.f;
-                        rec[4 + TMAX + fx] = anc ? coef * gram[fx * 2 * TMAX + TMAX + fv] : 0.f;
-                    } else {
-                        rec[0] = coef;
-                        rec[3] = gram[fv * 2 * TMAX + TMAX + fv];
-                    }
-                } else if (!TREE && fv < T && fx <= fv) {
+                if (fv < T && fx <= fv) {
                     const float* hrec = meta + Cfg::M_REC + fj * TMAX * RS;     // γ at [y * RS + 1]
                     float* rec = meta + Cfg::M_REC + (fj * TMAX + fv) * RS;
                     const int y0 = fx < fv ? fx + 1 : 0;
@@ -871,6 +979,7 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
                         rec[3] = gram[fv * 2 * TMAX + TMAX + fv];
                     }
                 }
+            }
             }
             if constexpr (Cfg::BIG) fence_async_smem();      // Gram writes before the next TMA fill
             named_bar(1, 128);
@@ -1108,59 +1217,102 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
             for (int j = 0; j < G; ++j) {
                 const int h = kh * G + j;
                 if constexpr (Cfg::BIG) {
-                    // P of this head: one accumulator per chain (k_t at column t, q_t at TMAX + t),
-                    // read 16 positions at a time; the coefficient rows are read 4 at a time
-                    const float* R = meta + Cfg::M_REC + j * TMAX * RS;
+                    // P of this head (one accumulator per chain: k_t at column t, q_t at TMAX + t),
+                    // 16 positions at a time. First the deltas: ak[t] = c0k_t P_k[t] + Σ_x CK[t][x]
+                    // δ_x takes the earlier blocks' δ as independent products, then inside the
+                    // block each δ_t is pushed into the later t as soon as it is known. Then the
+                    // outputs: aq[t] = c0q_t P_q[t] + Σ_x CQ[t][x] δ_x, every δ known, no serial
+                    // dependence. Positions t >= T are computed and never stored (their
+                    // coefficients are zero; nothing flows back to t < T).
+                    const float* hb = meta + Cfg::M_REC + j * Cfg::RJ;
                     const float* vv = meta + Cfg::M_V + size_t(j) * TMAX * D + i;
+                    const size_t ostep = size_t(Hv) * D;                 // next position, same head
+                    float* tdp = a.tape_delta + (lb * T * Hv + h) * size_t(D) + i;
+                    IO* op = out + (lb * T * Hv + h) * size_t(D) + i;
                     float dl[TMAX];
 #pragma unroll
                     for (int blk = 0; blk < TMAX / 16; ++blk) {
-                        float pk[16], pq[16];
+                        const uint32_t ca = dt + (j * S) * Cfg::CH_COLS + 16 * blk;
+                        {
+                            float ak[16];
+                            tmem_ld16(ca, ak);
 #pragma unroll
-                        for (int e = 0; e < 16; ++e) { pk[e] = 0.f; pq[e] = 0.f; }
+                            for (int sc = 1; sc < S; ++sc) {          // the odd K-step chain
+                                float pp[16];
+                                tmem_ld16(ca + sc * Cfg::CH_COLS, pp);
 #pragma unroll
-                        for (int sc = 0; sc < S; ++sc) {
-                            const uint32_t ca = dt + (j * S + sc) * Cfg::CH_COLS;
-                            float part[16];
-                            tmem_ld16(ca + 16 * blk, part);
+                                for (int e = 0; e < 16; ++e) ak[e] += pp[e];
+                            }
 #pragma unroll
-                            for (int e = 0; e < 16; ++e) pk[e] += part[e];
-                            tmem_ld16(ca + TMAX + 16 * blk, part);
+                            for (int t4 = 0; t4 < 4; ++t4) {
+                                const float4 ck = *reinterpret_cast<const float4*>(hb + Cfg::F_C0K + 16 * blk + 4 * t4);
+                                ak[4 * t4] *= ck.x; ak[4 * t4 + 1] *= ck.y; ak[4 * t4 + 2] *= ck.z; ak[4 * t4 + 3] *= ck.w;
+                            }
 #pragma unroll
-                            for (int e = 0; e < 16; ++e) pq[e] += part[e];
-                        }
-                        if (blk == TMAX / 16 - 1 && j == G - 1) {
-                            tc_fence_before();
-                            __syncwarp();
-                            if (lane == 0) mbar_arrive(&tempty[ps]);
-                        }
+                            for (int x = 0; x < 16 * blk; ++x) {
 #pragma unroll
-                        for (int tt = 0; tt < 16; ++tt) {
-                            const int t = 16 * blk + tt;
-                            dl[t] = 0.f;
-                            if (t < T) {
-                                const float4 hd = *reinterpret_cast<const float4*>(R + t * RS);  // c0 γ β kq
-                                float sk = hd.x * pk[tt], sq = hd.x * pq[tt];
-#pragma unroll
-                                for (int q = 0; q < (t + 3) / 4; ++q) {
-                                    const float4 x = *reinterpret_cast<const float4*>(R + t * RS + 4 + 4 * q);
-                                    const float4 y = *reinterpret_cast<const float4*>(R + t * RS + 4 + TMAX + 4 * q);
-                                    const float xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
-#pragma unroll
-                                    for (int e = 0; e < 4; ++e) {
-                                        if (4 * q + e < t) {
-                                            sk = fmaf(xs[e], dl[4 * q + e], sk);
-                                            sq = fmaf(ys[e], dl[4 * q + e], sq);
-                                        }
-                                    }
+                                for (int g4 = 0; g4 < 4; ++g4) {
+                                    const float4 xk = *reinterpret_cast<const float4*>(hb + Cfg::F_CKT + x * TMAX + 16 * blk + 4 * g4);
+                                    ak[4 * g4] = fmaf(xk.x, dl[x], ak[4 * g4]);
+                                    ak[4 * g4 + 1] = fmaf(xk.y, dl[x], ak[4 * g4 + 1]);
+                                    ak[4 * g4 + 2] = fmaf(xk.z, dl[x], ak[4 * g4 + 2]);
+                                    ak[4 * g4 + 3] = fmaf(xk.w, dl[x], ak[4 * g4 + 3]);
                                 }
-                                const float u = hd.y * sk;
-                                const float d = hd.z * (vv[t * D] - u);
+                            }
+#pragma unroll
+                            for (int tt = 0; tt < 16; ++tt) {
+                                const int t = 16 * blk + tt;
+                                const float d = hb[Cfg::F_BET + t] * (vv[t * D] - hb[Cfg::F_GAM + t] * ak[tt]);
                                 dl[t] = d;
-                                const float o = scale * fmaf(d, hd.w, hd.y * sq);
-                                const size_t oi = ((lb * T + t) * Hv + h) * size_t(D) + i;
-                                a.tape_delta[oi] = d;
-                                IoTraits<IO>::store(out, oi, o);
+                                if (t < T) *tdp = d;
+                                tdp = opaque_advance(tdp, ostep);
+#pragma unroll
+                                for (int g4 = (tt + 1) / 4; g4 < 4; ++g4) {
+                                    const float4 x = *reinterpret_cast<const float4*>(hb + Cfg::F_CKT + t * TMAX + 16 * blk + 4 * g4);
+                                    const float xs[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+                                    for (int e = 0; e < 4; ++e)
+                                        if (4 * g4 + e > tt) ak[4 * g4 + e] = fmaf(xs[e], d, ak[4 * g4 + e]);
+                                }
+                            }
+                        }
+                        {
+                            float aq[16];
+                            tmem_ld16(ca + TMAX, aq);
+#pragma unroll
+                            for (int sc = 1; sc < S; ++sc) {
+                                float pp[16];
+                                tmem_ld16(ca + sc * Cfg::CH_COLS + TMAX, pp);
+#pragma unroll
+                                for (int e = 0; e < 16; ++e) aq[e] += pp[e];
+                            }
+                            if (blk == TMAX / 16 - 1 && j == G - 1) {
+                                tc_fence_before();
+                                __syncwarp();
+                                if (lane == 0) mbar_arrive(&tempty[ps]);
+                            }
+#pragma unroll
+                            for (int t4 = 0; t4 < 4; ++t4) {
+                                const float4 cq = *reinterpret_cast<const float4*>(hb + Cfg::F_C0Q + 16 * blk + 4 * t4);
+                                aq[4 * t4] *= cq.x; aq[4 * t4 + 1] *= cq.y; aq[4 * t4 + 2] *= cq.z; aq[4 * t4 + 3] *= cq.w;
+                            }
+#pragma unroll
+                            for (int x = 0; x < 16 * blk + 15; ++x) {
+#pragma unroll
+                                for (int g4 = (x < 16 * blk ? 0 : (x - 16 * blk + 1) / 4); g4 < 4; ++g4) {
+                                    const float4 xq = *reinterpret_cast<const float4*>(hb + Cfg::F_CQT + x * TMAX + 16 * blk + 4 * g4);
+                                    const float xs[4] = {xq.x, xq.y, xq.z, xq.w};
+#pragma unroll
+                                    for (int e = 0; e < 4; ++e)
+                                        if (x < 16 * blk + 4 * g4 + e) aq[4 * g4 + e] = fmaf(xs[e], dl[x], aq[4 * g4 + e]);
+                                }
+                            }
+#pragma unroll
+                            for (int tt = 0; tt < 16; ++tt) {
+                                const int t = 16 * blk + tt;
+                                const float o = scale * fmaf(dl[t], hb[Cfg::F_KQ + t], hb[Cfg::F_GAM + t] * aq[tt]);
+                                if (t < T) IoTraits<IO>::store(op, 0, o);
+                                op = opaque_advance(op, ostep);
                             }
                         }
                     }
@@ -1213,19 +1365,42 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
                     dl[t] = 0.f;
                     if (t < T) {
                         const float4 hd = *reinterpret_cast<const float4*>(R + t * RS);  // c0 γ β kq
-                        float ck[TMAX], cq[TMAX];
+                        float sk, sq;
+                        if constexpr (TREE) {
+                            const float4 h2 = *reinterpret_cast<const float4*>(R + t * RS + 4);  // c0q mask
+                            const unsigned gmask = __float_as_uint(h2.y);
+                            sk = hd.x * pr[t];
+                            sq = h2.x * pr[TMAX + t];
 #pragma unroll
-                        for (int q = 0; q < (t + 3) / 4; ++q) {
-                            const float4 x = *reinterpret_cast<const float4*>(R + t * RS + 4 + 4 * q);
-                            const float4 y = *reinterpret_cast<const float4*>(R + t * RS + 4 + TMAX + 4 * q);
-                            ck[4 * q] = x.x; ck[4 * q + 1] = x.y; ck[4 * q + 2] = x.z; ck[4 * q + 3] = x.w;
-                            cq[4 * q] = y.x; cq[4 * q + 1] = y.y; cq[4 * q + 2] = y.z; cq[4 * q + 3] = y.w;
-                        }
-                        float sk = hd.x * pr[t], sq = hd.x * pr[TMAX + t];
+                            for (int q = 0; q < (t + 3) / 4; ++q) {
+                                if (!((gmask >> q) & 1u)) continue;       // no ancestor in 4q .. 4q+3
+                                const float4 x = *reinterpret_cast<const float4*>(R + t * RS + Cfg::HDR + 4 * q);
+                                const float4 y = *reinterpret_cast<const float4*>(R + t * RS + Cfg::HDR + TMAX + 4 * q);
+                                const float xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
 #pragma unroll
-                        for (int s = 0; s < t; ++s) {
-                            sk = fmaf(ck[s], dl[s], sk);
-                            sq = fmaf(cq[s], dl[s], sq);
+                                for (int e = 0; e < 4; ++e) {
+                                    if (4 * q + e < t) {
+                                        sk = fmaf(xs[e], dl[4 * q + e], sk);
+                                        sq = fmaf(ys[e], dl[4 * q + e], sq);
+                                    }
+                                }
+                            }
+                        } else {
+                            float ck[TMAX], cq[TMAX];
+#pragma unroll
+                            for (int q = 0; q < (t + 3) / 4; ++q) {
+                                const float4 x = *reinterpret_cast<const float4*>(R + t * RS + 4 + 4 * q);
+                                const float4 y = *reinterpret_cast<const float4*>(R + t * RS + 4 + TMAX + 4 * q);
+                                ck[4 * q] = x.x; ck[4 * q + 1] = x.y; ck[4 * q + 2] = x.z; ck[4 * q + 3] = x.w;
+                                cq[4 * q] = y.x; cq[4 * q + 1] = y.y; cq[4 * q + 2] = y.z; cq[4 * q + 3] = y.w;
+                            }
+                            sk = hd.x * pr[t];
+                            sq = hd.x * pr[TMAX + t];
+#pragma unroll
+                            for (int s = 0; s < t; ++s) {
+                                sk = fmaf(ck[s], dl[s], sk);
+                                sq = fmaf(cq[s], dl[s], sq);
+                            }
                         }
                         const float u = hd.y * sk;
                         const float d = hd.z * (vv[t * D] - u);
