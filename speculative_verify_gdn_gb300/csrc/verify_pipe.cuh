@@ -50,7 +50,7 @@ namespace gdn {
 
 template <typename IO, int TMAX, int G, bool COMMIT, bool TREE>
 struct PipeCfg {
-    static constexpr int D = 128, KB = 4, ES = int(sizeof(IO));
+    static constexpr int D = 128, KB = 4, ES = int(sizeof(IO)), TMAX_ = TMAX;
     // T up to 32 (trees): one slot each for the B tile, the records and the staging (a unit's
     // prologue then waits for the previous unit's epilogue), one accumulator per chain
     static constexpr bool BIG = TMAX >= 32;
@@ -278,9 +278,89 @@ __device__ __forceinline__ P* opaque_advance(P* p, size_t n) {
     return q;
 }
 
+// global stores under a predicate, without a branch (unrolled loops stay one basic block)
+__device__ __forceinline__ void st_global_if(float* p, float v, bool c) {
+    asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %2, 0;\n\t@q st.global.f32 [%0], %1;\n\t}"
+                 ::"l"(__cvta_generic_to_global(p)), "f"(v), "r"(int(c)));
+}
+__device__ __forceinline__ void st_global_if(__nv_bfloat16* p, float v, bool c) {
+    const unsigned short h = __bfloat16_as_ushort(__float2bfloat16_rn(v));
+    asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %2, 0;\n\t@q st.global.b16 [%0], %1;\n\t}"
+                 ::"l"(__cvta_generic_to_global(p)), "h"(h), "r"(int(c)));
+}
+__device__ __forceinline__ void st_global_if(float* p, float4 v, bool c) {
+    asm volatile("{\n\t.reg .pred q;\n\tsetp.ne.b32 q, %5, 0;\n\t@q st.global.v4.f32 [%0], {%1, %2, %3, %4};\n\t}"
+                 ::"l"(__cvta_generic_to_global(p)), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(int(c)));
+}
+
 // two bf16 values packed in a 32-bit word (element 0 in the low half) to floats (exact)
 __device__ __forceinline__ float bf2_lo(uint32_t u) { return __uint_as_float(u << 16); }
 __device__ __forceinline__ float bf2_hi(uint32_t u) { return __uint_as_float(u & 0xFFFF0000u); }
+
+// Tree conv + SiLU of NPH consecutive parts (from part0, all of them q / k when TO_X, all v
+// heads otherwise) over channels c2, c2 + 1 for every node: node t's window is the staged rows at
+// element offsets win[4 t + d] (tap d = distance d). Nodes go in groups: every load of a group is
+// issued before any store, so the loads overlap instead of queueing behind the previous node's
+// stores; the loop body has no branch. q (part 0) and k (part 1) go to B-tile rows TMAX + t and
+// t with their tf32 remainders at NP + row; v heads to the meta slot.
+template <typename Cfg, int NPH, bool TO_X, typename IO>
+__device__ __forceinline__ void tree_conv_parts(int part0, int c2, const IO* qs, const IO* cws, int NR,
+                                                int W, int T, const int* win, unsigned char* Xb,
+                                                float* meta) {
+    constexpr int TMAX = Cfg::TMAX_, D = Cfg::D, NP = Cfg::NP, XKB = Cfg::XKB;
+    constexpr int NB = NPH == 1 ? 8 : 4;                 // nodes per group
+    static_assert(sizeof(IO) == 2, "the tree conv reads bf16 pairs");
+    float wr[NPH][4][2];
+    const IO* col[NPH];
+    int rbase[NPH];
+#pragma unroll
+    for (int k = 0; k < NPH; ++k) {
+        const int part = part0 + k;
+        const IO* wp = cws + (size_t(part) * D + c2) * W;
+#pragma unroll
+        for (int d = 0; d < 4; ++d)
+#pragma unroll
+            for (int c = 0; c < 2; ++c) wr[k][d][c] = d < W ? io_to_f(wp[c * W + W - 1 - d]) : 0.f;
+        col[k] = qs + size_t(part) * NR * D + c2;
+        rbase[k] = TO_X ? (part == 0 ? TMAX : 0) : (part - 2) * TMAX;
+    }
+    const int4* win4 = reinterpret_cast<const int4*>(win);
+#pragma unroll 1
+    for (int t0 = 0; t0 < TMAX; t0 += NB) {
+        uint32_t u[NB][NPH][4];
+#pragma unroll
+        for (int tb = 0; tb < NB; ++tb) {
+            const int4 w4 = win4[t0 + tb];
+            const int src[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+            for (int k = 0; k < NPH; ++k)
+#pragma unroll
+                for (int d = 0; d < 4; ++d) u[tb][k][d] = *reinterpret_cast<const uint32_t*>(col[k] + src[d]);
+        }
+#pragma unroll
+        for (int tb = 0; tb < NB; ++tb) {
+            const int t = t0 + tb;
+#pragma unroll
+            for (int k = 0; k < NPH; ++k) {
+                float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+                for (int d = 3; d >= 0; --d) {
+                    a0 = fmaf(wr[k][d][0], bf2_lo(u[tb][k][d]), a0);
+                    a1 = fmaf(wr[k][d][1], bf2_hi(u[tb][k][d]), a1);
+                }
+                const float y0 = t < T ? silu_fast(a0) : 0.f, y1 = t < T ? silu_fast(a1) : 0.f;
+                const int r = rbase[k] + t;
+                if constexpr (TO_X) {
+                    *reinterpret_cast<float2*>(Xb + sw128_off(r, c2, XKB)) = make_float2(y0, y1);
+                    *reinterpret_cast<float2*>(Xb + sw128_off(NP + r, c2, XKB)) =
+                        make_float2(y0 - tf32_trunc(y0), y1 - tf32_trunc(y1));
+                } else {
+                    *reinterpret_cast<float2*>(meta + Cfg::M_V + r * D + c2) = make_float2(y0, y1);
+                }
+            }
+        }
+    }
+}
 
 template <typename IO, int TMAX, int G, bool COMMIT, bool TREE>
 __global__ void __launch_bounds__(PipeCfg<IO, TMAX, G, COMMIT, TREE>::NTHR, 1)
@@ -618,55 +698,19 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
             pwait(&uempty[us], ((iu / NXS) & 1) ^ 1, abort_flag, a.status);
             if constexpr (TREE) {
                 named_bar(1, 128);      // windows written
-                // conv + SiLU over each node's window: thread p takes channels 2 (p mod 64) + {0, 1}
-                // of parts 2 (p / 64) + {0, 1} (q, k | v heads), 8 independent bf16-pair loads
-                // per node. Raw k, q (and their tf32 remainders) go to B-tile rows t, TMAX + t.
-                static_assert(sizeof(IO) == 2, "the tree conv reads bf16 pairs");
-                {
-                    const int half = p >> 6, c2 = 2 * (p & 63);
-                    constexpr int NPH = 2;                       // parts per thread
-                    float wr[NPH][4][2];
-                    bool on[NPH];
-#pragma unroll
-                    for (int k = 0; k < NPH; ++k) {
-                        const int part = 2 * half + k;
-                        on[k] = part < Cfg::NPARTS;
-                        const IO* wp = cws + (size_t(on[k] ? part : 0) * D + c2) * W;
-#pragma unroll
-                        for (int d = 0; d < 4; ++d)
-#pragma unroll
-                            for (int c = 0; c < 2; ++c)
-                                wr[k][d][c] = (d < W && on[k]) ? io_to_f(wp[c * W + W - 1 - d]) : 0.f;
-                    }
-                    const int4* win4 = reinterpret_cast<const int4*>(win_s);
-#pragma unroll 2
-                    for (int t = 0; t < TMAX; ++t) {
-                        const int4 w4 = win4[t];
-                        const int src[4] = {w4.x, w4.y, w4.z, w4.w};
-#pragma unroll
-                        for (int k = 0; k < NPH; ++k) {
-                            const int part = 2 * half + k;
-                            const IO* col = qs + size_t(on[k] ? part : 0) * NR * D + c2;
-                            float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-                            for (int d = 3; d >= 0; --d) {
-                                const uint32_t u = *reinterpret_cast<const uint32_t*>(col + src[d]);
-                                a0 = fmaf(wr[k][d][0], bf2_lo(u), a0);
-                                a1 = fmaf(wr[k][d][1], bf2_hi(u), a1);
-                            }
-                            const float y0 = t < T ? silu_fast(a0) : 0.f, y1 = t < T ? silu_fast(a1) : 0.f;
-                            if (!on[k]) continue;
-                            if (part < 2) {
-                                const int r = part == 0 ? TMAX + t : t;
-                                *reinterpret_cast<float2*>(Xb + sw128_off(r, c2, XKB)) = make_float2(y0, y1);
-                                *reinterpret_cast<float2*>(Xb + sw128_off(NP + r, c2, XKB)) =
-                                    make_float2(y0 - tf32_trunc(y0), y1 - tf32_trunc(y1));
-                            } else {
-                                *reinterpret_cast<float2*>(meta + Cfg::M_V + ((part - 2) * TMAX + t) * D + c2) =
-                                    make_float2(y0, y1);
-                            }
-                        }
-                    }
+                // conv + SiLU over each node's window. Trees of 32 nodes share it with the
+                // epilogue warps (idle until this unit's products): the prep warps take q and k,
+                // the epilogue warps the v heads, one part and two channels per thread. Smaller
+                // trees: thread p takes channels 2 (p mod 64) + {0, 1} of parts 2 (p / 64) + {0, 1}.
+                if constexpr (Cfg::BIG) {
+                    named_bar(3, 256);      // staged rows landed, windows written, meta slot free
+                    tree_conv_parts<Cfg, 1, true>(p >> 6, 2 * (p & 63), qs, cws, NR, W, T, win_s, Xb, meta);
+                    named_bar(4, 256);
+                } else {
+                    if (p < 64)
+                        tree_conv_parts<Cfg, 2, true>(0, 2 * p, qs, cws, NR, W, T, win_s, Xb, meta);
+                    else
+                        tree_conv_parts<Cfg, G, false>(2, 2 * (p - 64), qs, cws, NR, W, T, win_s, Xb, meta);
                 }
                 named_bar(1, 128);
                 if (!Cfg::BIG && p == 0) mbar_arrive(&sempty[ss]);     // every staged row has been read
@@ -680,10 +724,9 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
 #pragma unroll
                     for (int o = 16; o > 0; o >>= 1) sv += __shfl_xor_sync(0xffffffffu, sv, o);
                     const float iv = inv_sqrt_nr(sv + a.l2_eps);
-                    if (lane == 0) inv[r] = iv;
-                    if (r < T)
-                        *reinterpret_cast<float4*>(a.tape_k + ((lb * T + r) * Hk + kh) * size_t(D) + 4 * lane) =
-                            make_float4(x.x * iv, x.y * iv, x.z * iv, x.w * iv);
+                    inv[r] = iv;                                 // every lane writes the same value
+                    st_global_if(a.tape_k + ((lb * T + r) * Hk + kh) * size_t(D) + 4 * lane,
+                                 make_float4(x.x * iv, x.y * iv, x.z * iv, x.w * iv), r < T);
                 }
 #pragma unroll
                 for (int n2 = 2 * TMAX; n2 < NP; ++n2) {
@@ -1148,6 +1191,19 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
             const float* meta = reinterpret_cast<const float*>(smem + Cfg::OFF_META + size_t(us) * Cfg::META_BYTES);
             const int n = n_prev(b);
             const float* kp = reinterpret_cast<const float*>(smem + Cfg::OFF_KP + size_t(iu & 1) * Cfg::KP_BYTES);
+            if constexpr (Cfg::BIG) {
+                // the v heads' share of this unit's tree conv (the prep warps take q and k)
+                const int et = tid - 320;
+                const IO* qs = reinterpret_cast<const IO*>(smem + Cfg::OFF_STAGE + size_t(iu % NSS) * Cfg::STAGE_BYTES);
+                named_bar(3, 256);
+                if (2 + (et >> 6) < Cfg::NPARTS)
+                    tree_conv_parts<Cfg, 1, false>(2 + (et >> 6), 2 * (et & 63), qs,
+                                                   qs + size_t(Cfg::NPARTS) * NR * D, NR, W, T,
+                                                   reinterpret_cast<const int*>(scr + Cfg::S_WIN),
+                                                   smem + Cfg::OFF_X + size_t(us) * Cfg::X_BYTES,
+                                                   const_cast<float*>(meta));
+                named_bar(4, 256);
+            }
             if (COMMIT) pwait(&kpfull[iu & 1], (iu >> 1) & 1, abort_flag, a.status);
             pwait(&ufull[us], (iu / NXS) & 1, abort_flag, a.status);
             if (COMMIT && n > 0) {
@@ -1264,7 +1320,7 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
                                 const int t = 16 * blk + tt;
                                 const float d = hb[Cfg::F_BET + t] * (vv[t * D] - hb[Cfg::F_GAM + t] * ak[tt]);
                                 dl[t] = d;
-                                if (t < T) *tdp = d;
+                                st_global_if(tdp, d, t < T);
                                 tdp = opaque_advance(tdp, ostep);
 #pragma unroll
                                 for (int g4 = (tt + 1) / 4; g4 < 4; ++g4) {
@@ -1311,7 +1367,7 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
                             for (int tt = 0; tt < 16; ++tt) {
                                 const int t = 16 * blk + tt;
                                 const float o = scale * fmaf(dl[t], hb[Cfg::F_KQ + t], hb[Cfg::F_GAM + t] * aq[tt]);
-                                if (t < T) IoTraits<IO>::store(op, 0, o);
+                                st_global_if(op, o, t < T);
                                 op = opaque_advance(op, ostep);
                             }
                         }
