@@ -717,16 +717,25 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
                 // norms: warp pw takes rows pw, pw + 4, ..; lane = 4 channels (one 16-byte chunk).
                 // The tape keeps the normalised k; the B tile stays raw (the coefficients and the
                 // epilogue apply the inverse norms).
-#pragma unroll 4
-                for (int r = pw; r < 2 * TMAX; r += 4) {
-                    const float4 x = *reinterpret_cast<const float4*>(Xb + sw128_off(r, 4 * lane, XKB));
-                    float sv = x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w;
+                {
+                    constexpr int RPW = 2 * TMAX / 4;          // rows per warp (a power of 2)
+                    float sq[RPW];
 #pragma unroll
-                    for (int o = 16; o > 0; o >>= 1) sv += __shfl_xor_sync(0xffffffffu, sv, o);
-                    const float iv = inv_sqrt_nr(sv + a.l2_eps);
-                    inv[r] = iv;                                 // every lane writes the same value
-                    st_global_if(a.tape_k + ((lb * T + r) * Hk + kh) * size_t(D) + 4 * lane,
-                                 make_float4(x.x * iv, x.y * iv, x.z * iv, x.w * iv), r < T);
+                    for (int m = 0; m < RPW; ++m) {
+                        const float4 x = *reinterpret_cast<const float4*>(Xb + sw128_off(pw + 4 * m, 4 * lane, XKB));
+                        sq[m] = x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w;
+                    }
+                    int ix;                                    // row pw + 4 ix, held by lanes ix * 32 / RPW ..
+                    const float iv = inv_sqrt_nr(warp_sum_many<RPW>(sq, lane, &ix) + a.l2_eps);
+                    inv[pw + 4 * ix] = iv;                     // lanes sharing ix write the same value
+#pragma unroll
+                    for (int m = 0; m < TMAX / 4; ++m) {       // k rows: pw + 4 m < TMAX
+                        const int r = pw + 4 * m;
+                        const float ivm = __shfl_sync(0xffffffffu, iv, m * (32 / RPW));
+                        const float4 x = *reinterpret_cast<const float4*>(Xb + sw128_off(r, 4 * lane, XKB));
+                        st_global_if(a.tape_k + ((lb * T + r) * Hk + kh) * size_t(D) + 4 * lane,
+                                     make_float4(x.x * ivm, x.y * ivm, x.z * ivm, x.w * ivm), r < T);
+                    }
                 }
 #pragma unroll
                 for (int n2 = 2 * TMAX; n2 < NP; ++n2) {
@@ -1304,31 +1313,60 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
                                 const float4 ck = *reinterpret_cast<const float4*>(hb + Cfg::F_C0K + 16 * blk + 4 * t4);
                                 ak[4 * t4] *= ck.x; ak[4 * t4 + 1] *= ck.y; ak[4 * t4 + 2] *= ck.z; ak[4 * t4 + 3] *= ck.w;
                             }
+                            // coefficient rows are loaded one step ahead of their use (here and below)
+                            if (blk > 0) {
+                                float4 cr[2][4];
 #pragma unroll
-                            for (int x = 0; x < 16 * blk; ++x) {
+                                for (int g4 = 0; g4 < 4; ++g4)
+                                    cr[0][g4] = *reinterpret_cast<const float4*>(hb + Cfg::F_CKT + 16 * blk + 4 * g4);
 #pragma unroll
-                                for (int g4 = 0; g4 < 4; ++g4) {
-                                    const float4 xk = *reinterpret_cast<const float4*>(hb + Cfg::F_CKT + x * TMAX + 16 * blk + 4 * g4);
-                                    ak[4 * g4] = fmaf(xk.x, dl[x], ak[4 * g4]);
-                                    ak[4 * g4 + 1] = fmaf(xk.y, dl[x], ak[4 * g4 + 1]);
-                                    ak[4 * g4 + 2] = fmaf(xk.z, dl[x], ak[4 * g4 + 2]);
-                                    ak[4 * g4 + 3] = fmaf(xk.w, dl[x], ak[4 * g4 + 3]);
+                                for (int x = 0; x < 16 * blk; ++x) {
+                                    const int c = x & 1;
+                                    if (x + 1 < 16 * blk) {
+#pragma unroll
+                                        for (int g4 = 0; g4 < 4; ++g4)
+                                            cr[c ^ 1][g4] = *reinterpret_cast<const float4*>(hb + Cfg::F_CKT + (x + 1) * TMAX + 16 * blk + 4 * g4);
+                                    }
+#pragma unroll
+                                    for (int g4 = 0; g4 < 4; ++g4) {
+                                        ak[4 * g4] = fmaf(cr[c][g4].x, dl[x], ak[4 * g4]);
+                                        ak[4 * g4 + 1] = fmaf(cr[c][g4].y, dl[x], ak[4 * g4 + 1]);
+                                        ak[4 * g4 + 2] = fmaf(cr[c][g4].z, dl[x], ak[4 * g4 + 2]);
+                                        ak[4 * g4 + 3] = fmaf(cr[c][g4].w, dl[x], ak[4 * g4 + 3]);
+                                    }
                                 }
                             }
+                            {
+                                float4 pr[2][4];
+                                float bq[2], gq[2], vq[2];
 #pragma unroll
-                            for (int tt = 0; tt < 16; ++tt) {
-                                const int t = 16 * blk + tt;
-                                const float d = hb[Cfg::F_BET + t] * (vv[t * D] - hb[Cfg::F_GAM + t] * ak[tt]);
-                                dl[t] = d;
-                                st_global_if(tdp, d, t < T);
-                                tdp = opaque_advance(tdp, ostep);
+                                for (int g4 = 0; g4 < 4; ++g4)
+                                    pr[0][g4] = *reinterpret_cast<const float4*>(hb + Cfg::F_CKT + (16 * blk) * TMAX + 16 * blk + 4 * g4);
+                                bq[0] = hb[Cfg::F_BET + 16 * blk];
+                                gq[0] = hb[Cfg::F_GAM + 16 * blk];
+                                vq[0] = vv[(16 * blk) * D];
 #pragma unroll
-                                for (int g4 = (tt + 1) / 4; g4 < 4; ++g4) {
-                                    const float4 x = *reinterpret_cast<const float4*>(hb + Cfg::F_CKT + t * TMAX + 16 * blk + 4 * g4);
-                                    const float xs[4] = {x.x, x.y, x.z, x.w};
+                                for (int tt = 0; tt < 16; ++tt) {
+                                    const int t = 16 * blk + tt, c = tt & 1;
+                                    if (tt + 1 < 16) {
 #pragma unroll
-                                    for (int e = 0; e < 4; ++e)
-                                        if (4 * g4 + e > tt) ak[4 * g4 + e] = fmaf(xs[e], d, ak[4 * g4 + e]);
+                                        for (int g4 = (tt + 2) / 4; g4 < 4; ++g4)
+                                            pr[c ^ 1][g4] = *reinterpret_cast<const float4*>(hb + Cfg::F_CKT + (t + 1) * TMAX + 16 * blk + 4 * g4);
+                                        bq[c ^ 1] = hb[Cfg::F_BET + t + 1];
+                                        gq[c ^ 1] = hb[Cfg::F_GAM + t + 1];
+                                        vq[c ^ 1] = vv[(t + 1) * D];
+                                    }
+                                    const float d = bq[c] * (vq[c] - gq[c] * ak[tt]);
+                                    dl[t] = d;
+                                    st_global_if(tdp, d, t < T);
+                                    tdp = opaque_advance(tdp, ostep);
+#pragma unroll
+                                    for (int g4 = (tt + 1) / 4; g4 < 4; ++g4) {
+                                        const float xs[4] = {pr[c][g4].x, pr[c][g4].y, pr[c][g4].z, pr[c][g4].w};
+#pragma unroll
+                                        for (int e = 0; e < 4; ++e)
+                                            if (4 * g4 + e > tt) ak[4 * g4 + e] = fmaf(xs[e], d, ak[4 * g4 + e]);
+                                    }
                                 }
                             }
                         }
@@ -1352,21 +1390,40 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
                                 const float4 cq = *reinterpret_cast<const float4*>(hb + Cfg::F_C0Q + 16 * blk + 4 * t4);
                                 aq[4 * t4] *= cq.x; aq[4 * t4 + 1] *= cq.y; aq[4 * t4 + 2] *= cq.z; aq[4 * t4 + 3] *= cq.w;
                             }
+                            {
+                                float4 cr[2][4];
 #pragma unroll
-                            for (int x = 0; x < 16 * blk + 15; ++x) {
+                                for (int g4 = 0; g4 < 4; ++g4)
+                                    cr[0][g4] = *reinterpret_cast<const float4*>(hb + Cfg::F_CQT + 16 * blk + 4 * g4);
 #pragma unroll
-                                for (int g4 = (x < 16 * blk ? 0 : (x - 16 * blk + 1) / 4); g4 < 4; ++g4) {
-                                    const float4 xq = *reinterpret_cast<const float4*>(hb + Cfg::F_CQT + x * TMAX + 16 * blk + 4 * g4);
-                                    const float xs[4] = {xq.x, xq.y, xq.z, xq.w};
+                                for (int x = 0; x < 16 * blk + 15; ++x) {
+                                    const int c = x & 1;
+                                    if (x + 1 < 16 * blk + 15) {
 #pragma unroll
-                                    for (int e = 0; e < 4; ++e)
-                                        if (x < 16 * blk + 4 * g4 + e) aq[4 * g4 + e] = fmaf(xs[e], dl[x], aq[4 * g4 + e]);
+                                        for (int g4 = (x + 1 < 16 * blk ? 0 : (x + 1 - 16 * blk + 1) / 4); g4 < 4; ++g4)
+                                            cr[c ^ 1][g4] = *reinterpret_cast<const float4*>(hb + Cfg::F_CQT + (x + 1) * TMAX + 16 * blk + 4 * g4);
+                                    }
+#pragma unroll
+                                    for (int g4 = (x < 16 * blk ? 0 : (x - 16 * blk + 1) / 4); g4 < 4; ++g4) {
+                                        const float xs[4] = {cr[c][g4].x, cr[c][g4].y, cr[c][g4].z, cr[c][g4].w};
+#pragma unroll
+                                        for (int e = 0; e < 4; ++e)
+                                            if (x < 16 * blk + 4 * g4 + e) aq[4 * g4 + e] = fmaf(xs[e], dl[x], aq[4 * g4 + e]);
+                                    }
                                 }
+                            }
+                            float kqs[16], gms[16];
+#pragma unroll
+                            for (int t4 = 0; t4 < 4; ++t4) {
+                                const float4 k4 = *reinterpret_cast<const float4*>(hb + Cfg::F_KQ + 16 * blk + 4 * t4);
+                                const float4 g4v = *reinterpret_cast<const float4*>(hb + Cfg::F_GAM + 16 * blk + 4 * t4);
+                                kqs[4 * t4] = k4.x; kqs[4 * t4 + 1] = k4.y; kqs[4 * t4 + 2] = k4.z; kqs[4 * t4 + 3] = k4.w;
+                                gms[4 * t4] = g4v.x; gms[4 * t4 + 1] = g4v.y; gms[4 * t4 + 2] = g4v.z; gms[4 * t4 + 3] = g4v.w;
                             }
 #pragma unroll
                             for (int tt = 0; tt < 16; ++tt) {
                                 const int t = 16 * blk + tt;
-                                const float o = scale * fmaf(dl[t], hb[Cfg::F_KQ + t], hb[Cfg::F_GAM + t] * aq[tt]);
+                                const float o = scale * fmaf(dl[t], kqs[tt], gms[tt] * aq[tt]);
                                 st_global_if(op, o, t < T);
                                 op = opaque_advance(op, ostep);
                             }
