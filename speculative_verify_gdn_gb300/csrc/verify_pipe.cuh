@@ -65,12 +65,16 @@ struct PipeCfg {
     static constexpr int S = G == 1 ? 2 : 1;
     // TMEM: NUS unit slots of 2 chains x (hi pass: 2NP columns at +0, lo pass: NP columns at
     // +2NP; 32-aligned — or, BIG, one NP-column accumulator that all three products add into),
-    // then a ring of NTS K-block slots (hi 32 + lo 32 columns)
+    // then a ring of NTS K-block slots (hi 32 + lo 32 columns); BIG: then the conv outputs v of
+    // the unit's value heads, column j TMAX + t, lane = value row (written by the epilogue warps)
     static constexpr int TMEM_COLS = 512;
     static constexpr int CH_COLS = BIG ? NP : (3 * NP + 31) / 32 * 32, P_COLS = 2 * CH_COLS;
     static constexpr int NUS = (TMAX <= 8 || BIG) ? 2 : 1;
     static constexpr int T_RING = NUS * P_COLS;
-    static constexpr int NTS = (TMEM_COLS - T_RING) / 64 < 4 ? (TMEM_COLS - T_RING) / 64 : 4;
+    static constexpr int V_COLS = BIG ? G * TMAX : 0;
+    static constexpr int NTS_FIT = (TMEM_COLS - T_RING - V_COLS) / 64;
+    static constexpr int NTS = NTS_FIT < 4 ? NTS_FIT : 4;
+    static constexpr int T_V = T_RING + NTS * 64;
     static constexpr int NPARTS = 2 + G;                     // q, k, v of each value head
     // staged rows per part (W <= 4): W-1 old conv-state rows, the T qkv rows and, when committing,
     // W-1 rows of the previous round's qkv ending at its accepted count
@@ -90,7 +94,8 @@ struct PipeCfg {
     static constexpr int RJ = BIG ? 5 * TMAX + 2 * TMAX * TMAX : TMAX * RS;
     static constexpr int F_C0K = 0, F_C0Q = TMAX, F_GAM = 2 * TMAX, F_BET = 3 * TMAX, F_KQ = 4 * TMAX,
                          F_CKT = 5 * TMAX, F_CQT = 5 * TMAX + TMAX * TMAX;
-    static constexpr int M_REC = 0, M_V = G * RJ, M_GP = M_V + G * TMAX * D,
+    // BIG keeps v in TMEM; its meta slot holds the Gram block [TMAX][2 TMAX] instead (M_V)
+    static constexpr int M_REC = 0, M_V = G * RJ, M_GP = M_V + (BIG ? 2 * TMAX * TMAX : G * TMAX * D),
                          M_CW = M_GP + (COMMIT ? 2 * TMAX * TMAX : 0),
                          M_FLOATS = M_CW + (COMMIT ? (NPARTS * 3 * D * ES + 3) / 4 : 0);
     static constexpr int META_BYTES = (M_FLOATS * 4 + 127) / 128 * 128;
@@ -127,17 +132,16 @@ struct PipeCfg {
     static constexpr size_t OFF_KP = OFF_META + NXS * size_t(META_BYTES);
     static constexpr size_t OFF_SCR = OFF_KP + 2 * size_t(KP_BYTES);
     static constexpr size_t OFF_BAR = (OFF_SCR + size_t(S_FLOATS) * 4 + 15) / 16 * 16;
-    static constexpr int NBAR = 3 * NKS + 2 * NTS + 8 * 2 + 1;
+    static constexpr int NBAR = 3 * NKS + 2 * NTS + 8 * 2 + 3;
     static constexpr size_t OFF_MISC = OFF_BAR + NBAR * 8;   // TMEM base, abort flag
     static constexpr size_t SMEM = OFF_MISC + 16 + 1024;
 
-    static_assert(T_RING + NTS * 64 <= TMEM_COLS && NTS >= G, "TMEM budget");
+    static_assert(T_V + V_COLS <= TMEM_COLS && NTS >= G, "TMEM budget");
     static_assert(NKS >= 2 * G, "shared-memory ring");
     static_assert(G * S == 2, "two accumulator chains per unit");
     static_assert(!COMMIT || TMAX <= 8, "the fused rollback serves T <= 8");
     static_assert(!(COMMIT && TREE), "the fused rollback serves chains");
     static_assert(!BIG || TREE, "T = 32 is the tree workload's size");
-    static_assert(!BIG || STAGE_BYTES >= 2 * TMAX * TMAX * 4, "the Gram block fits in the staging slot");
     static_assert(SMEM <= 227 * 1024, "shared memory budget");
     static_assert(OFF_X % 1024 == 0 && X_BYTES % 1024 == 0, "swizzle atoms need 1024-byte bases");
     static_assert((RS * 4) % 16 == 0 && (RJ * 4) % 16 == 0 && (M_V * 4) % 16 == 0 && (M_GP * 4) % 16 == 0 &&
@@ -362,6 +366,46 @@ __device__ __forceinline__ void tree_conv_parts(int part0, int c2, const IO* qs,
     }
 }
 
+// Tree conv + SiLU of the v heads for value row i (the calling thread's TMEM lane): head j, node
+// t goes to TMEM column tv + j TMAX + t. Groups of 16 nodes: loads first, then math, then one
+// 16-column store.
+template <typename Cfg, typename IO>
+__device__ __forceinline__ void tree_vconv_tmem(int i, const IO* qs, const IO* cws, int NR, int W, int T,
+                                                const int* win, uint32_t tv) {
+    constexpr int TMAX = Cfg::TMAX_, D = Cfg::D, G = Cfg::NPARTS - 2;
+    const int4* win4 = reinterpret_cast<const int4*>(win);
+#pragma unroll 1
+    for (int j = 0; j < G; ++j) {
+        const IO* wp = cws + (size_t(2 + j) * D + i) * W;
+        float wr[4];
+#pragma unroll
+        for (int d = 0; d < 4; ++d) wr[d] = d < W ? io_to_f(wp[W - 1 - d]) : 0.f;
+        const IO* col = qs + size_t(2 + j) * NR * D + i;
+#pragma unroll 1
+        for (int t0 = 0; t0 < TMAX; t0 += 16) {
+            float x[16][4];
+#pragma unroll
+            for (int tb = 0; tb < 16; ++tb) {
+                const int4 w4 = win4[t0 + tb];
+                x[tb][0] = io_to_f(col[w4.x]);
+                x[tb][1] = io_to_f(col[w4.y]);
+                x[tb][2] = io_to_f(col[w4.z]);
+                x[tb][3] = io_to_f(col[w4.w]);
+            }
+            uint32_t y[16];
+#pragma unroll
+            for (int tb = 0; tb < 16; ++tb) {
+                float acc = 0.f;
+#pragma unroll
+                for (int d = 3; d >= 0; --d) acc = fmaf(wr[d], x[tb][d], acc);
+                y[tb] = __float_as_uint(t0 + tb < T ? silu_fast(acc) : 0.f);
+            }
+            tmem_st16(tv + j * TMAX + t0, y);
+        }
+    }
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 template <typename IO, int TMAX, int G, bool COMMIT, bool TREE>
 __global__ void __launch_bounds__(PipeCfg<IO, TMAX, G, COMMIT, TREE>::NTHR, 1)
 gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap smap,
@@ -391,6 +435,8 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
     uint64_t* kpfull = uempty + 2;               // COMMIT: previous round's tape rows staged
     uint64_t* kpempty = kpfull + 2;              // COMMIT: commit slot read by convert and epilogue
     uint64_t* mdone = kpempty + 2;               // every MMA of this CTA complete
+    uint64_t* winfull = mdone + 1;               // BIG: the unit's conv windows written (prep)
+    uint64_t* vdone = mdone + 2;                 // BIG: v in TMEM, staged rows read (4 epilogue warps)
     uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + Cfg::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::OFF_MISC + 4);
     float* scr = reinterpret_cast<float*>(smem + Cfg::OFF_SCR);
@@ -405,7 +451,7 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
             uint64_t* bb = &bars[i];
             const bool four = (!COMMIT && bb >= kempty && bb < kempty + NKS) ||
                               (bb >= kconv && bb < kconv + NKS) || (bb >= tmfull && bb < tmfull + NTS) ||
-                              (bb >= tempty && bb < tempty + 2);
+                              (bb >= tempty && bb < tempty + 2) || bb == vdone;
             const bool kpe = bb >= kpempty && bb < kpempty + 2;
             mbar_init(bb, four ? 4 : kpe ? 8 : (bb >= uempty && bb < uempty + 2) ? 5 : 1);
         }
@@ -693,19 +739,27 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
                         win_s[p * 4 + d] = src * D;
                     }
                 }
+                if constexpr (Cfg::BIG) {
+                    named_bar(1, 128);
+                    if (p == 0) mbar_arrive(winfull);      // the epilogue warps' v conv may start
+                }
             }
             pwait(&sfull[ss], (iu / NSS) & 1, abort_flag, a.status);
-            pwait(&uempty[us], ((iu / NXS) & 1) ^ 1, abort_flag, a.status);
+            if constexpr (Cfg::BIG) {
+                // one meta slot: the B tile is free once the previous unit's products are done;
+                // its records are waited for just before this unit's are written (below)
+                if (iu > 0) pwait(&tfull[(iu - 1) % Cfg::NUS], uint32_t((iu - 1) / Cfg::NUS) & 1u, abort_flag, a.status);
+            } else {
+                pwait(&uempty[us], ((iu / NXS) & 1) ^ 1, abort_flag, a.status);
+            }
             if constexpr (TREE) {
                 named_bar(1, 128);      // windows written
-                // conv + SiLU over each node's window. Trees of 32 nodes share it with the
-                // epilogue warps (idle until this unit's products): the prep warps take q and k,
-                // the epilogue warps the v heads, one part and two channels per thread. Smaller
-                // trees: thread p takes channels 2 (p mod 64) + {0, 1} of parts 2 (p / 64) + {0, 1}.
+                // conv + SiLU over each node's window. Trees of 32 nodes: the prep warps take q and
+                // k (one part and two channels per thread), the epilogue warps the v heads (into
+                // TMEM). Smaller trees: thread p takes channels 2 (p mod 64) + {0, 1} of parts
+                // 2 (p / 64) + {0, 1}.
                 if constexpr (Cfg::BIG) {
-                    named_bar(3, 256);      // staged rows landed, windows written, meta slot free
                     tree_conv_parts<Cfg, 1, true>(p >> 6, 2 * (p & 63), qs, cws, NR, W, T, win_s, Xb, meta);
-                    named_bar(4, 256);
                 } else {
                     if (p < 64)
                         tree_conv_parts<Cfg, 2, true>(0, 2 * p, qs, cws, NR, W, T, win_s, Xb, meta);
@@ -742,15 +796,10 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
                     *reinterpret_cast<float*>(Xb + sw128_off(n2, p, XKB)) = 0.f;
                     *reinterpret_cast<float*>(Xb + sw128_off(NP + n2, p, XKB)) = 0.f;
                 }
-                if (p < G * TMAX) {
-                    if constexpr (Cfg::BIG) {
-                        meta[Cfg::M_REC + gj * Cfg::RJ + Cfg::F_GAM + gt] = g_in;
-                        meta[Cfg::M_REC + gj * Cfg::RJ + Cfg::F_BET + gt] = b_in;
-                    } else {
-                        float* rec = meta + Cfg::M_REC + p * RS;
-                        rec[1] = g_in;
-                        rec[2] = b_in;
-                    }
+                if (!Cfg::BIG && p < G * TMAX) {
+                    float* rec = meta + Cfg::M_REC + p * RS;
+                    rec[1] = g_in;
+                    rec[2] = b_in;
                 }
             } else {
             // conv + SiLU of channel p of every part (one loop body for all parts keeps the code
@@ -852,7 +901,7 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
             fence_async_smem();
             named_bar(1, 128);
             // BIG: the Gram block lives in the staging slot (its rows have been read)
-            if constexpr (Cfg::BIG) gram = reinterpret_cast<float*>(st);
+            if constexpr (Cfg::BIG) gram = meta + Cfg::M_V;
             // Gram block on the warp tensor path: D[m][n] = X_m · k_n, 3xTF32 (hi·hi + hi·lo + lo·hi);
             // rows m: k_0.., q_0.. (zero beyond 2 TMAX). One 16 x 8 tile: each warp takes 32 channels
             // and the partials are summed; four tiles (TMAX = 16): warp pw takes tile pw, all channels.
@@ -957,6 +1006,12 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
                 // ancestors strictly between x and v; zero for every other x. c0 = every
                 // ancestor's gate. The Gram block is raw: the inverse norms are applied here.
                 if constexpr (Cfg::BIG) {
+                    // the previous unit's epilogue has read its records
+                    pwait(&uempty[us], ((iu / NXS) & 1) ^ 1, abort_flag, a.status);
+                    if (p < G * TMAX) {
+                        meta[Cfg::M_REC + gj * Cfg::RJ + Cfg::F_GAM + gt] = g_in;
+                        meta[Cfg::M_REC + gj * Cfg::RJ + Cfg::F_BET + gt] = b_in;
+                    }
                     constexpr int NZ = 2 * TMAX * TMAX / 4;          // CK, CQ of one head in float4
 #pragma unroll 1
                     for (int z = p; z < G * NZ; z += 128) {
@@ -1033,11 +1088,12 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
                 }
             }
             }
-            if constexpr (Cfg::BIG) fence_async_smem();      // Gram writes before the next TMA fill
             named_bar(1, 128);
-            if (p == 0) {
-                mbar_arrive(&ufull[us]);
-                if (Cfg::BIG) mbar_arrive(&sempty[ss]);      // the Gram block is done with it
+            if (p == 0) mbar_arrive(&ufull[us]);
+            if constexpr (Cfg::BIG) {
+                // staged rows and windows stay until the epilogue warps' v conv has read them
+                pwait(vdone, uint32_t(iu & 1), abort_flag, a.status);
+                if (p == 0) mbar_arrive(&sempty[ss]);
             }
         }
     } else if (warp < 10) {
@@ -1201,17 +1257,18 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
             const int n = n_prev(b);
             const float* kp = reinterpret_cast<const float*>(smem + Cfg::OFF_KP + size_t(iu & 1) * Cfg::KP_BYTES);
             if constexpr (Cfg::BIG) {
-                // the v heads' share of this unit's tree conv (the prep warps take q and k)
-                const int et = tid - 320;
+                // the v heads of this unit's tree conv, into TMEM (the prep warps take q and k); the
+                // previous unit's epilogue, just finished by these warps, has read the old v
                 const IO* qs = reinterpret_cast<const IO*>(smem + Cfg::OFF_STAGE + size_t(iu % NSS) * Cfg::STAGE_BYTES);
-                named_bar(3, 256);
-                if (2 + (et >> 6) < Cfg::NPARTS)
-                    tree_conv_parts<Cfg, 1, false>(2 + (et >> 6), 2 * (et & 63), qs,
-                                                   qs + size_t(Cfg::NPARTS) * NR * D, NR, W, T,
-                                                   reinterpret_cast<const int*>(scr + Cfg::S_WIN),
-                                                   smem + Cfg::OFF_X + size_t(us) * Cfg::X_BYTES,
-                                                   const_cast<float*>(meta));
-                named_bar(4, 256);
+                pwait(winfull, uint32_t(iu & 1), abort_flag, a.status);
+                pwait(&sfull[iu % NSS], uint32_t(iu / NSS) & 1u, abort_flag, a.status);
+                tc_fence_after();
+                tree_vconv_tmem<Cfg>(i, qs, qs + size_t(Cfg::NPARTS) * NR * D, NR, W, T,
+                                     reinterpret_cast<const int*>(scr + Cfg::S_WIN),
+                                     tbase + Cfg::T_V + (uint32_t(32 * q4) << 16));
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(vdone);
             }
             if (COMMIT) pwait(&kpfull[iu & 1], (iu >> 1) & 1, abort_flag, a.status);
             pwait(&ufull[us], (iu / NXS) & 1, abort_flag, a.status);
@@ -1290,7 +1347,7 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
                     // dependence. Positions t >= T are computed and never stored (their
                     // coefficients are zero; nothing flows back to t < T).
                     const float* hb = meta + Cfg::M_REC + j * Cfg::RJ;
-                    const float* vv = meta + Cfg::M_V + size_t(j) * TMAX * D + i;
+                    const uint32_t tvj = tbase + Cfg::T_V + (uint32_t(32 * q4) << 16) + j * TMAX;
                     const size_t ostep = size_t(Hv) * D;                 // next position, same head
                     float* tdp = a.tape_delta + (lb * T * Hv + h) * size_t(D) + i;
                     IO* op = out + (lb * T * Hv + h) * size_t(D) + i;
@@ -1337,14 +1394,15 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
                                 }
                             }
                             {
+                                float vb[16];
+                                tmem_ld16(tvj + 16 * blk, vb);
                                 float4 pr[2][4];
-                                float bq[2], gq[2], vq[2];
+                                float bq[2], gq[2];
 #pragma unroll
                                 for (int g4 = 0; g4 < 4; ++g4)
                                     pr[0][g4] = *reinterpret_cast<const float4*>(hb + Cfg::F_CKT + (16 * blk) * TMAX + 16 * blk + 4 * g4);
                                 bq[0] = hb[Cfg::F_BET + 16 * blk];
                                 gq[0] = hb[Cfg::F_GAM + 16 * blk];
-                                vq[0] = vv[(16 * blk) * D];
 #pragma unroll
                                 for (int tt = 0; tt < 16; ++tt) {
                                     const int t = 16 * blk + tt, c = tt & 1;
@@ -1354,9 +1412,8 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
                                             pr[c ^ 1][g4] = *reinterpret_cast<const float4*>(hb + Cfg::F_CKT + (t + 1) * TMAX + 16 * blk + 4 * g4);
                                         bq[c ^ 1] = hb[Cfg::F_BET + t + 1];
                                         gq[c ^ 1] = hb[Cfg::F_GAM + t + 1];
-                                        vq[c ^ 1] = vv[(t + 1) * D];
                                     }
-                                    const float d = bq[c] * (vq[c] - gq[c] * ak[tt]);
+                                    const float d = bq[c] * (vb[tt] - gq[c] * ak[tt]);
                                     dl[t] = d;
                                     st_global_if(tdp, d, t < T);
                                     tdp = opaque_advance(tdp, ostep);
