@@ -1529,11 +1529,15 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
                 }
                 const float* R = meta + Cfg::M_REC + j * TMAX * RS;
                 const float* vv = meta + Cfg::M_V + size_t(j) * TMAX * D + i;
+                // every position is computed (no branch in the unrolled body); positions t >= T
+                // are never stored and feed only later positions >= T
+                const size_t ostep = size_t(Hv) * D;
+                float* tdp = a.tape_delta + (lb * T * Hv + h) * size_t(D) + i;
+                IO* op = out + (lb * T * Hv + h) * size_t(D) + i;
                 float dl[TMAX];
 #pragma unroll
                 for (int t = 0; t < TMAX; ++t) {
-                    dl[t] = 0.f;
-                    if (t < T) {
+                    {
                         const float4 hd = *reinterpret_cast<const float4*>(R + t * RS);  // c0 γ β kq
                         float sk, sq;
                         if constexpr (TREE) {
@@ -1576,9 +1580,10 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
                         const float d = hd.z * (vv[t * D] - u);
                         dl[t] = d;
                         const float o = scale * fmaf(d, hd.w, hd.y * sq);
-                        const size_t oi = ((lb * T + t) * Hv + h) * size_t(D) + i;
-                        a.tape_delta[oi] = d;
-                        IoTraits<IO>::store(out, oi, o);
+                        st_global_if(tdp, d, t < T);
+                        st_global_if(op, o, t < T);
+                        tdp = opaque_advance(tdp, ostep);
+                        op = opaque_advance(op, ostep);
                     }
                 }
                 }
