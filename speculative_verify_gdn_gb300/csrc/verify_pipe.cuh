@@ -885,7 +885,7 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
                 *reinterpret_cast<float*>(Xb + sw128_off(NP + t, p, XKB)) = kn - tf32_trunc(kn);
                 *reinterpret_cast<float*>(Xb + sw128_off(TMAX + t, p, XKB)) = qn;
                 *reinterpret_cast<float*>(Xb + sw128_off(NP + TMAX + t, p, XKB)) = qn - tf32_trunc(qn);
-                if (t < T) a.tape_k[((lb * T + t) * Hk + kh) * size_t(D) + p] = kn;
+                st_global_if(a.tape_k + ((lb * T + t) * Hk + kh) * size_t(D) + p, kn, t < T);
             }
 #pragma unroll
             for (int n2 = 2 * TMAX; n2 < NP; ++n2) {
