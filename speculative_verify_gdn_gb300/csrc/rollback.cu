@@ -69,7 +69,9 @@ gdn_rollback_kernel(const RollbackArgs a) {
     }
     if (n == 0) return;              // the snapshot is still in place
 
-    // issue the whole state slice of this thread first: its latency hides the tape prologue
+    // every load is issued before the first wait: the state slice of this thread, the gates, the
+    // tape rows (chains: rows 0 .. n-1; paths: the path's nodes, read by every thread, clamped to
+    // a valid row until the check below)
     float* S = a.state + (lb * Hv + h) * size_t(D) * D;   // row-major S: [i][j]
     const int j0 = lane * CPL;
     float v[RPW][CPL];
@@ -77,13 +79,39 @@ gdn_rollback_kernel(const RollbackArgs a) {
     for (int u = 0; u < RPW; ++u) ld_rows_cs<CPL>(S + size_t(warp + NW * u) * D + j0, v[u]);
 
     if (tid == 0) bad = 0;
+    auto node_of = [&](int s2) -> int {
+        if (!PATH) return s2;
+        const int nd = __ldg(a.path + size_t(b) * a.P + s2);
+        return (nd >= 0 && nd < T) ? nd : -1;
+    };
+    float gv = 0.f;
+    int my_node = 0;
+    if (tid < n) {
+        my_node = node_of(tid);
+        gv = __ldg(a.g + (lb * T + (my_node < 0 ? 0 : my_node)) * Hv + h);
+    }
+    float kr[NMAX][CPL];   // k_s[j0 .. j0+CPL) of this lane's columns
+#pragma unroll
+    for (int s = 0; s < NMAX; ++s) {
+#pragma unroll
+        for (int r = 0; r < CPL; ++r) kr[s][r] = 0.f;
+        if (s < n) {
+            const int nd = node_of(s);
+            const float* src = a.tape_k + ((lb * T + (nd < 0 ? 0 : nd)) * Hk + kh) * size_t(D) + j0;
+#pragma unroll
+            for (int r = 0; r < CPL; ++r) kr[s][r] = __ldg(src + r);
+        }
+    }
+    for (int idx = tid; idx < n * D; idx += 256) {       // raw δ_s[i]; Γ_{s+1..n-1} applied below
+        const int s2 = idx / D, i = idx - s2 * D;
+        const int nd = node_of(s2);
+        Ds[s2][i] = __ldg(a.tape_delta + ((lb * T + (nd < 0 ? 0 : nd)) * Hv + h) * size_t(D) + i);
+    }
     __syncthreads();
     if (tid < n) {
-        const int nd = PATH ? __ldg(a.path + size_t(b) * a.P + tid) : tid;
-        const bool ok = nd >= 0 && nd < T;
-        if (!ok) atomicOr(&bad, 1);
-        nodes[tid] = ok ? nd : 0;
-        gs[tid] = ok ? __ldg(a.g + (lb * T + nd) * Hv + h) : 0.f;
+        nodes[tid] = my_node < 0 ? 0 : my_node;
+        gs[tid] = gv;
+        if (my_node < 0) atomicOr(&bad, 1);
     }
     __syncthreads();
     if (bad) {
@@ -92,43 +120,27 @@ gdn_rollback_kernel(const RollbackArgs a) {
     }
     if (tid == 0) {
         float c = 1.f;
-        for (int s = n - 1; s >= 0; --s) {
-            coef[s] = c;                                   // Γ_{s+1..n-1}
-            c *= gs[s];
+        for (int s2 = n - 1; s2 >= 0; --s2) {
+            coef[s2] = c;                                  // Γ_{s+1..n-1}
+            c *= gs[s2];
         }
         gtot = c;                                          // Γ_{0..n-1}
-    }
-    float kr[NMAX][CPL];   // k_s[j0 .. j0+CPL) of this lane's columns
-#pragma unroll
-    for (int s = 0; s < NMAX; ++s) {
-#pragma unroll
-        for (int r = 0; r < CPL; ++r) kr[s][r] = 0.f;
-        if (s < n) {
-            const float* src = a.tape_k + ((lb * T + nodes[s]) * Hk + kh) * size_t(D) + j0;
-#pragma unroll
-            for (int r = 0; r < CPL; ++r) kr[s][r] = __ldg(src + r);
-        }
-    }
-    __syncthreads();
-    for (int idx = tid; idx < n * D; idx += 256) {
-        const int s = idx / D, i = idx - s * D;
-        Ds[s][i] = coef[s] * __ldg(a.tape_delta + ((lb * T + nodes[s]) * Hv + h) * size_t(D) + i);
     }
     __syncthreads();
     const float G = gtot;
 
-    // S_n[i][j] = Γ_total S_0[i][j] + Σ_s δ'_s[i] k_s[j]
+    // S_n[i][j] = Γ_total S_0[i][j] + Σ_s Γ_{s+1..n-1} δ_s[i] k_s[j]
 #pragma unroll
     for (int u = 0; u < RPW; ++u) {
         const int i = warp + NW * u;
 #pragma unroll
         for (int r = 0; r < CPL; ++r) v[u][r] *= G;
 #pragma unroll
-        for (int s = 0; s < NMAX; ++s) {
-            if (s < n) {
-                const float d = Ds[s][i];
+        for (int s2 = 0; s2 < NMAX; ++s2) {
+            if (s2 < n) {
+                const float d = coef[s2] * Ds[s2][i];
 #pragma unroll
-                for (int r = 0; r < CPL; ++r) v[u][r] = fmaf(d, kr[s][r], v[u][r]);
+                for (int r = 0; r < CPL; ++r) v[u][r] = fmaf(d, kr[s2][r], v[u][r]);
             }
         }
         st_rows_cs<CPL>(S + size_t(i) * D + j0, v[u]);
