@@ -9,51 +9,42 @@
 // the replay of n steps is folded into one pass over the state:
 //     S_n = Γ_total · S_0 + Σ_{s<n} (Γ_{s+1..n-1} δ_s) k_sᵀ,   Γ_total = Π_{s<n} g_s,
 // which reads and writes each state element once (HBM-bound) with n+1 FMAs per element.
-// The state is row-major S ([i][j], j contiguous): lanes own consecutive key columns j (16-byte
-// accesses, coalesced rows), warps own rows i. One 256-thread CTA per (layer, sequence, value
-// head); n is read on the device, so a CTA whose sequence accepted nothing exits at once and the
-// whole call needs no host synchronisation.
+// The state is row-major S ([i][j], j contiguous). One 256-thread CTA per (layer, sequence, value
+// head) moves its slice by bulk copy into shared memory and back (64 KiB at d = 128, so three
+// CTAs per SM keep ~200 KiB of state in flight; registers would hold two); lanes own consecutive
+// key columns j, warps own rows i. n is read on the device, so a CTA whose sequence accepted
+// nothing exits at once and the whole call needs no host synchronisation.
 #include "common.cuh"
 #include "kernels.h"
 
 namespace gdn {
 
-template <int RPL>
-__device__ __forceinline__ void ld_rows_cs(const float* p, float (&v)[RPL]) {
-    if constexpr (RPL == 4) {
-        const float4 x = __ldcs(reinterpret_cast<const float4*>(p));
-        v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
-    } else if constexpr (RPL == 2) {
-        const float2 x = __ldcs(reinterpret_cast<const float2*>(p));
-        v[0] = x.x; v[1] = x.y;
-    } else {
-        v[0] = __ldcs(p);
-    }
-}
-
-template <int RPL>
-__device__ __forceinline__ void st_rows_cs(float* p, const float (&v)[RPL]) {
-    if constexpr (RPL == 4) {
-        __stcs(reinterpret_cast<float4*>(p), make_float4(v[0], v[1], v[2], v[3]));
-    } else if constexpr (RPL == 2) {
-        __stcs(reinterpret_cast<float2*>(p), make_float2(v[0], v[1]));
-    } else {
-        __stcs(p, v[0]);
-    }
-}
+// shared memory of one CTA: the state slice [D][D], then δ_s [NMAX][D] and k_s [NMAX][D]
+template <int D, int NMAX>
+struct RbSmem {
+    static constexpr size_t SLICE = size_t(D) * D * 4, CHUNK = SLICE < 16384 ? SLICE : 16384;
+    static constexpr size_t OFF_D = SLICE, OFF_K = OFF_D + size_t(NMAX) * D * 4;
+    static constexpr size_t BYTES = OFF_K + size_t(NMAX) * D * 4;
+    static_assert(SLICE % CHUNK == 0 && CHUNK % 16 == 0, "bulk-copy chunks");
+};
 
 template <typename IO, int D, int NMAX, bool PATH>
-__global__ void __launch_bounds__(256, (NMAX <= 8 ? 2 : 1))
+__global__ void __launch_bounds__(256)
 gdn_rollback_kernel(const RollbackArgs a) {
+    using Sm = RbSmem<D, NMAX>;
     constexpr int CPL = D / 32;      // consecutive key columns j per lane
     constexpr int NW = 8;            // warps; warp w owns state rows i = w, w + 8, ...
     constexpr int RPW = D / NW;
-    __shared__ float Ds[NMAX][D];    // scaled innovations δ'_s[i] = Γ_{s+1..n-1} δ_s[i]
+    extern __shared__ __align__(128) unsigned char rb_smem[];
+    float* Sl = reinterpret_cast<float*>(rb_smem);                    // state slice S_0 -> S_n
+    float (*Ds)[D] = reinterpret_cast<float (*)[D]>(rb_smem + Sm::OFF_D);   // innovations δ_s[i]
+    float (*Ks)[D] = reinterpret_cast<float (*)[D]>(rb_smem + Sm::OFF_K);   // keys k_s[j]
     __shared__ float coef[NMAX];
     __shared__ float gs[NMAX];
     __shared__ int nodes[NMAX];
     __shared__ float gtot;
-    __shared__ int bad;
+    __shared__ int bad, load_ok;
+    __shared__ __align__(8) uint64_t bar;
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int h = blockIdx.x, b = blockIdx.y, l = blockIdx.z;
@@ -69,16 +60,19 @@ gdn_rollback_kernel(const RollbackArgs a) {
     }
     if (n == 0) return;              // the snapshot is still in place
 
-    // every load is issued before the first wait: the state slice of this thread, the gates, the
-    // tape rows (chains: rows 0 .. n-1; paths: the path's nodes, read by every thread, clamped to
-    // a valid row until the check below)
+    // the state slice streams into shared memory by bulk copy while the tape is read: every load
+    // is issued before the first wait (paths: the path's nodes are read by every thread, clamped
+    // to a valid row until the check below)
     float* S = a.state + (lb * Hv + h) * size_t(D) * D;   // row-major S: [i][j]
-    const int j0 = lane * CPL;
-    float v[RPW][CPL];
-#pragma unroll
-    for (int u = 0; u < RPW; ++u) ld_rows_cs<CPL>(S + size_t(warp + NW * u) * D + j0, v[u]);
-
-    if (tid == 0) bad = 0;
+    if (tid == 0) {
+        bad = 0;
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+        mbar_arrive_expect_tx(&bar, uint32_t(Sm::SLICE));
+#pragma unroll 1
+        for (size_t o = 0; o < Sm::SLICE; o += Sm::CHUNK)
+            bulk_g2s(rb_smem + o, reinterpret_cast<const unsigned char*>(S) + o, uint32_t(Sm::CHUNK), &bar);
+    }
     auto node_of = [&](int s2) -> int {
         if (!PATH) return s2;
         const int nd = __ldg(a.path + size_t(b) * a.P + s2);
@@ -90,22 +84,11 @@ gdn_rollback_kernel(const RollbackArgs a) {
         my_node = node_of(tid);
         gv = __ldg(a.g + (lb * T + (my_node < 0 ? 0 : my_node)) * Hv + h);
     }
-    float kr[NMAX][CPL];   // k_s[j0 .. j0+CPL) of this lane's columns
-#pragma unroll
-    for (int s = 0; s < NMAX; ++s) {
-#pragma unroll
-        for (int r = 0; r < CPL; ++r) kr[s][r] = 0.f;
-        if (s < n) {
-            const int nd = node_of(s);
-            const float* src = a.tape_k + ((lb * T + (nd < 0 ? 0 : nd)) * Hk + kh) * size_t(D) + j0;
-#pragma unroll
-            for (int r = 0; r < CPL; ++r) kr[s][r] = __ldg(src + r);
-        }
-    }
-    for (int idx = tid; idx < n * D; idx += 256) {       // raw δ_s[i]; Γ_{s+1..n-1} applied below
+    for (int idx = tid; idx < n * D; idx += 256) {       // raw δ_s[i] (Γ_{s+1..n-1} applied below), k_s[j]
         const int s2 = idx / D, i = idx - s2 * D;
-        const int nd = node_of(s2);
-        Ds[s2][i] = __ldg(a.tape_delta + ((lb * T + (nd < 0 ? 0 : nd)) * Hv + h) * size_t(D) + i);
+        const int nd = node_of(s2), row = nd < 0 ? 0 : nd;
+        Ds[s2][i] = __ldg(a.tape_delta + ((lb * T + row) * Hv + h) * size_t(D) + i);
+        Ks[s2][i] = __ldg(a.tape_k + ((lb * T + row) * Hk + kh) * size_t(D) + i);
     }
     __syncthreads();
     if (tid < n) {
@@ -114,10 +97,6 @@ gdn_rollback_kernel(const RollbackArgs a) {
         if (my_node < 0) atomicOr(&bad, 1);
     }
     __syncthreads();
-    if (bad) {
-        if (tid == 0 && h == 0 && l == 0) set_status(a.status, GDN_STATUS_BAD_PATH);
-        return;
-    }
     if (tid == 0) {
         float c = 1.f;
         for (int s2 = n - 1; s2 >= 0; --s2) {
@@ -125,25 +104,70 @@ gdn_rollback_kernel(const RollbackArgs a) {
             c *= gs[s2];
         }
         gtot = c;                                          // Γ_{0..n-1}
+        // the slice must land before this CTA may leave, whatever happens below
+        load_ok = mbar_wait_bounded(&bar, 0) ? 1 : 0;
+        if (!load_ok) {
+            set_status(a.status, GDN_STATUS_WAIT_TIMEOUT);
+            mbar_wait_bounded(&bar, 0);
+        }
     }
     __syncthreads();
+    if (!load_ok || bad) {
+        if (bad && tid == 0 && h == 0 && l == 0) set_status(a.status, GDN_STATUS_BAD_PATH);
+        return;
+    }
+    mbar_try_wait(&bar, 0);          // completed: each thread observes the slice
     const float G = gtot;
+    const int j0 = lane * CPL;
 
-    // S_n[i][j] = Γ_total S_0[i][j] + Σ_s Γ_{s+1..n-1} δ_s[i] k_s[j]
+    // S_n[i][j] = Γ_total S_0[i][j] + Σ_s Γ_{s+1..n-1} δ_s[i] k_s[j], in place in shared memory
+    float kr[NMAX <= 8 ? NMAX : 1][CPL];
+    if constexpr (NMAX <= 8) {
 #pragma unroll
+        for (int s2 = 0; s2 < NMAX; ++s2)
+#pragma unroll
+            for (int r = 0; r < CPL; ++r) kr[s2][r] = s2 < n ? Ks[s2][j0 + r] : 0.f;
+    }
+#pragma unroll 4
     for (int u = 0; u < RPW; ++u) {
         const int i = warp + NW * u;
+        float v[CPL];
+        if constexpr (CPL == 4) {
+            const float4 x4 = *reinterpret_cast<const float4*>(Sl + i * D + j0);
+            v[0] = G * x4.x; v[1] = G * x4.y; v[2] = G * x4.z; v[3] = G * x4.w;
+        } else {
 #pragma unroll
-        for (int r = 0; r < CPL; ++r) v[u][r] *= G;
+            for (int r = 0; r < CPL; ++r) v[r] = G * Sl[i * D + j0 + r];
+        }
+        if constexpr (NMAX <= 8) {
 #pragma unroll
-        for (int s2 = 0; s2 < NMAX; ++s2) {
-            if (s2 < n) {
+            for (int s2 = 0; s2 < NMAX; ++s2) {
+                const float d = s2 < n ? coef[s2] * Ds[s2][i] : 0.f;
+#pragma unroll
+                for (int r = 0; r < CPL; ++r) v[r] = fmaf(d, kr[s2][r], v[r]);
+            }
+        } else {
+#pragma unroll 1
+            for (int s2 = 0; s2 < n; ++s2) {
                 const float d = coef[s2] * Ds[s2][i];
 #pragma unroll
-                for (int r = 0; r < CPL; ++r) v[u][r] = fmaf(d, kr[s2][r], v[u][r]);
+                for (int r = 0; r < CPL; ++r) v[r] = fmaf(d, Ks[s2][j0 + r], v[r]);
             }
         }
-        st_rows_cs<CPL>(S + size_t(i) * D + j0, v[u]);
+        if constexpr (CPL == 4) {
+            *reinterpret_cast<float4*>(Sl + i * D + j0) = make_float4(v[0], v[1], v[2], v[3]);
+        } else {
+#pragma unroll
+            for (int r = 0; r < CPL; ++r) Sl[i * D + j0 + r] = v[r];
+        }
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // the bulk store reads them
+    __syncthreads();
+    if (tid == 0) {
+#pragma unroll 1
+        for (size_t o = 0; o < Sm::SLICE; o += Sm::CHUNK)
+            bulk_s2g(reinterpret_cast<unsigned char*>(S) + o, rb_smem + o, uint32_t(Sm::CHUNK));
+        bulk_commit();
     }
 
     // conv state: last W-1 rows of (conv_state ++ accepted raw rows); channels split over heads
@@ -165,12 +189,21 @@ gdn_rollback_kernel(const RollbackArgs a) {
         for (int r = 0; r < 3; ++r)
             if (r < W - 1) cs[size_t(r) * C + c] = vals[r];
     }
+    if (tid == 0) bulk_wait_read_all();   // the slice stays until the store has read it
 }
 
 template <typename IO, int D, int NMAX, bool PATH>
 static cudaError_t launch_rb(const RollbackArgs& a, cudaStream_t s) {
+    constexpr size_t SMEM = RbSmem<D, NMAX>::BYTES;
+    auto kern = gdn_rollback_kernel<IO, D, NMAX, PATH>;
+    static bool attr_done = false;   // benign race: setting the attribute twice is harmless
+    if (!attr_done) {
+        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(SMEM));
+        if (e != cudaSuccess) return e;
+        attr_done = true;
+    }
     dim3 grid(a.Hv, a.B, a.L);
-    gdn_rollback_kernel<IO, D, NMAX, PATH><<<grid, 256, 0, s>>>(a);
+    kern<<<grid, 256, SMEM, s>>>(a);
     return cudaGetLastError();
 }
 
