@@ -342,7 +342,7 @@ def run_gpu(args, w, world, rank, device):
     pool = make_pool(w, seed, device, POOL)
     r = SpecRound(w, device)
     stream = torch.cuda.current_stream(device)
-    fused = not args.separate and w.accept != "tree"
+    fused = args.fused and not args.separate and w.accept != "tree"
 
     def step(k, rnd, evs=None):
         s = pool[k % POOL]
@@ -491,9 +491,11 @@ def main(argv=None):
     ap.add_argument("--config", type=int, default=DEFAULT_CONFIG)
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--fused", action="store_true",
+                    help="time the fused step (gdn_rollback_verify + accept) instead of the "
+                         "default three calls (verify / accept / rollback)")
     ap.add_argument("--separate", action="store_true",
-                    help="time verify / accept / rollback as three calls instead of the fused "
-                         "step (gdn_rollback_verify + accept)")
+                    help="the three calls (the default; overrides --fused)")
     ap.add_argument("--e2e-steps", type=int, default=50)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
