@@ -897,13 +897,16 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
               constexpr int NTN = (TMAX + 7) / 8, TPW = Cfg::GRAM_TILES / 4;
               static_assert(TPW == 1 || NTN == 4, "a warp's tiles share their column block");
               const int nt = pw % NTN;
-              float acc[TPW][4], acl[TPW][4];
+              // one tile per warp: four accumulator sets, rotated over the K-steps
+              constexpr int NACC = TPW == 1 ? 4 : 1, KUNROLL = TPW == 1 ? 4 : 2;
+              float acc[TPW * NACC][4], acl[TPW * NACC][4];
 #pragma unroll
-              for (int m = 0; m < TPW; ++m)
+              for (int m = 0; m < TPW * NACC; ++m)
 #pragma unroll
                   for (int e = 0; e < 4; ++e) { acc[m][e] = 0.f; acl[m][e] = 0.f; }
-#pragma unroll 2
+#pragma unroll (KUNROLL)
               for (int ks = 0; ks < 16; ++ks) {
+                const int ka = NACC == 1 ? 0 : (ks & 3);
                 const int ch = 8 * ks + gt4;
                 const float bv0 = *reinterpret_cast<const float*>(Xb + sw128_off(8 * nt + gq, ch, XKB));
                 const float bv1 = *reinterpret_cast<const float*>(Xb + sw128_off(8 * nt + gq, ch + 4, XKB));
@@ -928,13 +931,17 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
                 }
 #pragma unroll
                 for (int m = 0; m < TPW; ++m) {
-                    mma_tf32_16x8x8(acc[m], ahi[m], __float_as_uint(bh0), __float_as_uint(bh1));
-                    mma_tf32_16x8x8(acl[m], ahi[m], bl0, bl1);
+                    mma_tf32_16x8x8(acc[m + ka], ahi[m], __float_as_uint(bh0), __float_as_uint(bh1));
+                    mma_tf32_16x8x8(acl[m + ka], ahi[m], bl0, bl1);
                 }
 #pragma unroll
                 for (int m = 0; m < TPW; ++m)
-                    mma_tf32_16x8x8(acc[m], alo[m], __float_as_uint(bh0), __float_as_uint(bh1));
+                    mma_tf32_16x8x8(acc[m + ka], alo[m], __float_as_uint(bh0), __float_as_uint(bh1));
               }
+#pragma unroll
+              for (int q2 = 1; q2 < NACC; ++q2)
+#pragma unroll
+                  for (int e = 0; e < 4; ++e) { acc[0][e] += acc[q2][e]; acl[0][e] += acl[q2][e]; }
               // Gr[a][c] = k_a · X_c = D[c][a]
 #pragma unroll
               for (int m = 0; m < TPW; ++m) {
@@ -1051,6 +1058,25 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
                     }
                 }
             } else {
+            if constexpr (TMAX >= 16) {
+            // per (value head, position v), walking back over x = v-1 .. 0: CK[v][x] =
+            // Γ(x+1..v-1) k_x·k_v and CQ[v][x] = Γ(x+1..v-1) k_x·q_v; c0[v] = Γ(0..v-1), k_v·q_v
+            for (int idx = p; idx < G * TMAX; idx += 128) {
+                const int fj = idx / TMAX, fv = idx - fj * TMAX;
+                if (fv < T) {
+                    const float* hrec = meta + Cfg::M_REC + fj * TMAX * RS;     // γ at [y * RS + 1]
+                    float* rec = meta + Cfg::M_REC + idx * RS;
+                    float coef = 1.f;
+                    for (int fx = fv - 1; fx >= 0; --fx) {
+                        rec[4 + fx] = coef * gram[fx * 2 * TMAX + fv];
+                        rec[4 + TMAX + fx] = coef * gram[fx * 2 * TMAX + TMAX + fv];
+                        coef *= hrec[fx * RS + 1];
+                    }
+                    rec[0] = coef;
+                    rec[3] = gram[fv * 2 * TMAX + TMAX + fv];
+                }
+            }
+            } else {
             // per value head, one thread per (v, x ≤ v): CK[v][x] = Γ(x→v-1) k_x·k_v and
             // CQ[v][x] = Γ(x→v-1) k_x·q_v for x < v; c0[v] = Γ(root→v-1) and k_v·q_v for x = v
             for (int idx = p; idx < G * TMAX * TMAX; idx += 128) {
@@ -1071,6 +1097,7 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
                         rec[3] = gram[fv * 2 * TMAX + TMAX + fv];
                     }
                 }
+            }
             }
             }
             named_bar(1, 128);
