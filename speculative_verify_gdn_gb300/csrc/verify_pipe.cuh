@@ -391,6 +391,165 @@ __device__ __forceinline__ void tree_vconv_tmem(int i, const IO* qs, const IO* c
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// Gram block and coefficient records of a chain unit (the epilogue warps run this for chains of
+// 16 positions, where the prep warps are the busiest role; the prep warps run the same code for
+// the other shapes): 128 threads, w4 = warp in the group, t128 = thread in the group, named
+// barrier `bar` among them.
+template <typename Cfg>
+__device__ __forceinline__ void chain_gram_fold(int w4, int lane, int t128, int bar, int T,
+                                                const unsigned char* Xb, float* meta, float* gram,
+                                                float* gp) {
+    constexpr int TMAX = Cfg::TMAX_, G = Cfg::NPARTS - 2, RS = Cfg::RS, XKB = Cfg::XKB;
+    const int gq = lane >> 2, gt4 = lane & 3;
+    // Gram block on the warp tensor path: D[m][n] = X_m · k_n, 3xTF32 (hi·hi + hi·lo + lo·hi);
+    // rows m: k_0.., q_0.. (zero beyond 2 TMAX). One 16 x 8 tile: each warp takes 32 channels
+    // and the partials are summed; four tiles (TMAX = 16): warp w4 takes tile w4, all channels.
+    if constexpr (Cfg::GRAM_TILES >= 4) {
+      // a warp's tiles (one, or four sharing the column block k_{8 w4 ..}) in one pass over
+      // the channels, hi·hi + lo·hi and hi·lo in separate accumulators: 2 TPW independent
+      // chains
+      constexpr int NTN = (TMAX + 7) / 8, TPW = Cfg::GRAM_TILES / 4;
+      static_assert(TPW == 1 || NTN == 4, "a warp's tiles share their column block");
+      const int nt = w4 % NTN;
+      // one tile per warp: four accumulator sets, rotated over the K-steps
+      constexpr int NACC = TPW == 1 ? 4 : 1, KUNROLL = TPW == 1 ? 4 : 2;
+      float acc[TPW * NACC][4], acl[TPW * NACC][4];
+#pragma unroll
+      for (int m = 0; m < TPW * NACC; ++m)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) { acc[m][e] = 0.f; acl[m][e] = 0.f; }
+#pragma unroll (KUNROLL)
+      for (int ks = 0; ks < 16; ++ks) {
+        const int ka = NACC == 1 ? 0 : (ks & 3);
+        const int ch = 8 * ks + gt4;
+        const float bv0 = *reinterpret_cast<const float*>(Xb + sw128_off(8 * nt + gq, ch, XKB));
+        const float bv1 = *reinterpret_cast<const float*>(Xb + sw128_off(8 * nt + gq, ch + 4, XKB));
+        const float bh0 = tf32_trunc(bv0), bh1 = tf32_trunc(bv1);
+        const uint32_t bl0 = __float_as_uint(tf32_trunc(bv0 - bh0));
+        const uint32_t bl1 = __float_as_uint(tf32_trunc(bv1 - bh1));
+        uint32_t ahi[TPW][4], alo[TPW][4];
+#pragma unroll
+        for (int m = 0; m < TPW; ++m) {
+            const int mt = TPW == 1 ? w4 / NTN : m;
+            float av[4];
+            av[0] = *reinterpret_cast<const float*>(Xb + sw128_off(16 * mt + gq, ch, XKB));
+            av[2] = *reinterpret_cast<const float*>(Xb + sw128_off(16 * mt + gq, ch + 4, XKB));
+            av[1] = *reinterpret_cast<const float*>(Xb + sw128_off(16 * mt + gq + 8, ch, XKB));
+            av[3] = *reinterpret_cast<const float*>(Xb + sw128_off(16 * mt + gq + 8, ch + 4, XKB));
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float h = tf32_trunc(av[e]);
+                ahi[m][e] = __float_as_uint(h);
+                alo[m][e] = __float_as_uint(tf32_trunc(av[e] - h));
+            }
+        }
+#pragma unroll
+        for (int m = 0; m < TPW; ++m) {
+            mma_tf32_16x8x8(acc[m + ka], ahi[m], __float_as_uint(bh0), __float_as_uint(bh1));
+            mma_tf32_16x8x8(acl[m + ka], ahi[m], bl0, bl1);
+        }
+#pragma unroll
+        for (int m = 0; m < TPW; ++m)
+            mma_tf32_16x8x8(acc[m + ka], alo[m], __float_as_uint(bh0), __float_as_uint(bh1));
+      }
+#pragma unroll
+      for (int q2 = 1; q2 < NACC; ++q2)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) { acc[0][e] += acc[q2][e]; acl[0][e] += acl[q2][e]; }
+      // Gr[a][c] = k_a · X_c = D[c][a]
+#pragma unroll
+      for (int m = 0; m < TPW; ++m) {
+        const int mt = TPW == 1 ? w4 / NTN : m;
+        const int c0 = 16 * mt + gq, a0 = 8 * nt + 2 * gt4;
+        gram[a0 * 2 * TMAX + c0] = acc[m][0] + acl[m][0];
+        gram[(a0 + 1) * 2 * TMAX + c0] = acc[m][1] + acl[m][1];
+        gram[a0 * 2 * TMAX + c0 + 8] = acc[m][2] + acl[m][2];
+        gram[(a0 + 1) * 2 * TMAX + c0 + 8] = acc[m][3] + acl[m][3];
+      }
+    } else {
+      {
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+            const int ch = 32 * w4 + 8 * ks + gt4;
+            float av[4];
+            av[0] = *reinterpret_cast<const float*>(Xb + sw128_off(gq, ch, XKB));
+            av[2] = *reinterpret_cast<const float*>(Xb + sw128_off(gq, ch + 4, XKB));
+            av[1] = (gq + 8 < 2 * TMAX) ? *reinterpret_cast<const float*>(Xb + sw128_off(gq + 8, ch, XKB)) : 0.f;
+            av[3] = (gq + 8 < 2 * TMAX) ? *reinterpret_cast<const float*>(Xb + sw128_off(gq + 8, ch + 4, XKB)) : 0.f;
+            const float bv0 = gq < TMAX ? av[0] : 0.f, bv1 = gq < TMAX ? av[2] : 0.f;
+            uint32_t ahi[4], alo[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float h = tf32_trunc(av[e]);
+                ahi[e] = __float_as_uint(h);
+                alo[e] = __float_as_uint(tf32_trunc(av[e] - h));
+            }
+            const float bh0 = tf32_trunc(bv0), bh1 = tf32_trunc(bv1);
+            const uint32_t bl0 = __float_as_uint(tf32_trunc(bv0 - bh0));
+            const uint32_t bl1 = __float_as_uint(tf32_trunc(bv1 - bh1));
+            mma_tf32_16x8x8(acc, ahi, __float_as_uint(bh0), __float_as_uint(bh1));
+            mma_tf32_16x8x8(acc, ahi, bl0, bl1);
+            mma_tf32_16x8x8(acc, alo, __float_as_uint(bh0), __float_as_uint(bh1));
+        }
+        float* g4 = gp + w4 * 128;
+        g4[gq * 8 + 2 * gt4] = acc[0];
+        g4[gq * 8 + 2 * gt4 + 1] = acc[1];
+        g4[(gq + 8) * 8 + 2 * gt4] = acc[2];
+        g4[(gq + 8) * 8 + 2 * gt4 + 1] = acc[3];
+      }
+      named_bar(bar, 128);
+      {
+        const int m = t128 >> 3, nn = t128 & 7;
+        if (m < 2 * TMAX && nn < TMAX)
+            gram[nn * 2 * TMAX + m] = gp[t128] + gp[128 + t128] + gp[256 + t128] + gp[384 + t128];
+      }
+    }
+    named_bar(bar, 128);
+    if constexpr (TMAX >= 16) {
+    // per (value head, position v), walking back over x = v-1 .. 0: CK[v][x] =
+    // Γ(x+1..v-1) k_x·k_v and CQ[v][x] = Γ(x+1..v-1) k_x·q_v; c0[v] = Γ(0..v-1), k_v·q_v
+    for (int idx = t128; idx < G * TMAX; idx += 128) {
+        const int fj = idx / TMAX, fv = idx - fj * TMAX;
+        if (fv < T) {
+            const float* hrec = meta + Cfg::M_REC + fj * TMAX * RS;     // γ at [y * RS + 1]
+            float* rec = meta + Cfg::M_REC + idx * RS;
+            float coef = 1.f;
+            for (int fx = fv - 1; fx >= 0; --fx) {
+                rec[4 + fx] = coef * gram[fx * 2 * TMAX + fv];
+                rec[4 + TMAX + fx] = coef * gram[fx * 2 * TMAX + TMAX + fv];
+                coef *= hrec[fx * RS + 1];
+            }
+            rec[0] = coef;
+            rec[3] = gram[fv * 2 * TMAX + TMAX + fv];
+        }
+    }
+    } else {
+    // per value head, one thread per (v, x ≤ v): CK[v][x] = Γ(x→v-1) k_x·k_v and
+    // CQ[v][x] = Γ(x→v-1) k_x·q_v for x < v; c0[v] = Γ(root→v-1) and k_v·q_v for x = v
+    for (int idx = t128; idx < G * TMAX * TMAX; idx += 128) {
+        const int fj = idx / (TMAX * TMAX), fv = (idx / TMAX) % TMAX, fx = idx % TMAX;
+        if (fv < T && fx <= fv) {
+            const float* hrec = meta + Cfg::M_REC + fj * TMAX * RS;     // γ at [y * RS + 1]
+            float* rec = meta + Cfg::M_REC + (fj * TMAX + fv) * RS;
+            const int y0 = fx < fv ? fx + 1 : 0;
+            float coef = 1.f;
+#pragma unroll
+            for (int yy = 0; yy < TMAX - 1; ++yy)
+                if (yy >= y0 && yy < fv) coef *= hrec[yy * RS + 1];
+            if (fx < fv) {
+                rec[4 + fx] = coef * gram[fx * 2 * TMAX + fv];
+                rec[4 + TMAX + fx] = coef * gram[fx * 2 * TMAX + TMAX + fv];
+            } else {
+                rec[0] = coef;
+                rec[3] = gram[fv * 2 * TMAX + TMAX + fv];
+            }
+        }
+    }
+    }
+    named_bar(bar, 128);
+}
+
 template <typename IO, int TMAX, int G, bool COMMIT, bool TREE>
 __global__ void __launch_bounds__(PipeCfg<IO, TMAX, G, COMMIT, TREE>::NTHR, 1)
 gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap smap,
@@ -887,6 +1046,7 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
             named_bar(1, 128);
             // BIG: the Gram block lives in the staging slot (its rows have been read)
             if constexpr (Cfg::BIG) gram = meta + Cfg::M_V;
+            if constexpr (TREE || TMAX < 16) {   // 16-position chains: the epilogue warps do this
             // Gram block on the warp tensor path: D[m][n] = X_m · k_n, 3xTF32 (hi·hi + hi·lo + lo·hi);
             // rows m: k_0.., q_0.. (zero beyond 2 TMAX). One 16 x 8 tile: each warp takes 32 channels
             // and the partials are summed; four tiles (TMAX = 16): warp pw takes tile pw, all channels.
@@ -1100,6 +1260,7 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
             }
             }
             }
+            }
             named_bar(1, 128);
             if (p == 0) mbar_arrive(&ufull[us]);
             if constexpr (Cfg::BIG) {
@@ -1284,6 +1445,10 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
             }
             if (COMMIT) pwait(&kpfull[iu & 1], (iu >> 1) & 1, abort_flag, a.status);
             pwait(&ufull[us], (iu / NXS) & 1, abort_flag, a.status);
+            if constexpr (!TREE && TMAX >= 16)   // 16-position chains: Gram block and records here
+                chain_gram_fold<Cfg>(warp - 10, lane, tid - 320, 2, T,
+                                     smem + Cfg::OFF_X + size_t(us) * Cfg::X_BYTES,
+                                     const_cast<float*>(meta), scr + Cfg::S_GRAM, scr + Cfg::S_GP);
             if (COMMIT && n > 0) {
                 const int et = tid - 320, ew = warp - 10;
                 // the new conv-state rows, stashed by the prep warps, to HBM as 16-byte vectors
