@@ -435,50 +435,82 @@ def run_gpu(args, w, world, rank, device):
 
 
 def run_e2e(args, w, r, pool, cw, state, conv_state, device, seed, fused=False):
+    """The round through the public API with host-resident inputs, as a serving loop runs it:
+    each step's inputs are copied from pinned host memory on a copy stream (step k+1's copy
+    overlaps step k's kernels; three device sets, since a fused step also reads the previous
+    round's set) and the accept results are copied back after each step. Every copy of the K
+    steps lies inside the timed region."""
     import torch
     keys = ("qkv", "g", "beta", "logits", "drafts")
     host = []
     for s in pool[:2]:
         host.append({k: s[k].cpu().pin_memory() for k in keys})
-    # two device sets: a fused step commits the previous round from its qkv / g
-    devs = [{k: torch.empty_like(pool[0][k]) for k in keys} for _ in range(2)]
+    NS = 3
+    devs = [{k: torch.empty_like(pool[0][k]) for k in keys} for _ in range(NS)]
     parent = pool[0]["parent"]
     out_h = torch.empty((w.B, r.out_tokens.shape[1]), dtype=torch.int32).pin_memory()
     n_h = torch.empty((w.B,), dtype=torch.int32).pin_memory()
     stream = torch.cuda.current_stream(device)
+    # several copy streams, each taking a slice of every input (more than one copy engine)
+    NCS = max(1, args.e2e_copy_streams)
+    copy_streams = [torch.cuda.Stream(device) for _ in range(NCS)]
+    copied = [[torch.cuda.Event() for _ in range(NCS)] for _ in range(NS)]
+    done = [torch.cuda.Event() for _ in range(NS)]
     h2d = sum(host[0][k].numel() * host[0][k].element_size() for k in keys)
     d2h = out_h.numel() * 4 + n_h.numel() * 4
     K = max(3, min(args.steps, args.e2e_steps))
 
-    def step(k):
-        hs = host[k % len(host)]
-        dev = devs[k % 2]
-        for key in keys:
-            dev[key].copy_(hs[key], non_blocking=True)
+    def issue_copy(k):
+        hs, dev = host[k % len(host)], devs[k % NS]
+        for c, cs in enumerate(copy_streams):
+            with torch.cuda.stream(cs):
+                if k >= 2:
+                    cs.wait_event(done[(k - 2) % NS])        # this set's last readers are done
+                for key in keys:
+                    n0 = hs[key].shape[0]
+                    lo, hi = n0 * c // NCS, n0 * (c + 1) // NCS
+                    if hi > lo:
+                        dev[key][lo:hi].copy_(hs[key][lo:hi], non_blocking=True)
+                copied[k % NS][c].record(cs)
+
+    def run_step(k):
+        dev = devs[k % NS]
+        for ev in copied[k % NS]:
+            stream.wait_event(ev)
         if fused:
             r.step_fused(dev["qkv"], dev["g"], dev["beta"], dev["logits"], dev["drafts"], cw,
                          state, conv_state, round_=k, seed=seed)
         else:
             r.step(dev["qkv"], dev["g"], dev["beta"], dev["logits"], dev["drafts"], cw, state,
                    conv_state, round_=k, seed=seed, parent=parent)
+        done[k % NS].record(stream)
         n_h.copy_(r.n_acc, non_blocking=True)
         out_h.copy_(r.out_tokens, non_blocking=True)
 
-    for k in range(2):
-        step(k)
+    def run(nsteps, t0=None):
+        if t0 is not None:
+            for cs in copy_streams:
+                cs.wait_event(t0)                          # the first copies start after t0
+        issue_copy(0)
+        for k in range(nsteps):
+            if k + 1 < nsteps:
+                issue_copy(k + 1)
+            run_step(k)
+
+    run(2)
     torch.cuda.synchronize(device)
     barrier(device)
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     t0.record(stream)
-    for k in range(K):
-        step(k)
+    run(K, t0)
     t1.record(stream)
     torch.cuda.synchronize(device)
     ms = reduce_max(t0.elapsed_time(t1), device) / K
     world = dist_env()[0]
     return {"value": aggregate_tokens_per_s(world, w.B, w.N, ms), "unit": UNIT,
-            "ms_per_step": ms, "steps": K, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+            "ms_per_step": ms, "steps": K, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "copies": "inputs on %d copy streams, step k+1's overlapping step k's kernels" % NCS}
 
 
 # ------------------------------------------------------------------------------ main
@@ -497,6 +529,7 @@ def main(argv=None):
     ap.add_argument("--separate", action="store_true",
                     help="the three calls (the default; overrides --fused)")
     ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--e2e-copy-streams", type=int, default=1)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0)
     ap.add_argument("--batch", type=int, default=None,
