@@ -107,6 +107,45 @@ def test_rollback_matches_oracle(gdnlib, D, T):
     assert torch.equal(dst[:, 0].cpu(), st[:, 0])
 
 
+@pytest.mark.parametrize("D,T,W", [(128, 8, 1), (128, 8, 2), (64, 6, 3), (32, 16, 2)])
+def test_rollback_conv_widths(gdnlib, D, T, W):
+    """Shorter conv windows: fewer conv-state rows rebuilt (W - 1 of them, none for W = 1)."""
+    w = small(I.WORKLOADS[1], L=2, B=4, N=T, Hk=2, Hv=4, D=D, W=W, V=64)
+    r, ref, host, dev = run_verify_case(w, seed=3 * W + T)
+    qkv, cw, cs, g, beta, st = host
+    dq, dcw, dcs, dg, db, dst = dev
+    n = np.array([T, 1, 0, T - 1], np.int32)
+    r.n_acc.copy_(torch.from_numpy(n))
+    r.rollback(dq, dg, dst, dcs)
+    r.check_status()
+    st_ref, cs_ref, bad = oracle_rollback(w, n, ref, g, qkv, st, cs)
+    assert bad == 0
+    assert_close(f64(dst), st_ref, "state")
+    assert np.array_equal(f64(dcs), cs_ref)
+
+
+def test_rollback_path_bad_node_sets_status_and_skips(gdnlib):
+    """A path entry outside [0, T) is reported and that sequence's state is left as it was; the
+    other sequence commits normally."""
+    w, par = tree_case(B=2, T=8, D=128, depth=4)
+    r, ref, host, dev = run_verify_case(w, parent=par)
+    qkv, cw, cs, g, beta, st = host
+    dq, dcw, dcs, dg, db, dst = dev
+    path = np.zeros((w.B, r.path.shape[1]), np.int32)
+    path[0, :2] = [0, 1]
+    path[1, :2] = [0, 9]                       # node 9 does not exist (T = 8)
+    r.path.copy_(torch.from_numpy(path))
+    r.n_acc.copy_(torch.tensor([2, 2], dtype=torch.int32))
+    before = dst.clone()
+    r.rollback(dq, dg, dst, dcs)
+    torch.cuda.synchronize()
+    assert int(r.status.item()) & 0x8
+    assert torch.equal(dst[:, 1].cpu(), before[:, 1].cpu())
+    st_ref, _, bad = oracle_rollback(w, np.array([2, 0], np.int32), ref, g, qkv, st, cs,
+                                     path=path)
+    assert_close(f64(dst[:, :1]), st_ref[:, :1], "state of the valid sequence")
+
+
 def test_rollback_bad_count_sets_status_and_skips(gdnlib):
     w = small(I.WORKLOADS[1], L=1, B=2, N=4, Hk=2, Hv=4, D=32, V=64)
     r, ref, host, dev = run_verify_case(w)
