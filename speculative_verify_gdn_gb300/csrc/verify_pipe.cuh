@@ -1,5 +1,6 @@
 // verify_pipe.cuh — persistent, warp-specialised gdn_verify for the Qwen3.6 head shape
-// (Dk = Dv = 128, chain of T <= 8 positions, bf16 I/O, up to 2 value heads per key head).
+// (Dk = Dv = 128, bf16 I/O, up to 2 value heads per key head; chains of T <= 16 positions, trees
+// of T <= 32 nodes, and the fused rollback + verify for chains of T <= 8).
 //
 // Same computation as verify_impl.cuh (see its header for the method and the sources): per value
 // head, P = S_0·[K|Q] in three TF32 products on tcgen05, the Gram block, and the per-row
@@ -20,7 +21,9 @@
 //                              value head, even and odd K-steps) in turn, so that consecutive MMAs
 //                              never update the same accumulator (2 unit slots of P in TMEM)
 //   warps 2-5    prep          per unit: conv + SiLU, norms, the [X_hi ; X_lo] tile, the Gram block
-//                              (mma.sync, 3xTF32) and each value head's coefficient records
+//                              (mma.sync, 3xTF32) and each value head's coefficient records (for
+//                              16-position chains the Gram block and records are the epilogue
+//                              warps' first task, while the unit's products run)
 //   warps 10-13  epilogue      per head: P rows from TMEM (sum of its partial accumulators),
 //                              recurrence, o and δ stores
 //
@@ -35,13 +38,21 @@
 // committed state. With n = n_acc_prev[b], c_s = Γ(s+1 .. n-1), Γ = Γ(0 .. n-1) and the rank-n
 // term A Kᵀ (A[i][s] = c_s δ_s[i], K[j][s] = k_s[j] of the previous round):
 //     S_n = Γ · S_0 + A Kᵀ,        S_n · X = Γ · (S_0 · X) + A · (Kᵀ X).
-// So the tensor-core products still run on the loaded S_0; the prep warps add Kᵀ X (n x 2T, beside
-// the Gram block) and the epilogue applies Γ and A · (Kᵀ X) to each P row. For the write-back the
-// convert warps form S_n = Γ S_0 + A Kᵀ of each K-block in shared memory with warp-level mma.sync
-// (3xTF32, K = 8) and a store warp (warp 15) writes it back by TMA store. The conv window is the last
-// W-1 rows of (old conv state ++ the previous round's accepted raw rows), staged from both buffers;
-// the prep warps write those rows back as the new conv state. So each state tile is read once and
-// written once per round, instead of read by verify, read and written by rollback.
+// So the tensor-core products still run on the loaded S_0; the epilogue forms Kᵀ X (n x 2T,
+// mma.sync) and applies Γ and A · (Kᵀ X) to each P row. For the write-back the convert warps form
+// S_n = Γ S_0 + A Kᵀ of each K-block in shared memory with warp-level mma.sync (3xTF32, K = 8) and
+// a store warp (warp 15) writes it back by TMA store. The conv window is the last W-1 rows of (old
+// conv state ++ the previous round's accepted raw rows), staged from both buffers; the prep warps
+// stash those rows and the epilogue writes them out as the new conv state. So each state tile is
+// read once and written once per round, instead of read by verify, read and written by rollback.
+//
+// TREE: node v's products come from the same S_0 · [K|Q] through the ancestor-sum identity
+// (S_p k_v = Γ(root→p) S_0 k_v + Σ_{a ancestor of v} Γ(a→p) δ_a (k_a·k_v), the same with q_v): the
+// coefficient records hold Γ(a→p) times the Gram entry for ancestors and zero elsewhere, and each
+// node's conv window is itself, its nearest ancestors, then the conv state's rows. The B tile keeps
+// raw q, k; the inverse norms go into the coefficients. T = 32 (BIG) keeps one B-tile / meta slot:
+// the next unit's prep starts once this unit's products are done and waits for this unit's
+// epilogue only before writing its records; the epilogue warps compute v into TMEM themselves.
 #pragma once
 
 #include "verify_impl.cuh"
@@ -51,8 +62,8 @@ namespace gdn {
 template <typename IO, int TMAX, int G, bool COMMIT, bool TREE>
 struct PipeCfg {
     static constexpr int D = 128, KB = 4, ES = int(sizeof(IO)), TMAX_ = TMAX;
-    // T up to 32 (trees): one slot each for the B tile, the records and the staging (a unit's
-    // prologue then waits for the previous unit's epilogue), one accumulator per chain
+    // T up to 32 (trees): one slot each for the B tile, the records and the staging (the next
+    // unit's prep overlaps this unit's epilogue; see the kernel), one accumulator per chain
     static constexpr bool BIG = TMAX >= 32;
     static constexpr int NXS = BIG ? 1 : 2;                  // B-tile / meta slots
     static constexpr int NSS = BIG ? 1 : 2;                  // staging slots
@@ -111,8 +122,8 @@ struct PipeCfg {
     // split over the 4 prep warps by channels, or 4 / 16 tiles (TMAX = 16 / 32), a quarter per warp
     static constexpr int GRAM_TILES = ((2 * TMAX + 15) / 16) * ((TMAX + 7) / 8);
     // prep scratch (floats): norm partials [4][2TMAX], inverse norms [2TMAX], Gram partials
-    // [4 warps][16][8] (one-tile case), Gram [TMAX][2TMAX] (BIG: in the staging slot, which the
-    // conv has finished with), tree parents [TMAX] and conv-window rows [TMAX][4] (ints)
+    // [4 warps][16][8] (one-tile case), Gram [TMAX][2TMAX] (BIG: in the meta slot instead),
+    // tree parents [TMAX] and conv-window offsets [TMAX][4] (ints)
     // (COMMIT) epilogue: partials of k'_s · X_c [4 warps][16][8]
     static constexpr int S_NRM = 0, S_INV = S_NRM + 8 * TMAX, S_GP = S_INV + 2 * TMAX,
                          S_GRAM = S_GP + (GRAM_TILES == 1 ? 4 * 128 : 0),
@@ -1044,7 +1055,7 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
             }   // chain
             fence_async_smem();
             named_bar(1, 128);
-            // BIG: the Gram block lives in the staging slot (its rows have been read)
+            // BIG: the Gram block lives in the meta slot
             if constexpr (Cfg::BIG) gram = meta + Cfg::M_V;
             if constexpr (TREE || TMAX < 16) {   // 16-position chains: the epilogue warps do this
             // Gram block on the warp tensor path: D[m][n] = X_m · k_n, 3xTF32 (hi·hi + hi·lo + lo·hi);
