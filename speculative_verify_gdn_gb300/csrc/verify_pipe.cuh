@@ -727,18 +727,23 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
                 const int ks = iu & 1;
                 float* kp = reinterpret_cast<float*>(smem + Cfg::OFF_KP + size_t(ks) * Cfg::KP_BYTES);
                 if (!pwait_warp(&kpempty[ks], ((iu >> 1) & 1) ^ 1, abort_flag, a.status)) break;
+                {
+                    // c_s = Γ(s+1 .. n-1) and Γ(0 .. n-1) by a suffix-product scan over the lanes
+                    // (lane j TMAX + s holds g'_s, 1 for s >= n): log2(TMAX) steps instead of a
+                    // chain of TMAX shuffles
+                    const int sj = lane / TMAX, ss2 = lane - sj * TMAX;
+                    float x = gv;                    // becomes Π_{r = s .. TMAX-1} g'_r
 #pragma unroll
-                for (int j = 0; j < G; ++j) {
-                    float c = 1.f;                   // the rollback kernel's order: c_s = Γ(s+1 .. n-1)
-#pragma unroll
-                    for (int s2 = TMAX - 1; s2 >= 0; --s2) {
-                        const float gsv = __shfl_sync(0xffffffffu, gv, j * TMAX + s2);
-                        if (s2 < n) {
-                            if (lane == 0) kp[Cfg::KP_C + j * TMAX + s2] = c;
-                            c *= gsv;
-                        }
+                    for (int o = 1; o < TMAX; o <<= 1) {
+                        const float y = __shfl_down_sync(0xffffffffu, x, o);
+                        if (ss2 + o < TMAX) x *= y;
                     }
-                    if (lane == 0) kp[Cfg::KP_GAM + j] = c;
+                    const float nx = __shfl_down_sync(0xffffffffu, x, 1);
+                    const float cs = ss2 + 1 < TMAX ? nx : 1.f;
+                    if (sj < G) {
+                        if (ss2 < n) kp[Cfg::KP_C + sj * TMAX + ss2] = cs;
+                        if (ss2 == 0) kp[Cfg::KP_GAM + sj] = x;
+                    }
                 }
                 __syncwarp();
                 if (lane == 0) {
