@@ -236,6 +236,22 @@ GDN_API int spec_accept(const spec_dims* d, const void* logits, const int32_t* d
 GDN_API size_t spec_workspace_bytes(const spec_dims* d, int32_t mode);
 
 /*
+ * spec_stats_accumulate — acceptance statistics for an adaptive speculation switch (colibrì
+ * ch.08 §4.1: drafting is turned off once enough drafts were proposed and fewer than one in ten
+ * was accepted; the policy itself is the caller's, see speculative_verify_gdn_gb300.adaptive).
+ *   B, N    sequences and drafts per sequence of the spec_accept / spec_accept_tree call
+ *   n_acc   [B] int32 device, the accepted counts that call wrote (n in [0, N])
+ *   stats   [N + 3] uint64 device, accumulated across calls (the caller zeroes it once):
+ *           stats[0] += B·N proposed drafts, stats[1] += Σ n accepted drafts,
+ *           stats[2 + k] += number of sequences with n = k (k = 0 .. N)
+ *   status  optional device word: a count outside [0, N] sets GDN_STATUS_BAD_NACC and adds
+ *           nothing but its N proposals
+ * One small kernel on `stream`; never synchronises. B = 0 is a no-op.
+ */
+GDN_API int spec_stats_accumulate(int32_t B, int32_t N, const int32_t* n_acc, uint64_t* stats,
+                                  uint32_t* status, void* stream);
+
+/*
  * spec_accept_tree — greedy acceptance of the longest matching root-to-leaf path of a draft
  * tree (GDN investigation §2.2 / §8: DDTree verification). Rows: row 0 judges the children of
  * the committed context, row 1+v judges the children of node v. From the context, repeatedly

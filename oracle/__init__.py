@@ -16,4 +16,6 @@ from .oracle import (  # noqa: F401
     weights,
     philox4x32_10,
     draw,
+    accept_stats,
+    adaptive_enabled,
 )

@@ -227,3 +227,27 @@ def philox4x32_10(ctr, key):
 def draw(seed, round_, seq, row, purpose, Z):
     return int(_load().oracle_draw(int(seed), int(round_) & 0xFFFFFFFF, int(seq), int(row),
                                    int(purpose), int(Z)))
+
+
+def accept_stats(calls, N):
+    """Acceptance counters over a sequence of accept calls (colibrì ch.08 §4.1 counts proposals
+    and acceptances): proposed = Σ B·N, accepted = Σ n, hist[k] = #sequences with n = k. A count
+    outside [0, N] adds only its N proposals; the returned flag says whether any was seen."""
+    proposed, accepted, hist, bad = 0, 0, [0] * (N + 1), False
+    for n_acc in calls:
+        for n in [int(x) for x in n_acc]:
+            proposed += N
+            if n < 0 or n > N:
+                bad = True
+                continue
+            accepted += n
+            hist[n] += 1
+    return proposed, accepted, hist, bad
+
+
+def adaptive_enabled(proposed, accepted, min_proposed=24, num=1, den=10):
+    """The off-switch rule as the page states it: drafting stops once at least min_proposed
+    drafts were proposed and accepted * 10 < proposed (num / den generalises the 1/10)."""
+    if proposed < min_proposed:
+        return True
+    return not (accepted * den < proposed * num)

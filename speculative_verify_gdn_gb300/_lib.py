@@ -31,7 +31,7 @@ STATUS_BITS = {
 # exported entry points of include/gdnspec.h
 EXPORTS = ("gdn_verify", "gdn_verify_tree", "gdn_rollback", "gdn_rollback_path",
            "gdn_rollback_verify", "gdn_tape_bytes", "spec_accept", "spec_workspace_bytes", "spec_accept_tree",
-           "spec_accept_static", "gdn_last_error")
+           "spec_accept_static", "spec_stats_accumulate", "gdn_last_error")
 
 
 class GdnError(RuntimeError):
@@ -85,6 +85,8 @@ def load(require_file=True):
     lib.spec_accept_tree.restype = ct.c_int
     lib.spec_accept_static.argtypes = [P, P, P, i32, f32, u64, u64, P, P, P, P]
     lib.spec_accept_static.restype = ct.c_int
+    lib.spec_stats_accumulate.argtypes = [i32, i32, P, P, P, P]
+    lib.spec_stats_accumulate.restype = ct.c_int
     lib.gdn_last_error.argtypes = []
     lib.gdn_last_error.restype = ct.c_char_p
     _lib = lib
@@ -286,6 +288,16 @@ def spec_accept(logits, drafts, n_acc, out_tokens, workspace, mode=SPEC_MODE_GRE
                          _ptr(out_tokens, torch.int32, (B, N + 1), "out_tokens"),
                          _ptr(status, torch.int32, None, "status"), _stream(stream))
     _check(rc, "spec_accept")
+
+
+def spec_stats_accumulate(n_acc, N, stats, status=None, stream=None):
+    """spec_stats_accumulate: stats (int64 [N + 3], holding the uint64 counters) += proposed,
+    accepted and the histogram of accepted lengths of this call's n_acc ([B] int32)."""
+    B = int(n_acc.shape[0]) if n_acc.dim() == 1 else -1
+    rc = load().spec_stats_accumulate(B, int(N), _ptr(n_acc, torch.int32, (B,), "n_acc"),
+                                      _ptr(stats, torch.int64, (int(N) + 3,), "stats"),
+                                      _ptr(status, torch.int32, None, "status"), _stream(stream))
+    _check(rc, "spec_stats_accumulate")
 
 
 def spec_accept_tree(logits, parent, tokens, path, n_acc, out_tokens, workspace, status=None,

@@ -342,6 +342,20 @@ int spec_accept(const spec_dims* d, const void* logits, const int32_t* drafts, i
     return GDN_OK;
 }
 
+int spec_stats_accumulate(int32_t B, int32_t N, const int32_t* n_acc, uint64_t* stats,
+                          uint32_t* status, void* stream) {
+    if (B < 0 || N < 0) return fail(GDN_ERR_INVALID_ARG, "B = %d, N = %d", B, N);
+    if (N > 64) return fail(GDN_ERR_UNSUPPORTED, "N = %d > 64", N);
+    if (B == 0) return GDN_OK;
+    if (!n_acc || !stats) return fail(GDN_ERR_INVALID_ARG, "NULL pointer");
+    if (!aligned(n_acc, 4) || !aligned(stats, 8))
+        return fail(GDN_ERR_INVALID_ARG, "misaligned n_acc or stats");
+    const cudaError_t e =
+        gdn::launch_spec_stats(B, N, n_acc, stats, status, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "spec_stats_accumulate launch");
+    return GDN_OK;
+}
+
 size_t spec_workspace_bytes(const spec_dims* d, int32_t mode) {
     if (check_spec(d) != GDN_OK) return 0;
     if (mode != SPEC_MODE_GREEDY && mode != SPEC_MODE_SAMPLE) return 0;

@@ -100,5 +100,8 @@ void accept_chunking(int rows, int V, int* CH, int* CS);
 cudaError_t launch_accept_greedy(const AcceptArgs& a, int dtype, cudaStream_t s);
 cudaError_t launch_accept_sample(const AcceptArgs& a, int dtype, cudaStream_t s);
 cudaError_t launch_accept_tree(const AcceptArgs& a, int dtype, cudaStream_t s);
+// acceptance counters (spec_stats_accumulate); N <= 64
+cudaError_t launch_spec_stats(int B, int N, const int32_t* n_acc, uint64_t* stats, uint32_t* status,
+                              cudaStream_t s);
 
 }  // namespace gdn
