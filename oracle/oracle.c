@@ -117,17 +117,31 @@ void oracle_verify(const oracle_dims* dm, const int32_t* parent, const double* q
                     const double* k = y + IDX2(v, koff + hk * Dk, C);
                     const double* q = y + IDX2(v, qoff + hk * Dk, C);
                     const double* vv = y + IDX2(v, voff + h * Dv, C);
-                    const double gv = g[(lb * T + v) * Hv + h];
                     const double bv = beta[(lb * T + v) * Hv + h];
                     double* Sv = S_nodes + (size_t)v * Dv * Dk;
-                    for (int i = 0; i < Dv; ++i) {
-                        double sk = 0.0;
-                        for (int j = 0; j < Dk; ++j) sk += Sp[IDX2(i, j, Dk)] * k[j];
-                        double u = gv * sk;
-                        double delta = bv * (vv[i] - u);
-                        tape_delta[(((lb * T + v) * Hv) + h) * (size_t)Dv + i] = delta;
-                        for (int j = 0; j < Dk; ++j)
-                            Sv[IDX2(i, j, Dk)] = gv * Sp[IDX2(i, j, Dk)] + delta * k[j];
+                    if (!dm->gate_dk) {
+                        const double gv = g[(lb * T + v) * Hv + h];
+                        for (int i = 0; i < Dv; ++i) {
+                            double sk = 0.0;
+                            for (int j = 0; j < Dk; ++j) sk += Sp[IDX2(i, j, Dk)] * k[j];
+                            double u = gv * sk;
+                            double delta = bv * (vv[i] - u);
+                            tape_delta[(((lb * T + v) * Hv) + h) * (size_t)Dv + i] = delta;
+                            for (int j = 0; j < Dk; ++j)
+                                Sv[IDX2(i, j, Dk)] = gv * Sp[IDX2(i, j, Dk)] + delta * k[j];
+                        }
+                    } else {
+                        /* per-key-channel gate a_j ([GDN] §4 tape layout [B, T, Hv, Dk]): the
+                         * decayed state S_p diag(a) takes the place of g S_p */
+                        const double* av = g + ((lb * T + v) * Hv + h) * (size_t)Dk;
+                        for (int i = 0; i < Dv; ++i) {
+                            double u = 0.0;
+                            for (int j = 0; j < Dk; ++j) u += (av[j] * Sp[IDX2(i, j, Dk)]) * k[j];
+                            double delta = bv * (vv[i] - u);
+                            tape_delta[(((lb * T + v) * Hv) + h) * (size_t)Dv + i] = delta;
+                            for (int j = 0; j < Dk; ++j)
+                                Sv[IDX2(i, j, Dk)] = av[j] * Sp[IDX2(i, j, Dk)] + delta * k[j];
+                        }
                     }
                     for (int i = 0; i < Dv; ++i) {
                         double o = 0.0;
@@ -179,13 +193,21 @@ int oracle_rollback(const oracle_dims* dm, const int32_t* path, int P, const int
                 double* S = state + (lb * Hv + h) * (size_t)Dv * Dk; /* [i][j] */
                 for (int s = 0; s < n; ++s) {
                     const int t = nodes[s];
-                    const double gt = g[(lb * T + t) * Hv + h];
                     const double* dl = tape_delta + ((lb * T + t) * Hv + h) * (size_t)Dv;
                     const double* kt = tape_k + ((lb * T + t) * Hk + hk) * (size_t)Dk;
-                    /* state = state * g[t] + k[t] * tape[t], elementwise S(i,j) */
-                    for (int i = 0; i < Dv; ++i)
-                        for (int j = 0; j < Dk; ++j)
-                            S[IDX2(i, j, Dk)] = gt * S[IDX2(i, j, Dk)] + dl[i] * kt[j];
+                    /* state = state * g[t] + k[t] * tape[t], elementwise S(i,j); g[t] is one
+                     * value per head, or one per key channel j */
+                    if (!dm->gate_dk) {
+                        const double gt = g[(lb * T + t) * Hv + h];
+                        for (int i = 0; i < Dv; ++i)
+                            for (int j = 0; j < Dk; ++j)
+                                S[IDX2(i, j, Dk)] = gt * S[IDX2(i, j, Dk)] + dl[i] * kt[j];
+                    } else {
+                        const double* at = g + ((lb * T + t) * Hv + h) * (size_t)Dk;
+                        for (int i = 0; i < Dv; ++i)
+                            for (int j = 0; j < Dk; ++j)
+                                S[IDX2(i, j, Dk)] = at[j] * S[IDX2(i, j, Dk)] + dl[i] * kt[j];
+                    }
                 }
             }
             /* conv state: last W-1 raw rows of (conv_state ++ accepted qkv rows) */

@@ -15,11 +15,13 @@ extern "C" {
 typedef struct oracle_dims {
     int L, B, T, Hk, Hv, Dk, Dv, W, C;
     int act_silu;     /* 1: y = silu(conv(x)); 0: no activation (literal reading test mode) */
+    int gate_dk;      /* 0: g [L][B][T][Hv]; 1: per-key-channel gates g [L][B][T][Hv][Dk] */
     double qk_scale;
     double l2_eps;
 } oracle_dims;
 
-/* qkv [L][B][T][C], conv_w [L][C][W], conv_state [L][B][W-1][C], g/beta [L][B][T][Hv],
+/* qkv [L][B][T][C], conv_w [L][C][W], conv_state [L][B][W-1][C], g/beta [L][B][T][Hv] (g
+ * [L][B][T][Hv][Dk] when gate_dk),
  * state [L][B][Hv][Dv][Dk] (row-major S: S(i,j) at [i][j]); out [L][B][T][Hv][Dv], tape_delta
  * same, tape_k [L][B][T][Hk][Dk]; node_state (optional) [L][B][T][Hv][Dv][Dk] = state after node.
  * parent [B][T] or NULL for a chain. */

@@ -49,8 +49,8 @@ def _load():
 
 class _CDims(ct.Structure):
     _fields_ = [(n, ct.c_int) for n in ("L", "B", "T", "Hk", "Hv", "Dk", "Dv", "W", "C",
-                                         "act_silu")] + [("qk_scale", ct.c_double),
-                                                         ("l2_eps", ct.c_double)]
+                                         "act_silu", "gate_dk")] + [("qk_scale", ct.c_double),
+                                                                    ("l2_eps", ct.c_double)]
 
 
 @dataclass
@@ -71,9 +71,10 @@ class OracleDims:
     def C(self):
         return 2 * self.Hk * self.Dk + self.Hv * self.Dv
 
-    def c(self):
+    def c(self, gate_dk=False):
         return _CDims(self.L, self.B, self.T, self.Hk, self.Hv, self.Dk, self.Dv, self.W, self.C,
-                      1 if self.act_silu else 0, float(self.qk_scale), float(self.l2_eps))
+                      1 if self.act_silu else 0, 1 if gate_dk else 0, float(self.qk_scale),
+                      float(self.l2_eps))
 
 
 def _f64(a):
@@ -106,7 +107,10 @@ def verify(dims: OracleDims, qkv, conv_w, conv_state, g, beta, state, parent=Non
     assert qkv.shape == (d.L, d.B, d.T, d.C), qkv.shape
     assert conv_w.shape == (d.L, d.C, d.W)
     assert conv_state.shape == (d.L, d.B, d.W - 1, d.C)
-    assert g.shape == (d.L, d.B, d.T, d.Hv) and beta.shape == g.shape
+    # g per value head [L,B,T,Hv], or per key channel [L,B,T,Hv,Dk]
+    gate_dk = g.ndim == 5
+    assert g.shape == ((d.L, d.B, d.T, d.Hv, d.Dk) if gate_dk else (d.L, d.B, d.T, d.Hv)), g.shape
+    assert beta.shape == (d.L, d.B, d.T, d.Hv)
     assert state.shape == (d.L, d.B, d.Hv, d.Dv, d.Dk)
     par = None if parent is None else _i32(parent)
     if par is not None:
@@ -115,7 +119,7 @@ def verify(dims: OracleDims, qkv, conv_w, conv_state, g, beta, state, parent=Non
     tdl = np.zeros_like(out)
     tk = np.zeros((d.L, d.B, d.T, d.Hk, d.Dk))
     ns = np.zeros((d.L, d.B, d.T, d.Hv, d.Dv, d.Dk)) if node_states else None
-    cd = d.c()
+    cd = d.c(gate_dk)
     lib.oracle_verify(ct.byref(cd), _p(par), _p(qkv), _p(conv_w), _p(conv_state), _p(g),
                       _p(beta), _p(state), _p(out), _p(tdl), _p(tk), _p(ns))
     res = dict(out=out, tape_delta=tdl, tape_k=tk)
@@ -133,9 +137,10 @@ def rollback(dims: OracleDims, n_acc, tape_delta, tape_k, g, qkv, state, conv_st
     cs = _f64(conv_state).copy()
     pth = None if path is None else _i32(path)
     P = 0 if pth is None else pth.shape[1]
-    cd = d.c()
+    g = _f64(g)
+    cd = d.c(g.ndim == 5)
     bad = lib.oracle_rollback(ct.byref(cd), _p(pth), P, _p(n_acc), _p(_f64(tape_delta)),
-                              _p(_f64(tape_k)), _p(_f64(g)), _p(_f64(qkv)), _p(st), _p(cs))
+                              _p(_f64(tape_k)), _p(g), _p(_f64(qkv)), _p(st), _p(cs))
     return st, cs, bad
 
 
