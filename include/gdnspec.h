@@ -89,6 +89,10 @@ typedef struct gdn_dims {
     int32_t io_dtype;
     float qk_scale;
     float l2_eps;
+    int32_t gate_dk;     /* 0: g is [L][B][T][Hv]; 1: g is [L][B][T][Hv][Dk], one decay per key
+                            channel (GDN investigation §4 tape layout [B, T, Hv, Dk]):
+                            S ← S·diag(g_t) + δ_t k_tᵀ with u = S·diag(g_t)·k_t. Chains only
+                            (gdn_verify, gdn_rollback, gdn_rollback_verify); trees reject it. */
 } gdn_dims;
 
 /*
@@ -105,7 +109,9 @@ typedef struct gdn_dims {
  *   qkv        [L][B][T][C]        io_dtype   raw projections of the T verify positions
  *   conv_w     [L][C][W]           io_dtype   depthwise conv taps
  *   conv_state [L][B][W-1][C]      io_dtype   last W-1 raw rows before the round (read only)
- *   g, beta    [L][B][T][Hv]       f32        decay gate in (0,1] and write strength
+ *   g, beta    [L][B][T][Hv]       f32        decay gate in (0,1] and write strength; with
+ *                                             d->gate_dk, g is [L][B][T][Hv][Dk] (one decay
+ *                                             per key channel, S ← S·diag(g_t) + δ_t k_tᵀ)
  *   state      [L][B][Hv][Dv][Dk]  f32        S_0, row-major: element (i,j) of S — row i in
  *                                             Dv, column j in Dk — is at [i][j] (read only)
  *   out        [L][B][T][Hv][Dv]   io_dtype   o_t
@@ -127,6 +133,7 @@ GDN_API int gdn_verify(const gdn_dims* d, const void* qkv, const void* conv_w, c
  * Node v starts from its parent's state (S_0 for parent -1); its conv window is its own raw row
  * and its W-1 nearest ancestors' rows, continued into conv_state when the path is shorter.
  * Other arguments and layouts as gdn_verify with T = node count; the tape is per node.
+ * d->gate_dk = 1 returns GDN_ERR_UNSUPPORTED (as does gdn_rollback_path).
  * A bad parent sets GDN_STATUS_BAD_PARENT; that sequence's out / tape rows are then unspecified
  * (left unwritten, or computed as if the nodes formed one chain).
  */
@@ -138,7 +145,7 @@ GDN_API int gdn_verify_tree(const gdn_dims* d, const int32_t* parent, const void
 /*
  * gdn_rollback — tape-replay rollback (GDN investigation §4 "Tape-Replay 回滚"): for every layer
  * and sequence with n = n_acc[b] > 0, replay the accepted steps
- *     S ← g_t S + δ_t k_tᵀ,  t = 0..n-1,
+ *     S ← g_t S + δ_t k_tᵀ,  t = 0..n-1      (with d->gate_dk: S ← S·diag(g_t) + δ_t k_tᵀ),
  * from the untouched snapshot S_0 and store S_n in place; rebuild the conv state as the last W-1
  * rows of (conv_state ++ qkv rows 0..n-1). n = 0 leaves both untouched. Cost O(n), all L layers
  * in one launch; n is read on the device (no host sync).

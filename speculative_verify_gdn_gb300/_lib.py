@@ -41,7 +41,8 @@ class GdnError(RuntimeError):
 class _Dims(ct.Structure):
     _fields_ = [(n, ct.c_int32) for n in ("L", "B", "T", "Hk", "Hv", "Dk", "Dv", "W", "C",
                                            "io_dtype")] + [("qk_scale", ct.c_float),
-                                                           ("l2_eps", ct.c_float)]
+                                                           ("l2_eps", ct.c_float),
+                                                           ("gate_dk", ct.c_int32)]
 
 
 class _SpecDims(ct.Structure):
@@ -116,6 +117,7 @@ class GdnShape:
     io_dtype: torch.dtype = torch.bfloat16
     qk_scale: float = 1.0
     l2_eps: float = 1e-6
+    gate_dk: bool = False      # g per key channel [L, B, T, Hv, Dk]
 
     @property
     def C(self):
@@ -124,7 +126,7 @@ class GdnShape:
     def c(self):
         dt = GDN_DTYPE_BF16 if self.io_dtype == torch.bfloat16 else GDN_DTYPE_F32
         return _Dims(self.L, self.B, self.T, self.Hk, self.Hv, self.Dk, self.Dv, self.W, self.C,
-                     dt, self.qk_scale, self.l2_eps)
+                     dt, self.qk_scale, self.l2_eps, 1 if self.gate_dk else 0)
 
     # expected tensor shapes
     def qkv_shape(self):
@@ -137,6 +139,10 @@ class GdnShape:
         return (self.L, self.B, self.W - 1, self.C)
 
     def gate_shape(self):
+        """Shape of g: per value head, or per key channel when gate_dk."""
+        return (self.L, self.B, self.T, self.Hv) + ((self.Dk,) if self.gate_dk else ())
+
+    def beta_shape(self):
         return (self.L, self.B, self.T, self.Hv)
 
     def state_shape(self):
@@ -182,7 +188,7 @@ def verify(shape: GdnShape, qkv, conv_w, conv_state, g, beta, state, out, tape_d
     args = [_ptr(qkv, io, shape.qkv_shape(), "qkv"),
             _ptr(conv_w, io, shape.conv_w_shape(), "conv_w"),
             _ptr(conv_state, io, shape.conv_state_shape(), "conv_state"),
-            _ptr(g, f32, shape.gate_shape(), "g"), _ptr(beta, f32, shape.gate_shape(), "beta"),
+            _ptr(g, f32, shape.gate_shape(), "g"), _ptr(beta, f32, shape.beta_shape(), "beta"),
             _ptr(state, f32, shape.state_shape(), "state"),
             _ptr(out, io, shape.out_shape(), "out"),
             _ptr(tape_delta, f32, shape.out_shape(), "tape_delta"),
@@ -235,7 +241,7 @@ def rollback_verify(shape: GdnShape, n_acc_prev, tape_delta_prev, tape_k_prev, g
             _ptr(qkv, io, shape.qkv_shape(), "qkv"),
             _ptr(conv_w, io, shape.conv_w_shape(), "conv_w"),
             _ptr(conv_state, io, shape.conv_state_shape(), "conv_state"),
-            _ptr(g, f32, shape.gate_shape(), "g"), _ptr(beta, f32, shape.gate_shape(), "beta"),
+            _ptr(g, f32, shape.gate_shape(), "g"), _ptr(beta, f32, shape.beta_shape(), "beta"),
             _ptr(state, f32, shape.state_shape(), "state"),
             _ptr(out, io, shape.out_shape(), "out"),
             _ptr(tape_delta, f32, shape.out_shape(), "tape_delta"),

@@ -52,6 +52,8 @@ int check_dims(const gdn_dims* d) {
         return fail(GDN_ERR_UNSUPPORTED, "grid limits: B, L, Hv must be <= 65535");
     if (!(d->l2_eps >= 0.f) || !std::isfinite(d->qk_scale))
         return fail(GDN_ERR_INVALID_ARG, "l2_eps must be >= 0 and qk_scale finite");
+    if (d->gate_dk != 0 && d->gate_dk != 1)
+        return fail(GDN_ERR_INVALID_ARG, "gate_dk=%d must be 0 or 1", d->gate_dk);
     return GDN_OK;
 }
 
@@ -129,6 +131,8 @@ int verify_common(const gdn_dims* d, const int32_t* parent, const void* qkv, con
                   bool tree) {
     int rc = check_dims(d);
     if (rc) return rc;
+    if (tree && d->gate_dk)
+        return fail(GDN_ERR_UNSUPPORTED, "gdn_verify_tree takes one gate per value head (gate_dk=0)");
     if (empty(d)) return GDN_OK;
     if (!qkv || !conv_w || !g || !beta || !state || !out || !tape_delta || !tape_k ||
         (d->W > 1 && !conv_state) || (tree && !parent))
@@ -146,7 +150,7 @@ int verify_common(const gdn_dims* d, const int32_t* parent, const void* qkv, con
     a.qk_scale = d->qk_scale; a.l2_eps = d->l2_eps;
     a.qkv = qkv; a.conv_w = conv_w; a.conv_state = conv_state; a.g = g; a.beta = beta;
     a.state = state; a.out = out; a.tape_delta = tape_delta; a.tape_k = tape_k;
-    a.parent = tree ? parent : nullptr; a.status = status;
+    a.parent = tree ? parent : nullptr; a.status = status; a.gate_dk = d->gate_dk;
     gdn::VerifyMaps maps;
     rc = state_tensor_map(d, state, &maps.state);
     if (rc) return rc;
@@ -188,6 +192,8 @@ int rollback_common(const gdn_dims* d, const int32_t* path, int32_t P, const int
     int rc = check_dims(d);
     if (rc) return rc;
     if (path && P < 0) return fail(GDN_ERR_INVALID_ARG, "path capacity P=%d < 0", P);
+    if (path && d->gate_dk)
+        return fail(GDN_ERR_UNSUPPORTED, "gdn_rollback_path takes one gate per value head (gate_dk=0)");
     if (empty(d) || (path && P == 0)) return GDN_OK;
     if (!n_acc || !tape_delta || !tape_k || !g || !qkv || !state || (d->W > 1 && !conv_state))
         return fail(GDN_ERR_INVALID_ARG, "NULL tensor pointer");
@@ -202,6 +208,7 @@ int rollback_common(const gdn_dims* d, const int32_t* path, int32_t P, const int
     a.P = path ? P : 0;
     a.n_acc = n_acc; a.path = path; a.tape_delta = tape_delta; a.tape_k = tape_k; a.g = g;
     a.qkv = qkv; a.state = state; a.conv_state = conv_state; a.status = status;
+    a.gate_dk = d->gate_dk;
     cudaError_t e = gdn::launch_rollback(a, d->Dk, d->io_dtype, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, path ? "gdn_rollback_path launch" : "gdn_rollback launch");
     return GDN_OK;
@@ -416,14 +423,14 @@ int gdn_rollback_verify(const gdn_dims* d, const int32_t* n_acc_prev, const floa
     const void* outs[3] = {tape_delta, tape_k, out};
     const size_t out_n[3] = {dl_bytes, k_bytes, o_bytes};
     const void* ins[4] = {tape_delta_prev, tape_k_prev, qkv_prev, g_prev};
-    const size_t in_n[4] = {dl_bytes, k_bytes, q_bytes, lbt * d->Hv * 4};
+    const size_t in_n[4] = {dl_bytes, k_bytes, q_bytes, lbt * d->Hv * (d->gate_dk ? d->Dk : 1) * 4};
     for (int i = 0; i < 3; ++i)
         for (int j = 0; j < 4; ++j)
             if (overlaps(outs[i], out_n[i], ins[j], in_n[j]))
                 return fail(GDN_ERR_INVALID_ARG,
                             "this round's tape / out overlap the previous round's tape, qkv or g");
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (d->io_dtype == GDN_DTYPE_BF16) {
+    if (d->io_dtype == GDN_DTYPE_BF16 && !d->gate_dk) {
         gdn::VerifyArgs a{};
         a.L = d->L; a.B = d->B; a.T = d->T; a.Hk = d->Hk; a.Hv = d->Hv; a.W = d->W; a.C = d->C;
         a.qk_scale = d->qk_scale; a.l2_eps = d->l2_eps;

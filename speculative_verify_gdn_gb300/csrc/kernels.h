@@ -21,6 +21,7 @@ struct VerifyArgs {
     float* tape_k;
     const int32_t* parent;   // tree only (null for the chain)
     uint32_t* status;
+    int gate_dk;             // g is [L][B][T][Hv][Dk] (per key channel) instead of [..][Hv]
     // gdn_rollback_verify only (null otherwise): the previous round's accepted counts [B], tape
     // (δ [L][B][T][Hv][Dv], k [L][B][T][Hk][Dk]), gates [L][B][T][Hv] and raw rows [L][B][T][C];
     // the state and conv_state buffers are then updated in place
@@ -66,6 +67,7 @@ struct RollbackArgs {
     float* state;
     void* conv_state;
     uint32_t* status;
+    int gate_dk;              // g per key channel [L][B][T][Hv][Dk]
 };
 cudaError_t launch_rollback(const RollbackArgs& a, int D, int io_dtype, cudaStream_t s);
 

@@ -9,6 +9,8 @@
 // the replay of n steps is folded into one pass over the state:
 //     S_n = Γ_total · S_0 + Σ_{s<n} (Γ_{s+1..n-1} δ_s) k_sᵀ,   Γ_total = Π_{s<n} g_s,
 // which reads and writes each state element once (HBM-bound) with n+1 FMAs per element.
+// With one gate per key channel (g [B, T, Hv, Dk]) the products are per column j: Γ_total[j]
+// scales column j of S_0 and k_s[j] carries Π_{s<r<n} a_r[j]; the pass is otherwise the same.
 // The state is row-major S ([i][j], j contiguous). One 256-thread CTA per (layer, sequence, value
 // head) moves its slice by bulk copy into shared memory and back (64 KiB at d = 128, so three
 // CTAs per SM keep ~200 KiB of state in flight; registers would hold two); lanes own consecutive
@@ -43,6 +45,7 @@ gdn_rollback_kernel(const RollbackArgs a) {
     __shared__ float gs[NMAX];
     __shared__ int nodes[NMAX];
     __shared__ float gtot;
+    __shared__ float gcol[D];        // per-key-channel gates: Γ_total per column j
     __shared__ int bad, load_ok;
     __shared__ __align__(8) uint64_t bar;
 
@@ -82,7 +85,7 @@ gdn_rollback_kernel(const RollbackArgs a) {
     int my_node = 0;
     if (tid < n) {
         my_node = node_of(tid);
-        gv = __ldg(a.g + (lb * T + (my_node < 0 ? 0 : my_node)) * Hv + h);
+        gv = a.gate_dk ? 1.f : __ldg(a.g + (lb * T + (my_node < 0 ? 0 : my_node)) * Hv + h);
     }
     for (int idx = tid; idx < n * D; idx += 256) {       // raw δ_s[i] (Γ_{s+1..n-1} applied below), k_s[j]
         const int s2 = idx / D, i = idx - s2 * D;
@@ -97,6 +100,22 @@ gdn_rollback_kernel(const RollbackArgs a) {
         if (my_node < 0) atomicOr(&bad, 1);
     }
     __syncthreads();
+    if (a.gate_dk && tid < D) {      // column j = tid: k_s[j] *= Π_{s<r<n} a_r[j], Γ_total[j]
+        const int j = tid;
+        float av[NMAX];
+#pragma unroll
+        for (int s2 = 0; s2 < NMAX; ++s2)
+            av[s2] = s2 < n ? __ldg(a.g + ((lb * T + nodes[s2]) * Hv + h) * size_t(D) + j) : 1.f;
+        float c = 1.f;
+#pragma unroll
+        for (int s2 = NMAX - 1; s2 >= 0; --s2) {
+            if (s2 < n) {
+                Ks[s2][j] *= c;
+                c *= av[s2];
+            }
+        }
+        gcol[j] = c;
+    }
     if (tid == 0) {
         float c = 1.f;
         for (int s2 = n - 1; s2 >= 0; --s2) {
@@ -117,8 +136,10 @@ gdn_rollback_kernel(const RollbackArgs a) {
         return;
     }
     mbar_try_wait(&bar, 0);          // completed: each thread observes the slice
-    const float G = gtot;
     const int j0 = lane * CPL;
+    float G[CPL];                    // Γ_total of this lane's columns
+#pragma unroll
+    for (int r = 0; r < CPL; ++r) G[r] = a.gate_dk ? gcol[j0 + r] : gtot;
 
     // S_n[i][j] = Γ_total S_0[i][j] + Σ_s Γ_{s+1..n-1} δ_s[i] k_s[j], in place in shared memory
     float kr[NMAX <= 8 ? NMAX : 1][CPL];
@@ -134,10 +155,10 @@ gdn_rollback_kernel(const RollbackArgs a) {
         float v[CPL];
         if constexpr (CPL == 4) {
             const float4 x4 = *reinterpret_cast<const float4*>(Sl + i * D + j0);
-            v[0] = G * x4.x; v[1] = G * x4.y; v[2] = G * x4.z; v[3] = G * x4.w;
+            v[0] = G[0] * x4.x; v[1] = G[1] * x4.y; v[2] = G[2] * x4.z; v[3] = G[3] * x4.w;
         } else {
 #pragma unroll
-            for (int r = 0; r < CPL; ++r) v[r] = G * Sl[i * D + j0 + r];
+            for (int r = 0; r < CPL; ++r) v[r] = G[r] * Sl[i * D + j0 + r];
         }
         if constexpr (NMAX <= 8) {
 #pragma unroll

@@ -6,6 +6,9 @@
 //   rule u = g S k, δ = β (v − u), S ← g S + δ kᵀ, o = scale · S q, from the snapshot S_0,
 //   node by node (chain: node t's parent is t−1; tree: an explicit parent array).
 //   Writes o, the tape (δ per value head, normalised k per key head). S_0 is never written.
+//   Chains also take one gate per key channel (g [B, T, Hv, Dk], §4's tape layout):
+//   S ← S·diag(a_t) + δ kᵀ with u = S·diag(a_t)·k; then the dense product reads the decayed
+//   columns A_t ⊙ k_t, A_t ⊙ q_t and the Gram block carries the per-channel decays.
 //
 // How (GB300 design):
 //   * The state update is never materialised. With Γ(a→p) the product of the gates strictly
@@ -34,7 +37,7 @@
 
 namespace gdn {
 
-template <typename IO, int D, int TMAX, bool TREE>
+template <typename IO, int D, int TMAX, bool TREE, bool GDK = false>
 struct VerifyCfg {
     static constexpr int NWARP = 8;
     static constexpr int NTHR = 256;
@@ -56,7 +59,8 @@ struct VerifyCfg {
     static constexpr int M_GAM = 0, M_BET = M_GAM + TMAX, M_C0 = M_BET + TMAX,
                          M_KQ = M_C0 + TMAX, M_INV = M_KQ + TMAX, M_NRM = M_INV + 2 * TMAX,
                          M_CK = M_NRM + NWARP * TMAX, M_CQ = M_CK + TMAX * TMAX,
-                         M_DL = M_CQ + TMAX * TMAX, M_FLOATS = M_DL + (TREE ? TMAX * D : 0);
+                         M_DL = M_CQ + TMAX * TMAX, M_GA = M_DL + (TREE ? TMAX * D : 0),
+                         M_FLOATS = M_GA + (GDK ? TMAX * D : 0);
     static constexpr int I_PAR = 0, I_NANC = I_PAR + TMAX, I_ANC = I_NANC + TMAX,
                          I_WIN = I_ANC + (TREE ? TMAX * TMAX : 0),
                          I_FLAG = I_WIN + (TREE ? TMAX * 4 : 0), I_INTS = I_FLAG + 4;
@@ -78,6 +82,7 @@ struct VerifyCfg {
     }
 
     static_assert(D == 32 || D == 64 || D == 128, "head dim");
+    static_assert(!(GDK && TREE), "per-key-channel gates are built for chains");
     static_assert(OFF_A % 1024 == 0, "swizzle atoms need 1024-byte bases");
 };
 
@@ -196,10 +201,10 @@ __device__ __forceinline__ float io_to_f(IO x) {
     else return x;
 }
 
-template <typename IO, int D, int TMAX, bool TREE>
+template <typename IO, int D, int TMAX, bool TREE, bool GDK>
 __global__ void __launch_bounds__(256)
 gdn_verify_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap smap) {
-    using Cfg = VerifyCfg<IO, D, TMAX, TREE>;
+    using Cfg = VerifyCfg<IO, D, TMAX, TREE, GDK>;
     using Tr = IoTraits<IO>;
     constexpr int NP = Cfg::NP, KB = Cfg::KB, XKB = Cfg::XKB, XS = Cfg::XP_STRIDE;
 
@@ -223,6 +228,7 @@ gdn_verify_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap smap) 
     float* CK = mf + Cfg::M_CK;
     float* CQ = mf + Cfg::M_CQ;
     float* DL = mf + Cfg::M_DL;
+    float* GA = mf + Cfg::M_GA;                     // per-key-channel gates a_t[j] (GDK)
     int* par = mi + Cfg::I_PAR;
     int* nanc = mi + Cfg::I_NANC;
     int* anc = mi + Cfg::I_ANC;
@@ -293,8 +299,12 @@ gdn_verify_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap smap) 
     // this thread's gate pair (tid < T): loaded now, stored once the conv is under way
     float g_in = 0.f, b_in = 0.f;
     if (tid < T) {
-        g_in = __ldg(a.g + (lb * T + tid) * Hv + h);
+        if constexpr (!GDK) g_in = __ldg(a.g + (lb * T + tid) * Hv + h);
         b_in = __ldg(a.beta + (lb * T + tid) * Hv + h);
+    }
+    if constexpr (GDK) {   // the head's T x D gate rows, coalesced, into the meta block
+        for (int e = tid; e < T * D; e += Cfg::NTHR)
+            GA[e] = __ldg(a.g + ((lb * T + e / D) * Hv + h) * size_t(D) + (e % D));
     }
     tc_fence_before();
     __syncthreads();
@@ -423,14 +433,22 @@ gdn_verify_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap smap) 
     __syncthreads();
     // [K|Q] columns: n < TMAX -> k_n, TMAX <= n < 2 TMAX -> q, the rest zero. B tile rows n
     // (hi) and NP + n (lo) in the swizzled K-major layout; plain fp32 rows XP[n] for the Gram.
+    // Per-key-channel gates: the tile holds A_t ⊙ k_t and A_t ⊙ q_t with A_t[j] = Π_{r≤t} a_r[j]
+    // (S_0 decayed to step t, seen through column j); XP and the tape keep the plain vectors.
     if (part < 2) {
         const int n0 = part == 1 ? 0 : TMAX;
+        float cum = 1.f;
 #pragma unroll
         for (int t = 0; t < TMAX; ++t) {
             const float x = yqk[t] * inv[n0 + t];
-            const float hi = tf32_trunc(x);
+            float xw = x;
+            if constexpr (GDK) {
+                if (t < T) cum *= GA[t * D + idx];
+                xw = x * cum;
+            }
+            const float hi = tf32_trunc(xw);
             *reinterpret_cast<float*>(Xb + sw128_off(n0 + t, idx, XKB)) = hi;
-            *reinterpret_cast<float*>(Xb + sw128_off(NP + n0 + t, idx, XKB)) = x - hi;
+            *reinterpret_cast<float*>(Xb + sw128_off(NP + n0 + t, idx, XKB)) = xw - hi;
             XP[(n0 + t) * XS + idx] = x;
             if (part == 1 && (h % group) == 0 && t < T)
                 a.tape_k[((lb * T + t) * Hk + kh) * size_t(D) + idx] = x;
@@ -472,7 +490,55 @@ gdn_verify_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap smap) 
 
     // ---- 5. Gram block on CUDA cores: G[a][c] = k_a · X_c (a < TMAX, c < 2 TMAX), 2 threads
     //         per entry; CK[v][a] = k_a·k_v, CQ[v][a] = k_a·q_v
-    {
+    if constexpr (GDK) {
+        // Per-key-channel gates: the decay between write s and read t differs per column j, so
+        // the Gram carries it, CK[t][s] = Σ_j k_s[j] k_t[j] Π_{s<r≤t} a_r[j] (CQ with q_t), built
+        // as a running product per (s, j) in 8-lane groups (thread: s = tid/8, j ≡ tid mod 8),
+        // never as a ratio of cumulative products (which underflow). kqv[s] = k_s·q_s.
+        constexpr int NJ = D / 8;
+        const int s = tid >> 3, c = tid & 7;
+        const bool act = s < T;
+        float ks[NJ], w[NJ];
+        float kq = 0.f;
+#pragma unroll
+        for (int m = 0; m < NJ; ++m) {
+            const int j = c + 8 * m;
+            w[m] = 1.f;
+            ks[m] = 0.f;
+            if (act) {                     // rows s and TMAX + s exist only for s < T
+                ks[m] = XP[s * XS + j];
+                kq = fmaf(ks[m], XP[(TMAX + s) * XS + j], kq);
+            }
+        }
+        kq += __shfl_xor_sync(0xffffffffu, kq, 1);
+        kq += __shfl_xor_sync(0xffffffffu, kq, 2);
+        kq += __shfl_xor_sync(0xffffffffu, kq, 4);
+        if (c == 0 && act) {
+            kqv[s] = kq;
+            c0[s] = 1.f;
+        }
+        for (int t = 1; t < T; ++t) {          // warp-uniform trip count (shuffles below)
+            const bool on = t > s;
+            float ck = 0.f, cq = 0.f;
+#pragma unroll
+            for (int m = 0; m < NJ; ++m) {
+                const int j = c + 8 * m;
+                w[m] *= on ? GA[t * D + j] : 1.f;
+                const float kw = ks[m] * w[m];
+                ck = fmaf(kw, XP[t * XS + j], ck);
+                cq = fmaf(kw, XP[(TMAX + t) * XS + j], cq);
+            }
+#pragma unroll
+            for (int o = 1; o < 8; o <<= 1) {
+                ck += __shfl_xor_sync(0xffffffffu, ck, o);
+                cq += __shfl_xor_sync(0xffffffffu, cq, o);
+            }
+            if (c == 0 && on) {
+                CK[t * TMAX + s] = ck;
+                CQ[t * TMAX + s] = cq;
+            }
+        }
+    } else {
         constexpr int NENT = TMAX * 2 * TMAX;
         const int half = tid & 1;
         for (int e = tid >> 1; e < NENT; e += Cfg::NTHR / 2) {
@@ -496,24 +562,27 @@ gdn_verify_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap smap) 
             }
         }
     }
-    __syncthreads();
-    // fold the gate products in: CK[v][a] *= Γ(a→parent(v)); c0[v] = Γ(root→parent(v))
-    if (tid < T) {
-        const int v = tid;
-        float coef = 1.f;
-        int m = 0;
-        int x = TREE ? par[v] : v - 1;
-        kqv[v] = CQ[v * TMAX + v];
-        while (x >= 0) {
-            CK[v * TMAX + x] *= coef;
-            CQ[v * TMAX + x] *= coef;
-            if constexpr (TREE) anc[v * TMAX + m] = x;
-            ++m;
-            coef *= gam[x];
-            x = TREE ? par[x] : x - 1;
+    // fold the gate products in: CK[v][a] *= Γ(a→parent(v)); c0[v] = Γ(root→parent(v)) (the
+    // per-channel Gram above already carries its decays, and c0 = 1)
+    if constexpr (!GDK) {
+        __syncthreads();
+        if (tid < T) {
+            const int v = tid;
+            float coef = 1.f;
+            int m = 0;
+            int x = TREE ? par[v] : v - 1;
+            kqv[v] = CQ[v * TMAX + v];
+            while (x >= 0) {
+                CK[v * TMAX + x] *= coef;
+                CQ[v * TMAX + x] *= coef;
+                if constexpr (TREE) anc[v * TMAX + m] = x;
+                ++m;
+                coef *= gam[x];
+                x = TREE ? par[x] : x - 1;
+            }
+            c0[v] = coef;
+            if constexpr (TREE) nanc[v] = m;
         }
-        c0[v] = coef;
-        if constexpr (TREE) nanc[v] = m;
     }
 
     // ---- 6. once the first pass is done: S_0 tile -> S_lo in place; second pass S_lo·X_hi
@@ -574,10 +643,11 @@ gdn_verify_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap smap) 
                         sk = fmaf(CK[t * TMAX + s], dl[s], sk);
                         sq = fmaf(CQ[t * TMAX + s], dl[s], sq);
                     }
-                    const float u = gam[t] * sk;
+                    const float gt = GDK ? 1.f : gam[t];   // per-channel decay: in pr and CK
+                    const float u = gt * sk;
                     const float d = bet[t] * (yv[t] - u);
                     dl[t] = d;
-                    const float o = scale * fmaf(d, kqv[t], gam[t] * sq);
+                    const float o = scale * fmaf(d, kqv[t], gt * sq);
                     const size_t oi = ((lb * T + t) * Hv + h) * size_t(D) + i;
                     a.tape_delta[oi] = d;
                     Tr::store(out, oi, o);
@@ -616,10 +686,10 @@ gdn_verify_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap smap) 
                      ::"r"(tbase), "r"(uint32_t(Cfg::TMEM_COLS)));
 }
 
-template <typename IO, int D, int TMAX, bool TREE>
+template <typename IO, int D, int TMAX, bool TREE, bool GDK>
 cudaError_t launch_verify_t(const VerifyArgs& a, const CUtensorMap& map, cudaStream_t stream) {
-    using Cfg = VerifyCfg<IO, D, TMAX, TREE>;
-    auto kern = gdn_verify_kernel<IO, D, TMAX, TREE>;
+    using Cfg = VerifyCfg<IO, D, TMAX, TREE, GDK>;
+    auto kern = gdn_verify_kernel<IO, D, TMAX, TREE, GDK>;
     const size_t smem = Cfg::smem_bytes(a.T, a.W);
     if (smem > 227 * 1024) return cudaErrorInvalidValue;
     static int attr_set = 0;   // largest size configured so far (benign race: idempotent)
@@ -634,16 +704,27 @@ cudaError_t launch_verify_t(const VerifyArgs& a, const CUtensorMap& map, cudaStr
     return cudaGetLastError();
 }
 
-template <typename IO, bool TREE>
-cudaError_t launch_verify_io(const VerifyArgs& a, const CUtensorMap& map, int D, cudaStream_t s) {
+template <typename IO, bool TREE, bool GDK>
+cudaError_t launch_verify_gk(const VerifyArgs& a, const CUtensorMap& map, int D, cudaStream_t s) {
     const int tm = a.T <= 4 ? 4 : a.T <= 8 ? 8 : a.T <= 16 ? 16 : 32;
 #define GDN_V_CASE(DD, TM) \
-    if (D == DD && tm == TM) return launch_verify_t<IO, DD, TM, TREE>(a, map, s);
+    if (D == DD && tm == TM) return launch_verify_t<IO, DD, TM, TREE, GDK>(a, map, s);
     GDN_V_CASE(32, 4) GDN_V_CASE(32, 8) GDN_V_CASE(32, 16) GDN_V_CASE(32, 32)
     GDN_V_CASE(64, 4) GDN_V_CASE(64, 8) GDN_V_CASE(64, 16) GDN_V_CASE(64, 32)
     GDN_V_CASE(128, 4) GDN_V_CASE(128, 8) GDN_V_CASE(128, 16) GDN_V_CASE(128, 32)
 #undef GDN_V_CASE
     return cudaErrorInvalidValue;
+}
+
+template <typename IO, bool TREE>
+cudaError_t launch_verify_io(const VerifyArgs& a, const CUtensorMap& map, int D, cudaStream_t s) {
+    if constexpr (TREE) {
+        if (a.gate_dk) return cudaErrorInvalidValue;
+        return launch_verify_gk<IO, true, false>(a, map, D, s);
+    } else {
+        return a.gate_dk ? launch_verify_gk<IO, false, true>(a, map, D, s)
+                         : launch_verify_gk<IO, false, false>(a, map, D, s);
+    }
 }
 
 }  // namespace gdn

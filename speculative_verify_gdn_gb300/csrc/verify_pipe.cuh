@@ -1821,11 +1821,11 @@ cudaError_t launch_verify_pipe_t(const VerifyArgs& a, const VerifyMaps& m, cudaS
 }
 
 // The pipelined kernel serves the Qwen3.6 head shape (chains up to 16 positions, trees up to 32
-// nodes); everything else uses the per-head kernel.
+// nodes) with one gate per value head; everything else uses the per-head kernel.
 template <typename IO>
 bool verify_pipe_eligible(const VerifyArgs& a, const VerifyMaps& m, int D, bool tree, bool commit) {
     const int tmax = commit ? 8 : (tree ? 32 : 16);
-    return m.inputs_ok && !(tree && commit) && D == 128 && sizeof(IO) == 2 && a.T <= tmax &&
+    return m.inputs_ok && !a.gate_dk && !(tree && commit) && D == 128 && sizeof(IO) == 2 && a.T <= tmax &&
            (a.Hv == a.Hk || a.Hv == 2 * a.Hk);
 }
 

@@ -6,7 +6,8 @@ oracle's tests and the bench. Every tensor comes from a generator seeded by
 (seed, workload, round, tensor name), so any piece can be regenerated independently.
 
 Distributions (the workloads' own statements, with the readings listed in the design doc):
-  raw qkv ~ N(0, 1); beta = sigmoid(N(0, 1)); g = exp(-softplus(N(0, 1))); S_0 ~ N(0, 0.1)
+  raw qkv ~ N(0, 1); beta = sigmoid(N(0, 1)); g = exp(-softplus(N(0, 1))) (per value head, or
+  independently per key channel when gate_dk); S_0 ~ N(0, 0.1)
   (0.1 is the standard deviation); conv weights ~ N(0, 0.5); initial conv state ~ N(0, 1).
   Greedy logits ~ N(0, 1) with the accepted length planted; sampling logits ~ N(0, 2) with
   point-mass drafts at each row's argmax. Accept lengths are geometric: accept each position
@@ -41,6 +42,7 @@ class Workload:
     tree_depth: int = 0
     tree_branch: int = 0
     rounds: int = 1
+    gate_dk: bool = False       # one gate per key channel: g [L, B, T, Hv, D]
     notes: str = field(default="", compare=False)
 
     @property
@@ -117,13 +119,14 @@ def initial_state(w: Workload, seed=0, device="cpu"):
 
 
 def round_stream(w: Workload, round_, seed=0, device="cpu"):
-    """Per-round verify inputs: qkv [L, B, T, C] (io), g, beta [L, B, T, Hv] fp32."""
+    """Per-round verify inputs: qkv [L, B, T, C] (io), g [L, B, T, Hv] (or [L, B, T, Hv, D] when
+    gate_dk), beta [L, B, T, Hv] fp32."""
     wid = _wid(w)
     T = w.N
     qkv = torch.randn((w.L, w.B, T, w.C), generator=generator(seed, wid, round_, "qkv", device),
                       device=device).to(w.io_dtype)
-    a = torch.randn((w.L, w.B, T, w.Hv), generator=generator(seed, wid, round_, "g", device),
-                    device=device)
+    gsh = (w.L, w.B, T, w.Hv) + ((w.D,) if w.gate_dk else ())
+    a = torch.randn(gsh, generator=generator(seed, wid, round_, "g", device), device=device)
     g = torch.exp(-torch.nn.functional.softplus(a))
     bb = torch.randn((w.L, w.B, T, w.Hv), generator=generator(seed, wid, round_, "beta", device),
                      device=device)
@@ -135,8 +138,8 @@ def previous_round(w: Workload, seed=0, device="cpu"):
     """A synthetic previous round, the input of gdn_rollback_verify's commit half:
     (n_acc [B] int32, tape_delta [L, B, T, Hv, Dv] fp32, tape_k [L, B, T, Hk, Dk] fp32,
     g [L, B, T, Hv] fp32, qkv [L, B, T, C] io). Counts follow the workload's acceptance model;
-    δ ~ N(0, 0.5); k ~ N(0, 1/D) per element (about unit length); g and qkv as a round_stream
-    round."""
+    δ ~ N(0, 0.5); k ~ N(0, 1/D) per element (about unit length); g (of the workload's gate
+    layout) and qkv as a round_stream round."""
     wid = _wid(w)
     qkv, g, _ = round_stream(w, PREV_ROUND, seed, device)
     n = accept_lengths(w, PREV_ROUND, seed, device).to(torch.int32)

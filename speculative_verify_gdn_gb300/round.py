@@ -12,7 +12,7 @@ def fused_in_one_kernel(w: Workload):
     """Whether gdn_rollback_verify runs as one kernel for this workload (else as two calls)."""
     import torch as _t
     return (w.io_dtype == _t.bfloat16 and w.D == 128 and w.N <= 8 and w.accept != "tree"
-            and w.Hv in (w.Hk, 2 * w.Hk))
+            and w.Hv in (w.Hk, 2 * w.Hk) and not w.gate_dk)
 
 
 class SpecRound:
@@ -27,7 +27,7 @@ class SpecRound:
         dev = torch.device(device)
         self.device = dev
         self.shape = _lib.GdnShape(L=w.L, B=w.B, T=w.N, Hk=w.Hk, Hv=w.Hv, Dk=w.D, Dv=w.D,
-                                   W=w.W, io_dtype=w.io_dtype)
+                                   W=w.W, io_dtype=w.io_dtype, gate_dk=w.gate_dk)
         sh = self.shape
         self.out = torch.empty(sh.out_shape(), dtype=w.io_dtype, device=dev)
         self.tape_delta = torch.empty(sh.out_shape(), dtype=torch.float32, device=dev)

@@ -49,6 +49,7 @@ def assert_close(gpu, ref, name, rtol=RTOL, atol_frac=ATOL_FRAC, bf16=False):
 
 
 def oracle_dims(w, T=None, L=None, B=None):
+    # the oracle reads the gate layout (per value head or per key channel) from g's rank
     return OracleDims(L=w.L if L is None else L, B=w.B if B is None else B,
                       T=w.N if T is None else T, Hk=w.Hk, Hv=w.Hv, Dk=w.D, Dv=w.D, W=w.W)
 

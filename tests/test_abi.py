@@ -123,3 +123,45 @@ def test_rollback_verify_host_checks(lib):
     assert lib.gdn_rollback_verify(ct.byref(d), *mis, None, None) == 1
     assert "aligned" in _lib.last_error()
     assert lib.gdn_rollback_verify(ct.byref(qwen_shape(B=0).c()), *([None] * 15), None, None) == 0
+
+
+def test_struct_layouts_match_the_header(tmp_path):
+    """gdn_dims / spec_dims as the C compiler lays them out equal the ctypes mirrors in _lib."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    fields = {"gdn_dims": [f for f, _ in _lib._Dims._fields_],
+              "spec_dims": [f for f, _ in _lib._SpecDims._fields_]}
+    lines = ['#include <stddef.h>', '#include <stdio.h>', '#include "gdnspec.h"', "int main(void) {"]
+    for st, fs in fields.items():
+        lines.append('printf("%s %%zu\\n", sizeof(%s));' % (st, st))
+        for f in fs:
+            lines.append('printf("%s.%s %%zu\\n", offsetof(%s, %s));' % (st, f, st, f))
+    lines.append("return 0; }")
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "layout"
+    subprocess.run([cc, "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)],
+                   check=True)
+    got = dict(l.split() for l in subprocess.run([str(exe)], check=True, capture_output=True,
+                                                  text=True).stdout.splitlines())
+    for st, cls in (("gdn_dims", _lib._Dims), ("spec_dims", _lib._SpecDims)):
+        assert int(got[st]) == ct.sizeof(cls), st
+        for f in fields[st]:
+            assert int(got["%s.%s" % (st, f)]) == getattr(cls, f).offset, (st, f)
+
+
+def test_gate_dk_host_checks(lib):
+    """Per-key-channel gates: trees and tree paths refuse them, other values of the flag are
+    rejected, all before any device access."""
+    fake = ct.c_void_p(0x100000)
+    d = qwen_shape().c()
+    d.gate_dk = 1
+    assert lib.gdn_verify_tree(ct.byref(d), fake, *([fake] * 9), None, None) == 2
+    assert "gate" in _lib.last_error()
+    assert lib.gdn_rollback_path(ct.byref(d), fake, 4, *([fake] * 7), None, None) == 2
+    assert "gate" in _lib.last_error()
+    d.gate_dk = 2
+    assert call_verify(lib, d, [fake] * 9) == 1 and "gate_dk" in _lib.last_error()

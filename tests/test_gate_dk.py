@@ -59,3 +59,80 @@ def test_zero_gate_erases_its_key_column():
     for h in range(2):
         col = ref["tape_delta"][0, 0, T - 1, h] * ref["tape_k"][0, 0, T - 1, h // 2, j0]
         np.testing.assert_allclose(st[0, 0, h, :, j0], col, rtol=1e-13, atol=1e-15)
+
+
+# ------------------------------------------------------------------------------ GPU parity
+def gdk_workload(D, T, io=torch.float32, L=2, B=4, Hk=2, Hv=4, W=4):
+    from speculative_verify_gdn_gb300 import inputs as I
+    return I.custom(I.WORKLOADS[1], name="gdk_D%d_T%d_H%d_%d_W%d_%s" % (D, T, Hk, Hv, W, str(io)),
+                    L=L, B=B, N=T, Hk=Hk, Hv=Hv, D=D, W=W, V=64, io_dtype=io, gate_dk=True)
+
+
+def run_gdk_verify_rollback(w, seed, n):
+    from parity_util import assert_close, f64, oracle_rollback, oracle_verify, to_dev
+    from speculative_verify_gdn_gb300 import inputs as I
+    from speculative_verify_gdn_gb300.round import SpecRound
+    cw = I.model_weights(w, seed)
+    st, cs = I.initial_state(w, seed)
+    qkv, g, beta = I.round_stream(w, 0, seed)
+    assert g.shape == (w.L, w.B, w.N, w.Hv, w.D)
+    r = SpecRound(w)
+    dq, dcw, dcs, dg, db, dst = to_dev(qkv, cw, cs, g, beta, st)
+    r.verify(dq, dcw, dcs, dg, db, dst)
+    r.check_status()
+    ref = oracle_verify(w, qkv, cw, cs, g, beta, st)
+    bf16 = w.io_dtype == torch.bfloat16
+    assert_close(f64(r.out), ref["out"], "out", bf16=bf16)
+    assert_close(f64(r.tape_delta), ref["tape_delta"], "tape_delta")
+    assert_close(f64(r.tape_k), ref["tape_k"], "tape_k")
+    assert torch.equal(dst.cpu(), st)
+    r.n_acc.copy_(torch.from_numpy(np.asarray(n, np.int32)))
+    r.rollback(dq, dg, dst, dcs)
+    r.check_status()
+    st_ref, cs_ref, bad = oracle_rollback(w, n, ref, g, qkv, st, cs)
+    assert bad == 0
+    assert_close(f64(dst), st_ref, "state")
+    assert np.array_equal(f64(dcs), cs_ref)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("D", [32, 64, 128])
+@pytest.mark.parametrize("T", [1, 4, 7, 16, 32])
+def test_gpu_per_channel_gates_verify_and_rollback(gdnlib, D, T):
+    w = gdk_workload(D, T)
+    n = np.minimum(np.array([T, 0, 1, T // 2], np.int32), T)
+    run_gdk_verify_rollback(w, T * 3 + D, n)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("Hk,Hv,T,W", [(2, 4, 8, 4), (4, 4, 16, 4), (1, 2, 5, 2), (2, 2, 8, 1)])
+def test_gpu_per_channel_gates_bf16_qwen_heads(gdnlib, Hk, Hv, T, W):
+    """bf16 I/O at d = 128 with one and two value heads per key head (the Qwen3.6 head shape)."""
+    w = gdk_workload(128, T, io=torch.bfloat16, Hk=Hk, Hv=Hv, W=W)
+    run_gdk_verify_rollback(w, Hk * 10 + Hv + T, np.array([T, 2, 0, T - 1], np.int32))
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("D,T", [(128, 8), (64, 4)])
+def test_gpu_per_channel_gates_rollback_verify(gdnlib, D, T):
+    """gdn_rollback_verify with per-channel gates (served as its two calls) against the oracle's
+    rollback followed by its verify."""
+    from parity_util import assert_close, f64
+    from speculative_verify_gdn_gb300 import inputs as I
+    from test_gpu_fused import oracle_commit_then_verify, run_fused
+    w = gdk_workload(D, T, io=torch.bfloat16, B=5)
+    cw = I.model_weights(w, 3)
+    st, cs = I.initial_state(w, 3)
+    qkv, g, beta = I.round_stream(w, 1, 3)
+    prev = I.previous_round(w, 3)
+    assert prev[3].shape == g.shape
+    n = np.array([0, T, 1, 2, T // 2], np.int32)
+    dst, dcs, out, tdl, tk, status = run_fused(w, n, prev, qkv, cw, cs, g, beta, st)
+    assert int(status.item()) == 0
+    st1, cs1, bad, ref = oracle_commit_then_verify(w, n, prev, qkv, cw, cs, g, beta, st)
+    assert bad == 0
+    assert_close(f64(dst), st1, "committed state")
+    assert np.array_equal(f64(dcs), cs1)
+    assert_close(f64(out), ref["out"], "out", bf16=True)
+    assert_close(f64(tdl), ref["tape_delta"], "tape_delta")
+    assert_close(f64(tk), ref["tape_k"], "tape_k")

@@ -30,7 +30,7 @@ def oracle_commit_then_verify(w, n, prev, qkv, cw, cs, g, beta, st, L=None, B=No
 
 def run_fused(w, n, prev, qkv, cw, cs, g, beta, st, status=None):
     sh = _lib.GdnShape(L=w.L, B=w.B, T=w.N, Hk=w.Hk, Hv=w.Hv, Dk=w.D, Dv=w.D, W=w.W,
-                       io_dtype=w.io_dtype)
+                       io_dtype=w.io_dtype, gate_dk=w.gate_dk)
     _, dl, k, gp, qp = prev
     dn, ddl, dk, dgp, dqp, dq, dcw, dcs, dg, db, dst = to_dev(
         torch.as_tensor(n, dtype=torch.int32), dl, k, gp, qp, qkv, cw, cs, g, beta, st)
