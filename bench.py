@@ -79,13 +79,19 @@ def aggregate_tokens_per_s(world, B, N, ms_per_step):
 
 
 # ------------------------------------------------------------------------------ accounting
+def gate_bytes(w):
+    """Bytes of one position's gates: one fp32 per value head, or one per key channel."""
+    return 4 * w.Hv * (w.D if getattr(w, "gate_dk", False) else 1)
+
+
 def bytes_verify(w):
     """Algorithmic HBM bytes of one gdn_verify launch over the whole workload: each input read
     once, each output written once (state S_0 read, never written)."""
     io = 2 if str(w.io_dtype).endswith("bfloat16") else 4
     S = w.Hv * w.D * w.D * 4
     T, C = w.N, w.C
-    per_unit = (S + T * (io * C + 8 * w.Hv + io * w.Hv * w.D + 4 * w.Hv * w.D + 4 * w.Hk * w.D)
+    per_unit = (S + T * (io * C + 4 * w.Hv + gate_bytes(w) + io * w.Hv * w.D + 4 * w.Hv * w.D
+                         + 4 * w.Hk * w.D)
                 + io * (w.W - 1) * C)
     return w.L * w.B * per_unit + w.L * io * C * w.W
 
@@ -101,7 +107,7 @@ def bytes_rollback(w, n_list):
         if n <= 0:
             continue
         m = min(n, W - 1)
-        tot += (2 * S + n * (4 * w.Hv * w.D + 4 * w.Hk * w.D + 4 * w.Hv)
+        tot += (2 * S + n * (4 * w.Hv * w.D + 4 * w.Hk * w.D + gate_bytes(w))
                 + io * (W - 1 - m) * C + io * m * C + io * (W - 1) * C)
     return w.L * tot + 4 * w.B
 
@@ -119,7 +125,7 @@ def bytes_rollback_verify(w, n_list):
         n = int(n)
         if n <= 0:
             continue
-        tot += S + n * (4 * w.Hv * w.D + 4 * w.Hk * w.D + 4 * w.Hv) + 2 * io * (W - 1) * C
+        tot += S + n * (4 * w.Hv * w.D + 4 * w.Hk * w.D + gate_bytes(w)) + 2 * io * (W - 1) * C
     return bytes_verify(w) + w.L * tot + 4 * w.B
 
 
@@ -301,6 +307,8 @@ def workload_description(w):
          "state": "fp32 128x128 per value head, row-major S",
          "l2": "inputs larger than L2: the %.2f GB recurrent state is streamed from HBM every step"
                % (w.L * w.B * w.Hv * w.D * w.D * 4 / 1e9)}
+    if getattr(w, "gate_dk", False):
+        d["gates"] = "one decay per key channel, g [L, B, T, Hv, d]"
     if w.accept in ("greedy", "tree"):
         d["alphas"] = list(w.alphas)
     if w.accept == "sample":
@@ -536,12 +544,18 @@ def main(argv=None):
                     help="override the workload's batch (smaller profiling cases)")
     ap.add_argument("--layers", type=int, default=None,
                     help="override the workload's layer count (smaller profiling cases)")
+    ap.add_argument("--gate-dk", action="store_true",
+                    help="one gate per key channel (g [L, B, T, Hv, d]); chain workloads only")
     args = ap.parse_args(argv)
 
     from speculative_verify_gdn_gb300 import inputs as I
     w = I.WORKLOADS[args.config]
     if args.batch is not None or args.layers is not None:
         w = I.custom(w, name=w.name, B=args.batch or w.B, L=args.layers or w.L)
+    if args.gate_dk:
+        if w.accept == "tree":
+            raise SystemExit("--gate-dk: per-key-channel gates are built for chains")
+        w = I.custom(w, name=w.name + "_gdk", gate_dk=True)
     ws, rank, local = dist_env()
 
     if args.impl == "reference":
