@@ -18,4 +18,7 @@ from .oracle import (  # noqa: F401
     draw,
     accept_stats,
     adaptive_enabled,
+    AttnDims,
+    attn_verify,
+    attn_truncate,
 )

@@ -20,6 +20,9 @@
  *         longest prefix with draft == argmax, then append the target's argmax as correction.
  *  [COL]  colibrì analysis ch.08 "MTP 投机解码与预取", §5 rejection sampling: accept draft k with
  *         probability p(draft k); on rejection ban that token, zero it, renormalise, resample.
+ *  [GDN] §2.1 / §2.2 also fix the hybrid's other layer type: standard multi-head attention with a
+ *         KV cache, whose N verify positions are computed in parallel (oracle_attn_verify), and
+ *         whose rejected positions are dropped by truncating the cache length (oracle_attn_truncate).
  * The update rule itself is the standard gated delta rule
  *     S_t = g_t S_{t-1} (I − β_t k_t k_tᵀ) + β_t v_t k_tᵀ,  o_t = S_t q_t,
  * written here in its innovation form u = g_t S k_t, δ_t = β_t (v_t − u), S ← g_t S + δ_t k_tᵀ,
@@ -442,3 +445,80 @@ int oracle_accept_tree(int B, int T, int V, int64_t row_stride, int64_t seq_stri
     }
     return bad;
 }
+
+/* ------------------------------------------------------------------------------------------
+ * Full-attention layer verify ([GDN] §2.1: the hybrid's attention layers are standard multi-head
+ * attention over a KV cache; §2.2: the N verify positions run in parallel, not step by step).
+ * Per layer l and sequence b with n0 = kv_len[b] committed rows: the T new key / value rows are
+ * written to cache rows n0 .. n0+T-1 of their kv head; then query row (i, hq) reads kv head
+ * hq / (Hq / Hkv) and attends causally to rows 0 .. n0+i:
+ *     s_j = scale · q·k_j,   p = softmax(s),   o = Σ_j p_j v_j.
+ * The softmax is evaluated as exp(s_j − max s) / Σ exp(s_j − max s) (the same quotient).
+ * ------------------------------------------------------------------------------------------ */
+int oracle_attn_verify(const oracle_attn_dims* a, const int32_t* kv_len, const double* q,
+                       const double* k_new, const double* v_new, double* k_cache,
+                       double* v_cache, double* out) {
+    const int L = a->L, B = a->B, T = a->T, Hq = a->Hq, Hkv = a->Hkv, D = a->D, ctx = a->ctx;
+    const int group = Hq / Hkv;
+    int bad = 0;
+    double* s = (double*)malloc(sizeof(double) * (size_t)(ctx > 0 ? ctx : 1));
+    for (int b = 0; b < B; ++b) {
+        const int n0 = kv_len[b];
+        if (n0 < 0 || n0 > ctx - T) { bad |= 1; continue; }
+        for (int l = 0; l < L; ++l) {
+            const size_t lb = (size_t)l * B + b;
+            /* append the T new rows */
+            for (int i = 0; i < T; ++i)
+                for (int h = 0; h < Hkv; ++h) {
+                    const size_t src = ((lb * T + i) * Hkv + h) * (size_t)D;
+                    const size_t dst = ((lb * Hkv + h) * (size_t)ctx + (size_t)(n0 + i)) * D;
+                    for (int e = 0; e < D; ++e) {
+                        k_cache[dst + e] = k_new[src + e];
+                        v_cache[dst + e] = v_new[src + e];
+                    }
+                }
+            /* causal attention of every query row */
+            for (int i = 0; i < T; ++i)
+                for (int hq = 0; hq < Hq; ++hq) {
+                    const int h = hq / group;
+                    const double* qv = q + ((lb * T + i) * Hq + hq) * (size_t)D;
+                    const double* K = k_cache + (lb * Hkv + h) * (size_t)ctx * D;
+                    const double* V = v_cache + (lb * Hkv + h) * (size_t)ctx * D;
+                    const int n = n0 + i + 1;          /* visible rows 0 .. n0+i */
+                    double m = -INFINITY;
+                    for (int j = 0; j < n; ++j) {
+                        double dot = 0.0;
+                        for (int e = 0; e < D; ++e) dot += qv[e] * K[(size_t)j * D + e];
+                        s[j] = a->scale * dot;
+                        if (s[j] > m) m = s[j];
+                    }
+                    double z = 0.0;
+                    for (int j = 0; j < n; ++j) {
+                        s[j] = exp(s[j] - m);
+                        z += s[j];
+                    }
+                    double* o = out + ((lb * T + i) * Hq + hq) * (size_t)D;
+                    for (int e = 0; e < D; ++e) {
+                        double acc = 0.0;
+                        for (int j = 0; j < n; ++j) acc += s[j] * V[(size_t)j * D + e];
+                        o[e] = acc / z;
+                    }
+                }
+        }
+    }
+    free(s);
+    return bad;
+}
+
+/* KV truncation on reject: of the T appended rows the first n (the accepted drafts) stay, the
+ * rest are dropped by the length alone (their slots are overwritten next round). */
+int oracle_attn_truncate(int B, int T, const int32_t* n_acc, int32_t* kv_len) {
+    int bad = 0;
+    for (int b = 0; b < B; ++b) {
+        const int n = n_acc[b];
+        if (n < 0 || n > T) { bad |= 1; continue; }
+        kv_len[b] += n;
+    }
+    return bad;
+}
+

@@ -54,6 +54,21 @@ int oracle_accept_tree(int B, int T, int V, int64_t row_stride, int64_t seq_stri
                        const float* logits, const int32_t* parent, const int32_t* tokens, int P,
                        int32_t* path, int32_t* n_acc, int32_t* out_tokens);
 
+/* Full-attention layer verify and KV truncation (see oracle.c). q, out [L][B][T][Hq][D];
+ * k_new, v_new [L][B][T][Hkv][D]; k_cache, v_cache [L][B][Hkv][ctx][D] (token-major, appended in
+ * place); kv_len [B]. Returns 1 if some kv_len[b] is outside [0, ctx - T] (sequence skipped). */
+typedef struct oracle_attn_dims {
+    int L, B, T, Hq, Hkv, D, ctx;
+    double scale;
+} oracle_attn_dims;
+
+int oracle_attn_verify(const oracle_attn_dims* a, const int32_t* kv_len, const double* q,
+                       const double* k_new, const double* v_new, double* k_cache,
+                       double* v_cache, double* out);
+
+/* kv_len[b] += n_acc[b] for n in [0, T]; returns 1 (and skips b) for any other n. */
+int oracle_attn_truncate(int B, int T, const int32_t* n_acc, int32_t* kv_len);
+
 #ifdef __cplusplus
 }
 #endif

@@ -43,6 +43,10 @@ def _load():
         _lib.oracle_accept_tree.argtypes = ([ct.c_int] * 3 + [i64, i64, P, P, P, ct.c_int,
                                                                P, P, P])
         _lib.oracle_accept_tree.restype = ct.c_int
+        _lib.oracle_attn_verify.argtypes = [P] * 8
+        _lib.oracle_attn_verify.restype = ct.c_int
+        _lib.oracle_attn_truncate.argtypes = [ct.c_int, ct.c_int, P, P]
+        _lib.oracle_attn_truncate.restype = ct.c_int
         del i32
     return _lib
 
@@ -256,3 +260,55 @@ def adaptive_enabled(proposed, accepted, min_proposed=24, num=1, den=10):
     if proposed < min_proposed:
         return True
     return not (accepted * den < proposed * num)
+
+
+class _CAttnDims(ct.Structure):
+    _fields_ = [(n, ct.c_int) for n in ("L", "B", "T", "Hq", "Hkv", "D", "ctx")] + [
+        ("scale", ct.c_double)]
+
+
+@dataclass
+class AttnDims:
+    """Attention-layer shapes: L layers, B sequences, T verify positions, Hq query heads over Hkv
+    kv heads (query head h reads kv head h // (Hq / Hkv)), head dim D, cache capacity ctx rows;
+    scale defaults to 1 / sqrt(D)."""
+    L: int
+    B: int
+    T: int
+    Hq: int
+    Hkv: int
+    D: int
+    ctx: int
+    scale: float = None
+
+    def c(self):
+        sc = self.scale if self.scale is not None else 1.0 / np.sqrt(self.D)
+        return _CAttnDims(self.L, self.B, self.T, self.Hq, self.Hkv, self.D, self.ctx, float(sc))
+
+
+def attn_verify(dims: AttnDims, kv_len, q, k_new, v_new, k_cache, v_cache):
+    """Full-attention verify. q [L,B,T,Hq,D], k_new / v_new [L,B,T,Hkv,D], caches
+    [L,B,Hkv,ctx,D] token-major, kv_len [B]. Returns (out [L,B,T,Hq,D], k_cache, v_cache (new
+    arrays with the T rows appended), bad)."""
+    d = dims
+    q, k_new, v_new = _f64(q), _f64(k_new), _f64(v_new)
+    kc, vc = _f64(k_cache).copy(), _f64(v_cache).copy()
+    assert q.shape == (d.L, d.B, d.T, d.Hq, d.D), q.shape
+    assert k_new.shape == v_new.shape == (d.L, d.B, d.T, d.Hkv, d.D)
+    assert kc.shape == vc.shape == (d.L, d.B, d.Hkv, d.ctx, d.D)
+    assert d.Hq % d.Hkv == 0
+    n = _i32(kv_len)
+    out = np.zeros_like(q)
+    cd = d.c()
+    bad = _load().oracle_attn_verify(ct.byref(cd), _p(n), _p(q), _p(k_new), _p(v_new), _p(kc),
+                                     _p(vc), _p(out))
+    return out, kc, vc, bad
+
+
+def attn_truncate(T, n_acc, kv_len):
+    """KV truncation: returns (kv_len + n_acc where 0 <= n <= T, bad)."""
+    n = _i32(n_acc)
+    kl = _i32(kv_len).copy()
+    bad = _load().oracle_attn_truncate(len(kl), int(T), _p(n), _p(kl))
+    return kl, bad
+
