@@ -544,10 +544,15 @@ def main(argv=None):
                     help="override the workload's batch (smaller profiling cases)")
     ap.add_argument("--layers", type=int, default=None,
                     help="override the workload's layer count (smaller profiling cases)")
+    ap.add_argument("--attn", default=None,
+                    help="time the attention layers instead (an ATTN_WORKLOADS key, e.g. "
+                         "qwen36_attn_b64_n8)")
     ap.add_argument("--gate-dk", action="store_true",
                     help="one gate per key channel (g [L, B, T, Hv, d]); chain workloads only")
     args = ap.parse_args(argv)
 
+    if args.attn:
+        return run_attn(args)
     from speculative_verify_gdn_gb300 import inputs as I
     w = I.WORKLOADS[args.config]
     if args.batch is not None or args.layers is not None:
@@ -596,6 +601,102 @@ def main(argv=None):
                       "tokens/s = N / (L * unit + accept)" % (units, t_unit * 1e3, t_acc * 1e3)}
     if rank == 0:
         print(json.dumps(line), flush=True)
+    return 0
+
+
+ATTN_METRIC = ("attention-layer verified draft tokens/sec (KV append + causal GQA attention + "
+               "KV truncation); % HBM roofline")
+
+
+def bytes_attn(w, n0):
+    """Algorithmic bytes of one attn_verify call: the appended key / value rows read and written,
+    every attended key and value read once ((n0 + T) rows per (layer, sequence, kv head)), q read
+    and o written (bf16)."""
+    rows_new = w.L * w.B * w.T * w.Hkv * w.D * 2
+    kv = sum(2 * (int(n) + w.T) * w.D * 2 for n in n0) * w.L * w.Hkv
+    qo = 2 * w.L * w.B * w.T * w.Hq * w.D * 2
+    return 2 * 2 * rows_new + kv + qo
+
+
+def run_attn(args):
+    """The hybrid's attention layers: one step = attn_verify (append + attention, all layers) and
+    attn_truncate. The accepted counts are zero, so every step appends to and attends over the
+    same committed rows (constant work per step)."""
+    import torch
+    from speculative_verify_gdn_gb300 import _lib, build as lib_build, inputs as I
+    w = I.ATTN_WORKLOADS[args.attn]
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    lib_build.build()
+    sh = _lib.AttnShape(L=w.L, B=w.B, T=w.T, Hq=w.Hq, Hkv=w.Hkv, D=w.D, ctx=w.ctx)
+    kc, vc = I.attn_cache(w, args.seed, device)
+    vt = vc.transpose(-1, -2).contiguous()
+    del vc
+    kv_len = I.attn_lengths(w).to(device)
+    pool = [I.attn_round(w, k, args.seed, device) for k in range(POOL)]
+    out = torch.empty(sh.q_shape(), dtype=torch.bfloat16, device=device)
+    nws = _lib.attn_workspace_bytes(sh)
+    ws = torch.empty(max(nws, 16), dtype=torch.uint8, device=device) if nws else None
+    n_acc = torch.zeros(w.B, dtype=torch.int32, device=device)
+    status = torch.zeros(1, dtype=torch.int32, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def step(k, evs=None):
+        q, kn, vn = pool[k % POOL]
+        if evs is not None:
+            evs[0].record(stream)
+        _lib.attn_verify(sh, q, kn, vn, kc, vt, kv_len, out, workspace=ws, status=status)
+        if evs is not None:
+            evs[1].record(stream)
+        _lib.attn_truncate(n_acc, kv_len, w.T, status=status)
+        if evs is not None:
+            evs[2].record(stream)
+
+    for k in range(args.warmup):
+        step(k)
+    torch.cuda.synchronize(device)
+    assert int(status.item()) == 0, _lib.decode_status(int(status.item()))
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(0)
+    clocks.start()
+    torch.cuda.synchronize(device)
+    start.record(stream)
+    for k in range(K):
+        step(args.warmup + k, evs[k])
+    end.record(stream)
+    torch.cuda.synchronize(device)
+    clk = clocks.stop()
+    assert int(status.item()) == 0, _lib.decode_status(int(status.item()))
+    ms_step = start.elapsed_time(end) / K
+    t_att = statistics.mean(evs[k][0].elapsed_time(evs[k][1]) for k in range(K))
+    t_tr = statistics.mean(evs[k][1].elapsed_time(evs[k][2]) for k in range(K))
+    peak, peak_kind = read_peaks()
+    n0 = I.attn_lengths(w).tolist()
+    ba = bytes_attn(w, n0)
+    achieved = ba / (t_att / 1e3) / 1e9
+    splits = 1 if not nws else None
+    line = {
+        "metric": ATTN_METRIC, "value": w.B * w.T / (ms_step / 1e3), "unit": UNIT, "n_gpus": 1,
+        "steps": K, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": "%s: %d attention layers (Qwen3.6-shaped: %d query heads over %d kv "
+                               "heads of dim %d), batch %d, T=%d verify positions, %d committed "
+                               "cache rows (capacity %d); accepted counts 0, so the work per step "
+                               "is constant" % (w.name, w.L, w.Hq, w.Hkv, w.D, w.B, w.T,
+                                                w.lengths[0], w.ctx),
+                   "l2": "inputs larger than L2: %.2f GB of K / V cache read every step"
+                         % (sum(2 * (n + w.T) * w.D * 2 for n in n0) * w.L * w.Hkv / 1e9),
+                   "key_splits": "none" if splits == 1 else "flash-decoding split + combine"},
+        "roofline": {"bound": "hbm", "kernel": "attn_verify", "achieved": achieved, "peak": peak,
+                     "peak_source": "MEASURED_PEAKS.json hbm_gbs (%s)" % peak_kind, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None, "algorithmic_bytes_per_launch": ba},
+        "kernels": {"attn_verify": {"ms": t_att, "bytes": ba, "GBps": achieved},
+                    "attn_truncate": {"ms": t_tr}},
+        "gpu_launches": K * (3 if nws == 0 else 4), "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
     return 0
 
 

@@ -59,6 +59,8 @@ extern "C" {
 #define GDN_STATUS_BAD_TOKEN   0x4u  /* accept: draft / tree token outside [0, V) */
 #define GDN_STATUS_BAD_PATH    0x8u  /* path rollback: path node out of range */
 #define GDN_STATUS_EMPTY_DIST  0x10u /* sampling: a distribution with zero total weight */
+#define GDN_STATUS_WAIT_TIMEOUT 0x20u /* a bounded on-chip wait gave up (results unspecified) */
+#define GDN_STATUS_BAD_LEN     0x40u /* attention: kv_len outside [0, ctx - T] (or length overflow) */
 
 /* ---- element types ---------------------------------------------------------------------- */
 #define GDN_DTYPE_F32   0
@@ -299,6 +301,58 @@ GDN_API int spec_accept_static(const spec_dims* d, const void* logits, const int
 
 /* Thread-local message for the last non-OK return on this thread ("" if none). */
 GDN_API const char* gdn_last_error(void);
+
+/* ---- full-attention layers of the hybrid ------------------------------------------------ */
+/*
+ * Shapes of one attn_verify call (GDN investigation §2.1: the hybrid's other layer type is
+ * standard multi-head attention over a KV cache; §2.2: its N verify positions run in parallel).
+ *  L    attention layers covered by the call        B  sequences      T  verify positions
+ *  Hq, Hkv  query and kv heads, Hq a multiple of Hkv; query head h reads kv head h / (Hq/Hkv)
+ *  D    head dim (built for 128 and 256)            T * (Hq / Hkv) <= 128
+ *  ctx  cache capacity in rows per (layer, sequence, kv head), a multiple of 8
+ *  scale  multiplies q·k (1/sqrt(D) for the usual scaled dot product)
+ */
+typedef struct attn_dims {
+    int32_t L, B, T;
+    int32_t Hq, Hkv, D;
+    int32_t ctx;
+    float scale;
+} attn_dims;
+
+/*
+ * attn_verify — the T verify positions of every attention layer in one launch sequence:
+ * append their key / value rows to the cache at rows kv_len[b] .. kv_len[b]+T-1, then
+ *     o(i, h) = Σ_{j ≤ kv_len[b]+i} softmax_j(scale · q(i, h)·k_j) v_j
+ * over kv head h / (Hq/Hkv) (causal inside the new block). kv_len is read on the device and is
+ * not changed (attn_truncate moves it once the round is accepted).
+ * Arguments (device, bf16 unless noted):
+ *   q         [L][B][T][Hq][D]
+ *   k_new, v_new [L][B][T][Hkv][D]   the positions' projected keys / values
+ *   k_cache   [L][B][Hkv][ctx][D]    token-major: row j is the key of position j
+ *   vt_cache  [L][B][Hkv][D][ctx]    value cache stored transposed: column j is the value of
+ *                                    position j (both tensor-core operands then read K-major)
+ *   kv_len    [B] int32              committed rows per sequence (the same for every layer)
+ *   out       [L][B][T][Hq][D]
+ *   workspace attn_workspace_bytes(d) bytes (16-byte aligned; NULL when that is 0)
+ * Rows of the caches at or beyond kv_len[b] + T are never attended, but their values are
+ * multiplied by zero weights: keep them finite (allocate the caches zeroed). q, k_cache and
+ * vt_cache must be 16-byte aligned (TMA). A sequence with kv_len[b] outside [0, ctx − T] sets
+ * GDN_STATUS_BAD_LEN and is skipped (cache and out rows unwritten).
+ */
+GDN_API int attn_verify(const attn_dims* d, const void* q, const void* k_new, const void* v_new,
+                        void* k_cache, void* vt_cache, const int32_t* kv_len, void* out,
+                        void* workspace, size_t workspace_bytes, uint32_t* status, void* stream);
+
+/* Scratch bytes attn_verify needs for d (partial results when the cache is split across CTAs). */
+GDN_API size_t attn_workspace_bytes(const attn_dims* d);
+
+/*
+ * attn_truncate — KV truncation on reject: kv_len[b] += n_acc[b] (the accepted drafts' rows stay,
+ * the rest are dropped by the length alone and overwritten next round). n_acc, kv_len [B] int32
+ * device; n outside [0, T] sets GDN_STATUS_BAD_NACC and leaves kv_len[b].
+ */
+GDN_API int attn_truncate(int32_t B, int32_t T, const int32_t* n_acc, int32_t* kv_len,
+                          uint32_t* status, void* stream);
 
 #ifdef __cplusplus
 }

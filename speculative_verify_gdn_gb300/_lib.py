@@ -26,12 +26,14 @@ STATUS_BITS = {
     0x8: "BAD_PATH",
     0x10: "EMPTY_DIST",
     0x20: "WAIT_TIMEOUT",
+    0x40: "BAD_LEN",
 }
 
 # exported entry points of include/gdnspec.h
 EXPORTS = ("gdn_verify", "gdn_verify_tree", "gdn_rollback", "gdn_rollback_path",
            "gdn_rollback_verify", "gdn_tape_bytes", "spec_accept", "spec_workspace_bytes", "spec_accept_tree",
-           "spec_accept_static", "spec_stats_accumulate", "gdn_last_error")
+           "spec_accept_static", "spec_stats_accumulate", "attn_verify", "attn_workspace_bytes",
+           "attn_truncate", "gdn_last_error")
 
 
 class GdnError(RuntimeError):
@@ -43,6 +45,11 @@ class _Dims(ct.Structure):
                                            "io_dtype")] + [("qk_scale", ct.c_float),
                                                            ("l2_eps", ct.c_float),
                                                            ("gate_dk", ct.c_int32)]
+
+
+class _AttnDims(ct.Structure):
+    _fields_ = [(n, ct.c_int32) for n in ("L", "B", "T", "Hq", "Hkv", "D", "ctx")] + [
+        ("scale", ct.c_float)]
 
 
 class _SpecDims(ct.Structure):
@@ -88,6 +95,12 @@ def load(require_file=True):
     lib.spec_accept_static.restype = ct.c_int
     lib.spec_stats_accumulate.argtypes = [i32, i32, P, P, P, P]
     lib.spec_stats_accumulate.restype = ct.c_int
+    lib.attn_verify.argtypes = [P] * 9 + [sz, P, P]
+    lib.attn_verify.restype = ct.c_int
+    lib.attn_workspace_bytes.argtypes = [P]
+    lib.attn_workspace_bytes.restype = sz
+    lib.attn_truncate.argtypes = [i32, i32, P, P, P, P]
+    lib.attn_truncate.restype = ct.c_int
     lib.gdn_last_error.argtypes = []
     lib.gdn_last_error.restype = ct.c_char_p
     _lib = lib
@@ -326,3 +339,68 @@ def spec_accept_tree(logits, parent, tokens, path, n_acc, out_tokens, workspace,
 def decode_status(value):
     value = int(value) & 0xFFFFFFFF
     return [name for bit, name in STATUS_BITS.items() if value & bit]
+
+
+# ------------------------------------------------------------------ attention layers
+@dataclass
+class AttnShape:
+    """Shapes of one attn_verify call (see attn_dims in include/gdnspec.h); scale defaults to
+    1/sqrt(D)."""
+    L: int
+    B: int
+    T: int
+    Hq: int
+    Hkv: int
+    D: int
+    ctx: int
+    scale: float = None
+
+    def c(self):
+        sc = self.scale if self.scale is not None else 1.0 / self.D ** 0.5
+        return _AttnDims(self.L, self.B, self.T, self.Hq, self.Hkv, self.D, self.ctx, sc)
+
+    def q_shape(self):
+        return (self.L, self.B, self.T, self.Hq, self.D)
+
+    def kv_new_shape(self):
+        return (self.L, self.B, self.T, self.Hkv, self.D)
+
+    def k_cache_shape(self):
+        return (self.L, self.B, self.Hkv, self.ctx, self.D)
+
+    def vt_cache_shape(self):
+        return (self.L, self.B, self.Hkv, self.D, self.ctx)
+
+
+def attn_workspace_bytes(shape: AttnShape):
+    return int(load().attn_workspace_bytes(ct.byref(shape.c())))
+
+
+def attn_verify(shape: AttnShape, q, k_new, v_new, k_cache, vt_cache, kv_len, out,
+                workspace=None, status=None, stream=None):
+    """attn_verify: append the T positions' k / v rows at kv_len and attend causally over the
+    cache (kv_len itself is left for attn_truncate)."""
+    lib = load()
+    bf = torch.bfloat16
+    d = shape.c()
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    args = [_ptr(q, bf, shape.q_shape(), "q"),
+            _ptr(k_new, bf, shape.kv_new_shape(), "k_new"),
+            _ptr(v_new, bf, shape.kv_new_shape(), "v_new"),
+            _ptr(k_cache, bf, shape.k_cache_shape(), "k_cache"),
+            _ptr(vt_cache, bf, shape.vt_cache_shape(), "vt_cache"),
+            _ptr(kv_len, torch.int32, (shape.B,), "kv_len"),
+            _ptr(out, bf, shape.q_shape(), "out"),
+            _ptr(workspace, None, None, "workspace"), ct.c_size_t(ws_bytes),
+            _ptr(status, torch.int32, None, "status"), _stream(stream)]
+    _check(lib.attn_verify(ct.byref(d), *args), "attn_verify")
+
+
+def attn_truncate(n_acc, kv_len, T, status=None, stream=None):
+    """attn_truncate: kv_len[b] += n_acc[b] on the device."""
+    B = kv_len.shape[0]
+    _check(load().attn_truncate(B, int(T), _ptr(n_acc, torch.int32, (B,), "n_acc"),
+                                _ptr(kv_len, torch.int32, (B,), "kv_len"),
+                                _ptr(status, torch.int32, None, "status"), _stream(stream)),
+           "attn_truncate")
+

@@ -264,6 +264,51 @@ gdn::AcceptArgs accept_args(const spec_dims* d, const void* logits, void* worksp
     return a;
 }
 
+int check_attn(const attn_dims* d) {
+    if (!d) return fail(GDN_ERR_INVALID_ARG, "dims is NULL");
+    if (d->L < 0 || d->B < 0 || d->T < 0)
+        return fail(GDN_ERR_INVALID_ARG, "negative L/B/T (%d, %d, %d)", d->L, d->B, d->T);
+    if (d->Hkv < 1 || d->Hq < 1 || d->Hq % d->Hkv != 0)
+        return fail(GDN_ERR_INVALID_ARG, "Hq (%d) must be a positive multiple of Hkv (%d)", d->Hq,
+                    d->Hkv);
+    if (d->D != 128 && d->D != 256)
+        return fail(GDN_ERR_UNSUPPORTED, "attention head dim D=%d: built for 128 and 256", d->D);
+    if (1LL * d->T * (d->Hq / d->Hkv) > 128)
+        return fail(GDN_ERR_UNSUPPORTED, "T * Hq/Hkv = %lld query rows per kv head > 128",
+                    1LL * d->T * (d->Hq / d->Hkv));
+    if (d->ctx < 128 || d->ctx % 8 != 0)
+        return fail(GDN_ERR_UNSUPPORTED, "cache capacity ctx=%d: needs >= 128 and a multiple of 8",
+                    d->ctx);
+    if (d->T > d->ctx) return fail(GDN_ERR_INVALID_ARG, "T=%d > ctx=%d", d->T, d->ctx);
+    if (!std::isfinite(d->scale)) return fail(GDN_ERR_INVALID_ARG, "scale must be finite");
+    const long long heads = 1LL * d->L * d->B * d->Hkv;
+    if (heads * d->ctx >= (1LL << 31) || heads * d->D >= (1LL << 31) || d->B > 65535 ||
+        d->L > 65535)
+        return fail(GDN_ERR_UNSUPPORTED, "attention caches too large for 32-bit row indices");
+    return GDN_OK;
+}
+
+// Key splits: about two CTAs per SM of a 152-SM GB300 in total (a fixed target, so the workspace
+// size depends on the shapes alone).
+void attn_split(const attn_dims* d, int* splits, int* tiles_per_split) {
+    const long long units = 1LL * d->L * d->B * d->Hkv;
+    const int cap = (d->ctx + 127) / 128;
+    long long want = units > 0 ? (304 + units - 1) / units : 1;
+    int sp = int(want < cap ? want : cap);
+    if (sp < 1) sp = 1;
+    const int t = (cap + sp - 1) / sp;
+    *tiles_per_split = t;
+    *splits = (cap + t - 1) / t;
+}
+
+size_t attn_ws_bytes(const attn_dims* d) {
+    int sp, tps;
+    attn_split(d, &sp, &tps);
+    if (sp <= 1) return 0;
+    const size_t rows = size_t(sp) * d->L * d->B * d->Hkv * size_t(d->T) * (d->Hq / d->Hkv);
+    return rows * (size_t(d->D) + 2) * 4;
+}
+
 }  // namespace
 
 namespace gdn {
@@ -453,6 +498,89 @@ int gdn_rollback_verify(const gdn_dims* d, const int32_t* n_acc_prev, const floa
     if (rc) return rc;
     return verify_common(d, nullptr, qkv, conv_w, conv_state, g, beta, state, out, tape_delta,
                          tape_k, status, stream, false);
+}
+
+size_t attn_workspace_bytes(const attn_dims* d) {
+    if (check_attn(d) != GDN_OK) return 0;
+    return attn_ws_bytes(d);
+}
+
+int attn_verify(const attn_dims* d, const void* q, const void* k_new, const void* v_new,
+                void* k_cache, void* vt_cache, const int32_t* kv_len, void* out, void* workspace,
+                size_t workspace_bytes, uint32_t* status, void* stream) {
+    int rc = check_attn(d);
+    if (rc) return rc;
+    if (d->L == 0 || d->B == 0 || d->T == 0) return GDN_OK;
+    if (!q || !k_new || !v_new || !k_cache || !vt_cache || !kv_len || !out)
+        return fail(GDN_ERR_INVALID_ARG, "NULL tensor pointer");
+    if (!aligned(q, 16) || !aligned(k_new, 16) || !aligned(k_cache, 16) || !aligned(vt_cache, 16))
+        return fail(GDN_ERR_INVALID_ARG,
+                    "q, k_new, k_cache and vt_cache must be 16-byte aligned (TMA / vector copies)");
+    if (!aligned(v_new, 2) || !aligned(out, 2) || !aligned(kv_len, 4))
+        return fail(GDN_ERR_INVALID_ARG, "misaligned tensor pointer");
+    const size_t need = attn_ws_bytes(d);
+    if (need && (!workspace || workspace_bytes < need || !aligned(workspace, 16)))
+        return fail(GDN_ERR_INVALID_ARG, "workspace %zu bytes (16-byte aligned) < %zu required",
+                    workspace_bytes, need);
+    EncodeTiledFn enc = encode_tiled();
+    if (!enc) return fail(GDN_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable from the driver");
+    const cuuint64_t heads = cuuint64_t(d->L) * d->B * d->Hkv;
+    cuuint32_t estr[2] = {1, 1};
+    cuuint32_t box[2] = {64, 128};
+    CUtensorMap kmap, vmap;
+    {
+        cuuint64_t dims[2] = {cuuint64_t(d->D), heads * cuuint64_t(d->ctx)};
+        cuuint64_t strides[1] = {cuuint64_t(d->D) * 2};
+        if (enc(&kmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, k_cache, dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return fail(GDN_ERR_CUDA, "cuTensorMapEncodeTiled failed for the K cache");
+    }
+    {
+        cuuint64_t dims[2] = {cuuint64_t(d->ctx), heads * cuuint64_t(d->D)};
+        cuuint64_t strides[1] = {cuuint64_t(d->ctx) * 2};
+        if (enc(&vmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, vt_cache, dims, strides, box, estr,
+                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return fail(GDN_ERR_CUDA, "cuTensorMapEncodeTiled failed for the V cache");
+    }
+    gdn::AttnArgs a{};
+    a.L = d->L; a.B = d->B; a.T = d->T; a.Hq = d->Hq; a.Hkv = d->Hkv; a.D = d->D; a.ctx = d->ctx;
+    a.group = d->Hq / d->Hkv;
+    a.nq = d->T * a.group;
+    a.units = d->L * d->B * d->Hkv;
+    attn_split(d, &a.splits, &a.tiles_per_split);
+    a.sl2 = float(double(d->scale) * 1.4426950408889634);
+    a.q = static_cast<const __nv_bfloat16*>(q);
+    a.k_new = static_cast<const __nv_bfloat16*>(k_new);
+    a.v_new = static_cast<const __nv_bfloat16*>(v_new);
+    a.k_cache = static_cast<__nv_bfloat16*>(k_cache);
+    a.vt_cache = static_cast<__nv_bfloat16*>(vt_cache);
+    a.out = static_cast<__nv_bfloat16*>(out);
+    a.kv_len = kv_len;
+    a.status = status;
+    if (a.splits > 1) {
+        a.ws_o = static_cast<float*>(workspace);
+        a.ws_ml = a.ws_o + size_t(a.splits) * a.units * a.nq * d->D;
+    }
+    if (1LL * a.units * a.splits >= (1LL << 31))
+        return fail(GDN_ERR_UNSUPPORTED, "attention grid too large");
+    const cudaError_t e = gdn::launch_attn_verify(a, kmap, vmap, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "attn_verify launch");
+    return GDN_OK;
+}
+
+int attn_truncate(int32_t B, int32_t T, const int32_t* n_acc, int32_t* kv_len, uint32_t* status,
+                  void* stream) {
+    if (B < 0 || T < 0) return fail(GDN_ERR_INVALID_ARG, "B = %d, T = %d", B, T);
+    if (B == 0) return GDN_OK;
+    if (!n_acc || !kv_len) return fail(GDN_ERR_INVALID_ARG, "NULL pointer");
+    if (!aligned(n_acc, 4) || !aligned(kv_len, 4))
+        return fail(GDN_ERR_INVALID_ARG, "misaligned n_acc or kv_len");
+    const cudaError_t e =
+        gdn::launch_attn_truncate(B, T, n_acc, kv_len, status, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "attn_truncate launch");
+    return GDN_OK;
 }
 
 }  // extern "C"

@@ -1,0 +1,545 @@
+// attn.cu — the hybrid's full-attention layers in the verify step: append the T verify positions'
+// key / value rows to the KV cache, causal GQA attention of those positions over the cache, and
+// the KV truncation on reject (sm_103a, tcgen05 tensor cores).
+//
+// "Speculative Decoding on GDN Hybrid Architectures: A 31-Experiment Investigation", §2.1 (the
+// hybrid's attention layers are standard multi-head attention over a KV cache) and §2.2 (their
+// N verify positions run in one parallel pass, unlike the GDN layers).
+//
+// GB300 design:
+//   * A small kernel appends the T new rows; the attention kernel then reads every key through
+//     TMA. The K cache is token-major [ctx][D]; the V cache is stored transposed [D][ctx], so both
+//     tensor-core products read K-major, 128-byte-swizzled tiles exactly as the TMA boxes land.
+//   * One CTA per (layer, sequence, kv head, key split). Its query rows are the T·(Hq/Hkv)
+//     (position, head) pairs of the kv head, zero-padded to NQ ∈ {32, 64, 128}. Per 128-key tile:
+//         Sᵀ[key][row]  = K_tile · Qᵀ       tcgen05, M = 128 keys, N = NQ, K = D
+//         Oᵀ[d][row]   += Vᵀ_tile · Pᵀ      tcgen05, M = 128 d-rows per chunk, N = NQ, K = 128 keys
+//     Sᵀ is double-buffered in TMEM (the next tile's product overlaps this tile's softmax) and
+//     Oᵀ accumulates in TMEM across the tiles.
+//   * Softmax: 4 warps, thread = key = TMEM lane. Column maxima by a transposing warp reduction
+//     (31 shuffles per 32 columns) plus a 4-way shared-memory step. The running maximum moves only
+//     when a tile's maximum exceeds it by more than 8 (log2 units), so Oᵀ is rescaled rarely and
+//     the weights stay ≤ 2^8. P is rounded to bf16 for the tensor core; the normaliser sums the
+//     rounded values, so numerator and denominator use the same weights.
+//   * Warp roles: 0-3 softmax + epilogue, 4 TMA producer, 5 MMA issue + TMEM owner. The ring
+//     holds 32 KiB chunks (128 keys × 128 of the head dim, or 128 d-rows × 128 keys) in the order
+//     the tensor core consumes them: K(0), K(1), V(0), K(2), V(1), …
+//   * Short batches over long caches split the keys across CTAs (flash-decoding); a combine
+//     kernel merges the partial (max, sum, O).
+// Every wait is bounded (1 s); a timeout sets GDN_STATUS_WAIT_TIMEOUT, the CTA stops issuing
+// work, lets its copies land, waits for its tensor-core work and frees its TMEM.
+#include "common.cuh"
+#include "kernels.h"
+#include "tc.cuh"
+
+namespace gdn {
+
+template <int D, int NQ>
+struct AttnCfg {
+    static constexpr int NTHR = 192;
+    static constexpr int DCH = D / 128;                 // 128-wide chunks of the head dim
+    static constexpr int CHUNK = 128 * 128 * 2;         // one ring stage: two 64-wide swizzled blocks
+    static constexpr int NST = NQ >= 128 ? 3 : 4;       // ring stages
+    static constexpr int Q_KB = NQ * 128;               // bytes of one 64-element K-block of Q
+    static constexpr int Q_BYTES = (D / 64) * Q_KB;
+    static constexpr int P_KB = NQ * 128;               // bytes of one 64-key K-block of P
+    static constexpr int P_BYTES = 2 * P_KB;
+    static constexpr size_t OFF_RING = 0;
+    static constexpr size_t OFF_Q = OFF_RING + size_t(NST) * CHUNK;
+    static constexpr size_t OFF_P = OFF_Q + Q_BYTES;
+    static constexpr size_t OFF_F = OFF_P + P_BYTES;    // redA[4][NQ] redB[4][NQ] m, alpha, l [NQ]
+    static constexpr size_t OFF_LIM = OFF_F + size_t(11) * NQ * 4;   // int lim[NQ]
+    // barriers: full[NST] empty[NST] s_full[2] s_free[2] p_full pv_done fin
+    static constexpr int NBAR = 2 * NST + 7;
+    static constexpr size_t OFF_BAR = (OFF_LIM + size_t(NQ) * 4 + 7) / 8 * 8;
+    static constexpr size_t OFF_MISC = OFF_BAR + size_t(NBAR) * 8;   // abort flag, TMEM slot
+    static constexpr size_t SMEM = OFF_MISC + 16 + 1024;             // + base alignment slack
+    static constexpr int TM_S = 0;                       // Sᵀ buffers: columns [0, 2 NQ)
+    static constexpr int TM_O = 2 * NQ;                  // Oᵀ: DCH blocks of NQ columns
+    static constexpr int TM_USED = 2 * NQ + DCH * NQ;
+    static constexpr int TM_COLS = TM_USED <= 32 ? 32 : TM_USED <= 64 ? 64 : TM_USED <= 128 ? 128
+                                 : TM_USED <= 256 ? 256 : 512;
+    static_assert(D == 128 || D == 256, "head dim");
+    static_assert(NQ == 32 || NQ == 64 || NQ == 128, "query rows");
+    static_assert(TM_USED <= 512, "TMEM columns");
+    static_assert(OFF_Q % 1024 == 0 && OFF_P % 1024 == 0 && Q_KB % 1024 == 0, "swizzle atoms");
+    static_assert(SMEM <= 227 * 1024, "shared memory");
+};
+
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Reduce 32 per-lane values over the warp, column by column: after recursive halving (31
+// shuffles) this lane holds the total of column *col (max or sum).
+template <bool MAX>
+__device__ __forceinline__ float warp_cols32(float (&v)[32], int lane, int* col) {
+    int base = 0;
+#pragma unroll
+    for (int m = 32, o = 16; m > 1; m >>= 1, o >>= 1) {
+        const bool up = (lane & o) != 0;
+#pragma unroll
+        for (int k = 0; k < m / 2; ++k) {
+            const float send = up ? v[k] : v[k + m / 2];
+            const float keep = up ? v[k + m / 2] : v[k];
+            const float got = __shfl_xor_sync(0xffffffffu, send, o);
+            v[k] = MAX ? fmaxf(keep, got) : keep + got;
+        }
+        base += up ? m / 2 : 0;
+    }
+    *col = base;
+    return v[0];
+}
+
+// ------------------------------------------------------------------ append the new rows
+__global__ void __launch_bounds__(256) attn_append_kernel(const AttnArgs a) {
+    const int b = blockIdx.x, l = blockIdx.y;
+    const int n0 = __ldg(a.kv_len + b);
+    if (n0 < 0 || n0 > a.ctx - a.T) {
+        if (l == 0 && threadIdx.x == 0) set_status(a.status, GDN_STATUS_BAD_LEN);
+        return;
+    }
+    const size_t lb = size_t(l) * a.B + b;
+    const int D = a.D, T = a.T, H = a.Hkv, D8 = a.D / 8;
+    // keys: 16-byte pieces of whole rows
+    for (int e = threadIdx.x; e < T * H * D8; e += blockDim.x) {
+        const int d8 = e % D8, r = e / D8, h = r % H, i = r / H;
+        const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.k_new + ((lb * T + i) * H + h) * size_t(D)) + d8);
+        reinterpret_cast<uint4*>(a.k_cache + ((lb * H + h) * size_t(a.ctx) + n0 + i) * size_t(D))[d8] = v;
+    }
+    // values: position n0 + i is column n0 + i of every (h, d) row of the transposed cache
+    for (int e = threadIdx.x; e < H * D; e += blockDim.x) {
+        const int h = e / D, d = e - h * D;
+        __nv_bfloat16* dst = a.vt_cache + ((lb * H + h) * size_t(D) + d) * size_t(a.ctx) + n0;
+        for (int i = 0; i < T; ++i) dst[i] = a.v_new[((lb * T + i) * H + h) * size_t(D) + d];
+    }
+}
+
+// ------------------------------------------------------------------ attention
+template <int D, int NQ>
+__global__ void __launch_bounds__(192, 1)
+attn_verify_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap,
+                   const __grid_constant__ CUtensorMap vmap) {
+    using Cfg = AttnCfg<D, NQ>;
+    constexpr int NST = Cfg::NST, DCH = Cfg::DCH, NCB = NQ / 32;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    unsigned char* ring = smem + Cfg::OFF_RING;
+    unsigned char* Qs = smem + Cfg::OFF_Q;
+    unsigned char* Ps = smem + Cfg::OFF_P;
+    float* redA = reinterpret_cast<float*>(smem + Cfg::OFF_F);   // [4][NQ] tile maxima per warp
+    float* redB = redA + 4 * NQ;                                  // [4][NQ] tile sums per warp
+    float* m_run = redB + 4 * NQ;                                 // running maximum (log2 units)
+    float* alpha = m_run + NQ;                                    // this tile's rescale factor
+    float* lfin = alpha + NQ;                                     // final normaliser
+    int* lim = reinterpret_cast<int*>(smem + Cfg::OFF_LIM);       // last key each row may see
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + Cfg::OFF_BAR);
+    uint64_t* empty = full + NST;
+    uint64_t* s_full = empty + NST;
+    uint64_t* s_free = s_full + 2;
+    uint64_t* p_full = s_free + 2;
+    uint64_t* pv_done = p_full + 1;
+    uint64_t* fin = pv_done + 1;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::OFF_MISC);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + Cfg::OFF_MISC + 8);
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int split = blockIdx.x % a.splits, unit = blockIdx.x / a.splits;
+    const int kvh = unit % a.Hkv, lb = unit / a.Hkv, b = lb % a.B;
+    const int T = a.T, G = a.group;
+    const int n0 = __ldg(a.kv_len + b);
+    if (n0 < 0 || n0 > a.ctx - T) return;                 // reported by the append kernel
+    const int t0 = split * a.tiles_per_split;              // first 128-key tile of this CTA
+    const int ntiles = min(((n0 + T + 127) >> 7) - t0, a.tiles_per_split);
+    if (ntiles <= 0) {                                     // a split past the end: empty partial
+        if (tid < a.nq) {
+            float* ml = a.ws_ml + ((size_t(split) * a.units + unit) * a.nq + tid) * 2;
+            ml[0] = -INFINITY;
+            ml[1] = 0.f;
+        }
+        return;
+    }
+
+    if (tid == 0) {
+        for (int s = 0; s < NST; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(&s_full[0], 1);
+        mbar_init(&s_full[1], 1);
+        mbar_init(&s_free[0], 128);
+        mbar_init(&s_free[1], 128);
+        mbar_init(p_full, 128);
+        mbar_init(pv_done, 1);
+        mbar_init(fin, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 5) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(smem_u32(tslot)), "r"(uint32_t(Cfg::TM_COLS)));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    // query rows c = i·G + g (position i, head kvh·G + g) into the K-major swizzled B tile
+    {
+        const __nv_bfloat16* qh = a.q + (size_t(lb) * T * a.Hq + size_t(kvh) * G) * D;
+        for (int e = tid; e < NQ * (D / 8); e += Cfg::NTHR) {
+            const int c = e / (D / 8), j8 = e - c * (D / 8);
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (c < a.nq) {
+                const int i = c / G, g = c - i * G;
+                v = __ldg(reinterpret_cast<const uint4*>(qh + (size_t(i) * a.Hq + g) * D) + j8);
+            }
+            const int kb = j8 >> 3, ch = j8 & 7;
+            *reinterpret_cast<uint4*>(Qs + kb * Cfg::Q_KB + (c >> 3) * 1024 + (c & 7) * 128 +
+                                      ((ch ^ (c & 7)) << 4)) = v;
+        }
+        if (tid < NQ) {
+            m_run[tid] = -INFINITY;
+            lim[tid] = n0 + (tid < a.nq ? tid / G : T - 1);
+        }
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = *tslot;
+
+    if (warp == 4) {
+        // ---------------------------------------------------------------- TMA producer
+        if (lane == 0) {
+            const int krow0 = (lb * a.Hkv + kvh) * a.ctx;      // K map row of key 0
+            const int vrow0 = (lb * a.Hkv + kvh) * D;          // Vᵀ map row of d-row 0
+            int stage = 0, issued = 0;
+            uint32_t ph = 0;
+            bool ok = true;
+            auto load = [&](bool isv, int tile, int c) {
+                if (!ok) return;
+                if (!pwait(&empty[stage], ph ^ 1u, abort_flag, a.status)) {
+                    ok = false;
+                    return;
+                }
+                mbar_arrive_expect_tx(&full[stage], uint32_t(Cfg::CHUNK));
+                unsigned char* dst = ring + stage * Cfg::CHUNK;
+                const int key0 = (t0 + tile) * 128;
+                if (!isv) {
+                    tma_load_2d(dst, &kmap, c * 128, krow0 + key0, &full[stage]);
+                    tma_load_2d(dst + 16384, &kmap, c * 128 + 64, krow0 + key0, &full[stage]);
+                } else {
+                    tma_load_2d(dst, &vmap, key0, vrow0 + c * 128, &full[stage]);
+                    tma_load_2d(dst + 16384, &vmap, key0 + 64, vrow0 + c * 128, &full[stage]);
+                }
+                ++issued;
+                if (++stage == NST) {
+                    stage = 0;
+                    ph ^= 1u;
+                }
+            };
+            for (int c = 0; c < DCH; ++c) load(false, 0, c);
+            for (int j = 0; j < ntiles; ++j) {
+                if (j + 1 < ntiles)
+                    for (int c = 0; c < DCH; ++c) load(false, j + 1, c);
+                for (int c = 0; c < DCH; ++c) load(true, j, c);
+            }
+            // every copy issued lands before the CTA may exit
+            for (int s = 0; s < NST && s < issued; ++s) {
+                const int fills = (issued - s + NST - 1) / NST;
+                if (!mbar_wait_bounded(&full[s], uint32_t(fills - 1) & 1u))
+                    set_status(a.status, GDN_STATUS_WAIT_TIMEOUT);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 5) {
+        // ---------------------------------------------------------------- MMA issue
+        constexpr uint32_t IDESC = umma_idesc_bf16(128, NQ);
+        const uint32_t sQ = smem_u32(Qs), sP = smem_u32(Ps), sR = smem_u32(ring);
+        int stage = 0;
+        uint32_t ph = 0;
+        bool ok = true;
+        auto qk = [&](int j) {
+            const int buf = j & 1;
+            if (j >= 2 && !pwait_warp(&s_free[buf], uint32_t((j >> 1) - 1) & 1u, abort_flag, a.status)) {
+                ok = false;
+                return;
+            }
+            tc_fence_after();
+            for (int c = 0; c < DCH; ++c) {
+                if (!pwait_warp(&full[stage], ph, abort_flag, a.status)) {
+                    ok = false;
+                    return;
+                }
+                tc_fence_after();
+                const uint64_t da = umma_desc_sw128(sR + stage * Cfg::CHUNK);
+                const uint64_t db = umma_desc_sw128(sQ + 2 * c * Cfg::Q_KB);
+#pragma unroll
+                for (int kb = 0; kb < 2; ++kb)
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        umma_bf16_warp(tbase + Cfg::TM_S + buf * NQ,
+                                       da + uint64_t((kb * 16384 + ks * 32) >> 4),
+                                       db + uint64_t((kb * Cfg::Q_KB + ks * 32) >> 4), IDESC,
+                                       (c | kb | ks) ? 1u : 0u);
+                umma_commit_warp(&empty[stage]);
+                if (++stage == NST) {
+                    stage = 0;
+                    ph ^= 1u;
+                }
+            }
+            umma_commit_warp(&s_full[buf]);
+        };
+        auto pv = [&](int j) {
+            if (!pwait_warp(p_full, uint32_t(j) & 1u, abort_flag, a.status)) {
+                ok = false;
+                return;
+            }
+            tc_fence_after();
+            for (int c = 0; c < DCH; ++c) {
+                if (!pwait_warp(&full[stage], ph, abort_flag, a.status)) {
+                    ok = false;
+                    return;
+                }
+                tc_fence_after();
+                const uint64_t da = umma_desc_sw128(sR + stage * Cfg::CHUNK);
+                const uint64_t db = umma_desc_sw128(sP);
+#pragma unroll
+                for (int kb = 0; kb < 2; ++kb)
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        umma_bf16_warp(tbase + Cfg::TM_O + c * NQ,
+                                       da + uint64_t((kb * 16384 + ks * 32) >> 4),
+                                       db + uint64_t((kb * Cfg::P_KB + ks * 32) >> 4), IDESC,
+                                       (j > 0 || kb || ks) ? 1u : 0u);
+                umma_commit_warp(&empty[stage]);
+                if (++stage == NST) {
+                    stage = 0;
+                    ph ^= 1u;
+                }
+            }
+            umma_commit_warp(pv_done);
+        };
+        qk(0);
+        for (int j = 0; j < ntiles && ok; ++j) {
+            if (j + 1 < ntiles) qk(j + 1);
+            if (ok) pv(j);
+        }
+        umma_commit_warp(fin);          // arrives once every MMA issued above has completed
+    } else {
+        // ---------------------------------------------------------------- softmax (warps 0-3)
+        const uint32_t lane_off = uint32_t(warp * 32) << 16;
+        const float sl2 = a.sl2;
+        float l_acc = 0.f;              // thread c < NQ: running normaliser of row c
+        int done = 0;
+        for (int j = 0; j < ntiles; ++j) {
+            const int buf = j & 1;
+            const int key = (t0 + j) * 128 + tid;
+            const bool edge = (t0 + j) * 128 + 127 > n0;   // some row cannot see some key here
+            const bool got = pwait(&s_full[buf], uint32_t(j >> 1) & 1u, abort_flag, a.status);
+            if (named_bar_or(1, 128, !got)) break;
+            tc_fence_after();
+            const uint32_t tS = tbase + lane_off + Cfg::TM_S + buf * NQ;
+            // pass 1: column maxima of the tile
+#pragma unroll 1
+            for (int cb = 0; cb < NCB; ++cb) {
+                float s[32];
+                tmem_ld32(tS + cb * 32, s);
+#pragma unroll
+                for (int k = 0; k < 32; ++k) {
+                    const float x = s[k] * sl2;
+                    s[k] = (edge && key > lim[cb * 32 + k]) ? -INFINITY : x;
+                }
+                int col;
+                const float mx = warp_cols32<true>(s, lane, &col);
+                redA[warp * NQ + cb * 32 + col] = mx;
+            }
+            named_bar(1, 128);
+            bool resc = false;
+            if (tid < NQ) {
+                const float mt = fmaxf(fmaxf(redA[tid], redA[NQ + tid]),
+                                       fmaxf(redA[2 * NQ + tid], redA[3 * NQ + tid]));
+                const float mo = m_run[tid];
+                float al = 1.f;
+                if (mt > mo + 8.f) {            // never for mt = -inf (nothing visible yet)
+                    al = (mo == -INFINITY) ? 0.f : ex2(mo - mt);
+                    m_run[tid] = mt;
+                    resc = true;
+                }
+                alpha[tid] = al;
+                l_acc *= al;
+            }
+            resc = named_bar_or(1, 128, resc);
+            if (j > 0) {
+                // the previous tile's P·V is done before P is rewritten and Oᵀ rescaled
+                const bool g2 = pwait(pv_done, uint32_t(j - 1) & 1u, abort_flag, a.status);
+                if (named_bar_or(1, 128, !g2)) break;
+                tc_fence_after();
+                if (resc) {
+#pragma unroll 1
+                    for (int q = 0; q < DCH * NCB; ++q) {
+                        const int c2 = q / NCB, cb = q - c2 * NCB;
+                        const uint32_t tO = tbase + lane_off + Cfg::TM_O + c2 * NQ + cb * 32;
+                        float o[32];
+                        tmem_ld32(tO, o);
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) o[k] *= alpha[cb * 32 + k];
+                        tmem_st32(tO, o);
+                    }
+                    tmem_wait_st();
+                }
+            }
+            // pass 2: weights 2^(s - m) as bf16 into the P tile (row c, key tid), and their sums
+#pragma unroll 1
+            for (int cb = 0; cb < NCB; ++cb) {
+                float s[32];
+                tmem_ld32(tS + cb * 32, s);
+#pragma unroll
+                for (int k = 0; k < 32; ++k) {
+                    const int c = cb * 32 + k;
+                    const float m = m_run[c];
+                    float e = ex2(s[k] * sl2 - (m == -INFINITY ? 0.f : m));
+                    e = (edge && key > lim[c]) ? 0.f : e;
+                    const __nv_bfloat16 pb = __float2bfloat16_rn(e);
+                    s[k] = __bfloat162float(pb);
+                    *reinterpret_cast<__nv_bfloat16*>(
+                        Ps + (tid >> 6) * Cfg::P_KB + (c >> 3) * 1024 + (c & 7) * 128 +
+                        ((((tid & 63) >> 3) ^ (c & 7)) << 4) + (tid & 7) * 2) = pb;
+                }
+                int col;
+                const float sm = warp_cols32<false>(s, lane, &col);
+                redB[warp * NQ + cb * 32 + col] = sm;
+            }
+            tc_fence_before();
+            mbar_arrive(&s_free[buf]);          // Sᵀ(j) is in registers no more
+            fence_async_smem();                 // P visible to the tensor core
+            mbar_arrive(p_full);
+            named_bar(1, 128);
+            if (tid < NQ)
+                l_acc += (redB[tid] + redB[NQ + tid]) + (redB[2 * NQ + tid] + redB[3 * NQ + tid]);
+            done = j + 1;
+        }
+        // ---------------------------------------------------------------- epilogue
+        const bool okf = done == ntiles &&
+                         pwait(pv_done, uint32_t(ntiles - 1) & 1u, abort_flag, a.status);
+        if (tid < NQ) lfin[tid] = l_acc;
+        const bool bad = named_bar_or(1, 128, !okf);
+        tc_fence_after();
+        if (!bad) {
+            const size_t ws_row = (size_t(split) * a.units + unit) * a.nq;
+#pragma unroll 1
+            for (int q = 0; q < DCH * NCB; ++q) {
+                const int c2 = q / NCB, cb = q - c2 * NCB;
+                float o[32];
+                tmem_ld32(tbase + lane_off + Cfg::TM_O + c2 * NQ + cb * 32, o);
+                const int d = c2 * 128 + tid;
+#pragma unroll
+                for (int k = 0; k < 32; ++k) {
+                    const int c = cb * 32 + k;
+                    if (c < a.nq) {
+                        if (a.splits == 1) {
+                            const int i = c / G, g = c - i * G;
+                            a.out[((size_t(lb) * T + i) * a.Hq + kvh * G + g) * D + d] =
+                                __float2bfloat16_rn(o[k] / lfin[c]);
+                        } else {
+                            a.ws_o[(ws_row + c) * D + d] = o[k];
+                        }
+                    }
+                }
+            }
+            if (a.splits > 1 && tid < a.nq) {
+                float* ml = a.ws_ml + (ws_row + tid) * 2;
+                ml[0] = m_run[tid];
+                ml[1] = l_acc;
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 5) {
+        tc_fence_after();
+        if (!mbar_wait_bounded(fin, 0)) set_status(a.status, GDN_STATUS_WAIT_TIMEOUT);
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;"
+                     ::"r"(tbase), "r"(uint32_t(Cfg::TM_COLS)));
+    }
+}
+
+// ------------------------------------------------------------------ split merge
+__global__ void __launch_bounds__(256) attn_combine_kernel(const AttnArgs a) {
+    const int unit = blockIdx.x, c = blockIdx.y, d = threadIdx.x;
+    const int kvh = unit % a.Hkv, lb = unit / a.Hkv, b = lb % a.B;
+    const int n0 = __ldg(a.kv_len + b);
+    if (n0 < 0 || n0 > a.ctx - a.T) return;
+    float mstar = -INFINITY;
+    for (int s = 0; s < a.splits; ++s) {
+        const float* ml = a.ws_ml + ((size_t(s) * a.units + unit) * a.nq + c) * 2;
+        if (ml[1] > 0.f) mstar = fmaxf(mstar, ml[0]);
+    }
+    float num = 0.f, den = 0.f;
+    for (int s = 0; s < a.splits; ++s) {
+        const size_t row = (size_t(s) * a.units + unit) * a.nq + c;
+        const float* ml = a.ws_ml + row * 2;
+        if (ml[1] > 0.f) {
+            const float w = ex2(ml[0] - mstar);
+            num = fmaf(w, a.ws_o[row * a.D + d], num);
+            den = fmaf(w, ml[1], den);
+        }
+    }
+    const int i = c / a.group, g = c - i * a.group;
+    a.out[((size_t(lb) * a.T + i) * a.Hq + kvh * a.group + g) * a.D + d] = __float2bfloat16_rn(num / den);
+}
+
+// ------------------------------------------------------------------ truncation
+__global__ void attn_truncate_kernel(int B, int T, const int32_t* n_acc, int32_t* kv_len,
+                                     uint32_t* status) {
+    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= B) return;
+    const int n = n_acc[b];
+    if (n < 0 || n > T) {
+        set_status(status, GDN_STATUS_BAD_NACC);
+        return;
+    }
+    kv_len[b] += n;
+}
+
+template <int D, int NQ>
+static cudaError_t launch_attn_t(const AttnArgs& a, const CUtensorMap& kmap,
+                                 const CUtensorMap& vmap, cudaStream_t s) {
+    using Cfg = AttnCfg<D, NQ>;
+    auto kern = attn_verify_kernel<D, NQ>;
+    static bool attr_done = false;   // benign race: setting the attribute twice is harmless
+    if (!attr_done) {
+        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   int(Cfg::SMEM));
+        if (e != cudaSuccess) return e;
+        attr_done = true;
+    }
+    kern<<<unsigned(a.units) * unsigned(a.splits), Cfg::NTHR, Cfg::SMEM, s>>>(a, kmap, vmap);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_attn_verify(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                               cudaStream_t s) {
+    attn_append_kernel<<<dim3(a.B, a.L), 256, 0, s>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const int nqp = a.nq <= 32 ? 32 : a.nq <= 64 ? 64 : 128;
+    if (a.D == 128)
+        e = nqp == 32 ? launch_attn_t<128, 32>(a, kmap, vmap, s)
+          : nqp == 64 ? launch_attn_t<128, 64>(a, kmap, vmap, s)
+                      : launch_attn_t<128, 128>(a, kmap, vmap, s);
+    else
+        e = nqp == 32 ? launch_attn_t<256, 32>(a, kmap, vmap, s)
+          : nqp == 64 ? launch_attn_t<256, 64>(a, kmap, vmap, s)
+                      : launch_attn_t<256, 128>(a, kmap, vmap, s);
+    if (e != cudaSuccess || a.splits == 1) return e;
+    attn_combine_kernel<<<dim3(a.units, a.nq), a.D, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_attn_truncate(int B, int T, const int32_t* n_acc, int32_t* kv_len,
+                                 uint32_t* status, cudaStream_t s) {
+    attn_truncate_kernel<<<(B + 255) / 256, 256, 0, s>>>(B, T, n_acc, kv_len, status);
+    return cudaGetLastError();
+}
+
+}  // namespace gdn

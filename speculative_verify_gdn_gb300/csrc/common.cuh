@@ -11,9 +11,6 @@
 #error "gdnspec kernels are written for Blackwell (sm_103a)"
 #endif
 
-// Status bit for a bounded wait that gave up (not part of the public header on purpose: it can
-// only be raised if a bulk copy never lands, which would be a driver or hardware fault).
-#define GDN_STATUS_WAIT_TIMEOUT 0x20u
 
 namespace gdn {
 

@@ -161,41 +161,6 @@ struct PipeCfg {
     static_assert(GRAM_TILES == 1 || GRAM_TILES % 4 == 0, "Gram block: one tile, or a quarter per prep warp");
 };
 
-__device__ __forceinline__ void named_bar(int id, int nthreads) {
-    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
-}
-
-// bounded wait that gives up for good once any wait in the CTA has timed out
-__device__ __forceinline__ bool pwait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                      uint32_t* status) {
-    if (*abort_flag) return false;
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    while (true) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if (*abort_flag) return false;
-        if (globaltimer_ns() - t0 > 1000000000ull) {
-            set_status(status, GDN_STATUS_WAIT_TIMEOUT);
-            *abort_flag = 1;
-            return false;
-        }
-    }
-}
-
-// pwait by lane 0, result broadcast: every lane of the warp takes the same branch
-__device__ __forceinline__ bool pwait_warp(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                           uint32_t* status) {
-    int ok = 0;
-    if ((threadIdx.x & 31) == 0) ok = pwait(bar, parity, abort_flag, status) ? 1 : 0;
-    ok = __shfl_sync(0xffffffffu, ok, 0);
-    __syncwarp();
-    return ok != 0;
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
 // D[tmem] (+)= A[tmem] · B[smem descriptor]ᵀ, kind::tf32. Called by a whole converged warp with
 // warp-uniform operands; one elected lane issues. (Issue from a lone diverged lane costs about three
 // times as many cycles per MMA as the tensor core needs for these small shapes.)
@@ -206,13 +171,6 @@ __device__ __forceinline__ void umma_tf32_ts_warp(uint32_t dtmem, uint32_t atmem
         "@e tcgen05.mma.cta_group::1.kind::tf32 [%0], [%1], %2, %3, p;\n\t}"
         ::"r"(dtmem), "r"(atmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
-}
-
-__device__ __forceinline__ void umma_commit_warp(uint64_t* bar) {
-    asm volatile(
-        "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
-        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}"
-        ::"r"(smem_u32(bar)) : "memory");
 }
 
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
@@ -243,12 +201,6 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
           "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]),
           "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
         : "memory");
-}
-
-__device__ __forceinline__ bool elect_one() {
-    uint32_t e;
-    asm volatile("{\n\t.reg .pred p;\n\telect.sync _|p, 0xffffffff;\n\tselp.u32 %0, 1, 0, p;\n\t}" : "=r"(e));
-    return e != 0;
 }
 
 // warp-level D(16x8) += A(16x8) · B(8x8), TF32 operands (already truncated), fp32 accumulate

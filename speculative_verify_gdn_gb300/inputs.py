@@ -79,7 +79,8 @@ def custom(base: Workload, **kw) -> Workload:
 
 
 _TAGS = {"conv_w": 1, "state": 2, "conv_state": 3, "qkv": 4, "g": 5, "beta": 6, "logits": 7,
-         "drafts": 8, "lengths": 9, "tree": 10, "tokens": 11, "prev_delta": 12, "prev_k": 13}
+         "drafts": 8, "lengths": 9, "tree": 10, "tokens": 11, "prev_delta": 12, "prev_k": 13,
+         "attn_q": 14, "attn_k": 15, "attn_v": 16, "attn_kc": 17, "attn_vc": 18}
 
 # round index of the synthetic previous round (no round loop reaches it)
 PREV_ROUND = 0x7FFFFFFF
@@ -283,3 +284,67 @@ def tree_tokens_and_logits(w: Workload, parent, round_, seed=0):
                 break
             lg[b, row, am] = (lg[b, row].float().min() - 1.0).to(ldt)
     return torch.from_numpy(tokens.astype(np.int32)), lg.contiguous(), torch.from_numpy(Ls)
+
+
+# ------------------------------------------------------------------ attention layers
+@dataclass(frozen=True)
+class AttnWorkload:
+    """The hybrid's full-attention layers in one verify step: L layers, B sequences with
+    `lengths[b % len]` committed cache rows, T verify positions, Hq query heads over Hkv kv heads
+    of dim D, cache capacity ctx rows."""
+    name: str
+    L: int
+    B: int
+    T: int
+    Hq: int
+    Hkv: int
+    D: int
+    ctx: int
+    lengths: tuple
+    notes: str = field(default="", compare=False)
+
+
+# Qwen3.6-35B-A3B-shaped attention layers (10 of its 40 layers; 16 query heads over 2 kv heads of
+# dim 256) over a 4096-token context, at the GDN workloads' batch and draft count.
+ATTN_WORKLOADS = {
+    "qwen36_attn_b64_n8": AttnWorkload("qwen36_attn_b64_n8", L=10, B=64, T=8, Hq=16, Hkv=2,
+                                       D=256, ctx=4160, lengths=(4096,)),
+    "qwen36_attn_b1_n8": AttnWorkload("qwen36_attn_b1_n8", L=10, B=1, T=8, Hq=16, Hkv=2, D=256,
+                                      ctx=4160, lengths=(4096,)),
+}
+
+
+def _awid(w):
+    return 0x200 + (zlib.crc32(w.name.encode()) & 0xFFFFFF)
+
+
+def attn_lengths(w: AttnWorkload):
+    """Committed cache rows per sequence, int32 [B]."""
+    return torch.tensor([w.lengths[b % len(w.lengths)] for b in range(w.B)], dtype=torch.int32)
+
+
+def attn_round(w: AttnWorkload, round_, seed=0, device="cpu"):
+    """One verify step's projected q [L, B, T, Hq, D] and new k, v [L, B, T, Hkv, D], bf16,
+    every element N(0, 1)."""
+    wid = _awid(w)
+    out = []
+    for tag, h in (("attn_q", w.Hq), ("attn_k", w.Hkv), ("attn_v", w.Hkv)):
+        t = torch.randn((w.L, w.B, w.T, h, w.D), generator=generator(seed, wid, round_, tag, device),
+                        device=device)
+        out.append(t.to(torch.bfloat16))
+    return tuple(out)
+
+
+def attn_cache(w: AttnWorkload, seed=0, device="cpu"):
+    """(k_cache, v_cache) [L, B, Hkv, ctx, D] bf16, token-major: rows below each sequence's
+    committed length ~ N(0, 1), the rest zero (allocated zeroed, as a cache is)."""
+    wid = _awid(w)
+    kc = torch.randn((w.L, w.B, w.Hkv, w.ctx, w.D), generator=generator(seed, wid, 0, "attn_kc", device),
+                     device=device).to(torch.bfloat16)
+    vc = torch.randn((w.L, w.B, w.Hkv, w.ctx, w.D), generator=generator(seed, wid, 0, "attn_vc", device),
+                     device=device).to(torch.bfloat16)
+    n = attn_lengths(w).to(device)
+    keep = (torch.arange(w.ctx, device=device)[None, :] < n[:, None].long())   # [B, ctx]
+    m = keep[None, :, None, :, None]
+    return kc * m, vc * m
+

@@ -133,7 +133,8 @@ def test_struct_layouts_match_the_header(tmp_path):
     if cc is None:
         pytest.skip("no C compiler")
     fields = {"gdn_dims": [f for f, _ in _lib._Dims._fields_],
-              "spec_dims": [f for f, _ in _lib._SpecDims._fields_]}
+              "spec_dims": [f for f, _ in _lib._SpecDims._fields_],
+              "attn_dims": [f for f, _ in _lib._AttnDims._fields_]}
     lines = ['#include <stddef.h>', '#include <stdio.h>', '#include "gdnspec.h"', "int main(void) {"]
     for st, fs in fields.items():
         lines.append('printf("%s %%zu\\n", sizeof(%s));' % (st, st))
@@ -147,7 +148,8 @@ def test_struct_layouts_match_the_header(tmp_path):
                    check=True)
     got = dict(l.split() for l in subprocess.run([str(exe)], check=True, capture_output=True,
                                                   text=True).stdout.splitlines())
-    for st, cls in (("gdn_dims", _lib._Dims), ("spec_dims", _lib._SpecDims)):
+    for st, cls in (("gdn_dims", _lib._Dims), ("spec_dims", _lib._SpecDims),
+                    ("attn_dims", _lib._AttnDims)):
         assert int(got[st]) == ct.sizeof(cls), st
         for f in fields[st]:
             assert int(got["%s.%s" % (st, f)]) == getattr(cls, f).offset, (st, f)
@@ -165,3 +167,31 @@ def test_gate_dk_host_checks(lib):
     assert "gate" in _lib.last_error()
     d.gate_dk = 2
     assert call_verify(lib, d, [fake] * 9) == 1 and "gate_dk" in _lib.last_error()
+
+
+def test_attn_host_checks(lib):
+    """attn_verify / attn_truncate argument checks and the workspace size, with no device."""
+    fake = ct.c_void_p(0x100000)
+    sh = _lib.AttnShape(L=10, B=64, T=8, Hq=16, Hkv=2, D=256, ctx=4160)
+    d = sh.c()
+    call = lambda dd, ptrs, ws=None, nws=0: lib.attn_verify(ct.byref(dd), *ptrs, ws, nws, None,
+                                                            None)
+    assert call(d, [None] * 7) == 1 and "NULL" in _lib.last_error()
+    assert lib.attn_workspace_bytes(ct.byref(d)) == 0          # 1280 units: no key split
+    small = _lib.AttnShape(L=1, B=1, T=8, Hq=16, Hkv=2, D=256, ctx=4160)
+    assert _lib.attn_workspace_bytes(small) > 0
+    # the split case needs its workspace
+    assert call(small.c(), [fake] * 7) == 1 and "workspace" in _lib.last_error()
+    for bad, code in ((dict(D=64), 2), (dict(T=17), 2), (dict(ctx=100), 2), (dict(ctx=4100), 2),
+                      (dict(Hq=15), 1), (dict(Hkv=0), 1)):
+        kw = dict(sh.__dict__)
+        kw.update(bad)
+        assert call(_lib.AttnShape(**kw).c(), [fake] * 7) == code, bad
+    mis = [fake] * 7
+    mis[3] = ct.c_void_p(0x100008)            # k_cache not 16-byte aligned
+    assert call(d, mis) == 1 and "aligned" in _lib.last_error()
+    assert call(_lib.AttnShape(L=10, B=0, T=8, Hq=16, Hkv=2, D=256, ctx=4160).c(),
+                [None] * 7) == 0
+    assert lib.attn_truncate(4, 8, None, None, None, None) == 1
+    assert lib.attn_truncate(0, 8, None, None, None, None) == 0
+
