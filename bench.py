@@ -625,6 +625,9 @@ def run_attn(args):
     import torch
     from speculative_verify_gdn_gb300 import _lib, build as lib_build, inputs as I
     w = I.ATTN_WORKLOADS[args.attn]
+    if args.batch is not None or args.layers is not None:
+        import dataclasses
+        w = dataclasses.replace(w, B=args.batch or w.B, L=args.layers or w.L)
     device = torch.device("cuda", 0)
     torch.cuda.set_device(device)
     lib_build.build()

@@ -16,12 +16,16 @@
 //         Oᵀ[d][row]   += Vᵀ_tile · Pᵀ      tcgen05, M = 128 d-rows per chunk, N = NQ, K = 128 keys
 //     Sᵀ is double-buffered in TMEM (the next tile's product overlaps this tile's softmax) and
 //     Oᵀ accumulates in TMEM across the tiles.
-//   * Softmax: 4 warps, thread = key = TMEM lane. Column maxima by a transposing warp reduction
-//     (31 shuffles per 32 columns) plus a 4-way shared-memory step. The running maximum moves only
-//     when a tile's maximum exceeds it by more than 8 (log2 units), so Oᵀ is rescaled rarely and
-//     the weights stay ≤ 2^8. P is rounded to bf16 for the tensor core; the normaliser sums the
-//     rounded values, so numerator and denominator use the same weights.
-//   * Warp roles: 0-3 softmax + epilogue, 4 TMA producer, 5 MMA issue + TMEM owner. The ring
+//   * Softmax: one warp per (TMEM lane quarter, 32 query columns), thread = key = TMEM lane. The
+//     running maximum of a column moves only when a tile holds a score more than 8 (log2 units)
+//     above it, so in the common case a tile costs each thread one compare per score and one
+//     barrier; otherwise the tile maxima are reduced (a transposing warp reduction, 31 shuffles per
+//     32 columns, plus a 4-way shared-memory step) and Oᵀ and the partial sums are rescaled. The
+//     weights stay ≤ 2^8; P is rounded to bf16 for the tensor core (double-buffered, so the
+//     softmax of tile j overlaps P·V of tile j-1) and each thread sums its rounded weights,
+//     reduced once at the end, so numerator and denominator use the same weights.
+//   * Warp roles: softmax + epilogue, then one TMA producer warp, then one MMA issue + TMEM owner
+//     warp. The ring
 //     holds 32 KiB chunks (128 keys × 128 of the head dim, or 128 d-rows × 128 keys) in the order
 //     the tensor core consumes them: K(0), K(1), V(0), K(2), V(1), …
 //   * Short batches over long caches split the keys across CTAs (flash-decoding); a combine
@@ -36,21 +40,31 @@ namespace gdn {
 
 template <int D, int NQ>
 struct AttnCfg {
-    static constexpr int NTHR = 192;
+    // softmax warps: one per (TMEM lane quarter, 32 query columns), so every SM sub-partition
+    // interleaves NQ / 32 of them
+    static constexpr int NSW = 4 * (NQ / 32);
+    static constexpr int SMT = 32 * NSW;                // softmax threads
+    static constexpr int CW = 32;                       // columns per softmax warp
+    static constexpr int PRODUCER = NSW, MMAW = NSW + 1;
+    static constexpr int NTHR = 32 * (NSW + 2);
     static constexpr int DCH = D / 128;                 // 128-wide chunks of the head dim
     static constexpr int CHUNK = 128 * 128 * 2;         // one ring stage: two 64-wide swizzled blocks
-    static constexpr int NST = NQ >= 128 ? 3 : 4;       // ring stages
     static constexpr int Q_KB = NQ * 128;               // bytes of one 64-element K-block of Q
     static constexpr int Q_BYTES = (D / 64) * Q_KB;
     static constexpr int P_KB = NQ * 128;               // bytes of one 64-key K-block of P
-    static constexpr int P_BYTES = 2 * P_KB;
+    static constexpr int P_BYTES = 2 * P_KB;            // one P tile (two buffers are kept)
+    // ring stages: as many as the shared memory left over holds (at most 6)
+    static constexpr int FIXED = Q_BYTES + 2 * P_BYTES + 12 * NQ * 4 + 21 * 8 + 16 + 1024 + 64;
+    static constexpr int NST_FIT = (227 * 1024 - FIXED) / CHUNK;
+    static constexpr int NST = NST_FIT > 6 ? 6 : NST_FIT;
     static constexpr size_t OFF_RING = 0;
     static constexpr size_t OFF_Q = OFF_RING + size_t(NST) * CHUNK;
     static constexpr size_t OFF_P = OFF_Q + Q_BYTES;
-    static constexpr size_t OFF_F = OFF_P + P_BYTES;    // redA[4][NQ] redB[4][NQ] m, alpha, l [NQ]
+    static constexpr size_t OFF_F = OFF_P + 2 * P_BYTES;  // redA[4][NQ] redB[4][NQ] m, alpha, l [NQ]
     static constexpr size_t OFF_LIM = OFF_F + size_t(11) * NQ * 4;   // int lim[NQ]
-    // barriers: full[NST] empty[NST] s_full[2] s_free[2] p_full pv_done fin
-    static constexpr int NBAR = 2 * NST + 7;
+    // barriers: full[NST] empty[NST] s_full[2] s_free[2] p_full[2] pv_done[2] fin (one barrier per
+    // buffer, so no waiter is ever two phases behind)
+    static constexpr int NBAR = 2 * NST + 9;
     static constexpr size_t OFF_BAR = (OFF_LIM + size_t(NQ) * 4 + 7) / 8 * 8;
     static constexpr size_t OFF_MISC = OFF_BAR + size_t(NBAR) * 8;   // abort flag, TMEM slot
     static constexpr size_t SMEM = OFF_MISC + 16 + 1024;             // + base alignment slack
@@ -64,6 +78,7 @@ struct AttnCfg {
     static_assert(TM_USED <= 512, "TMEM columns");
     static_assert(OFF_Q % 1024 == 0 && OFF_P % 1024 == 0 && Q_KB % 1024 == 0, "swizzle atoms");
     static_assert(SMEM <= 227 * 1024, "shared memory");
+    static_assert(NST >= 2, "ring stages");
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -72,13 +87,17 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
-// Reduce 32 per-lane values over the warp, column by column: after recursive halving (31
-// shuffles) this lane holds the total of column *col (max or sum).
-template <bool MAX>
-__device__ __forceinline__ float warp_cols32(float (&v)[32], int lane, int* col) {
+// Reduce V ≤ 32 per-lane values over the warp, column by column: recursive halving (V - 1
+// shuffles) leaves each group of 32 / V lanes with one column, and log2(32 / V) more shuffles
+// combine the group. Returns the total of column *col (max or sum); lanes of a group agree.
+template <int V, bool MAX>
+__device__ __forceinline__ float warp_cols(const float* v0, int lane, int* col) {
+    float v[V];
+#pragma unroll
+    for (int k = 0; k < V; ++k) v[k] = v0[k];
     int base = 0;
 #pragma unroll
-    for (int m = 32, o = 16; m > 1; m >>= 1, o >>= 1) {
+    for (int m = V, o = 16; m > 1; m >>= 1, o >>= 1) {
         const bool up = (lane & o) != 0;
 #pragma unroll
         for (int k = 0; k < m / 2; ++k) {
@@ -89,8 +108,14 @@ __device__ __forceinline__ float warp_cols32(float (&v)[32], int lane, int* col)
         }
         base += up ? m / 2 : 0;
     }
+    float r = v[0];
+#pragma unroll
+    for (int o = 16 / V; o > 0; o >>= 1) {
+        const float got = __shfl_xor_sync(0xffffffffu, r, o);
+        r = MAX ? fmaxf(r, got) : r + got;
+    }
     *col = base;
-    return v[0];
+    return r;
 }
 
 // ------------------------------------------------------------------ append the new rows
@@ -119,11 +144,11 @@ __global__ void __launch_bounds__(256) attn_append_kernel(const AttnArgs a) {
 
 // ------------------------------------------------------------------ attention
 template <int D, int NQ>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(AttnCfg<D, NQ>::NTHR, 1)
 attn_verify_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap,
                    const __grid_constant__ CUtensorMap vmap) {
     using Cfg = AttnCfg<D, NQ>;
-    constexpr int NST = Cfg::NST, DCH = Cfg::DCH, NCB = NQ / 32;
+    constexpr int NST = Cfg::NST, DCH = Cfg::DCH, SMT = Cfg::SMT;
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     unsigned char* ring = smem + Cfg::OFF_RING;
@@ -140,8 +165,8 @@ attn_verify_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap,
     uint64_t* s_full = empty + NST;
     uint64_t* s_free = s_full + 2;
     uint64_t* p_full = s_free + 2;
-    uint64_t* pv_done = p_full + 1;
-    uint64_t* fin = pv_done + 1;
+    uint64_t* pv_done = p_full + 2;
+    uint64_t* fin = pv_done + 2;
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::OFF_MISC);
     uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + Cfg::OFF_MISC + 8);
 
@@ -169,15 +194,17 @@ attn_verify_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap,
         }
         mbar_init(&s_full[0], 1);
         mbar_init(&s_full[1], 1);
-        mbar_init(&s_free[0], 128);
-        mbar_init(&s_free[1], 128);
-        mbar_init(p_full, 128);
-        mbar_init(pv_done, 1);
+        mbar_init(&s_free[0], SMT);
+        mbar_init(&s_free[1], SMT);
+        mbar_init(&p_full[0], SMT);
+        mbar_init(&p_full[1], SMT);
+        mbar_init(&pv_done[0], 1);
+        mbar_init(&pv_done[1], 1);
         mbar_init(fin, 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 5) {
+    if (warp == Cfg::MMAW) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
                      ::"r"(smem_u32(tslot)), "r"(uint32_t(Cfg::TM_COLS)));
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
@@ -207,7 +234,7 @@ attn_verify_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap,
     tc_fence_after();
     const uint32_t tbase = *tslot;
 
-    if (warp == 4) {
+    if (warp == Cfg::PRODUCER) {
         // ---------------------------------------------------------------- TMA producer
         if (lane == 0) {
             const int krow0 = (lb * a.Hkv + kvh) * a.ctx;      // K map row of key 0
@@ -251,7 +278,7 @@ attn_verify_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap,
             }
         }
         __syncwarp();
-    } else if (warp == 5) {
+    } else if (warp == Cfg::MMAW) {
         // ---------------------------------------------------------------- MMA issue
         constexpr uint32_t IDESC = umma_idesc_bf16(128, NQ);
         const uint32_t sQ = smem_u32(Qs), sP = smem_u32(Ps), sR = smem_u32(ring);
@@ -290,7 +317,8 @@ attn_verify_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap,
             umma_commit_warp(&s_full[buf]);
         };
         auto pv = [&](int j) {
-            if (!pwait_warp(p_full, uint32_t(j) & 1u, abort_flag, a.status)) {
+            const int buf = j & 1;
+            if (!pwait_warp(&p_full[buf], uint32_t(j >> 1) & 1u, abort_flag, a.status)) {
                 ok = false;
                 return;
             }
@@ -302,7 +330,7 @@ attn_verify_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap,
                 }
                 tc_fence_after();
                 const uint64_t da = umma_desc_sw128(sR + stage * Cfg::CHUNK);
-                const uint64_t db = umma_desc_sw128(sP);
+                const uint64_t db = umma_desc_sw128(sP + buf * Cfg::P_BYTES);
 #pragma unroll
                 for (int kb = 0; kb < 2; ++kb)
 #pragma unroll
@@ -317,7 +345,7 @@ attn_verify_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap,
                     ph ^= 1u;
                 }
             }
-            umma_commit_warp(pv_done);
+            umma_commit_warp(&pv_done[buf]);
         };
         qk(0);
         for (int j = 0; j < ntiles && ok; ++j) {
@@ -326,115 +354,147 @@ attn_verify_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap,
         }
         umma_commit_warp(fin);          // arrives once every MMA issued above has completed
     } else {
-        // ---------------------------------------------------------------- softmax (warps 0-3)
-        const uint32_t lane_off = uint32_t(warp * 32) << 16;
+        // ---------------------------------------------------------------- softmax warps
+        // warp = (32 query columns from col0, TMEM lane quarter q4); row = key of the tile and
+        // d-row of Oᵀ. Per tile the common case is one barrier: each thread checks its scores
+        // against the running maxima + 8; only if some score is above (or a wait failed) do the
+        // warps reduce the tile maxima, move the maxima and rescale Oᵀ and the partial sums.
+        const int q4 = warp & 3, col0 = (warp >> 2) * 32, row = q4 * 32 + lane;
+        const uint32_t lane_off = uint32_t(q4 * 32) << 16;
         const float sl2 = a.sl2;
-        float l_acc = 0.f;              // thread c < NQ: running normaliser of row c
-        int done = 0;
+        float lsum[32];                 // partial normaliser of column col0 + k over this key lane
+#pragma unroll
+        for (int k = 0; k < 32; ++k) lsum[k] = 0.f;
+        bool ok = true;
         for (int j = 0; j < ntiles; ++j) {
             const int buf = j & 1;
-            const int key = (t0 + j) * 128 + tid;
+            const int key = (t0 + j) * 128 + row;
             const bool edge = (t0 + j) * 128 + 127 > n0;   // some row cannot see some key here
-            const bool got = pwait(&s_full[buf], uint32_t(j >> 1) & 1u, abort_flag, a.status);
-            if (named_bar_or(1, 128, !got)) break;
+            ok = pwait(&s_full[buf], uint32_t(j >> 1) & 1u, abort_flag, a.status) && ok;
             tc_fence_after();
-            const uint32_t tS = tbase + lane_off + Cfg::TM_S + buf * NQ;
-            // pass 1: column maxima of the tile
-#pragma unroll 1
-            for (int cb = 0; cb < NCB; ++cb) {
-                float s[32];
-                tmem_ld32(tS + cb * 32, s);
+            const uint32_t tS = tbase + lane_off + Cfg::TM_S + buf * NQ + col0;
+            uint32_t vis = 0xffffffffu;         // bit k: column col0 + k may see this key
+            if (edge) {
 #pragma unroll
-                for (int k = 0; k < 32; ++k) {
-                    const float x = s[k] * sl2;
-                    s[k] = (edge && key > lim[cb * 32 + k]) ? -INFINITY : x;
-                }
-                int col;
-                const float mx = warp_cols32<true>(s, lane, &col);
-                redA[warp * NQ + cb * 32 + col] = mx;
+                for (int k = 0; k < 32; ++k) vis &= ~(uint32_t(key > lim[col0 + k]) << k);
             }
-            named_bar(1, 128);
-            bool resc = false;
-            if (tid < NQ) {
-                const float mt = fmaxf(fmaxf(redA[tid], redA[NQ + tid]),
-                                       fmaxf(redA[2 * NQ + tid], redA[3 * NQ + tid]));
-                const float mo = m_run[tid];
-                float al = 1.f;
-                if (mt > mo + 8.f) {            // never for mt = -inf (nothing visible yet)
-                    al = (mo == -INFINITY) ? 0.f : ex2(mo - mt);
-                    m_run[tid] = mt;
-                    resc = true;
-                }
-                alpha[tid] = al;
-                l_acc *= al;
-            }
-            resc = named_bar_or(1, 128, resc);
-            if (j > 0) {
-                // the previous tile's P·V is done before P is rewritten and Oᵀ rescaled
-                const bool g2 = pwait(pv_done, uint32_t(j - 1) & 1u, abort_flag, a.status);
-                if (named_bar_or(1, 128, !g2)) break;
-                tc_fence_after();
-                if (resc) {
-#pragma unroll 1
-                    for (int q = 0; q < DCH * NCB; ++q) {
-                        const int c2 = q / NCB, cb = q - c2 * NCB;
-                        const uint32_t tO = tbase + lane_off + Cfg::TM_O + c2 * NQ + cb * 32;
-                        float o[32];
-                        tmem_ld32(tO, o);
+            float s[32];
+            tmem_ld32(tS, s);
+            bool over = false;
 #pragma unroll
-                        for (int k = 0; k < 32; ++k) o[k] *= alpha[cb * 32 + k];
-                        tmem_st32(tO, o);
+            for (int k4 = 0; k4 < 8; ++k4) {
+                const float4 m4 = *reinterpret_cast<const float4*>(m_run + col0 + 4 * k4);
+                const float mk[4] = {m4.x, m4.y, m4.z, m4.w};
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int k = 4 * k4 + u;
+                    s[k] *= sl2;
+                    over |= ((vis >> k) & 1u) && s[k] > mk[u] + 8.f;
+                }
+            }
+            if (named_bar_or(1, SMT, over || !ok)) {
+                // slow path: tile maxima of every column, new running maxima, rescale
+#pragma unroll
+                for (int k = 0; k < 32; ++k) s[k] = ((vis >> k) & 1u) ? s[k] : -INFINITY;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    int col;
+                    const float mx = warp_cols<16, true>(s + 16 * h, lane, &col);
+                    redA[q4 * NQ + col0 + 16 * h + col] = mx;
+                }
+                named_bar(1, SMT);
+                bool resc = false;
+                if (tid < NQ) {
+                    const float mt = fmaxf(fmaxf(redA[tid], redA[NQ + tid]),
+                                           fmaxf(redA[2 * NQ + tid], redA[3 * NQ + tid]));
+                    const float mo = m_run[tid];
+                    float al = 1.f;
+                    if (mt > mo + 8.f) {        // never for mt = -inf (nothing visible yet)
+                        al = (mo == -INFINITY) ? 0.f : ex2(mo - mt);
+                        m_run[tid] = mt;
+                        resc = true;
                     }
-                    tmem_wait_st();
+                    alpha[tid] = al;
                 }
-            }
-            // pass 2: weights 2^(s - m) as bf16 into the P tile (row c, key tid), and their sums
-#pragma unroll 1
-            for (int cb = 0; cb < NCB; ++cb) {
-                float s[32];
-                tmem_ld32(tS + cb * 32, s);
+                if (named_bar_or(1, SMT, resc)) {
 #pragma unroll
-                for (int k = 0; k < 32; ++k) {
-                    const int c = cb * 32 + k;
-                    const float m = m_run[c];
-                    float e = ex2(s[k] * sl2 - (m == -INFINITY ? 0.f : m));
-                    e = (edge && key > lim[c]) ? 0.f : e;
-                    const __nv_bfloat16 pb = __float2bfloat16_rn(e);
-                    s[k] = __bfloat162float(pb);
-                    *reinterpret_cast<__nv_bfloat16*>(
-                        Ps + (tid >> 6) * Cfg::P_KB + (c >> 3) * 1024 + (c & 7) * 128 +
-                        ((((tid & 63) >> 3) ^ (c & 7)) << 4) + (tid & 7) * 2) = pb;
+                    for (int k = 0; k < 32; ++k) lsum[k] *= alpha[col0 + k];
+                    if (j > 0) {
+                        // Oᵀ holds P·V up to tile j-1: that product must be done first
+                        ok = pwait(&pv_done[(j - 1) & 1], uint32_t((j - 1) >> 1) & 1u, abort_flag,
+                                   a.status) && ok;
+                        tc_fence_after();
+#pragma unroll 1
+                        for (int c2 = 0; c2 < DCH; ++c2) {
+                            const uint32_t tO = tbase + lane_off + Cfg::TM_O + c2 * NQ + col0;
+                            float o[32];
+                            tmem_ld32(tO, o);
+#pragma unroll
+                            for (int k = 0; k < 32; ++k) o[k] *= alpha[col0 + k];
+                            tmem_st32(tO, o);
+                        }
+                        tmem_wait_st();
+                    }
                 }
-                int col;
-                const float sm = warp_cols32<false>(s, lane, &col);
-                redB[warp * NQ + cb * 32 + col] = sm;
+                // the scores again (not kept in registers across the reduction)
+                tmem_ld32(tS, s);
+#pragma unroll
+                for (int k = 0; k < 32; ++k) s[k] *= sl2;
             }
             tc_fence_before();
-            mbar_arrive(&s_free[buf]);          // Sᵀ(j) is in registers no more
+            mbar_arrive(&s_free[buf]);          // Sᵀ(j) lives in registers now
+            // P buffer `buf` was last read by P·V of tile j-2
+            if (j >= 2)
+                ok = pwait(&pv_done[buf], uint32_t((j >> 1) - 1) & 1u, abort_flag, a.status) && ok;
+            unsigned char* Pb = Ps + buf * Cfg::P_BYTES + (row >> 6) * Cfg::P_KB;
+            const int rsw = (row & 63) >> 3, rb = (row & 7) * 2;
+#pragma unroll
+            for (int k4 = 0; k4 < 8; ++k4) {
+                const float4 m4 = *reinterpret_cast<const float4*>(m_run + col0 + 4 * k4);
+                const float mk[4] = {m4.x, m4.y, m4.z, m4.w};
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int k = 4 * k4 + u, c = col0 + k;
+                    float e = ex2(s[k] - mk[u]);
+                    e = ((vis >> k) & 1u) ? e : 0.f;
+                    const __nv_bfloat16 pb = __float2bfloat16_rn(e);
+                    lsum[k] += __bfloat162float(pb);
+                    *reinterpret_cast<__nv_bfloat16*>(Pb + (c >> 3) * 1024 + (c & 7) * 128 +
+                                                      ((rsw ^ (c & 7)) << 4) + rb) = pb;
+                }
+            }
             fence_async_smem();                 // P visible to the tensor core
-            mbar_arrive(p_full);
-            named_bar(1, 128);
-            if (tid < NQ)
-                l_acc += (redB[tid] + redB[NQ + tid]) + (redB[2 * NQ + tid] + redB[3 * NQ + tid]);
-            done = j + 1;
+            mbar_arrive(&p_full[buf]);
         }
         // ---------------------------------------------------------------- epilogue
-        const bool okf = done == ntiles &&
-                         pwait(pv_done, uint32_t(ntiles - 1) & 1u, abort_flag, a.status);
-        if (tid < NQ) lfin[tid] = l_acc;
-        const bool bad = named_bar_or(1, 128, !okf);
+        {   // normalisers: partial sums over the key lanes, then over the lane quarters
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                int col;
+                const float sm = warp_cols<16, false>(lsum + 16 * h, lane, &col);
+                redB[q4 * NQ + col0 + 16 * h + col] = sm;
+            }
+        }
+        ok = pwait(&pv_done[(ntiles - 1) & 1], uint32_t((ntiles - 1) >> 1) & 1u, abort_flag,
+                   a.status) && ok;
+        named_bar(1, SMT);
+        float l_fin = 0.f;
+        if (tid < NQ) {
+            l_fin = (redB[tid] + redB[NQ + tid]) + (redB[2 * NQ + tid] + redB[3 * NQ + tid]);
+            lfin[tid] = l_fin;
+        }
+        const bool bad = named_bar_or(1, SMT, !ok);
         tc_fence_after();
         if (!bad) {
             const size_t ws_row = (size_t(split) * a.units + unit) * a.nq;
 #pragma unroll 1
-            for (int q = 0; q < DCH * NCB; ++q) {
-                const int c2 = q / NCB, cb = q - c2 * NCB;
+            for (int c2 = 0; c2 < DCH; ++c2) {
                 float o[32];
-                tmem_ld32(tbase + lane_off + Cfg::TM_O + c2 * NQ + cb * 32, o);
-                const int d = c2 * 128 + tid;
+                tmem_ld32(tbase + lane_off + Cfg::TM_O + c2 * NQ + col0, o);
+                const int d = c2 * 128 + row;
 #pragma unroll
                 for (int k = 0; k < 32; ++k) {
-                    const int c = cb * 32 + k;
+                    const int c = col0 + k;
                     if (c < a.nq) {
                         if (a.splits == 1) {
                             const int i = c / G, g = c - i * G;
@@ -449,13 +509,13 @@ attn_verify_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap,
             if (a.splits > 1 && tid < a.nq) {
                 float* ml = a.ws_ml + (ws_row + tid) * 2;
                 ml[0] = m_run[tid];
-                ml[1] = l_acc;
+                ml[1] = l_fin;
             }
         }
     }
     tc_fence_before();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == Cfg::MMAW) {
         tc_fence_after();
         if (!mbar_wait_bounded(fin, 0)) set_status(a.status, GDN_STATUS_WAIT_TIMEOUT);
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;"
