@@ -143,11 +143,25 @@ def read_peaks():
     return 6800.0, "fallback"
 
 
-def kernel_sources_sha():
-    """Hash of the kernel sources: profile counters are stale once this changes."""
+# the sources each timed kernel is built from (its counters go stale when one of them changes)
+KERNEL_SOURCES = {
+    "gdn_verify": ("verify_pipe.cuh", "verify_impl.cuh", "verify_bf16.cu", "tc.cuh", "common.cuh",
+                   "kernels.h"),
+    "gdn_rollback_verify": ("verify_pipe.cuh", "verify_impl.cuh", "verify_bf16.cu", "tc.cuh",
+                            "common.cuh", "kernels.h"),
+    "gdn_rollback": ("rollback.cu", "common.cuh", "kernels.h"),
+    "spec_accept": ("accept.cu", "common.cuh", "kernels.h"),
+    "attn_verify": ("attn.cu", "tc.cuh", "common.cuh", "kernels.h"),
+}
+
+
+def kernel_sources_sha(kernel=None):
+    """Hash of a kernel's sources (all of csrc when kernel is None): profile counters are stale
+    once this changes."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "speculative_verify_gdn_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    names = KERNEL_SOURCES.get(kernel) if kernel else None
+    for name in sorted(names or os.listdir(csrc)):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
@@ -162,7 +176,7 @@ def profiled_traffic(workload_name, kernel):
         with open(p) as f:
             d = json.load(f)
         e = d.get(workload_name, {}).get(kernel)
-        if e and e.get("src_sha") == kernel_sources_sha():
+        if e and e.get("src_sha") == kernel_sources_sha(kernel):
             return float(e["dram_bytes_per_launch"])
     except Exception:
         return None
@@ -694,7 +708,8 @@ def run_attn(args):
                    "key_splits": "none" if splits == 1 else "flash-decoding split + combine"},
         "roofline": {"bound": "hbm", "kernel": "attn_verify", "achieved": achieved, "peak": peak,
                      "peak_source": "MEASURED_PEAKS.json hbm_gbs (%s)" % peak_kind, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": None, "algorithmic_bytes_per_launch": ba},
+                     "frac": achieved / peak, "traffic": profiled_traffic(w.name, "attn_verify"),
+                     "algorithmic_bytes_per_launch": ba},
         "kernels": {"attn_verify": {"ms": t_att, "bytes": ba, "GBps": achieved},
                     "attn_truncate": {"ms": t_tr}},
         "gpu_launches": K * (3 if nws == 0 else 4), "clocks": clk,
