@@ -647,7 +647,7 @@ def run_attn(args):
     lib_build.build()
     sh = _lib.AttnShape(L=w.L, B=w.B, T=w.T, Hq=w.Hq, Hkv=w.Hkv, D=w.D, ctx=w.ctx)
     kc, vc = I.attn_cache(w, args.seed, device)
-    vt = vc.transpose(-1, -2).contiguous()
+    vt = _lib.vt_from_v(vc)
     del vc
     kv_len = I.attn_lengths(w).to(device)
     pool = [I.attn_round(w, k, args.seed, device) for k in range(POOL)]

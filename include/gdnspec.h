@@ -309,7 +309,7 @@ GDN_API const char* gdn_last_error(void);
  *  L    attention layers covered by the call        B  sequences      T  verify positions
  *  Hq, Hkv  query and kv heads, Hq a multiple of Hkv; query head h reads kv head h / (Hq/Hkv)
  *  D    head dim (built for 128 and 256)            T * (Hq / Hkv) <= 128
- *  ctx  cache capacity in rows per (layer, sequence, kv head), a multiple of 8
+ *  ctx  cache capacity in rows per (layer, sequence, kv head), a multiple of 128
  *  scale  multiplies q·k (1/sqrt(D) for the usual scaled dot product)
  */
 typedef struct attn_dims {
@@ -329,8 +329,10 @@ typedef struct attn_dims {
  *   q         [L][B][T][Hq][D]
  *   k_new, v_new [L][B][T][Hkv][D]   the positions' projected keys / values
  *   k_cache   [L][B][Hkv][ctx][D]    token-major: row j is the key of position j
- *   vt_cache  [L][B][Hkv][D][ctx]    value cache stored transposed: column j is the value of
- *                                    position j (both tensor-core operands then read K-major)
+ *   vt_cache  [L][B][Hkv][ctx/128][D][128]  value cache transposed per 128-position tile: the
+ *                                    value of position j is column j % 128 of tile j / 128 (both
+ *                                    tensor-core operands then read K-major, and every tile is
+ *                                    one contiguous block)
  *   kv_len    [B] int32              committed rows per sequence (the same for every layer)
  *   out       [L][B][T][Hq][D]
  *   workspace attn_workspace_bytes(d) bytes (16-byte aligned; NULL when that is 0)

@@ -369,7 +369,20 @@ class AttnShape:
         return (self.L, self.B, self.Hkv, self.ctx, self.D)
 
     def vt_cache_shape(self):
-        return (self.L, self.B, self.Hkv, self.D, self.ctx)
+        return (self.L, self.B, self.Hkv, self.ctx // 128, self.D, 128)
+
+
+def vt_from_v(v_cache):
+    """A token-major value cache [..., ctx, D] in the library's tile-transposed layout
+    [..., ctx/128, D, 128] (layout plumbing: a view, a transpose and a copy)."""
+    *lead, ctx, D = v_cache.shape
+    return v_cache.reshape(*lead, ctx // 128, 128, D).transpose(-1, -2).contiguous()
+
+
+def v_from_vt(vt_cache):
+    """The inverse of vt_from_v: [..., ctx/128, D, 128] -> [..., ctx, D]."""
+    *lead, nt, D, _ = vt_cache.shape
+    return vt_cache.transpose(-1, -2).reshape(*lead, nt * 128, D)
 
 
 def attn_workspace_bytes(shape: AttnShape):

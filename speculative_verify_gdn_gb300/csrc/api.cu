@@ -276,13 +276,13 @@ int check_attn(const attn_dims* d) {
     if (1LL * d->T * (d->Hq / d->Hkv) > 128)
         return fail(GDN_ERR_UNSUPPORTED, "T * Hq/Hkv = %lld query rows per kv head > 128",
                     1LL * d->T * (d->Hq / d->Hkv));
-    if (d->ctx < 128 || d->ctx % 8 != 0)
-        return fail(GDN_ERR_UNSUPPORTED, "cache capacity ctx=%d: needs >= 128 and a multiple of 8",
+    if (d->ctx < 128 || d->ctx % 128 != 0)
+        return fail(GDN_ERR_UNSUPPORTED, "cache capacity ctx=%d: needs a positive multiple of 128",
                     d->ctx);
     if (d->T > d->ctx) return fail(GDN_ERR_INVALID_ARG, "T=%d > ctx=%d", d->T, d->ctx);
     if (!std::isfinite(d->scale)) return fail(GDN_ERR_INVALID_ARG, "scale must be finite");
     const long long heads = 1LL * d->L * d->B * d->Hkv;
-    if (heads * d->ctx >= (1LL << 31) || heads * d->D >= (1LL << 31) || d->B > 65535 ||
+    if (heads * d->ctx >= (1LL << 31) || heads * (d->ctx / 128) * d->D >= (1LL << 31) || d->B > 65535 ||
         d->L > 65535)
         return fail(GDN_ERR_UNSUPPORTED, "attention caches too large for 32-bit row indices");
     return GDN_OK;
@@ -537,8 +537,8 @@ int attn_verify(const attn_dims* d, const void* q, const void* k_new, const void
             return fail(GDN_ERR_CUDA, "cuTensorMapEncodeTiled failed for the K cache");
     }
     {
-        cuuint64_t dims[2] = {cuuint64_t(d->ctx), heads * cuuint64_t(d->D)};
-        cuuint64_t strides[1] = {cuuint64_t(d->ctx) * 2};
+        cuuint64_t dims[2] = {128, heads * cuuint64_t(d->ctx / 128) * cuuint64_t(d->D)};
+        cuuint64_t strides[1] = {256};
         if (enc(&vmap, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, vt_cache, dims, strides, box, estr,
                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                 CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)

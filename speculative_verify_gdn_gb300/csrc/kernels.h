@@ -124,8 +124,8 @@ struct AttnArgs {
     float* ws_ml;
     uint32_t* status;
 };
-// kmap: the K cache as rows [L·B·Hkv·ctx] x D; vmap: the transposed V cache as rows [L·B·Hkv·D] x
-// ctx; both bf16, boxes 64 x 128, 128-byte swizzle.
+// kmap: the K cache as rows [L·B·Hkv·ctx] x D; vmap: the tile-transposed V cache as rows
+// [L·B·Hkv·(ctx/128)·D] x 128; both bf16, boxes 64 x 128, 128-byte swizzle.
 cudaError_t launch_attn_verify(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                                cudaStream_t s);
 cudaError_t launch_attn_truncate(int B, int T, const int32_t* n_acc, int32_t* kv_len,

@@ -308,9 +308,9 @@ class AttnWorkload:
 # dim 256) over a 4096-token context, at the GDN workloads' batch and draft count.
 ATTN_WORKLOADS = {
     "qwen36_attn_b64_n8": AttnWorkload("qwen36_attn_b64_n8", L=10, B=64, T=8, Hq=16, Hkv=2,
-                                       D=256, ctx=4160, lengths=(4096,)),
+                                       D=256, ctx=4224, lengths=(4096,)),
     "qwen36_attn_b1_n8": AttnWorkload("qwen36_attn_b1_n8", L=10, B=1, T=8, Hq=16, Hkv=2, D=256,
-                                      ctx=4160, lengths=(4096,)),
+                                      ctx=4224, lengths=(4096,)),
 }
 
 

@@ -172,17 +172,17 @@ def test_gate_dk_host_checks(lib):
 def test_attn_host_checks(lib):
     """attn_verify / attn_truncate argument checks and the workspace size, with no device."""
     fake = ct.c_void_p(0x100000)
-    sh = _lib.AttnShape(L=10, B=64, T=8, Hq=16, Hkv=2, D=256, ctx=4160)
+    sh = _lib.AttnShape(L=10, B=64, T=8, Hq=16, Hkv=2, D=256, ctx=4224)
     d = sh.c()
     call = lambda dd, ptrs, ws=None, nws=0: lib.attn_verify(ct.byref(dd), *ptrs, ws, nws, None,
                                                             None)
     assert call(d, [None] * 7) == 1 and "NULL" in _lib.last_error()
     assert lib.attn_workspace_bytes(ct.byref(d)) == 0          # 1280 units: no key split
-    small = _lib.AttnShape(L=1, B=1, T=8, Hq=16, Hkv=2, D=256, ctx=4160)
+    small = _lib.AttnShape(L=1, B=1, T=8, Hq=16, Hkv=2, D=256, ctx=4224)
     assert _lib.attn_workspace_bytes(small) > 0
     # the split case needs its workspace
     assert call(small.c(), [fake] * 7) == 1 and "workspace" in _lib.last_error()
-    for bad, code in ((dict(D=64), 2), (dict(T=17), 2), (dict(ctx=100), 2), (dict(ctx=4100), 2),
+    for bad, code in ((dict(D=64), 2), (dict(T=17), 2), (dict(ctx=100), 2), (dict(ctx=4160), 2),
                       (dict(Hq=15), 1), (dict(Hkv=0), 1)):
         kw = dict(sh.__dict__)
         kw.update(bad)
@@ -190,8 +190,20 @@ def test_attn_host_checks(lib):
     mis = [fake] * 7
     mis[3] = ct.c_void_p(0x100008)            # k_cache not 16-byte aligned
     assert call(d, mis) == 1 and "aligned" in _lib.last_error()
-    assert call(_lib.AttnShape(L=10, B=0, T=8, Hq=16, Hkv=2, D=256, ctx=4160).c(),
+    assert call(_lib.AttnShape(L=10, B=0, T=8, Hq=16, Hkv=2, D=256, ctx=4224).c(),
                 [None] * 7) == 0
     assert lib.attn_truncate(4, 8, None, None, None, None) == 1
     assert lib.attn_truncate(0, 8, None, None, None, None) == 0
 
+
+
+def test_value_cache_tile_layout():
+    """The tile-transposed value cache: position j, dim d sits at [j // 128, d, j % 128]."""
+    import torch
+    v = torch.randn(2, 3, 256, 16)
+    vt = _lib.vt_from_v(v)
+    assert vt.shape == (2, 3, 2, 16, 128) and vt.is_contiguous()
+    for j in (0, 5, 127, 128, 200, 255):
+        for d in (0, 7, 15):
+            assert vt[1, 2, j // 128, d, j % 128] == v[1, 2, j, d]
+    assert torch.equal(_lib.v_from_vt(vt), v)
