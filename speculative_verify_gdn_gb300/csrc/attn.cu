@@ -23,9 +23,10 @@
 //     above it, so in the common case a tile costs each thread one compare per score and one
 //     barrier; otherwise the tile maxima are reduced (a transposing warp reduction, 31 shuffles per
 //     32 columns, plus a 4-way shared-memory step) and Oᵀ and the partial sums are rescaled. The
-//     weights stay ≤ 2^8; P is rounded to bf16 for the tensor core (double-buffered, so the
-//     softmax of tile j overlaps P·V of tile j-1) and each thread sums its rounded weights,
-//     reduced once at the end, so numerator and denominator use the same weights.
+//     weights stay ≤ 2^8; P is rounded to bf16 for the tensor core (one buffer: the softmax is
+//     not on the critical path, the shared memory is worth more as a ring stage) and each thread
+//     sums its rounded weights, reduced once at the end, so numerator and denominator use the
+//     same weights.
 //   * Warp roles: softmax + epilogue, then one TMA producer warp, then one MMA issue + TMEM owner
 //     warp. The ring
 //     holds 32 KiB chunks (128 keys × 128 of the head dim, or 128 d-rows × 128 keys), as many as
@@ -55,15 +56,16 @@ struct AttnCfg {
     static constexpr int Q_KB = NQ * 128;               // bytes of one 64-element K-block of Q
     static constexpr int Q_BYTES = (D / 64) * Q_KB;
     static constexpr int P_KB = NQ * 128;               // bytes of one 64-key K-block of P
-    static constexpr int P_BYTES = 2 * P_KB;            // one P tile (two buffers are kept)
+    static constexpr int P_BYTES = 2 * P_KB;            // the P tile (one buffer: its smem is
+                                                        // worth more as a ring stage)
     // ring stages: as many as the shared memory left over holds (at most 6)
-    static constexpr int FIXED = Q_BYTES + 2 * P_BYTES + 12 * NQ * 4 + 21 * 8 + 16 + 1024 + 64;
+    static constexpr int FIXED = Q_BYTES + P_BYTES + 12 * NQ * 4 + 21 * 8 + 16 + 1024 + 64;
     static constexpr int NST_FIT = (227 * 1024 - FIXED) / CHUNK;
     static constexpr int NST = NST_FIT > 6 ? 6 : NST_FIT;
     static constexpr size_t OFF_RING = 0;
     static constexpr size_t OFF_Q = OFF_RING + size_t(NST) * CHUNK;
     static constexpr size_t OFF_P = OFF_Q + Q_BYTES;
-    static constexpr size_t OFF_F = OFF_P + 2 * P_BYTES;  // redA[4][NQ] redB[4][NQ] m, alpha, l [NQ]
+    static constexpr size_t OFF_F = OFF_P + P_BYTES;    // redA[4][NQ] redB[4][NQ] m, alpha, l [NQ]
     static constexpr size_t OFF_LIM = OFF_F + size_t(11) * NQ * 4;   // int lim[NQ]
     // barriers: full[NST] empty[NST] s_full[2] s_free[2] p_full[2] pv_done[2] fin (one barrier per
     // buffer, so no waiter is ever two phases behind)
@@ -338,7 +340,7 @@ attn_verify_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap,
                 }
                 tc_fence_after();
                 const uint64_t da = umma_desc_sw128(sR + stage * Cfg::CHUNK);
-                const uint64_t db = umma_desc_sw128(sP + buf * Cfg::P_BYTES);
+                const uint64_t db = umma_desc_sw128(sP);
 #pragma unroll
                 for (int kb = 0; kb < 2; ++kb)
 #pragma unroll
@@ -451,10 +453,11 @@ attn_verify_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap,
             }
             tc_fence_before();
             mbar_arrive(&s_free[buf]);          // Sᵀ(j) lives in registers now
-            // P buffer `buf` was last read by P·V of tile j-2
-            if (j >= 2)
-                ok = pwait(&pv_done[buf], uint32_t((j >> 1) - 1) & 1u, abort_flag, a.status) && ok;
-            unsigned char* Pb = Ps + buf * Cfg::P_BYTES + (row >> 6) * Cfg::P_KB;
+            // the P tile was last read by P·V of tile j-1
+            if (j >= 1)
+                ok = pwait(&pv_done[(j - 1) & 1], uint32_t((j - 1) >> 1) & 1u, abort_flag,
+                           a.status) && ok;
+            unsigned char* Pb = Ps + (row >> 6) * Cfg::P_KB;
             const int rsw = (row & 63) >> 3, rb = (row & 7) * 2;
 #pragma unroll
             for (int k4 = 0; k4 < 8; ++k4) {
