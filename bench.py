@@ -561,12 +561,17 @@ def main(argv=None):
     ap.add_argument("--attn", default=None,
                     help="time the attention layers instead (an ATTN_WORKLOADS key, e.g. "
                          "qwen36_attn_b64_n8)")
+    ap.add_argument("--hybrid", default=None,
+                    help="time a whole hybrid round: the GDN workload plus this attention workload "
+                         "(e.g. qwen36_attn_b64_n8)")
     ap.add_argument("--gate-dk", action="store_true",
                     help="one gate per key channel (g [L, B, T, Hv, d]); chain workloads only")
     args = ap.parse_args(argv)
 
     if args.attn:
         return run_attn(args)
+    if args.hybrid:
+        return run_hybrid(args)
     from speculative_verify_gdn_gb300 import inputs as I
     w = I.WORKLOADS[args.config]
     if args.batch is not None or args.layers is not None:
@@ -713,6 +718,112 @@ def run_attn(args):
         "kernels": {"attn_verify": {"ms": t_att, "bytes": ba, "GBps": achieved},
                     "attn_truncate": {"ms": t_tr}},
         "gpu_launches": K * (3 if nws == 0 else 4), "clocks": clk,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+HYBRID_METRIC = ("hybrid-round verified draft tokens/sec (30 GDN + 10 attention layers: verify, "
+                 "accept, rollback + KV truncation); % HBM roofline")
+
+
+def run_hybrid(args):
+    """A whole hybrid round of the layers this library covers: gdn_verify (30 GDN layers),
+    attn_verify (10 attention layers), spec_accept, gdn_rollback and attn_truncate with the same
+    accepted counts. The committed cache length is reset to the workload's at the start of each
+    step (a 256-byte device copy), so every step attends over the same context."""
+    import torch
+    from speculative_verify_gdn_gb300 import _lib, build as lib_build, inputs as I
+    from speculative_verify_gdn_gb300.round import SpecRound
+    w = I.WORKLOADS[args.config]
+    aw = I.ATTN_WORKLOADS[args.hybrid]
+    assert (aw.B, aw.T) == (w.B, w.N) and w.accept != "tree", "attention workload must match"
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    lib_build.build()
+    seed = args.seed
+    cw = I.model_weights(w, seed, device)
+    state, conv_state = I.initial_state(w, seed, device)
+    pool = make_pool(w, seed, device, POOL)
+    apool = [I.attn_round(aw, k, seed, device) for k in range(POOL)]
+    kc, vc = I.attn_cache(aw, seed, device)
+    vt = _lib.vt_from_v(vc)
+    del vc
+    kv_base = I.attn_lengths(aw).to(device)
+    kv_len = kv_base.clone()
+    ash = _lib.AttnShape(L=aw.L, B=aw.B, T=aw.T, Hq=aw.Hq, Hkv=aw.Hkv, D=aw.D, ctx=aw.ctx)
+    aout = torch.empty(ash.q_shape(), dtype=torch.bfloat16, device=device)
+    nws = _lib.attn_workspace_bytes(ash)
+    aws = torch.empty(max(nws, 16), dtype=torch.uint8, device=device) if nws else None
+    r = SpecRound(w, device)
+    stream = torch.cuda.current_stream(device)
+    names = ("gdn_verify", "attn_verify", "spec_accept", "gdn_rollback", "attn_truncate")
+
+    def step(k, evs=None):
+        s, (q, kn, vn) = pool[k % POOL], apool[k % POOL]
+        kv_len.copy_(kv_base, non_blocking=True)
+        rec = (lambda i: evs[i].record(stream)) if evs is not None else (lambda i: None)
+        rec(0)
+        r.verify(s["qkv"], cw, conv_state, s["g"], s["beta"], state)
+        rec(1)
+        _lib.attn_verify(ash, q, kn, vn, kc, vt, kv_len, aout, workspace=aws, status=r.status)
+        rec(2)
+        r.accept(s["logits"], s["drafts"], round_=k, seed=seed)
+        rec(3)
+        r.rollback(s["qkv"], s["g"], state, conv_state)
+        rec(4)
+        _lib.attn_truncate(r.n_acc, kv_len, aw.T, status=r.status)
+        rec(5)
+
+    for k in range(args.warmup):
+        step(k)
+    r.check_status()
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(K)]
+    nlog = torch.zeros((K, w.B), dtype=torch.int32, device=device)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(0)
+    clocks.start()
+    torch.cuda.synchronize(device)
+    start.record(stream)
+    for k in range(K):
+        step(args.warmup + k, evs[k])
+        nlog[k].copy_(r.n_acc, non_blocking=True)
+    end.record(stream)
+    torch.cuda.synchronize(device)
+    clk = clocks.stop()
+    r.check_status()
+    ms_step = start.elapsed_time(end) / K
+    t = {n: statistics.mean(evs[k][i].elapsed_time(evs[k][i + 1]) for k in range(K))
+         for i, n in enumerate(names)}
+    nl = nlog.cpu().numpy()
+    peak, peak_kind = read_peaks()
+    by = {"gdn_verify": bytes_verify(w), "attn_verify": bytes_attn(aw, kv_base.tolist()),
+          "spec_accept": bytes_accept(w),
+          "gdn_rollback": statistics.mean(bytes_rollback(w, nl[k]) for k in range(K)),
+          "attn_truncate": 8 * w.B}
+    kern = {n: {"ms": t[n], "bytes": by[n], "GBps": by[n] / (t[n] / 1e3) / 1e9,
+                "frac_of_%s_peak" % peak_kind: by[n] / (t[n] / 1e3) / 1e9 / peak} for n in names}
+    dom = max(kern, key=lambda n: kern[n]["ms"])
+    step_bytes = sum(by.values())
+    line = {
+        "metric": HYBRID_METRIC, "value": w.B * w.N / (ms_step / 1e3), "unit": UNIT, "n_gpus": 1,
+        "steps": K, "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "io_dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": "%s + %s: 30 GDN layers and 10 attention layers of the Qwen3.6 "
+                               "hybrid, batch %d, N=%d, %d committed cache rows" % (
+                                   w.name, aw.name, w.B, w.N, aw.lengths[0]),
+                   "l2": "inputs larger than L2: %.2f GB moved per step" % (step_bytes / 1e9)},
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": kern[dom]["GBps"], "peak": peak,
+                     "peak_source": "MEASURED_PEAKS.json hbm_gbs (%s)" % peak_kind, "unit": "GB/s",
+                     "frac": kern[dom]["GBps"] / peak,
+                     "traffic": profiled_traffic(w.name if dom.startswith("gdn") else aw.name, dom),
+                     "algorithmic_bytes_per_launch": by[dom],
+                     "step_frac": step_bytes / (ms_step / 1e3) / 1e9 / peak},
+        "kernels": kern, "mean_accepted": float(nl.mean()),
+        "gpu_launches": K * (r.launches_per_step(False) + (2 if nws == 0 else 3) + 1),
+        "clocks": clk,
     }
     print(json.dumps(line), flush=True)
     return 0
