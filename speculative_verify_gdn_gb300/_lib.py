@@ -71,8 +71,8 @@ def load(require_file=True):
         return _lib
     path = _build.LIB
     if not os.path.exists(path):
-        raise GdnError("libgdnspec.so is not built (%s): run __graft_entry__.build() or "
-                       "speculative_verify_gdn_gb300/build.py" % path)
+        raise GdnError("libgdnspec.so is not built (%s): run "
+                       "python -m speculative_verify_gdn_gb300.build" % path)
     lib = ct.CDLL(path)
     P, i32, u64, f32, sz = ct.c_void_p, ct.c_int32, ct.c_uint64, ct.c_float, ct.c_size_t
     lib.gdn_verify.argtypes = [P] * 12

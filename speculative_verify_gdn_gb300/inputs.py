@@ -5,7 +5,7 @@ it holds none of the method's arithmetic and is the one piece shared by the CUDA
 oracle's tests and the bench. Every tensor comes from a generator seeded by
 (seed, workload, round, tensor name), so any piece can be regenerated independently.
 
-Distributions (the workloads' own statements, with the readings listed in the design doc):
+Distributions (the workloads' own statements; where they are silent, the plainest reading):
   raw qkv ~ N(0, 1); beta = sigmoid(N(0, 1)); g = exp(-softplus(N(0, 1))) (per value head, or
   independently per key channel when gate_dk); S_0 ~ N(0, 0.1)
   (0.1 is the standard deviation); conv weights ~ N(0, 0.5); initial conv state ~ N(0, 1).

@@ -62,6 +62,24 @@ def test_bench_byte_accounting():
     assert bench.aggregate_tokens_per_s(2, 64, 8, 2.0) == 2 * 64 * 8 / 2e-3
 
 
+def test_bench_byte_accounting_gates_and_attention():
+    import dataclasses
+    w = I.WORKLOADS[2]
+    # per-key-channel gates: the gate bytes grow from 4·Hv to 4·Hv·d per position, nothing else
+    gdk = I.custom(w, name=w.name, gate_dk=True)
+    assert bench.bytes_verify(gdk) - bench.bytes_verify(w) == 30 * 64 * 8 * 4 * 32 * 127
+    assert (bench.bytes_rollback(gdk, [2] + [0] * 63) - bench.bytes_rollback(w, [2] + [0] * 63)
+            == 30 * 2 * 4 * 32 * 127)
+    aw = I.ATTN_WORKLOADS["qwen36_attn_b64_n8"]
+    one = dataclasses.replace(aw, B=1)
+    assert bench.bytes_attn(aw, [4096] * 64) == 64 * bench.bytes_attn(one, [4096])
+    # one more committed row: one more key and value row read per layer and kv head
+    assert (bench.bytes_attn(one, [4097]) - bench.bytes_attn(one, [4096])
+            == 2 * aw.D * 2 * aw.L * aw.Hkv)
+    # the per-step reads at 4096 rows dominate: K and V of 4104 rows x 10 layers x 2 kv heads
+    assert bench.bytes_attn(one, [4096]) > 2 * 4104 * 256 * 2 * 10 * 2
+
+
 def _free_port():
     s = socket.socket()
     s.bind(("127.0.0.1", 0))
