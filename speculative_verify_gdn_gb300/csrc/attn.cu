@@ -11,7 +11,7 @@
 //     TMA. The K cache is token-major [ctx][D]; the V cache is stored transposed per 128-key tile,
 //     [ctx/128][D][128], so both tensor-core products read K-major, 128-byte-swizzled tiles exactly
 //     as the TMA boxes land and every tile of K and of V is one contiguous 64 KiB block in HBM (a
-//     plain [D][ctx] transpose reads 256-byte pieces 2·ctx bytes apart and runs ~35 % slower).
+//     plain [D][ctx] transpose reads 256-byte pieces 2·ctx bytes apart and ran ~5 % slower).
 //   * One CTA per (layer, sequence, kv head, key split). Its query rows are the T·(Hq/Hkv)
 //     (position, head) pairs of the kv head, zero-padded to NQ ∈ {32, 64, 128}. Per 128-key tile:
 //         Sᵀ[key][row]  = K_tile · Qᵀ       tcgen05, M = 128 keys, N = NQ, K = D
@@ -28,10 +28,10 @@
 //     sums its rounded weights, reduced once at the end, so numerator and denominator use the
 //     same weights.
 //   * Warp roles: softmax + epilogue, then one TMA producer warp, then one MMA issue + TMEM owner
-//     warp. The ring
-//     holds 32 KiB chunks (128 keys × 128 of the head dim, or 128 d-rows × 128 keys), as many as
-//     the shared memory left over holds, in the order the tensor core consumes them: K(0), K(1),
-//     V(0), K(2), V(1), …
+//     warp. The ring holds 32 KiB chunks (128 keys × 128 of the head dim, or 128 d-rows × 128
+//     keys), as many as the shared memory left over holds, in the order the tensor core consumes
+//     them: K(0), K(1), V(0), K(2), V(1), … Each CTA is bound by the bytes it keeps in flight, so
+//     shared memory goes to ring stages first.
 //   * Short batches over long caches split the keys across CTAs (flash-decoding); a combine
 //     kernel merges the partial (max, sum, O).
 // Every wait is bounded (1 s); a timeout sets GDN_STATUS_WAIT_TIMEOUT, the CTA stops issuing
