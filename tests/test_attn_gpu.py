@@ -202,7 +202,9 @@ def test_attn_full_size_sampled_units(gdnlib):
     units = [(0, 0), (7, 41)]
     for (l, b) in units:
         kc_before[(l, b)] = (kc[l, b].clone(), vc[l, b].clone())
-    _lib.attn_verify(sh, q, kn, vn, kc, vt, kv_len, out, status=st)
+    nws = _lib.attn_workspace_bytes(sh)
+    ws = torch.empty(max(nws, 16), dtype=torch.uint8, device=dev) if nws else None
+    _lib.attn_verify(sh, q, kn, vn, kc, vt, kv_len, out, workspace=ws, status=st)
     torch.cuda.synchronize()
     assert int(st.item()) == 0
     assert torch.isfinite(out.float()).all()
