@@ -93,8 +93,8 @@ typedef struct gdn_dims {
     float l2_eps;
     int32_t gate_dk;     /* 0: g is [L][B][T][Hv]; 1: g is [L][B][T][Hv][Dk], one decay per key
                             channel (GDN investigation §4 tape layout [B, T, Hv, Dk]):
-                            S ← S·diag(g_t) + δ_t k_tᵀ with u = S·diag(g_t)·k_t. Chains only
-                            (gdn_verify, gdn_rollback, gdn_rollback_verify); trees reject it. */
+                            S ← S·diag(g_t) + δ_t k_tᵀ with u = S·diag(g_t)·k_t. Every call
+                            takes it; trees with fp32 I/O and d = 128 are limited to T <= 16. */
 } gdn_dims;
 
 /*
@@ -135,7 +135,7 @@ GDN_API int gdn_verify(const gdn_dims* d, const void* qkv, const void* conv_w, c
  * Node v starts from its parent's state (S_0 for parent -1); its conv window is its own raw row
  * and its W-1 nearest ancestors' rows, continued into conv_state when the path is shorter.
  * Other arguments and layouts as gdn_verify with T = node count; the tape is per node.
- * d->gate_dk = 1 returns GDN_ERR_UNSUPPORTED (as does gdn_rollback_path).
+ * With d->gate_dk, fp32 I/O and Dk = 128, T is limited to 16 (GDN_ERR_UNSUPPORTED above).
  * A bad parent sets GDN_STATUS_BAD_PARENT; that sequence's out / tape rows are then unspecified
  * (left unwritten, or computed as if the nodes formed one chain).
  */

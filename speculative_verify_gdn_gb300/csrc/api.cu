@@ -131,8 +131,9 @@ int verify_common(const gdn_dims* d, const int32_t* parent, const void* qkv, con
                   bool tree) {
     int rc = check_dims(d);
     if (rc) return rc;
-    if (tree && d->gate_dk)
-        return fail(GDN_ERR_UNSUPPORTED, "gdn_verify_tree takes one gate per value head (gate_dk=0)");
+    if (tree && d->gate_dk && d->io_dtype == GDN_DTYPE_F32 && d->Dk == 128 && d->T > 16)
+        return fail(GDN_ERR_UNSUPPORTED,
+                    "gdn_verify_tree with per-key-channel gates, fp32 I/O and d=128: T <= 16");
     if (empty(d)) return GDN_OK;
     if (!qkv || !conv_w || !g || !beta || !state || !out || !tape_delta || !tape_k ||
         (d->W > 1 && !conv_state) || (tree && !parent))
@@ -192,8 +193,6 @@ int rollback_common(const gdn_dims* d, const int32_t* path, int32_t P, const int
     int rc = check_dims(d);
     if (rc) return rc;
     if (path && P < 0) return fail(GDN_ERR_INVALID_ARG, "path capacity P=%d < 0", P);
-    if (path && d->gate_dk)
-        return fail(GDN_ERR_UNSUPPORTED, "gdn_rollback_path takes one gate per value head (gate_dk=0)");
     if (empty(d) || (path && P == 0)) return GDN_OK;
     if (!n_acc || !tape_delta || !tape_k || !g || !qkv || !state || (d->W > 1 && !conv_state))
         return fail(GDN_ERR_INVALID_ARG, "NULL tensor pointer");

@@ -6,9 +6,10 @@
 //   rule u = g S k, δ = β (v − u), S ← g S + δ kᵀ, o = scale · S q, from the snapshot S_0,
 //   node by node (chain: node t's parent is t−1; tree: an explicit parent array).
 //   Writes o, the tape (δ per value head, normalised k per key head). S_0 is never written.
-//   Chains also take one gate per key channel (g [B, T, Hv, Dk], §4's tape layout):
+//   Chains and trees also take one gate per key channel (g [B, T, Hv, Dk], §4's tape layout):
 //   S ← S·diag(a_t) + δ kᵀ with u = S·diag(a_t)·k; then the dense product reads the decayed
-//   columns A_t ⊙ k_t, A_t ⊙ q_t and the Gram block carries the per-channel decays.
+//   columns A_t ⊙ k_t, A_t ⊙ q_t (A_t: the gates of t and its ancestors) and the Gram block
+//   carries the per-channel decays between each node and its ancestors.
 //
 // How (GB300 design):
 //   * The state update is never materialised. With Γ(a→p) the product of the gates strictly
@@ -83,7 +84,6 @@ struct VerifyCfg {
     }
 
     static_assert(D == 32 || D == 64 || D == 128, "head dim");
-    static_assert(!(GDK && TREE), "per-key-channel gates are built for chains");
     static_assert(OFF_A % 1024 == 0, "swizzle atoms need 1024-byte bases");
 };
 
@@ -372,7 +372,13 @@ gdn_verify_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap smap) 
             const float x = yqk[t] * inv[n0 + t];
             float xw = x;
             if constexpr (GDK) {
-                if (t < T) cum *= GA[t * D + idx];
+                if constexpr (TREE) {          // the gates of t and its ancestors, root-most last
+                    cum = 1.f;
+                    if (t < T)
+                        for (int y = t; y >= 0; y = par[y]) cum *= GA[y * D + idx];
+                } else if (t < T) {
+                    cum *= GA[t * D + idx];
+                }
                 xw = x * cum;
             }
             const float hi = tf32_trunc(xw);
@@ -446,6 +452,35 @@ gdn_verify_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap smap) 
             kqv[s] = kq;
             c0[s] = 1.f;
         }
+        if constexpr (TREE) {
+            // node v = s reads its ancestors x: CK[v][x] = Σ_j k_x[j] k_v[j] Π_{r ∈ (x, v]} a_r[j],
+            // the product running up the parent chain (v's own gate first). The 8 lanes of a
+            // group share v, so each group reduces with its own lane mask.
+            const unsigned gmask = 0xFFu << (lane & 24);
+            const int v = s;
+#pragma unroll
+            for (int m = 0; m < NJ; ++m) w[m] = act ? GA[v * D + c + 8 * m] : 1.f;
+            for (int x = act ? par[v] : -1; x >= 0; x = par[x]) {
+                float ck = 0.f, cq = 0.f;
+#pragma unroll
+                for (int m = 0; m < NJ; ++m) {
+                    const int j = c + 8 * m;
+                    const float xw = XP[x * XS + j] * w[m];
+                    ck = fmaf(xw, ks[m], ck);
+                    cq = fmaf(xw, XP[(TMAX + v) * XS + j], cq);
+                    w[m] *= GA[x * D + j];
+                }
+#pragma unroll
+                for (int o = 1; o < 8; o <<= 1) {
+                    ck += __shfl_xor_sync(gmask, ck, o);
+                    cq += __shfl_xor_sync(gmask, cq, o);
+                }
+                if (c == 0) {
+                    CK[v * TMAX + x] = ck;
+                    CQ[v * TMAX + x] = cq;
+                }
+            }
+        } else
         for (int t = 1; t < T; ++t) {          // warp-uniform trip count (shuffles below)
             const bool on = t > s;
             float ck = 0.f, cq = 0.f;
@@ -492,24 +527,27 @@ gdn_verify_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap smap) 
         }
     }
     // fold the gate products in: CK[v][a] *= Γ(a→parent(v)); c0[v] = Γ(root→parent(v)) (the
-    // per-channel Gram above already carries its decays, and c0 = 1)
-    if constexpr (!GDK) {
+    // per-channel Gram above already carries its decays, and c0 = 1); trees list each node's
+    // ancestors for the recurrence
+    if constexpr (!GDK || TREE) {
         __syncthreads();
         if (tid < T) {
             const int v = tid;
             float coef = 1.f;
             int m = 0;
             int x = TREE ? par[v] : v - 1;
-            kqv[v] = CQ[v * TMAX + v];
+            if constexpr (!GDK) kqv[v] = CQ[v * TMAX + v];
             while (x >= 0) {
-                CK[v * TMAX + x] *= coef;
-                CQ[v * TMAX + x] *= coef;
+                if constexpr (!GDK) {
+                    CK[v * TMAX + x] *= coef;
+                    CQ[v * TMAX + x] *= coef;
+                    coef *= gam[x];
+                }
                 if constexpr (TREE) anc[v * TMAX + m] = x;
                 ++m;
-                coef *= gam[x];
                 x = TREE ? par[x] : x - 1;
             }
-            c0[v] = coef;
+            if constexpr (!GDK) c0[v] = coef;
             if constexpr (TREE) nanc[v] = m;
         }
     }
@@ -596,10 +634,11 @@ gdn_verify_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap smap) 
                         sk = fmaf(CK[v * TMAX + an], da, sk);
                         sq = fmaf(CQ[v * TMAX + an], da, sq);
                     }
-                    const float u = gam[v] * sk;
+                    const float gv = GDK ? 1.f : gam[v];   // per-channel decay: in pr and CK
+                    const float u = gv * sk;
                     const float d = bet[v] * (DL[size_t(v) * D + i] - u);
                     DL[size_t(v) * D + i] = d;
-                    const float o = scale * fmaf(d, kqv[v], gam[v] * sq);
+                    const float o = scale * fmaf(d, kqv[v], gv * sq);
                     const size_t oi = ((lb * T + v) * Hv + h) * size_t(D) + i;
                     a.tape_delta[oi] = d;
                     Tr::store(out, oi, o);
@@ -648,8 +687,8 @@ cudaError_t launch_verify_gk(const VerifyArgs& a, const CUtensorMap& map, int D,
 template <typename IO, bool TREE>
 cudaError_t launch_verify_io(const VerifyArgs& a, const CUtensorMap& map, int D, cudaStream_t s) {
     if constexpr (TREE) {
-        if (a.gate_dk) return cudaErrorInvalidValue;
-        return launch_verify_gk<IO, true, false>(a, map, D, s);
+        return a.gate_dk ? launch_verify_gk<IO, true, true>(a, map, D, s)
+                         : launch_verify_gk<IO, true, false>(a, map, D, s);
     } else {
         return a.gate_dk ? launch_verify_gk<IO, false, true>(a, map, D, s)
                          : launch_verify_gk<IO, false, false>(a, map, D, s);

@@ -136,3 +136,70 @@ def test_gpu_per_channel_gates_rollback_verify(gdnlib, D, T):
     assert_close(f64(out), ref["out"], "out", bf16=True)
     assert_close(f64(tdl), ref["tape_delta"], "tape_delta")
     assert_close(f64(tk), ref["tape_k"], "tape_k")
+
+
+def random_parents(rng, B, T, depth):
+    """parent[b][v] in [-1, v): a chain of `depth` nodes first, the rest attached at random to a
+    node of depth < depth (or to the context)."""
+    par = np.full((B, T), -1, np.int32)
+    for b in range(B):
+        dep = [0] * T
+        for v in range(T):
+            if v < depth:
+                par[b, v] = v - 1
+            else:
+                cand = [-1] + [x for x in range(v) if dep[x] < depth - 1]
+                par[b, v] = cand[rng.integers(len(cand))]
+            dep[v] = 0 if par[b, v] < 0 else dep[par[b, v]] + 1
+    return par
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("D,T,io", [(32, 8, torch.float32), (64, 16, torch.float32),
+                                    (128, 16, torch.float32), (128, 32, torch.bfloat16),
+                                    (128, 12, torch.bfloat16)])
+def test_gpu_per_channel_gates_trees_and_path_rollback(gdnlib, D, T, io):
+    """Trees with one gate per key channel (per-head kernel), then the path rollback along each
+    sequence's accepted root-to-leaf prefix, against the oracle's node-by-node recurrence."""
+    from parity_util import assert_close, f64, oracle_rollback, oracle_verify, to_dev
+    from speculative_verify_gdn_gb300 import inputs as I
+    from speculative_verify_gdn_gb300.round import SpecRound
+    rng = np.random.default_rng(D + T)
+    w = gdk_workload(D, T, io=io, B=3)
+    w = I.custom(w, name=w.name + "_tree", accept="tree", tree_depth=min(T, 6), tree_branch=3)
+    cw = I.model_weights(w, 5)
+    st, cs = I.initial_state(w, 5)
+    qkv, g, beta = I.round_stream(w, 0, 5)
+    par = torch.from_numpy(random_parents(rng, w.B, T, min(T, 6)))
+    r = SpecRound(w)
+    dq, dcw, dcs, dg, db, dst = to_dev(qkv, cw, cs, g, beta, st)
+    r.verify(dq, dcw, dcs, dg, db, dst, parent=par.cuda())
+    r.check_status()
+    ref = oracle_verify(w, qkv, cw, cs, g, beta, st, parent=par)
+    assert_close(f64(r.out), ref["out"], "out", bf16=io == torch.bfloat16)
+    assert_close(f64(r.tape_delta), ref["tape_delta"], "tape_delta")
+    assert_close(f64(r.tape_k), ref["tape_k"], "tape_k")
+    # accepted paths: the deepest chain from the root (nodes 0, 1, ...) cut at various lengths
+    P = r.path.shape[1]
+    path = np.zeros((w.B, P), np.int32)
+    n = np.array([min(P, 3), 0, P], np.int32)
+    for b in range(w.B):
+        x, chain = int(np.argmax([len(list(_ancestors(par[b].numpy(), v))) for v in range(T)])), []
+        chain = list(_ancestors(par[b].numpy(), x))[::-1][:P]
+        path[b, :len(chain)] = chain
+        n[b] = min(n[b], len(chain))
+    r.path.copy_(torch.from_numpy(path))
+    r.n_acc.copy_(torch.from_numpy(n))
+    r.rollback(dq, dg, dst, dcs)
+    r.check_status()
+    st_ref, cs_ref, bad = oracle_rollback(w, n, ref, g, qkv, st, cs, path=path)
+    assert bad == 0
+    assert_close(f64(dst), st_ref, "state")
+    assert np.array_equal(f64(dcs), cs_ref)
+
+
+def _ancestors(par, v):
+    while v >= 0:
+        yield v
+        v = int(par[v])
+
