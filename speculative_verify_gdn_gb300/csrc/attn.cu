@@ -12,8 +12,10 @@
 //     [ctx/128][D][128], so both tensor-core products read K-major, 128-byte-swizzled tiles exactly
 //     as the TMA boxes land and every tile of K and of V is one contiguous 64 KiB block in HBM (a
 //     plain [D][ctx] transpose reads 256-byte pieces 2·ctx bytes apart and ran ~5 % slower).
-//   * One CTA per (layer, sequence, kv head, key split). Its query rows are the T·(Hq/Hkv)
-//     (position, head) pairs of the kv head, zero-padded to NQ ∈ {32, 64, 128}. Per 128-key tile:
+//   * One CTA per (layer, sequence, kv head, key split, group of 64 query rows). Its query rows
+//     are T·(Hq/Hkv) (position, head) pairs of the kv head, zero-padded to NQ ∈ {32, 64}; with more
+//     than 64 rows the groups run as adjacent CTAs that read the same K / V tiles, the second from
+//     L2. Per 128-key tile:
 //         Sᵀ[key][row]  = K_tile · Qᵀ       tcgen05, M = 128 keys, N = NQ, K = D
 //         Oᵀ[d][row]   += Vᵀ_tile · Pᵀ      tcgen05, M = 128 d-rows per chunk, N = NQ, K = 128 keys
 //     Sᵀ is double-buffered in TMEM (the next tile's product overlaps this tile's softmax) and
@@ -180,7 +182,11 @@ attn_verify_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap,
     uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + Cfg::OFF_MISC + 8);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int split = blockIdx.x % a.splits, unit = blockIdx.x / a.splits;
+    // block = (unit, key split, query-row group): the row groups of a unit are adjacent, so they
+    // run together and the second one's K / V tiles come from L2
+    const int rg = blockIdx.x % a.rgroups, rest = blockIdx.x / a.rgroups;
+    const int split = rest % a.splits, unit = rest / a.splits;
+    const int row0 = rg * NQ;                              // first query row of this CTA
     const int kvh = unit % a.Hkv, lb = unit / a.Hkv, b = lb % a.B;
     const int T = a.T, G = a.group;
     const int n0 = __ldg(a.kv_len + b);
@@ -188,8 +194,8 @@ attn_verify_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap,
     const int t0 = split * a.tiles_per_split;              // first 128-key tile of this CTA
     const int ntiles = min(((n0 + T + 127) >> 7) - t0, a.tiles_per_split);
     if (ntiles <= 0) {                                     // a split past the end: empty partial
-        if (tid < a.nq) {
-            float* ml = a.ws_ml + ((size_t(split) * a.units + unit) * a.nq + tid) * 2;
+        if (tid < NQ && row0 + tid < a.nq) {
+            float* ml = a.ws_ml + ((size_t(split) * a.units + unit) * a.nq + row0 + tid) * 2;
             ml[0] = -INFINITY;
             ml[1] = 0.f;
         }
@@ -224,8 +230,8 @@ attn_verify_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap,
         for (int e = tid; e < NQ * (D / 8); e += Cfg::NTHR) {
             const int c = e / (D / 8), j8 = e - c * (D / 8);
             uint4 v = make_uint4(0u, 0u, 0u, 0u);
-            if (c < a.nq) {
-                const int i = c / G, g = c - i * G;
+            if (row0 + c < a.nq) {
+                const int i = (row0 + c) / G, g = (row0 + c) - i * G;
                 v = __ldg(reinterpret_cast<const uint4*>(qh + (size_t(i) * a.Hq + g) * D) + j8);
             }
             const int kb = j8 >> 3, ch = j8 & 7;
@@ -234,7 +240,7 @@ attn_verify_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap,
         }
         if (tid < NQ) {
             m_run[tid] = -INFINITY;
-            lim[tid] = n0 + (tid < a.nq ? tid / G : T - 1);
+            lim[tid] = n0 + (row0 + tid < a.nq ? (row0 + tid) / G : T - 1);
         }
     }
     fence_async_smem();
@@ -505,20 +511,20 @@ attn_verify_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap,
                 const int d = c2 * 128 + row;
 #pragma unroll
                 for (int k = 0; k < 32; ++k) {
-                    const int c = col0 + k;
-                    if (c < a.nq) {
+                    const int c = col0 + k, cg = row0 + c;      // local and unit-wide row
+                    if (cg < a.nq) {
                         if (a.splits == 1) {
-                            const int i = c / G, g = c - i * G;
+                            const int i = cg / G, g = cg - i * G;
                             a.out[((size_t(lb) * T + i) * a.Hq + kvh * G + g) * D + d] =
                                 __float2bfloat16_rn(o[k] / lfin[c]);
                         } else {
-                            a.ws_o[(ws_row + c) * D + d] = o[k];
+                            a.ws_o[(ws_row + cg) * D + d] = o[k];
                         }
                     }
                 }
             }
-            if (a.splits > 1 && tid < a.nq) {
-                float* ml = a.ws_ml + (ws_row + tid) * 2;
+            if (a.splits > 1 && tid < NQ && row0 + tid < a.nq) {
+                float* ml = a.ws_ml + (ws_row + row0 + tid) * 2;
                 ml[0] = m_run[tid];
                 ml[1] = l_fin;
             }
@@ -584,24 +590,25 @@ static cudaError_t launch_attn_t(const AttnArgs& a, const CUtensorMap& kmap,
         if (e != cudaSuccess) return e;
         attr_done = true;
     }
-    kern<<<unsigned(a.units) * unsigned(a.splits), Cfg::NTHR, Cfg::SMEM, s>>>(a, kmap, vmap);
+    kern<<<unsigned(a.units) * unsigned(a.splits) * unsigned(a.rgroups), Cfg::NTHR, Cfg::SMEM, s>>>(
+        a, kmap, vmap);
     return cudaGetLastError();
 }
 
-cudaError_t launch_attn_verify(const AttnArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                               cudaStream_t s) {
+cudaError_t launch_attn_verify(const AttnArgs& a0, const CUtensorMap& kmap,
+                               const CUtensorMap& vmap, cudaStream_t s) {
+    // more than 64 query rows per kv head: groups of 64 rows in separate CTAs (each keeps the
+    // 64-row configuration's ring; the K / V tiles they share are read from HBM about once)
+    AttnArgs a = a0;
+    a.rgroups = (a.nq + 63) / 64;
     attn_append_kernel<<<dim3(a.B, a.L), 256, 0, s>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const int nqp = a.nq <= 32 ? 32 : a.nq <= 64 ? 64 : 128;
+    const int nqp = a.nq <= 32 ? 32 : 64;
     if (a.D == 128)
-        e = nqp == 32 ? launch_attn_t<128, 32>(a, kmap, vmap, s)
-          : nqp == 64 ? launch_attn_t<128, 64>(a, kmap, vmap, s)
-                      : launch_attn_t<128, 128>(a, kmap, vmap, s);
+        e = nqp == 32 ? launch_attn_t<128, 32>(a, kmap, vmap, s) : launch_attn_t<128, 64>(a, kmap, vmap, s);
     else
-        e = nqp == 32 ? launch_attn_t<256, 32>(a, kmap, vmap, s)
-          : nqp == 64 ? launch_attn_t<256, 64>(a, kmap, vmap, s)
-                      : launch_attn_t<256, 128>(a, kmap, vmap, s);
+        e = nqp == 32 ? launch_attn_t<256, 32>(a, kmap, vmap, s) : launch_attn_t<256, 64>(a, kmap, vmap, s);
     if (e != cudaSuccess || a.splits == 1) return e;
     attn_combine_kernel<<<dim3(a.units, a.nq), a.D, 0, s>>>(a);
     return cudaGetLastError();

@@ -311,6 +311,8 @@ ATTN_WORKLOADS = {
                                        D=256, ctx=4224, lengths=(4096,)),
     "qwen36_attn_b1_n8": AttnWorkload("qwen36_attn_b1_n8", L=10, B=1, T=8, Hq=16, Hkv=2, D=256,
                                       ctx=4224, lengths=(4096,)),
+    "qwen36_attn_b16_n16": AttnWorkload("qwen36_attn_b16_n16", L=10, B=16, T=16, Hq=16, Hkv=2,
+                                        D=256, ctx=4224, lengths=(4096,)),
 }
 
 
