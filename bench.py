@@ -151,7 +151,7 @@ KERNEL_SOURCES = {
                             "common.cuh", "kernels.h"),
     "gdn_rollback": ("rollback.cu", "common.cuh", "kernels.h"),
     "spec_accept": ("accept.cu", "common.cuh", "kernels.h"),
-    "attn_verify": ("attn.cu", "tc.cuh", "common.cuh", "kernels.h"),
+    "attn_verify": ("attn.cu", "attn.h", "tc.cuh", "common.cuh"),
 }
 
 

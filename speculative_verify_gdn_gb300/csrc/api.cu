@@ -10,6 +10,7 @@
 
 #include "../../include/gdnspec.h"
 #include "kernels.h"
+#include "attn.h"
 
 namespace {
 

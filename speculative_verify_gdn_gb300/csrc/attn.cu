@@ -40,6 +40,7 @@
 // work, lets its copies land, waits for its tensor-core work and frees its TMEM.
 #include "common.cuh"
 #include "kernels.h"
+#include "attn.h"
 #include "tc.cuh"
 
 namespace gdn {
