@@ -1,4 +1,5 @@
-"""CPU oracle for speculative verify / accept / rollback on GatedDeltaNet layers.
+"""CPU oracle for speculative verify / accept / rollback on GatedDeltaNet layers, and for the
+hybrid's attention layers in the verify step (KV append + causal attention, KV truncation).
 
 Test infrastructure only: tests, the smoke check and the bench's CPU-baseline leg use it; the
 library never does. See oracle.c for what each function computes and which page it follows.

@@ -28,7 +28,9 @@
  * written here in its innovation form u = g_t S k_t, δ_t = β_t (v_t − u), S ← g_t S + δ_t k_tᵀ,
  * which is exactly the form the [GDN] §4 replay rule replays.
  *
- * Parity pins (tests/test_oracle_pins.py) cover every function below; none is unpinned.
+ * Parity pins cover every function below; none is unpinned: tests/test_oracle_pins.py (verify,
+ * rollback, accept, the sampling contract), tests/test_gate_dk.py (per-key-channel gates),
+ * tests/test_attn_oracle.py (attention verify and truncation).
  */
 #include "oracle.h"
 
