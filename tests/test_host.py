@@ -120,3 +120,24 @@ def test_two_rank_gloo_bench_logic():
     assert s0 != s1 and x0 != x1                 # distinct sequences per rank
     assert t0 == t1 == 11.0                      # max over ranks
     assert v0 == v1 == pytest.approx(2 * 2 * 4 / 11e-3)
+
+
+def test_reference_arm_json_line():
+    """`bench.py --impl reference` (the oracle on the host cores) prints one JSON line with the
+    contract's keys, on the default workload's metric and unit."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference",
+                        "--steps", "1", "--warmup", "0"], capture_output=True, text=True,
+                       timeout=600, cwd=root)
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config", "e2e",
+                "cpu_baseline"):
+        assert key in line, key
+    assert line["impl"] == "reference" and line["metric"] == bench.METRIC
+    assert line["value"] > 0 and line["e2e"]["h2d_bytes_per_step"] == 0
+    assert line["cpu_baseline"]["kind"] == "oracle"
