@@ -29,7 +29,13 @@
  *    return nothing was enqueued. Host-side argument checks never touch the GPU.
  *  - `status` (optional, may be NULL): one device uint32_t. Kernels OR GDN_STATUS_* bits into it
  *    when they meet an out-of-range device value (an accepted count, a parent index, a token);
- *    the offending unit is skipped. Kernels never trap. Read it after synchronising the stream.
+ *    the offending unit is skipped. Kernels never trap. Read it after synchronising the stream;
+ *    gdn_status_check() maps a non-zero word to GDN_ERR_DEVICE_STATUS with a readable message.
+ *  - GDN_STATUS_WAIT_TIMEOUT means a bounded on-chip wait gave up (every mbarrier / copy wait in
+ *    the kernels is limited to about one second of wall time instead of spinning forever). After
+ *    it, every output of that call — of every unit, not only the one that timed out — is
+ *    undefined and must be discarded: a unit that gave up may have left a copy in flight into
+ *    shared memory that a later unit on the same SM then reuses.
  */
 #ifndef GDNSPEC_H
 #define GDNSPEC_H
@@ -52,6 +58,7 @@ extern "C" {
 #define GDN_ERR_INVALID_ARG   1  /* null pointer, negative or inconsistent size, misalignment */
 #define GDN_ERR_UNSUPPORTED   2  /* valid but not built: head dims, T, W outside the kernel set */
 #define GDN_ERR_CUDA          3  /* a CUDA launch or attribute call failed (message has the name) */
+#define GDN_ERR_DEVICE_STATUS 4  /* gdn_status_check: the kernels reported a device-side problem */
 
 /* ---- device status bits (OR-ed into *status by the kernels) ----------------------------- */
 #define GDN_STATUS_BAD_NACC    0x1u  /* rollback: accepted count outside [0, T] */
@@ -290,8 +297,9 @@ GDN_API int spec_accept_tree(const spec_dims* d, const void* logits, const int32
  *    GDN_ERR_UNSUPPORTED (use spec_accept with a workspace instead);
  *  - all calls on a device share the array: calls whose kernels may overlap on the GPU (different
  *    streams without ordering) race and must not be issued;
- *  - the first call on each device looks up the array's device address with that device current;
- *    make that first call outside of any stream capture.
+ *  - the first call on each device looks up the array's device address with that device current,
+ *    and looks it up again once the device's context has changed (after cudaDeviceReset); make
+ *    the first call on a device, and the first after a reset, outside of any stream capture.
  */
 #define GDN_STATIC_SCRATCH_BYTES (1u << 20)
 GDN_API int spec_accept_static(const spec_dims* d, const void* logits, const int32_t* drafts,
@@ -301,6 +309,13 @@ GDN_API int spec_accept_static(const spec_dims* d, const void* logits, const int
 
 /* Thread-local message for the last non-OK return on this thread ("" if none). */
 GDN_API const char* gdn_last_error(void);
+
+/*
+ * gdn_status_check — host-side mapping of a device status word (read back after synchronising the
+ * stream the calls ran on) to a return code: GDN_OK for 0, else GDN_ERR_DEVICE_STATUS with the
+ * names of the set GDN_STATUS_* bits in gdn_last_error(). Touches no GPU.
+ */
+GDN_API int gdn_status_check(uint32_t status_word);
 
 /* ---- full-attention layers of the hybrid ------------------------------------------------ */
 /*

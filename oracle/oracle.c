@@ -235,10 +235,15 @@ int oracle_rollback(const oracle_dims* dm, const int32_t* path, int P, const int
  * Greedy acceptance ([XS] §2 algorithm; [COL] §5 greedy path). Row i judges draft i; row N is
  * the bonus row. argmax returns the lowest index among equal maxima.
  * ------------------------------------------------------------------------------------------ */
+/* A NaN logit counts as −∞: it is never the maximum unless every entry is NaN or −∞, and then
+ * the lowest index (0) is returned, like any tie. */
+static float logit_or_neg_inf(float x) { return isnan(x) ? -INFINITY : x; }
+
 int oracle_argmax(const float* row, int V) {
     int best = 0;
+    float m = logit_or_neg_inf(row[0]);
     for (int v = 1; v < V; ++v)
-        if (row[v] > row[best]) best = v;
+        if (logit_or_neg_inf(row[v]) > m) { best = v; m = logit_or_neg_inf(row[v]); }
     return best;
 }
 
@@ -290,7 +295,8 @@ static void init_coefs(void) {
 float oracle_exp2_spec(float x) {
     if (!g_coef_ready) init_coefs();
     float n = rintf(x);                    /* round to nearest, ties to even */
-    if (n < -64.0f) return 0.0f;           /* 2^x < 2^-63.5: weight 0 either way */
+    if (!(n >= -64.0f)) return 0.0f;       /* 2^x < 2^-63.5, or x NaN (a NaN or −∞ logit
+                                              against a −∞ maximum): weight 0 */
     float f = x - n;                       /* exact */
     float p = g_coef[7];
     for (int k = 6; k >= 0; --k) p = fmaf(p, f, g_coef[k]);
@@ -303,12 +309,13 @@ float oracle_scale_c(float temperature) {
 
 /* weights of one row; ban < 0 for none. Returns Z = Σ w. */
 uint64_t oracle_weights(const float* row, int V, float c, int ban, uint64_t* w) {
-    float m = row[0];
+    /* NaN logits count as −∞ (weight 0), as in oracle_argmax */
+    float m = logit_or_neg_inf(row[0]);
     for (int v = 1; v < V; ++v)
-        if (row[v] > m) m = row[v];
+        if (logit_or_neg_inf(row[v]) > m) m = logit_or_neg_inf(row[v]);
     uint64_t Z = 0;
     for (int v = 0; v < V; ++v) {
-        float dlt = row[v] - m;
+        float dlt = logit_or_neg_inf(row[v]) - m;
         float x = dlt * c;
         float e = oracle_exp2_spec(x);
         uint64_t wv = (uint64_t)(e * 4294967296.0f);   /* e * 2^32 is exact; truncation = floor */

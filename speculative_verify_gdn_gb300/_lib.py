@@ -14,6 +14,7 @@ import torch
 from . import build as _build
 
 GDN_OK = 0
+GDN_ERR_DEVICE_STATUS = 4
 GDN_DTYPE_F32 = 0
 GDN_DTYPE_BF16 = 1
 SPEC_MODE_GREEDY = 0
@@ -33,7 +34,7 @@ STATUS_BITS = {
 EXPORTS = ("gdn_verify", "gdn_verify_tree", "gdn_rollback", "gdn_rollback_path",
            "gdn_rollback_verify", "gdn_tape_bytes", "spec_accept", "spec_workspace_bytes", "spec_accept_tree",
            "spec_accept_static", "spec_stats_accumulate", "attn_verify", "attn_workspace_bytes",
-           "attn_truncate", "gdn_last_error")
+           "attn_truncate", "gdn_last_error", "gdn_status_check")
 
 
 class GdnError(RuntimeError):
@@ -103,6 +104,8 @@ def load(require_file=True):
     lib.attn_truncate.restype = ct.c_int
     lib.gdn_last_error.argtypes = []
     lib.gdn_last_error.restype = ct.c_char_p
+    lib.gdn_status_check.argtypes = [ct.c_uint32]
+    lib.gdn_status_check.restype = ct.c_int
     _lib = lib
     return lib
 
@@ -339,6 +342,12 @@ def spec_accept_tree(logits, parent, tokens, path, n_acc, out_tokens, workspace,
 def decode_status(value):
     value = int(value) & 0xFFFFFFFF
     return [name for bit, name in STATUS_BITS.items() if value & bit]
+
+
+def status_check(value):
+    """Raises GdnError (the library's GDN_ERR_DEVICE_STATUS message) for a non-zero status word
+    read back after synchronising; host only."""
+    _check(load().gdn_status_check(int(value) & 0xFFFFFFFF), "device status")
 
 
 # ------------------------------------------------------------------ attention layers

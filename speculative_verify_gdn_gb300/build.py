@@ -51,8 +51,7 @@ def build(force=False, verbose_ptxas=False, jobs=None):
     os.makedirs(OBJ_DIR, exist_ok=True)
     os.makedirs(LIB_DIR, exist_ok=True)
     flags = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
-                    "-Xcompiler", "-fvisibility=hidden", "--use_fast_math=false"]
-    flags = [f for f in flags if f != "--use_fast_math=false"]
+                    "-Xcompiler", "-fvisibility=hidden"]
     if verbose_ptxas:
         flags += ["-Xptxas", "-v"]
 

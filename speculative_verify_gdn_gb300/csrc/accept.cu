@@ -10,6 +10,7 @@
 //
 // Structure (HBM-bound: every logits row is read once, sampling re-reads it from L2):
 //   K1 rowmax   grid (rows, chunks): chunk argmax, lowest index on ties, as a packed u64 key.
+//               A NaN logit is never taken (it counts as −∞); a row of NaN / −∞ gives index 0.
 //   K2 weights  grid (rows, chunks): chunk weight sums (u64) and the draft token's weight.
 //   K3 scan     one CTA per sequence: the sequential accept decisions of the pages' loop; a
 //               rejection or the bonus searches one chunk for the sampled token.
@@ -71,9 +72,11 @@ __device__ __forceinline__ int key_index(unsigned long long k) {
 // E), and p · 2^n · 2^32 is exact in fp32, so w = floor(M · 2^(E + n + 9)): a shift, no float to
 // 64-bit conversion. n comes from the bits of x + 1.5·2^23 (round to nearest even, exact for
 // |x| < 2^22).
+// A NaN logit counts as −∞ (weight 0; the row max never is NaN, the argmax pass skips NaN), and so
+// does a NaN x from a −∞ or NaN logit against a −∞ maximum.
 __device__ __forceinline__ unsigned long long weight_of(float l, float m, float c) {
     const float x = __fmul_rn(__fsub_rn(l, m), c);
-    if (x < -100.0f) return 0ull;                       // rint(x) < -64 as well
+    if (!(x >= -100.0f)) return 0ull;                   // rint(x) < -64 as well, or x NaN
     const float t = __fadd_rn(x, 12582912.0f);
     const int n = __float_as_int(t) - 0x4B400000;       // rint(x)
     if (n < -64) return 0ull;

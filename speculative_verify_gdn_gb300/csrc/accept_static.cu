@@ -15,7 +15,10 @@
 //    write every scratch word they read before reading it, so nothing has to start at zero, but two
 //    calls whose kernels overlap on the GPU (different streams, no ordering) race on the array.
 //  - The first call on each device looks up the array's device address (cudaGetSymbolAddress with
-//    that device current); make that first call outside of any stream capture.
+//    that device current) and keeps it for that device's current context; a call made after the
+//    context changed (cudaDeviceReset reloads the module, possibly at another address) looks it up
+//    again. Make the first call on a device, and the first after a reset, outside of any stream
+//    capture.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -28,10 +31,14 @@ namespace {
 __device__ __align__(256) unsigned char g_accept_scratch[GDN_STATIC_SCRATCH_BYTES];
 
 constexpr int kMaxDevices = 64;
+struct ScratchAddr {
+    unsigned long long ctx;   // context the address belongs to (gdn::current_context_id)
+    void* addr;
+};
 std::mutex g_mu;
-void* g_scratch_addr[kMaxDevices] = {};
+ScratchAddr g_scratch[kMaxDevices] = {};
 
-// Device address of the scratch array on the current device (looked up once per device).
+// Device address of the scratch array in the current device's current context.
 int scratch_for_current_device(void** out) {
     int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);
@@ -41,16 +48,20 @@ int scratch_for_current_device(void** out) {
     if (dev < 0 || dev >= kMaxDevices)
         return gdn::report_error(GDN_ERR_UNSUPPORTED, "spec_accept_static: device %d", dev);
     std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_scratch_addr[dev]) {
+    const unsigned long long ctx = gdn::current_context_id();
+    ScratchAddr& slot = g_scratch[dev];
+    if (!slot.addr || !ctx || slot.ctx != ctx) {
         void* p = nullptr;
         e = cudaGetSymbolAddress(&p, g_accept_scratch);
         if (e != cudaSuccess || !p)
             return gdn::report_error(GDN_ERR_CUDA,
                                      "spec_accept_static: cudaGetSymbolAddress failed: %s",
                                      cudaGetErrorString(e));
-        g_scratch_addr[dev] = p;
+        // the lookup makes the device's primary context current if none was
+        slot.ctx = ctx ? ctx : gdn::current_context_id();
+        slot.addr = p;
     }
-    *out = g_scratch_addr[dev];
+    *out = slot.addr;
     return GDN_OK;
 }
 

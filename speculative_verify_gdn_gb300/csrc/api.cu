@@ -440,6 +440,31 @@ int spec_accept_tree(const spec_dims* d, const void* logits, const int32_t* pare
 
 const char* gdn_last_error(void) { return g_err; }
 
+int gdn_status_check(uint32_t status_word) {
+    if (status_word == 0) return GDN_OK;
+    static const struct {
+        uint32_t bit;
+        const char* name;
+    } kBits[] = {{GDN_STATUS_BAD_NACC, "BAD_NACC (accepted count outside [0, T])"},
+                 {GDN_STATUS_BAD_PARENT, "BAD_PARENT (tree parent not in [-1, v))"},
+                 {GDN_STATUS_BAD_TOKEN, "BAD_TOKEN (draft / tree token outside [0, V))"},
+                 {GDN_STATUS_BAD_PATH, "BAD_PATH (path node out of range)"},
+                 {GDN_STATUS_EMPTY_DIST, "EMPTY_DIST (a sampling row with zero total weight)"},
+                 {GDN_STATUS_WAIT_TIMEOUT, "WAIT_TIMEOUT (a bounded wait gave up; discard the outputs)"},
+                 {GDN_STATUS_BAD_LEN, "BAD_LEN (kv_len outside [0, ctx - T])"}};
+    char msg[480];
+    int n = snprintf(msg, sizeof msg, "device status 0x%x:", status_word);
+    uint32_t known = 0;
+    for (const auto& b : kBits) {
+        known |= b.bit;
+        if ((status_word & b.bit) && n > 0 && size_t(n) < sizeof msg)
+            n += snprintf(msg + n, sizeof msg - size_t(n), " %s", b.name);
+    }
+    if ((status_word & ~known) && n > 0 && size_t(n) < sizeof msg)
+        snprintf(msg + n, sizeof msg - size_t(n), " unknown bits 0x%x", status_word & ~known);
+    return fail(GDN_ERR_DEVICE_STATUS, "%s", msg);
+}
+
 int gdn_rollback_verify(const gdn_dims* d, const int32_t* n_acc_prev, const float* tape_delta_prev,
                         const float* tape_k_prev, const float* g_prev, const void* qkv_prev,
                         const void* qkv, const void* conv_w, void* conv_state, const float* g,

@@ -584,13 +584,8 @@ static cudaError_t launch_attn_t(const AttnArgs& a, const CUtensorMap& kmap,
                                  const CUtensorMap& vmap, cudaStream_t s) {
     using Cfg = AttnCfg<D, NQ>;
     auto kern = attn_verify_kernel<D, NQ>;
-    static bool attr_done = false;   // benign race: setting the attribute twice is harmless
-    if (!attr_done) {
-        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   int(Cfg::SMEM));
-        if (e != cudaSuccess) return e;
-        attr_done = true;
-    }
+    const cudaError_t e = smem_optin(reinterpret_cast<const void*>(kern), Cfg::SMEM);
+    if (e != cudaSuccess) return e;
     kern<<<unsigned(a.units) * unsigned(a.splits) * unsigned(a.rgroups), Cfg::NTHR, Cfg::SMEM, s>>>(
         a, kmap, vmap);
     return cudaGetLastError();

@@ -94,6 +94,15 @@ struct AcceptArgs {
     uint32_t* status;
 };
 
+// Opts `kernel` in to `bytes` of dynamic shared memory in the current context (remembered per
+// context and kernel under a mutex, so a second GPU or a reset device is set up again).
+cudaError_t smem_optin(const void* kernel, size_t bytes);
+// SM count of the current device (looked up once per device).
+cudaError_t device_sm_count(int* n);
+// Unique id (+1) of the calling thread's current CUDA context; 0 if none is current or the
+// driver does not expose it.
+unsigned long long current_context_id();
+
 // Sets the calling thread's gdn_last_error() message and returns `code`.
 int report_error(int code, const char* fmt, ...);
 

@@ -217,12 +217,8 @@ template <typename IO, int D, int NMAX, bool PATH>
 static cudaError_t launch_rb(const RollbackArgs& a, cudaStream_t s) {
     constexpr size_t SMEM = RbSmem<D, NMAX>::BYTES;
     auto kern = gdn_rollback_kernel<IO, D, NMAX, PATH>;
-    static bool attr_done = false;   // benign race: setting the attribute twice is harmless
-    if (!attr_done) {
-        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(SMEM));
-        if (e != cudaSuccess) return e;
-        attr_done = true;
-    }
+    const cudaError_t e = smem_optin(reinterpret_cast<const void*>(kern), SMEM);
+    if (e != cudaSuccess) return e;
     dim3 grid(a.Hv, a.B, a.L);
     kern<<<grid, 256, SMEM, s>>>(a);
     return cudaGetLastError();

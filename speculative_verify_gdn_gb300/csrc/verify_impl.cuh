@@ -660,13 +660,8 @@ cudaError_t launch_verify_t(const VerifyArgs& a, const CUtensorMap& map, cudaStr
     auto kern = gdn_verify_kernel<IO, D, TMAX, TREE, GDK>;
     const size_t smem = Cfg::smem_bytes(a.T, a.W);
     if (smem > 227 * 1024) return cudaErrorInvalidValue;
-    static int attr_set = 0;   // largest size configured so far (benign race: idempotent)
-    if (int(smem) > attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             int(smem));
-        if (e != cudaSuccess) return e;
-        attr_set = int(smem);
-    }
+    const cudaError_t e = smem_optin(reinterpret_cast<const void*>(kern), smem);
+    if (e != cudaSuccess) return e;
     dim3 grid(a.Hv, a.B, a.L);
     kern<<<grid, Cfg::NTHR, smem, stream>>>(a, map);
     return cudaGetLastError();

@@ -1752,19 +1752,11 @@ template <typename IO, int TMAX, int G, bool COMMIT, bool TREE = false>
 cudaError_t launch_verify_pipe_t(const VerifyArgs& a, const VerifyMaps& m, cudaStream_t stream) {
     using Cfg = PipeCfg<IO, TMAX, G, COMMIT, TREE>;
     auto kern = gdn_verify_pipe_kernel<IO, TMAX, G, COMMIT, TREE>;
-    static bool attr_done = false;   // benign race: setting the attribute twice is harmless
-    static int nsm = 0;
-    if (!attr_done) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             int(Cfg::SMEM));
-        if (e != cudaSuccess) return e;
-        int dev = 0;
-        e = cudaGetDevice(&dev);
-        if (e != cudaSuccess) return e;
-        e = cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess) return e;
-        attr_done = true;
-    }
+    cudaError_t e = smem_optin(reinterpret_cast<const void*>(kern), Cfg::SMEM);
+    if (e != cudaSuccess) return e;
+    int nsm = 0;
+    e = device_sm_count(&nsm);
+    if (e != cudaSuccess) return e;
     const int n_units = a.L * a.B * a.Hk;
     const int grid = n_units < nsm ? n_units : nsm;
     kern<<<grid, Cfg::NTHR, Cfg::SMEM, stream>>>(a, m.state, m.qkv, m.conv_state,

@@ -123,6 +123,4 @@ class SpecRound:
 
     def check_status(self):
         torch.cuda.synchronize(self.device)
-        v = int(self.status.item())
-        if v:
-            raise _lib.GdnError("device status 0x%x: %s" % (v, _lib.decode_status(v)))
+        _lib.status_check(int(self.status.item()))

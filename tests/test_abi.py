@@ -206,3 +206,15 @@ def test_value_cache_tile_layout():
         for d in (0, 7, 15):
             assert vt[1, 2, j // 128, d, j % 128] == v[1, 2, j, d]
     assert torch.equal(_lib.v_from_vt(vt), v)
+
+
+def test_status_check_maps_device_bits_to_an_error(lib):
+    assert lib.gdn_status_check(0) == _lib.GDN_OK
+    assert lib.gdn_status_check(0x1 | 0x20) == _lib.GDN_ERR_DEVICE_STATUS
+    msg = _lib.last_error()
+    assert "BAD_NACC" in msg and "WAIT_TIMEOUT" in msg and "BAD_TOKEN" not in msg
+    assert lib.gdn_status_check(0x80000000) == _lib.GDN_ERR_DEVICE_STATUS
+    assert "unknown bits 0x80000000" in _lib.last_error()
+    with pytest.raises(_lib.GdnError, match="BAD_PATH"):
+        _lib.status_check(0x8)
+    _lib.status_check(0)

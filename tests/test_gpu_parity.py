@@ -211,6 +211,52 @@ def test_accept_bad_draft_token(gdnlib):
     assert np.array_equal(r.out_tokens.cpu().numpy(), out_ref)
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_accept_nan_logits(gdnlib, dtype):
+    """NaN logits count as −∞ on both sides: greedy never picks one (a row of NaN / −∞ gives
+    index 0), sampling gives it weight 0. Token ids and counts bit-exact with the oracle."""
+    B, N, V = 8, 3, 1000
+    gen = torch.Generator().manual_seed(5)
+    lg = torch.randn(B, N + 1, V, generator=gen).to(dtype)
+    nan, inf = float("nan"), float("inf")
+    lg[0, 0, 0] = nan
+    lg[0, 1, :17] = nan
+    lg[1, 0, int(lg[1, 0].float().argmax())] = nan       # the maximum itself becomes NaN
+    lg[2, 2, :] = nan                                     # a whole NaN row
+    lg[3, 1, :] = -inf
+    lg[3, 1, 500:] = nan                                  # a row of −∞ and NaN
+    lg[4, 3, 1::2] = nan
+    lg[5, :, 900:] = nan                                  # NaN tail across the chunks
+    lf = logits_f32(lg)
+    am = np.array([[oracle.argmax(lf[b, i]) for i in range(N + 1)] for b in range(B)])
+    dr = torch.from_numpy(am[:, :N].astype(np.int32))
+    dr[6, 1] = (dr[6, 1] + 1) % V
+    dlg, ddr = to_dev(lg, dr)
+    n_acc = torch.empty(B, dtype=torch.int32, device="cuda")
+    out = torch.empty(B, N + 1, dtype=torch.int32, device="cuda")
+    ws = torch.empty(_lib.workspace_bytes(B, N, V, _lib.SPEC_MODE_GREEDY, dtype), dtype=torch.uint8,
+                     device="cuda")
+    _lib.spec_accept(dlg, ddr, n_acc, out, ws)
+    torch.cuda.synchronize()
+    n_ref, out_ref, _ = oracle.accept_greedy(lf, dr.numpy())
+    assert np.array_equal(n_acc.cpu().numpy(), n_ref)
+    assert np.array_equal(out.cpu().numpy(), out_ref)
+    ws = torch.empty(_lib.workspace_bytes(B, N, V, _lib.SPEC_MODE_SAMPLE, dtype), dtype=torch.uint8,
+                     device="cuda")
+    for rnd in range(4):
+        _lib.spec_accept(dlg, ddr, n_acc, out, ws, mode=_lib.SPEC_MODE_SAMPLE, temperature=0.7,
+                         seed=13, round_=rnd)
+        torch.cuda.synchronize()
+        n_ref, out_ref, _ = oracle.accept_sample(lf, dr.numpy(), 0.7, 13, rnd)
+        assert np.array_equal(n_acc.cpu().numpy(), n_ref)
+        assert np.array_equal(out.cpu().numpy(), out_ref)
+        tok = out.cpu().numpy()
+        for b in range(B):
+            for i in range(N + 1):
+                if tok[b, i] >= 0:
+                    assert not np.isnan(lf[b, i, tok[b, i]])
+
+
 # ------------------------------------------------------------------------------ sampling accept
 @pytest.mark.parametrize("V,B,N", [(4096, 16, 16), (151936, 16, 16), (1000, 5, 0), (333, 9, 3)])
 def test_sample_accept_bit_exact(gdnlib, V, B, N):

@@ -473,6 +473,93 @@ def test_tree_matches_chain_along_every_path():
             assert np.array_equal(tr["node_state"][:, b, path], ch["node_state"][:, 0])
 
 
+def root_to_leaf(par_b, leaf):
+    path, u = [], int(leaf)
+    while u >= 0:
+        path.append(u)
+        u = int(par_b[u])
+    return path[::-1]
+
+
+@pytest.mark.parametrize("gate_dk", [False, True])
+def test_path_rollback_equals_chain_over_the_path(gate_dk):
+    """GDN investigation §4 tape replay along an accepted tree path (§2.2 tree verification):
+    restoring the snapshot and replaying the tape of nodes path[0..n-1] equals the sequential
+    recurrence run over only those nodes' rows, bit for bit (the same expression in the same
+    order), and equals the tree verify's own state of node path[n-1]; the conv state becomes the
+    last W-1 rows of conv_state ++ qkv[path[:n]] (the path nodes' raw rows, not rows 0..n-1)."""
+    rng = np.random.default_rng(60 + int(gate_dk))
+    T, L, B, Hk, Hv, D, W, depth = 13, 2, 3, 1, 2, 5, 4, 6
+    dims, x = rand_inputs(rng, L=L, B=B, T=T, Hk=Hk, Hv=Hv, D=D, W=W)
+    if gate_dk:
+        x["g"] = np.exp(-np.logaddexp(0.0, rng.standard_normal((L, B, T, Hv, D))))
+    par = np.stack([tree_parents(rng, T, depth, 3) for _ in range(B)])
+    tr = oracle.verify(dims, parent=par, node_states=True, **x)
+    # each sequence accepts a path to a random leaf that is not the creation-order chain 0,1,2..
+    paths = []
+    for b in range(B):
+        leaves = [v for v in range(T) if v not in par[b]]
+        cand = [lf for lf in leaves if root_to_leaf(par[b], lf) != list(range(len(root_to_leaf(par[b], lf))))]
+        paths.append(root_to_leaf(par[b], rng.choice(cand if cand else leaves)))
+    assert any(p != list(range(len(p))) for p in paths)
+    P = depth
+    pth = np.full((B, P), -1, np.int32)
+    for b, p in enumerate(paths):
+        pth[b, :len(p)] = p
+    cuts = [sorted({0, 1, len(p) - 1, len(p)}) for p in paths]
+    for k in range(4):
+        n_acc = np.array([c[min(k, len(c) - 1)] for c in cuts], np.int32)
+        st, cs, bad = oracle.rollback(dims, n_acc, tr["tape_delta"], tr["tape_k"], x["g"],
+                                      x["qkv"], x["state"], x["conv_state"], path=pth)
+        assert bad == 0
+        for b, n in enumerate(n_acc):
+            n = int(n)
+            if n == 0:
+                assert np.array_equal(st[:, b], x["state"][:, b])
+                assert np.array_equal(cs[:, b], x["conv_state"][:, b])
+                continue
+            nodes = paths[b][:n]
+            # the tree verify's state of the last accepted node
+            assert np.array_equal(st[:, b], tr["node_state"][:, b, nodes[-1]])
+            # the chain recurrence over only the path nodes' rows
+            sub = OracleDims(L=L, B=1, T=n, Hk=Hk, Hv=Hv, Dk=D, Dv=D, W=W)
+            xs = dict(qkv=x["qkv"][:, b:b + 1, nodes], g=x["g"][:, b:b + 1, nodes],
+                      beta=x["beta"][:, b:b + 1, nodes], conv_state=x["conv_state"][:, b:b + 1],
+                      state=x["state"][:, b:b + 1], conv_w=x["conv_w"])
+            ch = oracle.verify(sub, node_states=True, **xs)
+            assert np.array_equal(st[:, b], ch["node_state"][:, 0, n - 1])
+            xh = np.concatenate([x["conv_state"][:, b], x["qkv"][:, b, nodes]], axis=1)
+            assert np.array_equal(cs[:, b], xh[:, -(W - 1):])
+
+
+def test_path_rollback_rejects_bad_nodes_and_counts():
+    """A path node outside [0, T) sets bit 8, a count beyond the path capacity bit 1; either
+    leaves that sequence's state and conv state untouched while the others commit."""
+    rng = np.random.default_rng(62)
+    T, depth = 8, 4
+    dims, x = rand_inputs(rng, L=1, B=3, T=T, Hk=1, Hv=2, D=4)
+    par = np.stack([tree_parents(rng, T, depth, 3) for _ in range(3)])
+    tr = oracle.verify(dims, parent=par, **x)
+    pth = np.full((3, depth), -1, np.int32)
+    for b in range(3):
+        p = root_to_leaf(par[b], [v for v in range(T) if v not in par[b]][0])
+        pth[b, :len(p)] = p
+    pth[0, 1] = T                     # out of range node
+    n_acc = np.array([2, 1, depth + 1], np.int32)
+    st, cs, bad = oracle.rollback(dims, n_acc, tr["tape_delta"], tr["tape_k"], x["g"], x["qkv"],
+                                  x["state"], x["conv_state"], path=pth)
+    assert bad == (8 | 1)
+    for b in (0, 2):
+        assert np.array_equal(st[:, b], x["state"][:, b])
+        assert np.array_equal(cs[:, b], x["conv_state"][:, b])
+    assert not np.array_equal(st[:, 1], x["state"][:, 1])
+    pth[0, 1] = -2                    # negative node
+    st, cs, bad = oracle.rollback(dims, np.array([2, 0, 0], np.int32), tr["tape_delta"],
+                                  tr["tape_k"], x["g"], x["qkv"], x["state"], x["conv_state"],
+                                  path=pth)
+    assert bad == 8 and np.array_equal(st, x["state"]) and np.array_equal(cs, x["conv_state"])
+
+
 def test_chain_shaped_tree_equals_chain():
     rng = np.random.default_rng(41)
     dims, x = rand_inputs(rng, L=1, B=2, T=5)
@@ -527,3 +614,25 @@ def test_all_accepted_probability_matches_printed_values():
         sd = np.sqrt(a ** N * (1 - a ** N) / w.B)
         assert abs(frac - a ** N) < 5 * sd
     del torch
+
+
+# ------------------------------------------------------------------------------ NaN logits
+def test_nan_logits_count_as_negative_infinity():
+    """The one NaN rule of both sides: a NaN logit is never the argmax (a row of NaN / −∞ gives
+    index 0, like a tie) and has sampling weight 0."""
+    nan, inf = np.float32("nan"), np.float32("inf")
+    row = np.array([nan, 1.0, 3.0, nan, 3.0, -2.0], np.float32)
+    assert oracle.argmax(row) == 2
+    assert oracle.argmax(np.full(7, nan, np.float32)) == 0
+    assert oracle.argmax(np.array([nan, -inf, nan, -inf], np.float32)) == 0
+    assert oracle.argmax(np.array([nan, nan, -5.0, nan], np.float32)) == 2
+    lg = np.stack([row, np.where(np.isnan(row), -inf, row)])[None]         # [1, 2, 6]
+    # greedy: the NaN row behaves as the row with −∞ in place of each NaN
+    n, out, _ = oracle.accept_greedy(lg, np.array([[2]], np.int32))
+    assert n[0] == 1 and list(out[0]) == [2, 2]
+    # sampling: the NaN positions are never drawn, and the two rows give the same draws
+    for seed in range(200):
+        a = oracle.accept_sample(lg[:, :1].repeat(2, 1), np.array([[1]], np.int32), 0.7, seed, 0)
+        b = oracle.accept_sample(lg[:, 1:].repeat(2, 1), np.array([[1]], np.int32), 0.7, seed, 0)
+        assert np.array_equal(a[1], b[1]) and a[0][0] == b[0][0]
+        assert not np.isnan(row[a[1][0, 0]])
