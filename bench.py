@@ -129,9 +129,15 @@ def bytes_rollback_verify(w, n_list):
     return bytes_verify(w) + w.L * tot + 4 * w.B
 
 
-def bytes_accept(w):
+def bytes_accept(w, n_list):
+    """Algorithmic bytes of one accept call: the logits rows the accept loop reaches, n + 1 per
+    sequence for n accepted drafts (rows 0..n: the judged drafts and the row of the correction,
+    resample or bonus), plus the drafts read and the tokens and counts written. The greedy kernels
+    read all N + 1 rows in parallel; the sampling kernel reads only the rows it reaches (and
+    prefetches one more)."""
     io = 2 if str(w.io_dtype).endswith("bfloat16") else 4
-    return w.B * (w.N + 1) * w.V * io + 4 * w.B * (2 * w.N + 2)
+    rows = sum(int(n) + 1 for n in n_list)
+    return rows * w.V * io + 4 * w.B * (2 * w.N + 2)
 
 
 def read_peaks():
@@ -418,7 +424,7 @@ def run_gpu(args, w, world, rank, device):
     nl = nlog.cpu().numpy()
 
     peak, peak_kind = read_peaks()
-    ba = bytes_accept(w)
+    ba = statistics.mean(bytes_accept(w, nl[k]) for k in range(K))
     if fused:
         nprev = [nlog0.cpu().numpy()] + [nl[k] for k in range(K - 1)]
         brv = [bytes_rollback_verify(w, nprev[k]) for k in range(K)]
@@ -799,7 +805,7 @@ def run_hybrid(args):
     nl = nlog.cpu().numpy()
     peak, peak_kind = read_peaks()
     by = {"gdn_verify": bytes_verify(w), "attn_verify": bytes_attn(aw, kv_base.tolist()),
-          "spec_accept": bytes_accept(w),
+          "spec_accept": statistics.mean(bytes_accept(w, nl[k]) for k in range(K)),
           "gdn_rollback": statistics.mean(bytes_rollback(w, nl[k]) for k in range(K)),
           "attn_truncate": 8 * w.B}
     kern = {n: {"ms": t[n], "bytes": by[n], "GBps": by[n] / (t[n] / 1e3) / 1e9,

@@ -16,6 +16,10 @@
 //               rejection or the bonus searches one chunk for the sampled token.
 // Every vocabulary row is split into CH chunks of CS elements; rows start on 16-byte boundaries
 // and are read with 16-byte vector loads.
+#include <map>
+#include <mutex>
+#include <tuple>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -68,18 +72,18 @@ __device__ __forceinline__ int key_index(unsigned long long k) {
 // The integer weight w = floor(2^32 · 2^x), x = (l − m)·c ≤ 0, with this library's 2^x: Cody–Waite
 // reduction x = n + f (n = rint(x), f in [-1/2, 1/2]), the degree-7 Taylor polynomial p of 2^f
 // (coefficients (ln 2)^k / k! rounded to fp32, Horner with fused multiply-adds), 2^x = p · 2^n,
-// zero for n < -64. p lies in [2^-1/2, 2^1/2] (a normal fp32 with 24-bit significand M, exponent
-// E), and p · 2^n · 2^32 is exact in fp32, so w = floor(M · 2^(E + n + 9)): a shift, no float to
-// 64-bit conversion. n comes from the bits of x + 1.5·2^23 (round to nearest even, exact for
-// |x| < 2^22).
-// A NaN logit counts as −∞ (weight 0; the row max never is NaN, the argmax pass skips NaN), and so
-// does a NaN x from a −∞ or NaN logit against a −∞ maximum.
+// zero for n < -64. p lies in [2^-1/2, 1] (a normal fp32 with 24-bit significand M and biased
+// exponent E), and p · 2^n · 2^32 is exact in fp32, so w = floor(M · 2^sh), sh = E − 127 + n + 9,
+// a shift with no float-to-integer conversion: with a = M · 2^8 (32 bits), w = a >> (8 − sh) for
+// sh ≤ 8 (a right shift by 32 or more gives 0, which covers n < -64), and w = 2a for sh = 9 (p = 1,
+// n = 0: the row maximum). n comes from the bits of x + 1.5·2^23 (round to nearest even, exact
+// for |x| < 2^22; x is clamped to [-100, 0] first, where every weight is 0 below -64.5).
+// A NaN logit counts as −∞ (weight 0: fmaxf turns a NaN x into -100), and so does a NaN x from a
+// −∞ or NaN logit against a −∞ maximum. The row max never is NaN (the max passes skip NaN).
 __device__ __forceinline__ unsigned long long weight_of(float l, float m, float c) {
-    const float x = __fmul_rn(__fsub_rn(l, m), c);
-    if (!(x >= -100.0f)) return 0ull;                   // rint(x) < -64 as well, or x NaN
+    const float x = fmaxf(__fmul_rn(__fsub_rn(l, m), c), -100.0f);
     const float t = __fadd_rn(x, 12582912.0f);
     const int n = __float_as_int(t) - 0x4B400000;       // rint(x)
-    if (n < -64) return 0ull;
     const float f = __fsub_rn(x, __fsub_rn(t, 12582912.0f));
     float p = 0x1.ffcbfcp-17f;
     p = __fmaf_rn(p, f, 0x1.430912p-13f);
@@ -90,9 +94,11 @@ __device__ __forceinline__ unsigned long long weight_of(float l, float m, float 
     p = __fmaf_rn(p, f, 0x1.62e430p-1f);
     p = __fmaf_rn(p, f, 1.0f);
     const uint32_t pb = __float_as_uint(p);
-    const unsigned long long M = (pb & 0x7FFFFFu) | 0x800000u;
-    const int sh = int(pb >> 23) - 127 + n + 9;
-    return sh >= 0 ? (M << sh) : (M >> (-sh));
+    const uint32_t a = (pb << 8) | 0x80000000u;          // M · 2^8
+    const int s = 126 - int(pb >> 23) - n;              // 8 − sh, >= -1
+    uint32_t w;
+    asm("shr.b32 %0, %1, %2;" : "=r"(w) : "r"(a), "r"(s));   // amounts >= 32 give 0
+    return s < 0 ? (static_cast<unsigned long long>(a) << 1) : static_cast<unsigned long long>(w);
 }
 
 // Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11), counter (c0..c3), key (k0, k1).
@@ -516,6 +522,443 @@ __global__ void __launch_bounds__(kAccThreads) accept_tree_scan_kernel(const Acc
     }
 }
 
+// ---------------------------------------------------------------- sampling: one cluster per sequence
+// The accept loop looks at row i only once drafts 0..i-1 were accepted, so only the rows up to the
+// first rejection (or the bonus row) need their weights. One cluster of CL CTAs per sequence walks
+// the rows in that order. CTA k of the cluster keeps the vocabulary slice [k·SL, (k+1)·SL) of the
+// current row in shared memory, each thread a contiguous run of K 16-byte vectors of it (K odd:
+// the run stride then spreads a quarter warp's 16-byte reads over all banks).
+//
+// Each row's slice arrives by TMA bulk copies (one thread issues them; the wait on their mbarrier
+// is bounded) into one of two stages, the next row's while the current one is weighed.
+//
+// One cluster barrier per row. Before barrier r every CTA publishes, into a slot of every peer's
+// shared memory, its weight sum and draft weight of row r-1 and its maximum of row r (whose slice
+// was prefetched while row r-1 was being weighed). After the barrier every thread of every CTA
+// takes the same accept decision on row r-1 from the same slots; an accepted row r-1 frees its
+// stage for the prefetch of row r+1, and row r's weights follow at once (its maximum is known). A
+// rejection (or the bonus row) resamples: the CTA whose slice holds the draw finds the thread by a
+// block scan of the per-thread sums, and that thread finds the token in its own run.
+// Waits: hardware barriers (cluster, CTA), and the copies' mbarrier, whose wait gives up after about
+// a second (GDN_STATUS_WAIT_TIMEOUT) and is repeated before the CTA exits.
+//
+// The cluster size is chosen on the host among 1..16 (above 8 where the GPU allows non-portable
+// clusters): the fewest waves of B clusters (cudaOccupancyMaxActiveClusters; a GPC holds a whole
+// cluster), each wave weighed as one CTA's share of a row plus a fixed part.
+constexpr int kMaxCL = 16;
+
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// the copy of `local` (a shared-memory location of this CTA) in CTA `rank` of the cluster
+__device__ __forceinline__ uint32_t peer_addr(const void* local, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(local)), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ void st_peer_u64(uint32_t addr, unsigned long long v) {
+    asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(addr), "l"(v) : "memory");
+}
+__device__ __forceinline__ void st_peer_f32(uint32_t addr, float v) {
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+// the VN logits of one 16-byte vector, as float
+template <typename LT>
+__device__ __forceinline__ void unpack16(const uint4& u, float (&x)[16 / sizeof(LT)]) {
+    if constexpr (sizeof(LT) == 2) {
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            x[2 * k] = __uint_as_float(w[k] << 16);
+            x[2 * k + 1] = __uint_as_float(w[k] & 0xffff0000u);
+        }
+    } else {
+        x[0] = __uint_as_float(u.x); x[1] = __uint_as_float(u.y);
+        x[2] = __uint_as_float(u.z); x[3] = __uint_as_float(u.w);
+    }
+}
+// element k of a run in shared memory, as float
+template <typename LT>
+__device__ __forceinline__ float run_elem(const uint4* run, int k) {
+    if constexpr (sizeof(LT) == 2)
+        return __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(run)[k]);
+    else
+        return reinterpret_cast<const float*>(run)[k];
+}
+
+struct LazySlots {
+    float mx[2][kMaxCL];                 // by row parity: each CTA's slice maximum
+    unsigned long long sum[2][kMaxCL];   // each CTA's weight sum
+    unsigned long long wd[2][kMaxCL];    // the draft's weight (non-zero only from its slice's CTA)
+};
+
+template <typename LT>
+__global__ void __launch_bounds__(1024, 1)
+    accept_sample_lazy_kernel(const AcceptArgs a, const int SL, const int K) {
+    constexpr int VN = LogitVec<LT>::N;       // logits per 16-byte vector
+    extern __shared__ uint4 s_stage[];        // [2][blockDim.x * K]: two rows' slices, then the
+                                              // sequence's N drafts (int32)
+    __shared__ LazySlots slots;
+    __shared__ unsigned long long s_rs[32], s_rw[32];
+    __shared__ float s_rm[32];
+    __shared__ uint64_t s_bar[2];             // per stage: its bulk copies landed
+    __shared__ int s_bad, s_ok;
+    const int NT = blockDim.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int nwarps = NT >> 5;
+    const uint32_t rank = cluster_ctarank(), CL = cluster_nctarank();
+    const int b = blockIdx.x / int(CL), N = a.N, V = a.V, RS = N + 1;
+    const int lo = int(rank) * SL, hi = min(V, lo + SL);
+    const int SLV = NT * K;                   // vectors per stage
+    const int t0 = lo + tid * K * VN;         // this thread's first logit
+    const int t1 = min(hi, t0 + K * VN);      // one past its last (t1 <= t0: an idle thread)
+    // the bulk copies bring [lo, hv), a whole number of 16-byte vectors; the rest of the slice,
+    // [hv, hi), is less than one vector (a vocabulary that is not a multiple of it) and is read
+    // from global memory by its thread
+    const uint32_t bulk_bytes = hi > lo ? (uint32_t(hi - lo) * uint32_t(sizeof(LT))) & ~15u : 0u;
+    const int hv = lo + int(bulk_bytes / sizeof(LT));
+    const int32_t* dr_g = a.drafts + size_t(b) * N;
+    int32_t* dr = reinterpret_cast<int32_t*>(s_stage + size_t(2) * NT * K);   // [N] in shared memory
+
+    auto row_of = [&](int i) { return static_cast<const LT*>(row_ptr(a, b, i, sizeof(LT))); };
+    auto run_of = [&](int i) { return s_stage + size_t(i & 1) * SLV + size_t(tid) * K; };
+    uint32_t pending = 0, pend_par = 0;       // thread 0, bit per stage: copies issued and not yet
+                                              // seen landing, and their mbarrier phase parity
+    auto issue_row = [&](int i) {
+        if (tid == 0 && bulk_bytes) {
+            uint64_t* bar = &s_bar[i & 1];
+            mbar_arrive_expect_tx(bar, bulk_bytes);
+            const char* src = reinterpret_cast<const char*>(row_of(i) + lo);
+            char* dst = reinterpret_cast<char*>(s_stage + size_t(i & 1) * SLV);
+            for (uint32_t off = 0; off < bulk_bytes; off += 32768u)
+                bulk_g2s(dst + off, src + off, min(32768u, bulk_bytes - off), bar);
+            pending |= 1u << (i & 1);
+            pend_par = (pend_par & ~(1u << (i & 1))) | (((uint32_t(i) >> 1) & 1u) << (i & 1));
+        }
+    };
+    // row i's copies have landed (stage i & 1 is used for the (i >> 1)-th time)
+    auto wait_row = [&](int i) {
+        if (!bulk_bytes) return;
+        if (tid == 0) {
+            const bool ok = mbar_wait_bounded(&s_bar[i & 1], uint32_t(i >> 1) & 1u);
+            if (ok) pending &= ~(1u << (i & 1));
+            else set_status(a.status, GDN_STATUS_WAIT_TIMEOUT);
+            s_ok = ok;
+        }
+        __syncthreads();
+        if (s_ok) (void)mbar_try_wait(&s_bar[i & 1], uint32_t(i >> 1) & 1u);   // completed: acquire
+    };
+    // the VN logits of vector k of this thread's run of row i (−∞ past the slice)
+#define LAZY_LOAD_VEC(i_, run_, k_, x_)                                                        \
+    do {                                                                                      \
+        const int e0_ = t0 + (k_) * VN;                                                       \
+        if (e0_ + VN <= hv) {                                                                 \
+            unpack16<LT>((run_)[k_], x_);                                                     \
+        } else {                                                                              \
+            const LT* row_ = row_of(i_);                                                      \
+            _Pragma("unroll") for (int j_ = 0; j_ < VN; ++j_)                                 \
+                x_[j_] = e0_ + j_ < hi ? LogitVec<LT>::one(row_ + e0_ + j_) : -INFINITY;      \
+        }                                                                                     \
+    } while (0)
+    // this thread's maximum of row i (NaN never wins: fmaxf returns the other operand)
+    auto run_max = [&](int i) {
+        const uint4* run = run_of(i);
+        float mx = -INFINITY;
+        for (int k = 0; k < K && t0 + k * VN < hi; ++k) {
+            float x[VN];
+            LAZY_LOAD_VEC(i, run, k, x);
+#pragma unroll
+            for (int j = 0; j < VN; ++j) mx = fmaxf(mx, x[j]);
+        }
+        return mx;
+    };
+    // publish this CTA's (sum, draft weight) of row i and maximum of row i + 1 into every peer
+    auto publish = [&](int i, unsigned long long ts, unsigned long long wdv, float mxn) {
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            ts += __shfl_xor_sync(0xffffffffu, ts, o);
+            wdv += __shfl_xor_sync(0xffffffffu, wdv, o);
+            mxn = fmaxf(mxn, __shfl_xor_sync(0xffffffffu, mxn, o));
+        }
+        if (lane == 0) { s_rs[warp] = ts; s_rw[warp] = wdv; s_rm[warp] = mxn; }
+        __syncthreads();
+        if (warp == 0) {
+            ts = lane < nwarps ? s_rs[lane] : 0ull;
+            wdv = lane < nwarps ? s_rw[lane] : 0ull;
+            mxn = lane < nwarps ? s_rm[lane] : -INFINITY;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                ts += __shfl_xor_sync(0xffffffffu, ts, o);
+                wdv += __shfl_xor_sync(0xffffffffu, wdv, o);
+                mxn = fmaxf(mxn, __shfl_xor_sync(0xffffffffu, mxn, o));
+            }
+            for (int r = lane; r < int(CL); r += 32) {
+                if (i >= 0) {
+                    st_peer_u64(peer_addr(&slots.sum[i & 1][rank], uint32_t(r)), ts);
+                    st_peer_u64(peer_addr(&slots.wd[i & 1][rank], uint32_t(r)), wdv);
+                }
+                st_peer_f32(peer_addr(&slots.mx[(i + 1) & 1][rank], uint32_t(r)), mxn);
+            }
+        }
+        cluster_sync_all();
+    };
+
+    if (tid == 0) {
+        s_bad = 0;
+        mbar_init(&s_bar[0], 1);
+        mbar_init(&s_bar[1], 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    issue_row(0);
+    if (N >= 1) issue_row(1);
+    // the drafts, while the first rows are in flight; one outside [0, V) ends the sequence (every
+    // CTA sees the same drafts and leaves, after its copies have landed, before any peer access)
+    for (int q = tid; q < N; q += NT) {
+        const int32_t v = dr_g[q];
+        dr[q] = v;
+        if (v < 0 || v >= V) s_bad = 1;
+    }
+    __syncthreads();
+    if (s_bad) {
+        if (rank == 0) {
+            int32_t* out = a.out_tokens + size_t(b) * RS;
+            for (int q = tid; q < RS; q += NT) out[q] = -1;
+            if (tid == 0) { a.n_acc[b] = 0; set_status(a.status, GDN_STATUS_BAD_TOKEN); }
+        }
+        if (tid == 0)
+            for (int q = 0; q < 2; ++q)
+                if ((pending >> q) & 1u) (void)mbar_wait_bounded(&s_bar[q], (pend_par >> q) & 1u);
+        return;
+    }
+    cluster_sync_all();   // every CTA of the cluster runs before the first peer store
+    wait_row(0);
+    publish(-1, 0ull, 0ull, run_max(0));
+
+    const float c = a.c;
+    int i = 0, act = 0, ban = -1;
+    unsigned long long rr = 0, ts = 0, wd = 0, Z = 0;
+    float m = -INFINITY;
+    for (;; ++i) {
+        // row i's maximum is in the slots: the exact weights of this thread's run
+        m = slots.mx[i & 1][0];
+        for (int k = 1; k < int(CL); ++k) m = fmaxf(m, slots.mx[i & 1][k]);
+        const uint4* run = run_of(i);
+        ts = 0;
+        int k = 0;
+        for (; k + 1 < K && t0 + (k + 1) * VN < hi; k += 2) {   // two vectors at a time
+            float x[VN], y[VN];
+            LAZY_LOAD_VEC(i, run, k, x);
+            LAZY_LOAD_VEC(i, run, k + 1, y);
+            unsigned long long s0 = 0, s1 = 0;
+#pragma unroll
+            for (int j = 0; j < VN; ++j) {
+                s0 += weight_of(x[j], m, c);
+                s1 += weight_of(y[j], m, c);
+            }
+            ts += s0 + s1;
+        }
+        if (k < K && t0 + k * VN < hi) {
+            float x[VN];
+            LAZY_LOAD_VEC(i, run, k, x);
+#pragma unroll
+            for (int j = 0; j < VN; ++j) ts += weight_of(x[j], m, c);
+        }
+        const int d = i < N ? dr[i] : -1;
+        unsigned long long wdv = 0;
+        if (d >= t0 && d < t1)
+            wdv = weight_of(d < hv ? run_elem<LT>(run, d - t0) : LogitVec<LT>::one(row_of(i) + d), m, c);
+        float mxn = -INFINITY;
+        if (i < N) {
+            wait_row(i + 1);                         // prefetched while row i was weighed
+            mxn = run_max(i + 1);
+        }
+        publish(i, ts, wdv, mxn);
+
+        // the decision, taken identically by every thread of every CTA from the same slots
+        Z = 0;
+        wd = 0;
+        for (int q = 0; q < int(CL); ++q) { Z += slots.sum[i & 1][q]; wd += slots.wd[i & 1][q]; }
+        if (i < N) {
+            const unsigned long long u = draw_uniform(a.seed, a.round, b, i, 0u, Z);
+            if (u < wd) {                            // accepted: row i's stage takes row i + 2
+                if (i + 2 <= N) issue_row(i + 2);
+                continue;
+            }
+            act = 1;                                 // rejected: ban the draft, resample
+            ban = d;
+            Z -= wd;
+            rr = draw_uniform(a.seed, a.round, b, i, 1u, Z);
+        } else {
+            act = 2;                                 // all accepted: the bonus row
+            rr = draw_uniform(a.seed, a.round, b, i, 1u, Z);
+        }
+        break;
+    }
+
+    // the CTA whose slice holds rr: its prefix over the slices before it (ban removed)
+    const int ban_cta = ban >= 0 ? ban / SL : -1;
+    const unsigned long long wban = ban >= 0 ? wd : 0ull;
+    unsigned long long pre = 0;
+    for (int q = 0; q < int(rank); ++q) pre += slots.sum[i & 1][q] - (q == ban_cta ? wban : 0ull);
+    const unsigned long long mine = slots.sum[i & 1][rank] - (int(rank) == ban_cta ? wban : 0ull);
+    int32_t* out = a.out_tokens + size_t(b) * RS;
+    if (rr >= pre && rr - pre < mine) {
+        // block exclusive scan of the per-thread sums (the banned token's thread without it)
+        const unsigned long long tsb = ts - ((ban >= t0 && ban < t1) ? wban : 0ull);
+        unsigned long long inc = tsb;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned long long y = __shfl_up_sync(0xffffffffu, inc, o);
+            if (lane >= o) inc += y;
+        }
+        if (lane == 31) s_rs[warp] = inc;
+        __syncthreads();
+        unsigned long long base = 0;
+        for (int w = 0; w < warp; ++w) base += s_rs[w];
+        const unsigned long long tpre = base + inc - tsb, r2 = rr - pre;
+        if (r2 >= tpre && r2 - tpre < tsb) {
+            // this thread's run: the first logit whose running sum passes r2
+            const uint4* run = run_of(i);
+            unsigned long long acc = tpre;
+            int tok = -1;
+            for (int k = 0; k < K && tok < 0 && t0 + k * VN < hi; ++k) {
+                const int e0 = t0 + k * VN;
+                float x[VN];
+                LAZY_LOAD_VEC(i, run, k, x);
+                unsigned long long w[VN];
+#pragma unroll
+                for (int j = 0; j < VN; ++j) w[j] = e0 + j != ban ? weight_of(x[j], m, c) : 0ull;
+#pragma unroll
+                for (int j = 0; j < VN; ++j) {
+                    acc += w[j];
+                    if (tok < 0 && acc > r2) tok = e0 + j;
+                }
+            }
+            out[i] = tok;
+        }
+    } else if (rank == 0 && tid == 0 && rr >= Z) {
+        out[i] = -1;                                 // nothing left to draw from
+    }
+    // rank 0 writes everything but the drawn position: the accepted drafts and the padding
+    if (rank == 0) {
+        if (tid == 0 && Z == 0) set_status(a.status, GDN_STATUS_EMPTY_DIST);
+        for (int k = tid; k < RS; k += NT)
+            if (k != i) out[k] = k < i ? dr[k] : -1;
+        if (tid == 0) a.n_acc[b] = act == 1 ? i : N;
+    }
+    // a copy whose wait gave up may still be landing in this CTA's stages: wait once more
+    if (tid == 0) {
+        for (int q = 0; q < 2; ++q)
+            if ((pending >> q) & 1u) (void)mbar_wait_bounded(&s_bar[q], (pend_par >> q) & 1u);
+    }
+}
+#undef LAZY_LOAD_VEC
+
+// Launch plan of the cluster path: cluster size CL, slice SL, vectors per thread K, threads NT.
+struct LazyPlan {
+    int CL, SL, K, NT;
+    size_t smem;
+};
+
+static std::mutex g_plan_mu;
+static std::map<std::tuple<unsigned long long, int, int, int, int>, LazyPlan> g_plans;
+
+// The cluster path serves vocabularies of 8192 and more whose two-row slices fit shared memory;
+// among the cluster sizes that fit, it takes the one with the fewest waves of clusters, weighing
+// a wave as the row work of one CTA (1/CL) plus a fixed part (barriers, latency).
+template <typename LT>
+static bool lazy_plan(int V, int B, int N, LazyPlan* out) {
+    if (V < 8192) return false;
+    constexpr int VN = 16 / int(sizeof(LT));
+    const unsigned long long ctx = current_context_id();
+    const auto key = std::make_tuple(ctx, int(sizeof(LT)), V, B, N);
+    std::lock_guard<std::mutex> lock(g_plan_mu);
+    if (ctx) {
+        auto it = g_plans.find(key);
+        if (it != g_plans.end()) {
+            *out = it->second;
+            return out->CL > 0;
+        }
+    }
+    auto kern = accept_sample_lazy_kernel<LT>;
+    constexpr size_t kMaxDyn = 225 * 1024;
+    LazyPlan best{0, 0, 0, 0, 0};
+    double best_cost = 1e300;
+    int nsm = 0;
+    if (device_sm_count(&nsm) == cudaSuccess && nsm > 0 &&
+        smem_optin(reinterpret_cast<const void*>(kern), kMaxDyn) == cudaSuccess) {
+        const bool big = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed,
+                                              1) == cudaSuccess;
+        (void)cudaGetLastError();
+        for (int CL = big ? kMaxCL : 8; CL >= 1; --CL) {
+            int SL = (V + CL - 1) / CL;
+            SL = (SL + VN - 1) / VN * VN;
+            const int nvec = SL / VN;
+            int K = 1;
+            while ((nvec + K - 1) / K > 1024) K += 2;
+            int NT = ((nvec + K - 1) / K + 31) / 32 * 32;
+            const size_t smem = size_t(2) * NT * K * 16 + (size_t(N) * 4 + 15) / 16 * 16;
+            if (smem > kMaxDyn) continue;
+            cudaLaunchConfig_t cfg = {};
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = unsigned(CL);
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.gridDim = dim3(unsigned(CL));
+            cfg.blockDim = dim3(unsigned(NT));
+            cfg.dynamicSmemBytes = smem;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            int n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n <= 0) {
+                (void)cudaGetLastError();
+                continue;
+            }
+            // within one wave, CTAs beyond one per SM share SMs (a cluster waits for its slowest)
+            const int waves = (B + n - 1) / n;
+            const int per_sm = waves == 1 ? (B * CL + nsm - 1) / nsm : 1;
+            const double cost = double(waves) * (double(per_sm) / CL + 0.25);
+            if (cost < best_cost) {
+                best_cost = cost;
+                best = LazyPlan{CL, SL, K, NT, smem};
+            }
+        }
+    }
+    (void)cudaGetLastError();
+    if (ctx) g_plans[key] = best;
+    *out = best;
+    return best.CL > 0;
+}
+
+template <typename LT>
+static cudaError_t launch_lazy(const AcceptArgs& a, const LazyPlan& p, cudaStream_t s) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = unsigned(p.CL);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(unsigned(a.B) * unsigned(p.CL));
+    cfg.blockDim = dim3(unsigned(p.NT));
+    cfg.dynamicSmemBytes = p.smem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, accept_sample_lazy_kernel<LT>, a, p.SL, p.K);
+}
+
 // ---------------------------------------------------------------- host launchers
 void accept_chunking(int rows, int V, int* CH, int* CS) {
     int ch = rows > 0 ? (1216 + rows - 1) / rows : 1;
@@ -537,6 +980,11 @@ static cudaError_t greedy_t(const AcceptArgs& a, cudaStream_t s) {
 
 template <typename LT>
 static cudaError_t sample_t(const AcceptArgs& a, cudaStream_t s) {
+    LazyPlan p;
+    if (a.B <= 0x7fffffff / kMaxCL && a.N <= 4096 && lazy_plan<LT>(a.V, a.B, a.N, &p)) {
+        const cudaError_t e = launch_lazy<LT>(a, p, s);
+        return e != cudaSuccess ? e : cudaGetLastError();
+    }
     const unsigned rows = unsigned(a.B) * unsigned(a.N + 1);
     accept_rowmax_kernel<LT><<<dim3(rows, a.CH), kAccThreads, 0, s>>>(a);
     accept_weights_kernel<LT><<<dim3(rows, a.CH), kAccThreads, 0, s>>>(a);

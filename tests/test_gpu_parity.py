@@ -282,6 +282,102 @@ def test_sample_accept_bit_exact(gdnlib, V, B, N):
         assert np.array_equal(out.cpu().numpy(), out_ref)
 
 
+def sample_case(B, N, V, dtype, temperature, seed, rounds, plant=None, std=2.0):
+    """Sampling accept through the C ABI against the oracle, bit-exact, over `rounds` rounds.
+    Rows are padded to a 16-byte stride with values that must never be read. `plant(lg, dr, g)`
+    may edit the logits / drafts (a numpy generator is passed)."""
+    g = np.random.default_rng(seed)
+    VN = 8 if dtype == torch.bfloat16 else 4
+    Vpad = (V + VN - 1) // VN * VN
+    ws = torch.empty(_lib.workspace_bytes(B, N, V, _lib.SPEC_MODE_SAMPLE, dtype), dtype=torch.uint8,
+                     device="cuda")
+    n_acc = torch.empty(B, dtype=torch.int32, device="cuda")
+    out = torch.empty(B, N + 1, dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    lengths = []
+    for rnd in range(rounds):
+        lg = torch.from_numpy((g.standard_normal((B, N + 1, V)) * std).astype(np.float32))
+        dr = lg[:, :N].argmax(-1).to(torch.int32)
+        if plant is not None:
+            plant(lg, dr, g)
+        lg = lg.to(dtype)
+        pad = torch.full((B, N + 1, Vpad), 1e4).to(dtype)       # padding is never read
+        pad[..., :V] = lg
+        dlg, ddr = to_dev(pad, dr)
+        _lib.spec_accept(dlg, ddr, n_acc, out, ws, mode=_lib.SPEC_MODE_SAMPLE,
+                         temperature=temperature, seed=seed, round_=rnd, V=V, status=status)
+        torch.cuda.synchronize()
+        n, out_ref, bad = oracle.accept_sample(logits_f32(lg), dr.numpy(), temperature, seed, rnd)
+        assert bad == 0
+        assert np.array_equal(n_acc.cpu().numpy(), n), (rnd, n_acc.cpu().numpy(), n)
+        assert np.array_equal(out.cpu().numpy(), out_ref), rnd
+        lengths += list(n)
+    assert int(status.item()) == 0
+    return np.array(lengths)
+
+
+# vocabularies on both sides of the switch between the parallel three-kernel path (V < 8192, or
+# two rows' slices beyond shared memory: fp32 above ~230K) and the one-cluster-per-sequence path;
+# ragged slices and runs; batch sizes that need one and several waves of clusters
+@pytest.mark.parametrize("V,dtype,B", [(8192, torch.bfloat16, 5), (8191, torch.bfloat16, 5),
+                                       (50001, torch.bfloat16, 5), (262147, torch.bfloat16, 3),
+                                       (151936, torch.float32, 5), (163841, torch.float32, 4),
+                                       (262144, torch.float32, 2), (12345, torch.float32, 7),
+                                       (151936, torch.bfloat16, 37), (20000, torch.bfloat16, 200)])
+def test_sample_accept_vocab_sizes(gdnlib, V, dtype, B):
+    sample_case(B=B, N=3, V=V, dtype=dtype, temperature=0.7, seed=V % 97, rounds=2)
+
+
+def test_sample_accept_long_accept_runs(gdnlib):
+    """Drafts that carry most of the probability (a planted margin at low temperature) are
+    accepted for many rows in a row, so the cluster walks deep into the block and often reaches
+    the bonus row; a few rows plant a rejection at a random depth."""
+    B, N, V = 12, 16, 151936
+
+    def plant(lg, dr, g):
+        for b in range(B):
+            stop = int(g.integers(0, N + 3))            # >= N: no planted rejection
+            for i in range(N):
+                d = int(g.integers(0, V))
+                dr[b, i] = d
+                lg[b, i, d] = lg[b, i].max() + (4.0 if i != stop else -3.0)
+
+    n = sample_case(B=B, N=N, V=V, dtype=torch.bfloat16, temperature=0.5, seed=21, rounds=3,
+                    plant=plant)
+    assert n.max() == N and (n > N // 2).mean() > 0.3
+
+
+def test_sample_accept_zero_draft_rows(gdnlib):
+    """N = 0: only the bonus row, sampled by the cluster path."""
+    sample_case(B=9, N=0, V=151936, dtype=torch.bfloat16, temperature=1.3, seed=5, rounds=3)
+
+
+def test_sample_accept_bad_draft_on_cluster_path(gdnlib):
+    """A draft outside [0, V) on the cluster path: that sequence reports n = 0 and -1 tokens with
+    BAD_TOKEN (its CTAs leave once their row copies have landed); the others are unaffected."""
+    B, N, V = 6, 5, 151936
+    g = np.random.default_rng(8)
+    lg = torch.from_numpy((g.standard_normal((B, N + 1, V)) * 2).astype(np.float32)).to(torch.bfloat16)
+    dr = lg[:, :N].float().argmax(-1).to(torch.int32)
+    dr[2, 3] = V + 1
+    dr[4, 0] = -7
+    ws = torch.empty(_lib.workspace_bytes(B, N, V, _lib.SPEC_MODE_SAMPLE), dtype=torch.uint8,
+                     device="cuda")
+    n_acc = torch.empty(B, dtype=torch.int32, device="cuda")
+    out = torch.empty(B, N + 1, dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    dlg, ddr = to_dev(lg, dr)
+    _lib.spec_accept(dlg, ddr, n_acc, out, ws, mode=_lib.SPEC_MODE_SAMPLE, temperature=0.7,
+                     seed=3, round_=1, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) & 0x4
+    n, out_ref, bad = oracle.accept_sample(logits_f32(lg), dr.numpy(), 0.7, 3, 1)
+    assert bad == 4
+    assert np.array_equal(n_acc.cpu().numpy(), n)
+    assert np.array_equal(out.cpu().numpy(), out_ref)
+    assert (out_ref[2] == -1).all() and (out_ref[4] == -1).all()
+
+
 def test_sample_accept_chi_square_gpu(gdnlib):
     """Emitted first tokens follow p over 10^6 GPU draws (all sequences share one logits block)."""
     from scipy import stats

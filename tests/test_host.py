@@ -58,7 +58,9 @@ def test_bench_byte_accounting():
     assert bench.bytes_rollback(w, [0] * 64) == 4 * 64
     one = bench.bytes_rollback(w, [3] + [0] * 63) - 4 * 64
     assert one == 30 * (2 * S + 3 * (4 * 32 * 128 + 4 * 16 * 128 + 4 * 32) + 2 * 3 * 8192 * 2)
-    assert bench.bytes_accept(w) == 64 * 9 * 151936 * 2 + 4 * 64 * 18
+    # the rows the accept loop reaches: n + 1 per sequence
+    assert bench.bytes_accept(w, [8] * 64) == 64 * 9 * 151936 * 2 + 4 * 64 * 18
+    assert bench.bytes_accept(w, [0] * 63 + [3]) == (63 + 4) * 151936 * 2 + 4 * 64 * 18
     assert bench.aggregate_tokens_per_s(2, 64, 8, 2.0) == 2 * 64 * 8 / 2e-3
 
 
