@@ -251,65 +251,80 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------------------ CPU oracle leg
-def oracle_unit_times(w, seed, budget_s, units_min):
+def host_cores():
+    """Host cores this process may run on (the affinity mask, else the CPU count)."""
+    try:
+        return len(os.sched_getaffinity(0))
+    except (AttributeError, OSError):
+        return os.cpu_count() or 1
+
+
+def oracle_unit_times(w, seed, budget_s, units_min, threads=1):
     """Time the CPU oracle on (layer, sequence) units of verify+rollback and on per-sequence
-    accepts of the workload. Returns (seconds per unit, seconds per accepted sequence, units)."""
+    accepts of the workload, with `threads` oracle threads: each call covers one sequence per
+    thread, and the times are per unit / per sequence of that throughput. Returns (seconds per
+    unit, seconds per accepted sequence, units, threads in effect)."""
     import numpy as np
     import torch
     import oracle
     from speculative_verify_gdn_gb300 import inputs as I
 
-    small = I.custom(w, name=w.name, L=1, B=1)
-    cw = I.model_weights(small, seed).double().numpy()
-    st, cs = I.initial_state(small, seed)
-    st, cs = st.double().numpy(), cs.double().numpy()
-    qkv, g, beta = I.round_stream(small, 0, seed)
-    qkv, g, beta = qkv.double().numpy(), g.double().numpy(), beta.double().numpy()
-    d = oracle.OracleDims(L=1, B=1, T=w.N, Hk=w.Hk, Hv=w.Hv, Dk=w.D, Dv=w.D, W=w.W)
-    parent = None
-    if w.accept == "tree":
-        parent = I.random_tree(I.custom(w, name=w.name, B=1), 0, seed).numpy()
-    t0 = time.perf_counter()
-    units = 0
-    while units < units_min or time.perf_counter() - t0 < budget_s:
-        ref = oracle.verify(d, qkv, cw, cs, g, beta, st, parent=parent)
-        n = np.array([max(1, w.N // 2)], np.int32)
+    threads = oracle.set_threads(threads)
+    try:
+        nb = threads
+        small = I.custom(w, name=w.name, L=1, B=nb)
+        cw = I.model_weights(small, seed).double().numpy()
+        st, cs = I.initial_state(small, seed)
+        st, cs = st.double().numpy(), cs.double().numpy()
+        qkv, g, beta = I.round_stream(small, 0, seed)
+        qkv, g, beta = qkv.double().numpy(), g.double().numpy(), beta.double().numpy()
+        d = oracle.OracleDims(L=1, B=nb, T=w.N, Hk=w.Hk, Hv=w.Hv, Dk=w.D, Dv=w.D, W=w.W)
+        parent = None
+        if w.accept == "tree":
+            parent = np.tile(I.random_tree(I.custom(w, name=w.name, B=1), 0, seed).numpy(), (nb, 1))
+        n = np.full(nb, max(1, w.N // 2), np.int32)
         path = None
         if parent is not None:
-            path = np.full((1, w.P), -1, np.int32)
+            path = np.full((nb, w.P), -1, np.int32)
             x, k = 0, 0
             while x >= 0 and k < n[0]:
-                path[0, k] = x
+                path[:, k] = x
                 k += 1
                 ch = [v for v in range(w.N) if parent[0, v] == x]
                 x = ch[0] if ch else -1
-            n = np.array([k], np.int32)
-        oracle.rollback(d, n, ref["tape_delta"], ref["tape_k"], g, qkv, st, cs, path=path)
-        units += 1
-    t_unit = (time.perf_counter() - t0) / units
-    # accept: one sequence's N+1 rows
-    one = I.custom(w, name=w.name, B=1)
-    if w.accept == "sample":
-        lg, dr = I.sample_logits(one, 0, seed)
-    elif w.accept == "tree":
-        par = I.random_tree(one, 0, seed)
-        tok, lg, _ = I.tree_tokens_and_logits(one, par, 0, seed)
-    else:
-        lg, dr, _ = I.greedy_logits(one, 0, seed)
-    lgf = lg.float().numpy()
-    reps = 0
-    t1 = time.perf_counter()
-    while reps < 2 or time.perf_counter() - t1 < min(2.0, budget_s / 5):
+            n[:] = k
+        t0 = time.perf_counter()
+        units = 0
+        while units < units_min or time.perf_counter() - t0 < budget_s:
+            ref = oracle.verify(d, qkv, cw, cs, g, beta, st, parent=parent)
+            oracle.rollback(d, n, ref["tape_delta"], ref["tape_k"], g, qkv, st, cs, path=path)
+            units += nb
+        t_unit = (time.perf_counter() - t0) / units
+        # accept: one sequence's N+1 rows per thread
+        one = I.custom(w, name=w.name, B=nb)
         if w.accept == "sample":
-            oracle.accept_sample(lgf, dr.numpy(), w.temperature, seed, reps)
+            lg, dr = I.sample_logits(one, 0, seed)
         elif w.accept == "tree":
-            oracle.accept_tree(lgf, par.numpy(), tok.numpy(), w.P)
+            par = I.random_tree(one, 0, seed)
+            tok, lg, _ = I.tree_tokens_and_logits(one, par, 0, seed)
         else:
-            oracle.accept_greedy(lgf, dr.numpy())
-        reps += 1
-    t_acc = (time.perf_counter() - t1) / reps
+            lg, dr, _ = I.greedy_logits(one, 0, seed)
+        lgf = lg.float().numpy()
+        reps = 0
+        t1 = time.perf_counter()
+        while reps < 2 or time.perf_counter() - t1 < min(2.0, budget_s / 5):
+            if w.accept == "sample":
+                oracle.accept_sample(lgf, dr.numpy(), w.temperature, seed, reps)
+            elif w.accept == "tree":
+                oracle.accept_tree(lgf, par.numpy(), tok.numpy(), w.P)
+            else:
+                oracle.accept_greedy(lgf, dr.numpy())
+            reps += 1
+        t_acc = (time.perf_counter() - t1) / (reps * nb)
+    finally:
+        oracle.set_threads(1)
     del torch
-    return t_unit, t_acc, units
+    return t_unit, t_acc, units, threads
 
 
 def cpu_tokens_per_s(w, t_unit, t_acc):
@@ -617,13 +632,21 @@ def main(argv=None):
         "e2e": res.get("e2e"),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        t_unit, t_acc, units = oracle_unit_times(w, args.seed, args.cpu_budget, w.L)
+        # the oracle single-threaded, then on every host core (one sequence per thread)
+        t1u, t1a, u1, _ = oracle_unit_times(w, args.seed, args.cpu_budget / 2, w.L, 1)
+        ncores = host_cores()
+        tnu, tna, un, thr = oracle_unit_times(w, args.seed, args.cpu_budget / 2, w.L, ncores)
         line["cpu_baseline"] = {
-            "value": cpu_tokens_per_s(w, t_unit, t_acc), "unit": UNIT, "cores": 1,
+            "value": cpu_tokens_per_s(w, tnu, tna), "unit": UNIT, "cores": thr, "nproc": ncores,
             "kind": "oracle",
-            "sample": "%d (layer, sequence) units of verify+rollback (%.1f ms each) and one "
-                      "sequence's accept (%.1f ms) of this workload, single-threaded fp64 oracle; "
-                      "tokens/s = N / (L * unit + accept)" % (units, t_unit * 1e3, t_acc * 1e3)}
+            "sample": "%d (layer, sequence) units of verify+rollback and %d sequences' accepts of "
+                      "this workload, %d sequences at a time on %d oracle threads (fp64, OpenMP "
+                      "over independent sequences): %.2f ms per unit, %.2f ms per accept of "
+                      "throughput; tokens/s = N / (L * unit + accept)"
+                      % (un, thr, thr, thr, tnu * 1e3, tna * 1e3),
+            "single_core": {"value": cpu_tokens_per_s(w, t1u, t1a), "cores": 1,
+                            "sample": "%d units (%.1f ms each) and one sequence's accept (%.1f "
+                                      "ms), one thread" % (u1, t1u * 1e3, t1a * 1e3)}}
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0
@@ -843,12 +866,14 @@ def run_reference(args, w):
     from speculative_verify_gdn_gb300 import inputs as I
 
     seed = args.seed
-    small = I.custom(w, name=w.name, L=1, B=1)
+    # every host core: one sequence per oracle thread in each call
+    nb = oracle.set_threads(host_cores())
+    small = I.custom(w, name=w.name, L=1, B=nb)
     cw = I.model_weights(small, seed).double().numpy()
     st, cs = I.initial_state(small, seed)
     st, cs = st.double().numpy(), cs.double().numpy()
-    d = oracle.OracleDims(L=1, B=1, T=w.N, Hk=w.Hk, Hv=w.Hv, Dk=w.D, Dv=w.D, W=w.W)
-    one = I.custom(w, name=w.name, B=1)
+    d = oracle.OracleDims(L=1, B=nb, T=w.N, Hk=w.Hk, Hv=w.Hv, Dk=w.D, Dv=w.D, W=w.W)
+    one = I.custom(w, name=w.name, B=nb)
     parent = tok = None
     if w.accept == "sample":
         lg, dr = I.sample_logits(one, 0, seed)
@@ -866,11 +891,11 @@ def run_reference(args, w):
         qkv, g, beta = streams[k % 2]
         ref = oracle.verify(d, qkv, cw, cs, g, beta, st, parent=parent)
         path = None
-        n = np.array([max(1, w.N // 2)], np.int32)
+        n = np.full(nb, max(1, w.N // 2), np.int32)
         if parent is not None:
-            path = np.full((1, w.P), -1, np.int32)
-            path[0, 0] = 0
-            n = np.array([1], np.int32)
+            path = np.full((nb, w.P), -1, np.int32)
+            path[:, 0] = 0
+            n[:] = 1
         oracle.rollback(d, n, ref["tape_delta"], ref["tape_k"], g, qkv, st, cs, path=path)
         if k % w.L == w.L - 1:
             if w.accept == "sample":
@@ -886,17 +911,20 @@ def run_reference(args, w):
     for k in range(args.steps):
         step(k)
     dt = time.perf_counter() - t0
+    oracle.set_threads(1)
     ms_step = dt / args.steps * 1e3
-    value = w.N * (args.steps / w.L) / dt
+    value = w.N * nb * (args.steps / w.L) / dt
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 0,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "config": workload_description(w),
-        "cpu_baseline": {"value": value, "unit": UNIT, "kind": "oracle", "cores": 1,
-                         "sample": "each step one (layer, sequence) unit of verify+rollback, one "
-                                   "sequence's accept every %d steps; tokens/s = N per %d steps"
-                                   % (w.L, w.L)},
+        "cpu_baseline": {"value": value, "unit": UNIT, "kind": "oracle", "cores": nb,
+                         "nproc": host_cores(),
+                         "sample": "each step %d (layer, sequence) units of verify+rollback on %d "
+                                   "oracle threads (one sequence each), %d sequences' accepts "
+                                   "every %d steps; tokens/s = N x %d per %d steps"
+                                   % (nb, nb, nb, w.L, nb, w.L)},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)

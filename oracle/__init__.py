@@ -22,4 +22,5 @@ from .oracle import (  # noqa: F401
     AttnDims,
     attn_verify,
     attn_truncate,
+    set_threads,
 )

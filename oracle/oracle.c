@@ -39,6 +39,26 @@
 #include <string.h>
 
 /* ------------------------------------------------------------------------------------------
+ * Threads. Layers, sequences and value heads are independent units of verify and rollback, and
+ * sequences of accept ([GDN] §2.2: verification is per sequence; the state is per layer and head),
+ * so with more than one thread the loops over them are split between OpenMP threads, each with
+ * its own scratch. Every unit is still computed by one thread with the same expressions in the
+ * same order: the results are bit-identical to the single-threaded run (a CPU test checks it).
+ * ------------------------------------------------------------------------------------------ */
+static int g_threads = 1;
+
+void oracle_set_threads(int n) { g_threads = n < 1 ? 1 : n; }
+int oracle_get_threads(void) { return g_threads; }
+/* 1 when built with OpenMP (else the thread count has no effect) */
+int oracle_openmp(void) {
+#ifdef _OPENMP
+    return 1;
+#else
+    return 0;
+#endif
+}
+
+/* ------------------------------------------------------------------------------------------
  * Indexing helpers. Layouts are those of the C ABI, dense row-major.
  * ------------------------------------------------------------------------------------------ */
 #define IDX2(a, b, nb) ((size_t)(a) * (size_t)(nb) + (size_t)(b))
@@ -68,11 +88,14 @@ void oracle_verify(const oracle_dims* dm, const int32_t* parent, const double* q
     const int qoff = 0, koff = Hk * Dk, voff = 2 * Hk * Dk;
     const int group = Hv / Hk;
 
+#pragma omp parallel num_threads(g_threads) if (g_threads > 1)
+    {
     double* y = (double*)malloc(sizeof(double) * (size_t)T * C);   /* conv+act output */
     int* anc = (int*)malloc(sizeof(int) * (size_t)(T + 1));
     double* S_nodes = (double*)malloc(sizeof(double) * (size_t)T * Dv * Dk); /* S per node */
     double* Sp = (double*)malloc(sizeof(double) * (size_t)Dv * Dk);
 
+#pragma omp for collapse(2) schedule(dynamic)
     for (int l = 0; l < L; ++l) {
         for (int b = 0; b < B; ++b) {
             const size_t lb = (size_t)l * B + b;
@@ -166,6 +189,7 @@ void oracle_verify(const oracle_dims* dm, const int32_t* parent, const double* q
     free(S_nodes);
     free(anc);
     free(y);
+    }
 }
 
 /* ------------------------------------------------------------------------------------------
@@ -178,8 +202,11 @@ int oracle_rollback(const oracle_dims* dm, const int32_t* path, int P, const int
               Dv = dm->Dv, W = dm->W, C = dm->C;
     const int group = Hv / Hk;
     int bad = 0;
+#pragma omp parallel num_threads(g_threads) if (g_threads > 1) reduction(| : bad)
+    {
     int* nodes = (int*)malloc(sizeof(int) * (size_t)(T + 1));
     double* rows = (double*)malloc(sizeof(double) * (size_t)(W - 1 + T + 1));
+#pragma omp for schedule(dynamic)
     for (int b = 0; b < B; ++b) {
         int n = n_acc[b];
         int cap = path ? P : T;
@@ -228,6 +255,7 @@ int oracle_rollback(const oracle_dims* dm, const int32_t* path, int P, const int
     }
     free(rows);
     free(nodes);
+    }
     return bad;
 }
 
@@ -251,6 +279,7 @@ int oracle_accept_greedy(int B, int N, int V, int64_t row_stride, int64_t seq_st
                          const float* logits, const int32_t* drafts, int32_t* n_acc,
                          int32_t* out_tokens) {
     int bad = 0;
+#pragma omp parallel for num_threads(g_threads) if (g_threads > 1) reduction(| : bad) schedule(dynamic)
     for (int b = 0; b < B; ++b) {
         const float* lg = logits + (size_t)b * seq_stride;
         const int32_t* dr = drafts + (size_t)b * N;
@@ -376,9 +405,13 @@ int oracle_accept_sample(int B, int N, int V, int64_t row_stride, int64_t seq_st
         return oracle_accept_greedy(B, N, V, row_stride, seq_stride, logits, drafts, n_acc,
                                     out_tokens);
     int bad = 0;
+    if (!g_coef_ready) init_coefs();     /* before the threads share the table */
     const float c = oracle_scale_c(temperature);
     const uint32_t rnd = (uint32_t)round;
+#pragma omp parallel num_threads(g_threads) if (g_threads > 1) reduction(| : bad)
+    {
     uint64_t* w = (uint64_t*)malloc(sizeof(uint64_t) * (size_t)V);
+#pragma omp for schedule(dynamic)
     for (int b = 0; b < B; ++b) {
         const float* lg = logits + (size_t)b * seq_stride;
         const int32_t* dr = drafts + (size_t)b * N;
@@ -411,6 +444,7 @@ int oracle_accept_sample(int B, int N, int V, int64_t row_stride, int64_t seq_st
         n_acc[b] = n;
     }
     free(w);
+    }
     return bad;
 }
 
@@ -422,6 +456,7 @@ int oracle_accept_tree(int B, int T, int V, int64_t row_stride, int64_t seq_stri
                        const float* logits, const int32_t* parent, const int32_t* tokens, int P,
                        int32_t* path, int32_t* n_acc, int32_t* out_tokens) {
     int bad = 0;
+#pragma omp parallel for num_threads(g_threads) if (g_threads > 1) reduction(| : bad) schedule(dynamic)
     for (int b = 0; b < B; ++b) {
         const float* lg = logits + (size_t)b * seq_stride;
         const int32_t* par = parent + (size_t)b * T;

@@ -35,6 +35,12 @@ int oracle_rollback(const oracle_dims* dm, const int32_t* path, int P, const int
                     const double* tape_delta, const double* tape_k, const double* g,
                     const double* qkv, double* state, double* conv_state);
 
+/* Threads for the loops over independent units (layers x sequences, sequences); 1 by default.
+ * Results do not depend on it. */
+void oracle_set_threads(int n);
+int oracle_get_threads(void);
+int oracle_openmp(void);
+
 int oracle_argmax(const float* row, int V);
 int oracle_accept_greedy(int B, int N, int V, int64_t row_stride, int64_t seq_stride,
                          const float* logits, const int32_t* drafts, int32_t* n_acc,

@@ -47,8 +47,22 @@ def _load():
         _lib.oracle_attn_verify.restype = ct.c_int
         _lib.oracle_attn_truncate.argtypes = [ct.c_int, ct.c_int, P, P]
         _lib.oracle_attn_truncate.restype = ct.c_int
+        _lib.oracle_set_threads.argtypes = [ct.c_int]
+        _lib.oracle_set_threads.restype = None
+        _lib.oracle_get_threads.argtypes = []
+        _lib.oracle_get_threads.restype = ct.c_int
+        _lib.oracle_openmp.argtypes = []
+        _lib.oracle_openmp.restype = ct.c_int
         del i32
     return _lib
+
+
+def set_threads(n):
+    """Threads for the loops over independent units (results do not depend on it). Returns the
+    count in effect: 1 when the library was built without OpenMP."""
+    lib = _load()
+    lib.oracle_set_threads(int(n))
+    return lib.oracle_get_threads() if lib.oracle_openmp() else 1
 
 
 class _CDims(ct.Structure):

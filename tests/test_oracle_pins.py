@@ -636,3 +636,35 @@ def test_nan_logits_count_as_negative_infinity():
         b = oracle.accept_sample(lg[:, 1:].repeat(2, 1), np.array([[1]], np.int32), 0.7, seed, 0)
         assert np.array_equal(a[1], b[1]) and a[0][0] == b[0][0]
         assert not np.isnan(row[a[1][0, 0]])
+
+
+# ------------------------------------------------------------------------------ threads
+def test_threaded_oracle_is_bit_identical_to_serial():
+    """The oracle's thread count only splits independent units (layers x sequences, sequences)
+    between threads: every output is bit-identical to the single-threaded run."""
+    rng = np.random.default_rng(70)
+    dims, x = rand_inputs(rng, L=3, B=5, T=6, Hk=2, Hv=4, D=8)
+    par = np.stack([tree_parents(rng, 6, 4, 3) for _ in range(5)])
+    V = 300
+    lg = (rng.standard_normal((5, 7, V)) * 2).astype(np.float32)
+    dr = lg[:, :6].argmax(-1).astype(np.int32)
+    dr[::2, 1] = (dr[::2, 1] + 1) % V
+    tok = rng.integers(0, V, (5, 6)).astype(np.int32)
+    res = []
+    for threads in (1, 4):
+        oracle.set_threads(threads)
+        try:
+            v = oracle.verify(dims, **x)
+            t = oracle.verify(dims, parent=par, node_states=True, **x)
+            n = np.array([0, 6, 3, 1, 5], np.int32)
+            r = oracle.rollback(dims, n, v["tape_delta"], v["tape_k"], x["g"], x["qkv"], x["state"],
+                                x["conv_state"])
+            a = oracle.accept_sample(lg, dr, 0.7, 9, 2)
+            gr = oracle.accept_greedy(lg, dr)
+            tr = oracle.accept_tree(lg, par, tok, 4)
+        finally:
+            oracle.set_threads(1)
+        res.append([v["out"], v["tape_delta"], v["tape_k"], t["out"], t["node_state"], r[0], r[1],
+                    a[0], a[1], gr[0], gr[1], tr[0], tr[1], tr[2]])
+    for u, w in zip(*res):
+        assert np.array_equal(u, w)
