@@ -187,6 +187,10 @@ GDN_API int gdn_rollback_path(const gdn_dims* d, const int32_t* path, int32_t P,
  * n_acc_prev[b] > 0, writes the tile back and verifies the new round from it; other shapes run the
  * two calls. A round loop is then: gdn_rollback_verify (with the previous round's accept result; a
  * first round passes n_acc_prev = 0), spec_accept; after the last round, gdn_rollback.
+ * Speed on GB300: it moves about a quarter fewer bytes than the two calls, but the one kernel
+ * runs further below the copy bandwidth than either of them (issue contention between its roles),
+ * so today the separate gdn_rollback + gdn_verify calls finish sooner (1.65 against 1.89 ms a
+ * round at batch 64, N = 8); it stays for callers that want one launch per round.
  * Arguments: the previous round's n_acc_prev [B], tape_delta_prev, tape_k_prev, g_prev, qkv_prev
  * (as gdn_rollback takes them) and this round's verify arguments (as gdn_verify). state and
  * conv_state are updated in place. tape_delta, tape_k and out must not overlap the previous round's
@@ -316,6 +320,17 @@ GDN_API const char* gdn_last_error(void);
  * names of the set GDN_STATUS_* bits in gdn_last_error(). Touches no GPU.
  */
 GDN_API int gdn_status_check(uint32_t status_word);
+
+/*
+ * gdn_set_wait_limit_ns — how long the pipelined verify kernel (bf16, Dk = Dv = 128: gdn_verify,
+ * gdn_verify_tree, gdn_rollback_verify) lets one of its on-chip pipeline waits spin before it
+ * gives up, sets GDN_STATUS_WAIT_TIMEOUT and lets the CTA run to its end without waiting (the
+ * call's outputs are then undefined). 0 restores the default of one second. The waits that drain
+ * copies and tensor-core work before a CTA exits always keep the full second. Process-wide, read
+ * at each launch; a hook for testing the give-up path (a limit of a few nanoseconds makes it run
+ * out). Host only; always GDN_OK. The pages have no counterpart.
+ */
+GDN_API int gdn_set_wait_limit_ns(uint64_t ns);
 
 /* ---- full-attention layers of the hybrid ------------------------------------------------ */
 /*

@@ -34,7 +34,7 @@ STATUS_BITS = {
 EXPORTS = ("gdn_verify", "gdn_verify_tree", "gdn_rollback", "gdn_rollback_path",
            "gdn_rollback_verify", "gdn_tape_bytes", "spec_accept", "spec_workspace_bytes", "spec_accept_tree",
            "spec_accept_static", "spec_stats_accumulate", "attn_verify", "attn_workspace_bytes",
-           "attn_truncate", "gdn_last_error", "gdn_status_check")
+           "attn_truncate", "gdn_last_error", "gdn_status_check", "gdn_set_wait_limit_ns")
 
 
 class GdnError(RuntimeError):
@@ -106,6 +106,8 @@ def load(require_file=True):
     lib.gdn_last_error.restype = ct.c_char_p
     lib.gdn_status_check.argtypes = [ct.c_uint32]
     lib.gdn_status_check.restype = ct.c_int
+    lib.gdn_set_wait_limit_ns.argtypes = [ct.c_uint64]
+    lib.gdn_set_wait_limit_ns.restype = ct.c_int
     _lib = lib
     return lib
 
@@ -342,6 +344,11 @@ def spec_accept_tree(logits, parent, tokens, path, n_acc, out_tokens, workspace,
 def decode_status(value):
     value = int(value) & 0xFFFFFFFF
     return [name for bit, name in STATUS_BITS.items() if value & bit]
+
+
+def set_wait_limit_ns(ns):
+    """Give-up time of the pipelined verify kernel's pipeline waits (0: the default second)."""
+    _check(load().gdn_set_wait_limit_ns(int(ns)), "gdn_set_wait_limit_ns")
 
 
 def status_check(value):

@@ -12,9 +12,13 @@
 #include "kernels.h"
 #include "attn.h"
 
+#include <atomic>
+
 namespace {
 
 thread_local char g_err[512] = "";
+// gdn_set_wait_limit_ns: give-up time of the pipelined verify kernel's pipeline waits (0: 1 s)
+std::atomic<unsigned long long> g_wait_ns{0};
 
 int fail(int code, const char* fmt, ...) {
     va_list ap;
@@ -153,6 +157,7 @@ int verify_common(const gdn_dims* d, const int32_t* parent, const void* qkv, con
     a.qkv = qkv; a.conv_w = conv_w; a.conv_state = conv_state; a.g = g; a.beta = beta;
     a.state = state; a.out = out; a.tape_delta = tape_delta; a.tape_k = tape_k;
     a.parent = tree ? parent : nullptr; a.status = status; a.gate_dk = d->gate_dk;
+    a.wait_ns = g_wait_ns.load();
     gdn::VerifyMaps maps;
     rc = state_tensor_map(d, state, &maps.state);
     if (rc) return rc;
@@ -440,6 +445,11 @@ int spec_accept_tree(const spec_dims* d, const void* logits, const int32_t* pare
 
 const char* gdn_last_error(void) { return g_err; }
 
+int gdn_set_wait_limit_ns(uint64_t ns) {
+    g_wait_ns.store(ns);
+    return GDN_OK;
+}
+
 int gdn_status_check(uint32_t status_word) {
     if (status_word == 0) return GDN_OK;
     static const struct {
@@ -509,6 +519,7 @@ int gdn_rollback_verify(const gdn_dims* d, const int32_t* n_acc_prev, const floa
         a.parent = nullptr; a.status = status;
         a.n_acc_prev = n_acc_prev; a.tape_delta_prev = tape_delta_prev; a.tape_k_prev = tape_k_prev;
         a.g_prev = g_prev; a.qkv_prev = qkv_prev; a.conv_state_out = conv_state;
+        a.wait_ns = g_wait_ns.load();
         gdn::VerifyMaps maps;
         rc = state_tensor_map(d, state, &maps.state);
         if (rc) return rc;

@@ -32,6 +32,7 @@ struct VerifyArgs {
     const float* g_prev;
     const void* qkv_prev;
     void* conv_state_out;
+    uint64_t wait_ns;         // give-up time of the pipelined kernel's pipeline waits (0: 1 s)
 };
 
 // TMA maps of one verify call. `state`: rows [L*B*Hv*Dv] x cols [Dk], 32 x Dv boxes, 128-byte

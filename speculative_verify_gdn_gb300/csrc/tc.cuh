@@ -143,16 +143,20 @@ __device__ __forceinline__ void named_bar(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
-// bounded wait that gives up for good once any wait in the CTA has timed out
+// The give-up time of a wait: about one second of wall time unless a pipeline limit is set.
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+
+// bounded wait (limit_ns of wall time) that gives up for good once any wait in the CTA has timed
+// out
 __device__ __forceinline__ bool pwait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                      uint32_t* status) {
+                                      uint32_t* status, uint64_t limit_ns = kWaitLimitNs) {
     if (*abort_flag) return false;
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
-        if (globaltimer_ns() - t0 > 1000000000ull) {
+        if (globaltimer_ns() - t0 > limit_ns) {
             set_status(status, GDN_STATUS_WAIT_TIMEOUT);
             *abort_flag = 1;
             return false;
@@ -162,9 +166,9 @@ __device__ __forceinline__ bool pwait(uint64_t* bar, uint32_t parity, volatile i
 
 // pwait by lane 0, result broadcast: every lane of the warp takes the same branch
 __device__ __forceinline__ bool pwait_warp(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                           uint32_t* status) {
+                                           uint32_t* status, uint64_t limit_ns = kWaitLimitNs) {
     int ok = 0;
-    if ((threadIdx.x & 31) == 0) ok = pwait(bar, parity, abort_flag, status) ? 1 : 0;
+    if ((threadIdx.x & 31) == 0) ok = pwait(bar, parity, abort_flag, status, limit_ns) ? 1 : 0;
     ok = __shfl_sync(0xffffffffu, ok, 0);
     __syncwarp();
     return ok != 0;

@@ -31,7 +31,9 @@
 // takes both operand halves from TMEM), and a shared-memory slot is held only from its TMA until
 // its K-block has been split, so the loader runs ahead of the unit prologue by the whole ring.
 // Every wait is bounded: on a timeout the CTA records WAIT_TIMEOUT, the producers stop issuing, and
-// the other roles run on without waiting (results are then garbage, never a hang).
+// the other roles run on without waiting (results are then garbage, never a hang). The pipeline
+// waits give up after VerifyArgs::wait_ns (default one second; gdn_set_wait_limit_ns); the drains
+// before the CTA exits (copies in flight, MMAs before TMEM is released) keep the full second.
 //
 // COMMIT (gdn_rollback_verify): the same pass first commits the previous round's accepted steps,
 // as gdn_rollback does ("GDN investigation" §4, tape replay), then verifies the new round from the
@@ -550,6 +552,8 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int T = a.T, Hk = a.Hk, Hv = a.Hv, C = a.C, W = a.W, B = a.B;
+    // give-up time of the pipeline waits (the drains at the end keep the full limit)
+    const uint64_t lim = a.wait_ns ? a.wait_ns : kWaitLimitNs;
     const int NR = COMMIT ? 2 * (W - 1) + T : W - 1 + T;
     const int n_my = blockIdx.x < n_units ? (n_units - 1 - int(blockIdx.x)) / int(gridDim.x) + 1 : 0;
 
@@ -603,7 +607,7 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
             for (int kb = 0; kb < Cfg::KB && ok; ++kb) {
                 for (int j = 0; j < G; ++j) {
                     const int row0 = int((lb * Hv + kh * G + j) * D);
-                    if (!pwait_warp(&kempty[s], ph ^ 1, abort_flag, a.status)) { ok = false; break; }
+                    if (!pwait_warp(&kempty[s], ph ^ 1, abort_flag, a.status, lim)) { ok = false; break; }
                     if (elect_one()) {
                         mbar_arrive_expect_tx(&kfull[s], uint32_t(Cfg::KSLOT));
                         tma_load_2d(smem + Cfg::OFF_RING + size_t(s) * Cfg::KSLOT, &smap, kb * 32, row0,
@@ -655,7 +659,7 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
                 n = n_prev(b);
                 gv_next = prev_gate(iu + 1);
             }
-            if (!pwait_warp(&sempty[ss], ((iu / NSS) & 1) ^ 1, abort_flag, a.status)) break;
+            if (!pwait_warp(&sempty[ss], ((iu / NSS) & 1) ^ 1, abort_flag, a.status, lim)) break;
             if (lane == 0) {
                 const int rows = (W - 1) + T + ((COMMIT && n > 0) ? W - 1 : 0);
                 mbar_arrive_expect_tx(&sfull[ss], uint32_t(Cfg::NPARTS * (rows * D + D * W) * Cfg::ES));
@@ -678,7 +682,7 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
                 // previous round's tape rows and gate coefficients of this unit
                 const int ks = iu & 1;
                 float* kp = reinterpret_cast<float*>(smem + Cfg::OFF_KP + size_t(ks) * Cfg::KP_BYTES);
-                if (!pwait_warp(&kpempty[ks], ((iu >> 1) & 1) ^ 1, abort_flag, a.status)) break;
+                if (!pwait_warp(&kpempty[ks], ((iu >> 1) & 1) ^ 1, abort_flag, a.status, lim)) break;
                 {
                     // c_s = Γ(s+1 .. n-1) and Γ(0 .. n-1) by a suffix-product scan over the lanes
                     // (lane j TMAX + s holds g'_s, 1 for s >= n): log2(TMAX) steps instead of a
@@ -734,15 +738,15 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
         bool ok = true;
         for (int iu = 0; iu < n_my && ok; ++iu) {
             const int us = iu % NXS, ps = iu % Cfg::NUS;
-            if (!pwait_warp(&ufull[us], (iu / NXS) & 1, abort_flag, a.status)) break;
-            if (!pwait_warp(&tempty[ps], ((iu / Cfg::NUS) & 1) ^ 1, abort_flag, a.status)) break;
+            if (!pwait_warp(&ufull[us], (iu / NXS) & 1, abort_flag, a.status, lim)) break;
+            if (!pwait_warp(&tempty[ps], ((iu / Cfg::NUS) & 1) ^ 1, abort_flag, a.status, lim)) break;
             const uint64_t db = umma_desc_sw128(sX0 + us * Cfg::X_BYTES);
             const uint32_t dt = tbase + ps * Cfg::P_COLS;
             for (int kb = 0; kb < Cfg::KB; ++kb) {
                 int slot[G];
 #pragma unroll
                 for (int j = 0; j < G; ++j) {
-                    if (!pwait_warp(&tmfull[ts], tph, abort_flag, a.status)) ok = false;
+                    if (!pwait_warp(&tmfull[ts], tph, abort_flag, a.status, lim)) ok = false;
                     slot[j] = ts;
                     if (++ts == NTS) { ts = 0; tph ^= 1; }
                 }
@@ -856,13 +860,13 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
                     if (p == 0) mbar_arrive(winfull);      // the epilogue warps' v conv may start
                 }
             }
-            pwait(&sfull[ss], (iu / NSS) & 1, abort_flag, a.status);
+            pwait(&sfull[ss], (iu / NSS) & 1, abort_flag, a.status, lim);
             if constexpr (Cfg::BIG) {
                 // one meta slot: the B tile is free once the previous unit's products are done;
                 // its records are waited for just before this unit's are written (below)
-                if (iu > 0) pwait(&tfull[(iu - 1) % Cfg::NUS], uint32_t((iu - 1) / Cfg::NUS) & 1u, abort_flag, a.status);
+                if (iu > 0) pwait(&tfull[(iu - 1) % Cfg::NUS], uint32_t((iu - 1) / Cfg::NUS) & 1u, abort_flag, a.status, lim);
             } else {
-                pwait(&uempty[us], ((iu / NXS) & 1) ^ 1, abort_flag, a.status);
+                pwait(&uempty[us], ((iu / NXS) & 1) ^ 1, abort_flag, a.status, lim);
             }
             if constexpr (TREE) {
                 named_bar(1, 128);      // windows written
@@ -1127,7 +1131,7 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
                 // ancestor's gate. The Gram block is raw: the inverse norms are applied here.
                 if constexpr (Cfg::BIG) {
                     // the previous unit's epilogue has read its records
-                    pwait(&uempty[us], ((iu / NXS) & 1) ^ 1, abort_flag, a.status);
+                    pwait(&uempty[us], ((iu / NXS) & 1) ^ 1, abort_flag, a.status, lim);
                     if (p < G * TMAX) {
                         meta[Cfg::M_REC + gj * Cfg::RJ + Cfg::F_GAM + gt] = g_in;
                         meta[Cfg::M_REC + gj * Cfg::RJ + Cfg::F_BET + gt] = b_in;
@@ -1233,7 +1237,7 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
             if (p == 0) mbar_arrive(&ufull[us]);
             if constexpr (Cfg::BIG) {
                 // staged rows and windows stay until the epilogue warps' v conv has read them
-                pwait(vdone, uint32_t(iu & 1), abort_flag, a.status);
+                pwait(vdone, uint32_t(iu & 1), abort_flag, a.status, lim);
                 if (p == 0) mbar_arrive(&sempty[ss]);
             }
         }
@@ -1255,12 +1259,12 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
             unit_of(iu, l, b, kh);
             const int n = n_prev(b);
             const float* kp = reinterpret_cast<const float*>(smem + Cfg::OFF_KP + size_t(iu & 1) * Cfg::KP_BYTES);
-            if (COMMIT) pwait(&kpfull[iu & 1], (iu >> 1) & 1, abort_flag, a.status);
+            if (COMMIT) pwait(&kpfull[iu & 1], (iu >> 1) & 1, abort_flag, a.status, lim);
             for (int kb = 0; kb < Cfg::KB; ++kb) {
 #pragma unroll 1
                 for (int j = 0; j < G; ++j) {
-                    pwait(&kfull[s], ph, abort_flag, a.status);
-                    pwait(&tmempty[ts], tph ^ 1, abort_flag, a.status);
+                    pwait(&kfull[s], ph, abort_flag, a.status, lim);
+                    pwait(&tmempty[ts], tph ^ 1, abort_flag, a.status, lim);
                     tc_fence_after();
                     unsigned char* Ab = smem + Cfg::OFF_RING + size_t(s) * Cfg::KSLOT;
                     const unsigned char* At = Ab + row * 128;
@@ -1368,7 +1372,7 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
             const int n = n_prev(b);
             for (int kb = 0; kb < Cfg::KB && ok; ++kb) {
                 for (int j = 0; j < G; ++j) {
-                    if (!pwait_warp(&kconv[s], ph, abort_flag, a.status)) { ok = false; break; }
+                    if (!pwait_warp(&kconv[s], ph, abort_flag, a.status, lim)) { ok = false; break; }
                     if (n > 0 && lane == 0) {
                         tma_store_2d(&smap, smem + Cfg::OFF_RING + size_t(s) * Cfg::KSLOT, kb * 32,
                                      int((lb * Hv + kh * G + j) * D));
@@ -1401,8 +1405,8 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
                 // the v heads of this unit's tree conv, into TMEM (the prep warps take q and k); the
                 // previous unit's epilogue, just finished by these warps, has read the old v
                 const IO* qs = reinterpret_cast<const IO*>(smem + Cfg::OFF_STAGE + size_t(iu % NSS) * Cfg::STAGE_BYTES);
-                pwait(winfull, uint32_t(iu & 1), abort_flag, a.status);
-                pwait(&sfull[iu % NSS], uint32_t(iu / NSS) & 1u, abort_flag, a.status);
+                pwait(winfull, uint32_t(iu & 1), abort_flag, a.status, lim);
+                pwait(&sfull[iu % NSS], uint32_t(iu / NSS) & 1u, abort_flag, a.status, lim);
                 tc_fence_after();
                 tree_vconv_tmem<Cfg>(i, qs, qs + size_t(Cfg::NPARTS) * NR * D, NR, W, T,
                                      reinterpret_cast<const int*>(scr + Cfg::S_WIN),
@@ -1411,8 +1415,8 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
                 __syncwarp();
                 if (lane == 0) mbar_arrive(vdone);
             }
-            if (COMMIT) pwait(&kpfull[iu & 1], (iu >> 1) & 1, abort_flag, a.status);
-            pwait(&ufull[us], (iu / NXS) & 1, abort_flag, a.status);
+            if (COMMIT) pwait(&kpfull[iu & 1], (iu >> 1) & 1, abort_flag, a.status, lim);
+            pwait(&ufull[us], (iu / NXS) & 1, abort_flag, a.status, lim);
             if constexpr (!TREE && TMAX >= 16)   // 16-position chains: Gram block and records here
                 chain_gram_fold<Cfg>(warp - 10, lane, tid - 320, 2, T,
                                      smem + Cfg::OFF_X + size_t(us) * Cfg::X_BYTES,
@@ -1477,7 +1481,7 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
                 named_bar(2, 128);
             }
             const int ps = iu % Cfg::NUS;
-            pwait(&tfull[ps], (iu / Cfg::NUS) & 1, abort_flag, a.status);
+            pwait(&tfull[ps], (iu / Cfg::NUS) & 1, abort_flag, a.status, lim);
             tc_fence_after();
             const uint32_t dt = tbase + ps * Cfg::P_COLS + (uint32_t(32 * q4) << 16);
 #pragma unroll 1
