@@ -48,6 +48,13 @@
 // stash those rows and the epilogue writes them out as the new conv state. So each state tile is
 // read once and written once per round, instead of read by verify, read and written by rollback.
 //
+// GDK (one decay per key channel, g [L][B][T][Hv][Dk]; chains of T <= 8): the decay of S_0 up to
+// step t is a per-column factor, so each value head has its own B tile [A_t ⊙ k_t ; A_t ⊙ q_t]
+// (A_t[c] = Π_{r≤t} a_r[c]) and the MMAs of head j read tile j; the Gram entries carry the decay
+// of each column between write s and read t, CK[t][s] = Σ_c k_s[c] k_t[c] Π_{s<r≤t} a_r[c] (CQ
+// with q_t), built by the epilogue warps as running products (never a ratio of cumulative
+// products, so a zero gate stays exact); the recurrence then runs with γ = c0 = 1.
+//
 // TREE: node v's products come from the same S_0 · [K|Q] through the ancestor-sum identity
 // (S_p k_v = Γ(root→p) S_0 k_v + Σ_{a ancestor of v} Γ(a→p) δ_a (k_a·k_v), the same with q_v): the
 // coefficient records hold Γ(a→p) times the Gram entry for ancestors and zero elsewhere, and each
@@ -61,9 +68,11 @@
 
 namespace gdn {
 
-template <typename IO, int TMAX, int G, bool COMMIT, bool TREE>
+template <typename IO, int TMAX, int G, bool COMMIT, bool TREE, bool GDK = false>
 struct PipeCfg {
     static constexpr int D = 128, KB = 4, ES = int(sizeof(IO)), TMAX_ = TMAX;
+    // B tiles per unit slot: one per value head with per-key-channel gates, else one shared
+    static constexpr int NXT = GDK ? G : 1;
     // T up to 32 (trees): one slot each for the B tile, the records and the staging (the next
     // unit's prep overlaps this unit's epilogue; see the kernel), one accumulator per chain
     static constexpr bool BIG = TMAX >= 32;
@@ -108,9 +117,11 @@ struct PipeCfg {
     static constexpr int F_C0K = 0, F_C0Q = TMAX, F_GAM = 2 * TMAX, F_BET = 3 * TMAX, F_KQ = 4 * TMAX,
                          F_CKT = 5 * TMAX, F_CQT = 5 * TMAX + TMAX * TMAX;
     // BIG keeps v in TMEM; its meta slot holds the Gram block [TMAX][2 TMAX] instead (M_V)
+    // GDK: then the plain normalised rows k_t, q_t [2 TMAX][D] for the epilogue's Gram (M_XP)
     static constexpr int M_REC = 0, M_V = G * RJ, M_GP = M_V + (BIG ? 2 * TMAX * TMAX : G * TMAX * D),
                          M_CW = M_GP + (COMMIT ? 2 * TMAX * TMAX : 0),
-                         M_FLOATS = M_CW + (COMMIT ? (NPARTS * 3 * D * ES + 3) / 4 : 0);
+                         M_XP = M_CW + (COMMIT ? (NPARTS * 3 * D * ES + 3) / 4 : 0),
+                         M_FLOATS = M_XP + (GDK ? 2 * TMAX * D : 0);
     static constexpr int META_BYTES = (M_FLOATS * 4 + 127) / 128 * 128;
     // commit slot (floats): previous round's k_s rows [TMAX][D], δ_s rows [G][TMAX][D],
     // c_s = Γ(s+1 .. n-1) [G][TMAX], Γ(0 .. n-1) [G]
@@ -133,14 +144,14 @@ struct PipeCfg {
                          S_EGP = S_WIN + (TREE ? 4 * TMAX + 4 : 0),
                          S_FLOATS = S_EGP + (COMMIT ? 4 * 128 : 0);
     // shared-memory K-block ring: as many 16 KiB slots as the rest leaves room for (at most 8)
-    static constexpr size_t REST = NXS * size_t(X_BYTES) + NSS * size_t(STAGE_BYTES) + NXS * size_t(META_BYTES) +
+    static constexpr size_t REST = NXS * NXT * size_t(X_BYTES) + NSS * size_t(STAGE_BYTES) + NXS * size_t(META_BYTES) +
                                    2 * size_t(KP_BYTES) + size_t(S_FLOATS) * 4 + 64 * 8 + 16 + 16 + 1024;
     static constexpr int NKS_FIT = int((227 * 1024 - REST) / KSLOT);
     static constexpr int NKS = NKS_FIT > 8 ? 8 : NKS_FIT;
 
     static constexpr size_t OFF_RING = 0;
     static constexpr size_t OFF_X = OFF_RING + size_t(NKS) * KSLOT;
-    static constexpr size_t OFF_STAGE = OFF_X + NXS * size_t(X_BYTES);
+    static constexpr size_t OFF_STAGE = OFF_X + NXS * NXT * size_t(X_BYTES);
     static constexpr size_t OFF_META = OFF_STAGE + NSS * size_t(STAGE_BYTES);
     static constexpr size_t OFF_KP = OFF_META + NXS * size_t(META_BYTES);
     static constexpr size_t OFF_SCR = OFF_KP + 2 * size_t(KP_BYTES);
@@ -161,6 +172,7 @@ struct PipeCfg {
                   (M_CW * 4) % 16 == 0, "records are read as float4, CW rows as 16-byte vectors");
     static_assert((KP_DL * 4) % 16 == 0 && (KP_KS * 4) % 16 == 0, "bulk-copy destinations");
     static_assert(GRAM_TILES == 1 || GRAM_TILES % 4 == 0, "Gram block: one tile, or a quarter per prep warp");
+    static_assert(!GDK || (!TREE && !COMMIT && TMAX <= 8), "per-key-channel gates: chains of T <= 8");
 };
 
 // D[tmem] (+)= A[tmem] · B[smem descriptor]ᵀ, kind::tf32. Called by a whole converged warp with
@@ -515,12 +527,71 @@ __device__ __forceinline__ void chain_gram_fold(int w4, int lane, int t128, int 
     named_bar(bar, 128);
 }
 
-template <typename IO, int TMAX, int G, bool COMMIT, bool TREE>
-__global__ void __launch_bounds__(PipeCfg<IO, TMAX, G, COMMIT, TREE>::NTHR, 1)
+// Gram block and coefficient records of a chain unit with one decay per key channel (the epilogue
+// warps run it; 128 threads, t128 = thread in the group, named barrier `bar` among them). Thread
+// (head j, write s, channel group c8) keeps w[m] = Π_{s<r≤t} a_r[c] for its channels c = c8 + 8m
+// and walks t upward: CK[t][s] = Σ_c k_s[c] w[c] k_t[c], CQ[t][s] with q_t, summed over the 8
+// lanes of the group. Also c0 = 1 (the decays of S_0 are in the B tiles) and k_s·q_s. `g_lb` is
+// the unit's gates, g + (l B + b) T Hv D.
+template <typename Cfg>
+__device__ __forceinline__ void gdk_gram_records(int t128, int kh, int Hv, int T, int bar,
+                                                 const float* g_lb, float* meta) {
+    constexpr int TMAX = Cfg::TMAX_, G = Cfg::NPARTS - 2, RS = Cfg::RS, D = Cfg::D, NJ = D / 8;
+    static_assert(TMAX <= 8 && G * TMAX * 8 <= 128, "one thread per (head, write, channel group)");
+    const int j = t128 >> 6, s = (t128 >> 3) & 7, c8 = t128 & 7;
+    const bool act = j < G && s < T;
+    const int h = kh * G + (j < G ? j : 0);
+    const float* XP = meta + Cfg::M_XP;
+    float* recj = meta + Cfg::M_REC + (j < G ? j : 0) * TMAX * RS;
+    float ks[NJ], w[NJ];
+    float kq = 0.f;
+#pragma unroll
+    for (int m = 0; m < NJ; ++m) {
+        const int c = c8 + 8 * m;
+        w[m] = 1.f;
+        ks[m] = act ? XP[s * D + c] : 0.f;
+        kq = fmaf(ks[m], act ? XP[(TMAX + s) * D + c] : 0.f, kq);
+    }
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) kq += __shfl_xor_sync(0xffffffffu, kq, o);
+    if (c8 == 0 && act) {
+        recj[s * RS + 0] = 1.f;
+        recj[s * RS + 3] = kq;
+    }
+#pragma unroll 1
+    for (int t = 1; t < TMAX; ++t) {              // the same trip count in every lane (shuffles)
+        const bool on = act && t > s && t < T;
+        float ck = 0.f, cq = 0.f;
+        if (on) {
+            const float* ga = g_lb + (size_t(t) * Hv + h) * D;
+#pragma unroll
+            for (int m = 0; m < NJ; ++m) {
+                const int c = c8 + 8 * m;
+                w[m] *= __ldg(ga + c);
+                const float kw = ks[m] * w[m];
+                ck = fmaf(kw, XP[t * D + c], ck);
+                cq = fmaf(kw, XP[(TMAX + t) * D + c], cq);
+            }
+        }
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) {
+            ck += __shfl_xor_sync(0xffffffffu, ck, o);
+            cq += __shfl_xor_sync(0xffffffffu, cq, o);
+        }
+        if (c8 == 0 && on) {
+            recj[t * RS + 4 + s] = ck;
+            recj[t * RS + 4 + TMAX + s] = cq;
+        }
+    }
+    named_bar(bar, 128);
+}
+
+template <typename IO, int TMAX, int G, bool COMMIT, bool TREE, bool GDK>
+__global__ void __launch_bounds__(PipeCfg<IO, TMAX, G, COMMIT, TREE, GDK>::NTHR, 1)
 gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap smap,
                        const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap cmap,
                        const __grid_constant__ CUtensorMap pmap, int n_units) {
-    using Cfg = PipeCfg<IO, TMAX, G, COMMIT, TREE>;
+    using Cfg = PipeCfg<IO, TMAX, G, COMMIT, TREE, GDK>;
     constexpr int D = Cfg::D, NP = Cfg::NP, XKB = Cfg::XKB, RS = Cfg::RS;
     constexpr int NXS = Cfg::NXS, NSS = Cfg::NSS;
     constexpr int NKS = Cfg::NKS, NTS = Cfg::NTS;
@@ -740,7 +811,7 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
             const int us = iu % NXS, ps = iu % Cfg::NUS;
             if (!pwait_warp(&ufull[us], (iu / NXS) & 1, abort_flag, a.status, lim)) break;
             if (!pwait_warp(&tempty[ps], ((iu / Cfg::NUS) & 1) ^ 1, abort_flag, a.status, lim)) break;
-            const uint64_t db = umma_desc_sw128(sX0 + us * Cfg::X_BYTES);
+            const uint64_t db = umma_desc_sw128(sX0 + us * Cfg::NXT * Cfg::X_BYTES);
             const uint32_t dt = tbase + ps * Cfg::P_COLS;
             for (int kb = 0; kb < Cfg::KB; ++kb) {
                 int slot[G];
@@ -772,17 +843,20 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
                             umma_tf32_ts_warp(dt + (j * S + ks % S) * Cfg::CH_COLS,
                                               tbase + Cfg::T_RING + slot[j] * 64 + 32 + ks * 8, bk, IDESC2, 1u);
                     } else {
+                        // GDK: head j reads its own B tile
 #pragma unroll
                         for (int j = 0; j < G; ++j) {
                             const int c = j * S + ks % S;
+                            const uint64_t bj = bk + uint64_t(((GDK ? j : 0) * Cfg::X_BYTES) >> 4);
                             umma_tf32_ts_warp(dt + c * Cfg::CH_COLS, tbase + Cfg::T_RING + slot[j] * 64 + ks * 8,
-                                              bk, IDESC1, acc);
+                                              bj, IDESC1, acc);
                         }
 #pragma unroll
                         for (int j = 0; j < G; ++j) {
                             const int c = j * S + ks % S;
+                            const uint64_t bj = bk + uint64_t(((GDK ? j : 0) * Cfg::X_BYTES) >> 4);
                             umma_tf32_ts_warp(dt + c * Cfg::CH_COLS + 2 * NP,
-                                              tbase + Cfg::T_RING + slot[j] * 64 + 32 + ks * 8, bk, IDESC2, acc);
+                                              tbase + Cfg::T_RING + slot[j] * 64 + 32 + ks * 8, bj, IDESC2, acc);
                         }
                     }
                 }
@@ -814,14 +888,23 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
             unsigned char* st = smem + Cfg::OFF_STAGE + size_t(ss) * Cfg::STAGE_BYTES;
             const IO* qs = reinterpret_cast<const IO*>(st);
             const IO* cws = qs + size_t(Cfg::NPARTS) * NR * D;
-            unsigned char* Xb = smem + Cfg::OFF_X + size_t(us) * Cfg::X_BYTES;
+            unsigned char* Xb = smem + Cfg::OFF_X + size_t(us) * Cfg::NXT * Cfg::X_BYTES;
             float* meta = reinterpret_cast<float*>(smem + Cfg::OFF_META + size_t(us) * Cfg::META_BYTES);
-            // gates of this thread's (value head gj, position gt), loaded early
-            float g_in = 0.f, b_in = 0.f;
+            // gates of this thread's (value head gj, position gt), loaded early; with one decay per
+            // key channel the record's γ is 1 and the thread loads its channel p of every gate row
+            float g_in = GDK ? 1.f : 0.f, b_in = 0.f;
             const int gj = p / TMAX, gt = p - gj * TMAX;
             if (p < G * TMAX && gt < T) {
-                g_in = __ldg(a.g + (lb * T + gt) * Hv + kh * G + gj);
+                if constexpr (!GDK) g_in = __ldg(a.g + (lb * T + gt) * Hv + kh * G + gj);
                 b_in = __ldg(a.beta + (lb * T + gt) * Hv + kh * G + gj);
+            }
+            float gch[GDK ? TMAX : 1][GDK ? G : 1];
+            if constexpr (GDK) {
+#pragma unroll
+                for (int t = 0; t < TMAX; ++t)
+#pragma unroll
+                    for (int j = 0; j < G; ++j)
+                        gch[t][j] = t < T ? __ldg(a.g + ((lb * T + t) * Hv + kh * G + j) * size_t(D) + p) : 1.f;
             }
             // conv window row r (0 .. W-2): old conv-state row r + n, or (COMMIT, r + n ≥ W-1) the
             // previous round's raw row staged at W-1+T+r
@@ -993,7 +1076,31 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
                                       nrm[6 * TMAX + p] + a.l2_eps);
             named_bar(1, 128);
             // B tile rows n < NP: X as raw fp32 (the tensor core reads it as X_hi = trunc_tf32(X));
-            // rows NP + n: X_lo = X − X_hi. Also the tape k, v values, gates.
+            // rows NP + n: X_lo = X − X_hi. Also the tape k, v values, gates. GDK: tile j holds
+            // A_t ⊙ k_t and A_t ⊙ q_t with head j's running product A_t of channel p's gates, and
+            // the plain rows go to the meta slot for the epilogue's Gram.
+            if constexpr (GDK) {
+                float cum[G];
+#pragma unroll
+                for (int j = 0; j < G; ++j) cum[j] = 1.f;
+#pragma unroll
+                for (int t = 0; t < TMAX; ++t) {
+                    const float kn = yk[t] * inv[t], qn = yq[t] * inv[TMAX + t];
+                    meta[Cfg::M_XP + t * D + p] = kn;
+                    meta[Cfg::M_XP + (TMAX + t) * D + p] = qn;
+                    st_global_if(a.tape_k + ((lb * T + t) * Hk + kh) * size_t(D) + p, kn, t < T);
+#pragma unroll
+                    for (int j = 0; j < G; ++j) {
+                        cum[j] *= gch[t][j];
+                        unsigned char* Xj = Xb + size_t(j) * Cfg::X_BYTES;
+                        const float xk = kn * cum[j], xq = qn * cum[j];
+                        *reinterpret_cast<float*>(Xj + sw128_off(t, p, XKB)) = xk;
+                        *reinterpret_cast<float*>(Xj + sw128_off(NP + t, p, XKB)) = xk - tf32_trunc(xk);
+                        *reinterpret_cast<float*>(Xj + sw128_off(TMAX + t, p, XKB)) = xq;
+                        *reinterpret_cast<float*>(Xj + sw128_off(NP + TMAX + t, p, XKB)) = xq - tf32_trunc(xq);
+                    }
+                }
+            } else {
 #pragma unroll
             for (int t = 0; t < TMAX; ++t) {
                 const float kn = yk[t] * inv[t], qn = yq[t] * inv[TMAX + t];
@@ -1003,10 +1110,15 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
                 *reinterpret_cast<float*>(Xb + sw128_off(NP + TMAX + t, p, XKB)) = qn - tf32_trunc(qn);
                 st_global_if(a.tape_k + ((lb * T + t) * Hk + kh) * size_t(D) + p, kn, t < T);
             }
+            }
 #pragma unroll
-            for (int n2 = 2 * TMAX; n2 < NP; ++n2) {
-                *reinterpret_cast<float*>(Xb + sw128_off(n2, p, XKB)) = 0.f;
-                *reinterpret_cast<float*>(Xb + sw128_off(NP + n2, p, XKB)) = 0.f;
+            for (int j = 0; j < Cfg::NXT; ++j) {
+                unsigned char* Xj = Xb + size_t(j) * Cfg::X_BYTES;
+#pragma unroll
+                for (int n2 = 2 * TMAX; n2 < NP; ++n2) {
+                    *reinterpret_cast<float*>(Xj + sw128_off(n2, p, XKB)) = 0.f;
+                    *reinterpret_cast<float*>(Xj + sw128_off(NP + n2, p, XKB)) = 0.f;
+                }
             }
             if (p < G * TMAX) {
                 float* rec = meta + Cfg::M_REC + p * RS;      // record (gj, gt)
@@ -1018,7 +1130,7 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
             named_bar(1, 128);
             // BIG: the Gram block lives in the meta slot
             if constexpr (Cfg::BIG) gram = meta + Cfg::M_V;
-            if constexpr (TREE || TMAX < 16) {   // 16-position chains: the epilogue warps do this
+            if constexpr ((TREE || TMAX < 16) && !GDK) {   // 16-position chains and GDK: the epilogue warps
             // Gram block on the warp tensor path: D[m][n] = X_m · k_n, 3xTF32 (hi·hi + hi·lo + lo·hi);
             // rows m: k_0.., q_0.. (zero beyond 2 TMAX). One 16 x 8 tile: each warp takes 32 channels
             // and the partials are summed; four tiles (TMAX = 16): warp pw takes tile pw, all channels.
@@ -1421,6 +1533,9 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
                 chain_gram_fold<Cfg>(warp - 10, lane, tid - 320, 2, T,
                                      smem + Cfg::OFF_X + size_t(us) * Cfg::X_BYTES,
                                      const_cast<float*>(meta), scr + Cfg::S_GRAM, scr + Cfg::S_GP);
+            if constexpr (GDK)                   // per-key-channel gates: the decayed Gram here
+                gdk_gram_records<Cfg>(tid - 320, kh, Hv, T, 2, a.g + lb * T * size_t(Hv) * D,
+                                      const_cast<float*>(meta));
             if (COMMIT && n > 0) {
                 const int et = tid - 320, ew = warp - 10;
                 // the new conv-state rows, stashed by the prep warps, to HBM as 16-byte vectors
@@ -1752,10 +1867,10 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
                      ::"r"(tbase), "r"(uint32_t(Cfg::TMEM_COLS)));
 }
 
-template <typename IO, int TMAX, int G, bool COMMIT, bool TREE = false>
+template <typename IO, int TMAX, int G, bool COMMIT, bool TREE = false, bool GDK = false>
 cudaError_t launch_verify_pipe_t(const VerifyArgs& a, const VerifyMaps& m, cudaStream_t stream) {
-    using Cfg = PipeCfg<IO, TMAX, G, COMMIT, TREE>;
-    auto kern = gdn_verify_pipe_kernel<IO, TMAX, G, COMMIT, TREE>;
+    using Cfg = PipeCfg<IO, TMAX, G, COMMIT, TREE, GDK>;
+    auto kern = gdn_verify_pipe_kernel<IO, TMAX, G, COMMIT, TREE, GDK>;
     cudaError_t e = smem_optin(reinterpret_cast<const void*>(kern), Cfg::SMEM);
     if (e != cudaSuccess) return e;
     int nsm = 0;
@@ -1769,23 +1884,27 @@ cudaError_t launch_verify_pipe_t(const VerifyArgs& a, const VerifyMaps& m, cudaS
 }
 
 // The pipelined kernel serves the Qwen3.6 head shape (chains up to 16 positions, trees up to 32
-// nodes) with one gate per value head; everything else uses the per-head kernel.
+// nodes) with one gate per value head, and chains up to 8 positions with one gate per key channel;
+// everything else uses the per-head kernel.
 template <typename IO>
 bool verify_pipe_eligible(const VerifyArgs& a, const VerifyMaps& m, int D, bool tree, bool commit) {
     const int tmax = commit ? 8 : (tree ? 32 : 16);
-    return m.inputs_ok && !a.gate_dk && !(tree && commit) && D == 128 && sizeof(IO) == 2 && a.T <= tmax &&
-           (a.Hv == a.Hk || a.Hv == 2 * a.Hk);
+    return m.inputs_ok && (!a.gate_dk || (!tree && !commit && a.T <= 8)) && !(tree && commit) &&
+           D == 128 && sizeof(IO) == 2 && a.T <= tmax && (a.Hv == a.Hk || a.Hv == 2 * a.Hk);
 }
 
-template <typename IO, int TMAX, bool COMMIT, bool TREE>
+template <typename IO, int TMAX, bool COMMIT, bool TREE, bool GDK = false>
 cudaError_t launch_verify_pipe_g(const VerifyArgs& a, const VerifyMaps& m, cudaStream_t s) {
-    return a.Hv == a.Hk ? launch_verify_pipe_t<IO, TMAX, 1, COMMIT, TREE>(a, m, s)
-                        : launch_verify_pipe_t<IO, TMAX, 2, COMMIT, TREE>(a, m, s);
+    return a.Hv == a.Hk ? launch_verify_pipe_t<IO, TMAX, 1, COMMIT, TREE, GDK>(a, m, s)
+                        : launch_verify_pipe_t<IO, TMAX, 2, COMMIT, TREE, GDK>(a, m, s);
 }
 
 template <typename IO, bool COMMIT>
 cudaError_t launch_verify_pipe(const VerifyArgs& a, const VerifyMaps& m, bool tree, cudaStream_t s) {
     if constexpr (!COMMIT) {
+        if (a.gate_dk)   // chains of T <= 8 (verify_pipe_eligible)
+            return a.T <= 4 ? launch_verify_pipe_g<IO, 4, false, false, true>(a, m, s)
+                            : launch_verify_pipe_g<IO, 8, false, false, true>(a, m, s);
         if (tree) {
             if (a.T <= 8) return launch_verify_pipe_g<IO, 8, false, true>(a, m, s);
             if (a.T <= 16) return launch_verify_pipe_g<IO, 16, false, true>(a, m, s);

@@ -113,6 +113,67 @@ def test_gpu_per_channel_gates_bf16_qwen_heads(gdnlib, Hk, Hv, T, W):
 
 
 @pytest.mark.gpu
+@pytest.mark.parametrize("Hk,Hv,T,W", [(2, 4, 1, 4), (2, 4, 3, 3), (1, 1, 4, 4), (2, 4, 4, 4),
+                                       (3, 3, 7, 4), (2, 4, 6, 2)])
+def test_gpu_per_channel_gates_pipelined_chain_lengths(gdnlib, Hk, Hv, T, W):
+    """The pipelined kernel's per-key-channel path (bf16, d = 128, chains of T <= 8: one B tile
+    per value head, the decayed Gram from the epilogue warps) at every chain-length class and
+    both head groupings, then the rollback from its tape."""
+    w = gdk_workload(128, T, io=torch.bfloat16, Hk=Hk, Hv=Hv, W=W, B=3)
+    run_gdk_verify_rollback(w, 50 + T * 7 + Hv, np.array([T, 0, max(T - 1, 0)], np.int32))
+
+
+@pytest.mark.gpu
+def test_gpu_per_channel_gates_zero_gates_stay_exact(gdnlib):
+    """Exact zero gates on some channels and positions (a closed key channel) on the pipelined
+    path: the running-product Gram has no ratio of cumulative products, so nothing divides by
+    the zero and the outputs match the oracle's per-step recurrence."""
+    from parity_util import assert_close, f64, oracle_verify, to_dev
+    from speculative_verify_gdn_gb300 import inputs as I
+    from speculative_verify_gdn_gb300.round import SpecRound
+    w = gdk_workload(128, 8, io=torch.bfloat16, Hk=2, Hv=4, B=2, L=1)
+    cw = I.model_weights(w, 9)
+    st, cs = I.initial_state(w, 9)
+    qkv, g, beta = I.round_stream(w, 0, 9)
+    g[0, 0, 2, :, ::5] = 0.0          # channels 0, 5, 10, .. closed at step 2 of sequence 0
+    g[0, 1, 0, 1, :64] = 0.0          # head 1 of sequence 1 forgets half its columns at step 0
+    g[0, 1, 5, 3, 100:] = 0.0
+    r = SpecRound(w)
+    dq, dcw, dcs, dg, db, dst = to_dev(qkv, cw, cs, g, beta, st)
+    r.verify(dq, dcw, dcs, dg, db, dst)
+    r.check_status()
+    ref = oracle_verify(w, qkv, cw, cs, g, beta, st)
+    assert_close(f64(r.out), ref["out"], "out", bf16=True)
+    assert_close(f64(r.tape_delta), ref["tape_delta"], "tape_delta")
+
+
+@pytest.mark.gpu
+def test_gpu_per_channel_gates_full_size_sampled(gdnlib):
+    """The --gate-dk workload (30 layers, batch 64, N = 8, g [L, B, T, Hv, 128]) in the bench's
+    launch configuration: 8 random (layer, sequence) units of verify compared with the oracle."""
+    from parity_util import assert_close, f64, oracle_verify
+    from speculative_verify_gdn_gb300 import inputs as I
+    from speculative_verify_gdn_gb300.round import SpecRound
+    w = I.custom(I.WORKLOADS[2], name=I.WORKLOADS[2].name + "_gdk", gate_dk=True)
+    dev = "cuda"
+    cw = I.model_weights(w, 0, dev)
+    st, cs = I.initial_state(w, 0, dev)
+    qkv, g, beta = I.round_stream(w, 0, 0, dev)
+    r = SpecRound(w)
+    r.verify(qkv, cw, cs, g, beta, st)
+    r.check_status()
+    rng = np.random.default_rng(17)
+    units = {(int(rng.integers(0, w.L)), int(rng.integers(0, w.B))) for _ in range(8)}
+    for (l, b) in sorted(units):
+        sl = lambda t: t[l:l + 1, b:b + 1].cpu()
+        ref = oracle_verify(w, sl(qkv), cw[l:l + 1].cpu(), sl(cs), sl(g), sl(beta), sl(st),
+                            L=1, B=1)
+        assert_close(f64(r.out[l:l + 1, b:b + 1]), ref["out"], "out (l=%d,b=%d)" % (l, b), bf16=True)
+        assert_close(f64(r.tape_delta[l:l + 1, b:b + 1]), ref["tape_delta"], "delta")
+        assert_close(f64(r.tape_k[l:l + 1, b:b + 1]), ref["tape_k"], "tape_k")
+
+
+@pytest.mark.gpu
 @pytest.mark.parametrize("D,T", [(128, 8), (64, 4)])
 def test_gpu_per_channel_gates_rollback_verify(gdnlib, D, T):
     """gdn_rollback_verify with per-channel gates (served as its two calls) against the oracle's
