@@ -156,7 +156,7 @@ struct PipeCfg {
     static constexpr size_t OFF_KP = OFF_META + NXS * size_t(META_BYTES);
     static constexpr size_t OFF_SCR = OFF_KP + 2 * size_t(KP_BYTES);
     static constexpr size_t OFF_BAR = (OFF_SCR + size_t(S_FLOATS) * 4 + 15) / 16 * 16;
-    static constexpr int NBAR = 3 * NKS + 2 * NTS + 8 * 2 + 3;
+    static constexpr int NBAR = 3 * NKS + 2 * NTS + 8 * 2 + 3 + 2;
     static constexpr size_t OFF_MISC = OFF_BAR + NBAR * 8;   // TMEM base, abort flag
     static constexpr size_t SMEM = OFF_MISC + 16 + 1024;
 
@@ -610,13 +610,15 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
     uint64_t* tempty = tfull + 2;                // unit's P slot read by the 4 epilogue warps
     uint64_t* sfull = tempty + 2;                // staged inputs landed
     uint64_t* sempty = sfull + 2;                // staging slot released by prep
-    uint64_t* ufull = sempty + 2;                // unit prologue (X tile, meta) ready
+    uint64_t* ufull = sempty + 2;                // unit prologue (records, meta) ready: epilogue
     uint64_t* uempty = ufull + 2;                // unit slot free: last MMA commit + 4 epilogue warps
     uint64_t* kpfull = uempty + 2;               // COMMIT: previous round's tape rows staged
     uint64_t* kpempty = kpfull + 2;              // COMMIT: commit slot read by convert and epilogue
     uint64_t* mdone = kpempty + 2;               // every MMA of this CTA complete
     uint64_t* winfull = mdone + 1;               // BIG: the unit's conv windows written (prep)
     uint64_t* vdone = mdone + 2;                 // BIG: v in TMEM, staged rows read (4 epilogue warps)
+    uint64_t* xfull = mdone + 3;                 // unit's B tile written (prep): the MMAs may start,
+                                                 // while prep goes on to the Gram block and records
     uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + Cfg::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::OFF_MISC + 4);
     float* scr = reinterpret_cast<float*>(smem + Cfg::OFF_SCR);
@@ -809,7 +811,10 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
         bool ok = true;
         for (int iu = 0; iu < n_my && ok; ++iu) {
             const int us = iu % NXS, ps = iu % Cfg::NUS;
-            if (!pwait_warp(&ufull[us], (iu / NXS) & 1, abort_flag, a.status, lim)) break;
+            // the B tile alone is enough to start; 32-node trees wait for the records too (started
+            // early, their products ran beside the prep warps' warp-level Gram and measured slower)
+            if (!pwait_warp(Cfg::BIG ? &ufull[us] : &xfull[us], (iu / NXS) & 1, abort_flag, a.status, lim))
+                break;
             if (!pwait_warp(&tempty[ps], ((iu / Cfg::NUS) & 1) ^ 1, abort_flag, a.status, lim)) break;
             const uint64_t db = umma_desc_sw128(sX0 + us * Cfg::NXT * Cfg::X_BYTES);
             const uint32_t dt = tbase + ps * Cfg::P_COLS;
@@ -1128,6 +1133,7 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
             }   // chain
             fence_async_smem();
             named_bar(1, 128);
+            if (p == 0) mbar_arrive(&xfull[us]);   // the B tile is complete: the MMAs may start
             // BIG: the Gram block lives in the meta slot
             if constexpr (Cfg::BIG) gram = meta + Cfg::M_V;
             if constexpr ((TREE || TMAX < 16) && !GDK) {   // 16-position chains and GDK: the epilogue warps
