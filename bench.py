@@ -471,10 +471,58 @@ def run_gpu(args, w, world, rank, device):
     res = dict(ms_step=ms_step, kernels=kern, roofline=roof, clocks=clk, mean_n=mean_n,
                launches=K * r.launches_per_step(fused), ms_total=ms_total, fused=fused)
 
+    # ---- the same steps launched from CUDA graphs
+    if args.graph:
+        res["graph"] = run_graph(args, w, r, pool, step, device)
+        res["graph"]["gpu_launches"] = res["launches"]
+
     # ---- end to end: host (pinned) inputs copied in, results copied out, every step
     if not args.no_e2e:
         res["e2e"] = run_e2e(args, w, r, pool, cw, state, conv_state, device, seed, fused)
     return res
+
+
+def run_graph(args, w, r, pool, step, device):
+    """The timed steps again, each launched as one CUDA graph replay instead of its calls one by
+    one: one graph per input-pool slot, captured in the order the slots come after the steps run
+    so far (so a fused step's double-buffered tape alternates as it does eagerly), each graph
+    holding the step's kernels and a copy of its accepted counts. The round counter the sampling
+    draws use is a launch argument, fixed at capture: the draws repeat every pool length, and the
+    accepted counts are logged, as in the eager loop."""
+    import torch
+    stream = torch.cuda.current_stream(device)
+    done = args.warmup + args.steps
+    logs = [torch.empty_like(r.n_acc) for _ in range(POOL)]
+    graphs = []
+    torch.cuda.synchronize(device)
+    for j in range(POOL):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            step(done + j, done + j)
+            logs[j].copy_(r.n_acc)
+        graphs.append(g)
+    K = args.steps
+    for j in range(max(args.warmup, POOL)):
+        graphs[j % POOL].replay()
+    r.check_status()
+    nlog = torch.zeros((K, w.B), dtype=torch.int32, device=device)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(device)
+    torch.cuda.synchronize(device)
+    base = max(args.warmup, POOL)
+    start.record(stream)
+    for k in range(K):
+        graphs[(base + k) % POOL].replay()
+        nlog[k].copy_(logs[(base + k) % POOL], non_blocking=True)
+    end.record(stream)
+    torch.cuda.synchronize(device)
+    barrier(device)
+    r.check_status()
+    ms = reduce_max(start.elapsed_time(end), device) / K
+    world = dist_env()[0]
+    return {"value": aggregate_tokens_per_s(world, w.B, w.N, ms), "unit": UNIT,
+            "ms_per_step": ms, "steps": K, "graphs": POOL,
+            "mean_accepted": float(nlog.float().mean().item())}
 
 
 def run_e2e(args, w, r, pool, cw, state, conv_state, device, seed, fused=False):
@@ -585,6 +633,8 @@ def main(argv=None):
     ap.add_argument("--hybrid", default=None,
                     help="time a whole hybrid round: the GDN workload plus this attention workload "
                          "(e.g. qwen36_attn_b64_n8)")
+    ap.add_argument("--graph", action="store_true",
+                    help="also time the steps launched as CUDA graph replays")
     ap.add_argument("--gate-dk", action="store_true",
                     help="one gate per key channel (g [L, B, T, Hv, d]); chain workloads only")
     args = ap.parse_args(argv)
@@ -631,6 +681,8 @@ def main(argv=None):
         "gpu_launches": res["launches"], "clocks": res["clocks"],
         "e2e": res.get("e2e"),
     }
+    if "graph" in res:
+        line["graph"] = res["graph"]
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         # the oracle single-threaded, then on every host core (one sequence per thread)
         t1u, t1a, u1, _ = oracle_unit_times(w, args.seed, args.cpu_budget / 2, w.L, 1)

@@ -116,9 +116,14 @@ class SpecRound:
         self._prev, self._cur = buf(), buf()
 
     def launches_per_step(self, fused=False):
-        """Kernel launches one step() (verify 1, accept 2 or 3, rollback 1) or one step_fused()
-        (rollback_verify 1, accept 2 or 3) enqueues, for shapes the fused kernel serves."""
-        acc = 3 if self.mode == _lib.SPEC_MODE_SAMPLE and self.w.accept != "tree" else 2
+        """Kernel launches one step() (verify 1, accept 1 to 3, rollback 1) or one step_fused()
+        (rollback_verify 1, accept 1 to 3) enqueues, for shapes the fused kernel serves: sampling
+        accept is one cluster kernel from a vocabulary of 8192 on (three kernels below), greedy and
+        tree accept two."""
+        if self.mode == _lib.SPEC_MODE_SAMPLE and self.w.accept != "tree":
+            acc = 1 if self.w.V >= 8192 else 3
+        else:
+            acc = 2
         return (1 if fused and fused_in_one_kernel(self.w) else 2) + acc
 
     def check_status(self):
