@@ -599,7 +599,7 @@ int attn_verify(const attn_dims* d, const void* q, const void* k_new, const void
         a.ws_o = static_cast<float*>(workspace);
         a.ws_ml = a.ws_o + size_t(a.splits) * a.units * a.nq * d->D;
     }
-    if (1LL * a.units * a.splits * ((a.nq + 63) / 64) >= (1LL << 31))
+    if (1LL * a.units * a.splits >= (1LL << 31))
         return fail(GDN_ERR_UNSUPPORTED, "attention grid too large");
     const cudaError_t e = gdn::launch_attn_verify(a, kmap, vmap, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "attn_verify launch");

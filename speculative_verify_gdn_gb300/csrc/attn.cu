@@ -12,10 +12,10 @@
 //     [ctx/128][D][128], so both tensor-core products read K-major, 128-byte-swizzled tiles exactly
 //     as the TMA boxes land and every tile of K and of V is one contiguous 64 KiB block in HBM (a
 //     plain [D][ctx] transpose reads 256-byte pieces 2·ctx bytes apart and ran ~5 % slower).
-//   * One CTA per (layer, sequence, kv head, key split, group of 64 query rows). Its query rows
-//     are T·(Hq/Hkv) (position, head) pairs of the kv head, zero-padded to NQ ∈ {32, 64}; with more
-//     than 64 rows the groups run as adjacent CTAs that read the same K / V tiles, the second from
-//     L2. Per 128-key tile:
+//   * Up to 64 query rows per kv head: one CTA per (layer, sequence, kv head, key split). Its
+//     query rows are T·(Hq/Hkv) (position, head) pairs of the kv head, zero-padded to NQ ∈ {32,
+//     64}. (65 to 128 rows run in the kernel further below, with the rows on the TMEM lanes.) Per
+//     128-key tile:
 //         Sᵀ[key][row]  = K_tile · Qᵀ       tcgen05, M = 128 keys, N = NQ, K = D
 //         Oᵀ[d][row]   += Vᵀ_tile · Pᵀ      tcgen05, M = 128 d-rows per chunk, N = NQ, K = 128 keys
 //     Sᵀ is double-buffered in TMEM (the next tile's product overlaps this tile's softmax) and
@@ -155,6 +155,58 @@ __global__ void __launch_bounds__(256) attn_append_kernel(const AttnArgs a) {
 }
 
 // ------------------------------------------------------------------ attention
+// TMA producer of both attention kernels (one lane): the ring in the order the tensor core
+// consumes it, K(0), K(1), V(0), K(2), V(1), ..., each stage a 32 KiB chunk of 128 keys x 128 of
+// the head dim (K) or 128 d-rows x 128 keys (Vᵀ), as two 64-wide swizzled boxes. Every copy
+// issued lands before it returns.
+template <int NST, int DCH>
+__device__ __forceinline__ void attn_produce(const AttnArgs& a, const CUtensorMap* kmap,
+                                             const CUtensorMap* vmap, unsigned char* ring,
+                                             uint64_t* full, uint64_t* empty,
+                                             volatile int* abort_flag, int lb, int kvh, int t0,
+                                             int ntiles) {
+    constexpr int D = DCH * 128, CHUNK = 128 * 128 * 2;
+    const int krow0 = (lb * a.Hkv + kvh) * a.ctx;                  // K map row of key 0
+    const int vrow0 = (lb * a.Hkv + kvh) * (a.ctx >> 7) * D;       // Vᵀ map row of tile 0
+    int stage = 0, issued = 0;
+    uint32_t ph = 0;
+    bool ok = true;
+    auto load = [&](bool isv, int tile, int c) {
+        if (!ok) return;
+        if (!pwait(&empty[stage], ph ^ 1u, abort_flag, a.status)) {
+            ok = false;
+            return;
+        }
+        mbar_arrive_expect_tx(&full[stage], uint32_t(CHUNK));
+        unsigned char* dst = ring + stage * CHUNK;
+        const int key0 = (t0 + tile) * 128;
+        if (!isv) {
+            tma_load_2d(dst, kmap, c * 128, krow0 + key0, &full[stage]);
+            tma_load_2d(dst + 16384, kmap, c * 128 + 64, krow0 + key0, &full[stage]);
+        } else {
+            const int vrow = vrow0 + (t0 + tile) * D + c * 128;
+            tma_load_2d(dst, vmap, 0, vrow, &full[stage]);
+            tma_load_2d(dst + 16384, vmap, 64, vrow, &full[stage]);
+        }
+        ++issued;
+        if (++stage == NST) {
+            stage = 0;
+            ph ^= 1u;
+        }
+    };
+    for (int c = 0; c < DCH; ++c) load(false, 0, c);
+    for (int j = 0; j < ntiles; ++j) {
+        if (j + 1 < ntiles)
+            for (int c = 0; c < DCH; ++c) load(false, j + 1, c);
+        for (int c = 0; c < DCH; ++c) load(true, j, c);
+    }
+    for (int s = 0; s < NST && s < issued; ++s) {
+        const int fills = (issued - s + NST - 1) / NST;
+        if (!mbar_wait_bounded(&full[s], uint32_t(fills - 1) & 1u))
+            set_status(a.status, GDN_STATUS_WAIT_TIMEOUT);
+    }
+}
+
 template <int D, int NQ>
 __global__ void __launch_bounds__(AttnCfg<D, NQ>::NTHR, 1)
 attn_verify_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap,
@@ -183,11 +235,9 @@ attn_verify_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap,
     uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + Cfg::OFF_MISC + 8);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    // block = (unit, key split, query-row group): the row groups of a unit are adjacent, so they
-    // run together and the second one's K / V tiles come from L2
-    const int rg = blockIdx.x % a.rgroups, rest = blockIdx.x / a.rgroups;
-    const int split = rest % a.splits, unit = rest / a.splits;
-    const int row0 = rg * NQ;                              // first query row of this CTA
+    // block = (unit, key split)
+    const int split = blockIdx.x % a.splits, unit = blockIdx.x / a.splits;
+    constexpr int row0 = 0;                                // first query row of this CTA
     const int kvh = unit % a.Hkv, lb = unit / a.Hkv, b = lb % a.B;
     const int T = a.T, G = a.group;
     const int n0 = __ldg(a.kv_len + b);
@@ -252,48 +302,8 @@ attn_verify_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap,
 
     if (warp == Cfg::PRODUCER) {
         // ---------------------------------------------------------------- TMA producer
-        if (lane == 0) {
-            const int krow0 = (lb * a.Hkv + kvh) * a.ctx;      // K map row of key 0
-            const int vrow0 = (lb * a.Hkv + kvh) * (a.ctx >> 7) * D;   // Vᵀ map row of tile 0
-            int stage = 0, issued = 0;
-            uint32_t ph = 0;
-            bool ok = true;
-            auto load = [&](bool isv, int tile, int c) {
-                if (!ok) return;
-                if (!pwait(&empty[stage], ph ^ 1u, abort_flag, a.status)) {
-                    ok = false;
-                    return;
-                }
-                mbar_arrive_expect_tx(&full[stage], uint32_t(Cfg::CHUNK));
-                unsigned char* dst = ring + stage * Cfg::CHUNK;
-                const int key0 = (t0 + tile) * 128;
-                if (!isv) {
-                    tma_load_2d(dst, &kmap, c * 128, krow0 + key0, &full[stage]);
-                    tma_load_2d(dst + 16384, &kmap, c * 128 + 64, krow0 + key0, &full[stage]);
-                } else {
-                    const int vrow = vrow0 + (t0 + tile) * D + c * 128;
-                    tma_load_2d(dst, &vmap, 0, vrow, &full[stage]);
-                    tma_load_2d(dst + 16384, &vmap, 64, vrow, &full[stage]);
-                }
-                ++issued;
-                if (++stage == NST) {
-                    stage = 0;
-                    ph ^= 1u;
-                }
-            };
-            for (int c = 0; c < DCH; ++c) load(false, 0, c);
-            for (int j = 0; j < ntiles; ++j) {
-                if (j + 1 < ntiles)
-                    for (int c = 0; c < DCH; ++c) load(false, j + 1, c);
-                for (int c = 0; c < DCH; ++c) load(true, j, c);
-            }
-            // every copy issued lands before the CTA may exit
-            for (int s = 0; s < NST && s < issued; ++s) {
-                const int fills = (issued - s + NST - 1) / NST;
-                if (!mbar_wait_bounded(&full[s], uint32_t(fills - 1) & 1u))
-                    set_status(a.status, GDN_STATUS_WAIT_TIMEOUT);
-            }
-        }
+        if (lane == 0)
+            attn_produce<NST, DCH>(a, &kmap, &vmap, ring, full, empty, abort_flag, lb, kvh, t0, ntiles);
         __syncwarp();
     } else if (warp == Cfg::MMAW) {
         // ---------------------------------------------------------------- MMA issue
@@ -541,6 +551,346 @@ attn_verify_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap,
     }
 }
 
+// ------------------------------------------------------------------ attention, 65-128 query rows
+// One CTA per (unit, key split) holds all of a kv head's query rows, on the TMEM lanes (M = 128).
+// Per 128-key tile:
+//     S[row][key]  = Q · K_tileᵀ     tcgen05, A = Q (shared memory), B = K tile, N = 128 keys
+//     O[row][d]   += P · V_tile      tcgen05, A = P (TMEM), B = Vᵀ tile, N = 128 d-rows per chunk
+// Two softmax threads per row (TMEM lane), one per half of the tile's keys; the row keeps one
+// running maximum, which both threads hold (when a tile may move it, they exchange their tile
+// maxima through shared memory).
+// P is written back as packed bf16 pairs over the first 64 columns of its tile's S buffer (S is
+// double-buffered; tile j+2's scores reuse tile j's buffer once P·V of tile j is done), so the
+// shared memory holds only Q (128 rows) and the ring. Each CTA reads every K / V tile of its key
+// range once: the 64-row kernel would run these rows as two CTAs, each reading all of them. The
+// lazy running maximum, the bf16 weights and the sums of the rounded weights are those of the
+// 64-row kernel.
+template <int D>
+struct AttnRowsCfg {
+    static constexpr int NQ = 128, DCH = D / 128;
+    // warps 0-7: softmax, warp w on TMEM lane quarter w & 3 and key half w >> 2
+    static constexpr int NSW = 8, PRODUCER = 8, MMAW = 9, NTHR = 320;
+    static constexpr int CHUNK = 128 * 128 * 2;
+    static constexpr int Q_KB = NQ * 128, Q_BYTES = (D / 64) * Q_KB;
+    static constexpr int FIXED = Q_BYTES + 2 * NQ * 4 + 17 * 8 + 16 + 1024;
+    static constexpr int NST_FIT = (227 * 1024 - FIXED) / CHUNK;
+    static constexpr int NST = NST_FIT > 6 ? 6 : NST_FIT;
+    static constexpr size_t OFF_RING = 0;
+    static constexpr size_t OFF_Q = OFF_RING + size_t(NST) * CHUNK;
+    static constexpr size_t OFF_X = OFF_Q + Q_BYTES;               // float xch[2][NQ]
+    // barriers: full[NST] empty[NST] s_full[2] p_full[2] pv_done[2] fin
+    static constexpr int NBAR = 2 * NST + 7;
+    static constexpr size_t OFF_BAR = (OFF_X + size_t(2 * NQ) * 4 + 7) / 8 * 8;
+    static constexpr size_t OFF_MISC = OFF_BAR + size_t(NBAR) * 8;   // abort flag, TMEM slot
+    static constexpr size_t SMEM = OFF_MISC + 16 + 1024;             // + base alignment slack
+    // TMEM: S buffers at [0, 128) and [128, 256) (P over the first 64 columns of each), O at
+    // [256, 256 + D)
+    static constexpr int TM_S = 0, TM_O = 256, TM_COLS = 512;
+    static_assert(D == 128 || D == 256, "head dim");
+    static_assert(OFF_Q % 1024 == 0 && Q_KB % 1024 == 0, "swizzle atoms");
+    static_assert(SMEM <= 227 * 1024 && NST >= 2, "shared memory");
+};
+
+template <int D>
+__global__ void __launch_bounds__(AttnRowsCfg<D>::NTHR, 1)
+attn_rows_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap,
+                 const __grid_constant__ CUtensorMap vmap) {
+    using Cfg = AttnRowsCfg<D>;
+    constexpr int NST = Cfg::NST, DCH = Cfg::DCH, NQ = Cfg::NQ;
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    unsigned char* ring = smem + Cfg::OFF_RING;
+    unsigned char* Qs = smem + Cfg::OFF_Q;
+    float* xch = reinterpret_cast<float*>(smem + Cfg::OFF_X);      // [key half][row]
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + Cfg::OFF_BAR);
+    uint64_t* empty = full + NST;
+    uint64_t* s_full = empty + NST;
+    uint64_t* p_full = s_full + 2;
+    uint64_t* pv_done = p_full + 2;
+    uint64_t* fin = pv_done + 2;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::OFF_MISC);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + Cfg::OFF_MISC + 8);
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int split = blockIdx.x % a.splits, unit = blockIdx.x / a.splits;
+    const int kvh = unit % a.Hkv, lb = unit / a.Hkv, b = lb % a.B;
+    const int T = a.T, G = a.group;
+    const int n0 = __ldg(a.kv_len + b);
+    if (n0 < 0 || n0 > a.ctx - T) return;                 // reported by the append kernel
+    const int t0 = split * a.tiles_per_split;              // first 128-key tile of this CTA
+    const int ntiles = min(((n0 + T + 127) >> 7) - t0, a.tiles_per_split);
+    if (ntiles <= 0) {                                     // a split past the end: empty partial
+        if (tid < a.nq) {
+            float* ml = a.ws_ml + ((size_t(split) * a.units + unit) * a.nq + tid) * 2;
+            ml[0] = -INFINITY;
+            ml[1] = 0.f;
+        }
+        return;
+    }
+
+    if (tid == 0) {
+        for (int s = 0; s < NST; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int k = 0; k < 2; ++k) {
+            mbar_init(&s_full[k], 1);
+            mbar_init(&p_full[k], Cfg::NSW);           // one lane of each softmax warp
+            mbar_init(&pv_done[k], 1);
+        }
+        mbar_init(fin, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == Cfg::MMAW) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     ::"r"(smem_u32(tslot)), "r"(uint32_t(Cfg::TM_COLS)));
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+    }
+    // query rows c = i·G + g (position i, head kvh·G + g) into the K-major swizzled A tile, zero
+    // beyond nq
+    {
+        const __nv_bfloat16* qh = a.q + (size_t(lb) * T * a.Hq + size_t(kvh) * G) * D;
+        for (int e = tid; e < NQ * (D / 8); e += Cfg::NTHR) {
+            const int c = e / (D / 8), j8 = e - c * (D / 8);
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (c < a.nq) {
+                const int i = c / G, g = c - i * G;
+                v = __ldg(reinterpret_cast<const uint4*>(qh + (size_t(i) * a.Hq + g) * D) + j8);
+            }
+            const int kb = j8 >> 3, ch = j8 & 7;
+            *reinterpret_cast<uint4*>(Qs + kb * Cfg::Q_KB + (c >> 3) * 1024 + (c & 7) * 128 +
+                                      ((ch ^ (c & 7)) << 4)) = v;
+        }
+    }
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tbase = *tslot;
+
+    if (warp == Cfg::PRODUCER) {
+        // ---------------------------------------------------------------- TMA producer
+        if (lane == 0)
+            attn_produce<NST, DCH>(a, &kmap, &vmap, ring, full, empty, abort_flag, lb, kvh, t0, ntiles);
+        __syncwarp();
+    } else if (warp == Cfg::MMAW) {
+        // ---------------------------------------------------------------- MMA issue
+        constexpr uint32_t IDESC = umma_idesc_bf16(128, 128);
+        const uint32_t sQ = smem_u32(Qs), sR = smem_u32(ring);
+        int stage = 0;
+        uint32_t ph = 0;
+        bool ok = true;
+        auto qk = [&](int j) {
+            const int buf = j & 1;
+            // the buffer's previous tile (j - 2): its P has been read by its P·V
+            if (j >= 2 && !pwait_warp(&pv_done[buf], uint32_t((j - 2) >> 1) & 1u, abort_flag, a.status)) {
+                ok = false;
+                return;
+            }
+            tc_fence_after();
+            for (int c = 0; c < DCH; ++c) {
+                if (!pwait_warp(&full[stage], ph, abort_flag, a.status)) {
+                    ok = false;
+                    return;
+                }
+                tc_fence_after();
+                const uint64_t da = umma_desc_sw128(sQ + 2 * c * Cfg::Q_KB);
+                const uint64_t db = umma_desc_sw128(sR + stage * Cfg::CHUNK);
+#pragma unroll
+                for (int kb = 0; kb < 2; ++kb)
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        umma_bf16_warp(tbase + Cfg::TM_S + buf * 128,
+                                       da + uint64_t((kb * Cfg::Q_KB + ks * 32) >> 4),
+                                       db + uint64_t((kb * 16384 + ks * 32) >> 4), IDESC,
+                                       (c | kb | ks) ? 1u : 0u);
+                umma_commit_warp(&empty[stage]);
+                if (++stage == NST) {
+                    stage = 0;
+                    ph ^= 1u;
+                }
+            }
+            umma_commit_warp(&s_full[buf]);
+        };
+        auto pv = [&](int j) {
+            const int buf = j & 1;
+            if (!pwait_warp(&p_full[buf], uint32_t(j >> 1) & 1u, abort_flag, a.status)) {
+                ok = false;
+                return;
+            }
+            tc_fence_after();
+            for (int c = 0; c < DCH; ++c) {
+                if (!pwait_warp(&full[stage], ph, abort_flag, a.status)) {
+                    ok = false;
+                    return;
+                }
+                tc_fence_after();
+                const uint64_t db = umma_desc_sw128(sR + stage * Cfg::CHUNK);
+#pragma unroll
+                for (int kb = 0; kb < 2; ++kb)
+#pragma unroll
+                    for (int ks = 0; ks < 4; ++ks)
+                        umma_bf16_ts_warp(tbase + Cfg::TM_O + c * 128,
+                                          tbase + Cfg::TM_S + buf * 128 + (kb * 4 + ks) * 8,
+                                          db + uint64_t((kb * 16384 + ks * 32) >> 4), IDESC,
+                                          (j > 0 || kb || ks) ? 1u : 0u);
+                umma_commit_warp(&empty[stage]);
+                if (++stage == NST) {
+                    stage = 0;
+                    ph ^= 1u;
+                }
+            }
+            umma_commit_warp(&pv_done[buf]);
+        };
+        // the ring order: K(0), K(1), V(0), K(2), V(1), ...
+        qk(0);
+        if (ntiles > 1 && ok) qk(1);
+        for (int j = 0; j < ntiles && ok; ++j) {
+            pv(j);
+            if (ok && j + 2 < ntiles) qk(j + 2);
+        }
+        umma_commit_warp(fin);          // arrives once every MMA issued above has completed
+    } else {
+        // ---------------------------------------------------------------- softmax warps
+        // thread = (query row = TMEM lane, key half hf). Per tile: its 64 scores; the lazy maximum
+        // (it moves only when the tile holds a score more than 8 above it: then the two threads
+        // of the row exchange their tile maxima, take the same new maximum, and rescale O, each
+        // half of its columns, and their partial sums); its weights rounded to bf16 over its half
+        // of the packed P columns, and the sum of its rounded weights.
+        const int q4 = warp & 3, hf = warp >> 2;
+        const int row = q4 * 32 + lane;
+        const uint32_t lane_off = uint32_t(q4 * 32) << 16;
+        const int pbar = 1 + q4;                     // named barrier of the quarter's two warps
+        const float sl2 = a.sl2;
+        const int mylim = n0 + (row < a.nq ? row / G : T - 1);   // the last key the row may see
+        float m = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < ntiles; ++j) {
+            const int buf = j & 1;
+            const int nvis = mylim - (t0 + j) * 128 - 64 * hf + 1;   // keys k < nvis of my half
+            ok = pwait(&s_full[buf], uint32_t(j >> 1) & 1u, abort_flag, a.status) && ok;
+            tc_fence_after();
+            const uint32_t tS = tbase + lane_off + Cfg::TM_S + buf * 128;
+            float s[64];
+            {
+                uint32_t r0[32], r1[32];
+                tmem_ld32_nw(tS + 64 * hf, r0);
+                tmem_ld32_nw(tS + 64 * hf + 32, r1);
+                tmem_wait_ld();
+#pragma unroll
+                for (int k = 0; k < 32; ++k) {
+                    s[k] = __uint_as_float(r0[k]) * sl2;
+                    s[32 + k] = __uint_as_float(r1[k]) * sl2;
+                }
+            }
+            float mh[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+            for (int k = 0; k < 64; ++k) mh[k & 3] = k < nvis ? fmaxf(mh[k & 3], s[k]) : mh[k & 3];
+            const float mhalf = fmaxf(fmaxf(mh[0], mh[1]), fmaxf(mh[2], mh[3]));
+            // both halves' S read (P may overwrite it); does any row of the quarter move?
+            if (named_bar_or(pbar, 64, mhalf > m + 8.f)) {
+                xch[hf * NQ + row] = mhalf;
+                named_bar(pbar, 64);
+                const float mt = fmaxf(xch[row], xch[NQ + row]);
+                named_bar(pbar, 64);                 // both read before the next exchange
+                const bool up = mt > m + 8.f;        // never for mt = -inf; the same in both
+              if (__any_sync(0xffffffffu, up)) {
+                const float al = up ? ((m == -INFINITY) ? 0.f : ex2(m - mt)) : 1.f;
+                if (up) {
+                    l *= al;
+                    m = mt;
+                }
+                if (j > 0) {
+                    // O holds P·V up to tile j-1: that product must be done first
+                    ok = pwait(&pv_done[(j - 1) & 1], uint32_t((j - 1) >> 1) & 1u, abort_flag,
+                               a.status) && ok;
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int c2 = 0; c2 < D / 64; ++c2) {
+                        const uint32_t tO = tbase + lane_off + Cfg::TM_O + hf * (D / 2) + 32 * c2;
+                        float o[32];
+                        tmem_ld32(tO, o);
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) o[k] *= al;
+                        tmem_st32(tO, o);
+                    }
+                    tmem_wait_st();
+                }
+              }
+            }
+            float pk[32];
+            float lp[2] = {0.f, 0.f};
+#pragma unroll
+            for (int k2 = 0; k2 < 32; ++k2) {
+                const float e0 = 2 * k2 < nvis ? ex2(s[2 * k2] - m) : 0.f;
+                const float e1 = 2 * k2 + 1 < nvis ? ex2(s[2 * k2 + 1] - m) : 0.f;
+                const __nv_bfloat162 p2 = __floats2bfloat162_rn(e0, e1);     // e0 in the low half
+                lp[k2 & 1] += __low2float(p2) + __high2float(p2);
+                pk[k2] = __uint_as_float(*reinterpret_cast<const uint32_t*>(&p2));
+            }
+            l += lp[0] + lp[1];
+            tmem_st32(tS + 32 * hf, pk);                 // packed columns of keys 64 hf ..
+            tmem_wait_st();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&p_full[buf]);
+        }
+        // ---------------------------------------------------------------- epilogue
+        ok = pwait(&pv_done[(ntiles - 1) & 1], uint32_t((ntiles - 1) >> 1) & 1u, abort_flag,
+                   a.status) && ok;
+        tc_fence_after();
+        named_bar(pbar, 64);                         // the last tile's maxima have been read
+        xch[hf * NQ + row] = l;
+        named_bar(pbar, 64);
+        const float lrow = xch[row] + xch[NQ + row];
+        if (!__any_sync(0xffffffffu, !ok)) {
+            const bool mine = row < a.nq;
+            const size_t ws_row = (size_t(split) * a.units + unit) * a.nq + row;
+            const int i = row / G, g = row - i * G;
+            __nv_bfloat16* op = a.out + ((size_t(lb) * T + i) * a.Hq + kvh * G + g) * D + hf * (D / 2);
+#pragma unroll 1
+            for (int c2 = 0; c2 < D / 64; ++c2) {
+                float o[32];
+                tmem_ld32(tbase + lane_off + Cfg::TM_O + hf * (D / 2) + 32 * c2, o);
+                if (!mine) continue;
+                if (a.splits == 1) {
+#pragma unroll
+                    for (int k8 = 0; k8 < 4; ++k8) {
+                        uint32_t w4[4];
+#pragma unroll
+                        for (int h = 0; h < 4; ++h) {
+                            const __nv_bfloat162 v2 = __floats2bfloat162_rn(o[8 * k8 + 2 * h] / lrow,
+                                                                            o[8 * k8 + 2 * h + 1] / lrow);
+                            w4[h] = *reinterpret_cast<const uint32_t*>(&v2);
+                        }
+                        *reinterpret_cast<uint4*>(op + 32 * c2 + 8 * k8) = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                    }
+                } else {
+                    float* wo = a.ws_o + ws_row * D + hf * (D / 2) + 32 * c2;
+#pragma unroll
+                    for (int k4 = 0; k4 < 8; ++k4)
+                        *reinterpret_cast<float4*>(wo + 4 * k4) =
+                            make_float4(o[4 * k4], o[4 * k4 + 1], o[4 * k4 + 2], o[4 * k4 + 3]);
+                }
+            }
+            if (a.splits > 1 && mine && hf == 0) {
+                float* ml = a.ws_ml + ws_row * 2;
+                ml[0] = m;
+                ml[1] = lrow;
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == Cfg::MMAW) {
+        tc_fence_after();
+        if (!mbar_wait_bounded(fin, 0)) set_status(a.status, GDN_STATUS_WAIT_TIMEOUT);
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;"
+                     ::"r"(tbase), "r"(uint32_t(Cfg::TM_COLS)));
+    }
+}
+
 // ------------------------------------------------------------------ split merge
 __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnArgs a) {
     const int unit = blockIdx.x, c = blockIdx.y, d = threadIdx.x;
@@ -586,20 +936,35 @@ static cudaError_t launch_attn_t(const AttnArgs& a, const CUtensorMap& kmap,
     auto kern = attn_verify_kernel<D, NQ>;
     const cudaError_t e = smem_optin(reinterpret_cast<const void*>(kern), Cfg::SMEM);
     if (e != cudaSuccess) return e;
-    kern<<<unsigned(a.units) * unsigned(a.splits) * unsigned(a.rgroups), Cfg::NTHR, Cfg::SMEM, s>>>(
+    kern<<<unsigned(a.units) * unsigned(a.splits), Cfg::NTHR, Cfg::SMEM, s>>>(
         a, kmap, vmap);
+    return cudaGetLastError();
+}
+
+template <int D>
+static cudaError_t launch_attn_rows(const AttnArgs& a, const CUtensorMap& kmap,
+                                   const CUtensorMap& vmap, cudaStream_t s) {
+    using Cfg = AttnRowsCfg<D>;
+    auto kern = attn_rows_kernel<D>;
+    const cudaError_t e = smem_optin(reinterpret_cast<const void*>(kern), Cfg::SMEM);
+    if (e != cudaSuccess) return e;
+    kern<<<unsigned(a.units) * unsigned(a.splits), Cfg::NTHR, Cfg::SMEM, s>>>(a, kmap, vmap);
     return cudaGetLastError();
 }
 
 cudaError_t launch_attn_verify(const AttnArgs& a0, const CUtensorMap& kmap,
                                const CUtensorMap& vmap, cudaStream_t s) {
-    // more than 64 query rows per kv head: groups of 64 rows in separate CTAs (each keeps the
-    // 64-row configuration's ring; the K / V tiles they share are read from HBM about once)
     AttnArgs a = a0;
-    a.rgroups = (a.nq + 63) / 64;
     attn_append_kernel<<<dim3(a.B, a.L), 256, 0, s>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    if (a.nq > 64) {
+        // 65-128 query rows per kv head: one CTA holds them all
+        e = a.D == 128 ? launch_attn_rows<128>(a, kmap, vmap, s) : launch_attn_rows<256>(a, kmap, vmap, s);
+        if (e != cudaSuccess || a.splits == 1) return e;
+        attn_combine_kernel<<<dim3(a.units, a.nq), a.D, 0, s>>>(a);
+        return cudaGetLastError();
+    }
     const int nqp = a.nq <= 32 ? 32 : 64;
     if (a.D == 128)
         e = nqp == 32 ? launch_attn_t<128, 32>(a, kmap, vmap, s) : launch_attn_t<128, 64>(a, kmap, vmap, s);

@@ -14,7 +14,6 @@ namespace gdn {
 // hold the per-split partials when splits > 1. sl2 = scale·log2(e).
 struct AttnArgs {
     int L, B, T, Hq, Hkv, D, ctx, group, nq, units, splits, tiles_per_split;
-    int rgroups;                      // CTAs per (unit, split), each taking 64 query rows
     float sl2;
     const __nv_bfloat16* q;
     const __nv_bfloat16* k_new;

@@ -113,6 +113,16 @@ def test_attn_split_keys(gdnlib):
     check_case(w, seed=11)
 
 
+@pytest.mark.parametrize("ctx,lengths,L,B", [(2048, (2000,), 1, 1), (128, (0, 112, 57), 2, 3),
+                                             (640, (600, 1, 128), 1, 3)])
+def test_attn_128_query_rows(gdnlib, ctx, lengths, L, B):
+    """T = 16 over 8 query heads per kv head: 128 query rows per kv head, run as two 64-row CTAs
+    of one cluster sharing every K / V load; with the keys split across CTAs (first case), an
+    empty cache, a cache filled to capacity by the append, and one key."""
+    check_case(workload(L=L, B=B, T=16, Hq=16, Hkv=2, D=256, ctx=ctx, lengths=lengths),
+               seed=ctx + B)
+
+
 def test_attn_large_scores_stay_finite(gdnlib):
     """Scores of a few hundred (q and k scaled up): the running maximum moves by large steps and
     the rescaling of O must keep everything finite and exact to the tolerance."""
@@ -185,11 +195,12 @@ def test_attn_round_trip_append_truncate_append(gdnlib):
     assert np.array_equal(f64(_lib.v_from_vt(dvt)), vc2)
 
 
-def test_attn_full_size_sampled_units(gdnlib):
-    """The benchmarked workload (10 layers, 64 sequences, 4096 committed rows, T = 8, 16 query
-    heads over 2 kv heads of dim 256), inputs drawn on the device; two (layer, sequence) units
-    compared with the oracle, and every output finite."""
-    w = I.ATTN_WORKLOADS["qwen36_attn_b64_n8"]
+@pytest.mark.parametrize("name", ["qwen36_attn_b64_n8", "qwen36_attn_b16_n16"])
+def test_attn_full_size_sampled_units(gdnlib, name):
+    """The benchmarked workloads (10 layers, 4096 committed rows, 16 query heads over 2 kv heads
+    of dim 256; batch 64 at T = 8, batch 16 at T = 16), inputs drawn on the device; two (layer,
+    sequence) units compared with the oracle, and every output finite."""
+    w = I.ATTN_WORKLOADS[name]
     dev = "cuda"
     q, kn, vn = I.attn_round(w, 0, 0, dev)
     kc, vc = I.attn_cache(w, 0, dev)
@@ -199,7 +210,7 @@ def test_attn_full_size_sampled_units(gdnlib):
     out = torch.empty(sh.q_shape(), dtype=torch.bfloat16, device=dev)
     st = torch.zeros(1, dtype=torch.int32, device=dev)
     kc_before = {}
-    units = [(0, 0), (7, 41)]
+    units = [(0, 0), (7, min(41, w.B - 1))]
     for (l, b) in units:
         kc_before[(l, b)] = (kc[l, b].clone(), vc[l, b].clone())
     nws = _lib.attn_workspace_bytes(sh)
