@@ -367,8 +367,9 @@ typedef struct attn_dims {
  *   out       [L][B][T][Hq][D]
  *   workspace attn_workspace_bytes(d) bytes (16-byte aligned; NULL when that is 0)
  * Rows of the caches at or beyond kv_len[b] + T are never attended, but their values are
- * multiplied by zero weights: keep them finite (allocate the caches zeroed). q, k_cache and
- * vt_cache must be 16-byte aligned (TMA). A sequence with kv_len[b] outside [0, ctx − T] sets
+ * multiplied by zero weights: keep them finite (allocate the caches zeroed). q, k_new, v_new,
+ * k_cache and vt_cache must be 16-byte aligned (TMA and 16-byte copies); otherwise
+ * GDN_ERR_INVALID_ARG. A sequence with kv_len[b] outside [0, ctx − T] sets
  * GDN_STATUS_BAD_LEN and is skipped (cache and out rows unwritten).
  */
 GDN_API int attn_verify(const attn_dims* d, const void* q, const void* k_new, const void* v_new,

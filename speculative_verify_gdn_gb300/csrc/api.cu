@@ -549,10 +549,11 @@ int attn_verify(const attn_dims* d, const void* q, const void* k_new, const void
     if (d->L == 0 || d->B == 0 || d->T == 0) return GDN_OK;
     if (!q || !k_new || !v_new || !k_cache || !vt_cache || !kv_len || !out)
         return fail(GDN_ERR_INVALID_ARG, "NULL tensor pointer");
-    if (!aligned(q, 16) || !aligned(k_new, 16) || !aligned(k_cache, 16) || !aligned(vt_cache, 16))
+    if (!aligned(q, 16) || !aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_cache, 16) ||
+        !aligned(vt_cache, 16))
         return fail(GDN_ERR_INVALID_ARG,
-                    "q, k_new, k_cache and vt_cache must be 16-byte aligned (TMA / vector copies)");
-    if (!aligned(v_new, 2) || !aligned(out, 2) || !aligned(kv_len, 4))
+                    "q, k_new, v_new, k_cache and vt_cache must be 16-byte aligned (TMA / vector copies)");
+    if (!aligned(out, 2) || !aligned(kv_len, 4))
         return fail(GDN_ERR_INVALID_ARG, "misaligned tensor pointer");
     const size_t need = attn_ws_bytes(d);
     if (need && (!workspace || workspace_bytes < need || !aligned(workspace, 16)))

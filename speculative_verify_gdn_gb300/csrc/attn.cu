@@ -127,29 +127,48 @@ __device__ __forceinline__ float warp_cols(const float* v0, int lane, int* col) 
 }
 
 // ------------------------------------------------------------------ append the new rows
+// One block per (sequence, layer, kv head). Keys: 16-byte pieces of whole rows. Values: position
+// p = n0 + i is column p % 128 of row d of tile p / 128, so the new rows go through shared memory
+// (16-byte loads, rows padded by two elements against bank conflicts) and consecutive threads
+// write consecutive positions of one d-row (contiguous runs in the transposed cache).
 __global__ void __launch_bounds__(256) attn_append_kernel(const AttnArgs a) {
-    const int b = blockIdx.x, l = blockIdx.y;
+    const int b = blockIdx.x, l = blockIdx.y, h = blockIdx.z;
     const int n0 = __ldg(a.kv_len + b);
     if (n0 < 0 || n0 > a.ctx - a.T) {
-        if (l == 0 && threadIdx.x == 0) set_status(a.status, GDN_STATUS_BAD_LEN);
+        if (l == 0 && h == 0 && threadIdx.x == 0) set_status(a.status, GDN_STATUS_BAD_LEN);
         return;
     }
     const size_t lb = size_t(l) * a.B + b;
     const int D = a.D, T = a.T, H = a.Hkv, D8 = a.D / 8;
-    // keys: 16-byte pieces of whole rows
-    for (int e = threadIdx.x; e < T * H * D8; e += blockDim.x) {
-        const int d8 = e % D8, r = e / D8, h = r % H, i = r / H;
+    if (D > 256) return;                                   // the launcher serves D <= 256
+#pragma unroll 4
+    for (int e = threadIdx.x; e < T * D8; e += blockDim.x) {
+        const int d8 = e % D8, i = e / D8;
         const uint4 v = __ldg(reinterpret_cast<const uint4*>(a.k_new + ((lb * T + i) * H + h) * size_t(D)) + d8);
         reinterpret_cast<uint4*>(a.k_cache + ((lb * H + h) * size_t(a.ctx) + n0 + i) * size_t(D))[d8] = v;
     }
-    // values: position p = n0 + i is column p % 128 of row d of tile p / 128
-    const int NT = a.ctx >> 7;
-    for (int e = threadIdx.x; e < H * D; e += blockDim.x) {
-        const int h = e / D, d = e - h * D;
-        for (int i = 0; i < T; ++i) {
-            const int p = n0 + i;
-            a.vt_cache[(((lb * H + h) * NT + (p >> 7)) * size_t(D) + d) * 128 + (p & 127)] =
-                a.v_new[((lb * T + i) * H + h) * size_t(D) + d];
+    __shared__ __nv_bfloat16 sv[16384];
+    const int NT = a.ctx >> 7, SP = D + 2;
+    const int TC = min(T, 16384 / SP);                     // positions per chunk (>= 63)
+    const __nv_bfloat16* vsrc = a.v_new + (lb * T * H + h) * size_t(D);
+    __nv_bfloat16* vdst = a.vt_cache + (lb * H + h) * size_t(NT) * D * 128;
+    for (int i0 = 0; i0 < T; i0 += TC) {
+        const int tc = min(TC, T - i0);
+        __syncthreads();
+#pragma unroll 4
+        for (int e = threadIdx.x; e < tc * D8; e += blockDim.x) {
+            const int t = e / D8, d8 = e - t * D8;
+            const uint4 v = __ldg(reinterpret_cast<const uint4*>(vsrc + size_t(i0 + t) * H * D) + d8);
+            const __nv_bfloat16* pv = reinterpret_cast<const __nv_bfloat16*>(&v);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) sv[t * SP + 8 * d8 + k] = pv[k];
+        }
+        __syncthreads();
+#pragma unroll 4
+        for (int e = threadIdx.x; e < tc * D; e += blockDim.x) {
+            const int d = e / tc, t = e - d * tc;
+            const int p = n0 + i0 + t;
+            vdst[((p >> 7) * size_t(D) + d) * 128 + (p & 127)] = sv[t * SP + d];
         }
     }
 }
@@ -955,7 +974,7 @@ static cudaError_t launch_attn_rows(const AttnArgs& a, const CUtensorMap& kmap,
 cudaError_t launch_attn_verify(const AttnArgs& a0, const CUtensorMap& kmap,
                                const CUtensorMap& vmap, cudaStream_t s) {
     AttnArgs a = a0;
-    attn_append_kernel<<<dim3(a.B, a.L), 256, 0, s>>>(a);
+    attn_append_kernel<<<dim3(a.B, a.L, a.Hkv), 256, 0, s>>>(a);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (a.nq > 64) {

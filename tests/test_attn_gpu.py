@@ -140,6 +140,26 @@ def test_attn_large_scores_stay_finite(gdnlib):
     assert_attn_close(f64(out), ref, ref_abs)
 
 
+def test_attn_misaligned_new_values_are_rejected(gdnlib):
+    """v_new is read in 16-byte pieces: a pointer off that boundary is refused before any launch,
+    and nothing is written."""
+    w = workload(L=1, B=1, T=4, Hq=4, Hkv=2, D=128, ctx=256, lengths=(10,))
+    sh = shape_of(w)
+    q, kn, vn = [t.cuda() for t in I.attn_round(w, 0, 1)]
+    kc, vc = I.attn_cache(w, 1)
+    dkc, dvt = kc.cuda(), _lib.vt_from_v(vc).cuda()
+    vbuf = torch.zeros(vn.numel() + 8, dtype=torch.bfloat16, device="cuda")
+    vshift = vbuf[1:1 + vn.numel()].view(vn.shape)          # 2 bytes past a 16-byte boundary
+    vshift.copy_(vn)
+    out = torch.full(sh.q_shape(), 7.0, dtype=torch.bfloat16, device="cuda")
+    before = dkc.clone()
+    with pytest.raises(_lib.GdnError, match="16-byte"):
+        _lib.attn_verify(sh, q, kn, vshift, dkc, dvt, torch.tensor([10], dtype=torch.int32,
+                                                                 device="cuda"), out)
+    torch.cuda.synchronize()
+    assert torch.equal(dkc, before) and bool((out == 7.0).all())
+
+
 def test_attn_bad_length_is_reported_and_skipped(gdnlib):
     w = workload(L=1, B=2, T=4, Hq=4, Hkv=2, D=128, ctx=256, lengths=(100, 100))
     q, kn, vn = I.attn_round(w, 0, 1)
