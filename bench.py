@@ -457,9 +457,15 @@ def run_gpu(args, w, world, rank, device):
             "gdn_rollback": {"ms": statistics.mean(t_rb), "bytes": statistics.mean(brb)},
         }
         step_bytes = bv + ba + statistics.mean(brb)
+    # the accept's bytes are the rows its loop reaches; beside them, every row of the call (what
+    # a pass over all N + 1 rows, such as the greedy kernels', reads)
+    io = 2 if str(w.io_dtype).endswith("bfloat16") else 4
+    kern["spec_accept"]["bytes_all_rows"] = w.B * (w.N + 1) * w.V * io + 4 * w.B * (2 * w.N + 2)
     for name, e in kern.items():
         e["GBps"] = e["bytes"] / (e["ms"] / 1e3) / 1e9
         e["frac_of_%s_peak" % peak_kind] = e["GBps"] / peak
+        if "bytes_all_rows" in e:
+            e["frac_all_rows"] = e["bytes_all_rows"] / (e["ms"] / 1e3) / 1e9 / peak
     dom = max(kern, key=lambda n: kern[n]["ms"])
     roof = {"bound": "hbm", "kernel": dom, "achieved": kern[dom]["GBps"], "peak": peak,
             "peak_source": "MEASURED_PEAKS.json hbm_gbs (%s)" % peak_kind, "unit": "GB/s",

@@ -277,7 +277,8 @@ GDN_API int spec_stats_accumulate(int32_t B, int32_t N, const int32_t* n_acc, ui
  * the committed context, row 1+v judges the children of node v. From the context, repeatedly
  * move to the lowest-numbered child whose token equals the argmax of the current row; stop when
  * none matches or after P steps. The argmax of the last row reached is the bonus token.
- *   d          B, N = T (nodes; rows per sequence are T + 1), V, dtype, strides as spec_dims
+ *   d          B, N = T (nodes, at most 4096, else GDN_ERR_UNSUPPORTED; rows per sequence are
+ *              T + 1), V, dtype, strides as spec_dims
  *   parent     [B][T] int32, tokens [B][T] int32 device (tree of gdn_verify_tree)
  *   path       [B][P] int32 device: accepted nodes root-most first, -1 padded
  *   n_acc      [B] int32; out_tokens [B][P+1] int32 (path tokens, bonus, -1 padding)

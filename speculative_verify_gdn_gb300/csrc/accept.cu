@@ -476,18 +476,21 @@ __global__ void __launch_bounds__(kAccThreads) accept_sample_scan_kernel(const A
 
 // ---------------------------------------------------------------- K3: tree walk
 __global__ void __launch_bounds__(kAccThreads) accept_tree_scan_kernel(const AcceptArgs a) {
-    extern __shared__ int s_am[];   // [T + 1]
+    extern __shared__ int s_am[];   // [T + 1], then the parents [T] and the tokens [T]
     __shared__ int s_bad;
     const int b = blockIdx.x, T = a.N, RS = T + 1, P = a.P;
-    const int32_t* par = a.parent + size_t(b) * T;
-    const int32_t* tok = a.drafts + size_t(b) * T;
+    int32_t* par = s_am + RS;       // staged in shared memory for the walk below
+    int32_t* tok = par + T;
     if (threadIdx.x == 0) s_bad = 0;
     __syncthreads();
     for (int i = threadIdx.x; i < RS; i += kAccThreads) {
         s_am[i] = key_index(row_best_key(a, b * RS + i));
         if (i < T) {
-            if (par[i] < -1 || par[i] >= i) atomicOr(&s_bad, 1);
-            if (tok[i] < 0 || tok[i] >= a.V) atomicOr(&s_bad, 2);
+            const int32_t pv = a.parent[size_t(b) * T + i], tv = a.drafts[size_t(b) * T + i];
+            par[i] = pv;
+            tok[i] = tv;
+            if (pv < -1 || pv >= i) atomicOr(&s_bad, 1);
+            if (tv < 0 || tv >= a.V) atomicOr(&s_bad, 2);
         }
     }
     __syncthreads();
@@ -996,7 +999,7 @@ template <typename LT>
 static cudaError_t tree_t(const AcceptArgs& a, cudaStream_t s) {
     const unsigned rows = unsigned(a.B) * unsigned(a.N + 1);
     accept_rowmax_kernel<LT><<<dim3(rows, a.CH), kAccThreads, 0, s>>>(a);
-    accept_tree_scan_kernel<<<a.B, kAccThreads, (a.N + 1) * sizeof(int), s>>>(a);
+    accept_tree_scan_kernel<<<a.B, kAccThreads, (3 * a.N + 1) * sizeof(int), s>>>(a);
     return cudaGetLastError();
 }
 

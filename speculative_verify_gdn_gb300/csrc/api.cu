@@ -426,6 +426,7 @@ int spec_accept_tree(const spec_dims* d, const void* logits, const int32_t* pare
     int rc = check_spec(d);
     if (rc) return rc;
     if (P < 0) return fail(GDN_ERR_INVALID_ARG, "path capacity P=%d < 0", P);
+    if (d->N > 4096) return fail(GDN_ERR_UNSUPPORTED, "tree of %d nodes > 4096", d->N);
     if (d->B == 0) return GDN_OK;
     if (!logits || !n_acc || !out_tokens || !workspace || !path ||
         (d->N > 0 && (!parent || !tokens)))

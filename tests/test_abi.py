@@ -103,6 +103,11 @@ def test_host_validation_rejects_bad_arguments_without_a_gpu(lib):
     assert "workspace" in _lib.last_error()
     assert lib.spec_accept(ct.byref(sd), fake, fake, 7, 0.0, 0, 0, fake, 1 << 20, fake, fake,
                            None, None) == 1
+    # tree accept: at most 4096 nodes (the walk stages parents and tokens in shared memory)
+    td = _lib._SpecDims(2, 4097, 1000, _lib.GDN_DTYPE_BF16, 1000, 4098 * 1000)
+    assert lib.spec_accept_tree(ct.byref(td), fake, fake, fake, 8, fake, 1 << 30, fake, fake,
+                                fake, None, None) == 2
+    assert "4096" in _lib.last_error()
 
 
 def test_rollback_verify_host_checks(lib):
