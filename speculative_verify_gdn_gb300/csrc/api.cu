@@ -293,24 +293,38 @@ int check_attn(const attn_dims* d) {
     return GDN_OK;
 }
 
-// Key splits: about two CTAs per SM of a 152-SM GB300 in total (a fixed target, so the workspace
-// size depends on the shapes alone).
-void attn_split(const attn_dims* d, int* splits, int* tiles_per_split) {
+// Work plan of the attention kernels, whose CTAs each take one SM: whole waves of units over the
+// 152 SMs of a GB300 run whole (one CTA per unit); the units left over are split into key ranges
+// so that the last wave is filled with short CTAs (at most one wave of them), and only those
+// units' partial results go through the workspace and the combine kernel. The plan depends on
+// the shapes alone, so the workspace size does too.
+void attn_plan(const attn_dims* d, int* n_full, int* splits, int* tiles_per_split) {
+    constexpr long long kSMs = 152;
     const long long units = 1LL * d->L * d->B * d->Hkv;
     const int cap = (d->ctx + 127) / 128;
-    long long want = units > 0 ? (304 + units - 1) / units : 1;
-    int sp = int(want < cap ? want : cap);
+    const long long rest = units % kSMs;
+    *n_full = int(units - rest);
+    *splits = 1;
+    *tiles_per_split = cap;
+    if (rest == 0 || cap <= 1) {
+        *n_full = int(units);
+        return;
+    }
+    long long sp = kSMs / rest;
+    if (sp > cap) sp = cap;
     if (sp < 1) sp = 1;
-    const int t = (cap + sp - 1) / sp;
+    const int t = int((cap + sp - 1) / sp);
     *tiles_per_split = t;
     *splits = (cap + t - 1) / t;
+    if (*splits == 1) *n_full = int(units);
 }
 
 size_t attn_ws_bytes(const attn_dims* d) {
-    int sp, tps;
-    attn_split(d, &sp, &tps);
-    if (sp <= 1) return 0;
-    const size_t rows = size_t(sp) * d->L * d->B * d->Hkv * size_t(d->T) * (d->Hq / d->Hkv);
+    int nf, sp, tps;
+    attn_plan(d, &nf, &sp, &tps);
+    const long long tail = 1LL * d->L * d->B * d->Hkv - nf;
+    if (sp <= 1 || tail <= 0) return 0;
+    const size_t rows = size_t(sp) * size_t(tail) * size_t(d->T) * (d->Hq / d->Hkv);
     return rows * (size_t(d->D) + 2) * 4;
 }
 
@@ -587,7 +601,7 @@ int attn_verify(const attn_dims* d, const void* q, const void* k_new, const void
     a.group = d->Hq / d->Hkv;
     a.nq = d->T * a.group;
     a.units = d->L * d->B * d->Hkv;
-    attn_split(d, &a.splits, &a.tiles_per_split);
+    attn_plan(d, &a.n_full, &a.splits, &a.tiles_per_split);
     a.sl2 = float(double(d->scale) * 1.4426950408889634);
     a.q = static_cast<const __nv_bfloat16*>(q);
     a.k_new = static_cast<const __nv_bfloat16*>(k_new);
@@ -597,11 +611,11 @@ int attn_verify(const attn_dims* d, const void* q, const void* k_new, const void
     a.out = static_cast<__nv_bfloat16*>(out);
     a.kv_len = kv_len;
     a.status = status;
-    if (a.splits > 1) {
+    if (a.splits > 1 && a.units > a.n_full) {
         a.ws_o = static_cast<float*>(workspace);
-        a.ws_ml = a.ws_o + size_t(a.splits) * a.units * a.nq * d->D;
+        a.ws_ml = a.ws_o + size_t(a.splits) * size_t(a.units - a.n_full) * a.nq * d->D;
     }
-    if (1LL * a.units * a.splits >= (1LL << 31))
+    if (1LL * a.n_full + 1LL * (a.units - a.n_full) * a.splits >= (1LL << 31))
         return fail(GDN_ERR_UNSUPPORTED, "attention grid too large");
     const cudaError_t e = gdn::launch_attn_verify(a, kmap, vmap, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "attn_verify launch");

@@ -205,6 +205,33 @@ __global__ void __launch_bounds__(256) attn_append_kernel(const AttnArgs a) {
 }
 
 // ------------------------------------------------------------------ attention
+// The work of block blk: units 0 .. n_full-1 whole (one block each, writing out), then each of the
+// remaining (tail) units as `splits` key ranges whose partial (max, sum, O) the combine kernel
+// merges. The tail fills the last wave of CTAs with short blocks instead of a few long ones.
+struct AttnWork {
+    int unit, split, tail, t0, tmax;
+    bool whole;
+};
+__device__ __forceinline__ AttnWork attn_work(const AttnArgs& a, int blk) {
+    AttnWork w;
+    if (blk < a.n_full) {
+        w.unit = blk; w.split = 0; w.tail = 0; w.t0 = 0; w.tmax = 0x3fffffff; w.whole = true;
+    } else {
+        const int j = blk - a.n_full;
+        w.tail = j / a.splits;
+        w.split = j - w.tail * a.splits;
+        w.unit = a.n_full + w.tail;
+        w.t0 = w.split * a.tiles_per_split;
+        w.tmax = a.tiles_per_split;
+        w.whole = a.splits == 1;
+    }
+    return w;
+}
+// first row of a tail block's partial results in the workspace
+__device__ __forceinline__ size_t attn_ws_row(const AttnArgs& a, const AttnWork& w) {
+    return (size_t(w.split) * (a.units - a.n_full) + w.tail) * a.nq;
+}
+
 // TMA producer of both attention kernels (one lane): the ring in the order the tensor core
 // consumes it, K(0), K(1), V(0), K(2), V(1), ..., each stage a 32 KiB chunk of 128 keys x 128 of
 // the head dim (K) or 128 d-rows x 128 keys (Vᵀ), as two 64-wide swizzled boxes. Every copy
@@ -285,18 +312,18 @@ attn_verify_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap,
     uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + Cfg::OFF_MISC + 8);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    // block = (unit, key split)
-    const int split = blockIdx.x % a.splits, unit = blockIdx.x / a.splits;
+    const AttnWork wk = attn_work(a, blockIdx.x);
+    const int unit = wk.unit;
     constexpr int row0 = 0;                                // first query row of this CTA
     const int kvh = unit % a.Hkv, lb = unit / a.Hkv, b = lb % a.B;
     const int T = a.T, G = a.group;
     const int n0 = __ldg(a.kv_len + b);
     if (n0 < 0 || n0 > a.ctx - T) return;                 // reported by the append kernel
-    const int t0 = split * a.tiles_per_split;              // first 128-key tile of this CTA
-    const int ntiles = min(((n0 + T + 127) >> 7) - t0, a.tiles_per_split);
+    const int t0 = wk.t0;                                  // first 128-key tile of this CTA
+    const int ntiles = min(((n0 + T + 127) >> 7) - t0, wk.tmax);
     if (ntiles <= 0) {                                     // a split past the end: empty partial
         if (tid < NQ && row0 + tid < a.nq) {
-            float* ml = a.ws_ml + ((size_t(split) * a.units + unit) * a.nq + row0 + tid) * 2;
+            float* ml = a.ws_ml + (attn_ws_row(a, wk) + row0 + tid) * 2;
             ml[0] = -INFINITY;
             ml[1] = 0.f;
         }
@@ -564,7 +591,7 @@ attn_verify_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap,
         const bool bad = named_bar_or(1, SMT, !ok);
         tc_fence_after();
         if (!bad) {
-            const size_t ws_row = (size_t(split) * a.units + unit) * a.nq;
+            const size_t ws_row = attn_ws_row(a, wk);
 #pragma unroll 1
             for (int c2 = 0; c2 < DCH; ++c2) {
                 float o[32];
@@ -574,7 +601,7 @@ attn_verify_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap,
                 for (int k = 0; k < 32; ++k) {
                     const int c = col0 + k, cg = row0 + c;      // local and unit-wide row
                     if (cg < a.nq) {
-                        if (a.splits == 1) {
+                        if (wk.whole) {
                             const int i = cg / G, g = cg - i * G;
                             a.out[((size_t(lb) * T + i) * a.Hq + kvh * G + g) * D + d] =
                                 __float2bfloat16_rn(o[k] / lfin[c]);
@@ -584,7 +611,7 @@ attn_verify_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap,
                     }
                 }
             }
-            if (a.splits > 1 && tid < NQ && row0 + tid < a.nq) {
+            if (!wk.whole && tid < NQ && row0 + tid < a.nq) {
                 float* ml = a.ws_ml + (ws_row + row0 + tid) * 2;
                 ml[0] = m_run[tid];
                 ml[1] = l_fin;
@@ -662,16 +689,17 @@ attn_rows_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap,
     uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + Cfg::OFF_MISC + 8);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int split = blockIdx.x % a.splits, unit = blockIdx.x / a.splits;
+    const AttnWork wk = attn_work(a, blockIdx.x);
+    const int unit = wk.unit;
     const int kvh = unit % a.Hkv, lb = unit / a.Hkv, b = lb % a.B;
     const int T = a.T, G = a.group;
     const int n0 = __ldg(a.kv_len + b);
     if (n0 < 0 || n0 > a.ctx - T) return;                 // reported by the append kernel
-    const int t0 = split * a.tiles_per_split;              // first 128-key tile of this CTA
-    const int ntiles = min(((n0 + T + 127) >> 7) - t0, a.tiles_per_split);
+    const int t0 = wk.t0;                                  // first 128-key tile of this CTA
+    const int ntiles = min(((n0 + T + 127) >> 7) - t0, wk.tmax);
     if (ntiles <= 0) {                                     // a split past the end: empty partial
         if (tid < a.nq) {
-            float* ml = a.ws_ml + ((size_t(split) * a.units + unit) * a.nq + tid) * 2;
+            float* ml = a.ws_ml + (attn_ws_row(a, wk) + tid) * 2;
             ml[0] = -INFINITY;
             ml[1] = 0.f;
         }
@@ -896,7 +924,7 @@ attn_rows_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap,
         const float lrow = xch[row] + xch[NQ + row];
         if (!__any_sync(0xffffffffu, !ok)) {
             const bool mine = row < a.nq;
-            const size_t ws_row = (size_t(split) * a.units + unit) * a.nq + row;
+            const size_t ws_row = attn_ws_row(a, wk) + row;
             const int i = row / G, g = row - i * G;
             __nv_bfloat16* op = a.out + ((size_t(lb) * T + i) * a.Hq + kvh * G + g) * D + hf * (D / 2);
 #pragma unroll 1
@@ -904,7 +932,7 @@ attn_rows_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap,
                 float o[32];
                 tmem_ld32(tbase + lane_off + Cfg::TM_O + hf * (D / 2) + 32 * c2, o);
                 if (!mine) continue;
-                if (a.splits == 1) {
+                if (wk.whole) {
 #pragma unroll
                     for (int k8 = 0; k8 < 4; ++k8) {
                         uint32_t w4[4];
@@ -924,7 +952,7 @@ attn_rows_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap,
                             make_float4(o[4 * k4], o[4 * k4 + 1], o[4 * k4 + 2], o[4 * k4 + 3]);
                 }
             }
-            if (a.splits > 1 && mine && hf == 0) {
+            if (!wk.whole && mine && hf == 0) {
                 float* ml = a.ws_ml + ws_row * 2;
                 ml[0] = m;
                 ml[1] = lrow;
@@ -942,28 +970,59 @@ attn_rows_kernel(const AttnArgs a, const __grid_constant__ CUtensorMap kmap,
 }
 
 // ------------------------------------------------------------------ split merge
+// block (tail unit, group of kCombRows query rows), thread = d; the partials of split s are at
+// row (s · n_tail + tail) · nq. A split that saw no key has sum 0 and an unwritten O (read, never
+// used).
+constexpr int kCombRows = 8;
 __global__ void __launch_bounds__(256) attn_combine_kernel(const AttnArgs a) {
-    const int unit = blockIdx.x, c = blockIdx.y, d = threadIdx.x;
+    const int tail = blockIdx.x, unit = a.n_full + tail, d = threadIdx.x;
+    const int c0 = blockIdx.y * kCombRows;
+    const size_t n_tail = size_t(a.units - a.n_full);
     const int kvh = unit % a.Hkv, lb = unit / a.Hkv, b = lb % a.B;
     const int n0 = __ldg(a.kv_len + b);
     if (n0 < 0 || n0 > a.ctx - a.T) return;
-    float mstar = -INFINITY;
+    const size_t sstride = n_tail * a.nq;                  // rows between splits
+    const float2* mlp = reinterpret_cast<const float2*>(a.ws_ml);
+    float mstar[kCombRows], num[kCombRows], den[kCombRows];
+#pragma unroll
+    for (int r = 0; r < kCombRows; ++r) { mstar[r] = -INFINITY; num[r] = 0.f; den[r] = 0.f; }
+    const int nr = min(kCombRows, a.nq - c0);
     for (int s = 0; s < a.splits; ++s) {
-        const float* ml = a.ws_ml + ((size_t(s) * a.units + unit) * a.nq + c) * 2;
-        if (ml[1] > 0.f) mstar = fmaxf(mstar, ml[0]);
-    }
-    float num = 0.f, den = 0.f;
-    for (int s = 0; s < a.splits; ++s) {
-        const size_t row = (size_t(s) * a.units + unit) * a.nq + c;
-        const float* ml = a.ws_ml + row * 2;
-        if (ml[1] > 0.f) {
-            const float w = ex2(ml[0] - mstar);
-            num = fmaf(w, a.ws_o[row * a.D + d], num);
-            den = fmaf(w, ml[1], den);
+        const size_t row0 = s * sstride + size_t(tail) * a.nq + c0;
+#pragma unroll
+        for (int r = 0; r < kCombRows; ++r) {
+            if (r < nr) {
+                const float2 ml = mlp[row0 + r];
+                mstar[r] = ml.y > 0.f ? fmaxf(mstar[r], ml.x) : mstar[r];
+            }
         }
     }
-    const int i = c / a.group, g = c - i * a.group;
-    a.out[((size_t(lb) * a.T + i) * a.Hq + kvh * a.group + g) * a.D + d] = __float2bfloat16_rn(num / den);
+    for (int s = 0; s < a.splits; ++s) {
+        const size_t row0 = s * sstride + size_t(tail) * a.nq + c0;
+        float2 ml[kCombRows];
+        float o[kCombRows];
+#pragma unroll
+        for (int r = 0; r < kCombRows; ++r) {
+            ml[r] = r < nr ? mlp[row0 + r] : make_float2(0.f, 0.f);
+            o[r] = r < nr ? a.ws_o[(row0 + r) * a.D + d] : 0.f;
+        }
+#pragma unroll
+        for (int r = 0; r < kCombRows; ++r) {
+            if (ml[r].y > 0.f) {
+                const float w = ex2(ml[r].x - mstar[r]);
+                num[r] = fmaf(w, o[r], num[r]);
+                den[r] = fmaf(w, ml[r].y, den[r]);
+            }
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < kCombRows; ++r) {
+        if (r < nr) {
+            const int c = c0 + r, i = c / a.group, g = c - i * a.group;
+            a.out[((size_t(lb) * a.T + i) * a.Hq + kvh * a.group + g) * a.D + d] =
+                __float2bfloat16_rn(num[r] / den[r]);
+        }
+    }
 }
 
 // ------------------------------------------------------------------ truncation
@@ -986,8 +1045,8 @@ static cudaError_t launch_attn_t(const AttnArgs& a, const CUtensorMap& kmap,
     auto kern = attn_verify_kernel<D, NQ>;
     const cudaError_t e = smem_optin(reinterpret_cast<const void*>(kern), Cfg::SMEM);
     if (e != cudaSuccess) return e;
-    kern<<<unsigned(a.units) * unsigned(a.splits), Cfg::NTHR, Cfg::SMEM, s>>>(
-        a, kmap, vmap);
+    kern<<<unsigned(a.n_full) + unsigned(a.units - a.n_full) * unsigned(a.splits), Cfg::NTHR,
+           Cfg::SMEM, s>>>(a, kmap, vmap);
     return cudaGetLastError();
 }
 
@@ -998,7 +1057,8 @@ static cudaError_t launch_attn_rows(const AttnArgs& a, const CUtensorMap& kmap,
     auto kern = attn_rows_kernel<D>;
     const cudaError_t e = smem_optin(reinterpret_cast<const void*>(kern), Cfg::SMEM);
     if (e != cudaSuccess) return e;
-    kern<<<unsigned(a.units) * unsigned(a.splits), Cfg::NTHR, Cfg::SMEM, s>>>(a, kmap, vmap);
+    kern<<<unsigned(a.n_full) + unsigned(a.units - a.n_full) * unsigned(a.splits), Cfg::NTHR,
+           Cfg::SMEM, s>>>(a, kmap, vmap);
     return cudaGetLastError();
 }
 
@@ -1011,8 +1071,8 @@ cudaError_t launch_attn_verify(const AttnArgs& a0, const CUtensorMap& kmap,
     if (a.nq > 64) {
         // 65-128 query rows per kv head: one CTA holds them all
         e = a.D == 128 ? launch_attn_rows<128>(a, kmap, vmap, s) : launch_attn_rows<256>(a, kmap, vmap, s);
-        if (e != cudaSuccess || a.splits == 1) return e;
-        attn_combine_kernel<<<dim3(a.units, a.nq), a.D, 0, s>>>(a);
+        if (e != cudaSuccess || a.splits == 1 || a.units == a.n_full) return e;
+        attn_combine_kernel<<<dim3(a.units - a.n_full, (a.nq + kCombRows - 1) / kCombRows), a.D, 0, s>>>(a);
         return cudaGetLastError();
     }
     const int nqp = a.nq <= 32 ? 32 : 64;
@@ -1020,8 +1080,8 @@ cudaError_t launch_attn_verify(const AttnArgs& a0, const CUtensorMap& kmap,
         e = nqp == 32 ? launch_attn_t<128, 32>(a, kmap, vmap, s) : launch_attn_t<128, 64>(a, kmap, vmap, s);
     else
         e = nqp == 32 ? launch_attn_t<256, 32>(a, kmap, vmap, s) : launch_attn_t<256, 64>(a, kmap, vmap, s);
-    if (e != cudaSuccess || a.splits == 1) return e;
-    attn_combine_kernel<<<dim3(a.units, a.nq), a.D, 0, s>>>(a);
+    if (e != cudaSuccess || a.splits == 1 || a.units == a.n_full) return e;
+    attn_combine_kernel<<<dim3(a.units - a.n_full, (a.nq + kCombRows - 1) / kCombRows), a.D, 0, s>>>(a);
     return cudaGetLastError();
 }
 

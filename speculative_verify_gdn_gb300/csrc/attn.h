@@ -14,6 +14,8 @@ namespace gdn {
 // hold the per-split partials when splits > 1. sl2 = scale·log2(e).
 struct AttnArgs {
     int L, B, T, Hq, Hkv, D, ctx, group, nq, units, splits, tiles_per_split;
+    int n_full;                       // units 0 .. n_full-1 run whole (one CTA each); the others
+                                      // are split into `splits` key ranges of tiles_per_split
     float sl2;
     const __nv_bfloat16* q;
     const __nv_bfloat16* k_new;

@@ -181,7 +181,11 @@ def test_attn_host_checks(lib):
     call = lambda dd, ptrs, ws=None, nws=0: lib.attn_verify(ct.byref(dd), *ptrs, ws, nws, None,
                                                             None)
     assert call(d, [None] * 7) == 1 and "NULL" in _lib.last_error()
-    assert lib.attn_workspace_bytes(ct.byref(d)) == 0          # 1280 units: no key split
+    # 1280 units: 1216 run whole (8 waves over 152 SMs), the 64 left over as 2 key ranges each,
+    # whose partials (64 query rows of D + 2 floats) go through the workspace
+    assert lib.attn_workspace_bytes(ct.byref(d)) == 2 * 64 * 64 * (256 + 2) * 4
+    whole = _lib.AttnShape(L=4, B=19, T=8, Hq=16, Hkv=2, D=256, ctx=4224)     # 152 units
+    assert _lib.attn_workspace_bytes(whole) == 0
     small = _lib.AttnShape(L=1, B=1, T=8, Hq=16, Hkv=2, D=256, ctx=4224)
     assert _lib.attn_workspace_bytes(small) > 0
     # the split case needs its workspace

@@ -123,6 +123,16 @@ def test_attn_128_query_rows(gdnlib, ctx, lengths, L, B):
                seed=ctx + B)
 
 
+@pytest.mark.parametrize("T", [8, 16])
+def test_attn_whole_and_split_units_in_one_call(gdnlib, T):
+    """154 units: 152 run whole (one wave over 152 SMs), the 2 left over as key ranges whose
+    partials the combine kernel merges; both kernels (64 and 128 query rows), ragged lengths."""
+    w = workload(L=1, B=77, T=T, Hq=16, Hkv=2, D=128, ctx=512,
+                 lengths=(0, 300, 512 - T, 129, 77, 200, 1))
+    assert _lib.attn_workspace_bytes(shape_of(w)) > 0
+    check_case(w, seed=T)
+
+
 def test_attn_large_scores_stay_finite(gdnlib):
     """Scores of a few hundred (q and k scaled up): the running maximum moves by large steps and
     the rescaling of O must keep everything finite and exact to the tolerance."""
@@ -230,7 +240,7 @@ def test_attn_full_size_sampled_units(gdnlib, name):
     out = torch.empty(sh.q_shape(), dtype=torch.bfloat16, device=dev)
     st = torch.zeros(1, dtype=torch.int32, device=dev)
     kc_before = {}
-    units = [(0, 0), (7, min(41, w.B - 1))]
+    units = [(0, 0), (7, min(41, w.B - 1)), (w.L - 1, w.B - 1)]   # the last: a key-split tail unit
     for (l, b) in units:
         kc_before[(l, b)] = (kc[l, b].clone(), vc[l, b].clone())
     nws = _lib.attn_workspace_bytes(sh)
