@@ -187,6 +187,18 @@ __device__ __forceinline__ void umma_tf32_ts_warp(uint32_t dtmem, uint32_t atmem
         : "memory");
 }
 
+// ldmatrix with 16-bit 8 x 8 matrices on fp32 data: each lane receives the 32-bit word (row
+// lane / 4, word lane % 4) of each matrix, which are the m16n8k8 tf32 fragment positions. Lanes
+// 8j .. 8j+7 give the 16-byte row addresses of matrix j.
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]) : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t (&r)[2]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];"
+                 : "=r"(r[0]), "=r"(r[1]) : "r"(addr));
+}
+
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,"
@@ -399,8 +411,10 @@ __device__ __forceinline__ void chain_gram_fold(int w4, int lane, int t128, int 
       for (int ks = 0; ks < 16; ++ks) {
         const int ka = NACC == 1 ? 0 : (ks & 3);
         const int ch = 8 * ks + gt4;
-        const float bv0 = *reinterpret_cast<const float*>(Xb + sw128_off(8 * nt + gq, ch, XKB));
-        const float bv1 = *reinterpret_cast<const float*>(Xb + sw128_off(8 * nt + gq, ch + 4, XKB));
+        // B: rows 8 nt .., channels 8 ks + 0..3 and + 4..7 (ldmatrix, lanes 0..15)
+        uint32_t rb[2];
+        ldsm_x2(smem_u32(Xb + sw128_off(8 * nt + (lane & 7), 8 * ks + ((lane >> 3) & 1) * 4, XKB)), rb);
+        const float bv0 = __uint_as_float(rb[0]), bv1 = __uint_as_float(rb[1]);
         const float bh0 = tf32_trunc(bv0), bh1 = tf32_trunc(bv1);
         const uint32_t bl0 = __float_as_uint(tf32_trunc(bv0 - bh0));
         const uint32_t bl1 = __float_as_uint(tf32_trunc(bv1 - bh1));
@@ -408,11 +422,12 @@ __device__ __forceinline__ void chain_gram_fold(int w4, int lane, int t128, int 
 #pragma unroll
         for (int m = 0; m < TPW; ++m) {
             const int mt = TPW == 1 ? w4 / NTN : m;
-            float av[4];
-            av[0] = *reinterpret_cast<const float*>(Xb + sw128_off(16 * mt + gq, ch, XKB));
-            av[2] = *reinterpret_cast<const float*>(Xb + sw128_off(16 * mt + gq, ch + 4, XKB));
-            av[1] = *reinterpret_cast<const float*>(Xb + sw128_off(16 * mt + gq + 8, ch, XKB));
-            av[3] = *reinterpret_cast<const float*>(Xb + sw128_off(16 * mt + gq + 8, ch + 4, XKB));
+            // A: rows 16 mt + 0..7 / 8..15, channels 8 ks + 0..3 / 4..7 (ldmatrix)
+            uint32_t ra[4];
+            ldsm_x4(smem_u32(Xb + sw128_off(16 * mt + ((lane >> 3) & 1) * 8 + (lane & 7),
+                                            8 * ks + (lane >> 4) * 4, XKB)), ra);
+            const float av[4] = {__uint_as_float(ra[0]), __uint_as_float(ra[1]), __uint_as_float(ra[2]),
+                                 __uint_as_float(ra[3])};
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
                 const float h = tf32_trunc(av[e]);
@@ -1158,8 +1173,10 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
               for (int ks = 0; ks < 16; ++ks) {
                 const int ka = NACC == 1 ? 0 : (ks & 3);
                 const int ch = 8 * ks + gt4;
-                const float bv0 = *reinterpret_cast<const float*>(Xb + sw128_off(8 * nt + gq, ch, XKB));
-                const float bv1 = *reinterpret_cast<const float*>(Xb + sw128_off(8 * nt + gq, ch + 4, XKB));
+                // B: rows 8 nt .., channels 8 ks + 0..3 and + 4..7 (ldmatrix, lanes 0..15)
+                uint32_t rb[2];
+                ldsm_x2(smem_u32(Xb + sw128_off(8 * nt + (lane & 7), 8 * ks + ((lane >> 3) & 1) * 4, XKB)), rb);
+                const float bv0 = __uint_as_float(rb[0]), bv1 = __uint_as_float(rb[1]);
                 const float bh0 = tf32_trunc(bv0), bh1 = tf32_trunc(bv1);
                 const uint32_t bl0 = __float_as_uint(tf32_trunc(bv0 - bh0));
                 const uint32_t bl1 = __float_as_uint(tf32_trunc(bv1 - bh1));
@@ -1167,11 +1184,12 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
 #pragma unroll
                 for (int m = 0; m < TPW; ++m) {
                     const int mt = TPW == 1 ? pw / NTN : m;
-                    float av[4];
-                    av[0] = *reinterpret_cast<const float*>(Xb + sw128_off(16 * mt + gq, ch, XKB));
-                    av[2] = *reinterpret_cast<const float*>(Xb + sw128_off(16 * mt + gq, ch + 4, XKB));
-                    av[1] = *reinterpret_cast<const float*>(Xb + sw128_off(16 * mt + gq + 8, ch, XKB));
-                    av[3] = *reinterpret_cast<const float*>(Xb + sw128_off(16 * mt + gq + 8, ch + 4, XKB));
+                    // A: rows 16 mt + 0..7 / 8..15, channels 8 ks + 0..3 / 4..7 (ldmatrix)
+                    uint32_t ra[4];
+                    ldsm_x4(smem_u32(Xb + sw128_off(16 * mt + ((lane >> 3) & 1) * 8 + (lane & 7),
+                                                    8 * ks + (lane >> 4) * 4, XKB)), ra);
+                    const float av[4] = {__uint_as_float(ra[0]), __uint_as_float(ra[1]), __uint_as_float(ra[2]),
+                                         __uint_as_float(ra[3])};
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const float h = tf32_trunc(av[e]);
