@@ -91,34 +91,46 @@ struct PipeCfg {
     // the unit's value heads, column j TMAX + t, lane = value row (written by the epilogue warps)
     static constexpr int TMEM_COLS = 512;
     static constexpr int CH_COLS = BIG ? NP : (3 * NP + 31) / 32 * 32, P_COLS = 2 * CH_COLS;
-    static constexpr int NUS = (TMAX <= 8 || BIG) ? 2 : 1;
+    static constexpr int NUS = TMAX <= 8 ? 2 : 1;
     static constexpr int T_RING = NUS * P_COLS;
     static constexpr int V_COLS = BIG ? G * TMAX : 0;
-    static constexpr int NTS_FIT = (TMEM_COLS - T_RING - V_COLS) / 64;
+    // BIG: the epilogue's triangular solve on the tensor core: its A operand r (hi 32 + lo 32
+    // columns) at T_R, its accumulator [δ | o] (64 columns) at T_D, both 64-column aligned ahead of v
+    static constexpr int UT_COLS = BIG ? 128 : 0;
+    static constexpr int NTS_FIT = (TMEM_COLS - T_RING - V_COLS - UT_COLS) / 64;
     static constexpr int NTS = NTS_FIT < 4 ? NTS_FIT : 4;
-    static constexpr int T_V = T_RING + NTS * 64;
+    static constexpr int T_R = T_RING + NTS * 64, T_D = T_R + 64, T_V = T_R + UT_COLS;
     static constexpr int NPARTS = 2 + G;                     // q, k, v of each value head
     // staged rows per part (W <= 4): W-1 old conv-state rows, the T qkv rows and, when committing,
     // W-1 rows of the previous round's qkv ending at its accepted count
     static constexpr int NRMAX = 3 + TMAX + (COMMIT ? 3 : 0);
     static constexpr int RAW_BYTES = NPARTS * NRMAX * D * ES + NPARTS * D * 4 * ES;
-    static constexpr int STAGE_BYTES = (RAW_BYTES + 127) / 128 * 128;
+    // (BIG: a 1024-byte multiple, so the meta slot after it starts on a swizzle-atom boundary)
+    static constexpr int STAGE_BYTES = BIG ? (RAW_BYTES + 1023) / 1024 * 1024 : (RAW_BYTES + 127) / 128 * 128;
     // meta slot (floats): per value head j and position t a record {c0, γ, β, k_t·q_t, (TREE)
     // c0q, group mask, 0, 0, CK[TMAX], CQ[TMAX]} (16-byte aligned), the conv outputs V[G][TMAX][D]
     // and, COMMIT, GP[s][c] = k'_s·X_c of the previous round's k'_s and the new conv-state rows
     // CW[NPARTS][3][D] (io type). Trees keep raw (unnormalised) q, k in the B tile: c0 and c0q
     // carry 1/|k_t| and 1/|q_t|, and bit g of the mask is set when CK / CQ entries 4g .. 4g+3 can
     // be nonzero (ancestors only).
-    // BIG (T = 32 trees) uses a per-head block instead: fields c0k, c0q, γ, β, k·q [5][TMAX], then
-    // CK and CQ transposed ([x][t], the epilogue pushes δ_x into every later t)
+    // BIG (T = 32 trees) uses per-head blocks instead: CK and CQ transposed ([x][t], zero for
+    // non-ancestors) of each head (M_REC, RJ apart), a 16 KiB operand tile (M_UT), then the fields
+    // c0k, c0q, γ, β, k·q [5][TMAX] of each head (M_FLD, FJ apart), the unit's parents [TMAX] (ints,
+    // M_PAR; -1 past T). The epilogue turns CK, CQ into
+    // the solve's B operand [M | N] (64 rows x 32 fp32, hi rows then lo rows, 128-byte swizzle):
+    // head 0's into M_UT, head 1's over the CK / CQ blocks once every thread has read them.
     static constexpr int HDR = TREE ? 8 : 4;
     static constexpr int RS = HDR + 2 * TMAX;
-    static constexpr int RJ = BIG ? 5 * TMAX + 2 * TMAX * TMAX : TMAX * RS;
+    static constexpr int RJ = BIG ? 2 * TMAX * TMAX : TMAX * RS;
+    static constexpr int F_CKT = 0, F_CQT = TMAX * TMAX;
     static constexpr int F_C0K = 0, F_C0Q = TMAX, F_GAM = 2 * TMAX, F_BET = 3 * TMAX, F_KQ = 4 * TMAX,
-                         F_CKT = 5 * TMAX, F_CQT = 5 * TMAX + TMAX * TMAX;
+                         FJ = 5 * TMAX;
+    static constexpr int UT_FLOATS = BIG ? 2 * 64 * 32 : 0;
     // BIG keeps v in TMEM; its meta slot holds the Gram block [TMAX][2 TMAX] instead (M_V)
     // GDK: then the plain normalised rows k_t, q_t [2 TMAX][D] for the epilogue's Gram (M_XP)
-    static constexpr int M_REC = 0, M_V = G * RJ, M_GP = M_V + (BIG ? 2 * TMAX * TMAX : G * TMAX * D),
+    static constexpr int M_REC = 0, M_UT = G * RJ, M_FLD = M_UT + UT_FLOATS, M_PAR = M_FLD + (BIG ? G * FJ : 0),
+                         M_V = M_PAR + (BIG ? TMAX : 0),
+                         M_GP = M_V + (BIG ? 2 * TMAX * TMAX : G * TMAX * D),
                          M_CW = M_GP + (COMMIT ? 2 * TMAX * TMAX : 0),
                          M_XP = M_CW + (COMMIT ? (NPARTS * 3 * D * ES + 3) / 4 : 0),
                          M_FLOATS = M_XP + (GDK ? 2 * TMAX * D : 0);
@@ -134,11 +146,11 @@ struct PipeCfg {
     // Gram block X_m · k_n (m < 2 TMAX, n < TMAX) in 16 x 8 mma.sync tiles: one tile (TMAX <= 8)
     // split over the 4 prep warps by channels, or 4 / 16 tiles (TMAX = 16 / 32), a quarter per warp
     static constexpr int GRAM_TILES = ((2 * TMAX + 15) / 16) * ((TMAX + 7) / 8);
-    // prep scratch (floats): norm partials [4][2TMAX], inverse norms [2TMAX], Gram partials
+    // prep scratch (floats): norm partials [4][2TMAX] (chains), inverse norms [2TMAX], Gram partials
     // [4 warps][16][8] (one-tile case), Gram [TMAX][2TMAX] (BIG: in the meta slot instead),
     // tree parents [TMAX] and conv-window offsets [TMAX][4] (ints)
     // (COMMIT) epilogue: partials of k'_s · X_c [4 warps][16][8]
-    static constexpr int S_NRM = 0, S_INV = S_NRM + 8 * TMAX, S_GP = S_INV + 2 * TMAX,
+    static constexpr int S_NRM = 0, S_INV = S_NRM + (TREE ? 0 : 8 * TMAX), S_GP = S_INV + 2 * TMAX,
                          S_GRAM = S_GP + (GRAM_TILES == 1 ? 4 * 128 : 0),
                          S_PAR = S_GRAM + (BIG ? 0 : 2 * TMAX * TMAX), S_WIN = S_PAR + (TREE ? TMAX : 0),
                          S_EGP = S_WIN + (TREE ? 4 * TMAX + 4 : 0),
@@ -156,11 +168,13 @@ struct PipeCfg {
     static constexpr size_t OFF_KP = OFF_META + NXS * size_t(META_BYTES);
     static constexpr size_t OFF_SCR = OFF_KP + 2 * size_t(KP_BYTES);
     static constexpr size_t OFF_BAR = (OFF_SCR + size_t(S_FLOATS) * 4 + 15) / 16 * 16;
-    static constexpr int NBAR = 3 * NKS + 2 * NTS + 8 * 2 + 3 + 2;
+    static constexpr int NBAR = 3 * NKS + 2 * NTS + 8 * 2 + 3 + 2 + 2;
     static constexpr size_t OFF_MISC = OFF_BAR + NBAR * 8;   // TMEM base, abort flag
     static constexpr size_t SMEM = OFF_MISC + 16 + 1024;
 
     static_assert(T_V + V_COLS <= TMEM_COLS && NTS >= G, "TMEM budget");
+    static_assert(!BIG || (OFF_META % 1024 == 0 && (M_UT * 4) % 1024 == 0 && (M_FLD * 4) % 16 == 0),
+                  "the solve's B tiles need 1024-byte bases");
     static_assert(NKS >= 2 * G, "shared-memory ring");
     static_assert(G * S == 2, "two accumulator chains per unit");
     static_assert(!COMMIT || TMAX <= 8, "the fused rollback serves T <= 8");
@@ -634,6 +648,8 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
     uint64_t* vdone = mdone + 2;                 // BIG: v in TMEM, staged rows read (4 epilogue warps)
     uint64_t* xfull = mdone + 3;                 // unit's B tile written (prep): the MMAs may start,
                                                  // while prep goes on to the Gram block and records
+    uint64_t* ebar = mdone + 5;                  // BIG: the epilogue's solve products complete (commit)
+    uint64_t* edone = mdone + 6;                 // BIG: drain of the epilogue's products
     uint32_t* tslot = reinterpret_cast<uint32_t*>(smem + Cfg::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Cfg::OFF_MISC + 4);
     float* scr = reinterpret_cast<float*>(smem + Cfg::OFF_SCR);
@@ -826,9 +842,8 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
         bool ok = true;
         for (int iu = 0; iu < n_my && ok; ++iu) {
             const int us = iu % NXS, ps = iu % Cfg::NUS;
-            // the B tile alone is enough to start; 32-node trees wait for the records too (started
-            // early, their products ran beside the prep warps' warp-level Gram and measured slower)
-            if (!pwait_warp(Cfg::BIG ? &ufull[us] : &xfull[us], (iu / NXS) & 1, abort_flag, a.status, lim))
+            // the B tile alone is enough to start (the records are read by the epilogue warps only)
+            if (!pwait_warp(&xfull[us], (iu / NXS) & 1, abort_flag, a.status, lim))
                 break;
             if (!pwait_warp(&tempty[ps], ((iu / Cfg::NUS) & 1) ^ 1, abort_flag, a.status, lim)) break;
             const uint64_t db = umma_desc_sw128(sX0 + us * Cfg::NXT * Cfg::X_BYTES);
@@ -1269,9 +1284,10 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
                     // the previous unit's epilogue has read its records
                     pwait(&uempty[us], ((iu / NXS) & 1) ^ 1, abort_flag, a.status, lim);
                     if (p < G * TMAX) {
-                        meta[Cfg::M_REC + gj * Cfg::RJ + Cfg::F_GAM + gt] = g_in;
-                        meta[Cfg::M_REC + gj * Cfg::RJ + Cfg::F_BET + gt] = b_in;
+                        meta[Cfg::M_FLD + gj * Cfg::FJ + Cfg::F_GAM + gt] = g_in;
+                        meta[Cfg::M_FLD + gj * Cfg::FJ + Cfg::F_BET + gt] = b_in;
                     }
+                    if (p < TMAX) reinterpret_cast<int*>(meta + Cfg::M_PAR)[p] = p < T ? par_s[p] : -1;
                     constexpr int NZ = 2 * TMAX * TMAX / 4;          // CK, CQ of one head in float4
 #pragma unroll 1
                     for (int z = p; z < G * NZ; z += 128) {
@@ -1284,6 +1300,7 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
                         const int fj = idx / TMAX, fv = idx - fj * TMAX;
                         if (fv >= T) continue;
                         float* hb = meta + Cfg::M_REC + fj * Cfg::RJ;
+                        float* fb = meta + Cfg::M_FLD + fj * Cfg::FJ;
                         const float ik = inv[fv], iq = inv[TMAX + fv];
                         float coef = 1.f;
                         int y = par_s[fv];
@@ -1291,12 +1308,12 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
                             const float iy = inv[y] * coef;
                             hb[Cfg::F_CKT + y * TMAX + fv] = iy * ik * gram[y * 2 * TMAX + fv];
                             hb[Cfg::F_CQT + y * TMAX + fv] = iy * iq * gram[y * 2 * TMAX + TMAX + fv];
-                            coef *= hb[Cfg::F_GAM + y];
+                            coef *= fb[Cfg::F_GAM + y];
                             y = par_s[y];
                         }
-                        hb[Cfg::F_C0K + fv] = coef * ik;
-                        hb[Cfg::F_C0Q + fv] = coef * iq;
-                        hb[Cfg::F_KQ + fv] = gram[fv * 2 * TMAX + TMAX + fv] * ik * iq;
+                        fb[Cfg::F_C0K + fv] = coef * ik;
+                        fb[Cfg::F_C0Q + fv] = coef * iq;
+                        fb[Cfg::F_KQ + fv] = gram[fv * 2 * TMAX + TMAX + fv] * ik * iq;
                     }
                 } else
                 for (int idx = p; idx < G * TMAX; idx += 128) {
@@ -1620,161 +1637,227 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
                 named_bar(2, 128);
             }
             const int ps = iu % Cfg::NUS;
+            if constexpr (Cfg::BIG) {
+                // δ and o of both value heads, each as one triangular solve on the tensor core: the
+                // recurrence δ_t = β_t (v_t − γ_t (c0k_t P_k[t] + Σ_x CK[t][x] δ_x)) over the
+                // 128 value rows at once is δ = M r with M = (I + diag(βγ) CK)⁻¹ and
+                // r_t = β_t (v_t − γ_t c0k_t P_k[t]); the outputs are o = e ∘ P_q + N r with
+                // N = scale (diag(k·q) + diag(γ) CQ) M and e_t = scale γ_t c0q_t. CK and CQ are zero
+                // off each node's ancestors, so M and N are too: row t of M (and of N) lives on t's
+                // root path. Thread (head jc, node tn, part) solves it by back-substitution up that
+                // path p_0 = tn, p_1 = parent, ..: v_0 = 1 and v_j = −Σ_{k<j} v_k L[p_k][p_j] for M,
+                // v_0 = scale k·q_tn and v_j = scale γ_tn CQ[tn][p_j] − Σ_{k<j} v_k L[p_k][p_j] for N,
+                // with L[p_k][p_j] = β γ of p_k times CK[p_k][p_j] (y (I + L) = e_tn, z (I + L) = q_tn).
+                // Threads past the unit's heads idle. This runs while the unit's products are on the
+                // tensor core.
+                const int e_t = tid - 320, jc = e_t >> 6, tn = (e_t >> 1) & 31, part = e_t & 1;
+                float* mw = const_cast<float*>(meta);
+                if (jc >= G) {
+                    named_bar(2, 128);
+                } else {
+                    const float* ck = meta + Cfg::M_REC + jc * Cfg::RJ;
+                    const float* fb = meta + Cfg::M_FLD + jc * Cfg::FJ;
+                    const int* pm = reinterpret_cast<const int*>(meta + Cfg::M_PAR);
+                    // paths of up to PR nodes in registers; a longer one (a deeper tree) walks
+                    // thread-local arrays
+                    constexpr int PR = 8;
+                    int pr[PR];
+                    float vr[PR];
+                    int dr = 0;
+                    bool deep = false;
+                    int pn[TMAX];
+                    float vv[TMAX], uu[TMAX];
+                    int d = 0;
+                    if (tn < T) {
+                        const float gt = fb[Cfg::F_GAM + tn];
+                        const float v0 = part ? scale * fb[Cfg::F_KQ + tn] : 1.f;
+                        int y = pm[tn];
+                        pr[0] = tn;
+#pragma unroll
+                        for (int j = 1; j < PR; ++j) {
+                            pr[j] = y >= 0 ? y : 0;
+                            dr += y >= 0 ? 1 : 0;
+                            y = y >= 0 ? pm[y] : -1;
+                        }
+                        dr += 1;
+                        deep = y >= 0;
+                        if (!deep) {
+                            float ur[PR];
+                            vr[0] = v0;
+                            ur[0] = v0 * (fb[Cfg::F_BET + tn] * gt);
+#pragma unroll
+                            for (int j = 1; j < PR; ++j) {
+                                const int yj = pr[j];
+                                const float* crow = ck + Cfg::F_CKT + yj * TMAX;
+                                float acc = part ? scale * (gt * ck[Cfg::F_CQT + yj * TMAX + tn]) : 0.f;
+#pragma unroll
+                                for (int k = 0; k < j; ++k) acc = fmaf(-ur[k], crow[pr[k]], acc);
+                                vr[j] = acc;
+                                ur[j] = j < dr ? acc * (fb[Cfg::F_BET + yj] * fb[Cfg::F_GAM + yj]) : 0.f;
+                            }
+                        } else {
+                            pn[0] = tn;
+                            vv[0] = v0;
+                            uu[0] = v0 * (fb[Cfg::F_BET + tn] * gt);
+                            d = 1;
+                            for (int y2 = pm[tn]; y2 >= 0 && d < TMAX; y2 = pm[y2], ++d) {
+                                const float* crow = ck + Cfg::F_CKT + y2 * TMAX;
+                                float acc = part ? scale * (gt * ck[Cfg::F_CQT + y2 * TMAX + tn]) : 0.f;
+                                for (int k = 0; k < d; ++k) acc = fmaf(-uu[k], crow[pn[k]], acc);
+                                pn[d] = y2;
+                                vv[d] = acc;
+                                uu[d] = acc * (fb[Cfg::F_BET + y2] * fb[Cfg::F_GAM + y2]);
+                            }
+                        }
+                    }
+                    named_bar(2, 128);     // every CK / CQ entry has been read: head 1's tile goes there
+                    unsigned char* tile = reinterpret_cast<unsigned char*>(mw + (jc == 0 ? Cfg::M_UT : Cfg::M_REC));
+                    const int row = (part ? 32 : 0) + tn;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        *reinterpret_cast<float4*>(tile + sw128_off(row, 4 * c, 0)) = make_float4(0.f, 0.f, 0.f, 0.f);
+                        *reinterpret_cast<float4*>(tile + sw128_off(64 + row, 4 * c, 0)) = make_float4(0.f, 0.f, 0.f, 0.f);
+                    }
+                    if (!deep) {
+#pragma unroll
+                        for (int k = 0; k < PR; ++k) {
+                            if (k < dr) {
+                                const float v = vr[k];
+                                *reinterpret_cast<float*>(tile + sw128_off(row, pr[k], 0)) = v;
+                                *reinterpret_cast<float*>(tile + sw128_off(64 + row, pr[k], 0)) = v - tf32_trunc(v);
+                            }
+                        }
+                    } else {
+                        for (int k = 0; k < d; ++k) {
+                            const float v = vv[k];
+                            *reinterpret_cast<float*>(tile + sw128_off(row, pn[k], 0)) = v;
+                            *reinterpret_cast<float*>(tile + sw128_off(64 + row, pn[k], 0)) = v - tf32_trunc(v);
+                        }
+                    }
+                    fence_async_smem();
+                }
+                pwait(&tfull[ps], (iu / Cfg::NUS) & 1, abort_flag, a.status, lim);
+                tc_fence_after();
+                const uint32_t lq = uint32_t(32 * q4) << 16;
+                const uint32_t dt = tbase + ps * Cfg::P_COLS + lq;
+                constexpr uint32_t IDESC = umma_idesc_tf32(128, 64);
+                const size_t ostep = size_t(Hv) * D;                 // next position, same head
+#pragma unroll 1
+                for (int j = 0; j < G; ++j) {
+                    const int h = kh * G + j;
+                    const float* fb = meta + Cfg::M_FLD + j * Cfg::FJ;
+                    {
+                        // A operand: r (zero past T) as hi (raw fp32, read as tf32) and lo columns
+                        float pk[32], vv[32];
+                        tmem_ld32(dt + j * S * Cfg::CH_COLS, pk);
+#pragma unroll
+                        for (int sc = 1; sc < S; ++sc) {           // the odd K-steps' chain
+                            float pp[32];
+                            tmem_ld32(dt + (j * S + sc) * Cfg::CH_COLS, pp);
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) pk[e] += pp[e];
+                        }
+                        tmem_ld32(tbase + Cfg::T_V + lq + j * TMAX, vv);
+                        uint32_t rh[32], rl[32];
+#pragma unroll
+                        for (int t4 = 0; t4 < TMAX / 4; ++t4) {
+                            const float4 b4 = *reinterpret_cast<const float4*>(fb + Cfg::F_BET + 4 * t4);
+                            const float4 g4 = *reinterpret_cast<const float4*>(fb + Cfg::F_GAM + 4 * t4);
+                            const float4 c4 = *reinterpret_cast<const float4*>(fb + Cfg::F_C0K + 4 * t4);
+                            const float bs[4] = {b4.x, b4.y, b4.z, b4.w}, gs[4] = {g4.x, g4.y, g4.z, g4.w},
+                                        cs[4] = {c4.x, c4.y, c4.z, c4.w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const int t = 4 * t4 + e;
+                                const float r = bs[e] * (vv[t] - gs[e] * (cs[e] * pk[t]));
+                                const float rr = t < T ? r : 0.f;
+                                rh[t] = __float_as_uint(rr);
+                                rl[t] = __float_as_uint(rr - tf32_trunc(rr));
+                            }
+                        }
+                        tmem_st32(tbase + Cfg::T_R + lq, rh);
+                        tmem_st32(tbase + Cfg::T_R + lq + 32, rl);
+                    }
+                    {
+                        // accumulator: [0 | e ∘ P_q]
+                        float pq[32];
+                        tmem_ld32(dt + j * S * Cfg::CH_COLS + TMAX, pq);
+#pragma unroll
+                        for (int sc = 1; sc < S; ++sc) {
+                            float pp[32];
+                            tmem_ld32(dt + (j * S + sc) * Cfg::CH_COLS + TMAX, pp);
+#pragma unroll
+                            for (int e = 0; e < 32; ++e) pq[e] += pp[e];
+                        }
+                        if (j == G - 1) {          // the unit's P slot has been read
+                            tc_fence_before();
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(&tempty[ps]);
+                        }
+                        uint32_t zq[32], eq[32];
+#pragma unroll
+                        for (int t4 = 0; t4 < TMAX / 4; ++t4) {
+                            const float4 g4 = *reinterpret_cast<const float4*>(fb + Cfg::F_GAM + 4 * t4);
+                            const float4 c4 = *reinterpret_cast<const float4*>(fb + Cfg::F_C0Q + 4 * t4);
+                            const float gs[4] = {g4.x, g4.y, g4.z, g4.w}, cs[4] = {c4.x, c4.y, c4.z, c4.w};
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const int t = 4 * t4 + e;
+                                const float ev = scale * (gs[e] * cs[e]) * pq[t];
+                                zq[t] = 0u;
+                                eq[t] = __float_as_uint(t < T ? ev : 0.f);
+                            }
+                        }
+                        tmem_st32(tbase + Cfg::T_D + lq, zq);
+                        tmem_st32(tbase + Cfg::T_D + lq + 32, eq);
+                    }
+                    tmem_wait_st();
+                    tc_fence_before();
+                    named_bar(2, 128);     // r, the accumulator and this head's B tile are in place
+                    if (warp == 10) {
+                        tc_fence_after();
+                        const uint64_t bd = umma_desc_sw128(smem_u32(mw + (j == 0 ? Cfg::M_UT : Cfg::M_REC)));
+#pragma unroll
+                        for (int ks = 0; ks < 4; ++ks) {
+                            const uint64_t bk = bd + uint64_t((ks * 32) >> 4);
+                            const uint64_t bl = bk + uint64_t((64 * 128) >> 4);
+                            umma_tf32_ts_warp(tbase + Cfg::T_D, tbase + Cfg::T_R + ks * 8, bk, IDESC, 1u);
+                            umma_tf32_ts_warp(tbase + Cfg::T_D, tbase + Cfg::T_R + ks * 8, bl, IDESC, 1u);
+                            umma_tf32_ts_warp(tbase + Cfg::T_D, tbase + Cfg::T_R + 32 + ks * 8, bk, IDESC, 1u);
+                        }
+                        umma_commit_warp(ebar);
+                    }
+                    pwait(ebar, uint32_t(j & 1), abort_flag, a.status, lim);
+                    tc_fence_after();
+                    float* tdp = a.tape_delta + (lb * T * Hv + h) * size_t(D) + i;
+                    IO* op = out + (lb * T * Hv + h) * size_t(D) + i;
+                    {
+                        float dv[32];
+                        tmem_ld32(tbase + Cfg::T_D + lq, dv);
+#pragma unroll
+                        for (int t = 0; t < TMAX; ++t) {
+                            st_global_if(tdp, dv[t], t < T);
+                            tdp = opaque_advance(tdp, ostep);
+                        }
+                    }
+                    {
+                        float ov[32];
+                        tmem_ld32(tbase + Cfg::T_D + lq + 32, ov);
+#pragma unroll
+                        for (int t = 0; t < TMAX; ++t) {
+                            st_global_if(op, ov[t], t < T);
+                            op = opaque_advance(op, ostep);
+                        }
+                    }
+                }
+            } else {
             pwait(&tfull[ps], (iu / Cfg::NUS) & 1, abort_flag, a.status, lim);
             tc_fence_after();
             const uint32_t dt = tbase + ps * Cfg::P_COLS + (uint32_t(32 * q4) << 16);
 #pragma unroll 1
             for (int j = 0; j < G; ++j) {
                 const int h = kh * G + j;
-                if constexpr (Cfg::BIG) {
-                    // P of this head (one accumulator per chain: k_t at column t, q_t at TMAX + t),
-                    // 16 positions at a time. First the deltas: ak[t] = c0k_t P_k[t] + Σ_x CK[t][x]
-                    // δ_x takes the earlier blocks' δ as independent products, then inside the
-                    // block each δ_t is pushed into the later t as soon as it is known. Then the
-                    // outputs: aq[t] = c0q_t P_q[t] + Σ_x CQ[t][x] δ_x, every δ known, no serial
-                    // dependence. Positions t >= T are computed and never stored (their
-                    // coefficients are zero; nothing flows back to t < T).
-                    const float* hb = meta + Cfg::M_REC + j * Cfg::RJ;
-                    const uint32_t tvj = tbase + Cfg::T_V + (uint32_t(32 * q4) << 16) + j * TMAX;
-                    const size_t ostep = size_t(Hv) * D;                 // next position, same head
-                    float* tdp = a.tape_delta + (lb * T * Hv + h) * size_t(D) + i;
-                    IO* op = out + (lb * T * Hv + h) * size_t(D) + i;
-                    float dl[TMAX];
-#pragma unroll
-                    for (int blk = 0; blk < TMAX / 16; ++blk) {
-                        const uint32_t ca = dt + (j * S) * Cfg::CH_COLS + 16 * blk;
-                        {
-                            float ak[16];
-                            tmem_ld16(ca, ak);
-#pragma unroll
-                            for (int sc = 1; sc < S; ++sc) {          // the odd K-step chain
-                                float pp[16];
-                                tmem_ld16(ca + sc * Cfg::CH_COLS, pp);
-#pragma unroll
-                                for (int e = 0; e < 16; ++e) ak[e] += pp[e];
-                            }
-#pragma unroll
-                            for (int t4 = 0; t4 < 4; ++t4) {
-                                const float4 ck = *reinterpret_cast<const float4*>(hb + Cfg::F_C0K + 16 * blk + 4 * t4);
-                                ak[4 * t4] *= ck.x; ak[4 * t4 + 1] *= ck.y; ak[4 * t4 + 2] *= ck.z; ak[4 * t4 + 3] *= ck.w;
-                            }
-                            // coefficient rows are loaded one step ahead of their use (here and below)
-                            if (blk > 0) {
-                                float4 cr[2][4];
-#pragma unroll
-                                for (int g4 = 0; g4 < 4; ++g4)
-                                    cr[0][g4] = *reinterpret_cast<const float4*>(hb + Cfg::F_CKT + 16 * blk + 4 * g4);
-#pragma unroll
-                                for (int x = 0; x < 16 * blk; ++x) {
-                                    const int c = x & 1;
-                                    if (x + 1 < 16 * blk) {
-#pragma unroll
-                                        for (int g4 = 0; g4 < 4; ++g4)
-                                            cr[c ^ 1][g4] = *reinterpret_cast<const float4*>(hb + Cfg::F_CKT + (x + 1) * TMAX + 16 * blk + 4 * g4);
-                                    }
-#pragma unroll
-                                    for (int g4 = 0; g4 < 4; ++g4) {
-                                        ak[4 * g4] = fmaf(cr[c][g4].x, dl[x], ak[4 * g4]);
-                                        ak[4 * g4 + 1] = fmaf(cr[c][g4].y, dl[x], ak[4 * g4 + 1]);
-                                        ak[4 * g4 + 2] = fmaf(cr[c][g4].z, dl[x], ak[4 * g4 + 2]);
-                                        ak[4 * g4 + 3] = fmaf(cr[c][g4].w, dl[x], ak[4 * g4 + 3]);
-                                    }
-                                }
-                            }
-                            {
-                                float vb[16];
-                                tmem_ld16(tvj + 16 * blk, vb);
-                                float4 pr[2][4];
-                                float bq[2], gq[2];
-#pragma unroll
-                                for (int g4 = 0; g4 < 4; ++g4)
-                                    pr[0][g4] = *reinterpret_cast<const float4*>(hb + Cfg::F_CKT + (16 * blk) * TMAX + 16 * blk + 4 * g4);
-                                bq[0] = hb[Cfg::F_BET + 16 * blk];
-                                gq[0] = hb[Cfg::F_GAM + 16 * blk];
-#pragma unroll
-                                for (int tt = 0; tt < 16; ++tt) {
-                                    const int t = 16 * blk + tt, c = tt & 1;
-                                    if (tt + 1 < 16) {
-#pragma unroll
-                                        for (int g4 = (tt + 2) / 4; g4 < 4; ++g4)
-                                            pr[c ^ 1][g4] = *reinterpret_cast<const float4*>(hb + Cfg::F_CKT + (t + 1) * TMAX + 16 * blk + 4 * g4);
-                                        bq[c ^ 1] = hb[Cfg::F_BET + t + 1];
-                                        gq[c ^ 1] = hb[Cfg::F_GAM + t + 1];
-                                    }
-                                    const float d = bq[c] * (vb[tt] - gq[c] * ak[tt]);
-                                    dl[t] = d;
-                                    st_global_if(tdp, d, t < T);
-                                    tdp = opaque_advance(tdp, ostep);
-#pragma unroll
-                                    for (int g4 = (tt + 1) / 4; g4 < 4; ++g4) {
-                                        const float xs[4] = {pr[c][g4].x, pr[c][g4].y, pr[c][g4].z, pr[c][g4].w};
-#pragma unroll
-                                        for (int e = 0; e < 4; ++e)
-                                            if (4 * g4 + e > tt) ak[4 * g4 + e] = fmaf(xs[e], d, ak[4 * g4 + e]);
-                                    }
-                                }
-                            }
-                        }
-                        {
-                            float aq[16];
-                            tmem_ld16(ca + TMAX, aq);
-#pragma unroll
-                            for (int sc = 1; sc < S; ++sc) {
-                                float pp[16];
-                                tmem_ld16(ca + sc * Cfg::CH_COLS + TMAX, pp);
-#pragma unroll
-                                for (int e = 0; e < 16; ++e) aq[e] += pp[e];
-                            }
-                            if (blk == TMAX / 16 - 1 && j == G - 1) {
-                                tc_fence_before();
-                                __syncwarp();
-                                if (lane == 0) mbar_arrive(&tempty[ps]);
-                            }
-#pragma unroll
-                            for (int t4 = 0; t4 < 4; ++t4) {
-                                const float4 cq = *reinterpret_cast<const float4*>(hb + Cfg::F_C0Q + 16 * blk + 4 * t4);
-                                aq[4 * t4] *= cq.x; aq[4 * t4 + 1] *= cq.y; aq[4 * t4 + 2] *= cq.z; aq[4 * t4 + 3] *= cq.w;
-                            }
-                            {
-                                float4 cr[2][4];
-#pragma unroll
-                                for (int g4 = 0; g4 < 4; ++g4)
-                                    cr[0][g4] = *reinterpret_cast<const float4*>(hb + Cfg::F_CQT + 16 * blk + 4 * g4);
-#pragma unroll
-                                for (int x = 0; x < 16 * blk + 15; ++x) {
-                                    const int c = x & 1;
-                                    if (x + 1 < 16 * blk + 15) {
-#pragma unroll
-                                        for (int g4 = (x + 1 < 16 * blk ? 0 : (x + 1 - 16 * blk + 1) / 4); g4 < 4; ++g4)
-                                            cr[c ^ 1][g4] = *reinterpret_cast<const float4*>(hb + Cfg::F_CQT + (x + 1) * TMAX + 16 * blk + 4 * g4);
-                                    }
-#pragma unroll
-                                    for (int g4 = (x < 16 * blk ? 0 : (x - 16 * blk + 1) / 4); g4 < 4; ++g4) {
-                                        const float xs[4] = {cr[c][g4].x, cr[c][g4].y, cr[c][g4].z, cr[c][g4].w};
-#pragma unroll
-                                        for (int e = 0; e < 4; ++e)
-                                            if (x < 16 * blk + 4 * g4 + e) aq[4 * g4 + e] = fmaf(xs[e], dl[x], aq[4 * g4 + e]);
-                                    }
-                                }
-                            }
-                            float kqs[16], gms[16];
-#pragma unroll
-                            for (int t4 = 0; t4 < 4; ++t4) {
-                                const float4 k4 = *reinterpret_cast<const float4*>(hb + Cfg::F_KQ + 16 * blk + 4 * t4);
-                                const float4 g4v = *reinterpret_cast<const float4*>(hb + Cfg::F_GAM + 16 * blk + 4 * t4);
-                                kqs[4 * t4] = k4.x; kqs[4 * t4 + 1] = k4.y; kqs[4 * t4 + 2] = k4.z; kqs[4 * t4 + 3] = k4.w;
-                                gms[4 * t4] = g4v.x; gms[4 * t4 + 1] = g4v.y; gms[4 * t4 + 2] = g4v.z; gms[4 * t4 + 3] = g4v.w;
-                            }
-#pragma unroll
-                            for (int tt = 0; tt < 16; ++tt) {
-                                const int t = 16 * blk + tt;
-                                const float o = scale * fmaf(dl[t], kqs[tt], gms[tt] * aq[tt]);
-                                st_global_if(op, o, t < T);
-                                op = opaque_advance(op, ostep);
-                            }
-                        }
-                    }
-                } else {
+                {
                 // P row i of this head: S_hi·X_hi + S_hi·X_lo + S_lo·X_hi over its chains
                 float pr[NP];
 #pragma unroll
@@ -1876,10 +1959,19 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
                 }
                 }
             }
+            }
             __syncwarp();
             if (lane == 0) {
                 mbar_arrive(&uempty[us]);
                 if (COMMIT) mbar_arrive(&kpempty[iu & 1]);
+            }
+        }
+        if constexpr (Cfg::BIG) {
+            // every product this warp issued has completed before TMEM is released
+            if (warp == 10) {
+                umma_commit_warp(edone);
+                volatile int no_abort = 0;
+                pwait_warp(edone, 0, &no_abort, a.status);
             }
         }
     }
