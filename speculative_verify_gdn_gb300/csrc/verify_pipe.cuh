@@ -1827,7 +1827,7 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
                         }
                         umma_commit_warp(ebar);
                     }
-                    pwait(ebar, uint32_t(j & 1), abort_flag, a.status, lim);
+                    pwait(ebar, uint32_t(iu * G + j) & 1u, abort_flag, a.status, lim);   // G commits a unit
                     tc_fence_after();
                     float* tdp = a.tape_delta + (lb * T * Hv + h) * size_t(D) + i;
                     IO* op = out + (lb * T * Hv + h) * size_t(D) + i;

@@ -425,6 +425,20 @@ def test_tree_verify_matches_oracle(gdnlib, T, D, Hv, depth):
     run_verify_case(w, parent=par)
 
 
+@pytest.mark.parametrize("T,tree,Hv", [(16, False, 4), (16, False, 8), (32, True, 4), (32, True, 8)])
+def test_pipe_several_units_per_cta(gdnlib, T, tree, Hv):
+    """More units than SMs (320 (layer, sequence, key head) units), so each CTA of the pipelined
+    kernel runs two or three in turn: every per-unit barrier phase, including the epilogue's
+    tensor-core solve of 16-position chains and 32-node trees, with one and two value heads per
+    key head."""
+    if tree:
+        w = I.custom(I.WORKLOADS[4], name="tree_many_%d_%d" % (T, Hv), L=1, B=80, N=T, Hk=4,
+                     Hv=Hv, D=128, V=64, tree_depth=8)
+        run_verify_case(w, parent=I.random_tree(w, 0, 0))
+    else:
+        run_verify_case(small(I.WORKLOADS[1], L=1, B=80, N=T, Hk=4, Hv=Hv, D=128, V=64), seed=5)
+
+
 @pytest.mark.parametrize("shape", ["chain", "star"])
 def test_tree_verify_degenerate_trees(gdnlib, shape):
     """A tree that is one chain (every node the child of the one before) equals the chain
