@@ -643,6 +643,10 @@ def main(argv=None):
                     help="also time the steps launched as CUDA graph replays")
     ap.add_argument("--gate-dk", action="store_true",
                     help="one gate per key channel (g [L, B, T, Hv, d]); chain workloads only")
+    ap.add_argument("--no-others", action="store_true",
+                    help="skip the bounded runs of the other single-GPU workloads that the default "
+                         "run appends to its line (other_workloads)")
+    ap.add_argument("--others-steps", type=int, default=200)
     args = ap.parse_args(argv)
 
     if args.attn:
@@ -689,6 +693,10 @@ def main(argv=None):
     }
     if "graph" in res:
         line["graph"] = res["graph"]
+    default_run = (args.config == DEFAULT_CONFIG and not (args.fused or args.gate_dk or args.graph)
+                   and args.batch is None and args.layers is None)
+    if world == 1 and default_run and not args.no_others:
+        line["other_workloads"] = other_workloads(args, device)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         # the oracle single-threaded, then on every host core (one sequence per thread)
         t1u, t1a, u1, _ = oracle_unit_times(w, args.seed, args.cpu_budget / 2, w.L, 1)
@@ -710,6 +718,41 @@ def main(argv=None):
     return 0
 
 
+def other_workloads(args, device):
+    """Bounded runs of the other single-GPU workloads (the N = 16 sampling workload, the 32-node
+    trees, both attention workloads), each timed as its own bench line would be but with fewer
+    steps and no e2e leg, so that one default run records them all."""
+    import argparse as _ap
+    from speculative_verify_gdn_gb300 import inputs as I
+    out = {}
+
+    def brief(d, kernels):
+        return {"value": d["value"], "unit": d["unit"], "ms_per_step": d["ms_per_step"],
+                "steps": d["steps"], "warmup": d["warmup"],
+                "kernels": {k: {"ms": v["ms"], "frac_of_measured_peak": v.get("frac_of_measured_peak")}
+                            for k, v in kernels.items()},
+                "roofline": {k: d["roofline"].get(k) for k in ("kernel", "achieved", "frac",
+                                                                "step_frac") if k in d["roofline"]},
+                "clocks": d.get("clocks")}
+    for c in (3, 4):
+        a2 = _ap.Namespace(**vars(args))
+        a2.config, a2.steps, a2.warmup, a2.no_e2e, a2.graph = c, args.others_steps, 5, True, False
+        w = I.WORKLOADS[c]
+        res = run_gpu(a2, w, 1, 0, device)
+        d = {"value": aggregate_tokens_per_s(1, w.B, w.N, res["ms_step"]), "unit": UNIT,
+             "ms_per_step": res["ms_step"], "steps": a2.steps, "warmup": a2.warmup,
+             "roofline": res["roofline"], "clocks": res["clocks"]}
+        out[w.name] = dict(brief(d, res["kernels"]), workload=workload_description(w)["workload"])
+    for name in ("qwen36_attn_b64_n8", "qwen36_attn_b16_n16"):
+        a2 = _ap.Namespace(**vars(args))
+        a2.attn, a2.steps, a2.warmup, a2.batch, a2.layers = name, max(args.others_steps // 2, 10), 5, None, None
+        d = attn_line(a2)
+        kernels = {k: dict(v, frac_of_measured_peak=(v["GBps"] / d["roofline"]["peak"]) if "GBps" in v else None)
+                   for k, v in d["kernels"].items()}
+        out[name] = dict(brief(d, kernels), metric=d["metric"])
+    return out
+
+
 ATTN_METRIC = ("attention-layer verified draft tokens/sec (KV append + causal GQA attention + "
                "KV truncation); % HBM roofline")
 
@@ -725,6 +768,11 @@ def bytes_attn(w, n0):
 
 
 def run_attn(args):
+    print(json.dumps(attn_line(args)), flush=True)
+    return 0
+
+
+def attn_line(args):
     """The hybrid's attention layers: one step = attn_verify (append + attention, all layers) and
     attn_truncate. The accepted counts are zero, so every step appends to and attends over the
     same committed rows (constant work per step)."""
@@ -806,8 +854,7 @@ def run_attn(args):
                     "attn_truncate": {"ms": t_tr}},
         "gpu_launches": K * (3 if nws == 0 else 4), "clocks": clk,
     }
-    print(json.dumps(line), flush=True)
-    return 0
+    return line
 
 
 HYBRID_METRIC = ("hybrid-round verified draft tokens/sec (30 GDN + 10 attention layers: verify, "
