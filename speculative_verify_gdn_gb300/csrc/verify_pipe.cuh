@@ -424,7 +424,6 @@ __device__ __forceinline__ void chain_gram_fold(int w4, int lane, int t128, int 
 #pragma unroll (KUNROLL)
       for (int ks = 0; ks < 16; ++ks) {
         const int ka = NACC == 1 ? 0 : (ks & 3);
-        const int ch = 8 * ks + gt4;
         // B: rows 8 nt .., channels 8 ks + 0..3 and + 4..7 (ldmatrix, lanes 0..15)
         uint32_t rb[2];
         ldsm_x2(smem_u32(Xb + sw128_off(8 * nt + (lane & 7), 8 * ks + ((lane >> 3) & 1) * 4, XKB)), rb);
@@ -1187,7 +1186,6 @@ gdn_verify_pipe_kernel(const VerifyArgs a, const __grid_constant__ CUtensorMap s
 #pragma unroll (KUNROLL)
               for (int ks = 0; ks < 16; ++ks) {
                 const int ka = NACC == 1 ? 0 : (ks & 3);
-                const int ch = 8 * ks + gt4;
                 // B: rows 8 nt .., channels 8 ks + 0..3 and + 4..7 (ldmatrix, lanes 0..15)
                 uint32_t rb[2];
                 ldsm_x2(smem_u32(Xb + sw128_off(8 * nt + (lane & 7), 8 * ks + ((lane >> 3) & 1) * 4, XKB)), rb);
