@@ -100,13 +100,17 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
     return t;
 }
 
-// Wait for phase `parity` of `bar` for at most ~1 s of wall time. Returns false on timeout.
+// Give-up time of every bounded wait in the kernels (the pipelined verify's can be shortened per
+// call: gdn_set_wait_limit_ns).
+constexpr uint64_t kWaitLimitNs = 1000000000ull;
+
+// Wait for phase `parity` of `bar` for at most kWaitLimitNs of wall time. Returns false on timeout.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (globaltimer_ns() - t0 > 1000000000ull) return false;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
     }
 }
 

@@ -143,9 +143,6 @@ __device__ __forceinline__ void named_bar(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
-// The give-up time of a wait: about one second of wall time unless a pipeline limit is set.
-constexpr uint64_t kWaitLimitNs = 1000000000ull;
-
 // bounded wait (limit_ns of wall time) that gives up for good once any wait in the CTA has timed
 // out
 __device__ __forceinline__ bool pwait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
