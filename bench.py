@@ -173,6 +173,12 @@ def kernel_sources_sha(kernel=None):
     return h.hexdigest()[:16]
 
 
+def full_size(args):
+    """Whether the run is the named workload itself (no --batch / --layers override): the
+    profiled traffic records are per launch of the full workload."""
+    return getattr(args, "batch", None) is None and getattr(args, "layers", None) is None
+
+
 def profiled_traffic(workload_name, kernel):
     """dram read+write bytes per launch from a committed ncu summary, if it matches the sources."""
     p = os.path.join(ROOT, "profiles", "dram_traffic.json")
@@ -470,7 +476,7 @@ def run_gpu(args, w, world, rank, device):
     roof = {"bound": "hbm", "kernel": dom, "achieved": kern[dom]["GBps"], "peak": peak,
             "peak_source": "MEASURED_PEAKS.json hbm_gbs (%s)" % peak_kind, "unit": "GB/s",
             "frac": kern[dom]["GBps"] / peak,
-            "traffic": profiled_traffic(w.name, dom),
+            "traffic": profiled_traffic(w.name, dom) if full_size(args) else None,
             "algorithmic_bytes_per_launch": kern[dom]["bytes"],
             "step_frac": step_bytes / (ms_step / 1e3) / 1e9 / peak}
     mean_n = float(nl.mean())
@@ -848,7 +854,8 @@ def attn_line(args):
                    "key_splits": "none" if splits == 1 else "flash-decoding split + combine"},
         "roofline": {"bound": "hbm", "kernel": "attn_verify", "achieved": achieved, "peak": peak,
                      "peak_source": "MEASURED_PEAKS.json hbm_gbs (%s)" % peak_kind, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": profiled_traffic(w.name, "attn_verify"),
+                     "frac": achieved / peak,
+                     "traffic": profiled_traffic(w.name, "attn_verify") if full_size(args) else None,
                      "algorithmic_bytes_per_launch": ba},
         "kernels": {"attn_verify": {"ms": t_att, "bytes": ba, "GBps": achieved},
                     "attn_truncate": {"ms": t_tr}},
