@@ -61,7 +61,10 @@
 // node's conv window is itself, its nearest ancestors, then the conv state's rows. The B tile keeps
 // raw q, k; the inverse norms go into the coefficients. T = 32 (BIG) keeps one B-tile / meta slot:
 // the next unit's prep starts once this unit's products are done and waits for this unit's
-// epilogue only before writing its records; the epilogue warps compute v into TMEM themselves.
+// epilogue only before writing its records; the epilogue warps compute v into TMEM themselves and
+// solve each value head's recurrence as one triangular system on the tensor core (the rows of
+// (I + diag(βγ) CK)⁻¹ by back-substitution along each node's root path, then one product for all
+// 128 value rows).
 #pragma once
 
 #include "verify_impl.cuh"
