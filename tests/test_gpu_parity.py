@@ -416,10 +416,12 @@ def tree_case(B=3, T=12, D=32, L=2, depth=5, seed=0, Hv=4, branch=None):
 
 
 # D = 128 bf16 trees run on the pipelined kernel (node counts up to 8, 16 and 32, one and two
-# value heads per key head, ragged counts); the others on the per-head kernel
+# value heads per key head, ragged counts; 17 nodes is the smallest tree of the 32-node kernel, and
+# depth 16 takes its solve's path longer than its 8 register slots); the others on the per-head kernel
 @pytest.mark.parametrize("T,D,Hv,depth", [(12, 32, 4, 8), (32, 64, 4, 8), (7, 128, 4, 7),
                                           (16, 128, 4, 8), (13, 128, 2, 5), (32, 128, 4, 8),
-                                          (32, 128, 2, 6), (24, 128, 4, 3), (29, 128, 2, 12)])
+                                          (32, 128, 2, 6), (24, 128, 4, 3), (29, 128, 2, 12),
+                                          (17, 128, 4, 6), (32, 128, 4, 16)])
 def test_tree_verify_matches_oracle(gdnlib, T, D, Hv, depth):
     w, par = tree_case(T=T, D=D, depth=depth, Hv=Hv, B=4)
     run_verify_case(w, parent=par)
